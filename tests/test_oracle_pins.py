@@ -1,0 +1,218 @@
+"""Pins for the fp64 oracle against facts fixed by the mathematics (CPU only).
+
+The pages print no worked numeric example, so every pin is a closed form, an
+independent formulation, a special case or an invariant the pages state:
+
+* conv + SiLU equals PyTorch's grouped conv1d (a library routine) per sequence;
+* the token recurrence equals the quadratic (masked-attention) SSD form;
+* constant inputs with N = P = 1 give the geometric-series closed form;
+* a -> 0 gives a memoryless output; B = 0 or C = 0 gives y = D x exactly;
+* any segment count gives the unsegmented result, and the segment transform is
+  affine in its initial state, S_out = a_block * S_in + S_ext (Megatron-LM PR
+  #6808 "Add state-passing context parallelism for Mamba2", description);
+* seq_idx resets make a packed row equal separate per-sequence runs (NeMo
+  Automodel PR #1441, Key changes: seq_idx from cu_seqlens);
+* the backward equals central finite differences of the forward in every input.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from mamba2_ssd_selective_gb300.inputs import SsdShape, make_inputs
+from tests.ref_math import conv_silu_torch, quadratic_ssd
+
+SMALL = SsdShape(batch=2, seqlen=96, nheads=4, headdim=8, dstate=6, ngroups=2, chunk=16, n_segments=4)
+TINY = SsdShape(1, 512, 4, 32, 16, 1, 64, 4)
+
+
+def rel(a, b):
+    return float(np.linalg.norm(np.asarray(a) - np.asarray(b)) / max(np.linalg.norm(np.asarray(b)), 1e-300))
+
+
+def f64(inp):
+    return {k: (v.double() if torch.is_tensor(v) and v.is_floating_point() else v) for k, v in inp.items()}
+
+
+@pytest.mark.parametrize("seq", [None, [30, 2, 41, 23]])
+def test_conv_matches_torch_conv1d(oracle_lib, seq):
+    inp = make_inputs(SMALL, 11, "f32", seq_lengths=seq)
+    v_ref, u_ref = conv_silu_torch(inp, SMALL)
+    for b in range(SMALL.batch):
+        u, v, ch = oracle_lib.conv(inp, SMALL, b=b)
+        assert sorted(ch.tolist()) == list(range(SMALL.conv_dim))
+        assert rel(v, v_ref[b][:, ch]) < 1e-14
+        assert rel(u, u_ref[b][:, ch]) < 1e-14
+
+
+@pytest.mark.parametrize("shape,seq", [
+    (SMALL, None),
+    (SMALL, [30, 2, 41, 23]),
+    (SsdShape(1, 200, 3, 5, 7, 1, 8, 1), [1, 1, 3, 195]),
+    (TINY, None),
+])
+def test_recurrence_equals_quadratic_form(oracle_lib, shape, seq):
+    inp = make_inputs(shape, 5, "f32", seq_lengths=seq)
+    y_ref, fin_ref = quadratic_ssd(inp, shape)
+    out = oracle_lib.forward(inp, shape, n_segments=1)
+    assert rel(out["y"], y_ref) < 1e-12
+    assert rel(out["final_state"], fin_ref) < 1e-12
+
+
+def test_geometric_series_closed_form(oracle_lib):
+    L = 300
+    shape = SsdShape(1, L, 1, 1, 1, 1, 4, 1)
+    cx, cb, cc, zr = 0.7, -0.4, 1.3, 0.25
+    xBC = torch.tensor([[[cx, cb, cc]] * L], dtype=torch.float64)
+    inp = {
+        "xBC": xBC, "dt_raw": torch.full((1, L, 1), zr, dtype=torch.float64),
+        "dt_bias": torch.tensor([-1.0], dtype=torch.float64), "A_log": torch.tensor([np.log(0.8)]),
+        "D": torch.tensor([0.3], dtype=torch.float64),
+        "conv_w": torch.tensor([[0.0, 0.0, 0.0, 1.0]] * 3, dtype=torch.float64),
+        "conv_b": torch.zeros(3, dtype=torch.float64), "seq_idx": None,
+    }
+    silu = lambda v: v / (1 + np.exp(-v))  # noqa: E731
+    ux, uB, uC = silu(cx), silu(cb), silu(cc)
+    dt = np.log1p(np.exp(zr - 1.0))
+    a = np.exp(-0.8 * dt)
+    t = np.arange(L)
+    y_cf = uC * uB * dt * ux * (1 - a ** (t + 1)) / (1 - a) + 0.3 * ux
+    fin_cf = uB * dt * ux * (1 - a ** L) / (1 - a)
+    out = oracle_lib.forward(inp, shape, n_segments=1)
+    assert rel(out["y"][0, :, 0, 0], y_cf) < 1e-13
+    assert abs(out["final_state"][0, 0, 0, 0] - fin_cf) < 1e-13 * abs(fin_cf)
+    out4 = oracle_lib.forward(inp, shape.with_(n_segments=4), n_segments=4)
+    assert rel(out4["y"][0, :, 0, 0], y_cf) < 1e-13
+
+
+def test_memoryless_limit(oracle_lib):
+    inp = make_inputs(SMALL, 3, "f32")
+    inp["A_log"] = torch.full_like(inp["A_log"], 40.0)  # A = -e^40: a_t underflows to 0
+    _, u = conv_silu_torch(inp, SMALL)
+    H, P, N, G = SMALL.nheads, SMALL.headdim, SMALL.dstate, SMALL.ngroups
+    ux = u[..., : H * P].reshape(2, -1, H, P)
+    uB = u[..., H * P: H * P + G * N].reshape(2, -1, G, N)
+    uC = u[..., H * P + G * N:].reshape(2, -1, G, N)
+    dt = np.logaddexp(0, inp["dt_raw"].double().numpy() + inp["dt_bias"].double().numpy())
+    g = np.arange(H) // (H // G)
+    bc = np.einsum("blgn,blgn->blg", uB, uC)[:, :, g]
+    y_ref = dt[..., None] * ux * bc[..., None] + inp["D"].double().numpy()[None, None, :, None] * ux
+    out = oracle_lib.forward(inp, SMALL, n_segments=2)
+    assert rel(out["y"], y_ref) < 1e-13
+
+
+@pytest.mark.parametrize("which", ["B", "C"])
+def test_zero_B_or_C_gives_Dx(oracle_lib, which):
+    inp = make_inputs(SMALL, 4, "f32")
+    H, P, N, G = SMALL.nheads, SMALL.headdim, SMALL.dstate, SMALL.ngroups
+    lo = H * P + (0 if which == "B" else G * N)
+    inp["xBC"][..., lo: lo + G * N] = 0.0  # conv_b = 0 as well, so silu(0) = 0
+    _, u = conv_silu_torch(inp, SMALL)
+    ux = u[..., : H * P].reshape(2, -1, H, P)
+    out = oracle_lib.forward(inp, SMALL, n_segments=4)
+    # exact up to the last-bit difference between two SiLU evaluations
+    np.testing.assert_allclose(out["y"], inp["D"].double().numpy()[None, None, :, None] * ux, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("seq", [None, [100, 156, 7, 249]])
+def test_segment_count_invariance(oracle_lib, seq):
+    shape = SsdShape(1, 512, 4, 8, 8, 2, 16, 1)
+    inp = make_inputs(shape, 9, "f32", seq_lengths=seq)
+    base = oracle_lib.forward(inp, shape, n_segments=1)
+    for S in (2, 4, 8, 16):
+        out = oracle_lib.forward(inp, shape, n_segments=S)
+        assert rel(out["y"], base["y"]) < 1e-12, S
+        assert rel(out["final_state"], base["final_state"]) < 1e-12, S
+
+
+def test_affine_segment_identity(oracle_lib):
+    """Two rows share the second half (and the 3-token conv halo before it) but
+    differ earlier, so the second segment sees two different initial states."""
+    shape = SsdShape(2, 128, 2, 4, 5, 1, 8, 2)
+    inp = make_inputs(shape, 21, "f32")
+    inp["xBC"][1, 61:] = inp["xBC"][0, 61:]
+    inp["dt_raw"][1, 64:] = inp["dt_raw"][0, 64:]
+    inp["A_log"][:] = float(np.log(0.05))  # slow decay: a_block = O(1), no cancellation in d_out
+    out = oracle_lib.forward(inp, shape, n_segments=2)
+    s_ext, a_blk, s_in = out["s_ext"][:, 1], out["a_block"][:, 1], out["seg_in"][:, 1]
+    assert rel(s_ext[0], s_ext[1]) < 1e-15 and rel(a_blk[0], a_blk[1]) < 1e-15
+    assert rel(s_in[0], s_in[1]) > 1e-2  # genuinely different initial states
+    assert a_blk.min() > 0.1
+    d_out = out["final_state"][0] - out["final_state"][1]
+    d_in = s_in[0] - s_in[1]
+    assert rel(d_out, a_blk[0][:, None, None] * d_in) < 1e-13
+    # and S_out(0) = S_ext: the unsegmented run of the second half alone
+    fin = out["final_state"][0]
+    assert rel(fin, a_blk[0][:, None, None] * s_in[0] + s_ext[0]) < 1e-13
+
+
+def test_packed_equals_separate_runs(oracle_lib):
+    lens = [37, 3, 90, 1, 125]
+    L = sum(lens)
+    shape = SsdShape(1, L, 2, 6, 4, 1, 8, 1)
+    inp = make_inputs(shape, 13, "f32", seq_lengths=lens)
+    out = oracle_lib.forward(inp, shape, n_segments=1)
+    s0 = 0
+    for n in lens:
+        sub = {k: (v[:, s0:s0 + n] if k in ("xBC", "dt_raw") else v) for k, v in inp.items()}
+        sub["seq_idx"] = None
+        o = oracle_lib.forward(sub, shape.with_(seqlen=n), n_segments=1)
+        assert rel(out["y"][:, s0:s0 + n], o["y"]) < 1e-14
+        s0 += n
+    assert rel(out["final_state"], o["final_state"]) < 1e-14
+
+
+def test_head_subsets_match_full(oracle_lib):
+    shape = SsdShape(1, 64, 6, 4, 3, 3, 8, 2)
+    inp = make_inputs(shape, 17, "f32", dfinal=True)
+    full = oracle_lib.forward(inp, shape)
+    part = oracle_lib.forward(inp, shape, heads=(2, 4))
+    np.testing.assert_array_equal(part["y"], full["y"][:, :, 2:4])
+    gf = oracle_lib.backward(inp, shape)
+    gp = oracle_lib.backward(inp, shape, heads=(2, 4))
+    idx = [list(gf["channels"]).index(c) for c in gp["channels"]]
+    np.testing.assert_allclose(gp["dxBC"], gf["dxBC"][..., idx], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(gp["ddt_raw"], gf["ddt_raw"][..., 2:4], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(oracle_lib, inp, shape):
+    out = oracle_lib.forward(inp, shape, n_segments=1, nthreads=1)
+    y = out["y"].reshape(shape.batch, shape.seqlen, -1)
+    return float(np.sum(inp["dy"].double().numpy() * y) + np.sum(inp["dfinal"].double().numpy() * out["final_state"]))
+
+
+@pytest.mark.parametrize("shape,seq", [
+    (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), None),
+    (SsdShape(1, 60, 2, 4, 3, 1, 8, 1), [17, 1, 2, 40]),
+])
+def test_backward_matches_finite_differences(oracle_lib, shape, seq):
+    inp = f64(make_inputs(shape, 23, "f32", dfinal=True, seq_lengths=seq))
+    g = oracle_lib.backward(inp, shape, nthreads=1)
+    dxBC = np.zeros((shape.batch, shape.seqlen, shape.conv_dim))
+    dxBC[..., g["channels"]] = g["dxBC"]
+    dconv_w = np.zeros((shape.conv_dim, 4))
+    dconv_w[g["channels"]] = g["dconv_w"]
+    dconv_b = np.zeros(shape.conv_dim)
+    dconv_b[g["channels"]] = g["dconv_b"]
+    grads = {"xBC": dxBC, "dt_raw": g["ddt_raw"], "dt_bias": g["ddt_bias"], "A_log": g["dA_log"], "D": g["dD"],
+             "conv_w": dconv_w, "conv_b": dconv_b}
+    rng = np.random.default_rng(0)
+    HP, GN = shape.nheads * shape.headdim, shape.ngroups * shape.dstate
+    parts = {"x": slice(0, HP), "B": slice(HP, HP + GN), "C": slice(HP + GN, HP + 2 * GN)}
+    cases = [("xBC", k) for k in parts] + [(k, None) for k in grads if k != "xBC"]
+    for name, part in cases:
+        v = rng.standard_normal(grads[name].shape)
+        if part is not None:
+            mask = np.zeros_like(v)
+            mask[..., parts[part]] = 1.0
+            v *= mask
+        eps = 1e-5
+        plus, minus = dict(inp), dict(inp)
+        plus[name] = inp[name] + eps * torch.from_numpy(v)
+        minus[name] = inp[name] - eps * torch.from_numpy(v)
+        fd = (_loss(oracle_lib, plus, shape) - _loss(oracle_lib, minus, shape)) / (2 * eps)
+        an = float(np.sum(grads[name] * v))
+        assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, part, fd, an)
