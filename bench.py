@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Benchmark: SSD forward+backward tokens/s of the Mamba2 mixer core on GB300.
+
+One step = ssd_forward + ssd_backward (every kernel of the hot path: conv+SiLU,
+dt/cumsum, chunk contractions, segment summaries, exclusive segment scan,
+correction/output, and the backward mirror) over one batch of the
+"mamba2-1b-fwdbwd" workload: batch 4, L 8192, H 64, P 64, N 128, G 1,
+chunk 256, 8 segments, bf16 activations, seeded synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own
+batch (weak scaling, no data-path collective); the timed region is bracketed by
+a barrier and a device synchronise, and the time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mamba2_ssd_selective_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "SSD fwd+bwd tokens/s on 1 GB300 (L=8192, bf16) + % of tensor/HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mamba2-1b-fwdbwd"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SM_COUNT, FP32_LANES_PER_SM = 152, 128
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws: int):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def aggregate(elapsed_s: float, units: float, ws: int) -> tuple[float, float]:
+    """(max elapsed over ranks, sum of units over ranks).  Timing bookkeeping only."""
+    if ws == 1:
+        return elapsed_s, units
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- peaks / clocks
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.proc = gpu, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- algorithmic work per kernel launch
+
+def kernel_work(shape, dtype: str) -> dict:
+    """name -> (bound, amount per launch, unit): algorithmic flops (causal
+    products only) for contractions, algorithmic HBM bytes for streaming kernels."""
+    b, L, H, P, N, G, Q, S = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                              shape.chunk, shape.n_segments)
+    eb = 2 if dtype == "bf16" else 4
+    nc, Cd = L // Q, shape.conv_dim
+    tri = Q * (Q + 1) // 2
+    PN = P * N
+    return {
+        "conv_fwd": ("hbm", b * L * Cd * 2 * eb, "B"),
+        "dt_prep": ("hbm", b * L * H * (eb + 8), "B"),
+        "cb": ("alu", b * nc * G * tri * 2 * N, "flop"),
+        "chunk_state": ("alu", b * nc * H * 2 * P * N * Q, "flop"),
+        "local_pass": ("hbm", b * nc * H * PN * 8 + b * S * H * PN * 4, "B"),
+        "seg_scan": ("hbm", b * S * H * PN * 8 + b * H * PN * 4, "B"),
+        "chunk_out": ("alu", b * nc * H * (tri * 2 * P + 2 * Q * N * P), "flop"),
+        "chunk_z": ("alu", b * nc * H * 2 * P * N * Q, "flop"),
+        "local_rev": ("hbm", b * nc * H * PN * 8 + b * S * H * PN * 4, "B"),
+        "seg_rscan": ("hbm", b * S * H * PN * 8, "B"),
+        "chunk_w": ("alu", b * nc * H * tri * 2 * P, "flop"),
+        "chunk_dx": ("alu", b * nc * H * (tri * 2 * P + 2 * Q * N * P), "flop"),
+        "chunk_dcdb": ("alu", b * nc * H * (2 * tri * 2 * N + 2 * 2 * Q * P * N), "flop"),
+        "chunk_dt": ("hbm", b * L * H * (6 * 4 + eb + 2 * P * eb), "B"),
+        "bc_reduce": ("hbm", b * L * H * N * 8 + b * L * 2 * G * N * 4, "B"),
+        "conv_bwd": ("hbm", b * L * Cd * (eb + 4 + eb), "B"),
+        "param_reduce": ("hbm", b * nc * H * 12, "B"),
+    }
+
+
+def roofline_for(kt: list, shape, dtype: str, peaks: dict, peak_src: str, clocks: dict | None) -> dict:
+    work = kernel_work(shape, dtype)
+    name, launches, total_ms = max(kt, key=lambda r: r[2])
+    bound, amount, unit = work.get(name, ("hbm", 0, "B"))
+    avg_s = total_ms / 1e3 / max(launches, 1)
+    traffic = committed_traffic(name)
+    if bound == "hbm":
+        achieved = amount / avg_s / 1e9
+        peak, punit = peaks["hbm_gbs"], "GB/s"
+        note = f"HBM copy bandwidth ({peak_src})"
+    elif bound == "tensor":
+        achieved = amount / avg_s / 1e12
+        peak, punit = peaks["bf16_tflops"], "TFLOP/s"
+        note = f"dense bf16 burst ({peak_src})"
+    else:  # fp32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        achieved = amount / avg_s / 1e12
+        peak, punit = SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, "TFLOP/s"
+        note = f"fp32 FMA pipe at {mhz:.0f} MHz (derived)"
+    return {"bound": bound, "kernel": name, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": punit,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": note,
+            "algorithmic_per_launch": amount, "avg_launch_ms": round(avg_s * 1e3, 4)}
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel's file; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    e = d.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest() != e["source_sha256"]:
+            return None
+    return e["dram_bytes_per_launch"]
+
+
+# ---------------------------------------------------------------- CPU oracle timings
+
+def oracle_sample(inp: dict, shape, heads: tuple, nthreads: int = 0) -> float:
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.forward(inp, shape, heads=heads, rows=[0], nthreads=nthreads)
+    oracle.backward(inp, shape, heads=heads, rows=[0], nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp: dict, shape) -> dict:
+    import oracle
+
+    oracle.build()
+    cores = oracle.default_threads()
+    dt = oracle_sample(inp, shape, (0, shape.nheads))
+    return {"value": round(shape.seqlen / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 C oracle, fwd (S={shape.n_segments}) + bwd of batch row 0 (all {shape.nheads} heads, "
+                      f"{shape.seqlen} tokens) of the same workload: {dt:.1f} s"}
+
+
+def run_reference(args, shape, dtype, seed):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    cores = oracle.default_threads()
+    inp = make_inputs(shape, seed, dtype)
+    heads = (0, min(8, shape.nheads))
+    frac = (heads[1] - heads[0]) / shape.nheads
+    for _ in range(args.warmup):
+        oracle_sample(inp, shape, heads)
+    times = [oracle_sample(inp, shape, heads) for _ in range(args.steps)]
+    total = sum(times)
+    tok_per_step = shape.seqlen * frac
+    value = tok_per_step * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(shape, dtype, seed),
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: fp64 C oracle fwd+bwd of batch row 0, heads {heads[0]}-{heads[1] - 1} "
+                                   f"of {shape.nheads}, {shape.seqlen} tokens; value counts "
+                                   f"{tok_per_step:.0f} token-equivalents per step"},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(shape, dtype, seed) -> dict:
+    return {"workload": DEFAULT_WORKLOAD if shape == WORKLOADS[DEFAULT_WORKLOAD][0] else "custom",
+            "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads, "headdim": shape.headdim,
+            "dstate": shape.dstate, "ngroups": shape.ngroups, "d_conv": shape.d_conv, "chunk": shape.chunk,
+            "n_segments": shape.n_segments, "activations": dtype, "seed": seed,
+            "l2": "inputs larger than L2 (xBC 285 MB, dy 268 MB per step)"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, shape, dtype, seed):
+    import mamba2_ssd_selective_gb300 as ssd
+    from mamba2_ssd_selective_gb300.build import build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(ws, "nccl")
+    if rank == 0:
+        build()
+    barrier(ws)
+    if rank != 0:
+        build()  # stamp is current: only loads
+    ssd.load()
+    inp = make_inputs(shape, seed + 1000 * rank, dtype)
+    t = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    runner = ssd.SsdRunner(shape, dtype)
+    y, fin, seg = runner.alloc_outputs()
+    grads = runner.alloc_grads()
+    dfinal = None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        runner.forward(t, out=(y, fin, seg))
+        runner.backward(t, t["dy"], dfinal, seg, grads=grads)
+
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler.start()
+    # timed region 1: throughput
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    # timed region 2: the same steps with per-kernel events on the launch stream
+    ssd.ssd_profile_begin()
+    for _ in range(args.steps):
+        step()
+    kt = ssd.ssd_profile_end()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    # end to end through the public API with host buffers (pinned)
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: inp[k].pin_memory() for k in ("xBC", "dt_raw", "dy")}
+        host_out = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
+                    "final_state": torch.empty(fin.shape, dtype=fin.dtype).pin_memory()}
+        host_out.update({k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()})
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k, v in host_in.items():
+                t[k].copy_(v, non_blocking=True)
+            step()
+            host_out["y"].copy_(y, non_blocking=True)
+            host_out["final_state"].copy_(fin, non_blocking=True)
+            for k, v in grads.items():
+                host_out[k].copy_(v, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e3.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        el2, units2 = aggregate(e2.elapsed_time(e3) / 1e3, shape.tokens * args.steps, ws)
+        e2e = {"value": round(units2 / el2, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    el, units = aggregate(elapsed, shape.tokens * args.steps, ws)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": METRIC, "value": round(units / el, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": config_dict(shape, dtype, seed),
+        "roofline": roofline_for(kt, shape, dtype, peaks, peak_src, clocks),
+        "e2e": e2e,
+        "gpu_launches": int(sum(r[1] for r in kt)),
+        "clocks": clocks,
+        "kernels": [{"name": n, "launches": c, "ms_per_launch": round(ms / max(c, 1), 4),
+                     "share": round(ms / max(sum(r[2] for r in kt), 1e-9), 4)} for n, c, ms in kt],
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, shape)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
+    shape, dtype, seed = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape, dtype, seed)
+    else:
+        run_ours(args, shape, dtype, seed)
+    ws, _, _ = dist_env()
+    if ws > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * ssd.h -- C ABI of libssd: the Mamba2 mixer core (conv1d + SiLU over xBC,
+ * chunked SSD, causal segments with affine summaries, exclusive segment scan,
+ * correction), forward and backward, on one GB300 (sm_103a).
+ *
+ * Method.  Megatron-LM PR #6808 "Add state-passing context parallelism for
+ * Mamba2" (description): the SSD transform of one causal segment is affine in
+ * its initial state, S_out = a_block * S_in + S_ext; every segment computes its
+ * (S_ext, a_block) from a zero initial state, an exclusive causal scan over the
+ * summaries recovers each segment's true initial state, and a correction pass
+ * applies it; the conv halo is the previous segment's last d_conv-1 tokens;
+ * backward mirrors this with a reverse boundary scan and recomputes everything
+ * that scales with the sequence length.  Resets at packed-sequence boundaries
+ * follow seq_idx derived from cu_seqlens (NeMo Automodel PR #1441 "feat:
+ * context-parallel with nemotron v3", Key changes).  The per-token model is the
+ * Mamba2 selective SSM:
+ *     u      = SiLU(causal depthwise conv1d(xBC) + conv_b)      (x, B, C parts)
+ *     dt_t   = softplus(dt_raw_t + dt_bias),  A = -exp(A_log)
+ *     h_t    = exp(dt_t*A) * h_{t-1} + dt_t * x_t (outer) B_t    (P x N per head)
+ *     y_t    = h_t . C_t + D * x_t
+ * with the state zeroed where seq_idx changes and the conv taps masked there.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or synchronises the host; every call only enqueues
+ *    work on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - Arguments are validated before anything is launched.  A rejected call
+ *    returns a negative ssd_status and launches nothing.  SSD_ERR_CUDA means a
+ *    launch failed; the CUDA error is then also left for cudaGetLastError().
+ *  - Activations (x, B, C, dt_raw, y, dy and their grads) use `dims.dtype`;
+ *    parameters, states and parameter grads are fp32.  Arithmetic is fp32
+ *    (bf16 tensor-core operands with fp32 accumulation on the bf16 path).
+ *  - Shapes: b = batch, L = seqlen, H = nheads, P = headdim, N = dstate,
+ *    G = ngroups (head h reads group h / (H/G)), Q = chunk, S = n_segments.
+ *    Token-major layouts: element (b, t, c) of a tensor with token stride ts
+ *    lives at ptr[(b*L + t)*ts + c].  Channels within a token are contiguous.
+ */
+#ifndef SSD_H
+#define SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssd_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_DIMS = -1,   /* a dimension is <= 0, H % G != 0, or d_conv != 4 */
+  SSD_ERR_SEGMENT_ALIGN = -2,  /* L % (n_segments * chunk) != 0 */
+  SSD_ERR_NULL_PTR = -3,       /* a required pointer is NULL */
+  SSD_ERR_ALIGNMENT = -4,      /* pointer or token stride violates the alignment rules below */
+  SSD_ERR_DTYPE = -5,          /* dims.dtype is not an ssd_dtype */
+  SSD_ERR_WORKSPACE = -6,      /* workspace NULL or smaller than ssd_workspace_size() */
+  SSD_ERR_UNSUPPORTED = -7,    /* valid but outside the supported envelope (see ssd_forward) */
+  SSD_ERR_CUDA = -8,           /* a kernel launch failed */
+  SSD_ERR_DEVICE_TIMEOUT = -9  /* a bounded device-side wait gave up (see ssd_device_status) */
+} ssd_status;
+
+typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
+
+typedef struct {
+  int32_t batch, seqlen, nheads, headdim, dstate, ngroups;
+  int32_t d_conv;     /* must be 4 */
+  int32_t chunk;      /* Q: SSD chunk length */
+  int32_t n_segments; /* S: equal causal segments; each must be a multiple of chunk */
+  int32_t dtype;      /* ssd_dtype of the activations */
+} ssd_dims;
+
+/* Pre-conv activations as laid out by the in-projection (zero-copy views into
+ * one zxBCdt buffer are fine: pass each part's pointer and token stride).
+ *   x  (b, L, H*P)  B (b, L, G*N)  C (b, L, G*N)  dt (b, L, H)
+ * x, B, C: 16-byte aligned, token strides a multiple of 8 elements (bf16) or
+ * 4 elements (fp32).  dt: element aligned, any token stride >= H.
+ * Parameters (fp32, contiguous): dt_bias, A_log, D (H); conv_w (Cd, 4) where
+ * tap 3 multiplies the current token; conv_b (Cd); Cd = H*P + 2*G*N and the
+ * conv channel order is [x | B | C].
+ * seq_idx (b, L) int32, non-decreasing within a row, or NULL (one sequence per
+ * row).  The state and the conv taps are reset where it changes. */
+typedef struct {
+  const void *x;  int64_t x_tok_stride;
+  const void *B;  int64_t B_tok_stride;
+  const void *C;  int64_t C_tok_stride;
+  const void *dt; int64_t dt_tok_stride;
+  const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
+  const int32_t *seq_idx;
+} ssd_inputs;
+
+/* Gradients, written (not accumulated).  dx, dB, dC, ddt have the layout and
+ * alignment rules of x, B, C, dt, with their own token strides (they may be
+ * views into one d(zxBCdt) buffer).  ddt_bias, dA_log, dD (H), dconv_w (Cd,4),
+ * dconv_b (Cd) are fp32 and summed over batch and tokens. */
+typedef struct {
+  void *dx;  int64_t dx_tok_stride;
+  void *dB;  int64_t dB_tok_stride;
+  void *dC;  int64_t dC_tok_stride;
+  void *ddt; int64_t ddt_tok_stride;
+  float *ddt_bias, *dA_log, *dD, *dconv_w, *dconv_b;
+} ssd_grads;
+
+/* Bytes of device workspace ssd_forward (backward = 0) or ssd_backward
+ * (backward = 1) needs for `dims`; 0 if dims are invalid.  The workspace is
+ * scratch: its contents need not survive between calls. */
+size_t ssd_workspace_size(const ssd_dims *dims, int backward);
+
+/* Forward.  y (b, L, H*P) activation dtype, contiguous; final_state (b, H, P, N)
+ * fp32 = the state after each row's last token (with packing: of the row's last
+ * sequence), or NULL; seg_init_states (b, S, H, P, N) fp32 = each segment's true
+ * initial state recovered by the exclusive scan (what ssd_backward may reuse),
+ * or NULL.  Supported envelope: P and N multiples of 8 and <= 256, chunk a
+ * multiple of 32 and <= 256, n_segments <= 1024; otherwise SSD_ERR_UNSUPPORTED. */
+ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
+                       float *seg_init_states, void *workspace, size_t ws_bytes, ssd_stream_t stream);
+
+/* Backward of  L = <dy, y> + <dfinal_state, final_state>.
+ * dy (b, L, H*P) activation dtype, contiguous; dfinal_state (b, H, P, N) fp32 or
+ * NULL (zero); seg_init_states from ssd_forward on the same inputs, or NULL to
+ * have them recomputed.  Everything that scales with L is recomputed. */
+ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *dy, const float *dfinal_state,
+                        const float *seg_init_states, const ssd_grads *grads, void *workspace, size_t ws_bytes,
+                        ssd_stream_t stream);
+
+/* seq_idx[t] = i for cu_seqlens[i] <= t < cu_seqlens[i+1], t in [0, total_tokens)
+ * (NeMo Automodel PR #1441, Key changes: seq_idx computed from cu_seqlens).
+ * cu_seqlens (nseq + 1) int32 device array, non-decreasing, cu_seqlens[0] = 0 and
+ * cu_seqlens[nseq] = total_tokens (not checked on the host: tokens outside every
+ * range get seq_idx -1). */
+ssd_status ssd_cu_seqlens_to_seq_idx(const int32_t *cu_seqlens, int32_t nseq, int32_t *seq_idx,
+                                     int32_t total_tokens, ssd_stream_t stream);
+
+/* Reads the device status word kept in `workspace` by the last call that used
+ * it (synchronises `stream`): SSD_OK, or SSD_ERR_DEVICE_TIMEOUT if a bounded
+ * device-side wait gave up. */
+ssd_status ssd_device_status(const void *workspace, ssd_stream_t stream);
+
+/* Per-kernel timing for benchmarks.  After ssd_profile_begin(), every kernel
+ * that ssd_forward / ssd_backward launch (from this host thread) is bracketed
+ * by a pair of CUDA events recorded on the launch stream (events come from a
+ * fixed pool created on the first begin; at most 65536 launches are recorded,
+ * later ones run unrecorded).  ssd_profile_end() waits for the recorded events,
+ * writes up to max_entries per-kernel totals (name, launches, summed
+ * milliseconds) in first-launch order, stops recording and returns the number
+ * of entries, or a negative ssd_status.  Not for use during stream capture. */
+typedef struct {
+  const char *name; /* static string */
+  int32_t launches;
+  float total_ms;
+} ssd_kernel_time;
+
+ssd_status ssd_profile_begin(void);
+int32_t ssd_profile_end(ssd_kernel_time *out, int32_t max_entries);
+
+/* Static description of a status code. */
+const char *ssd_status_string(ssd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_H */

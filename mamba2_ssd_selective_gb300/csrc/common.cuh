@@ -1,0 +1,114 @@
+// Internal definitions shared by the libssd CUDA sources (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+// Problem description handed to every kernel by value.
+struct Problem {
+  int b, L, H, P, N, G, Q, S;
+  int Cd;   // H*P + 2*G*N conv channels, order [x | B | C]
+  int nc;   // chunks per row, L / Q
+  int cps;  // chunks per segment
+  int hpg;  // heads per group
+  const void *x, *B, *C, *dt;
+  long long xs, Bs, Cs, dts;  // token strides (elements)
+  const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
+  const int *seq_idx;  // (b, L) or nullptr
+};
+
+// ---------------------------------------------------------------- dtypes
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------- math
+__device__ __forceinline__ float softplus_f(float z) { return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z)); }
+__device__ __forceinline__ float sigmoid_f(float v) { return 1.f / (1.f + expf(-v)); }
+
+// seq id of token t of row b (0 when there is no seq_idx)
+__device__ __forceinline__ int seq_of(const Problem &pr, int b, int t) {
+  return pr.seq_idx ? __ldg(pr.seq_idx + (size_t)b * pr.L + t) : 0;
+}
+
+// Product of the per-token decays over chunk c of row b, head h: the factor that
+// carries the state entering the chunk to its end.  Zero at the row start and
+// when a packed sequence starts inside the chunk.  acs_bh: chunk-local inclusive
+// cumsum of dt*A for (b, h), length L.
+__device__ __forceinline__ float chunk_decay(const Problem &pr, const float *acs_bh, int b, int c) {
+  if (c == 0) return 0.f;
+  int t0 = c * pr.Q, t1 = t0 + pr.Q - 1;
+  if (pr.seq_idx && seq_of(pr, b, t0 - 1) != seq_of(pr, b, t1)) return 0.f;
+  return expf(acs_bh[t1]);
+}
+
+__host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- workspace
+// Offsets (bytes) of every scratch buffer; computed identically on host and
+// used to carve one caller-provided workspace.
+struct Workspace {
+  size_t status;                               // int32 device status word
+  size_t u;                                    // (b, L, Cd) act dtype: post-conv activations
+  size_t dtv, acs;                             // (b, H, L) f32: dt, chunk-local cumsum of dt*A
+  size_t cb;                                   // (b, nc, G, Q, Q) f32: C_i . B_j per chunk
+  size_t sst;                                  // (b, nc, H, P, N) f32: chunk states, then local S_in
+  size_t sext, segin;                          // (b, S, H, P, N) f32
+  size_t ablk;                                 // (b, S, H) f32
+  // backward only
+  size_t dsl;                                  // (b, nc, H, P, N) f32: Y_off adjoint, then local dS at chunk ends
+  size_t gext, gout;                           // (b, S, H, P, N) f32
+  size_t du;                                   // (b, L, Cd) f32: grad of post-conv activations
+  size_t w;                                    // (b, nc, H, Q, Q) f32: dM o L o dt
+  size_t tok;                                  // 6 x (b, H, L) f32 per-token adjoint pieces
+  size_t dcp, dbp;                             // (b, L, H, N) f32 per-head dC / dB partials
+  size_t chs;                                  // 4 x (b, nc, H) f32 per-chunk scalars
+  size_t convp;                                // (b, ntb, Cd, 5) f32 conv parameter partials
+  size_t total;
+  int ntb;                                     // conv backward token blocks per row
+};
+
+inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward) {
+  Workspace w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t b = pr.b, L = pr.L, H = pr.H, P = pr.P, N = pr.N, G = pr.G, Q = pr.Q, S = pr.S, nc = pr.nc,
+               Cd = pr.Cd;
+  w.status = take(256);
+  w.u = take(b * L * Cd * elem_bytes);
+  w.dtv = take(b * H * L * 4);
+  w.acs = take(b * H * L * 4);
+  w.cb = take(b * nc * G * Q * Q * 4);
+  w.sst = take(b * nc * H * P * N * 4);
+  w.sext = take(b * S * H * P * N * 4);
+  w.segin = take(b * S * H * P * N * 4);
+  w.ablk = take(b * S * H * 4);
+  w.ntb = (int)((L + 255) / 256);
+  if (backward) {
+    w.dsl = take(b * nc * H * P * N * 4);
+    w.gext = take(b * S * H * P * N * 4);
+    w.gout = take(b * S * H * P * N * 4);
+    w.du = take(b * L * Cd * 4);
+    w.w = take(b * nc * H * Q * Q * 4);
+    w.tok = take(6 * b * H * L * 4);
+    w.dcp = take(b * L * H * N * 4);
+    w.dbp = take(b * L * H * N * 4);
+    w.chs = take(4 * b * nc * H * 4);
+    w.convp = take(b * (size_t)w.ntb * Cd * 5 * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace ssd

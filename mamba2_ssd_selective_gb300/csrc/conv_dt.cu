@@ -1,0 +1,252 @@
+// Depthwise causal conv1d (width 4) + SiLU over the xBC channels, its backward,
+// the dt preprocessing with the chunk-local cumsum of dt*A, the parameter-grad
+// reductions, and cu_seqlens -> seq_idx.
+//
+// The conv halo: a chunk/segment starting at token t0 reads the raw inputs of
+// tokens t0-3..t0-1, i.e. the previous segment's last d_conv-1 tokens (Megatron-LM
+// PR #6808 "Add state-passing context parallelism for Mamba2", description; the
+// conv must be adapted across shards: state-spaces/mamba issue #482 "Sequence
+// parallelism in the mixer").  Taps that cross a packed-sequence boundary are
+// zero (seq_idx, NeMo Automodel PR #1441 "feat: context-parallel with nemotron v3").
+#include "kernels.h"
+
+namespace ssd {
+
+template <typename T>
+__device__ __forceinline__ const T *raw_channel(const Problem &pr, int bb, int c, long long &stride) {
+  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
+  if (c < HP) {
+    stride = pr.xs;
+    return static_cast<const T *>(pr.x) + (size_t)bb * pr.L * pr.xs + c;
+  }
+  if (c < HP + GN) {
+    stride = pr.Bs;
+    return static_cast<const T *>(pr.B) + (size_t)bb * pr.L * pr.Bs + (c - HP);
+  }
+  stride = pr.Cs;
+  return static_cast<const T *>(pr.C) + (size_t)bb * pr.L * pr.Cs + (c - HP - GN);
+}
+
+__device__ __forceinline__ void grad_channel(const Problem &pr, const GradOut &go, int bb, int c, void *&base,
+                                             long long &stride, int elem) {
+  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
+  char *p;
+  if (c < HP) {
+    stride = go.dxs;
+    p = static_cast<char *>(go.dx) + ((size_t)bb * pr.L * go.dxs + c) * elem;
+  } else if (c < HP + GN) {
+    stride = go.dBs;
+    p = static_cast<char *>(go.dB) + ((size_t)bb * pr.L * go.dBs + (c - HP)) * elem;
+  } else {
+    stride = go.dCs;
+    p = static_cast<char *>(go.dC) + ((size_t)bb * pr.L * go.dCs + (c - HP - GN)) * elem;
+  }
+  base = p;
+}
+
+constexpr int kConvTok = 64;
+
+// u[b, t, c] = silu(conv_b[c] + sum_k w[c,k] * xr[t-3+k, c]), taps masked at row
+// start and at seq_idx changes.  One thread per channel walks kConvTok tokens.
+template <typename T>
+__global__ void __launch_bounds__(128) conv_fwd_kernel(Problem pr, T *__restrict__ u) {
+  const int c = blockIdx.x * 128 + threadIdx.x;
+  if (c >= pr.Cd) return;
+  const int t0 = blockIdx.y * kConvTok, bb = blockIdx.z;
+  const int t1 = min(pr.L, t0 + kConvTok);
+  long long st;
+  const T *src = raw_channel<T>(pr, bb, c, st);
+  const float w0 = pr.conv_w[c * 4 + 0], w1 = pr.conv_w[c * 4 + 1], w2 = pr.conv_w[c * 4 + 2],
+              w3 = pr.conv_w[c * 4 + 3], bias = pr.conv_b[c];
+  float r0 = 0.f, r1 = 0.f, r2 = 0.f;
+  int s0 = 0, s1 = 0, s2 = 0;
+  if (t0 - 3 >= 0) { r0 = to_f(src[(size_t)(t0 - 3) * st]); s0 = seq_of(pr, bb, t0 - 3); }
+  if (t0 - 2 >= 0) { r1 = to_f(src[(size_t)(t0 - 2) * st]); s1 = seq_of(pr, bb, t0 - 2); }
+  if (t0 - 1 >= 0) { r2 = to_f(src[(size_t)(t0 - 1) * st]); s2 = seq_of(pr, bb, t0 - 1); }
+  T *dst = u + (size_t)bb * pr.L * pr.Cd + c;
+  for (int t = t0; t < t1; ++t) {
+    const float rt = to_f(src[(size_t)t * st]);
+    const int sq = seq_of(pr, bb, t);
+    float v = bias + w3 * rt;
+    v += (s2 == sq) ? w2 * r2 : 0.f;  // r* = 0 before token 0
+    v += (s1 == sq) ? w1 * r1 : 0.f;
+    v += (s0 == sq) ? w0 * r0 : 0.f;
+    dst[(size_t)t * pr.Cd] = from_f<T>(v * sigmoid_f(v));
+    r0 = r1; r1 = r2; r2 = rt;
+    s0 = s1; s1 = s2; s2 = sq;
+  }
+}
+
+template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s) {
+  dim3 grid((pr.Cd + 127) / 128, (pr.L + kConvTok - 1) / kConvTok, pr.b);
+  conv_fwd_kernel<T><<<grid, 128, 0, s>>>(pr, u);
+}
+
+// dt = softplus(dt_raw + dt_bias); acs = inclusive cumsum of dt*A within each
+// chunk (A = -exp(A_log)).  One warp per (b, h, chunk); layouts (b, H, L).
+template <typename T>
+__global__ void __launch_bounds__(32) dt_prep_kernel(Problem pr, float *__restrict__ dtv, float *__restrict__ acs) {
+  const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z, lane = threadIdx.x;
+  const float A = -expf(pr.A_log[h]), bias = pr.dt_bias[h];
+  const T *dtr = static_cast<const T *>(pr.dt) + (size_t)bb * pr.L * pr.dts + h;
+  const size_t ob = ((size_t)bb * pr.H + h) * pr.L;
+  float carry = 0.f;
+  for (int i0 = 0; i0 < pr.Q; i0 += 32) {
+    const int t = c * pr.Q + i0 + lane;
+    const float d = softplus_f(to_f(dtr[(size_t)t * pr.dts]) + bias);
+    float v = d * A;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      float n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    v += carry;
+    dtv[ob + t] = d;
+    acs[ob + t] = v;
+    carry = __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *acs, cudaStream_t s) {
+  dt_prep_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 32, 0, s>>>(pr, dtv, acs);
+}
+
+// Conv + SiLU backward for one channel over a block of 256 tokens:
+//   dv = du * silu'(v);  dxr[s] = sum_k w[k] dv[s+3-k] (same sequence);
+//   per-block partials of dconv_w[c,k] = sum dv[t] xr[t-3+k] and dconv_b[c] = sum dv.
+// v is recomputed from the raw inputs.
+template <typename T>
+__global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
+                                                       float *__restrict__ convp, int ntb) {
+  const int c = blockIdx.x * 128 + threadIdx.x;
+  if (c >= pr.Cd) return;
+  const int blk = blockIdx.y, bb = blockIdx.z;
+  const int t0 = blk * 256, tend = min(pr.L, t0 + 256);
+  long long st;
+  const T *src = raw_channel<T>(pr, bb, c, st);
+  void *dbase;
+  long long dstride;
+  grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
+  T *dst = static_cast<T *>(dbase);
+  const float w0 = pr.conv_w[c * 4 + 0], w1 = pr.conv_w[c * 4 + 1], w2 = pr.conv_w[c * 4 + 2],
+              w3 = pr.conv_w[c * 4 + 3], bias = pr.conv_b[c];
+  float r0 = 0.f, r1 = 0.f, r2 = 0.f;
+  int s0 = 0, s1 = 0, s2 = 0;
+  if (t0 - 3 >= 0) { r0 = to_f(src[(size_t)(t0 - 3) * st]); s0 = seq_of(pr, bb, t0 - 3); }
+  if (t0 - 2 >= 0) { r1 = to_f(src[(size_t)(t0 - 2) * st]); s1 = seq_of(pr, bb, t0 - 2); }
+  if (t0 - 1 >= 0) { r2 = to_f(src[(size_t)(t0 - 1) * st]); s2 = seq_of(pr, bb, t0 - 1); }
+  // dv window for tokens t-3..t and their seq ids
+  float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+  int q0 = 0, q1 = 0, q2 = 0;
+  float dw0 = 0.f, dw1 = 0.f, dw2 = 0.f, dw3 = 0.f, db = 0.f;
+  const float *dub = du + (size_t)bb * pr.L * pr.Cd + c;
+  for (int t = t0; t < t0 + 256 + 3; ++t) {
+    float dvt = 0.f;
+    int sq = 0;
+    if (t < pr.L) {
+      const float rt = to_f(src[(size_t)t * st]);
+      sq = seq_of(pr, bb, t);
+      float v = bias + w3 * rt;
+      v += (s2 == sq) ? w2 * r2 : 0.f;
+      v += (s1 == sq) ? w1 * r1 : 0.f;
+      v += (s0 == sq) ? w0 * r0 : 0.f;
+      const float sg = sigmoid_f(v);
+      dvt = dub[(size_t)t * pr.Cd] * sg * (1.f + v * (1.f - sg));
+      if (t < tend) {
+        db += dvt;
+        dw3 += dvt * rt;
+        dw2 += (s2 == sq) ? dvt * r2 : 0.f;
+        dw1 += (s1 == sq) ? dvt * r1 : 0.f;
+        dw0 += (s0 == sq) ? dvt * r0 : 0.f;
+      }
+      r0 = r1; r1 = r2; r2 = rt;
+      s0 = s1; s1 = s2; s2 = sq;
+    }
+    // output token s = t - 3 reads dv[s..s+3] = (d0, d1, d2, dvt)
+    const int s = t - 3;
+    if (s >= t0 && s < tend) {
+      float g = w3 * d0;
+      g += (q1 == q0) ? w2 * d1 : 0.f;
+      g += (q2 == q0) ? w1 * d2 : 0.f;
+      g += (sq == q0) ? w0 * dvt : 0.f;
+      dst[(size_t)s * dstride] = from_f<T>(g);
+    }
+    d0 = d1; d1 = d2; d2 = dvt;
+    q0 = q1; q1 = q2; q2 = sq;
+  }
+  float *pp = convp + (((size_t)bb * ntb + blk) * pr.Cd + c) * 5;
+  pp[0] = dw0; pp[1] = dw1; pp[2] = dw2; pp[3] = dw3; pp[4] = db;
+}
+
+template <typename T>
+void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s) {
+  dim3 grid((pr.Cd + 127) / 128, ntb, pr.b);
+  conv_bwd_kernel<T><<<grid, 128, 0, s>>>(pr, du, go, convp, ntb);
+}
+
+// Parameter gradients: fixed-order sums of per-chunk / per-block partials.
+__global__ void param_reduce_kernel(Problem pr, const float *__restrict__ chs, const float *__restrict__ convp,
+                                    int ntb, float *ddt_bias, float *dA_log, float *dD, float *dconv_w,
+                                    float *dconv_b) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t nch = (size_t)pr.b * pr.nc * pr.H;
+  if (i < pr.H) {
+    float sb = 0.f, sa = 0.f, sd = 0.f;
+    for (int bb = 0; bb < pr.b; ++bb)
+      for (int c = 0; c < pr.nc; ++c) {
+        const size_t o = ((size_t)bb * pr.nc + c) * pr.H + i;
+        sb += chs[o];
+        sa += chs[nch + o];
+        sd += chs[2 * nch + o];
+      }
+    ddt_bias[i] = sb;
+    dA_log[i] = sa * (-expf(pr.A_log[i]));  // dA/dA_log = A
+    dD[i] = sd;
+  }
+  if (i < pr.Cd) {
+    float acc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int bb = 0; bb < pr.b; ++bb)
+      for (int k = 0; k < ntb; ++k) {
+        const float *pp = convp + (((size_t)bb * ntb + k) * pr.Cd + i) * 5;
+#pragma unroll
+        for (int q = 0; q < 5; ++q) acc[q] += pp[q];
+      }
+    for (int q = 0; q < 4; ++q) dconv_w[i * 4 + q] = acc[q];
+    dconv_b[i] = acc[4];
+  }
+}
+
+void launch_param_reduce(const Problem &pr, const float *chs, const float *convp, int ntb, float *ddt_bias,
+                         float *dA_log, float *dD, float *dconv_w, float *dconv_b, cudaStream_t s) {
+  const int n = pr.Cd > pr.H ? pr.Cd : pr.H;
+  param_reduce_kernel<<<(n + 127) / 128, 128, 0, s>>>(pr, chs, convp, ntb, ddt_bias, dA_log, dD, dconv_w, dconv_b);
+}
+
+__global__ void cu_seqlens_kernel(const int *__restrict__ cu, int nseq, int *__restrict__ seq_idx, int total) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  int lo = 0, hi = nseq;  // find i with cu[i] <= t < cu[i+1]
+  if (t < cu[0] || t >= cu[nseq]) {
+    seq_idx[t] = -1;
+    return;
+  }
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid;
+  }
+  seq_idx[t] = lo;
+}
+
+void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStream_t s) {
+  cu_seqlens_kernel<<<(total + 255) / 256, 256, 0, s>>>(cu, nseq, seq_idx, total);
+}
+
+template void launch_conv_fwd<float>(const Problem &, float *, cudaStream_t);
+template void launch_conv_fwd<__nv_bfloat16>(const Problem &, __nv_bfloat16 *, cudaStream_t);
+template void launch_dt_prep<float>(const Problem &, float *, float *, cudaStream_t);
+template void launch_dt_prep<__nv_bfloat16>(const Problem &, float *, float *, cudaStream_t);
+template void launch_conv_bwd<float>(const Problem &, const float *, const GradOut &, float *, int, cudaStream_t);
+template void launch_conv_bwd<__nv_bfloat16>(const Problem &, const float *, const GradOut &, float *, int,
+                                             cudaStream_t);
+
+}  // namespace ssd

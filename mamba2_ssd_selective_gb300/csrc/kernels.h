@@ -1,0 +1,55 @@
+// Host-side launchers of the libssd kernels (internal; not part of the ABI).
+#pragma once
+
+#include "common.cuh"
+
+namespace ssd {
+
+struct GradOut {  // raw-input gradient destinations (activation dtype)
+  void *dx, *dB, *dC, *ddt;
+  long long dxs, dBs, dCs, ddts;
+};
+
+// conv + dt (conv_dt.cu)
+template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s);
+template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *acs, cudaStream_t s);
+template <typename T>
+void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s);
+void launch_param_reduce(const Problem &pr, const float *chs, const float *convp, int ntb, float *ddt_bias,
+                         float *dA_log, float *dD, float *dconv_w, float *dconv_b, cudaStream_t s);
+void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStream_t s);
+
+// segment summaries and scans (scan.cu)
+void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s);
+void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, float *segin, float *final_state,
+                     cudaStream_t s);
+void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s);
+void launch_seg_rscan(const Problem &pr, const float *gext, const float *ablk, const float *dfinal, float *gout,
+                      cudaStream_t s);
+
+// fp32 SIMT chunk kernels (simt_chunk.cu)
+template <typename T> void launch_cb(const Problem &pr, const T *u, float *cb, cudaStream_t s);
+template <typename T>
+void launch_chunk_state(const Problem &pr, const T *u, const float *dtv, const float *acs, float *sst, cudaStream_t s);
+template <typename T>
+void launch_chunk_out(const Problem &pr, const T *u, const float *dtv, const float *acs, const float *cb,
+                      const float *sst, const float *segin, T *y, cudaStream_t s);
+template <typename T>
+void launch_chunk_z(const Problem &pr, const T *u, const T *dy, const float *acs, float *dsl, cudaStream_t s);
+template <typename T>
+void launch_chunk_w(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs, const float *cb,
+                    float *wbuf, float *tok, cudaStream_t s);
+template <typename T>
+void launch_chunk_dx(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs, const float *cb,
+                     const float *dsl, const float *gout, float *du, cudaStream_t s);
+template <typename T>
+void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
+                       const float *wbuf, const float *sst, const float *segin, const float *dsl, const float *gout,
+                       float *dcp, float *dbp, float *tok, cudaStream_t s);
+template <typename T>
+void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
+                     const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
+                     const GradOut &go, float *chs, cudaStream_t s);
+void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, float *du, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,124 @@
+// Segment summaries and the segment scans (forward and reverse).
+//
+// Megatron-LM PR #6808 "Add state-passing context parallelism for Mamba2"
+// (description): the SSD over one causal segment is affine in its initial
+// state, S_out = a_block * S_in + S_ext.  Each segment runs its chunk state
+// passing from a zero state, giving (S_ext, a_block); an exclusive causal scan
+// over the summaries, in fixed segment order, recovers each segment's true
+// initial state.  Backward mirrors it with a reverse boundary scan.
+//
+// On one GPU the summary exchange is a write to / read from device memory at a
+// kernel boundary.  Every element of the P x N state is independent, so one
+// thread owns one element and walks the chunks (or segments) in order: the
+// result is bit-identical from run to run.
+#include "kernels.h"
+
+namespace ssd {
+
+// Local pass of segment k: S <- a_c * S + Sc[c] over the segment's chunks from
+// S = 0.  Overwrites sst[c] (the chunk's own state contribution Sc) with the
+// local state entering the chunk, and writes S_ext[k] and a_block[k].
+__global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float *__restrict__ acs,
+                                                         float *__restrict__ sst, float *__restrict__ sext,
+                                                         float *__restrict__ ablk) {
+  const int PN = pr.P * pr.N;
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  float S = 0.f, prod = 1.f;
+  for (int c = k * pr.cps; c < (k + 1) * pr.cps; ++c) {
+    const float a = chunk_decay(pr, acs_bh, bb, c);
+    prod *= a;
+    if (e < PN) {
+      float *p = sst + (((size_t)bb * pr.nc + c) * pr.H + h) * PN + e;
+      const float sc = *p;
+      *p = S;
+      S = fmaf(a, S, sc);
+    }
+  }
+  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h);
+  if (e < PN) sext[so * PN + e] = S;
+  if (e == 0) ablk[so] = prod;
+}
+
+void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s) {
+  dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b * pr.S);
+  local_pass_kernel<<<grid, 256, 0, s>>>(pr, acs, sst, sext, ablk);
+}
+
+// Exclusive scan: S_in[0] = 0, S_in[k] = a_block[k-1] * S_in[k-1] + S_ext[k-1];
+// final state = a_block[S-1] * S_in[S-1] + S_ext[S-1].
+__global__ void __launch_bounds__(256) seg_scan_kernel(Problem pr, const float *__restrict__ sext,
+                                                       const float *__restrict__ ablk, float *__restrict__ segin,
+                                                       float *__restrict__ final_state) {
+  const int PN = pr.P * pr.N;
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  const int h = blockIdx.y, bb = blockIdx.z;
+  if (e >= PN) return;
+  float s = 0.f;
+  for (int k = 0; k < pr.S; ++k) {
+    const size_t so = ((size_t)bb * pr.S + k) * pr.H + h;
+    segin[so * PN + e] = s;
+    s = fmaf(ablk[so], s, sext[so * PN + e]);
+  }
+  if (final_state) final_state[((size_t)bb * pr.H + h) * PN + e] = s;
+}
+
+void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, float *segin, float *final_state,
+                     cudaStream_t s) {
+  dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b);
+  seg_scan_kernel<<<grid, 256, 0, s>>>(pr, sext, ablk, segin, final_state);
+}
+
+// Local reverse pass of segment k from dS = 0 at the segment end:
+//   dS_end[c] = dS;  dS <- Z[c] + a_c * dS   (c from the last chunk down)
+// where Z[c] (held in dsl on entry) is the adjoint the chunk's own outputs send
+// to the state entering it.  Overwrites dsl[c] with the local gradient at the
+// chunk's end and writes g_ext[k] = gradient w.r.t. the segment's initial state.
+__global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float *__restrict__ acs,
+                                                        float *__restrict__ dsl, float *__restrict__ gext) {
+  const int PN = pr.P * pr.N;
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
+  if (e >= PN) return;
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  float dS = 0.f;
+  for (int c = (k + 1) * pr.cps - 1; c >= k * pr.cps; --c) {
+    const float a = chunk_decay(pr, acs_bh, bb, c);
+    float *p = dsl + (((size_t)bb * pr.nc + c) * pr.H + h) * PN + e;
+    const float z = *p;
+    *p = dS;
+    dS = fmaf(a, dS, z);
+  }
+  gext[(((size_t)bb * pr.S + k) * pr.H + h) * PN + e] = dS;
+}
+
+void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s) {
+  dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b * pr.S);
+  local_rev_kernel<<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
+}
+
+// Reverse exclusive scan: G_out[S-1] = dfinal; G_out[k-1] = a_block[k]*G_out[k] + g_ext[k].
+// G_out[k] is the gradient w.r.t. the state at the end of segment k.
+__global__ void __launch_bounds__(256) seg_rscan_kernel(Problem pr, const float *__restrict__ gext,
+                                                        const float *__restrict__ ablk,
+                                                        const float *__restrict__ dfinal, float *__restrict__ gout) {
+  const int PN = pr.P * pr.N;
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  const int h = blockIdx.y, bb = blockIdx.z;
+  if (e >= PN) return;
+  float g = dfinal ? dfinal[((size_t)bb * pr.H + h) * PN + e] : 0.f;
+  for (int k = pr.S - 1; k >= 0; --k) {
+    const size_t so = ((size_t)bb * pr.S + k) * pr.H + h;
+    gout[so * PN + e] = g;
+    g = fmaf(ablk[so], g, gext[so * PN + e]);
+  }
+}
+
+void launch_seg_rscan(const Problem &pr, const float *gext, const float *ablk, const float *dfinal, float *gout,
+                      cudaStream_t s) {
+  dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b);
+  seg_rscan_kernel<<<grid, 256, 0, s>>>(pr, gext, ablk, dfinal, gout);
+}
+
+}  // namespace ssd

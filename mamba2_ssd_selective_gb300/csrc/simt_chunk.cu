@@ -1,0 +1,580 @@
+// Chunked SSD kernels on CUDA cores (fp32 FMA): the path for fp32 activations
+// and for shapes outside the tensor-core kernels' envelope.
+//
+// Chunked form (the Mamba2 chunked algorithm that state-spaces/mamba issue #482
+// "Sequence parallelism in the mixer" builds on).  For chunk c of Q tokens,
+// local index i, head h with group g, Acs = chunk-local inclusive cumsum of
+// dt*A, and masks for packed sequences:
+//   CB[i,j]   = C_i . B_j                                      (per group)
+//   Y_diag[i] = sum_{j<=i, same seq} CB[i,j] exp(Acs_i - Acs_j) dt_j x_j
+//   Sc        = sum_j exp(Acs_Q-1 - Acs_j) dt_j x_j (outer) B_j   (j in the last token's sequence)
+//   Y_off[i]  = exp(Acs_i) [seq_i = seq of the token before the chunk] C_i . S_in[c]
+//   y         = Y_diag + Y_off + D x
+// with S_in[c] = S_loc_in[c] + d_c * S_seg_in[k] (local state from the segment
+// pass plus the segment's true initial state carried by the decay d_c from the
+// segment start to the chunk start: the correction pass of Megatron-LM PR #6808
+// "Add state-passing context parallelism for Mamba2").
+//
+// Backward: the adjoints of the same expressions, with the true state S_in and
+// the true state gradient at each chunk end rebuilt from the local passes and
+// the segment scans.  Nothing here uses atomics; every reduction has a fixed order.
+#include "kernels.h"
+#include "simt_gemm.cuh"
+
+namespace ssd {
+
+namespace {
+
+struct ChunkIds {
+  int c, h, g, bb, t0;
+};
+
+__device__ __forceinline__ ChunkIds chunk_ids(const Problem &pr) {
+  ChunkIds id;
+  id.c = blockIdx.x;
+  id.h = blockIdx.y;
+  id.bb = blockIdx.z;
+  id.g = id.h / pr.hpg;
+  id.t0 = id.c * pr.Q;
+  return id;
+}
+
+// Shared per-chunk vectors: Acs, dt, seq ids, and three derived weights.
+struct ChunkVecs {
+  float acs[256], dt[256], em[256], wdt[256], w[256];
+  int seq[256];
+};
+
+// em[i]  = exp(Acs_i) * [token i continues the sequence of the token before the chunk]
+// w[j]   = exp(Acs_last - Acs_j) * [token j is in the last token's sequence]
+// wdt[j] = w[j] * dt_j
+__device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkIds &id, const float *dtv,
+                                                const float *acs, ChunkVecs &v) {
+  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const float *dt_bh = dtv + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const int Q = pr.Q;
+  const int seq_prev = id.c > 0 ? seq_of(pr, id.bb, id.t0 - 1) : 0;
+  const int seq_last = seq_of(pr, id.bb, id.t0 + Q - 1);
+  const float acs_last = acs_bh[Q - 1];
+  for (int i = threadIdx.x; i < Q; i += blockDim.x) {
+    const int sq = seq_of(pr, id.bb, id.t0 + i);
+    const float a = acs_bh[i], d = dt_bh[i];
+    v.acs[i] = a;
+    v.dt[i] = d;
+    v.seq[i] = sq;
+    v.em[i] = (id.c > 0 && sq == seq_prev) ? expf(a) : 0.f;
+    const float w = (sq == seq_last) ? expf(acs_last - a) : 0.f;
+    v.w[i] = w;
+    v.wdt[i] = w * d;
+  }
+  __syncthreads();
+}
+
+// decay carrying the segment's initial state to the start of chunk c
+__device__ __forceinline__ float decay_seg_to_chunk(const Problem &pr, const float *acs_bh, int bb, int c) {
+  const int c0 = (c / pr.cps) * pr.cps;
+  float d = 1.f;
+  for (int cc = c0; cc < c; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
+  return d;
+}
+
+// decay carrying the state at the end of chunk c to the end of its segment
+__device__ __forceinline__ float decay_chunk_to_seg_end(const Problem &pr, const float *acs_bh, int bb, int c) {
+  const int c1 = (c / pr.cps + 1) * pr.cps;
+  float d = 1.f;
+  for (int cc = c + 1; cc < c1; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
+  return d;
+}
+
+template <typename F>
+__device__ __forceinline__ void for_tile(const float (&acc)[4][4], int m0, int M, int n0, int Nn, F f) {
+  const int tm = threadIdx.x >> 4, tn = threadIdx.x & 15;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + tm * 4 + i, n = n0 + tn * 4 + j;
+      if (m < M && n < Nn) f(m, n, acc[i][j]);
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- forward
+
+template <typename T>
+__global__ void __launch_bounds__(256) cb_kernel(Problem pr, const T *__restrict__ u, float *__restrict__ cb) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  const int c = blockIdx.x, g = blockIdx.y, bb = blockIdx.z, Q = pr.Q, N = pr.N, Cd = pr.Cd;
+  const T *ub = u + ((size_t)bb * pr.L + (size_t)c * Q) * Cd;
+  const int offB = pr.H * pr.P + g * N, offC = pr.H * pr.P + pr.G * N + g * N;
+  float *out = cb + (((size_t)bb * pr.nc + c) * pr.G + g) * Q * Q;
+  auto fa = [&](int i, int n) { return to_f(ub[(size_t)i * Cd + offC + n]); };
+  auto fb = [&](int n, int j) { return to_f(ub[(size_t)j * Cd + offB + n]); };
+  for (int ti = 0; ti * kTile < Q; ++ti)
+    for (int tj = 0; tj <= ti; ++tj) {
+      float acc[4][4];
+      zero_acc(acc);
+      gemm_tile<true, false>(acc, ti * kTile, Q, tj * kTile, Q, 0, N, fa, fb, smem);
+      for_tile(acc, ti * kTile, Q, tj * kTile, Q, [&](int i, int j, float v) { out[(size_t)i * Q + j] = v; });
+    }
+}
+
+template <typename T> void launch_cb(const Problem &pr, const T *u, float *cb, cudaStream_t s) {
+  cb_kernel<T><<<dim3(pr.nc, pr.G, pr.b), 256, 0, s>>>(pr, u, cb);
+}
+
+// Sc[p, n] = sum_j wdt_j x_j[p] B_j[n]
+template <typename T>
+__global__ void __launch_bounds__(256) state_kernel(Problem pr, const T *__restrict__ u, const float *__restrict__ dtv,
+                                                    const float *__restrict__ acs, float *__restrict__ sst) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  __shared__ ChunkVecs v;
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N;
+  const T *ub = u + ((size_t)id.bb * pr.L + id.t0) * Cd;
+  const int offX = id.h * P, offB = pr.H * P + id.g * N;
+  float *out = sst + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
+  auto fa = [&](int p, int j) { return to_f(ub[(size_t)j * Cd + offX + p]) * v.wdt[j]; };
+  auto fb = [&](int j, int n) { return to_f(ub[(size_t)j * Cd + offB + n]); };
+  for (int tp = 0; tp * kTile < P; ++tp)
+    for (int tn = 0; tn * kTile < N; ++tn) {
+      float acc[4][4];
+      zero_acc(acc);
+      gemm_tile<false, true>(acc, tp * kTile, P, tn * kTile, N, 0, pr.Q, fa, fb, smem);
+      for_tile(acc, tp * kTile, P, tn * kTile, N, [&](int p, int n, float x) { out[(size_t)p * N + n] = x; });
+    }
+}
+
+template <typename T>
+void launch_chunk_state(const Problem &pr, const T *u, const float *dtv, const float *acs, float *sst, cudaStream_t s) {
+  state_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dtv, acs, sst);
+}
+
+// y = Y_diag + Y_off + D x
+template <typename T>
+__global__ void __launch_bounds__(256) out_kernel(Problem pr, const T *__restrict__ u, const float *__restrict__ dtv,
+                                                  const float *__restrict__ acs, const float *__restrict__ cb,
+                                                  const float *__restrict__ sst, const float *__restrict__ segin,
+                                                  T *__restrict__ y) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  __shared__ ChunkVecs v;
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
+  const T *ub = u + ((size_t)id.bb * pr.L + id.t0) * Cd;
+  const int offX = id.h * P, offC = HP + pr.G * N + id.g * N;
+  const float *cbm = cb + (((size_t)id.bb * pr.nc + id.c) * pr.G + id.g) * Q * Q;
+  const int k = id.c / pr.cps;
+  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
+  const float dc = decay_seg_to_chunk(pr, acs_bh, id.bb, id.c);
+  const float *sloc = sst + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
+  const float *sseg = segin + (((size_t)id.bb * pr.S + k) * pr.H + id.h) * P * N;
+  const float Dh = pr.D[id.h];
+  T *yb = y + ((size_t)id.bb * pr.L + id.t0) * HP + offX;
+  auto fa1 = [&](int i, int j) {
+    return (j <= i && v.seq[i] == v.seq[j]) ? cbm[(size_t)i * Q + j] * expf(v.acs[i] - v.acs[j]) * v.dt[j] : 0.f;
+  };
+  auto fb1 = [&](int j, int p) { return to_f(ub[(size_t)j * Cd + offX + p]); };
+  auto fa2 = [&](int i, int n) { return to_f(ub[(size_t)i * Cd + offC + n]) * v.em[i]; };
+  auto fb2 = [&](int n, int p) { return sloc[(size_t)p * N + n] + dc * sseg[(size_t)p * N + n]; };
+  for (int ti = 0; ti * kTile < Q; ++ti)
+    for (int tp = 0; tp * kTile < P; ++tp) {
+      float acc[4][4];
+      zero_acc(acc);
+      gemm_tile<true, true>(acc, ti * kTile, Q, tp * kTile, P, 0, min(Q, (ti + 1) * kTile), fa1, fb1, smem);
+      if (id.c > 0) gemm_tile<true, false>(acc, ti * kTile, Q, tp * kTile, P, 0, N, fa2, fb2, smem);
+      for_tile(acc, ti * kTile, Q, tp * kTile, P, [&](int i, int p, float x) {
+        yb[(size_t)i * HP + p] = from_f<T>(x + Dh * to_f(ub[(size_t)i * Cd + offX + p]));
+      });
+    }
+}
+
+template <typename T>
+void launch_chunk_out(const Problem &pr, const T *u, const float *dtv, const float *acs, const float *cb,
+                      const float *sst, const float *segin, T *y, cudaStream_t s) {
+  out_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dtv, acs, cb, sst, segin, y);
+}
+
+// ---------------------------------------------------------------- backward
+
+// Z[c][p, n] = sum_i em_i dy_i[p] C_i[n]: what the chunk's off-diagonal outputs
+// send back to the state entering the chunk.
+template <typename T>
+__global__ void __launch_bounds__(256) z_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
+                                                const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                float *__restrict__ dsl) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  __shared__ ChunkVecs v;
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
+  const T *ub = u + ((size_t)id.bb * pr.L + id.t0) * Cd;
+  const T *dyb = dy + ((size_t)id.bb * pr.L + id.t0) * HP + id.h * P;
+  const int offC = HP + pr.G * N + id.g * N;
+  float *out = dsl + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
+  auto fa = [&](int p, int i) { return to_f(dyb[(size_t)i * HP + p]); };
+  auto fb = [&](int i, int n) { return to_f(ub[(size_t)i * Cd + offC + n]) * v.em[i]; };
+  for (int tp = 0; tp * kTile < P; ++tp)
+    for (int tn = 0; tn * kTile < N; ++tn) {
+      float acc[4][4];
+      zero_acc(acc);
+      gemm_tile<false, true>(acc, tp * kTile, P, tn * kTile, N, 0, pr.Q, fa, fb, smem);
+      for_tile(acc, tp * kTile, P, tn * kTile, N, [&](int p, int n, float x) { out[(size_t)p * N + n] = x; });
+    }
+}
+
+template <typename T>
+void launch_chunk_z(const Problem &pr, const T *u, const T *dy, const float *acs, float *dsl, cudaStream_t s) {
+  // dtv is not needed by Z but load_chunk_vecs reads it; acs doubles as a valid pointer
+  z_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, acs, acs, dsl);
+}
+
+// W[i, j] = dM[i,j] CB[i,j] exp(Acs_i - Acs_j) dt_j (causal, same seq), with
+// dM = dy . x over P; plus per-token sums  vrow_i = sum_j W, vcol_dt_j = sum_i W,
+// vcol_j = sum_i W / dt_j.
+template <typename T>
+__global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
+                                                const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                const float *__restrict__ cb, float *__restrict__ wbuf,
+                                                float *__restrict__ tok) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  __shared__ ChunkVecs v;
+  __shared__ float rowacc[kTile], colacc_dt[256], colacc[256], scratch[8 * kTile];
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, Q = pr.Q, HP = pr.H * pr.P;
+  const T *ub = u + ((size_t)id.bb * pr.L + id.t0) * Cd;
+  const T *dyb = dy + ((size_t)id.bb * pr.L + id.t0) * HP + id.h * P;
+  const int offX = id.h * P;
+  const float *cbm = cb + (((size_t)id.bb * pr.nc + id.c) * pr.G + id.g) * Q * Q;
+  float *wm = wbuf + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * Q * Q;
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  for (int i = threadIdx.x; i < 256; i += 256) { colacc_dt[i] = 0.f; colacc[i] = 0.f; }
+  __syncthreads();
+  auto fa = [&](int i, int p) { return to_f(dyb[(size_t)i * HP + p]); };
+  auto fb = [&](int p, int j) { return to_f(ub[(size_t)j * Cd + offX + p]); };
+  const int tm = threadIdx.x >> 4, tn = threadIdx.x & 15;
+  for (int ti = 0; ti * kTile < Q; ++ti) {
+    if (threadIdx.x < kTile) rowacc[threadIdx.x] = 0.f;
+    __syncthreads();
+    for (int tj = 0; tj <= ti; ++tj) {
+      float acc[4][4], wv[4][4], vv[4][4];
+      zero_acc(acc);
+      gemm_tile<true, false>(acc, ti * kTile, Q, tj * kTile, Q, 0, P, fa, fb, smem);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b2 = 0; b2 < 4; ++b2) {
+          const int i = ti * kTile + tm * 4 + a, j = tj * kTile + tn * 4 + b2;
+          float V = 0.f;
+          if (i < Q && j < Q && j <= i && v.seq[i] == v.seq[j])
+            V = acc[a][b2] * cbm[(size_t)i * Q + j] * expf(v.acs[i] - v.acs[j]);
+          vv[a][b2] = V;
+          wv[a][b2] = (j < Q) ? V * v.dt[j] : 0.f;
+          if (i < Q && j < Q) wm[(size_t)i * Q + j] = wv[a][b2];
+        }
+      tile_rowsum_add(wv, rowacc);
+      tile_colsum_add(wv, colacc_dt + tj * kTile, scratch);
+      tile_colsum_add(vv, colacc + tj * kTile, scratch);
+    }
+    if (threadIdx.x < kTile && ti * kTile + threadIdx.x < Q) tok[0 * BHL + tb + ti * kTile + threadIdx.x] = rowacc[threadIdx.x];
+    __syncthreads();
+  }
+  for (int j = threadIdx.x; j < Q; j += 256) {
+    tok[1 * BHL + tb + j] = colacc_dt[j];
+    tok[2 * BHL + tb + j] = colacc[j];
+  }
+}
+
+template <typename T>
+void launch_chunk_w(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs, const float *cb,
+                    float *wbuf, float *tok, cudaStream_t s) {
+  w_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, cb, wbuf, tok);
+}
+
+// du_x[j, p] = sum_{i>=j} M[i,j] dy_i[p] + wdt_j sum_n B_j[n] dS_end[p,n] + D dy_j[p]
+template <typename T>
+__global__ void __launch_bounds__(256) dx_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
+                                                 const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                 const float *__restrict__ cb, const float *__restrict__ dsl,
+                                                 const float *__restrict__ gout, float *__restrict__ du) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  __shared__ ChunkVecs v;
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
+  const T *ub = u + ((size_t)id.bb * pr.L + id.t0) * Cd;
+  const T *dyb = dy + ((size_t)id.bb * pr.L + id.t0) * HP + id.h * P;
+  const int offX = id.h * P, offB = HP + id.g * N;
+  const float *cbm = cb + (((size_t)id.bb * pr.nc + id.c) * pr.G + id.g) * Q * Q;
+  const int k = id.c / pr.cps;
+  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
+  const float de = decay_chunk_to_seg_end(pr, acs_bh, id.bb, id.c);
+  const float *dsc = dsl + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
+  const float *gk = gout + (((size_t)id.bb * pr.S + k) * pr.H + id.h) * P * N;
+  const float Dh = pr.D[id.h];
+  float *dub = du + ((size_t)id.bb * pr.L + id.t0) * Cd + offX;
+  auto fa1 = [&](int j, int i) {
+    return (i >= j && v.seq[i] == v.seq[j]) ? cbm[(size_t)i * Q + j] * expf(v.acs[i] - v.acs[j]) * v.dt[j] : 0.f;
+  };
+  auto fb1 = [&](int i, int p) { return to_f(dyb[(size_t)i * HP + p]); };
+  auto fa2 = [&](int j, int n) { return to_f(ub[(size_t)j * Cd + offB + n]) * v.wdt[j]; };
+  auto fb2 = [&](int n, int p) { return dsc[(size_t)p * N + n] + de * gk[(size_t)p * N + n]; };
+  for (int tj = 0; tj * kTile < Q; ++tj)
+    for (int tp = 0; tp * kTile < P; ++tp) {
+      float acc[4][4];
+      zero_acc(acc);
+      gemm_tile<false, true>(acc, tj * kTile, Q, tp * kTile, P, tj * kTile, Q, fa1, fb1, smem);
+      gemm_tile<true, false>(acc, tj * kTile, Q, tp * kTile, P, 0, N, fa2, fb2, smem);
+      for_tile(acc, tj * kTile, Q, tp * kTile, P, [&](int j, int p, float x) {
+        dub[(size_t)j * Cd + p] = x + Dh * to_f(dyb[(size_t)j * HP + p]);
+      });
+    }
+}
+
+template <typename T>
+void launch_chunk_dx(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs, const float *cb,
+                     const float *dsl, const float *gout, float *du, cudaStream_t s) {
+  dx_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, cb, dsl, gout, du);
+}
+
+// Per-head partials of the B and C gradients:
+//   dC_h[i] = sum_{j<=i} W[i,j] B_j + em_i S_in^T dy_i
+//   dB_h[j] = sum_{i>=j} W[i,j] C_i + wdt_j dS_end^T x_j
+// plus per-token dots r_i = C_i . (em_i S_in^T dy_i) and q_j = B_j . (dS_end^T x_j).
+template <typename T>
+__global__ void __launch_bounds__(256) dcdb_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
+                                                   const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                   const float *__restrict__ wbuf, const float *__restrict__ sst,
+                                                   const float *__restrict__ segin, const float *__restrict__ dsl,
+                                                   const float *__restrict__ gout, float *__restrict__ dcp,
+                                                   float *__restrict__ dbp, float *__restrict__ tok) {
+  __shared__ __align__(16) float smem[kGemmSmemFloats];
+  __shared__ ChunkVecs v;
+  __shared__ float rowacc[kTile];
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P, H = pr.H;
+  const T *ub = u + ((size_t)id.bb * pr.L + id.t0) * Cd;
+  const T *dyb = dy + ((size_t)id.bb * pr.L + id.t0) * HP + id.h * P;
+  const int offX = id.h * P, offB = HP + id.g * N, offC = HP + pr.G * N + id.g * N;
+  const float *wm = wbuf + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * Q * Q;
+  const int k = id.c / pr.cps;
+  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
+  const float dc = decay_seg_to_chunk(pr, acs_bh, id.bb, id.c);
+  const float de = decay_chunk_to_seg_end(pr, acs_bh, id.bb, id.c);
+  const size_t so = (((size_t)id.bb * pr.S + k) * pr.H + id.h) * P * N;
+  const size_t co = (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
+  const float *sloc = sst + co, *sseg = segin + so, *dsc = dsl + co, *gk = gout + so;
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const int tm = threadIdx.x >> 4, tn = threadIdx.x & 15;
+  // ---- dC
+  {
+    auto fa2 = [&](int i, int p) { return to_f(dyb[(size_t)i * HP + p]) * v.em[i]; };
+    auto fb2 = [&](int p, int n) { return sloc[(size_t)p * N + n] + dc * sseg[(size_t)p * N + n]; };
+    auto fa1 = [&](int i, int j) { return wm[(size_t)i * Q + j]; };
+    auto fb1 = [&](int j, int n) { return to_f(ub[(size_t)j * Cd + offB + n]); };
+    for (int ti = 0; ti * kTile < Q; ++ti) {
+      if (threadIdx.x < kTile) rowacc[threadIdx.x] = 0.f;
+      __syncthreads();
+      for (int tq = 0; tq * kTile < N; ++tq) {
+        float acc[4][4], prod[4][4];
+        zero_acc(acc);
+        if (id.c > 0) gemm_tile<true, true>(acc, ti * kTile, Q, tq * kTile, N, 0, P, fa2, fb2, smem);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b2 = 0; b2 < 4; ++b2) {
+            const int i = ti * kTile + tm * 4 + a, n = tq * kTile + tn * 4 + b2;
+            prod[a][b2] = (i < Q && n < N) ? acc[a][b2] * to_f(ub[(size_t)i * Cd + offC + n]) : 0.f;
+          }
+        tile_rowsum_add(prod, rowacc);
+        gemm_tile<true, true>(acc, ti * kTile, Q, tq * kTile, N, 0, min(Q, (ti + 1) * kTile), fa1, fb1, smem);
+        for_tile(acc, ti * kTile, Q, tq * kTile, N, [&](int i, int n, float x) {
+          dcp[(((size_t)id.bb * pr.L + id.t0 + i) * H + id.h) * N + n] = x;
+        });
+      }
+      if (threadIdx.x < kTile && ti * kTile + threadIdx.x < Q) tok[3 * BHL + tb + ti * kTile + threadIdx.x] = rowacc[threadIdx.x];
+      __syncthreads();
+    }
+  }
+  // ---- dB
+  {
+    auto fa2 = [&](int j, int p) { return to_f(ub[(size_t)j * Cd + offX + p]); };
+    auto fb2 = [&](int p, int n) { return dsc[(size_t)p * N + n] + de * gk[(size_t)p * N + n]; };
+    auto fa1 = [&](int j, int i) { return wm[(size_t)i * Q + j]; };
+    auto fb1 = [&](int i, int n) { return to_f(ub[(size_t)i * Cd + offC + n]); };
+    for (int tj = 0; tj * kTile < Q; ++tj) {
+      if (threadIdx.x < kTile) rowacc[threadIdx.x] = 0.f;
+      __syncthreads();
+      for (int tq = 0; tq * kTile < N; ++tq) {
+        float acc[4][4], prod[4][4];
+        zero_acc(acc);
+        gemm_tile<true, true>(acc, tj * kTile, Q, tq * kTile, N, 0, P, fa2, fb2, smem);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b2 = 0; b2 < 4; ++b2) {
+            const int j = tj * kTile + tm * 4 + a, n = tq * kTile + tn * 4 + b2;
+            prod[a][b2] = (j < Q && n < N) ? acc[a][b2] * to_f(ub[(size_t)j * Cd + offB + n]) : 0.f;
+            acc[a][b2] *= (j < Q) ? v.wdt[j] : 0.f;
+          }
+        tile_rowsum_add(prod, rowacc);
+        gemm_tile<false, true>(acc, tj * kTile, Q, tq * kTile, N, tj * kTile, Q, fa1, fb1, smem);
+        for_tile(acc, tj * kTile, Q, tq * kTile, N, [&](int j, int n, float x) {
+          dbp[(((size_t)id.bb * pr.L + id.t0 + j) * H + id.h) * N + n] = x;
+        });
+      }
+      if (threadIdx.x < kTile && tj * kTile + threadIdx.x < Q) tok[4 * BHL + tb + tj * kTile + threadIdx.x] = rowacc[threadIdx.x];
+      __syncthreads();
+    }
+  }
+}
+
+template <typename T>
+void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
+                       const float *wbuf, const float *sst, const float *segin, const float *dsl, const float *gout,
+                       float *dcp, float *dbp, float *tok, cudaStream_t s) {
+  dcdb_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp,
+                                                          tok);
+}
+
+// dt / A / D gradients of one (chunk, head).  With dAcs_i the total adjoint of
+// the chunk-local cumsum:
+//   dAcs_i = vrow_i - vcol_dt_i + r_i - wdt_i q_i  (+ sum_j wdt_j q_j + a_c <dS_end, S_in> at the last token)
+//   d(dA_t) = sum_{i>=t} dAcs_i;   d dt_t = vcol_t + w_t q_t + A d(dA_t);   dA += dt_t d(dA_t)
+//   d dt_raw = d dt * sigmoid(dt_raw + dt_bias)
+template <typename T>
+__global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
+                                                     const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                     const float *__restrict__ sst, const float *__restrict__ segin,
+                                                     const float *__restrict__ dsl, const float *__restrict__ gout,
+                                                     const float *__restrict__ tok, GradOut go,
+                                                     float *__restrict__ chs) {
+  __shared__ ChunkVecs v;
+  __shared__ float red[8], dacs[256], dda[256];
+  const ChunkIds id = chunk_ids(pr);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
+  const int PN = P * N;
+  const int k = id.c / pr.cps;
+  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
+  const float dc = decay_seg_to_chunk(pr, acs_bh, id.bb, id.c);
+  const float de = decay_chunk_to_seg_end(pr, acs_bh, id.bb, id.c);
+  const float ac = chunk_decay(pr, acs_bh, id.bb, id.c);
+  const size_t so = (((size_t)id.bb * pr.S + k) * pr.H + id.h) * PN;
+  const size_t co = (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * PN;
+  // a_c <dS_end, S_in>
+  float part = 0.f;
+  if (ac != 0.f)
+    for (int e = threadIdx.x; e < PN; e += 256)
+      part += (dsl[co + e] + de * gout[so + e]) * (sst[co + e] + dc * segin[so + e]);
+  const float dec = ac * block_sum256(part, red);
+
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const int i = threadIdx.x;
+  const bool valid = i < Q;
+  float q = 0.f, wq = 0.f;
+  if (valid) {
+    q = tok[4 * BHL + tb + i];
+    wq = v.wdt[i] * q;
+  }
+  const float ssum = block_sum256(wq, red);
+  if (valid) {
+    float d = tok[0 * BHL + tb + i] - tok[1 * BHL + tb + i] + tok[3 * BHL + tb + i] - wq;
+    if (i == Q - 1) d += ssum + dec;
+    dacs[i] = d;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float run = 0.f;
+    for (int j = Q - 1; j >= 0; --j) {
+      run += dacs[j];
+      dda[j] = run;
+    }
+  }
+  __syncthreads();
+  const float A = -expf(pr.A_log[id.h]);
+  float dA_part = 0.f, dz = 0.f, dD_part = 0.f;
+  if (valid) {
+    const int t = id.t0 + i;
+    const float ddt = tok[2 * BHL + tb + i] + v.w[i] * q + A * dda[i];
+    dA_part = v.dt[i] * dda[i];
+    const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)id.bb * pr.L + t) * pr.dts + id.h;
+    const float z = to_f(*dtr) + pr.dt_bias[id.h];
+    dz = ddt * sigmoid_f(z);
+    T *dst = static_cast<T *>(go.ddt) + ((size_t)id.bb * pr.L + t) * go.ddts + id.h;
+    *dst = from_f<T>(dz);
+    const T *xr = u + ((size_t)id.bb * pr.L + t) * Cd + id.h * P;
+    const T *dyr = dy + ((size_t)id.bb * pr.L + t) * HP + id.h * P;
+    for (int p = 0; p < P; ++p) dD_part += to_f(dyr[p]) * to_f(xr[p]);
+  }
+  const float s_dA = block_sum256(dA_part, red);
+  const float s_dz = block_sum256(dz, red);
+  const float s_dD = block_sum256(dD_part, red);
+  if (threadIdx.x == 0) {
+    const size_t nch = (size_t)pr.b * pr.nc * pr.H;
+    const size_t o = ((size_t)id.bb * pr.nc + id.c) * pr.H + id.h;
+    chs[o] = s_dz;
+    chs[nch + o] = s_dA;
+    chs[2 * nch + o] = s_dD;
+  }
+}
+
+template <typename T>
+void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
+                     const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
+                     const GradOut &go, float *chs, cudaStream_t s) {
+  dt_bwd_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, go, chs);
+}
+
+// du_B[t, g, n] = sum_{h in g} dB_h[t, n], du_C likewise, in head order.
+__global__ void __launch_bounds__(256) bc_reduce_kernel(Problem pr, const float *__restrict__ dcp,
+                                                        const float *__restrict__ dbp, float *__restrict__ du) {
+  const int GN = pr.G * pr.N;
+  const int idx = blockIdx.y * 256 + threadIdx.x;
+  if (idx >= GN) return;
+  const int g = idx / pr.N, n = idx % pr.N;
+  const size_t tok = blockIdx.x;  // flat (b, t) token index
+  float sb = 0.f, sc = 0.f;
+  for (int h = g * pr.hpg; h < (g + 1) * pr.hpg; ++h) {
+    sb += dbp[(tok * pr.H + h) * pr.N + n];
+    sc += dcp[(tok * pr.H + h) * pr.N + n];
+  }
+  const int HP = pr.H * pr.P;
+  du[tok * pr.Cd + HP + idx] = sb;
+  du[tok * pr.Cd + HP + GN + idx] = sc;
+}
+
+void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, float *du, cudaStream_t s) {
+  dim3 grid((unsigned)((size_t)pr.b * pr.L), (pr.G * pr.N + 255) / 256);
+  bc_reduce_kernel<<<grid, 256, 0, s>>>(pr, dcp, dbp, du);
+}
+
+#define SSD_INST(T)                                                                                                  \
+  template void launch_cb<T>(const Problem &, const T *, float *, cudaStream_t);                                     \
+  template void launch_chunk_state<T>(const Problem &, const T *, const float *, const float *, float *,             \
+                                      cudaStream_t);                                                                 \
+  template void launch_chunk_out<T>(const Problem &, const T *, const float *, const float *, const float *,         \
+                                    const float *, const float *, T *, cudaStream_t);                                \
+  template void launch_chunk_z<T>(const Problem &, const T *, const T *, const float *, float *, cudaStream_t);      \
+  template void launch_chunk_w<T>(const Problem &, const T *, const T *, const float *, const float *, const float *, \
+                                  float *, float *, cudaStream_t);                                                   \
+  template void launch_chunk_dx<T>(const Problem &, const T *, const T *, const float *, const float *,              \
+                                   const float *, const float *, const float *, float *, cudaStream_t);              \
+  template void launch_chunk_dcdb<T>(const Problem &, const T *, const T *, const float *, const float *,            \
+                                     const float *, const float *, const float *, const float *, const float *,      \
+                                     float *, float *, float *, cudaStream_t);                                       \
+  template void launch_chunk_dt<T>(const Problem &, const T *, const T *, const float *, const float *,              \
+                                   const float *, const float *, const float *, const float *, const float *,        \
+                                   const GradOut &, float *, cudaStream_t);
+
+SSD_INST(float)
+SSD_INST(__nv_bfloat16)
+
+}  // namespace ssd

@@ -1,0 +1,105 @@
+"""GPU parity: libssd through its C ABI against the fp64 oracle (relative L2).
+
+Tolerances: 1e-4 for the fp32 path, 1e-2 for bf16 activations with fp32
+accumulation.  Shapes span several chunk tiles, partial tiles (chunk 96,
+headdim 32, dstate 40), group mapping (G > 1), packed sequences with edge
+cases (a boundary at a chunk start, at a segment start, sequences of 1-3
+tokens and sequences shorter than a chunk), every segment count 1..16, and the
+bitwise replay the pages require of summaries, scans and outputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mamba2_ssd_selective_gb300 as ssd
+from mamba2_ssd_selective_gb300.inputs import WORKLOADS, SsdShape, make_inputs
+from tests.gpu_util import TOL, compare_backward, compare_forward, gpu_backward, gpu_forward, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba2_ssd_selective_gb300.build import build
+
+    build()
+    ssd.load()
+
+
+def test_tiny_fp32_forward_backward(oracle_lib):
+    shape, dtype, seed = WORKLOADS["tiny-fp32"]
+    inp = make_inputs(shape, seed, dtype, dfinal=True)
+    got, _ = gpu_forward(shape, dtype, inp)
+    compare_forward(got, oracle_lib.forward(inp, shape), TOL[dtype])
+    g = gpu_backward(shape, dtype, inp)
+    compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
+
+
+SHAPES = [
+    (SsdShape(2, 1024, 8, 64, 128, 2, 256, 2), None),
+    (SsdShape(1, 768, 4, 64, 64, 1, 96, 4), None),
+    (SsdShape(1, 512, 6, 32, 40, 3, 64, 8), None),
+    # boundaries at token 256 (a chunk start), 512 (a segment start), 1-3 token
+    # sequences, and sequences shorter than a chunk
+    (SsdShape(1, 2048, 4, 64, 128, 1, 256, 4), [256, 256, 1, 2, 3, 90, 160, 700, 580]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape,seq", SHAPES)
+def test_forward_backward_parity(oracle_lib, shape, seq, dtype):
+    inp = make_inputs(shape, 7, dtype, dfinal=True, seq_lengths=seq)
+    got, _ = gpu_forward(shape, dtype, inp)
+    compare_forward(got, oracle_lib.forward(inp, shape), TOL[dtype])
+    g = gpu_backward(shape, dtype, inp)
+    compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
+
+
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
+def test_segment_count_sweep(oracle_lib, S):
+    shape = SsdShape(1, 4096, 4, 64, 128, 1, 256, S)
+    inp = make_inputs(shape, 8, "f32")
+    ref = oracle_lib.forward(inp, shape, n_segments=1)
+    got, _ = gpu_forward(shape, "f32", inp)
+    assert rel(got["y"], ref["y"]) <= TOL["f32"]
+    assert rel(got["final_state"], ref["final_state"]) <= TOL["f32"]
+    g = gpu_backward(shape, "f32", inp, use_dfinal=False)
+    compare_backward(g, oracle_lib.backward(inp, shape, use_dfinal=False), shape, TOL["f32"])
+
+
+def test_backward_recomputes_segment_states(oracle_lib):
+    shape = SsdShape(1, 1024, 4, 64, 128, 1, 128, 4)
+    inp = make_inputs(shape, 12, "bf16", dfinal=True)
+    a = gpu_backward(shape, "bf16", inp, pass_seg=True)
+    b = gpu_backward(shape, "bf16", inp, pass_seg=False)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_replay_is_bitwise_identical():
+    shape = SsdShape(2, 2048, 8, 64, 128, 1, 256, 4)
+    inp = make_inputs(shape, 3, "bf16", dfinal=True, seq_lengths=[700, 3, 1345])
+    r = ssd.SsdRunner(shape, "bf16")
+    t = to_dev(inp)
+    y1, f1, s1 = [x.clone() for x in r.forward(t)]
+    g1 = {k: v.clone() for k, v in r.backward(t, t["dy"], t["dfinal"], s1).items()}
+    y2, f2, s2 = r.forward(t)
+    g2 = r.backward(t, t["dy"], t["dfinal"], s2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(f1, f2) and torch.equal(s1, s2)
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+    assert ssd.ssd_device_status(r.workspace) == 0
+
+
+def test_cu_seqlens_to_seq_idx():
+    lens = [5, 1, 300, 2, 700]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    out = torch.empty(int(cu[-1]), dtype=torch.int32, device="cuda")
+    ssd.ssd_cu_seqlens_to_seq_idx(cu, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), np.repeat(np.arange(len(lens)), lens))
