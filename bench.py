@@ -260,7 +260,9 @@ def config_dict(shape, dtype, seed) -> dict:
             "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads, "headdim": shape.headdim,
             "dstate": shape.dstate, "ngroups": shape.ngroups, "d_conv": shape.d_conv, "chunk": shape.chunk,
             "n_segments": shape.n_segments, "activations": dtype, "seed": seed,
-            "l2": "inputs larger than L2 (xBC 285 MB, dy 268 MB per step)"}
+            "l2": f"inputs larger than L2 (xBC {shape.tokens * shape.conv_dim * (2 if dtype == 'bf16' else 4) / 1e6:.0f}"
+                  f" MB, dy {shape.tokens * shape.nheads * shape.headdim * (2 if dtype == 'bf16' else 4) / 1e6:.0f}"
+                  f" MB per step; L2 is 129 MB)"}
 
 
 # ---------------------------------------------------------------- our arm
@@ -375,9 +377,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     shape, dtype, seed = WORKLOADS[args.workload]
+    if args.batch is not None:
+        shape = shape.with_(batch=args.batch)
     if args.impl == "reference":
         run_reference(args, shape, dtype, seed)
     else:

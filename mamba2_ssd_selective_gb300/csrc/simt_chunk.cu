@@ -231,9 +231,10 @@ void launch_chunk_z(const Problem &pr, const T *u, const T *dy, const float *acs
   z_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, acs, acs, dsl);
 }
 
-// W[i, j] = dM[i,j] CB[i,j] exp(Acs_i - Acs_j) dt_j (causal, same seq), with
-// dM = dy . x over P; plus per-token sums  vrow_i = sum_j W, vcol_dt_j = sum_i W,
-// vcol_j = sum_i W / dt_j.
+// With dM[i,j] = dy_i . x_j (over P) and L = exp(Acs_i - Acs_j) (causal, same seq):
+//   W[i,j] = dM L dt_j       -- the adjoint of CB[i,j], stored for the dB / dC products
+//   V[i,j] = dM CB L         -- reduced to per-token sums for the dt / Acs adjoints:
+//   vrow_i = sum_j V dt_j,  vcol_dt_j = sum_i V dt_j,  vcol_j = sum_i V.
 template <typename T>
 __global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
                                                 const float *__restrict__ dtv, const float *__restrict__ acs,
@@ -269,12 +270,15 @@ __global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict_
 #pragma unroll
         for (int b2 = 0; b2 < 4; ++b2) {
           const int i = ti * kTile + tm * 4 + a, j = tj * kTile + tn * 4 + b2;
-          float V = 0.f;
-          if (i < Q && j < Q && j <= i && v.seq[i] == v.seq[j])
-            V = acc[a][b2] * cbm[(size_t)i * Q + j] * expf(v.acs[i] - v.acs[j]);
-          vv[a][b2] = V;
-          wv[a][b2] = (j < Q) ? V * v.dt[j] : 0.f;
-          if (i < Q && j < Q) wm[(size_t)i * Q + j] = wv[a][b2];
+          float dML = 0.f, cbij = 0.f;  // dM o L (masked) and CB
+          if (i < Q && j < Q && j <= i && v.seq[i] == v.seq[j]) {
+            dML = acc[a][b2] * expf(v.acs[i] - v.acs[j]);
+            cbij = cbm[(size_t)i * Q + j];
+          }
+          const float dtj = (j < Q) ? v.dt[j] : 0.f;
+          vv[a][b2] = dML * cbij;       // V = dM o CB o L
+          wv[a][b2] = vv[a][b2] * dtj;  // V o dt: the dt / Acs adjoint pieces
+          if (i < Q && j < Q) wm[(size_t)i * Q + j] = dML * dtj;  // adjoint of CB
         }
       tile_rowsum_add(wv, rowacc);
       tile_colsum_add(wv, colacc_dt + tj * kTile, scratch);
@@ -341,7 +345,7 @@ void launch_chunk_dx(const Problem &pr, const T *u, const T *dy, const float *dt
   dx_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, cb, dsl, gout, du);
 }
 
-// Per-head partials of the B and C gradients:
+// Per-head partials of the B and C gradients (W = dM o L o dt, the adjoint of CB):
 //   dC_h[i] = sum_{j<=i} W[i,j] B_j + em_i S_in^T dy_i
 //   dB_h[j] = sum_{i>=j} W[i,j] C_i + wdt_j dS_end^T x_j
 // plus per-token dots r_i = C_i . (em_i S_in^T dy_i) and q_j = B_j . (dS_end^T x_j).

@@ -62,6 +62,9 @@ def compare_forward(got: dict, ref: dict, tol: float, heads=None, rows=None):
     return errs
 
 
+REPORT_ONLY = {"ddt_bias_rel"}
+
+
 def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=None):
     rows = list(range(shape.batch)) if rows is None else rows
     h0, h1 = heads if heads else (0, shape.nheads)
@@ -74,10 +77,15 @@ def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=N
         errs.update({
             "dconv_w": rel(got["dconv_w"][ch], ref["dconv_w"]),
             "dconv_b": rel(got["dconv_b"][ch], ref["dconv_b"]) if np.any(ref["dconv_b"]) else 0.0,
-            "ddt_bias": rel(got["ddt_bias"][h0:h1], ref["ddt_bias"]),
+            # a sum over b*L tokens with heavy cancellation: its error is judged
+            # against the root-sum-square of its per-token terms (the scale that
+            # per-term rounding produces), not against the cancelled sum itself
+            "ddt_bias": float(np.linalg.norm(got["ddt_bias"][h0:h1] - ref["ddt_bias"])
+                              / np.linalg.norm(np.sqrt(np.sum(ref["ddt_raw"] ** 2, axis=(0, 1))))),
+            "ddt_bias_rel": rel(got["ddt_bias"][h0:h1], ref["ddt_bias"]),
             "dA_log": rel(got["dA_log"][h0:h1], ref["dA_log"]),
             "dD": rel(got["dD"][h0:h1], ref["dD"]),
         })
     for k, e in errs.items():
-        assert e <= tol, (k, e, errs)
+        assert k in REPORT_ONLY or e <= tol, (k, e, errs)
     return errs

@@ -187,6 +187,8 @@ def _loss(oracle_lib, inp, shape):
 @pytest.mark.parametrize("shape,seq", [
     (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), None),
     (SsdShape(1, 60, 2, 4, 3, 1, 8, 1), [17, 1, 2, 40]),
+    # longer than the oracle's 256-token checkpoint interval
+    (SsdShape(1, 600, 2, 3, 2, 1, 8, 1), [255, 1, 344]),
 ])
 def test_backward_matches_finite_differences(oracle_lib, shape, seq):
     inp = f64(make_inputs(shape, 23, "f32", dfinal=True, seq_lengths=seq))
