@@ -123,6 +123,25 @@ ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *
                         const float *seg_init_states, const ssd_grads *grads, void *workspace, size_t ws_bytes,
                         ssd_stream_t stream);
 
+/* Forward without any workspace argument, for callers that cannot allocate
+ * device memory: code running inside a host framework that owns every device
+ * allocation and forbids new ones after start-up (inference plugins, real-time
+ * serving loops), or code for which a cudaMalloc would synchronise the device
+ * and break its latency budget.  Same arguments, results and rules as
+ * ssd_forward minus the workspace.  The scratch is one fixed array of
+ * SSD_STATIC_SCRATCH_BYTES in the library's device memory (each GPU that loads
+ * the library holds it until the process exits); problems whose forward needs
+ * more (ssd_workspace_size(dims, 0) > SSD_STATIC_SCRATCH_BYTES) are rejected
+ * with SSD_ERR_WORKSPACE before anything is launched.  The first call on each
+ * device looks up the array's device address (make that first call before any
+ * stream capture); no call allocates or frees memory.  All calls share the one
+ * array, so calls whose GPU work may overlap (other streams, other host
+ * threads) race on it and must be serialised by the caller.  This entry point
+ * has no counterpart in the pages the method comes from. */
+#define SSD_STATIC_SCRATCH_BYTES (32u << 20)
+ssd_status ssd_forward_static(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
+                              float *seg_init_states, ssd_stream_t stream);
+
 /* seq_idx[t] = i for cu_seqlens[i] <= t < cu_seqlens[i+1], t in [0, total_tokens)
  * (NeMo Automodel PR #1441, Key changes: seq_idx computed from cu_seqlens).
  * cu_seqlens (nseq + 1) int32 device array, non-decreasing, cu_seqlens[0] = 0 and

@@ -16,6 +16,7 @@ import torch
 
 __all__ = [
     "SsdError", "SsdDims", "SsdInputs", "SsdGrads", "load", "ssd_workspace_size", "ssd_forward", "ssd_backward",
+    "ssd_forward_static", "STATIC_SCRATCH_BYTES",
     "ssd_cu_seqlens_to_seq_idx", "ssd_device_status", "ssd_status_string", "ssd_profile_begin",
     "ssd_profile_end", "SsdKernelTime", "SsdRunner",
     "SSD_BF16", "SSD_F32",
@@ -76,6 +77,8 @@ def load():
         lib.ssd_workspace_size.restype = S
         lib.ssd_forward.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(SsdInputs), P, P, P, P, S, P]
         lib.ssd_forward.restype = I
+        lib.ssd_forward_static.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(SsdInputs), P, P, P, P]
+        lib.ssd_forward_static.restype = I
         lib.ssd_backward.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(SsdInputs), P, P, P,
                                      ctypes.POINTER(SsdGrads), P, S, P]
         lib.ssd_backward.restype = I
@@ -127,6 +130,16 @@ def ssd_forward(dims: SsdDims, inputs: SsdInputs, y, final_state, seg_init_state
     ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
     _check(load().ssd_forward(ctypes.byref(dims), ctypes.byref(inputs), _ptr(y), _ptr(final_state),
                               _ptr(seg_init_states), _ptr(workspace), ws_bytes, _stream(stream)), "ssd_forward")
+
+
+def ssd_forward_static(dims: SsdDims, inputs: SsdInputs, y, final_state, seg_init_states, stream=None) -> None:
+    """ssd_forward without a workspace: the library's fixed device scratch array is
+    used instead (for callers that cannot allocate; see include/ssd.h)."""
+    _check(load().ssd_forward_static(ctypes.byref(dims), ctypes.byref(inputs), _ptr(y), _ptr(final_state),
+                                     _ptr(seg_init_states), _stream(stream)), "ssd_forward_static")
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def ssd_backward(dims: SsdDims, inputs: SsdInputs, dy, dfinal_state, seg_init_states, grads: SsdGrads, workspace,

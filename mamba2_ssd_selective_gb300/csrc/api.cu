@@ -1,6 +1,7 @@
 // libssd C ABI: argument validation, workspace carving and the launch sequence
 // of the forward and backward passes.  Nothing here allocates or synchronises.
 #include <cstring>
+#include <mutex>
 
 #include "kernels.h"
 #include "ssd.h"
@@ -178,6 +179,28 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
   return launch_status();
 }
 
+// Scratch of ssd_forward_static: a fixed array in the library's device memory,
+// so that the call allocates nothing.  Host code must not use the symbol as an
+// address; it looks up the device address once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[SSD_STATIC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+// device address of g_static_scratch on the current device (looked up on the
+// first call per device), or nullptr on failure
+void *static_scratch_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
+    g_static_ptr[dev] = p;
+  }
+  return g_static_ptr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -203,6 +226,28 @@ ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, floa
   if (!aligned(workspace, 256)) return SSD_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
+  if (dims->dtype == SSD_BF16)
+    return forward_impl<__nv_bfloat16>(pr, static_cast<__nv_bfloat16 *>(y), final_state, seg_init_states, ws, w, s);
+  return forward_impl<float>(pr, static_cast<float *>(y), final_state, seg_init_states, ws, w, s);
+}
+
+ssd_status ssd_forward_static(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
+                              float *seg_init_states, ssd_stream_t stream) {
+  ssd_status st = check_dims(dims);
+  if (st != SSD_OK) return st;
+  Problem pr;
+  st = check_inputs(dims, in, pr);
+  if (st != SSD_OK) return st;
+  if (!y) return SSD_ERR_NULL_PTR;
+  if (!aligned(y, 16) || (final_state && !aligned(final_state, 16)) ||
+      (seg_init_states && !aligned(seg_init_states, 16)))
+    return SSD_ERR_ALIGNMENT;
+  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false);
+  if (w.total > SSD_STATIC_SCRATCH_BYTES) return SSD_ERR_WORKSPACE;
+  void *scratch = static_scratch_ptr();
+  if (!scratch) return SSD_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(scratch);
   if (dims->dtype == SSD_BF16)
     return forward_impl<__nv_bfloat16>(pr, static_cast<__nv_bfloat16 *>(y), final_state, seg_init_states, ws, w, s);
   return forward_impl<float>(pr, static_cast<float *>(y), final_state, seg_init_states, ws, w, s);
