@@ -2,6 +2,7 @@
 // of the forward and backward passes.  Nothing here allocates or synchronises.
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ssd.h"
@@ -119,6 +120,16 @@ ssd_status launch_status() {
 }
 
 template <typename T>
+constexpr bool kIsBf16 = std::is_same<T, __nv_bfloat16>::value;
+
+// bf16 activations inside the tensor-core kernels' envelope take the tcgen05
+// chunk kernels; everything else (fp32 activations, other shapes) the CUDA-core ones
+template <typename T>
+bool use_tc(const Problem &pr) {
+  return kIsBf16<T> && tc_envelope(pr);
+}
+
+template <typename T>
 ssd_status forward_impl(const Problem &pr, T *y, float *final_state, float *segin_user, char *ws,
                         const Workspace &w, cudaStream_t s) {
   cudaMemsetAsync(ws + w.status, 0, sizeof(int), s);
@@ -127,13 +138,26 @@ ssd_status forward_impl(const Problem &pr, T *y, float *final_state, float *segi
   float *cb = reinterpret_cast<float *>(ws + w.cb), *sst = reinterpret_cast<float *>(ws + w.sst);
   float *sext = reinterpret_cast<float *>(ws + w.sext), *ablk = reinterpret_cast<float *>(ws + w.ablk);
   float *segin = segin_user ? segin_user : reinterpret_cast<float *>(ws + w.segin);
+  int *status = reinterpret_cast<int *>(ws + w.status);
+  const bool tc = use_tc<T>(pr);
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
-  SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
-  SSD_LAUNCH("chunk_state", launch_chunk_state<T>(pr, u, dtv, acs, sst, s));
+  if constexpr (kIsBf16<T>) {
+    if (tc) {
+      SSD_LAUNCH("tc_cb", launch_tc_cb(pr, u, cb, status, s));
+      SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));
+    }
+  }
+  if (!tc) {
+    SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
+    SSD_LAUNCH("chunk_state", launch_chunk_state<T>(pr, u, dtv, acs, sst, s));
+  }
   SSD_LAUNCH("local_pass", launch_local_pass(pr, acs, sst, sext, ablk, s));
   SSD_LAUNCH("seg_scan", launch_seg_scan(pr, sext, ablk, segin, final_state, s));
-  SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, y, s));
+  if constexpr (kIsBf16<T>) {
+    if (tc) SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, cb, sst, segin, y, status, s));
+  }
+  if (!tc) SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, y, s));
   return launch_status();
 }
 
@@ -151,11 +175,21 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
   float *dcp = reinterpret_cast<float *>(ws + w.dcp), *dbp = reinterpret_cast<float *>(ws + w.dbp);
   float *chs = reinterpret_cast<float *>(ws + w.chs), *convp = reinterpret_cast<float *>(ws + w.convp);
   GradOut go{g->dx, g->dB, g->dC, g->ddt, g->dx_tok_stride, g->dB_tok_stride, g->dC_tok_stride, g->ddt_tok_stride};
+  int *status = reinterpret_cast<int *>(ws + w.status);
+  const bool tc = use_tc<T>(pr);
   // recompute: conv, dt, CB, chunk states, local segment passes (and the scan)
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
-  SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
-  SSD_LAUNCH("chunk_state", launch_chunk_state<T>(pr, u, dtv, acs, sst, s));
+  if constexpr (kIsBf16<T>) {
+    if (tc) {
+      SSD_LAUNCH("tc_cb", launch_tc_cb(pr, u, cb, status, s));
+      SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));
+    }
+  }
+  if (!tc) {
+    SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
+    SSD_LAUNCH("chunk_state", launch_chunk_state<T>(pr, u, dtv, acs, sst, s));
+  }
   SSD_LAUNCH("local_pass", launch_local_pass(pr, acs, sst, sext, ablk, s));
   const float *segin = segin_user;
   if (!segin) {
@@ -164,14 +198,32 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
     segin = sg;
   }
   // reverse boundary scan
-  SSD_LAUNCH("chunk_z", launch_chunk_z<T>(pr, u, dy, acs, dsl, s));
+  if constexpr (kIsBf16<T>) {
+    if (tc) SSD_LAUNCH("tc_chunk_z", launch_tc_z(pr, u, dy, dtv, acs, dsl, status, s));
+  }
+  if (!tc) SSD_LAUNCH("chunk_z", launch_chunk_z<T>(pr, u, dy, acs, dsl, s));
   SSD_LAUNCH("local_rev", launch_local_rev(pr, acs, dsl, gext, s));
   SSD_LAUNCH("seg_rscan", launch_seg_rscan(pr, gext, ablk, dfinal, gout, s));
   // chunk gradients
-  SSD_LAUNCH("chunk_w", launch_chunk_w<T>(pr, u, dy, dtv, acs, cb, wbuf, tok, s));
-  SSD_LAUNCH("chunk_dx", launch_chunk_dx<T>(pr, u, dy, dtv, acs, cb, dsl, gout, du, s));
-  SSD_LAUNCH("chunk_dcdb", launch_chunk_dcdb<T>(pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, s));
-  SSD_LAUNCH("chunk_dt", launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, go, chs, s));
+  int vcol_parts = 1;
+  if constexpr (kIsBf16<T>) {
+    if (tc) {
+      __nv_bfloat16 *wb = reinterpret_cast<__nv_bfloat16 *>(wbuf);
+      SSD_LAUNCH("tc_chunk_w", launch_tc_w(pr, u, dy, dtv, acs, cb, wb, tok, status, s));
+      SSD_LAUNCH("tc_chunk_dx", launch_tc_dx(pr, u, dy, dtv, acs, cb, dsl, gout, du, status, s));
+      SSD_LAUNCH("tc_chunk_dcdb",
+                 launch_tc_dcdb(pr, u, dy, dtv, acs, wb, sst, segin, dsl, gout, dcp, dbp, tok, status, s));
+      vcol_parts = pr.Q / 128;
+    }
+  }
+  if (!tc) {
+    SSD_LAUNCH("chunk_w", launch_chunk_w<T>(pr, u, dy, dtv, acs, cb, wbuf, tok, s));
+    SSD_LAUNCH("chunk_dx", launch_chunk_dx<T>(pr, u, dy, dtv, acs, cb, dsl, gout, du, s));
+    SSD_LAUNCH("chunk_dcdb",
+               launch_chunk_dcdb<T>(pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, s));
+  }
+  SSD_LAUNCH("chunk_dt",
+             launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, go, chs, s));
   SSD_LAUNCH("bc_reduce", launch_bc_reduce(pr, dcp, dbp, du, s));
   // conv backward and parameter reductions
   SSD_LAUNCH("conv_bwd", launch_conv_bwd<T>(pr, du, go, convp, w.ntb, s));

@@ -1,0 +1,80 @@
+// Per-chunk vectors and decays shared by the chunk kernels (CUDA-core and
+// tensor-core variants).
+#pragma once
+
+#include "common.cuh"
+
+namespace ssd {
+struct ChunkIds {
+  int c, h, g, bb, t0;
+};
+
+__device__ __forceinline__ ChunkIds chunk_ids(const Problem &pr) {
+  ChunkIds id;
+  id.c = blockIdx.x;
+  id.h = blockIdx.y;
+  id.bb = blockIdx.z;
+  id.g = id.h / pr.hpg;
+  id.t0 = id.c * pr.Q;
+  return id;
+}
+
+__device__ __forceinline__ ChunkIds make_ids(const Problem &pr, int c, int h, int bb) {
+  ChunkIds id;
+  id.c = c;
+  id.h = h;
+  id.bb = bb;
+  id.g = h / pr.hpg;
+  id.t0 = c * pr.Q;
+  return id;
+}
+
+// Shared per-chunk vectors: Acs, dt, seq ids, and three derived weights.
+struct ChunkVecs {
+  float acs[256], dt[256], em[256], wdt[256], w[256];
+  int seq[256];
+};
+
+// em[i]  = exp(Acs_i) * [token i continues the sequence of the token before the chunk]
+// w[j]   = exp(Acs_last - Acs_j) * [token j is in the last token's sequence]
+// wdt[j] = w[j] * dt_j
+__device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkIds &id, const float *dtv,
+                                                const float *acs, ChunkVecs &v) {
+  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const float *dt_bh = dtv + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const int Q = pr.Q;
+  const int seq_prev = id.c > 0 ? seq_of(pr, id.bb, id.t0 - 1) : 0;
+  const int seq_last = seq_of(pr, id.bb, id.t0 + Q - 1);
+  const float acs_last = acs_bh[Q - 1];
+  for (int i = threadIdx.x; i < Q; i += blockDim.x) {
+    const int sq = seq_of(pr, id.bb, id.t0 + i);
+    const float a = acs_bh[i], d = dt_bh[i];
+    v.acs[i] = a;
+    v.dt[i] = d;
+    v.seq[i] = sq;
+    v.em[i] = (id.c > 0 && sq == seq_prev) ? expf(a) : 0.f;
+    const float w = (sq == seq_last) ? expf(acs_last - a) : 0.f;
+    v.w[i] = w;
+    v.wdt[i] = w * d;
+  }
+  __syncthreads();
+}
+
+// decay carrying the segment's initial state to the start of chunk c
+__device__ __forceinline__ float decay_seg_to_chunk(const Problem &pr, const float *acs_bh, int bb, int c) {
+  const int c0 = (c / pr.cps) * pr.cps;
+  float d = 1.f;
+  for (int cc = c0; cc < c; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
+  return d;
+}
+
+// decay carrying the state at the end of chunk c to the end of its segment
+__device__ __forceinline__ float decay_chunk_to_seg_end(const Problem &pr, const float *acs_bh, int bb, int c) {
+  const int c1 = (c / pr.cps + 1) * pr.cps;
+  float d = 1.f;
+  for (int cc = c + 1; cc < c1; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
+  return d;
+}
+
+
+}  // namespace ssd

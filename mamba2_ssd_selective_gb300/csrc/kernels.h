@@ -49,7 +49,28 @@ void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *
 template <typename T>
 void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
-                     const GradOut &go, float *chs, cudaStream_t s);
+                     int vcol_parts, const GradOut &go, float *chs, cudaStream_t s);
 void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, float *du, cudaStream_t s);
+
+// bf16 tensor-core chunk kernels (tc_chunk.cu); envelope: see tc_envelope()
+inline bool tc_envelope(const Problem &pr) {
+  return pr.P == 64 && pr.N == 128 && (pr.Q == 128 || pr.Q == 256) && pr.hpg % 2 == 0;
+}
+void launch_tc_cb(const Problem &pr, const __nv_bfloat16 *u, float *cb, int *status, cudaStream_t s);
+void launch_tc_state(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, float *sst,
+                     int *status, cudaStream_t s);
+void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, const float *cb,
+                   const float *sst, const float *segin, __nv_bfloat16 *y, int *status, cudaStream_t s);
+void launch_tc_z(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
+                 const float *acs, float *dsl, int *status, cudaStream_t s);
+void launch_tc_w(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
+                 const float *acs, const float *cb, __nv_bfloat16 *wbuf, float *tok, int *status, cudaStream_t s);
+void launch_tc_dx(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
+                  const float *acs, const float *cb, const float *dsl, const float *gout, float *du, int *status,
+                  cudaStream_t s);
+void launch_tc_dcdb(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
+                    const float *acs, const __nv_bfloat16 *wbuf, const float *sst, const float *segin,
+                    const float *dsl, const float *gout, float *dcp, float *dbp, float *tok, int *status,
+                    cudaStream_t s);
 
 }  // namespace ssd

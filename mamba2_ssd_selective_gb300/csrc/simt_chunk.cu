@@ -18,73 +18,13 @@
 // Backward: the adjoints of the same expressions, with the true state S_in and
 // the true state gradient at each chunk end rebuilt from the local passes and
 // the segment scans.  Nothing here uses atomics; every reduction has a fixed order.
+#include "chunk_common.cuh"
 #include "kernels.h"
 #include "simt_gemm.cuh"
 
 namespace ssd {
 
 namespace {
-
-struct ChunkIds {
-  int c, h, g, bb, t0;
-};
-
-__device__ __forceinline__ ChunkIds chunk_ids(const Problem &pr) {
-  ChunkIds id;
-  id.c = blockIdx.x;
-  id.h = blockIdx.y;
-  id.bb = blockIdx.z;
-  id.g = id.h / pr.hpg;
-  id.t0 = id.c * pr.Q;
-  return id;
-}
-
-// Shared per-chunk vectors: Acs, dt, seq ids, and three derived weights.
-struct ChunkVecs {
-  float acs[256], dt[256], em[256], wdt[256], w[256];
-  int seq[256];
-};
-
-// em[i]  = exp(Acs_i) * [token i continues the sequence of the token before the chunk]
-// w[j]   = exp(Acs_last - Acs_j) * [token j is in the last token's sequence]
-// wdt[j] = w[j] * dt_j
-__device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkIds &id, const float *dtv,
-                                                const float *acs, ChunkVecs &v) {
-  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
-  const float *dt_bh = dtv + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
-  const int Q = pr.Q;
-  const int seq_prev = id.c > 0 ? seq_of(pr, id.bb, id.t0 - 1) : 0;
-  const int seq_last = seq_of(pr, id.bb, id.t0 + Q - 1);
-  const float acs_last = acs_bh[Q - 1];
-  for (int i = threadIdx.x; i < Q; i += blockDim.x) {
-    const int sq = seq_of(pr, id.bb, id.t0 + i);
-    const float a = acs_bh[i], d = dt_bh[i];
-    v.acs[i] = a;
-    v.dt[i] = d;
-    v.seq[i] = sq;
-    v.em[i] = (id.c > 0 && sq == seq_prev) ? expf(a) : 0.f;
-    const float w = (sq == seq_last) ? expf(acs_last - a) : 0.f;
-    v.w[i] = w;
-    v.wdt[i] = w * d;
-  }
-  __syncthreads();
-}
-
-// decay carrying the segment's initial state to the start of chunk c
-__device__ __forceinline__ float decay_seg_to_chunk(const Problem &pr, const float *acs_bh, int bb, int c) {
-  const int c0 = (c / pr.cps) * pr.cps;
-  float d = 1.f;
-  for (int cc = c0; cc < c; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
-  return d;
-}
-
-// decay carrying the state at the end of chunk c to the end of its segment
-__device__ __forceinline__ float decay_chunk_to_seg_end(const Problem &pr, const float *acs_bh, int bb, int c) {
-  const int c1 = (c / pr.cps + 1) * pr.cps;
-  float d = 1.f;
-  for (int cc = c + 1; cc < c1; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
-  return d;
-}
 
 template <typename F>
 __device__ __forceinline__ void for_tile(const float (&acc)[4][4], int m0, int M, int n0, int Nn, F f) {
@@ -447,9 +387,10 @@ void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *
                                                           tok);
 }
 
-// dt / A / D gradients of one (chunk, head).  With dAcs_i the total adjoint of
-// the chunk-local cumsum:
-//   dAcs_i = vrow_i - vcol_dt_i + r_i - wdt_i q_i  (+ sum_j wdt_j q_j + a_c <dS_end, S_in> at the last token)
+// dt / A / D gradients of one (chunk, head).  With vcol = sum over the
+// vcol_parts per-row-tile partial column sums (tok[2], tok[5]) and dAcs_i the
+// total adjoint of the chunk-local cumsum:
+//   dAcs_i = vrow_i - dt_i vcol_i + r_i - wdt_i q_i  (+ sum_j wdt_j q_j + a_c <dS_end, S_in> at the last token)
 //   d(dA_t) = sum_{i>=t} dAcs_i;   d dt_t = vcol_t + w_t q_t + A d(dA_t);   dA += dt_t d(dA_t)
 //   d dt_raw = d dt * sigmoid(dt_raw + dt_bias)
 template <typename T>
@@ -457,7 +398,7 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
                                                      const float *__restrict__ dtv, const float *__restrict__ acs,
                                                      const float *__restrict__ sst, const float *__restrict__ segin,
                                                      const float *__restrict__ dsl, const float *__restrict__ gout,
-                                                     const float *__restrict__ tok, GradOut go,
+                                                     const float *__restrict__ tok, int vcol_parts, GradOut go,
                                                      float *__restrict__ chs) {
   __shared__ ChunkVecs v;
   __shared__ float red[8], dacs[256], dda[256];
@@ -483,14 +424,15 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
   const int i = threadIdx.x;
   const bool valid = i < Q;
-  float q = 0.f, wq = 0.f;
+  float q = 0.f, wq = 0.f, vcol = 0.f;
   if (valid) {
     q = tok[4 * BHL + tb + i];
     wq = v.wdt[i] * q;
   }
   const float ssum = block_sum256(wq, red);
   if (valid) {
-    float d = tok[0 * BHL + tb + i] - tok[1 * BHL + tb + i] + tok[3 * BHL + tb + i] - wq;
+    vcol = tok[2 * BHL + tb + i] + (vcol_parts > 1 ? tok[5 * BHL + tb + i] : 0.f);
+    float d = tok[0 * BHL + tb + i] - v.dt[i] * vcol + tok[3 * BHL + tb + i] - wq;
     if (i == Q - 1) d += ssum + dec;
     dacs[i] = d;
   }
@@ -507,7 +449,7 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   float dA_part = 0.f, dz = 0.f, dD_part = 0.f;
   if (valid) {
     const int t = id.t0 + i;
-    const float ddt = tok[2 * BHL + tb + i] + v.w[i] * q + A * dda[i];
+    const float ddt = vcol + v.w[i] * q + A * dda[i];
     dA_part = v.dt[i] * dda[i];
     const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)id.bb * pr.L + t) * pr.dts + id.h;
     const float z = to_f(*dtr) + pr.dt_bias[id.h];
@@ -533,8 +475,9 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
 template <typename T>
 void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
-                     const GradOut &go, float *chs, cudaStream_t s) {
-  dt_bwd_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, go, chs);
+                     int vcol_parts, const GradOut &go, float *chs, cudaStream_t s) {
+  dt_bwd_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok,
+                                                            vcol_parts, go, chs);
 }
 
 // du_B[t, g, n] = sum_{h in g} dB_h[t, n], du_C likewise, in head order.
@@ -575,7 +518,7 @@ void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, flo
                                      const float *, const float *, const float *, const float *, const float *,      \
                                      float *, float *, float *, cudaStream_t);                                       \
   template void launch_chunk_dt<T>(const Problem &, const T *, const T *, const float *, const float *,              \
-                                   const float *, const float *, const float *, const float *, const float *,        \
+                                   const float *, const float *, const float *, const float *, const float *, int,   \
                                    const GradOut &, float *, cudaStream_t);
 
 SSD_INST(float)

@@ -1,0 +1,608 @@
+// Chunk kernels of the bf16 path on the 5th-generation tensor cores (tcgen05,
+// accumulators in TMEM), built on tc_engine.cuh.  Same decomposition and the
+// same formulas as the CUDA-core kernels in simt_chunk.cu (the chunked form of
+// the Mamba2 SSD, with the state correction of Megatron-LM PR #6808 "Add
+// state-passing context parallelism for Mamba2"); here every contraction runs
+// as 128 x N x 16 bf16 MMAs with fp32 accumulation, and the masks, decays and
+// dt scalings are applied while the operands are staged into shared memory.
+//
+// Envelope (checked on the host): bf16 activations, headdim 64, dstate 128,
+// chunk 128 or 256, an even number of heads per group.  Row tiles are 128
+// tokens; a chunk has Q/128 of them.
+#include "chunk_common.cuh"
+#include "kernels.h"
+#include "tc_engine.cuh"
+
+namespace ssd {
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+using tc::K_MAJOR;
+using tc::MN_MAJOR;
+
+template <class E>
+constexpr int dyn_smem() {
+  return 1024 + E::RING_BYTES + E::BAR_BYTES + 16;
+}
+
+template <class E>
+struct Carve {
+  uint8_t *ring;
+  uint64_t *bars;
+  uint32_t *tslot;
+  __device__ Carve(uint8_t *raw) {
+    ring = tc::aligned_smem(raw);
+    bars = reinterpret_cast<uint64_t *>(ring + E::RING_BYTES);
+    tslot = reinterpret_cast<uint32_t *>(ring + E::RING_BYTES + E::BAR_BYTES);
+  }
+};
+
+template <class K>
+void set_smem(K kernel, int bytes) {
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+__device__ __forceinline__ void store_row_f32(float *dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- CB = C B^T
+// CTA = (chunk, row tile I, group, batch); for each column tile J <= I the
+// 128 x 128 block of C_i . B_j is written in fp32 (upper blocks never read).
+using EngCB = tc::Engine<128, 2>;
+__global__ void __launch_bounds__(128) tc_cb_kernel(Problem pr, const bf16 *__restrict__ u, float *__restrict__ cb,
+                                                    int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  Carve<EngCB> sm(smem_raw);
+  const int NTI = pr.Q / 128;
+  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, g = blockIdx.y, bb = blockIdx.z;
+  const int Cd = pr.Cd, Q = pr.Q, N = pr.N, HP = pr.H * pr.P;
+  const bf16 *ub = u + ((size_t)bb * pr.L + (size_t)c * Q) * Cd;
+  const int offB = HP + g * N, offC = HP + pr.G * N + g * N;
+  EngCB eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
+  auto fa = [&](int m, int k) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offC + k); };
+  for (int J = 0; J <= I; ++J) {
+    auto fb = [&](int n, int k) { return tc::ldg16(ub + (size_t)(128 * J + n) * Cd + offB + k); };
+    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, fb, k0 > 0);
+  }
+  eng.finish();
+  const int i = 128 * I + threadIdx.x;
+  float *out = cb + (((size_t)bb * pr.nc + c) * pr.G + g) * Q * Q + (size_t)i * Q;
+  for (int J = 0; J <= I; ++J)
+    for (int cc = 0; cc < 4; ++cc) {
+      float v[32];
+      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 128 * J + 32 * cc), v);
+      store_row_f32(out + 128 * J + 32 * cc, v);
+    }
+  tc::tmem_free_cta(tmem, 256);
+}
+
+void launch_tc_cb(const Problem &pr, const bf16 *u, float *cb, int *status, cudaStream_t s) {
+  static bool once = (set_smem(tc_cb_kernel, dyn_smem<EngCB>()), true);
+  (void)once;
+  tc_cb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.G, pr.b), 128, dyn_smem<EngCB>(), s>>>(pr, u, cb, status);
+}
+
+// ---------------------------------------------------------------- chunk states
+// Sc^T[n, (h, p)] = sum_j B_j[n] wdt_h,j x_j[h, p] for a pair of heads of one
+// group: M = n (128), N = 2 x 64, K = the chunk's tokens.
+using EngPair = tc::Engine<128, 2>;
+__global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *__restrict__ u,
+                                                       const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                       float *__restrict__ sst, int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ChunkVecs v0, v1;
+  Carve<EngPair> sm(smem_raw);
+  const int c = blockIdx.x, h0 = 2 * blockIdx.y, bb = blockIdx.z;
+  const ChunkIds id0 = make_ids(pr, c, h0, bb), id1 = make_ids(pr, c, h0 + 1, bb);
+  load_chunk_vecs(pr, id0, dtv, acs, v0);
+  load_chunk_vecs(pr, id1, dtv, acs, v1);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
+  const bf16 *ub = u + ((size_t)bb * pr.L + id0.t0) * Cd;
+  const int offB = HP + id0.g * N;
+  EngPair eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
+  auto fa = [&](int m0, int k) { return tc::ldg16(ub + (size_t)k * Cd + offB + m0); };
+  auto fb = [&](int n0, int k) {
+    const int hl = n0 >> 6, p0 = n0 & 63;
+    float x[8];
+    tc::unpack8(tc::ldg16(ub + (size_t)k * Cd + (h0 + hl) * P + p0), x);
+    const float s = hl ? v1.wdt[k] : v0.wdt[k];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] *= s;
+    return tc::pack8(x);
+  };
+  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 0);
+  eng.finish();
+  const int n = threadIdx.x;
+  for (int cc = 0; cc < 4; ++cc) {
+    float v[32];
+    sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), v);
+    const int hl = cc >> 1;
+    float *o = sst + (((size_t)bb * pr.nc + c) * pr.H + h0 + hl) * P * N + n;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) o[(size_t)((cc & 1) * 32 + q) * N] = v[q];
+  }
+  tc::tmem_free_cta(tmem, 128);
+}
+
+void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, float *sst, int *status,
+                     cudaStream_t s) {
+  static bool once = (set_smem(tc_state_kernel, dyn_smem<EngPair>()), true);
+  (void)once;
+  tc_state_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), 128, dyn_smem<EngPair>(), s>>>(pr, u, dtv, acs, sst, status);
+}
+
+// ---------------------------------------------------------------- output
+// CTA = (chunk, row tile I, head, batch):
+//   Y_diag = (CB o L o dt) X over j < 128(I+1),  Y_off = C S_in^T,
+//   y = Y_diag + em * Y_off + D x.
+using EngOut = tc::Engine<64, 3>;
+__global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
+                                                     const float *__restrict__ dtv, const float *__restrict__ acs,
+                                                     const float *__restrict__ cb, const float *__restrict__ sst,
+                                                     const float *__restrict__ segin, bf16 *__restrict__ y,
+                                                     int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ChunkVecs v;
+  Carve<EngOut> sm(smem_raw);
+  const int NTI = pr.Q / 128;
+  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
+  const ChunkIds id = make_ids(pr, c, h, bb);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
+  const bf16 *ub = u + ((size_t)bb * pr.L + id.t0) * Cd;
+  const int offX = h * P, offC = HP + pr.G * N + id.g * N;
+  const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
+  const int k = c / pr.cps;
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  const float dc = decay_seg_to_chunk(pr, acs_bh, bb, c);
+  const float *sloc = sst + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
+  const float *sseg = segin + (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
+  EngOut eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
+  auto fa1 = [&](int m, int k0) {
+    const int i = 128 * I + m;
+    float cv[8], r[8];
+    tc::ld8f(cbm + (size_t)i * Q + k0, cv);
+    const float ai = v.acs[i];
+    const int si = v.seq[i];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = k0 + q;
+      r[q] = (j <= i && v.seq[j] == si) ? cv[q] * expf(ai - v.acs[j]) * v.dt[j] : 0.f;
+    }
+    return tc::pack8(r);
+  };
+  auto fb1 = [&](int n0, int j) { return tc::ldg16(ub + (size_t)j * Cd + offX + n0); };
+  for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa1, fb1, k0 > 0);
+  const bool has_off = c > 0;
+  if (has_off) {
+    auto fa2 = [&](int m, int k0) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offC + k0); };
+    auto fb2 = [&](int p, int k0) {
+      float a[8], b[8];
+      tc::ld8f(sloc + (size_t)p * N + k0, a);
+      tc::ld8f(sseg + (size_t)p * N + k0, b);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[q] += dc * b[q];
+      return tc::pack8(a);
+    };
+    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, fb2, k0 > 0);
+  }
+  eng.finish();
+  const int i = 128 * I + threadIdx.x;
+  const float em = v.em[i], Dh = pr.D[h];
+  const bf16 *xr = ub + (size_t)i * Cd + offX;
+  bf16 *yr = y + ((size_t)bb * pr.L + id.t0 + i) * HP + offX;
+  for (int cc = 0; cc < 2; ++cc) {
+    float yd[32], yo[32];
+    sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), yd);
+    if (has_off) sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 64 + 32 * cc), yo);
+#pragma unroll
+    for (int q8 = 0; q8 < 4; ++q8) {
+      float x[8], o[8];
+      tc::unpack8(tc::ldg16(xr + 32 * cc + 8 * q8), x);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = 8 * q8 + q;
+        o[q] = yd[col] + (has_off ? em * yo[col] : 0.f) + Dh * x[q];
+      }
+      *reinterpret_cast<uint4 *>(yr + 32 * cc + 8 * q8) = tc::pack8(o);
+    }
+  }
+  tc::tmem_free_cta(tmem, 128);
+}
+
+void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, const float *cb,
+                   const float *sst, const float *segin, bf16 *y, int *status, cudaStream_t s) {
+  static bool once = (set_smem(tc_out_kernel, dyn_smem<EngOut>()), true);
+  (void)once;
+  tc_out_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngOut>(), s>>>(pr, u, dtv, acs, cb, sst,
+                                                                                       segin, y, status);
+}
+
+// ---------------------------------------------------------------- backward: Z
+// Z^T[n, (h, p)] = sum_i C_i[n] em_h,i dy_i[h, p]  for a pair of heads.
+__global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__restrict__ u,
+                                                   const bf16 *__restrict__ dy, const float *__restrict__ dtv,
+                                                   const float *__restrict__ acs, float *__restrict__ dsl,
+                                                   int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ChunkVecs v0, v1;
+  Carve<EngPair> sm(smem_raw);
+  const int c = blockIdx.x, h0 = 2 * blockIdx.y, bb = blockIdx.z;
+  const ChunkIds id0 = make_ids(pr, c, h0, bb), id1 = make_ids(pr, c, h0 + 1, bb);
+  load_chunk_vecs(pr, id0, dtv, acs, v0);
+  load_chunk_vecs(pr, id1, dtv, acs, v1);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
+  const bf16 *ub = u + ((size_t)bb * pr.L + id0.t0) * Cd;
+  const bf16 *dyb = dy + ((size_t)bb * pr.L + id0.t0) * HP;
+  const int offC = HP + pr.G * N + id0.g * N;
+  EngPair eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
+  auto fa = [&](int m0, int i) { return tc::ldg16(ub + (size_t)i * Cd + offC + m0); };
+  auto fb = [&](int n0, int i) {
+    const int hl = n0 >> 6, p0 = n0 & 63;
+    float x[8];
+    tc::unpack8(tc::ldg16(dyb + (size_t)i * HP + (h0 + hl) * P + p0), x);
+    const float s = hl ? v1.em[i] : v0.em[i];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] *= s;
+    return tc::pack8(x);
+  };
+  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 0);
+  eng.finish();
+  const int n = threadIdx.x;
+  for (int cc = 0; cc < 4; ++cc) {
+    float vv[32];
+    sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), vv);
+    const int hl = cc >> 1;
+    float *o = dsl + (((size_t)bb * pr.nc + c) * pr.H + h0 + hl) * P * N + n;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) o[(size_t)((cc & 1) * 32 + q) * N] = vv[q];
+  }
+  tc::tmem_free_cta(tmem, 128);
+}
+
+void launch_tc_z(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs, float *dsl,
+                 int *status, cudaStream_t s) {
+  static bool once = (set_smem(tc_z_kernel, dyn_smem<EngPair>()), true);
+  (void)once;
+  tc_z_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), 128, dyn_smem<EngPair>(), s>>>(pr, u, dy, dtv, acs, dsl, status);
+}
+
+// ---------------------------------------------------------------- backward: W
+// dM = dy_i . x_j (K = P) per 128 x 128 block (J <= I); then, per element,
+//   W = dM L dt_j  (bf16, the adjoint of CB)   V = dM CB L
+// with row sums vrow_i = sum_j V dt_j (tok[0]) and this row tile's partial
+// column sums vcol_j = sum_i V (tok[2] for tile 0, tok[5] for tile 1).
+using EngW = tc::Engine<128, 2>;
+__global__ void __launch_bounds__(128) tc_w_kernel(Problem pr, const bf16 *__restrict__ u,
+                                                   const bf16 *__restrict__ dy, const float *__restrict__ dtv,
+                                                   const float *__restrict__ acs, const float *__restrict__ cb,
+                                                   bf16 *__restrict__ wbuf, float *__restrict__ tok, int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ChunkVecs v;
+  __shared__ float red[128][33];
+  __shared__ float part[4][32];
+  __shared__ float colacc[256];
+  Carve<EngW> sm(smem_raw);
+  const int NTI = pr.Q / 128;
+  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
+  const ChunkIds id = make_ids(pr, c, h, bb);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, Q = pr.Q, HP = pr.H * pr.P;
+  const bf16 *ub = u + ((size_t)bb * pr.L + id.t0) * Cd;
+  const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
+  const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
+  bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
+  for (int j = threadIdx.x; j < 256; j += 128) colacc[j] = 0.f;
+  EngW eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
+  auto fa = [&](int m, int k0) { return tc::ldg16(dyb + (size_t)(128 * I + m) * HP + k0); };
+  for (int J = 0; J <= I; ++J) {
+    auto fb = [&](int n, int k0) { return tc::ldg16(ub + (size_t)(128 * J + n) * Cd + h * P + k0); };
+    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, fb, k0 > 0);
+  }
+  eng.finish();
+  const int m = threadIdx.x, i = 128 * I + m;
+  const float ai = v.acs[i];
+  const int si = v.seq[i];
+  float rowsum = 0.f;
+  for (int J = 0; J <= I; ++J)
+    for (int cc = 0; cc < 4; ++cc) {
+      const int j0 = 128 * J + 32 * cc;
+      float a[32], cv[32], vv[32], wv[32];
+      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, j0), a);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float t8[8];
+        tc::ld8f(cbm + (size_t)i * Q + j0 + 8 * q8, t8);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) cv[8 * q8 + q] = t8[q];
+      }
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int j = j0 + q;
+        const float dml = (j <= i && v.seq[j] == si) ? a[q] * expf(ai - v.acs[j]) : 0.f;
+        vv[q] = dml * cv[q];
+        wv[q] = dml * v.dt[j];
+        rowsum += vv[q] * v.dt[j];
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float t8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t8[q] = wv[8 * q8 + q];
+        *reinterpret_cast<uint4 *>(wm + (size_t)i * Q + j0 + 8 * q8) = tc::pack8(t8);
+      }
+      // column sums over this tile's 128 rows, fixed order
+#pragma unroll
+      for (int q = 0; q < 32; ++q) red[m][q] = vv[q];
+      __syncthreads();
+      {
+        const int q = m & 31, quarter = m >> 5;
+        float s = 0.f;
+        for (int r = 0; r < 32; ++r) s += red[quarter * 32 + r][q];
+        part[quarter][q] = s;
+      }
+      __syncthreads();
+      if (m < 32) colacc[j0 + m] += (part[0][m] + part[1][m]) + (part[2][m] + part[3][m]);
+      __syncthreads();
+    }
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const size_t tb = ((size_t)bb * pr.H + h) * pr.L + id.t0;
+  tok[tb + i] = rowsum;
+  float *vcol = tok + (I == 0 ? 2 : 5) * BHL + tb;
+  for (int j = m; j < Q; j += 128) vcol[j] = colacc[j];
+  tc::tmem_free_cta(tmem, 256);
+}
+
+void launch_tc_w(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
+                 const float *cb, bf16 *wbuf, float *tok, int *status, cudaStream_t s) {
+  static bool once = (set_smem(tc_w_kernel, dyn_smem<EngW>()), true);
+  (void)once;
+  tc_w_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngW>(), s>>>(pr, u, dy, dtv, acs, cb, wbuf,
+                                                                                   tok, status);
+}
+
+// ---------------------------------------------------------------- backward: dX
+// rows j of tile I:  du_x[j] = sum_{i>=j} M[i,j] dy_i + wdt_j dS_end B_j + D dy_j
+using EngDx = tc::Engine<64, 3>;
+__global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
+                                                    const bf16 *__restrict__ dy, const float *__restrict__ dtv,
+                                                    const float *__restrict__ acs, const float *__restrict__ cb,
+                                                    const float *__restrict__ dsl, const float *__restrict__ gout,
+                                                    float *__restrict__ du, int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ChunkVecs v;
+  Carve<EngDx> sm(smem_raw);
+  const int NTI = pr.Q / 128;
+  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
+  const ChunkIds id = make_ids(pr, c, h, bb);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
+  const bf16 *ub = u + ((size_t)bb * pr.L + id.t0) * Cd;
+  const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
+  const int offB = HP + id.g * N;
+  const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
+  const int k = c / pr.cps;
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  const float de = decay_chunk_to_seg_end(pr, acs_bh, bb, c);
+  const float *dsc = dsl + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
+  const float *gk = gout + (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
+  EngDx eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 64);
+  auto fa1 = [&](int m0, int i) {
+    const int j0 = 128 * I + m0;
+    float cv[8], r[8];
+    tc::ld8f(cbm + (size_t)i * Q + j0, cv);
+    const float ai = v.acs[i];
+    const int si = v.seq[i];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = j0 + q;
+      r[q] = (j <= i && v.seq[j] == si) ? cv[q] * expf(ai - v.acs[j]) * v.dt[j] : 0.f;
+    }
+    return tc::pack8(r);
+  };
+  auto fb1 = [&](int n0, int i) { return tc::ldg16(dyb + (size_t)i * HP + n0); };
+  for (int k0 = 128 * I; k0 < Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1, fb1, k0 > 128 * I);
+  auto fa2 = [&](int m, int k0) {
+    const int j = 128 * I + m;
+    float b[8];
+    tc::unpack8(tc::ldg16(ub + (size_t)j * Cd + offB + k0), b);
+    const float s = v.wdt[j];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) b[q] *= s;
+    return tc::pack8(b);
+  };
+  auto fb2 = [&](int p, int k0) {
+    float a[8], b[8];
+    tc::ld8f(dsc + (size_t)p * N + k0, a);
+    tc::ld8f(gk + (size_t)p * N + k0, b);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) a[q] += de * b[q];
+    return tc::pack8(a);
+  };
+  for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem, k0, fa2, fb2, true);
+  eng.finish();
+  const int j = 128 * I + threadIdx.x;
+  const float Dh = pr.D[h];
+  float *dr = du + ((size_t)bb * pr.L + id.t0 + j) * Cd + h * P;
+  for (int cc = 0; cc < 2; ++cc) {
+    float a[32];
+    sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), a);
+#pragma unroll
+    for (int q8 = 0; q8 < 4; ++q8) {
+      float d8[8];
+      tc::unpack8(tc::ldg16(dyb + (size_t)j * HP + 32 * cc + 8 * q8), d8);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[8 * q8 + q] += Dh * d8[q];
+    }
+    store_row_f32(dr + 32 * cc, a);
+  }
+  tc::tmem_free_cta(tmem, 64);
+}
+
+void launch_tc_dx(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
+                  const float *cb, const float *dsl, const float *gout, float *du, int *status, cudaStream_t s) {
+  static bool once = (set_smem(tc_dx_kernel, dyn_smem<EngDx>()), true);
+  (void)once;
+  tc_dx_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngDx>(), s>>>(pr, u, dy, dtv, acs, cb, dsl,
+                                                                                     gout, du, status);
+}
+
+// ---------------------------------------------------------------- backward: dC, dB
+// Per-head partials.  Rows i of tile I:
+//   dC_h[i] = sum_{j<=i} W[i,j] B_j + em_i S_in^T dy_i,   r_i = C_i . (em_i S_in^T dy_i)
+// rows j of tile I:
+//   dB_h[j] = sum_{i>=j} W[i,j] C_i + wdt_j dS_end^T x_j, q_j = B_j . (dS_end^T x_j)
+using EngDcdb = tc::Engine<128, 2>;
+__global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__restrict__ u,
+                                                      const bf16 *__restrict__ dy, const float *__restrict__ dtv,
+                                                      const float *__restrict__ acs, const bf16 *__restrict__ wbuf,
+                                                      const float *__restrict__ sst, const float *__restrict__ segin,
+                                                      const float *__restrict__ dsl, const float *__restrict__ gout,
+                                                      float *__restrict__ dcp, float *__restrict__ dbp,
+                                                      float *__restrict__ tok, int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ChunkVecs v;
+  Carve<EngDcdb> sm(smem_raw);
+  const int NTI = pr.Q / 128;
+  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
+  const ChunkIds id = make_ids(pr, c, h, bb);
+  load_chunk_vecs(pr, id, dtv, acs, v);
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P, H = pr.H;
+  const bf16 *ub = u + ((size_t)bb * pr.L + id.t0) * Cd;
+  const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
+  const int offX = h * P, offB = HP + id.g * N, offC = HP + pr.G * N + id.g * N;
+  const bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
+  const int k = c / pr.cps;
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  const float dc = decay_seg_to_chunk(pr, acs_bh, bb, c);
+  const float de = decay_chunk_to_seg_end(pr, acs_bh, bb, c);
+  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
+  const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
+  const float *sloc = sst + co, *sseg = segin + so, *dsc = dsl + co, *gk = gout + so;
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const size_t tb = ((size_t)bb * pr.H + h) * pr.L + id.t0;
+  EngDcdb eng;
+  eng.init(sm.ring, sm.bars, status);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
+  const int m = threadIdx.x, r = 128 * I + m;  // row of this thread (i for dC, j for dB)
+  // ---- dC
+  const bool has_off = c > 0;
+  if (has_off) {
+    auto fa = [&](int mm, int p0) {
+      const int i = 128 * I + mm;
+      float d8[8];
+      tc::unpack8(tc::ldg16(dyb + (size_t)i * HP + p0), d8);
+      const float s = v.em[i];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) d8[q] *= s;
+      return tc::pack8(d8);
+    };
+    auto fb = [&](int n0, int p) {
+      float a[8], b[8];
+      tc::ld8f(sloc + (size_t)p * N + n0, a);
+      tc::ld8f(sseg + (size_t)p * N + n0, b);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[q] += dc * b[q];
+      return tc::pack8(a);
+    };
+    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, fb, k0 > 0);
+  }
+  {
+    auto fa = [&](int mm, int j0) { return tc::ldg16(wm + (size_t)(128 * I + mm) * Q + j0); };
+    auto fb = [&](int n0, int j) { return tc::ldg16(ub + (size_t)j * Cd + offB + n0); };
+    for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 0);
+  }
+  eng.finish();
+  {
+    float rsum = 0.f;
+    float *o = dcp + (((size_t)bb * pr.L + id.t0 + r) * H + h) * N;
+    for (int cc = 0; cc < 4; ++cc) {
+      float a[32], b[32];
+      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), a);
+      if (has_off) {
+        sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 128 + 32 * cc), b);
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float c8[8];
+          tc::unpack8(tc::ldg16(ub + (size_t)r * Cd + offC + 32 * cc + 8 * q8), c8);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) rsum += c8[q] * b[8 * q8 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) a[q] += b[q];
+      }
+      store_row_f32(o + 32 * cc, a);
+    }
+    tok[3 * BHL + tb + r] = rsum;
+  }
+  // ---- dB
+  {
+    auto fa = [&](int mm, int p0) { return tc::ldg16(ub + (size_t)(128 * I + mm) * Cd + offX + p0); };
+    auto fb = [&](int n0, int p) {
+      float a[8], b[8];
+      tc::ld8f(dsc + (size_t)p * N + n0, a);
+      tc::ld8f(gk + (size_t)p * N + n0, b);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[q] += de * b[q];
+      return tc::pack8(a);
+    };
+    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, fb, k0 > 0);
+  }
+  {
+    auto fa = [&](int m0, int i) { return tc::ldg16(wm + (size_t)i * Q + 128 * I + m0); };
+    auto fb = [&](int n0, int i) { return tc::ldg16(ub + (size_t)i * Cd + offC + n0); };
+    for (int k0 = 128 * I; k0 < Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 128 * I);
+  }
+  eng.finish();
+  {
+    float qsum = 0.f;
+    const float wdt = v.wdt[r];
+    float *o = dbp + (((size_t)bb * pr.L + id.t0 + r) * H + h) * N;
+    for (int cc = 0; cc < 4; ++cc) {
+      float a[32], b[32];
+      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), a);
+      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 128 + 32 * cc), b);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        float b8[8];
+        tc::unpack8(tc::ldg16(ub + (size_t)r * Cd + offB + 32 * cc + 8 * q8), b8);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) qsum += b8[q] * b[8 * q8 + q];
+      }
+#pragma unroll
+      for (int q = 0; q < 32; ++q) a[q] += wdt * b[q];
+      store_row_f32(o + 32 * cc, a);
+    }
+    tok[4 * BHL + tb + r] = qsum;
+  }
+  tc::tmem_free_cta(tmem, 256);
+}
+
+void launch_tc_dcdb(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
+                    const bf16 *wbuf, const float *sst, const float *segin, const float *dsl, const float *gout,
+                    float *dcp, float *dbp, float *tok, int *status, cudaStream_t s) {
+  static bool once = (set_smem(tc_dcdb_kernel, dyn_smem<EngDcdb>()), true);
+  (void)once;
+  tc_dcdb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngDcdb>(), s>>>(
+      pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, status);
+}
+
+}  // namespace ssd

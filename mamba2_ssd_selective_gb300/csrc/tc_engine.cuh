@@ -1,0 +1,187 @@
+// A small tcgen05 contraction engine for the chunk kernels of the bf16 path.
+//
+// One CTA of 128 threads owns a 128-row accumulator block in tensor memory
+// (TMEM lane = row).  A contraction  D[128 x NT] (+)= sum_k A[m,k] B[n,k]  is
+// fed 64 k at a time: every thread stages its share of the A and B tiles
+// straight into shared memory in the 128-byte-swizzled UMMA layout (so masks,
+// decays and scalings are applied while staging and nothing is materialised in
+// HBM), then one thread issues four 128 x NT x 16 tcgen05.mma and commits them
+// to the stage's mbarrier.  A ring of NSTAGE stages lets the staging of the
+// next 64-k slice overlap the tensor-core work of the previous ones.
+//
+// Operand functors return 8 bf16 values packed in a uint4:
+//   K-major operand:  f(m, k) -> elements (m, k .. k+7)
+//   MN-major operand: f(m, k) -> elements (m .. m+7, k)
+// (pick the one whose 8 elements are contiguous in the source).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "sm100.cuh"
+
+namespace ssd {
+namespace tc {
+
+using namespace sm100;
+
+enum Major : int { K_MAJOR = 0, MN_MAJOR = 1 };
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+__device__ __forceinline__ void unpack8(uint4 u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ void ld8f(const float *p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <int NT, int NSTAGE>
+struct Engine {
+  static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "UMMA N for M = 128");
+  static constexpr uint32_t A_BYTES = 128 * 128;  // 128 rows x 64 k bf16
+  static constexpr uint32_t B_BYTES = NT * 128;   // NT rows x 64 k bf16
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t RING_BYTES = NSTAGE * STAGE_BYTES;
+  static constexpr uint32_t BAR_BYTES = (NSTAGE + 1) * 8;
+
+  uint8_t *ring;   // 1024-aligned
+  uint64_t *bars;  // [0, NSTAGE): stage free;  [NSTAGE]: all issued MMAs done
+  int *status;
+  uint32_t uses[NSTAGE];
+  uint32_t done_uses;
+  int stage;
+
+  // call from all threads; thread 0 initialises the barriers (sync afterwards)
+  __device__ void init(uint8_t *ring_, uint64_t *bars_, int *status_) {
+    ring = ring_;
+    bars = bars_;
+    status = status_;
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) uses[s] = 0;
+    done_uses = 0;
+    stage = 0;
+    if (threadIdx.x == 0) {
+      for (int s = 0; s <= NSTAGE; ++s) mbar_init(&bars[s], 1);
+      fence_mbar_init();
+    }
+  }
+
+  template <int MA, class FA>
+  __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FA &fa) {
+    if constexpr (MA == K_MAJOR) {
+#pragma unroll 2
+      for (int e = threadIdx.x; e < 128 * 8; e += kThreads) {
+        const int m = e >> 3, c = e & 7;
+        *reinterpret_cast<uint4 *>(A + sw128_offset(m, c * 8)) = fa(m, k0 + c * 8);
+      }
+    } else {  // two 64-wide MN atoms, 64 k-rows each
+#pragma unroll 2
+      for (int e = threadIdx.x; e < 64 * 16; e += kThreads) {
+        const int r = e >> 4, c = e & 15;
+        *reinterpret_cast<uint4 *>(A + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8)) = fa(c * 8, k0 + r);
+      }
+    }
+  }
+
+  template <int MB, class FB>
+  __device__ __forceinline__ void stage_B(uint8_t *B, int k0, const FB &fb) {
+    if constexpr (MB == K_MAJOR) {
+#pragma unroll 2
+      for (int e = threadIdx.x; e < NT * 8; e += kThreads) {
+        const int n = e >> 3, c = e & 7;
+        *reinterpret_cast<uint4 *>(B + sw128_offset(n, c * 8)) = fb(n, k0 + c * 8);
+      }
+    } else {
+      static_assert(MB == K_MAJOR || NT % 64 == 0, "MN-major B needs whole 64-wide atoms");
+      constexpr int CPR = NT / 8;  // 16-byte chunks per k-row
+#pragma unroll 2
+      for (int e = threadIdx.x; e < 64 * CPR; e += kThreads) {
+        const int r = e / CPR, c = e % CPR;
+        *reinterpret_cast<uint4 *>(B + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8)) = fb(c * 8, k0 + r);
+      }
+    }
+  }
+
+  // Stage the 64-wide k slice [k0, k0+64) of A and B and issue its MMAs into the
+  // accumulator at TMEM address tmem_d.  Must be called by all 128 threads.
+  template <int MA, int MB, class FA, class FB>
+  __device__ __forceinline__ void slice(uint32_t tmem_d, int k0, const FA &fa, const FB &fb, bool accumulate) {
+    const int s = stage;
+    if (uses[s] > 0) mbar_wait(&bars[s], (uses[s] - 1) & 1, status);
+    uint8_t *A = ring + s * STAGE_BYTES;
+    uint8_t *B = A + A_BYTES;
+    stage_A<MA>(A, k0, fa);
+    stage_B<MB>(B, k0, fb);
+    fence_async_smem();
+    tc_fence_before();  // order this thread's earlier TMEM reads before the MMAs below
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+      constexpr uint32_t idesc = idesc_bf16(128, NT, MA == MN_MAJOR, MB == MN_MAJOR);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = MA == K_MAJOR ? desc_sw128(a0 + kk * 32, 16, 1024) : desc_sw128(a0 + kk * 2048, 8192, 1024);
+        const uint64_t bd = MB == K_MAJOR ? desc_sw128(b0 + kk * 32, 16, 1024) : desc_sw128(b0 + kk * 2048, 8192, 1024);
+        umma_bf16(tmem_d, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(&bars[s]);
+    }
+    uses[s] += 1;
+    stage = (s + 1 == NSTAGE) ? 0 : s + 1;
+  }
+
+  // Wait until every MMA issued so far has completed (all threads).
+  __device__ __forceinline__ void finish() {
+    if (threadIdx.x == 0) umma_commit(&bars[NSTAGE]);
+    mbar_wait(&bars[NSTAGE], done_uses & 1, status);
+    done_uses += 1;
+    tc_fence_after();
+  }
+};
+
+// Shared-memory carve-up helper for kernels built on the engine: returns the
+// 1024-aligned ring base inside the dynamic shared memory window.
+__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
+  const uint32_t a = smem_u32(raw);
+  return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// TMEM allocation by warp 0 of the CTA; returns the base address to all threads.
+__device__ __forceinline__ uint32_t tmem_alloc_cta(uint32_t *slot, uint32_t ncols) {
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *slot;
+}
+__device__ __forceinline__ void tmem_free_cta(uint32_t base, uint32_t ncols) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(base, ncols);
+}
+
+// TMEM address of (this thread's lane, column col) for a 128-thread CTA.
+__device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int col) {
+  return base + ((uint32_t)((threadIdx.x >> 5) * 32) << 16) + (uint32_t)col;
+}
+
+}  // namespace tc
+}  // namespace ssd
