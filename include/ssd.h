@@ -75,9 +75,9 @@ typedef struct {
  *   x  (b, L, H*P)  B (b, L, G*N)  C (b, L, G*N)  dt (b, L, H)
  * x, B, C: 16-byte aligned, token strides a multiple of 8 elements (bf16) or
  * 4 elements (fp32).  dt: element aligned, any token stride >= H.
- * Parameters (fp32, contiguous): dt_bias, A_log, D (H); conv_w (Cd, 4) where
- * tap 3 multiplies the current token; conv_b (Cd); Cd = H*P + 2*G*N and the
- * conv channel order is [x | B | C].
+ * Parameters (fp32, contiguous): dt_bias, A_log, D (H); conv_w (Cd, 4),
+ * 16-byte aligned, where tap 3 multiplies the current token; conv_b (Cd);
+ * Cd = H*P + 2*G*N and the conv channel order is [x | B | C].
  * seq_idx (b, L) int32, non-decreasing within a row, or NULL (one sequence per
  * row).  The state and the conv taps are reset where it changes. */
 typedef struct {

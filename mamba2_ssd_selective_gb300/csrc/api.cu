@@ -63,7 +63,7 @@ ssd_status check_inputs(const ssd_dims *d, const ssd_inputs *in, Problem &pr) {
   if (!aligned(in->x, 16) || !aligned(in->B, 16) || !aligned(in->C, 16) || !aligned(in->dt, eb) ||
       in->x_tok_stride % vec || in->B_tok_stride % vec || in->C_tok_stride % vec)
     return SSD_ERR_ALIGNMENT;
-  if (!aligned(in->dt_bias, 4) || !aligned(in->A_log, 4) || !aligned(in->D, 4) || !aligned(in->conv_w, 4) ||
+  if (!aligned(in->dt_bias, 4) || !aligned(in->A_log, 4) || !aligned(in->D, 4) || !aligned(in->conv_w, 16) ||
       !aligned(in->conv_b, 4) || (in->seq_idx && !aligned(in->seq_idx, 4)))
     return SSD_ERR_ALIGNMENT;
   pr = problem_from(d);

@@ -51,6 +51,8 @@ __device__ __forceinline__ float chunk_decay(const Problem &pr, const float *acs
 
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+constexpr int kConvBwdTok = 128;  // tokens per conv-backward block (one set of parameter partials each)
+
 // ---------------------------------------------------------------- workspace
 // Offsets (bytes) of every scratch buffer; computed identically on host and
 // used to carve one caller-provided workspace.
@@ -94,7 +96,7 @@ inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward
   w.sext = take(b * S * H * P * N * 4);
   w.segin = take(b * S * H * P * N * 4);
   w.ablk = take(b * S * H * 4);
-  w.ntb = (int)((L + 255) / 256);
+  w.ntb = (int)((L + kConvBwdTok - 1) / kConvBwdTok);
   if (backward) {
     w.dsl = take(b * nc * H * P * N * 4);
     w.gext = take(b * S * H * P * N * 4);

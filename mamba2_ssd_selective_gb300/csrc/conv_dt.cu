@@ -46,39 +46,83 @@ __device__ __forceinline__ void grad_channel(const Problem &pr, const GradOut &g
 
 constexpr int kConvTok = 64;
 
+// 8 consecutive channels of one token as fp32 (16-byte loads for bf16)
+template <typename T> __device__ __forceinline__ void load8(const T *p, float (&v)[8]);
+template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <> __device__ __forceinline__ void load8<float>(const float *p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <typename T> __device__ __forceinline__ void store8(T *p, const float (&v)[8]);
+template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *p, const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&b);
+  }
+  *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <> __device__ __forceinline__ void store8<float>(float *p, const float (&v)[8]) {
+  reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 // u[b, t, c] = silu(conv_b[c] + sum_k w[c,k] * xr[t-3+k, c]), taps masked at row
-// start and at seq_idx changes.  One thread per channel walks kConvTok tokens.
+// start and at seq_idx changes.  One thread owns 8 consecutive channels (every
+// part of [x | B | C] is a multiple of 8 wide) and walks kConvTok tokens.
 template <typename T>
 __global__ void __launch_bounds__(128) conv_fwd_kernel(Problem pr, T *__restrict__ u) {
-  const int c = blockIdx.x * 128 + threadIdx.x;
+  const int c = (blockIdx.x * 128 + threadIdx.x) * 8;
   if (c >= pr.Cd) return;
   const int t0 = blockIdx.y * kConvTok, bb = blockIdx.z;
   const int t1 = min(pr.L, t0 + kConvTok);
   long long st;
   const T *src = raw_channel<T>(pr, bb, c, st);
-  const float w0 = pr.conv_w[c * 4 + 0], w1 = pr.conv_w[c * 4 + 1], w2 = pr.conv_w[c * 4 + 2],
-              w3 = pr.conv_w[c * 4 + 3], bias = pr.conv_b[c];
-  float r0 = 0.f, r1 = 0.f, r2 = 0.f;
+  float w[8][4], bias[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
+    w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
+    bias[q] = pr.conv_b[c + q];
+  }
+  float r0[8], r1[8], r2[8];
   int s0 = 0, s1 = 0, s2 = 0;
-  if (t0 - 3 >= 0) { r0 = to_f(src[(size_t)(t0 - 3) * st]); s0 = seq_of(pr, bb, t0 - 3); }
-  if (t0 - 2 >= 0) { r1 = to_f(src[(size_t)(t0 - 2) * st]); s1 = seq_of(pr, bb, t0 - 2); }
-  if (t0 - 1 >= 0) { r2 = to_f(src[(size_t)(t0 - 1) * st]); s2 = seq_of(pr, bb, t0 - 1); }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) r0[q] = r1[q] = r2[q] = 0.f;
+  if (t0 - 3 >= 0) { load8(src + (size_t)(t0 - 3) * st, r0); s0 = seq_of(pr, bb, t0 - 3); }
+  if (t0 - 2 >= 0) { load8(src + (size_t)(t0 - 2) * st, r1); s1 = seq_of(pr, bb, t0 - 2); }
+  if (t0 - 1 >= 0) { load8(src + (size_t)(t0 - 1) * st, r2); s2 = seq_of(pr, bb, t0 - 1); }
   T *dst = u + (size_t)bb * pr.L * pr.Cd + c;
   for (int t = t0; t < t1; ++t) {
-    const float rt = to_f(src[(size_t)t * st]);
+    float rt[8], o[8];
+    load8(src + (size_t)t * st, rt);
     const int sq = seq_of(pr, bb, t);
-    float v = bias + w3 * rt;
-    v += (s2 == sq) ? w2 * r2 : 0.f;  // r* = 0 before token 0
-    v += (s1 == sq) ? w1 * r1 : 0.f;
-    v += (s0 == sq) ? w0 * r0 : 0.f;
-    dst[(size_t)t * pr.Cd] = from_f<T>(v * sigmoid_f(v));
-    r0 = r1; r1 = r2; r2 = rt;
+    const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;  // r* = 0 before token 0
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float v = bias[q] + w[q][3] * rt[q];
+      v += m2 ? w[q][2] * r2[q] : 0.f;
+      v += m1 ? w[q][1] * r1[q] : 0.f;
+      v += m0 ? w[q][0] * r0[q] : 0.f;
+      o[q] = v * sigmoid_f(v);
+      r0[q] = r1[q]; r1[q] = r2[q]; r2[q] = rt[q];
+    }
+    store8(dst + (size_t)t * pr.Cd, o);
     s0 = s1; s1 = s2; s2 = sq;
   }
 }
 
 template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s) {
-  dim3 grid((pr.Cd + 127) / 128, (pr.L + kConvTok - 1) / kConvTok, pr.b);
+  dim3 grid((pr.Cd / 8 + 127) / 128, (pr.L + kConvTok - 1) / kConvTok, pr.b);
   conv_fwd_kernel<T><<<grid, 128, 0, s>>>(pr, u);
 }
 
@@ -111,76 +155,102 @@ template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *
   dt_prep_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 32, 0, s>>>(pr, dtv, acs);
 }
 
-// Conv + SiLU backward for one channel over a block of 256 tokens:
+// Conv + SiLU backward for 8 channels over a block of kConvBwdTok tokens:
 //   dv = du * silu'(v);  dxr[s] = sum_k w[k] dv[s+3-k] (same sequence);
 //   per-block partials of dconv_w[c,k] = sum dv[t] xr[t-3+k] and dconv_b[c] = sum dv.
 // v is recomputed from the raw inputs.
 template <typename T>
 __global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
                                                        float *__restrict__ convp, int ntb) {
-  const int c = blockIdx.x * 128 + threadIdx.x;
+  const int c = (blockIdx.x * 128 + threadIdx.x) * 8;
   if (c >= pr.Cd) return;
   const int blk = blockIdx.y, bb = blockIdx.z;
-  const int t0 = blk * 256, tend = min(pr.L, t0 + 256);
+  const int t0 = blk * kConvBwdTok, tend = min(pr.L, t0 + kConvBwdTok);
   long long st;
   const T *src = raw_channel<T>(pr, bb, c, st);
   void *dbase;
   long long dstride;
   grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
   T *dst = static_cast<T *>(dbase);
-  const float w0 = pr.conv_w[c * 4 + 0], w1 = pr.conv_w[c * 4 + 1], w2 = pr.conv_w[c * 4 + 2],
-              w3 = pr.conv_w[c * 4 + 3], bias = pr.conv_b[c];
-  float r0 = 0.f, r1 = 0.f, r2 = 0.f;
-  int s0 = 0, s1 = 0, s2 = 0;
-  if (t0 - 3 >= 0) { r0 = to_f(src[(size_t)(t0 - 3) * st]); s0 = seq_of(pr, bb, t0 - 3); }
-  if (t0 - 2 >= 0) { r1 = to_f(src[(size_t)(t0 - 2) * st]); s1 = seq_of(pr, bb, t0 - 2); }
-  if (t0 - 1 >= 0) { r2 = to_f(src[(size_t)(t0 - 1) * st]); s2 = seq_of(pr, bb, t0 - 1); }
-  // dv window for tokens t-3..t and their seq ids
-  float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-  int q0 = 0, q1 = 0, q2 = 0;
-  float dw0 = 0.f, dw1 = 0.f, dw2 = 0.f, dw3 = 0.f, db = 0.f;
+  float w[8][4], bias[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
+    w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
+    bias[q] = pr.conv_b[c + q];
+  }
+  float r0[8], r1[8], r2[8], d0[8], d1[8], d2[8], dw[8][4], db[8];
+  int s0 = 0, s1 = 0, s2 = 0, q0 = 0, q1 = 0, q2 = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    r0[q] = r1[q] = r2[q] = d0[q] = d1[q] = d2[q] = db[q] = 0.f;
+    dw[q][0] = dw[q][1] = dw[q][2] = dw[q][3] = 0.f;
+  }
+  if (t0 - 3 >= 0) { load8(src + (size_t)(t0 - 3) * st, r0); s0 = seq_of(pr, bb, t0 - 3); }
+  if (t0 - 2 >= 0) { load8(src + (size_t)(t0 - 2) * st, r1); s1 = seq_of(pr, bb, t0 - 2); }
+  if (t0 - 1 >= 0) { load8(src + (size_t)(t0 - 1) * st, r2); s2 = seq_of(pr, bb, t0 - 1); }
   const float *dub = du + (size_t)bb * pr.L * pr.Cd + c;
-  for (int t = t0; t < t0 + 256 + 3; ++t) {
-    float dvt = 0.f;
+  for (int t = t0; t < t0 + kConvBwdTok + 3; ++t) {
+    float dvt[8];
     int sq = 0;
     if (t < pr.L) {
-      const float rt = to_f(src[(size_t)t * st]);
+      float rt[8], g8[8];
+      load8(src + (size_t)t * st, rt);
+      load8(dub + (size_t)t * pr.Cd, g8);
       sq = seq_of(pr, bb, t);
-      float v = bias + w3 * rt;
-      v += (s2 == sq) ? w2 * r2 : 0.f;
-      v += (s1 == sq) ? w1 * r1 : 0.f;
-      v += (s0 == sq) ? w0 * r0 : 0.f;
-      const float sg = sigmoid_f(v);
-      dvt = dub[(size_t)t * pr.Cd] * sg * (1.f + v * (1.f - sg));
-      if (t < tend) {
-        db += dvt;
-        dw3 += dvt * rt;
-        dw2 += (s2 == sq) ? dvt * r2 : 0.f;
-        dw1 += (s1 == sq) ? dvt * r1 : 0.f;
-        dw0 += (s0 == sq) ? dvt * r0 : 0.f;
+      const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;
+      const bool own = t < tend;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float v = bias[q] + w[q][3] * rt[q];
+        v += m2 ? w[q][2] * r2[q] : 0.f;
+        v += m1 ? w[q][1] * r1[q] : 0.f;
+        v += m0 ? w[q][0] * r0[q] : 0.f;
+        const float sg = sigmoid_f(v);
+        dvt[q] = g8[q] * sg * (1.f + v * (1.f - sg));
+        if (own) {
+          db[q] += dvt[q];
+          dw[q][3] += dvt[q] * rt[q];
+          dw[q][2] += m2 ? dvt[q] * r2[q] : 0.f;
+          dw[q][1] += m1 ? dvt[q] * r1[q] : 0.f;
+          dw[q][0] += m0 ? dvt[q] * r0[q] : 0.f;
+        }
+        r0[q] = r1[q]; r1[q] = r2[q]; r2[q] = rt[q];
       }
-      r0 = r1; r1 = r2; r2 = rt;
       s0 = s1; s1 = s2; s2 = sq;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dvt[q] = 0.f;
     }
     // output token s = t - 3 reads dv[s..s+3] = (d0, d1, d2, dvt)
     const int s = t - 3;
     if (s >= t0 && s < tend) {
-      float g = w3 * d0;
-      g += (q1 == q0) ? w2 * d1 : 0.f;
-      g += (q2 == q0) ? w1 * d2 : 0.f;
-      g += (sq == q0) ? w0 * dvt : 0.f;
-      dst[(size_t)s * dstride] = from_f<T>(g);
+      const bool m1 = q1 == q0, m2 = q2 == q0, m3 = sq == q0;
+      float g[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float a = w[q][3] * d0[q];
+        a += m1 ? w[q][2] * d1[q] : 0.f;
+        a += m2 ? w[q][1] * d2[q] : 0.f;
+        a += m3 ? w[q][0] * dvt[q] : 0.f;
+        g[q] = a;
+      }
+      store8(dst + (size_t)s * dstride, g);
     }
-    d0 = d1; d1 = d2; d2 = dvt;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { d0[q] = d1[q]; d1[q] = d2[q]; d2[q] = dvt[q]; }
     q0 = q1; q1 = q2; q2 = sq;
   }
-  float *pp = convp + (((size_t)bb * ntb + blk) * pr.Cd + c) * 5;
-  pp[0] = dw0; pp[1] = dw1; pp[2] = dw2; pp[3] = dw3; pp[4] = db;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float *pp = convp + (((size_t)bb * ntb + blk) * pr.Cd + c + q) * 5;
+    pp[0] = dw[q][0]; pp[1] = dw[q][1]; pp[2] = dw[q][2]; pp[3] = dw[q][3]; pp[4] = db[q];
+  }
 }
 
 template <typename T>
 void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s) {
-  dim3 grid((pr.Cd + 127) / 128, ntb, pr.b);
+  dim3 grid((pr.Cd / 8 + 127) / 128, ntb, pr.b);
   conv_bwd_kernel<T><<<grid, 128, 0, s>>>(pr, du, go, convp, ntb);
 }
 

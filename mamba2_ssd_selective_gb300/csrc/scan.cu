@@ -8,41 +8,62 @@
 // initial state.  Backward mirrors it with a reverse boundary scan.
 //
 // On one GPU the summary exchange is a write to / read from device memory at a
-// kernel boundary.  Every element of the P x N state is independent, so one
-// thread owns one element and walks the chunks (or segments) in order: the
+// kernel boundary.  Every element of the P x N state is independent, so each
+// thread owns a few elements and walks the chunks (or segments) in order: the
 // result is bit-identical from run to run.
 #include "kernels.h"
 
 namespace ssd {
 
+constexpr int kScanBatch = 8;  // chunks whose loads are in flight together
+
 // Local pass of segment k: S <- a_c * S + Sc[c] over the segment's chunks from
 // S = 0.  Overwrites sst[c] (the chunk's own state contribution Sc) with the
-// local state entering the chunk, and writes S_ext[k] and a_block[k].
+// local state entering the chunk, and writes S_ext[k] and a_block[k].  Each
+// thread owns 4 consecutive state elements (16-byte accesses) and keeps the
+// loads of kScanBatch chunks in flight; the chunk decays of a batch are
+// computed once per block.
 __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float *__restrict__ acs,
                                                          float *__restrict__ sst, float *__restrict__ sext,
                                                          float *__restrict__ ablk) {
-  const int PN = pr.P * pr.N;
-  const int e = blockIdx.x * 256 + threadIdx.x;
+  __shared__ float dec[kScanBatch];
+  const int PN = pr.P * pr.N, PN4 = PN / 4;
+  const int e4 = blockIdx.x * 256 + threadIdx.x;
+  const bool active = e4 < PN4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
   const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-  float S = 0.f, prod = 1.f;
-  for (int c = k * pr.cps; c < (k + 1) * pr.cps; ++c) {
-    const float a = chunk_decay(pr, acs_bh, bb, c);
-    prod *= a;
-    if (e < PN) {
-      float *p = sst + (((size_t)bb * pr.nc + c) * pr.H + h) * PN + e;
-      const float sc = *p;
-      *p = S;
-      S = fmaf(a, S, sc);
+  const size_t cstride = (size_t)pr.H * PN;  // floats between consecutive chunks
+  float4 *base = reinterpret_cast<float4 *>(sst + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN) + e4;
+  float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
+  float prod = 1.f;
+  for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
+    const int nb = min(kScanBatch, pr.cps - c0);
+    __syncthreads();
+    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, acs_bh, bb, k * pr.cps + c0 + threadIdx.x);
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int q = 0; q < nb; ++q) prod *= dec[q];
+    if (active) {
+      float4 v[kScanBatch];
+#pragma unroll
+      for (int q = 0; q < kScanBatch; ++q)
+        if (q < nb) v[q] = base[(size_t)(c0 + q) * (cstride / 4)];
+#pragma unroll
+      for (int q = 0; q < kScanBatch; ++q)
+        if (q < nb) {
+          base[(size_t)(c0 + q) * (cstride / 4)] = S;
+          const float a = dec[q];
+          S = make_float4(fmaf(a, S.x, v[q].x), fmaf(a, S.y, v[q].y), fmaf(a, S.z, v[q].z), fmaf(a, S.w, v[q].w));
+        }
     }
   }
   const size_t so = (((size_t)bb * pr.S + k) * pr.H + h);
-  if (e < PN) sext[so * PN + e] = S;
-  if (e == 0) ablk[so] = prod;
+  if (active) reinterpret_cast<float4 *>(sext + so * PN)[e4] = S;
+  if (blockIdx.x == 0 && threadIdx.x == 0) ablk[so] = prod;
 }
 
 void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s) {
-  dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b * pr.S);
+  dim3 grid((pr.P * pr.N / 4 + 255) / 256, pr.H, pr.b * pr.S);
   local_pass_kernel<<<grid, 256, 0, s>>>(pr, acs, sst, sext, ablk);
 }
 
@@ -75,26 +96,44 @@ void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, fl
 // where Z[c] (held in dsl on entry) is the adjoint the chunk's own outputs send
 // to the state entering it.  Overwrites dsl[c] with the local gradient at the
 // chunk's end and writes g_ext[k] = gradient w.r.t. the segment's initial state.
+// Same access pattern as local_pass_kernel, walking the chunks backwards.
 __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float *__restrict__ acs,
                                                         float *__restrict__ dsl, float *__restrict__ gext) {
-  const int PN = pr.P * pr.N;
-  const int e = blockIdx.x * 256 + threadIdx.x;
+  __shared__ float dec[kScanBatch];
+  const int PN = pr.P * pr.N, PN4 = PN / 4;
+  const int e4 = blockIdx.x * 256 + threadIdx.x;
+  const bool active = e4 < PN4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
-  if (e >= PN) return;
   const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-  float dS = 0.f;
-  for (int c = (k + 1) * pr.cps - 1; c >= k * pr.cps; --c) {
-    const float a = chunk_decay(pr, acs_bh, bb, c);
-    float *p = dsl + (((size_t)bb * pr.nc + c) * pr.H + h) * PN + e;
-    const float z = *p;
-    *p = dS;
-    dS = fmaf(a, dS, z);
+  const size_t cstride4 = (size_t)pr.H * PN / 4;
+  float4 *base = reinterpret_cast<float4 *>(dsl + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN) + e4;
+  float4 dS = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c1 = pr.cps; c1 > 0; c1 -= kScanBatch) {
+    const int nb = min(kScanBatch, c1);
+    const int c0 = c1 - nb;  // this batch covers chunks [c0, c1) of the segment, walked downwards
+    __syncthreads();
+    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, acs_bh, bb, k * pr.cps + c0 + threadIdx.x);
+    __syncthreads();
+    if (active) {
+      float4 z[kScanBatch];
+#pragma unroll
+      for (int q = 0; q < kScanBatch; ++q)
+        if (q < nb) z[q] = base[(size_t)(c0 + q) * cstride4];
+#pragma unroll
+      for (int q = kScanBatch - 1; q >= 0; --q)
+        if (q < nb) {
+          base[(size_t)(c0 + q) * cstride4] = dS;
+          const float a = dec[q];
+          dS = make_float4(fmaf(a, dS.x, z[q].x), fmaf(a, dS.y, z[q].y), fmaf(a, dS.z, z[q].z),
+                           fmaf(a, dS.w, z[q].w));
+        }
+    }
   }
-  gext[(((size_t)bb * pr.S + k) * pr.H + h) * PN + e] = dS;
+  if (active) reinterpret_cast<float4 *>(gext + (((size_t)bb * pr.S + k) * pr.H + h) * PN)[e4] = dS;
 }
 
 void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s) {
-  dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b * pr.S);
+  dim3 grid((pr.P * pr.N / 4 + 255) / 256, pr.H, pr.b * pr.S);
   local_rev_kernel<<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
 }
 

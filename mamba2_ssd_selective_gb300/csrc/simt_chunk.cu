@@ -415,9 +415,15 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   const size_t co = (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * PN;
   // a_c <dS_end, S_in>
   float part = 0.f;
-  if (ac != 0.f)
-    for (int e = threadIdx.x; e < PN; e += 256)
-      part += (dsl[co + e] + de * gout[so + e]) * (sst[co + e] + dc * segin[so + e]);
+  if (ac != 0.f) {
+    const float4 *a4 = reinterpret_cast<const float4 *>(dsl + co), *g4 = reinterpret_cast<const float4 *>(gout + so);
+    const float4 *s4 = reinterpret_cast<const float4 *>(sst + co), *q4 = reinterpret_cast<const float4 *>(segin + so);
+    for (int e = threadIdx.x; e < PN / 4; e += 256) {
+      const float4 a = a4[e], g = g4[e], x = s4[e], y = q4[e];
+      part += (a.x + de * g.x) * (x.x + dc * y.x) + (a.y + de * g.y) * (x.y + dc * y.y) +
+              (a.z + de * g.z) * (x.z + dc * y.z) + (a.w + de * g.w) * (x.w + dc * y.w);
+    }
+  }
   const float dec = ac * block_sum256(part, red);
 
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
