@@ -18,6 +18,8 @@
 // Backward: the adjoints of the same expressions, with the true state S_in and
 // the true state gradient at each chunk end rebuilt from the local passes and
 // the segment scans.  Nothing here uses atomics; every reduction has a fixed order.
+#include <type_traits>
+
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "simt_gemm.cuh"
@@ -443,14 +445,21 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
     dacs[i] = d;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float run = 0.f;
-    for (int j = Q - 1; j >= 0; --j) {
-      run += dacs[j];
-      dda[j] = run;
+  {  // suffix sums dda[i] = sum_{j >= i} dacs[j]: warp suffix scans, then warp totals (fixed order)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float x = valid ? dacs[i] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x += y;
     }
+    if (lane == 0) red[warp] = x;  // warp total
+    __syncthreads();
+    float later = 0.f;
+    for (int w2 = 7; w2 > warp; --w2) later += red[w2];
+    if (valid) dda[i] = x + later;
+    __syncthreads();
   }
-  __syncthreads();
   const float A = -expf(pr.A_log[id.h]);
   float dA_part = 0.f, dz = 0.f, dD_part = 0.f;
   if (valid) {
@@ -464,7 +473,18 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
     *dst = from_f<T>(dz);
     const T *xr = u + ((size_t)id.bb * pr.L + t) * Cd + id.h * P;
     const T *dyr = dy + ((size_t)id.bb * pr.L + t) * HP + id.h * P;
-    for (int p = 0; p < P; ++p) dD_part += to_f(dyr[p]) * to_f(xr[p]);
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+      for (int p = 0; p < P; p += 8) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(xr + p), b = *reinterpret_cast<const uint4 *>(dyr + p);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dD_part += __uint_as_float(wa[q] << 16) * __uint_as_float(wb[q] << 16) +
+                     __uint_as_float(wa[q] & 0xffff0000u) * __uint_as_float(wb[q] & 0xffff0000u);
+      }
+    } else {
+      for (int p = 0; p < P; ++p) dD_part += to_f(dyr[p]) * to_f(xr[p]);
+    }
   }
   const float s_dA = block_sum256(dA_part, red);
   const float s_dz = block_sum256(dz, red);

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(128) tc_cb_kernel(Problem pr, const bf16 *__re
   auto fa = [&](int m, int k) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offC + k); };
   for (int J = 0; J <= I; ++J) {
     auto fb = [&](int n, int k) { return tc::ldg16(ub + (size_t)(128 * J + n) * Cd + offB + k); };
-    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, fb, k0 > 0);
+    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 0);
   }
   eng.finish();
   const int i = 128 * I + threadIdx.x;
@@ -111,16 +111,16 @@ __global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *_
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
   auto fa = [&](int m0, int k) { return tc::ldg16(ub + (size_t)k * Cd + offB + m0); };
-  auto fb = [&](int n0, int k) {
-    const int hl = n0 >> 6, p0 = n0 & 63;
+  auto fbl = [&](int n0, int k) { return tc::ldg16(ub + (size_t)k * Cd + (h0 + (n0 >> 6)) * P + (n0 & 63)); };
+  auto fbm = [&](uint4 raw, int n0, int k) {
     float x[8];
-    tc::unpack8(tc::ldg16(ub + (size_t)k * Cd + (h0 + hl) * P + p0), x);
-    const float s = hl ? v1.wdt[k] : v0.wdt[k];
+    tc::unpack8(raw, x);
+    const float s = (n0 >> 6) ? v1.wdt[k] : v0.wdt[k];
 #pragma unroll
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 0);
+  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fbl, fbm, k0 > 0);
   eng.finish();
   const int n = threadIdx.x;
   for (int cc = 0; cc < 4; ++cc) {
@@ -145,7 +145,7 @@ void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const f
 // CTA = (chunk, row tile I, head, batch):
 //   Y_diag = (CB o L o dt) X over j < 128(I+1),  Y_off = C S_in^T,
 //   y = Y_diag + em * Y_off + D x.
-using EngOut = tc::Engine<64, 3>;
+using EngOut = tc::Engine<64, 2>;
 __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
                                                      const float *__restrict__ dtv, const float *__restrict__ acs,
                                                      const float *__restrict__ cb, const float *__restrict__ sst,
@@ -170,10 +170,11 @@ __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__r
   EngOut eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
-  auto fa1 = [&](int m, int k0) {
+  auto fa1l = [&](int m, int k0) { return tc::ldf8(cbm + (size_t)(128 * I + m) * Q + k0); };
+  auto fa1 = [&](const tc::F8 &raw, int m, int k0) {
     const int i = 128 * I + m;
     float cv[8], r[8];
-    tc::ld8f(cbm + (size_t)i * Q + k0, cv);
+    tc::f8_to(raw, cv);
     const float ai = v.acs[i];
     const int si = v.seq[i];
 #pragma unroll
@@ -184,19 +185,24 @@ __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__r
     return tc::pack8(r);
   };
   auto fb1 = [&](int n0, int j) { return tc::ldg16(ub + (size_t)j * Cd + offX + n0); };
-  for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa1, fb1, k0 > 0);
+  for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
+    eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::AsIs{}, k0 > 0);
   const bool has_off = c > 0;
   if (has_off) {
     auto fa2 = [&](int m, int k0) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offC + k0); };
-    auto fb2 = [&](int p, int k0) {
+    auto fb2l = [&](int p, int k0) {
+      return tc::F16{tc::ldf8(sloc + (size_t)p * N + k0), tc::ldf8(sseg + (size_t)p * N + k0)};
+    };
+    auto fb2 = [&](const tc::F16 &raw, int, int) {
       float a[8], b[8];
-      tc::ld8f(sloc + (size_t)p * N + k0, a);
-      tc::ld8f(sseg + (size_t)p * N + k0, b);
+      tc::f8_to(raw.x, a);
+      tc::f8_to(raw.y, b);
 #pragma unroll
       for (int q = 0; q < 8; ++q) a[q] += dc * b[q];
       return tc::pack8(a);
     };
-    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, fb2, k0 > 0);
+    for (int k0 = 0; k0 < N; k0 += 64)
+      eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::AsIs{}, fb2l, fb2, k0 > 0);
   }
   eng.finish();
   const int i = 128 * I + threadIdx.x;
@@ -251,16 +257,16 @@ __global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__res
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
   auto fa = [&](int m0, int i) { return tc::ldg16(ub + (size_t)i * Cd + offC + m0); };
-  auto fb = [&](int n0, int i) {
-    const int hl = n0 >> 6, p0 = n0 & 63;
+  auto fbl = [&](int n0, int i) { return tc::ldg16(dyb + (size_t)i * HP + (h0 + (n0 >> 6)) * P + (n0 & 63)); };
+  auto fbm = [&](uint4 raw, int n0, int i) {
     float x[8];
-    tc::unpack8(tc::ldg16(dyb + (size_t)i * HP + (h0 + hl) * P + p0), x);
-    const float s = hl ? v1.em[i] : v0.em[i];
+    tc::unpack8(raw, x);
+    const float s = (n0 >> 6) ? v1.em[i] : v0.em[i];
 #pragma unroll
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 0);
+  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fbl, fbm, k0 > 0);
   eng.finish();
   const int n = threadIdx.x;
   for (int cc = 0; cc < 4; ++cc) {
@@ -313,7 +319,8 @@ __global__ void __launch_bounds__(128) tc_w_kernel(Problem pr, const bf16 *__res
   auto fa = [&](int m, int k0) { return tc::ldg16(dyb + (size_t)(128 * I + m) * HP + k0); };
   for (int J = 0; J <= I; ++J) {
     auto fb = [&](int n, int k0) { return tc::ldg16(ub + (size_t)(128 * J + n) * Cd + h * P + k0); };
-    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, fb, k0 > 0);
+    for (int k0 = 0; k0 < P; k0 += 64)
+      eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 0);
   }
   eng.finish();
   const int m = threadIdx.x, i = 128 * I + m;
@@ -379,7 +386,7 @@ void launch_tc_w(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
 
 // ---------------------------------------------------------------- backward: dX
 // rows j of tile I:  du_x[j] = sum_{i>=j} M[i,j] dy_i + wdt_j dS_end B_j + D dy_j
-using EngDx = tc::Engine<64, 3>;
+using EngDx = tc::Engine<64, 2>;
 __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
                                                     const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                     const float *__restrict__ acs, const float *__restrict__ cb,
@@ -405,10 +412,11 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
   EngDx eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 64);
-  auto fa1 = [&](int m0, int i) {
+  auto fa1l = [&](int m0, int i) { return tc::ldf8(cbm + (size_t)i * Q + 128 * I + m0); };
+  auto fa1 = [&](const tc::F8 &raw, int m0, int i) {
     const int j0 = 128 * I + m0;
     float cv[8], r[8];
-    tc::ld8f(cbm + (size_t)i * Q + j0, cv);
+    tc::f8_to(raw, cv);
     const float ai = v.acs[i];
     const int si = v.seq[i];
 #pragma unroll
@@ -419,25 +427,29 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
     return tc::pack8(r);
   };
   auto fb1 = [&](int n0, int i) { return tc::ldg16(dyb + (size_t)i * HP + n0); };
-  for (int k0 = 128 * I; k0 < Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1, fb1, k0 > 128 * I);
-  auto fa2 = [&](int m, int k0) {
-    const int j = 128 * I + m;
+  for (int k0 = 128 * I; k0 < Q; k0 += 64)
+    eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::AsIs{}, k0 > 128 * I);
+  auto fa2l = [&](int m, int k0) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offB + k0); };
+  auto fa2 = [&](uint4 raw, int m, int) {
     float b[8];
-    tc::unpack8(tc::ldg16(ub + (size_t)j * Cd + offB + k0), b);
-    const float s = v.wdt[j];
+    tc::unpack8(raw, b);
+    const float s = v.wdt[128 * I + m];
 #pragma unroll
     for (int q = 0; q < 8; ++q) b[q] *= s;
     return tc::pack8(b);
   };
-  auto fb2 = [&](int p, int k0) {
+  auto fb2l = [&](int p, int k0) {
+    return tc::F16{tc::ldf8(dsc + (size_t)p * N + k0), tc::ldf8(gk + (size_t)p * N + k0)};
+  };
+  auto fb2 = [&](const tc::F16 &raw, int, int) {
     float a[8], b[8];
-    tc::ld8f(dsc + (size_t)p * N + k0, a);
-    tc::ld8f(gk + (size_t)p * N + k0, b);
+    tc::f8_to(raw.x, a);
+    tc::f8_to(raw.y, b);
 #pragma unroll
     for (int q = 0; q < 8; ++q) a[q] += de * b[q];
     return tc::pack8(a);
   };
-  for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem, k0, fa2, fb2, true);
+  for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem, k0, fa2l, fa2, fb2l, fb2, true);
   eng.finish();
   const int j = 128 * I + threadIdx.x;
   const float Dh = pr.D[h];
@@ -506,29 +518,33 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
   // ---- dC
   const bool has_off = c > 0;
   if (has_off) {
-    auto fa = [&](int mm, int p0) {
-      const int i = 128 * I + mm;
+    auto fal = [&](int mm, int p0) { return tc::ldg16(dyb + (size_t)(128 * I + mm) * HP + p0); };
+    auto fam = [&](uint4 raw, int mm, int) {
       float d8[8];
-      tc::unpack8(tc::ldg16(dyb + (size_t)i * HP + p0), d8);
-      const float s = v.em[i];
+      tc::unpack8(raw, d8);
+      const float s = v.em[128 * I + mm];
 #pragma unroll
       for (int q = 0; q < 8; ++q) d8[q] *= s;
       return tc::pack8(d8);
     };
-    auto fb = [&](int n0, int p) {
+    auto fbl = [&](int n0, int p) {
+      return tc::F16{tc::ldf8(sloc + (size_t)p * N + n0), tc::ldf8(sseg + (size_t)p * N + n0)};
+    };
+    auto fbm = [&](const tc::F16 &raw, int, int) {
       float a[8], b[8];
-      tc::ld8f(sloc + (size_t)p * N + n0, a);
-      tc::ld8f(sseg + (size_t)p * N + n0, b);
+      tc::f8_to(raw.x, a);
+      tc::f8_to(raw.y, b);
 #pragma unroll
       for (int q = 0; q < 8; ++q) a[q] += dc * b[q];
       return tc::pack8(a);
     };
-    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, fb, k0 > 0);
+    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fal, fam, fbl, fbm, k0 > 0);
   }
   {
     auto fa = [&](int mm, int j0) { return tc::ldg16(wm + (size_t)(128 * I + mm) * Q + j0); };
     auto fb = [&](int n0, int j) { return tc::ldg16(ub + (size_t)j * Cd + offB + n0); };
-    for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 0);
+    for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
+      eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 0);
   }
   eng.finish();
   {
@@ -556,20 +572,25 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
   // ---- dB
   {
     auto fa = [&](int mm, int p0) { return tc::ldg16(ub + (size_t)(128 * I + mm) * Cd + offX + p0); };
-    auto fb = [&](int n0, int p) {
+    auto fbl = [&](int n0, int p) {
+      return tc::F16{tc::ldf8(dsc + (size_t)p * N + n0), tc::ldf8(gk + (size_t)p * N + n0)};
+    };
+    auto fbm = [&](const tc::F16 &raw, int, int) {
       float a[8], b[8];
-      tc::ld8f(dsc + (size_t)p * N + n0, a);
-      tc::ld8f(gk + (size_t)p * N + n0, b);
+      tc::f8_to(raw.x, a);
+      tc::f8_to(raw.y, b);
 #pragma unroll
       for (int q = 0; q < 8; ++q) a[q] += de * b[q];
       return tc::pack8(a);
     };
-    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, fb, k0 > 0);
+    for (int k0 = 0; k0 < P; k0 += 64)
+      eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, tc::AsIs{}, fbl, fbm, k0 > 0);
   }
   {
     auto fa = [&](int m0, int i) { return tc::ldg16(wm + (size_t)i * Q + 128 * I + m0); };
     auto fb = [&](int n0, int i) { return tc::ldg16(ub + (size_t)i * Cd + offC + n0); };
-    for (int k0 = 128 * I; k0 < Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, fb, k0 > 128 * I);
+    for (int k0 = 128 * I; k0 < Q; k0 += 64)
+      eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 128 * I);
   }
   eng.finish();
   {

@@ -9,9 +9,10 @@
 // to the stage's mbarrier.  A ring of NSTAGE stages lets the staging of the
 // next 64-k slice overlap the tensor-core work of the previous ones.
 //
-// Operand functors return 8 bf16 values packed in a uint4:
-//   K-major operand:  f(m, k) -> elements (m, k .. k+7)
-//   MN-major operand: f(m, k) -> elements (m .. m+7, k)
+// Each operand is given as fetch(m, k) -> raw data and make(raw, m, k) -> 8 bf16
+// packed in a uint4:
+//   K-major operand:  elements (m, k .. k+7)
+//   MN-major operand: elements (m .. m+7, k)
 // (pick the one whose 8 elements are contiguous in the source).
 #pragma once
 
@@ -80,52 +81,78 @@ struct Engine {
     }
   }
 
-  template <int MA, class FA>
-  __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FA &fa) {
-    if constexpr (MA == K_MAJOR) {
-#pragma unroll 2
-      for (int e = threadIdx.x; e < 128 * 8; e += kThreads) {
-        const int m = e >> 3, c = e & 7;
-        *reinterpret_cast<uint4 *>(A + sw128_offset(m, c * 8)) = fa(m, k0 + c * 8);
+  // Operands come as two callables: fetch(m, k) issues the global loads and
+  // returns the raw data, make(raw, m, k) turns it into 8 packed bf16.  Every
+  // thread first issues the loads of kBatch chunks back to back, then
+  // transforms and stores them, so kBatch loads per thread are in flight.
+  static constexpr int kBatch = 4;
+
+  template <int MA, class FL, class FM>
+  __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FL &fl, const FM &fm) {
+    using Raw = decltype(fl(0, 0));
+    constexpr int PER = (128 * 8) / kThreads;  // 16-byte chunks per thread
+#pragma unroll
+    for (int g = 0; g < PER; g += kBatch) {
+      Raw raw[kBatch];
+      int mm[kBatch], kk[kBatch];
+      uint32_t off[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int e = threadIdx.x + (g + q) * kThreads;
+        if constexpr (MA == K_MAJOR) {
+          const int m = e >> 3, c = e & 7;
+          mm[q] = m; kk[q] = k0 + c * 8; off[q] = sw128_offset(m, c * 8);
+        } else {  // two 64-wide MN atoms, 64 k-rows each
+          const int r = e >> 4, c = e & 15;
+          mm[q] = c * 8; kk[q] = k0 + r; off[q] = (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8);
+        }
+        raw[q] = fl(mm[q], kk[q]);
       }
-    } else {  // two 64-wide MN atoms, 64 k-rows each
-#pragma unroll 2
-      for (int e = threadIdx.x; e < 64 * 16; e += kThreads) {
-        const int r = e >> 4, c = e & 15;
-        *reinterpret_cast<uint4 *>(A + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8)) = fa(c * 8, k0 + r);
-      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) *reinterpret_cast<uint4 *>(A + off[q]) = fm(raw[q], mm[q], kk[q]);
     }
   }
 
-  template <int MB, class FB>
-  __device__ __forceinline__ void stage_B(uint8_t *B, int k0, const FB &fb) {
-    if constexpr (MB == K_MAJOR) {
-#pragma unroll 2
-      for (int e = threadIdx.x; e < NT * 8; e += kThreads) {
-        const int n = e >> 3, c = e & 7;
-        *reinterpret_cast<uint4 *>(B + sw128_offset(n, c * 8)) = fb(n, k0 + c * 8);
+  template <int MB, class FL, class FM>
+  __device__ __forceinline__ void stage_B(uint8_t *B, int k0, const FL &fl, const FM &fm) {
+    using Raw = decltype(fl(0, 0));
+    static_assert(MB == K_MAJOR || NT % 64 == 0, "MN-major B needs whole 64-wide atoms");
+    constexpr int CPR = NT / 8;  // 16-byte chunks per k-row (MN-major)
+    constexpr int PER = (NT * 8) / kThreads;
+    static_assert(PER % kBatch == 0, "B chunks per thread");
+#pragma unroll
+    for (int g = 0; g < PER; g += kBatch) {
+      Raw raw[kBatch];
+      int nn[kBatch], kk[kBatch];
+      uint32_t off[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int e = threadIdx.x + (g + q) * kThreads;
+        if constexpr (MB == K_MAJOR) {
+          const int n = e >> 3, c = e & 7;
+          nn[q] = n; kk[q] = k0 + c * 8; off[q] = sw128_offset(n, c * 8);
+        } else {
+          const int r = e / CPR, c = e % CPR;
+          nn[q] = c * 8; kk[q] = k0 + r; off[q] = (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8);
+        }
+        raw[q] = fl(nn[q], kk[q]);
       }
-    } else {
-      static_assert(MB == K_MAJOR || NT % 64 == 0, "MN-major B needs whole 64-wide atoms");
-      constexpr int CPR = NT / 8;  // 16-byte chunks per k-row
-#pragma unroll 2
-      for (int e = threadIdx.x; e < 64 * CPR; e += kThreads) {
-        const int r = e / CPR, c = e % CPR;
-        *reinterpret_cast<uint4 *>(B + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8)) = fb(c * 8, k0 + r);
-      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) *reinterpret_cast<uint4 *>(B + off[q]) = fm(raw[q], nn[q], kk[q]);
     }
   }
 
   // Stage the 64-wide k slice [k0, k0+64) of A and B and issue its MMAs into the
   // accumulator at TMEM address tmem_d.  Must be called by all 128 threads.
-  template <int MA, int MB, class FA, class FB>
-  __device__ __forceinline__ void slice(uint32_t tmem_d, int k0, const FA &fa, const FB &fb, bool accumulate) {
+  template <int MA, int MB, class FAL, class FAM, class FBL, class FBM>
+  __device__ __forceinline__ void slice(uint32_t tmem_d, int k0, const FAL &fal, const FAM &fam, const FBL &fbl,
+                                        const FBM &fbm, bool accumulate) {
     const int s = stage;
     if (uses[s] > 0) mbar_wait(&bars[s], (uses[s] - 1) & 1, status);
     uint8_t *A = ring + s * STAGE_BYTES;
     uint8_t *B = A + A_BYTES;
-    stage_A<MA>(A, k0, fa);
-    stage_B<MB>(B, k0, fb);
+    stage_A<MA>(A, k0, fal, fam);
+    stage_B<MB>(B, k0, fbl, fbm);
     fence_async_smem();
     tc_fence_before();  // order this thread's earlier TMEM reads before the MMAs below
     __syncthreads();
@@ -152,6 +179,25 @@ struct Engine {
     done_uses += 1;
     tc_fence_after();
   }
+};
+
+// make() for operands that are already 8 packed bf16
+struct AsIs {
+  __device__ __forceinline__ uint4 operator()(uint4 r, int, int) const { return r; }
+};
+// 8 fp32 values fetched as two float4
+struct F8 {
+  float4 a, b;
+};
+__device__ __forceinline__ F8 ldf8(const float *p) {
+  return F8{__ldg(reinterpret_cast<const float4 *>(p)), __ldg(reinterpret_cast<const float4 *>(p) + 1)};
+}
+__device__ __forceinline__ void f8_to(const F8 &r, float (&v)[8]) {
+  v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w; v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+}
+// two fp32 rows fetched together (state + segment state, combined in make())
+struct F16 {
+  F8 x, y;
 };
 
 // Shared-memory carve-up helper for kernels built on the engine: returns the
