@@ -59,16 +59,17 @@ def test_forward_backward_parity(oracle_lib, shape, seq, dtype):
     compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
 
 
+@pytest.mark.parametrize("dtype,seq", [("f32", None), ("bf16", None), ("bf16", [1000, 3, 2093, 1000])])
 @pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
-def test_segment_count_sweep(oracle_lib, S):
+def test_segment_count_sweep(oracle_lib, S, dtype, seq):
     shape = SsdShape(1, 4096, 4, 64, 128, 1, 256, S)
-    inp = make_inputs(shape, 8, "f32")
+    inp = make_inputs(shape, 8, dtype, seq_lengths=seq)
     ref = oracle_lib.forward(inp, shape, n_segments=1)
-    got, _ = gpu_forward(shape, "f32", inp)
-    assert rel(got["y"], ref["y"]) <= TOL["f32"]
-    assert rel(got["final_state"], ref["final_state"]) <= TOL["f32"]
-    g = gpu_backward(shape, "f32", inp, use_dfinal=False)
-    compare_backward(g, oracle_lib.backward(inp, shape, use_dfinal=False), shape, TOL["f32"])
+    got, _ = gpu_forward(shape, dtype, inp)
+    assert rel(got["y"], ref["y"]) <= TOL[dtype]
+    assert rel(got["final_state"], ref["final_state"]) <= TOL[dtype]
+    g = gpu_backward(shape, dtype, inp, use_dfinal=False)
+    compare_backward(g, oracle_lib.backward(inp, shape, use_dfinal=False), shape, TOL[dtype])
 
 
 def test_backward_recomputes_segment_states(oracle_lib):
