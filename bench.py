@@ -129,62 +129,107 @@ class ClockSampler:
 # ---------------------------------------------------------------- algorithmic work per kernel launch
 
 def kernel_work(shape, dtype: str) -> dict:
-    """name -> (bound, amount per launch, unit): algorithmic flops (causal
-    products only) for contractions, algorithmic HBM bytes for streaming kernels."""
+    """name -> (engine, algorithmic flops, algorithmic bytes) per launch.
+
+    flops count the causal products a contraction has to do (the masked upper
+    triangle of the intra-chunk products is not counted); bytes count every
+    tensor the kernel must read or write once, for the kernel decomposition this
+    library uses (its intermediates -- CB, chunk states, W, per-head dB/dC
+    partials -- are part of that decomposition)."""
     b, L, H, P, N, G, Q, S = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
                               shape.chunk, shape.n_segments)
     eb = 2 if dtype == "bf16" else 4
-    nc, Cd = L // Q, shape.conv_dim
+    nc, Cd, HP, GN = L // Q, shape.conv_dim, H * P, G * N
     tri = Q * (Q + 1) // 2
     PN = P * N
-    return {
-        "conv_fwd": ("hbm", b * L * Cd * 2 * eb, "B"),
-        "dt_prep": ("hbm", b * L * H * (eb + 8), "B"),
-        "cb": ("alu", b * nc * G * tri * 2 * N, "flop"),
-        "chunk_state": ("alu", b * nc * H * 2 * P * N * Q, "flop"),
-        "local_pass": ("hbm", b * nc * H * PN * 8 + b * S * H * PN * 4, "B"),
-        "seg_scan": ("hbm", b * S * H * PN * 8 + b * H * PN * 4, "B"),
-        "chunk_out": ("alu", b * nc * H * (tri * 2 * P + 2 * Q * N * P), "flop"),
-        "chunk_z": ("alu", b * nc * H * 2 * P * N * Q, "flop"),
-        "local_rev": ("hbm", b * nc * H * PN * 8 + b * S * H * PN * 4, "B"),
-        "seg_rscan": ("hbm", b * S * H * PN * 8, "B"),
-        "chunk_w": ("alu", b * nc * H * tri * 2 * P, "flop"),
-        "chunk_dx": ("alu", b * nc * H * (tri * 2 * P + 2 * Q * N * P), "flop"),
-        "chunk_dcdb": ("alu", b * nc * H * (2 * tri * 2 * N + 2 * 2 * Q * P * N), "flop"),
-        "chunk_dt": ("hbm", b * L * H * (6 * 4 + eb + 2 * P * eb), "B"),
-        "bc_reduce": ("hbm", b * L * H * N * 8 + b * L * 2 * G * N * 4, "B"),
-        "conv_bwd": ("hbm", b * L * Cd * (eb + 4 + eb), "B"),
-        "param_reduce": ("hbm", b * nc * H * 12, "B"),
+    nti = max(Q // 128, 1)
+    tiles = nti * (nti + 1) // 2  # causal 128 x 128 blocks per chunk
+    x = b * L * HP * eb
+    bc = b * L * GN * eb
+    cb = b * nc * G * tiles * 128 * 128 * 4
+    st = b * nc * H * PN * 4  # one (b, chunk, head) state array
+    seg = b * S * H * PN * 4
+    wbytes = b * nc * H * tiles * 128 * 128 * 2
+    tok = b * H * L * 4
+    parts = b * L * H * N * 4
+    f_state = b * nc * H * 2 * P * N * Q
+    f_out = b * nc * H * (tri * 2 * P + 2 * Q * N * P)
+    f_w = b * nc * H * tri * 2 * P
+    f_dcdb = b * nc * H * (2 * tri * 2 * N + 2 * 2 * Q * P * N)
+    f_cb = b * nc * G * tri * 2 * N
+    w = {
+        "conv_fwd": ("mem", 0, b * L * Cd * 2 * eb),
+        "dt_prep": ("mem", 0, b * L * H * (eb + 8)),
+        "local_pass": ("mem", 0, 2 * st + seg),
+        "seg_scan": ("mem", 0, 2 * seg + b * H * PN * 4),
+        "local_rev": ("mem", 0, 2 * st + seg),
+        "seg_rscan": ("mem", 0, 2 * seg),
+        "chunk_dt": ("mem", 0, 5 * tok + 4 * st + 2 * x + b * L * H * eb),
+        "bc_reduce": ("mem", 0, 2 * parts + 2 * b * L * GN * 4),
+        "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 128) * Cd * 20),
+        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 128) * Cd * 20),
+        "tc_cb": ("tensor", f_cb, 2 * bc + cb),
+        "tc_chunk_state": ("tensor", f_state, x + bc + st),
+        "tc_chunk_out": ("tensor", f_out, 2 * x + bc + cb + st + seg),
+        "tc_chunk_z": ("tensor", f_state, x + bc + st),
+        "tc_chunk_w": ("tensor", f_w, 2 * x + cb + wbytes + 3 * tok),
+        "tc_chunk_dx": ("tensor", f_out, cb + x + bc + st + seg + b * L * HP * 4),
+        "tc_chunk_dcdb": ("tensor", f_dcdb, wbytes + 2 * x + 2 * bc + 2 * st + 2 * seg + 2 * parts + 2 * tok),
     }
+    for name, tcname in (("cb", "tc_cb"), ("chunk_state", "tc_chunk_state"), ("chunk_out", "tc_chunk_out"),
+                         ("chunk_z", "tc_chunk_z"), ("chunk_w", "tc_chunk_w"), ("chunk_dx", "tc_chunk_dx"),
+                         ("chunk_dcdb", "tc_chunk_dcdb")):
+        _, f, by = w[tcname]
+        w[name] = ("alu", f, by)
+    return w
 
 
 def roofline_for(kt: list, shape, dtype: str, peaks: dict, peak_src: str, clocks: dict | None) -> dict:
+    """Roofline of the kernel with the largest share of the step.  Kernels are
+    timed inside the step, so the tensor peak is the sustained one."""
     work = kernel_work(shape, dtype)
     name, launches, total_ms = max(kt, key=lambda r: r[2])
-    bound, amount, unit = work.get(name, ("hbm", 0, "B"))
+    engine, flops, nbytes = work.get(name, ("mem", 0, 0))
     avg_s = total_ms / 1e3 / max(launches, 1)
-    traffic = committed_traffic(name)
-    if bound == "hbm":
-        achieved = amount / avg_s / 1e9
-        peak, punit = peaks["hbm_gbs"], "GB/s"
-        note = f"HBM copy bandwidth ({peak_src})"
-    elif bound == "tensor":
-        achieved = amount / avg_s / 1e12
-        peak, punit = peaks["bf16_tflops"], "TFLOP/s"
-        note = f"dense bf16 burst ({peak_src})"
+    hbm = peaks["hbm_gbs"]
+    if engine == "tensor":
+        cpeak, cnote = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), f"dense bf16 sustained ({peak_src})"
     else:  # fp32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
         mhz = peaks.get("sm_max_mhz", 2070.0)
-        achieved = amount / avg_s / 1e12
-        peak, punit = SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, "TFLOP/s"
-        note = f"fp32 FMA pipe at {mhz:.0f} MHz (derived)"
-    return {"bound": bound, "kernel": name, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": punit,
-            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": note,
-            "algorithmic_per_launch": amount, "avg_launch_ms": round(avg_s * 1e3, 4)}
+        cpeak, cnote = SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, f"fp32 FMA pipe at {mhz:.0f} MHz (derived)"
+    t_flop = flops / (cpeak * 1e12) if flops else 0.0
+    t_byte = nbytes / (hbm * 1e9)
+    frac_c = flops / avg_s / 1e12 / cpeak if flops else None
+    frac_m = nbytes / avg_s / 1e9 / hbm
+    if engine == "mem" or t_byte >= t_flop:
+        bound, achieved, peak, unit, note = "hbm", nbytes / avg_s / 1e9, hbm, "GB/s", f"HBM copy bandwidth ({peak_src})"
+        amount = nbytes
+    else:
+        bound = "tensor" if engine == "tensor" else "alu"
+        achieved, peak, unit, note, amount = flops / avg_s / 1e12, cpeak, "TFLOP/s", cnote, flops
+    return {"bound": bound, "kernel": name, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": committed_traffic(name, shape),
+            "peak_source": note, "algorithmic_per_launch": amount, "avg_launch_ms": round(avg_s * 1e3, 4),
+            "frac_hbm": round(frac_m, 4), "frac_compute": None if frac_c is None else round(frac_c, 4)}
 
 
-def committed_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel's file; otherwise None."""
+def step_totals(kt: list, shape, dtype: str, ms_per_step: float, peaks: dict) -> dict:
+    """Whole-step algorithmic work against the peaks (all kernels, per step)."""
+    work = kernel_work(shape, dtype)
+    steps = max(r[1] for r in kt if r[0] in ("local_rev", "chunk_dt", "conv_bwd")) if kt else 1
+    flops = sum(work.get(n, ("mem", 0, 0))[1] * c for n, c, _ in kt) / steps
+    nbytes = sum(work.get(n, ("mem", 0, 0))[2] * c for n, c, _ in kt) / steps
+    s = ms_per_step / 1e3
+    return {"tensor_tflops": round(flops / s / 1e12, 2),
+            "frac_tensor_sustained": round(flops / s / 1e12 / peaks.get("bf16_tflops_sustained", 1742.8), 4),
+            "hbm_gbs": round(nbytes / s / 1e9, 1), "frac_hbm": round(nbytes / s / 1e9 / peaks["hbm_gbs"], 4),
+            "flop_per_step": flops, "bytes_per_step": nbytes}
+
+
+def committed_traffic(kernel: str, shape):
+    """DRAM bytes per launch from the committed ncu summary, scaled from the
+    captured batch to this workload's batch, if it was taken on the current
+    source of the kernel's file; otherwise None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -199,7 +244,7 @@ def committed_traffic(kernel: str):
     with open(src, "rb") as fh:
         if hashlib.sha256(fh.read()).hexdigest() != e["source_sha256"]:
             return None
-    return e["dram_bytes_per_launch"]
+    return int(e["dram_bytes_per_launch"] * shape.batch / e.get("captured_batch", shape.batch))
 
 
 # ---------------------------------------------------------------- CPU oracle timings
@@ -357,6 +402,7 @@ def run_ours(args, shape, dtype, seed):
         "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "config": config_dict(shape, dtype, seed),
         "roofline": roofline_for(kt, shape, dtype, peaks, peak_src, clocks),
+        "step_roofline": step_totals(kt, shape, dtype, el / args.steps * 1e3, peaks),
         "e2e": e2e,
         "gpu_launches": int(sum(r[1] for r in kt)),
         "clocks": clocks,
