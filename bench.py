@@ -166,8 +166,8 @@ def kernel_work(shape, dtype: str) -> dict:
         "seg_rscan": ("mem", 0, 2 * seg),
         "chunk_dt": ("mem", 0, 5 * tok + 4 * st + 2 * x + b * L * H * eb),
         "bc_reduce": ("mem", 0, 2 * parts + 2 * b * L * GN * 4),
-        "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 128) * Cd * 20),
-        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 128) * Cd * 20),
+        "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 32) * Cd * 20),
+        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 32) * Cd * 20),
         "tc_cb": ("tensor", f_cb, 2 * bc + cb),
         "tc_chunk_state": ("tensor", f_state, x + bc + st),
         "tc_chunk_out": ("tensor", f_out, 2 * x + bc + cb + st + seg),

@@ -51,7 +51,7 @@ __device__ __forceinline__ float chunk_decay(const Problem &pr, const float *acs
 
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kConvBwdTok = 128;  // tokens per conv-backward block (one set of parameter partials each)
+constexpr int kConvBwdTok = 32;  // tokens per conv-backward block (one set of parameter partials each)
 
 // ---------------------------------------------------------------- workspace
 // Offsets (bytes) of every scratch buffer; computed identically on host and

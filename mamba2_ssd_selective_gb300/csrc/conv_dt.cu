@@ -44,7 +44,7 @@ __device__ __forceinline__ void grad_channel(const Problem &pr, const GradOut &g
   base = p;
 }
 
-constexpr int kConvTok = 64;
+constexpr int kConvTok = 32;
 
 // 8 consecutive channels of one token as fp32 (16-byte loads for bf16)
 template <typename T> __device__ __forceinline__ void load8(const T *p, float (&v)[8]);
@@ -74,6 +74,26 @@ template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 
 template <> __device__ __forceinline__ void store8<float>(float *p, const float (&v)[8]) {
   reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
   reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// 4 consecutive channels (8-byte loads for bf16)
+template <typename T> __device__ __forceinline__ void load4(const T *p, float (&v)[4]);
+template <> __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+template <> __device__ __forceinline__ void load4<float>(const float *p, float (&v)[4]) {
+  const float4 a = *reinterpret_cast<const float4 *>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+template <typename T> __device__ __forceinline__ void store4(T *p, const float (&v)[4]);
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, const float (&v)[4]) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+}
+template <> __device__ __forceinline__ void store4<float>(float *p, const float (&v)[4]) {
+  *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // u[b, t, c] = silu(conv_b[c] + sum_k w[c,k] * xr[t-3+k, c]), taps masked at row
@@ -155,14 +175,14 @@ template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *
   dt_prep_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 32, 0, s>>>(pr, dtv, acs);
 }
 
-// Conv + SiLU backward for 8 channels over a block of kConvBwdTok tokens:
+// Conv + SiLU backward for 4 channels over a block of kConvBwdTok tokens:
 //   dv = du * silu'(v);  dxr[s] = sum_k w[k] dv[s+3-k] (same sequence);
 //   per-block partials of dconv_w[c,k] = sum dv[t] xr[t-3+k] and dconv_b[c] = sum dv.
 // v is recomputed from the raw inputs.
 template <typename T>
 __global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
                                                        float *__restrict__ convp, int ntb) {
-  const int c = (blockIdx.x * 128 + threadIdx.x) * 8;
+  const int c = (blockIdx.x * 128 + threadIdx.x) * 4;
   if (c >= pr.Cd) return;
   const int blk = blockIdx.y, bb = blockIdx.z;
   const int t0 = blk * kConvBwdTok, tend = min(pr.L, t0 + kConvBwdTok);
@@ -172,36 +192,36 @@ __global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *
   long long dstride;
   grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
   T *dst = static_cast<T *>(dbase);
-  float w[8][4], bias[8];
+  float w[4][4], bias[4];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
     w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
     bias[q] = pr.conv_b[c + q];
   }
-  float r0[8], r1[8], r2[8], d0[8], d1[8], d2[8], dw[8][4], db[8];
+  float r0[4], r1[4], r2[4], d0[4], d1[4], d2[4], dw[4][4], db[4];
   int s0 = 0, s1 = 0, s2 = 0, q0 = 0, q1 = 0, q2 = 0;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     r0[q] = r1[q] = r2[q] = d0[q] = d1[q] = d2[q] = db[q] = 0.f;
     dw[q][0] = dw[q][1] = dw[q][2] = dw[q][3] = 0.f;
   }
-  if (t0 - 3 >= 0) { load8(src + (size_t)(t0 - 3) * st, r0); s0 = seq_of(pr, bb, t0 - 3); }
-  if (t0 - 2 >= 0) { load8(src + (size_t)(t0 - 2) * st, r1); s1 = seq_of(pr, bb, t0 - 2); }
-  if (t0 - 1 >= 0) { load8(src + (size_t)(t0 - 1) * st, r2); s2 = seq_of(pr, bb, t0 - 1); }
+  if (t0 - 3 >= 0) { load4(src + (size_t)(t0 - 3) * st, r0); s0 = seq_of(pr, bb, t0 - 3); }
+  if (t0 - 2 >= 0) { load4(src + (size_t)(t0 - 2) * st, r1); s1 = seq_of(pr, bb, t0 - 2); }
+  if (t0 - 1 >= 0) { load4(src + (size_t)(t0 - 1) * st, r2); s2 = seq_of(pr, bb, t0 - 1); }
   const float *dub = du + (size_t)bb * pr.L * pr.Cd + c;
   for (int t = t0; t < t0 + kConvBwdTok + 3; ++t) {
-    float dvt[8];
+    float dvt[4];
     int sq = 0;
     if (t < pr.L) {
-      float rt[8], g8[8];
-      load8(src + (size_t)t * st, rt);
-      load8(dub + (size_t)t * pr.Cd, g8);
+      float rt[4], g8[4];
+      load4(src + (size_t)t * st, rt);
+      load4(dub + (size_t)t * pr.Cd, g8);
       sq = seq_of(pr, bb, t);
       const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;
       const bool own = t < tend;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         float v = bias[q] + w[q][3] * rt[q];
         v += m2 ? w[q][2] * r2[q] : 0.f;
         v += m1 ? w[q][1] * r1[q] : 0.f;
@@ -220,29 +240,29 @@ __global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *
       s0 = s1; s1 = s2; s2 = sq;
     } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) dvt[q] = 0.f;
+      for (int q = 0; q < 4; ++q) dvt[q] = 0.f;
     }
     // output token s = t - 3 reads dv[s..s+3] = (d0, d1, d2, dvt)
     const int s = t - 3;
     if (s >= t0 && s < tend) {
       const bool m1 = q1 == q0, m2 = q2 == q0, m3 = sq == q0;
-      float g[8];
+      float g[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         float a = w[q][3] * d0[q];
         a += m1 ? w[q][2] * d1[q] : 0.f;
         a += m2 ? w[q][1] * d2[q] : 0.f;
         a += m3 ? w[q][0] * dvt[q] : 0.f;
         g[q] = a;
       }
-      store8(dst + (size_t)s * dstride, g);
+      store4(dst + (size_t)s * dstride, g);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) { d0[q] = d1[q]; d1[q] = d2[q]; d2[q] = dvt[q]; }
+    for (int q = 0; q < 4; ++q) { d0[q] = d1[q]; d1[q] = d2[q]; d2[q] = dvt[q]; }
     q0 = q1; q1 = q2; q2 = sq;
   }
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     float *pp = convp + (((size_t)bb * ntb + blk) * pr.Cd + c + q) * 5;
     pp[0] = dw[q][0]; pp[1] = dw[q][1]; pp[2] = dw[q][2]; pp[3] = dw[q][3]; pp[4] = db[q];
   }
@@ -250,46 +270,66 @@ __global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *
 
 template <typename T>
 void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s) {
-  dim3 grid((pr.Cd / 8 + 127) / 128, ntb, pr.b);
+  dim3 grid((pr.Cd / 4 + 127) / 128, ntb, pr.b);
   conv_bwd_kernel<T><<<grid, 128, 0, s>>>(pr, du, go, convp, ntb);
 }
 
 // Parameter gradients: fixed-order sums of per-chunk / per-block partials.
-__global__ void param_reduce_kernel(Problem pr, const float *__restrict__ chs, const float *__restrict__ convp,
-                                    int ntb, float *ddt_bias, float *dA_log, float *dD, float *dconv_w,
-                                    float *dconv_b) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t nch = (size_t)pr.b * pr.nc * pr.H;
-  if (i < pr.H) {
-    float sb = 0.f, sa = 0.f, sd = 0.f;
-    for (int bb = 0; bb < pr.b; ++bb)
-      for (int c = 0; c < pr.nc; ++c) {
-        const size_t o = ((size_t)bb * pr.nc + c) * pr.H + i;
-        sb += chs[o];
-        sa += chs[nch + o];
-        sd += chs[2 * nch + o];
-      }
-    ddt_bias[i] = sb;
-    dA_log[i] = sa * (-expf(pr.A_log[i]));  // dA/dA_log = A
-    dD[i] = sd;
-  }
-  if (i < pr.Cd) {
-    float acc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int bb = 0; bb < pr.b; ++bb)
-      for (int k = 0; k < ntb; ++k) {
-        const float *pp = convp + (((size_t)bb * ntb + k) * pr.Cd + i) * 5;
+// One warp per channel (and per head for the dt / A / D grads): lane l sums the
+// partials l, l+32, ... in order, then a fixed xor-shuffle tree combines lanes.
+__device__ __forceinline__ float warp_tree_sum(float v) {
 #pragma unroll
-        for (int q = 0; q < 5; ++q) acc[q] += pp[q];
-      }
-    for (int q = 0; q < 4; ++q) dconv_w[i * 4 + q] = acc[q];
-    dconv_b[i] = acc[4];
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(256) param_reduce_kernel(Problem pr, const float *__restrict__ chs,
+                                                           const float *__restrict__ convp, int ntb,
+                                                           float *ddt_bias, float *dA_log, float *dD,
+                                                           float *dconv_w, float *dconv_b) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const size_t nch = (size_t)pr.b * pr.nc * pr.H;
+  if (warp < pr.Cd) {
+    const int c = warp;
+    const int nparts = pr.b * ntb;
+    float acc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = lane; k < nparts; k += 32) {
+      const float *pp = convp + ((size_t)k * pr.Cd + c) * 5;  // partial k = bb * ntb + blk
+#pragma unroll
+      for (int q = 0; q < 5; ++q) acc[q] += pp[q];
+    }
+#pragma unroll
+    for (int q = 0; q < 5; ++q) acc[q] = warp_tree_sum(acc[q]);
+    if (lane == 0) {
+      for (int q = 0; q < 4; ++q) dconv_w[c * 4 + q] = acc[q];
+      dconv_b[c] = acc[4];
+    }
+  } else if (warp < pr.Cd + pr.H) {
+    const int h = warp - pr.Cd;
+    const int nparts = pr.b * pr.nc;
+    float sb = 0.f, sa = 0.f, sd = 0.f;
+    for (int k = lane; k < nparts; k += 32) {  // k = bb * nc + c
+      const size_t o = (size_t)k * pr.H + h;
+      sb += chs[o];
+      sa += chs[nch + o];
+      sd += chs[2 * nch + o];
+    }
+    sb = warp_tree_sum(sb);
+    sa = warp_tree_sum(sa);
+    sd = warp_tree_sum(sd);
+    if (lane == 0) {
+      ddt_bias[h] = sb;
+      dA_log[h] = sa * (-expf(pr.A_log[h]));  // dA/dA_log = A
+      dD[h] = sd;
+    }
   }
 }
 
 void launch_param_reduce(const Problem &pr, const float *chs, const float *convp, int ntb, float *ddt_bias,
                          float *dA_log, float *dD, float *dconv_w, float *dconv_b, cudaStream_t s) {
-  const int n = pr.Cd > pr.H ? pr.Cd : pr.H;
-  param_reduce_kernel<<<(n + 127) / 128, 128, 0, s>>>(pr, chs, convp, ntb, ddt_bias, dA_log, dD, dconv_w, dconv_b);
+  const int warps = pr.Cd + pr.H;
+  param_reduce_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(pr, chs, convp, ntb, ddt_bias, dA_log, dD, dconv_w,
+                                                               dconv_b);
 }
 
 __global__ void cu_seqlens_kernel(const int *__restrict__ cu, int nseq, int *__restrict__ seq_idx, int total) {

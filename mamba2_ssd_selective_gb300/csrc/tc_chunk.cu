@@ -67,10 +67,10 @@ __global__ void __launch_bounds__(128) tc_cb_kernel(Problem pr, const bf16 *__re
   EngCB eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
-  auto fa = [&](int m, int k) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offC + k); };
+  auto fa = [&](int m, int k) { return static_cast<const void *>(ub + (size_t)(128 * I + m) * Cd + offC + k); };
   for (int J = 0; J <= I; ++J) {
-    auto fb = [&](int n, int k) { return tc::ldg16(ub + (size_t)(128 * J + n) * Cd + offB + k); };
-    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 0);
+    auto fb = [&](int n, int k) { return static_cast<const void *>(ub + (size_t)(128 * J + n) * Cd + offB + k); };
+    for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 0);
   }
   eng.finish();
   const int i = 128 * I + threadIdx.x;
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *_
   EngPair eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
-  auto fa = [&](int m0, int k) { return tc::ldg16(ub + (size_t)k * Cd + offB + m0); };
+  auto fa = [&](int m0, int k) { return static_cast<const void *>(ub + (size_t)k * Cd + offB + m0); };
   auto fbl = [&](int n0, int k) { return tc::ldg16(ub + (size_t)k * Cd + (h0 + (n0 >> 6)) * P + (n0 & 63)); };
   auto fbm = [&](uint4 raw, int n0, int k) {
     float x[8];
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *_
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fbl, fbm, k0 > 0);
+  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
   eng.finish();
   const int n = threadIdx.x;
   for (int cc = 0; cc < 4; ++cc) {
@@ -184,12 +184,12 @@ __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__r
     }
     return tc::pack8(r);
   };
-  auto fb1 = [&](int n0, int j) { return tc::ldg16(ub + (size_t)j * Cd + offX + n0); };
+  auto fb1 = [&](int n0, int j) { return static_cast<const void *>(ub + (size_t)j * Cd + offX + n0); };
   for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
-    eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::AsIs{}, k0 > 0);
+    eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::Async{}, k0 > 0);
   const bool has_off = c > 0;
   if (has_off) {
-    auto fa2 = [&](int m, int k0) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offC + k0); };
+    auto fa2 = [&](int m, int k0) { return static_cast<const void *>(ub + (size_t)(128 * I + m) * Cd + offC + k0); };
     auto fb2l = [&](int p, int k0) {
       return tc::F16{tc::ldf8(sloc + (size_t)p * N + k0), tc::ldf8(sseg + (size_t)p * N + k0)};
     };
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__r
       return tc::pack8(a);
     };
     for (int k0 = 0; k0 < N; k0 += 64)
-      eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::AsIs{}, fb2l, fb2, k0 > 0);
+      eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::Async{}, fb2l, fb2, k0 > 0);
   }
   eng.finish();
   const int i = 128 * I + threadIdx.x;
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__res
   EngPair eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
-  auto fa = [&](int m0, int i) { return tc::ldg16(ub + (size_t)i * Cd + offC + m0); };
+  auto fa = [&](int m0, int i) { return static_cast<const void *>(ub + (size_t)i * Cd + offC + m0); };
   auto fbl = [&](int n0, int i) { return tc::ldg16(dyb + (size_t)i * HP + (h0 + (n0 >> 6)) * P + (n0 & 63)); };
   auto fbm = [&](uint4 raw, int n0, int i) {
     float x[8];
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__res
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fbl, fbm, k0 > 0);
+  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
   eng.finish();
   const int n = threadIdx.x;
   for (int cc = 0; cc < 4; ++cc) {
@@ -316,11 +316,11 @@ __global__ void __launch_bounds__(128) tc_w_kernel(Problem pr, const bf16 *__res
   EngW eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
-  auto fa = [&](int m, int k0) { return tc::ldg16(dyb + (size_t)(128 * I + m) * HP + k0); };
+  auto fa = [&](int m, int k0) { return static_cast<const void *>(dyb + (size_t)(128 * I + m) * HP + k0); };
   for (int J = 0; J <= I; ++J) {
-    auto fb = [&](int n, int k0) { return tc::ldg16(ub + (size_t)(128 * J + n) * Cd + h * P + k0); };
+    auto fb = [&](int n, int k0) { return static_cast<const void *>(ub + (size_t)(128 * J + n) * Cd + h * P + k0); };
     for (int k0 = 0; k0 < P; k0 += 64)
-      eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 0);
+      eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 0);
   }
   eng.finish();
   const int m = threadIdx.x, i = 128 * I + m;
@@ -426,9 +426,9 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
     }
     return tc::pack8(r);
   };
-  auto fb1 = [&](int n0, int i) { return tc::ldg16(dyb + (size_t)i * HP + n0); };
+  auto fb1 = [&](int n0, int i) { return static_cast<const void *>(dyb + (size_t)i * HP + n0); };
   for (int k0 = 128 * I; k0 < Q; k0 += 64)
-    eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::AsIs{}, k0 > 128 * I);
+    eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::Async{}, k0 > 128 * I);
   auto fa2l = [&](int m, int k0) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offB + k0); };
   auto fa2 = [&](uint4 raw, int m, int) {
     float b[8];
@@ -541,10 +541,10 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
     for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fal, fam, fbl, fbm, k0 > 0);
   }
   {
-    auto fa = [&](int mm, int j0) { return tc::ldg16(wm + (size_t)(128 * I + mm) * Q + j0); };
-    auto fb = [&](int n0, int j) { return tc::ldg16(ub + (size_t)j * Cd + offB + n0); };
+    auto fa = [&](int mm, int j0) { return static_cast<const void *>(wm + (size_t)(128 * I + mm) * Q + j0); };
+    auto fb = [&](int n0, int j) { return static_cast<const void *>(ub + (size_t)j * Cd + offB + n0); };
     for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
-      eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 0);
+      eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 0);
   }
   eng.finish();
   {
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
   }
   // ---- dB
   {
-    auto fa = [&](int mm, int p0) { return tc::ldg16(ub + (size_t)(128 * I + mm) * Cd + offX + p0); };
+    auto fa = [&](int mm, int p0) { return static_cast<const void *>(ub + (size_t)(128 * I + mm) * Cd + offX + p0); };
     auto fbl = [&](int n0, int p) {
       return tc::F16{tc::ldf8(dsc + (size_t)p * N + n0), tc::ldf8(gk + (size_t)p * N + n0)};
     };
@@ -584,13 +584,13 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
       return tc::pack8(a);
     };
     for (int k0 = 0; k0 < P; k0 += 64)
-      eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, tc::AsIs{}, fbl, fbm, k0 > 0);
+      eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
   }
   {
-    auto fa = [&](int m0, int i) { return tc::ldg16(wm + (size_t)i * Q + 128 * I + m0); };
-    auto fb = [&](int n0, int i) { return tc::ldg16(ub + (size_t)i * Cd + offC + n0); };
+    auto fa = [&](int m0, int i) { return static_cast<const void *>(wm + (size_t)i * Q + 128 * I + m0); };
+    auto fb = [&](int n0, int i) { return static_cast<const void *>(ub + (size_t)i * Cd + offC + n0); };
     for (int k0 = 128 * I; k0 < Q; k0 += 64)
-      eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::AsIs{}, fb, tc::AsIs{}, k0 > 128 * I);
+      eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 128 * I);
   }
   eng.finish();
   {

@@ -18,6 +18,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "sm100.cuh"
 
 namespace ssd {
@@ -49,6 +51,13 @@ __device__ __forceinline__ void ld8f(const float *p, float (&v)[8]) {
   const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
+
+// make() marker for operands copied as they are: fetch(m, k) then returns the
+// global address of the 16 bytes, and the engine copies them with cp.async
+// straight into their swizzled slot (no registers, every copy in flight at once).
+struct Async {};
+template <class FM>
+constexpr bool kIsAsync = std::is_same<FM, Async>::value;
 
 template <int NT, int NSTAGE>
 struct Engine {
@@ -91,6 +100,21 @@ struct Engine {
   __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FL &fl, const FM &fm) {
     using Raw = decltype(fl(0, 0));
     constexpr int PER = (128 * 8) / kThreads;  // 16-byte chunks per thread
+    if constexpr (kIsAsync<FM>) {
+      const uint32_t a0 = smem_u32(A);
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int e = threadIdx.x + q * kThreads;
+        if constexpr (MA == K_MAJOR) {
+          const int m = e >> 3, c = e & 7;
+          cp_async16(a0 + sw128_offset(m, c * 8), fl(m, k0 + c * 8));
+        } else {
+          const int r = e >> 4, c = e & 15;
+          cp_async16(a0 + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8), fl(c * 8, k0 + r));
+        }
+      }
+      return;
+    } else {
 #pragma unroll
     for (int g = 0; g < PER; g += kBatch) {
       Raw raw[kBatch];
@@ -111,6 +135,7 @@ struct Engine {
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) *reinterpret_cast<uint4 *>(A + off[q]) = fm(raw[q], mm[q], kk[q]);
     }
+    }
   }
 
   template <int MB, class FL, class FM>
@@ -120,6 +145,21 @@ struct Engine {
     constexpr int CPR = NT / 8;  // 16-byte chunks per k-row (MN-major)
     constexpr int PER = (NT * 8) / kThreads;
     static_assert(PER % kBatch == 0, "B chunks per thread");
+    if constexpr (kIsAsync<FM>) {
+      const uint32_t b0 = smem_u32(B);
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int e = threadIdx.x + q * kThreads;
+        if constexpr (MB == K_MAJOR) {
+          const int n = e >> 3, c = e & 7;
+          cp_async16(b0 + sw128_offset(n, c * 8), fl(n, k0 + c * 8));
+        } else {
+          const int r = e / CPR, c = e % CPR;
+          cp_async16(b0 + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8), fl(c * 8, k0 + r));
+        }
+      }
+      return;
+    } else {
 #pragma unroll
     for (int g = 0; g < PER; g += kBatch) {
       Raw raw[kBatch];
@@ -140,6 +180,7 @@ struct Engine {
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) *reinterpret_cast<uint4 *>(B + off[q]) = fm(raw[q], nn[q], kk[q]);
     }
+    }
   }
 
   // Stage the 64-wide k slice [k0, k0+64) of A and B and issue its MMAs into the
@@ -153,6 +194,7 @@ struct Engine {
     uint8_t *B = A + A_BYTES;
     stage_A<MA>(A, k0, fal, fam);
     stage_B<MB>(B, k0, fbl, fbm);
+    if constexpr (kIsAsync<FAM> || kIsAsync<FBM>) cp_async_wait_all();
     fence_async_smem();
     tc_fence_before();  // order this thread's earlier TMEM reads before the MMAs below
     __syncthreads();
