@@ -205,15 +205,17 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
   SSD_LAUNCH("local_rev", launch_local_rev(pr, acs, dsl, gext, s));
   SSD_LAUNCH("seg_rscan", launch_seg_rscan(pr, gext, ablk, dfinal, gout, s));
   // chunk gradients
-  int vcol_parts = 1;
+  int vcol_parts = 1, nsub = pr.H, spg = pr.hpg;
   if constexpr (kIsBf16<T>) {
     if (tc) {
       __nv_bfloat16 *wb = reinterpret_cast<__nv_bfloat16 *>(wbuf);
       SSD_LAUNCH("tc_chunk_w", launch_tc_w(pr, u, dy, dtv, acs, cb, wb, tok, status, s));
-      SSD_LAUNCH("tc_chunk_dx", launch_tc_dx(pr, u, dy, dtv, acs, cb, dsl, gout, du, status, s));
+      SSD_LAUNCH("tc_chunk_dx", launch_tc_dx(pr, u, dy, dtv, acs, cb, dsl, gout, du, tok, status, s));
       SSD_LAUNCH("tc_chunk_dcdb",
                  launch_tc_dcdb(pr, u, dy, dtv, acs, wb, sst, segin, dsl, gout, dcp, dbp, tok, status, s));
       vcol_parts = pr.Q / 128;
+      nsub = pr.H / tc_head_subset(pr);
+      spg = pr.hpg / tc_head_subset(pr);
     }
   }
   if (!tc) {
@@ -224,7 +226,7 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
   }
   SSD_LAUNCH("chunk_dt",
              launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, go, chs, s));
-  SSD_LAUNCH("bc_reduce", launch_bc_reduce(pr, dcp, dbp, du, s));
+  SSD_LAUNCH("bc_reduce", launch_bc_reduce(pr, dcp, dbp, nsub, spg, du, s));
   // conv backward and parameter reductions
   SSD_LAUNCH("conv_bwd", launch_conv_bwd<T>(pr, du, go, convp, w.ntb, s));
   SSD_LAUNCH("param_reduce", launch_param_reduce(pr, chs, convp, w.ntb, g->ddt_bias, g->dA_log, g->dD, g->dconv_w, g->dconv_b, s));

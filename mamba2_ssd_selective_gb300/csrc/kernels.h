@@ -50,7 +50,10 @@ template <typename T>
 void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
                      int vcol_parts, const GradOut &go, float *chs, cudaStream_t s);
-void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, float *du, cudaStream_t s);
+// du_B/du_C = fixed-order sums of per-token partials: nsub partials per token,
+// the partials of group g being [g*spg, (g+1)*spg)
+void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int nsub, int spg, float *du,
+                      cudaStream_t s);
 
 // bf16 tensor-core chunk kernels (tc_chunk.cu); envelope: see tc_envelope()
 inline bool tc_envelope(const Problem &pr) {
@@ -66,11 +69,12 @@ void launch_tc_z(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 
 void launch_tc_w(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
                  const float *acs, const float *cb, __nv_bfloat16 *wbuf, float *tok, int *status, cudaStream_t s);
 void launch_tc_dx(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
-                  const float *acs, const float *cb, const float *dsl, const float *gout, float *du, int *status,
-                  cudaStream_t s);
+                  const float *acs, const float *cb, const float *dsl, const float *gout, float *du, float *tok,
+                  int *status, cudaStream_t s);
 void launch_tc_dcdb(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
                     const float *acs, const __nv_bfloat16 *wbuf, const float *sst, const float *segin,
                     const float *dsl, const float *gout, float *dcp, float *dbp, float *tok, int *status,
                     cudaStream_t s);
+int tc_head_subset(const Problem &pr);  // heads per dB/dC partial on the tensor-core path
 
 }  // namespace ssd

@@ -506,27 +506,30 @@ void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dt
                                                             vcol_parts, go, chs);
 }
 
-// du_B[t, g, n] = sum_{h in g} dB_h[t, n], du_C likewise, in head order.
+// du_B[t, g, n] = sum of the group's partials of dB[t, n] (one per head, or one
+// per head subset), du_C likewise, in a fixed order.
 __global__ void __launch_bounds__(256) bc_reduce_kernel(Problem pr, const float *__restrict__ dcp,
-                                                        const float *__restrict__ dbp, float *__restrict__ du) {
+                                                        const float *__restrict__ dbp, int nsub, int spg,
+                                                        float *__restrict__ du) {
   const int GN = pr.G * pr.N;
   const int idx = blockIdx.y * 256 + threadIdx.x;
   if (idx >= GN) return;
   const int g = idx / pr.N, n = idx % pr.N;
   const size_t tok = blockIdx.x;  // flat (b, t) token index
   float sb = 0.f, sc = 0.f;
-  for (int h = g * pr.hpg; h < (g + 1) * pr.hpg; ++h) {
-    sb += dbp[(tok * pr.H + h) * pr.N + n];
-    sc += dcp[(tok * pr.H + h) * pr.N + n];
+  for (int k = g * spg; k < (g + 1) * spg; ++k) {
+    sb += dbp[(tok * nsub + k) * pr.N + n];
+    sc += dcp[(tok * nsub + k) * pr.N + n];
   }
   const int HP = pr.H * pr.P;
   du[tok * pr.Cd + HP + idx] = sb;
   du[tok * pr.Cd + HP + GN + idx] = sc;
 }
 
-void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, float *du, cudaStream_t s) {
+void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int nsub, int spg, float *du,
+                      cudaStream_t s) {
   dim3 grid((unsigned)((size_t)pr.b * pr.L), (pr.G * pr.N + 255) / 256);
-  bc_reduce_kernel<<<grid, 256, 0, s>>>(pr, dcp, dbp, du);
+  bc_reduce_kernel<<<grid, 256, 0, s>>>(pr, dcp, dbp, nsub, spg, du);
 }
 
 #define SSD_INST(T)                                                                                                  \

@@ -385,13 +385,17 @@ void launch_tc_w(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
 }
 
 // ---------------------------------------------------------------- backward: dX
-// rows j of tile I:  du_x[j] = sum_{i>=j} M[i,j] dy_i + wdt_j dS_end B_j + D dy_j
+// rows j of tile I, two accumulators of P columns:
+//   T_j = sum_{i>=j} M[i,j] dy_i                    (K = the chunk's tokens)
+//   U_j = dS_end B_j                                 (K = N)
+// du_x[j] = T_j + wdt_j U_j + D dy_j, and q_j = x_j . U_j = B_j . (dS_end^T x_j),
+// the per-token piece of the chunk-state term of the dt adjoint.
 using EngDx = tc::Engine<64, 2>;
 __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
                                                     const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                     const float *__restrict__ acs, const float *__restrict__ cb,
                                                     const float *__restrict__ dsl, const float *__restrict__ gout,
-                                                    float *__restrict__ du, int *status) {
+                                                    float *__restrict__ du, float *__restrict__ tok, int *status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ ChunkVecs v;
   Carve<EngDx> sm(smem_raw);
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
   const float *gk = gout + (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
   EngDx eng;
   eng.init(sm.ring, sm.bars, status);
-  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 64);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
   auto fa1l = [&](int m0, int i) { return tc::ldf8(cbm + (size_t)i * Q + 128 * I + m0); };
   auto fa1 = [&](const tc::F8 &raw, int m0, int i) {
     const int j0 = 128 * I + m0;
@@ -429,15 +433,7 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
   auto fb1 = [&](int n0, int i) { return static_cast<const void *>(dyb + (size_t)i * HP + n0); };
   for (int k0 = 128 * I; k0 < Q; k0 += 64)
     eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::Async{}, k0 > 128 * I);
-  auto fa2l = [&](int m, int k0) { return tc::ldg16(ub + (size_t)(128 * I + m) * Cd + offB + k0); };
-  auto fa2 = [&](uint4 raw, int m, int) {
-    float b[8];
-    tc::unpack8(raw, b);
-    const float s = v.wdt[128 * I + m];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) b[q] *= s;
-    return tc::pack8(b);
-  };
+  auto fa2l = [&](int m, int k0) { return static_cast<const void *>(ub + (size_t)(128 * I + m) * Cd + offB + k0); };
   auto fb2l = [&](int p, int k0) {
     return tc::F16{tc::ldf8(dsc + (size_t)p * N + k0), tc::ldf8(gk + (size_t)p * N + k0)};
   };
@@ -449,39 +445,52 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
     for (int q = 0; q < 8; ++q) a[q] += de * b[q];
     return tc::pack8(a);
   };
-  for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem, k0, fa2l, fa2, fb2l, fb2, true);
+  for (int k0 = 0; k0 < N; k0 += 64)
+    eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2l, tc::Async{}, fb2l, fb2, k0 > 0);
   eng.finish();
   const int j = 128 * I + threadIdx.x;
-  const float Dh = pr.D[h];
+  const float Dh = pr.D[h], wdt = v.wdt[j];
   float *dr = du + ((size_t)bb * pr.L + id.t0 + j) * Cd + h * P;
+  float qsum = 0.f;
   for (int cc = 0; cc < 2; ++cc) {
-    float a[32];
+    float a[32], uu[32];
     sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), a);
+    sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 64 + 32 * cc), uu);
 #pragma unroll
     for (int q8 = 0; q8 < 4; ++q8) {
-      float d8[8];
+      float d8[8], x8[8];
       tc::unpack8(tc::ldg16(dyb + (size_t)j * HP + 32 * cc + 8 * q8), d8);
+      tc::unpack8(tc::ldg16(ub + (size_t)j * Cd + h * P + 32 * cc + 8 * q8), x8);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) a[8 * q8 + q] += Dh * d8[q];
+      for (int q = 0; q < 8; ++q) {
+        const int col = 8 * q8 + q;
+        qsum += x8[q] * uu[col];
+        a[col] += wdt * uu[col] + Dh * d8[q];
+      }
     }
     store_row_f32(dr + 32 * cc, a);
   }
-  tc::tmem_free_cta(tmem, 64);
+  tok[4 * (size_t)pr.b * pr.H * pr.L + ((size_t)bb * pr.H + h) * pr.L + id.t0 + j] = qsum;
+  tc::tmem_free_cta(tmem, 128);
 }
 
 void launch_tc_dx(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
-                  const float *cb, const float *dsl, const float *gout, float *du, int *status, cudaStream_t s) {
+                  const float *cb, const float *dsl, const float *gout, float *du, float *tok, int *status,
+                  cudaStream_t s) {
   static bool once = (set_smem(tc_dx_kernel, dyn_smem<EngDx>()), true);
   (void)once;
   tc_dx_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngDx>(), s>>>(pr, u, dy, dtv, acs, cb, dsl,
-                                                                                     gout, du, status);
+                                                                                     gout, du, tok, status);
 }
 
 // ---------------------------------------------------------------- backward: dC, dB
-// Per-head partials.  Rows i of tile I:
-//   dC_h[i] = sum_{j<=i} W[i,j] B_j + em_i S_in^T dy_i,   r_i = C_i . (em_i S_in^T dy_i)
-// rows j of tile I:
-//   dB_h[j] = sum_{i>=j} W[i,j] C_i + wdt_j dS_end^T x_j, q_j = B_j . (dS_end^T x_j)
+// CTA = (chunk, row tile I, subset of HS heads of one group, batch).  Over the
+// subset's heads the CTA accumulates in TMEM
+//   dC[i] += sum_{j<=i} W_h[i,j] B_j + em_h,i S_in,h^T dy_h,i       (rows i of tile I)
+//   dB[j] += sum_{i>=j} W_h[i,j] C_i + wdt_h,j dS_end,h^T x_h,j      (rows j of tile I)
+// and writes one partial per subset (summed over subsets in fixed order later).
+// The off-diagonal dC term is also issued into a per-head accumulator for
+//   r_i = C_i . (em_i S_in^T dy_i)   (per head, the Y_off piece of the dt adjoint).
 using EngDcdb = tc::Engine<128, 2>;
 __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__restrict__ u,
                                                       const bf16 *__restrict__ dy, const float *__restrict__ dtv,
@@ -489,72 +498,98 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
                                                       const float *__restrict__ sst, const float *__restrict__ segin,
                                                       const float *__restrict__ dsl, const float *__restrict__ gout,
                                                       float *__restrict__ dcp, float *__restrict__ dbp,
-                                                      float *__restrict__ tok, int *status) {
+                                                      float *__restrict__ tok, int hs_size, int *status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ ChunkVecs v;
   Carve<EngDcdb> sm(smem_raw);
   const int NTI = pr.Q / 128;
-  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
-  const ChunkIds id = make_ids(pr, c, h, bb);
-  load_chunk_vecs(pr, id, dtv, acs, v);
-  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P, H = pr.H;
-  const bf16 *ub = u + ((size_t)bb * pr.L + id.t0) * Cd;
-  const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
-  const int offX = h * P, offB = HP + id.g * N, offC = HP + pr.G * N + id.g * N;
-  const bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
+  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, sub = blockIdx.y, bb = blockIdx.z;
+  const int nsub = pr.H / hs_size;
+  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
+  const int h_first = sub * hs_size, g = h_first / pr.hpg;
+  const bf16 *ub = u + ((size_t)bb * pr.L + (size_t)c * Q) * Cd;
+  const int offB = HP + g * N, offC = HP + pr.G * N + g * N;
   const int k = c / pr.cps;
-  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-  const float dc = decay_seg_to_chunk(pr, acs_bh, bb, c);
-  const float de = decay_chunk_to_seg_end(pr, acs_bh, bb, c);
-  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
-  const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
-  const float *sloc = sst + co, *sseg = segin + so, *dsc = dsl + co, *gk = gout + so;
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
-  const size_t tb = ((size_t)bb * pr.H + h) * pr.L + id.t0;
   EngDcdb eng;
   eng.init(sm.ring, sm.bars, status);
-  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
-  const int m = threadIdx.x, r = 128 * I + m;  // row of this thread (i for dC, j for dB)
-  // ---- dC
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 512);
+  const uint32_t accC = tmem, accB = tmem + 128, accR = tmem + 256;
+  const int r = 128 * I + threadIdx.x;  // this thread's row (i for dC, j for dB)
   const bool has_off = c > 0;
-  if (has_off) {
-    auto fal = [&](int mm, int p0) { return tc::ldg16(dyb + (size_t)(128 * I + mm) * HP + p0); };
-    auto fam = [&](uint4 raw, int mm, int) {
-      float d8[8];
-      tc::unpack8(raw, d8);
-      const float s = v.em[128 * I + mm];
+  bool firstC = true, firstB = true;
+  auto combine = [](const tc::F16 &raw, float s) {
+    float a[8], b[8];
+    tc::f8_to(raw.x, a);
+    tc::f8_to(raw.y, b);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) d8[q] *= s;
-      return tc::pack8(d8);
-    };
-    auto fbl = [&](int n0, int p) {
-      return tc::F16{tc::ldf8(sloc + (size_t)p * N + n0), tc::ldf8(sseg + (size_t)p * N + n0)};
-    };
-    auto fbm = [&](const tc::F16 &raw, int, int) {
-      float a[8], b[8];
-      tc::f8_to(raw.x, a);
-      tc::f8_to(raw.y, b);
+    for (int q = 0; q < 8; ++q) a[q] += s * b[q];
+    return tc::pack8(a);
+  };
+  auto scaled = [](uint4 raw, float s) {
+    float x[8];
+    tc::unpack8(raw, x);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) a[q] += dc * b[q];
-      return tc::pack8(a);
-    };
-    for (int k0 = 0; k0 < P; k0 += 64) eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fal, fam, fbl, fbm, k0 > 0);
-  }
-  {
-    auto fa = [&](int mm, int j0) { return static_cast<const void *>(wm + (size_t)(128 * I + mm) * Q + j0); };
-    auto fb = [&](int n0, int j) { return static_cast<const void *>(ub + (size_t)j * Cd + offB + n0); };
-    for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
-      eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 0);
-  }
-  eng.finish();
-  {
+    for (int q = 0; q < 8; ++q) x[q] *= s;
+    return tc::pack8(x);
+  };
+  for (int hh = 0; hh < hs_size; ++hh) {
+    const int h = h_first + hh;
+    const ChunkIds id = make_ids(pr, c, h, bb);
+    __syncthreads();  // the previous head's functors are done with v
+    load_chunk_vecs(pr, id, dtv, acs, v);
+    const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
+    const bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
+    const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+    const float dc = decay_seg_to_chunk(pr, acs_bh, bb, c);
+    const float de = decay_chunk_to_seg_end(pr, acs_bh, bb, c);
+    const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
+    const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
+    const float *sloc = sst + co, *sseg = segin + so, *dsc = dsl + co, *gk = gout + so;
+    // ---- dC
+    if (has_off) {
+      auto fal = [&](int mm, int p0) { return tc::ldg16(dyb + (size_t)(128 * I + mm) * HP + p0); };
+      auto fam = [&](uint4 raw, int mm, int) { return scaled(raw, v.em[128 * I + mm]); };
+      auto fbl = [&](int n0, int p) {
+        return tc::F16{tc::ldf8(sloc + (size_t)p * N + n0), tc::ldf8(sseg + (size_t)p * N + n0)};
+      };
+      auto fbm = [&](const tc::F16 &raw, int, int) { return combine(raw, dc); };
+      for (int k0 = 0; k0 < P; k0 += 64)
+        eng.slice<K_MAJOR, MN_MAJOR>(accR, k0, fal, fam, fbl, fbm, k0 > 0, accC, !firstC || k0 > 0);
+      firstC = false;
+    }
+    {
+      auto fa = [&](int mm, int j0) { return static_cast<const void *>(wm + (size_t)(128 * I + mm) * Q + j0); };
+      auto fb = [&](int n0, int j) { return static_cast<const void *>(ub + (size_t)j * Cd + offB + n0); };
+      for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
+        eng.slice<K_MAJOR, MN_MAJOR>(accC, k0, fa, tc::Async{}, fb, tc::Async{}, !firstC || k0 > 0);
+      firstC = false;
+    }
+    // ---- dB
+    {
+      auto fal = [&](int mm, int p0) { return tc::ldg16(ub + (size_t)(128 * I + mm) * Cd + h * P + p0); };
+      auto fam = [&](uint4 raw, int mm, int) { return scaled(raw, v.wdt[128 * I + mm]); };
+      auto fbl = [&](int n0, int p) {
+        return tc::F16{tc::ldf8(dsc + (size_t)p * N + n0), tc::ldf8(gk + (size_t)p * N + n0)};
+      };
+      auto fbm = [&](const tc::F16 &raw, int, int) { return combine(raw, de); };
+      for (int k0 = 0; k0 < P; k0 += 64)
+        eng.slice<K_MAJOR, MN_MAJOR>(accB, k0, fal, fam, fbl, fbm, !firstB || k0 > 0);
+      firstB = false;
+    }
+    {
+      auto fa = [&](int m0, int i) { return static_cast<const void *>(wm + (size_t)i * Q + 128 * I + m0); };
+      auto fb = [&](int n0, int i) { return static_cast<const void *>(ub + (size_t)i * Cd + offC + n0); };
+      for (int k0 = 128 * I; k0 < Q; k0 += 64)
+        eng.slice<MN_MAJOR, MN_MAJOR>(accB, k0, fa, tc::Async{}, fb, tc::Async{}, true);
+    }
+    // ---- r for this head
     float rsum = 0.f;
-    float *o = dcp + (((size_t)bb * pr.L + id.t0 + r) * H + h) * N;
-    for (int cc = 0; cc < 4; ++cc) {
-      float a[32], b[32];
-      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), a);
-      if (has_off) {
-        sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 128 + 32 * cc), b);
+    if (has_off) {
+      eng.finish();
+      for (int cc = 0; cc < 4; ++cc) {
+        float b[32];
+        sm100::tmem_ld32(tc::tmem_lane_addr(accR, 32 * cc), b);
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           float c8[8];
@@ -562,59 +597,29 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
 #pragma unroll
           for (int q = 0; q < 8; ++q) rsum += c8[q] * b[8 * q8 + q];
         }
-#pragma unroll
-        for (int q = 0; q < 32; ++q) a[q] += b[q];
       }
-      store_row_f32(o + 32 * cc, a);
     }
-    tok[3 * BHL + tb + r] = rsum;
-  }
-  // ---- dB
-  {
-    auto fa = [&](int mm, int p0) { return static_cast<const void *>(ub + (size_t)(128 * I + mm) * Cd + offX + p0); };
-    auto fbl = [&](int n0, int p) {
-      return tc::F16{tc::ldf8(dsc + (size_t)p * N + n0), tc::ldf8(gk + (size_t)p * N + n0)};
-    };
-    auto fbm = [&](const tc::F16 &raw, int, int) {
-      float a[8], b[8];
-      tc::f8_to(raw.x, a);
-      tc::f8_to(raw.y, b);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) a[q] += de * b[q];
-      return tc::pack8(a);
-    };
-    for (int k0 = 0; k0 < P; k0 += 64)
-      eng.slice<K_MAJOR, MN_MAJOR>(tmem + 128, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
-  }
-  {
-    auto fa = [&](int m0, int i) { return static_cast<const void *>(wm + (size_t)i * Q + 128 * I + m0); };
-    auto fb = [&](int n0, int i) { return static_cast<const void *>(ub + (size_t)i * Cd + offC + n0); };
-    for (int k0 = 128 * I; k0 < Q; k0 += 64)
-      eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 128 * I);
+    tok[3 * BHL + ((size_t)bb * pr.H + h) * pr.L + (size_t)c * Q + r] = rsum;
   }
   eng.finish();
   {
-    float qsum = 0.f;
-    const float wdt = v.wdt[r];
-    float *o = dbp + (((size_t)bb * pr.L + id.t0 + r) * H + h) * N;
+    float *oc = dcp + (((size_t)bb * pr.L + (size_t)c * Q + r) * nsub + sub) * N;
+    float *ob = dbp + (((size_t)bb * pr.L + (size_t)c * Q + r) * nsub + sub) * N;
     for (int cc = 0; cc < 4; ++cc) {
-      float a[32], b[32];
-      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), a);
-      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 128 + 32 * cc), b);
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float b8[8];
-        tc::unpack8(tc::ldg16(ub + (size_t)r * Cd + offB + 32 * cc + 8 * q8), b8);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) qsum += b8[q] * b[8 * q8 + q];
-      }
-#pragma unroll
-      for (int q = 0; q < 32; ++q) a[q] += wdt * b[q];
-      store_row_f32(o + 32 * cc, a);
+      float a[32];
+      sm100::tmem_ld32(tc::tmem_lane_addr(accC, 32 * cc), a);
+      store_row_f32(oc + 32 * cc, a);
+      sm100::tmem_ld32(tc::tmem_lane_addr(accB, 32 * cc), a);
+      store_row_f32(ob + 32 * cc, a);
     }
-    tok[4 * BHL + tb + r] = qsum;
   }
-  tc::tmem_free_cta(tmem, 256);
+  tc::tmem_free_cta(tmem, 512);
+}
+
+int tc_head_subset(const Problem &pr) {
+  for (int hs : {16, 8, 4, 2})
+    if (pr.hpg % hs == 0) return hs;
+  return 1;
 }
 
 void launch_tc_dcdb(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
@@ -622,8 +627,9 @@ void launch_tc_dcdb(const Problem &pr, const bf16 *u, const bf16 *dy, const floa
                     float *dcp, float *dbp, float *tok, int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_dcdb_kernel, dyn_smem<EngDcdb>()), true);
   (void)once;
-  tc_dcdb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngDcdb>(), s>>>(
-      pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, status);
+  const int hs = tc_head_subset(pr);
+  tc_dcdb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H / hs, pr.b), 128, dyn_smem<EngDcdb>(), s>>>(
+      pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, hs, status);
 }
 
 }  // namespace ssd

@@ -185,9 +185,13 @@ struct Engine {
 
   // Stage the 64-wide k slice [k0, k0+64) of A and B and issue its MMAs into the
   // accumulator at TMEM address tmem_d.  Must be called by all 128 threads.
+  // With tmem_d2 != kNone the same staged operands are also issued into a
+  // second accumulator (accumulate2 selects whether that one accumulates).
+  static constexpr uint32_t kNone = 0xffffffffu;
   template <int MA, int MB, class FAL, class FAM, class FBL, class FBM>
   __device__ __forceinline__ void slice(uint32_t tmem_d, int k0, const FAL &fal, const FAM &fam, const FBL &fbl,
-                                        const FBM &fbm, bool accumulate) {
+                                        const FBM &fbm, bool accumulate, uint32_t tmem_d2 = kNone,
+                                        bool accumulate2 = false) {
     const int s = stage;
     if (uses[s] > 0) mbar_wait(&bars[s], (uses[s] - 1) & 1, status);
     uint8_t *A = ring + s * STAGE_BYTES;
@@ -207,6 +211,7 @@ struct Engine {
         const uint64_t ad = MA == K_MAJOR ? desc_sw128(a0 + kk * 32, 16, 1024) : desc_sw128(a0 + kk * 2048, 8192, 1024);
         const uint64_t bd = MB == K_MAJOR ? desc_sw128(b0 + kk * 32, 16, 1024) : desc_sw128(b0 + kk * 2048, 8192, 1024);
         umma_bf16(tmem_d, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        if (tmem_d2 != kNone) umma_bf16(tmem_d2, ad, bd, idesc, (accumulate2 || kk > 0) ? 1u : 0u);
       }
       umma_commit(&bars[s]);
     }
