@@ -55,7 +55,7 @@ __device__ __forceinline__ void store_row_f32(float *dst, const float (&v)[32]) 
 // CTA = (chunk, row tile I, group, batch); for each column tile J <= I the
 // 128 x 128 block of C_i . B_j is written in fp32 (upper blocks never read).
 using EngCB = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(128) tc_cb_kernel(Problem pr, const bf16 *__restrict__ u, float *__restrict__ cb,
+__global__ void __launch_bounds__(tc::kThreads) tc_cb_kernel(Problem pr, const bf16 *__restrict__ u, float *__restrict__ cb,
                                                     int *status) {
   extern __shared__ uint8_t smem_raw[];
   Carve<EngCB> sm(smem_raw);
@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(128) tc_cb_kernel(Problem pr, const bf16 *__re
     for (int k0 = 0; k0 < N; k0 += 64) eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 0);
   }
   eng.finish();
+  if (tc::owns_row()) {
   const int i = 128 * I + threadIdx.x;
   float *out = cb + (((size_t)bb * pr.nc + c) * pr.G + g) * Q * Q + (size_t)i * Q;
   for (int J = 0; J <= I; ++J)
@@ -81,20 +82,21 @@ __global__ void __launch_bounds__(128) tc_cb_kernel(Problem pr, const bf16 *__re
       sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 128 * J + 32 * cc), v);
       store_row_f32(out + 128 * J + 32 * cc, v);
     }
+  }
   tc::tmem_free_cta(tmem, 256);
 }
 
 void launch_tc_cb(const Problem &pr, const bf16 *u, float *cb, int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_cb_kernel, dyn_smem<EngCB>()), true);
   (void)once;
-  tc_cb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.G, pr.b), 128, dyn_smem<EngCB>(), s>>>(pr, u, cb, status);
+  tc_cb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.G, pr.b), tc::kThreads, dyn_smem<EngCB>(), s>>>(pr, u, cb, status);
 }
 
 // ---------------------------------------------------------------- chunk states
 // Sc^T[n, (h, p)] = sum_j B_j[n] wdt_h,j x_j[h, p] for a pair of heads of one
 // group: M = n (128), N = 2 x 64, K = the chunk's tokens.
 using EngPair = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads) tc_state_kernel(Problem pr, const bf16 *__restrict__ u,
                                                        const float *__restrict__ dtv, const float *__restrict__ acs,
                                                        float *__restrict__ sst, int *status) {
   extern __shared__ uint8_t smem_raw[];
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *_
   };
   for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
   eng.finish();
+  if (tc::owns_row()) {
   const int n = threadIdx.x;
   for (int cc = 0; cc < 4; ++cc) {
     float v[32];
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(128) tc_state_kernel(Problem pr, const bf16 *_
 #pragma unroll
     for (int q = 0; q < 32; ++q) o[(size_t)((cc & 1) * 32 + q) * N] = v[q];
   }
+  }
   tc::tmem_free_cta(tmem, 128);
 }
 
@@ -138,7 +142,7 @@ void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const f
                      cudaStream_t s) {
   static bool once = (set_smem(tc_state_kernel, dyn_smem<EngPair>()), true);
   (void)once;
-  tc_state_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), 128, dyn_smem<EngPair>(), s>>>(pr, u, dtv, acs, sst, status);
+  tc_state_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), tc::kThreads, dyn_smem<EngPair>(), s>>>(pr, u, dtv, acs, sst, status);
 }
 
 // ---------------------------------------------------------------- output
@@ -146,7 +150,7 @@ void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const f
 //   Y_diag = (CB o L o dt) X over j < 128(I+1),  Y_off = C S_in^T,
 //   y = Y_diag + em * Y_off + D x.
 using EngOut = tc::Engine<64, 2>;
-__global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
                                                      const float *__restrict__ dtv, const float *__restrict__ acs,
                                                      const float *__restrict__ cb, const float *__restrict__ sst,
                                                      const float *__restrict__ segin, bf16 *__restrict__ y,
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__r
       eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::Async{}, fb2l, fb2, k0 > 0);
   }
   eng.finish();
+  if (tc::owns_row()) {
   const int i = 128 * I + threadIdx.x;
   const float em = v.em[i], Dh = pr.D[h];
   const bf16 *xr = ub + (size_t)i * Cd + offX;
@@ -225,6 +230,7 @@ __global__ void __launch_bounds__(128) tc_out_kernel(Problem pr, const bf16 *__r
       *reinterpret_cast<uint4 *>(yr + 32 * cc + 8 * q8) = tc::pack8(o);
     }
   }
+  }
   tc::tmem_free_cta(tmem, 128);
 }
 
@@ -232,13 +238,13 @@ void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const flo
                    const float *sst, const float *segin, bf16 *y, int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_out_kernel, dyn_smem<EngOut>()), true);
   (void)once;
-  tc_out_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngOut>(), s>>>(pr, u, dtv, acs, cb, sst,
+  tc_out_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngOut>(), s>>>(pr, u, dtv, acs, cb, sst,
                                                                                        segin, y, status);
 }
 
 // ---------------------------------------------------------------- backward: Z
 // Z^T[n, (h, p)] = sum_i C_i[n] em_h,i dy_i[h, p]  for a pair of heads.
-__global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads) tc_z_kernel(Problem pr, const bf16 *__restrict__ u,
                                                    const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                    const float *__restrict__ acs, float *__restrict__ dsl,
                                                    int *status) {
@@ -268,6 +274,7 @@ __global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__res
   };
   for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
   eng.finish();
+  if (tc::owns_row()) {
   const int n = threadIdx.x;
   for (int cc = 0; cc < 4; ++cc) {
     float vv[32];
@@ -277,6 +284,7 @@ __global__ void __launch_bounds__(128) tc_z_kernel(Problem pr, const bf16 *__res
 #pragma unroll
     for (int q = 0; q < 32; ++q) o[(size_t)((cc & 1) * 32 + q) * N] = vv[q];
   }
+  }
   tc::tmem_free_cta(tmem, 128);
 }
 
@@ -284,7 +292,7 @@ void launch_tc_z(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
                  int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_z_kernel, dyn_smem<EngPair>()), true);
   (void)once;
-  tc_z_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), 128, dyn_smem<EngPair>(), s>>>(pr, u, dy, dtv, acs, dsl, status);
+  tc_z_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), tc::kThreads, dyn_smem<EngPair>(), s>>>(pr, u, dy, dtv, acs, dsl, status);
 }
 
 // ---------------------------------------------------------------- backward: W
@@ -293,7 +301,7 @@ void launch_tc_z(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
 // with row sums vrow_i = sum_j V dt_j (tok[0]) and this row tile's partial
 // column sums vcol_j = sum_i V (tok[2] for tile 0, tok[5] for tile 1).
 using EngW = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(128) tc_w_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads) tc_w_kernel(Problem pr, const bf16 *__restrict__ u,
                                                    const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                    const float *__restrict__ acs, const float *__restrict__ cb,
                                                    bf16 *__restrict__ wbuf, float *__restrict__ tok, int *status) {
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(128) tc_w_kernel(Problem pr, const bf16 *__res
   const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
   const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
   bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
-  for (int j = threadIdx.x; j < 256; j += 128) colacc[j] = 0.f;
+  for (int j = threadIdx.x; j < 256; j += tc::kThreads) colacc[j] = 0.f;
   EngW eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
@@ -323,56 +331,50 @@ __global__ void __launch_bounds__(128) tc_w_kernel(Problem pr, const bf16 *__res
       eng.slice<K_MAJOR, K_MAJOR>(tmem + 128 * J, k0, fa, tc::Async{}, fb, tc::Async{}, k0 > 0);
   }
   eng.finish();
-  const int m = threadIdx.x, i = 128 * I + m;
+  const bool ep = tc::owns_row();
+  const int m = threadIdx.x & (tc::kRows - 1), i = 128 * I + m;
   const float ai = v.acs[i];
   const int si = v.seq[i];
   float rowsum = 0.f;
   for (int J = 0; J <= I; ++J)
     for (int cc = 0; cc < 4; ++cc) {
       const int j0 = 128 * J + 32 * cc;
-      float a[32], cv[32], vv[32], wv[32];
-      sm100::tmem_ld32(tc::tmem_lane_addr(tmem, j0), a);
+      if (ep) {
+        float a[32];
+        sm100::tmem_ld32(tc::tmem_lane_addr(tmem, j0), a);
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float t8[8];
-        tc::ld8f(cbm + (size_t)i * Q + j0 + 8 * q8, t8);
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float cv[8], wv[8];
+          tc::ld8f(cbm + (size_t)i * Q + j0 + 8 * q8, cv);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) cv[8 * q8 + q] = t8[q];
+          for (int q = 0; q < 8; ++q) {
+            const int j = j0 + 8 * q8 + q;
+            const float dml = (j <= i && v.seq[j] == si) ? a[8 * q8 + q] * expf(ai - v.acs[j]) : 0.f;
+            const float vv = dml * cv[q];
+            wv[q] = dml * v.dt[j];
+            rowsum += vv * v.dt[j];
+            red[m][8 * q8 + q] = vv;
+          }
+          *reinterpret_cast<uint4 *>(wm + (size_t)i * Q + j0 + 8 * q8) = tc::pack8(wv);
+        }
       }
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int j = j0 + q;
-        const float dml = (j <= i && v.seq[j] == si) ? a[q] * expf(ai - v.acs[j]) : 0.f;
-        vv[q] = dml * cv[q];
-        wv[q] = dml * v.dt[j];
-        rowsum += vv[q] * v.dt[j];
-      }
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float t8[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) t8[q] = wv[8 * q8 + q];
-        *reinterpret_cast<uint4 *>(wm + (size_t)i * Q + j0 + 8 * q8) = tc::pack8(t8);
-      }
-      // column sums over this tile's 128 rows, fixed order
-#pragma unroll
-      for (int q = 0; q < 32; ++q) red[m][q] = vv[q];
+      // column sums of V over this tile's 128 rows, fixed order
       __syncthreads();
-      {
+      if (ep) {
         const int q = m & 31, quarter = m >> 5;
-        float s = 0.f;
-        for (int r = 0; r < 32; ++r) s += red[quarter * 32 + r][q];
-        part[quarter][q] = s;
+        float s2 = 0.f;
+        for (int rr = 0; rr < 32; ++rr) s2 += red[quarter * 32 + rr][q];
+        part[quarter][q] = s2;
       }
       __syncthreads();
-      if (m < 32) colacc[j0 + m] += (part[0][m] + part[1][m]) + (part[2][m] + part[3][m]);
+      if (threadIdx.x < 32) colacc[j0 + m] += (part[0][m] + part[1][m]) + (part[2][m] + part[3][m]);
       __syncthreads();
     }
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
   const size_t tb = ((size_t)bb * pr.H + h) * pr.L + id.t0;
-  tok[tb + i] = rowsum;
+  if (ep) tok[tb + i] = rowsum;
   float *vcol = tok + (I == 0 ? 2 : 5) * BHL + tb;
-  for (int j = m; j < Q; j += 128) vcol[j] = colacc[j];
+  for (int j = threadIdx.x; j < Q; j += tc::kThreads) vcol[j] = colacc[j];
   tc::tmem_free_cta(tmem, 256);
 }
 
@@ -380,7 +382,7 @@ void launch_tc_w(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
                  const float *cb, bf16 *wbuf, float *tok, int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_w_kernel, dyn_smem<EngW>()), true);
   (void)once;
-  tc_w_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngW>(), s>>>(pr, u, dy, dtv, acs, cb, wbuf,
+  tc_w_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngW>(), s>>>(pr, u, dy, dtv, acs, cb, wbuf,
                                                                                    tok, status);
 }
 
@@ -391,7 +393,7 @@ void launch_tc_w(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
 // du_x[j] = T_j + wdt_j U_j + D dy_j, and q_j = x_j . U_j = B_j . (dS_end^T x_j),
 // the per-token piece of the chunk-state term of the dt adjoint.
 using EngDx = tc::Engine<64, 2>;
-__global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
                                                     const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                     const float *__restrict__ acs, const float *__restrict__ cb,
                                                     const float *__restrict__ dsl, const float *__restrict__ gout,
@@ -448,6 +450,7 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
   for (int k0 = 0; k0 < N; k0 += 64)
     eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2l, tc::Async{}, fb2l, fb2, k0 > 0);
   eng.finish();
+  if (tc::owns_row()) {
   const int j = 128 * I + threadIdx.x;
   const float Dh = pr.D[h], wdt = v.wdt[j];
   float *dr = du + ((size_t)bb * pr.L + id.t0 + j) * Cd + h * P;
@@ -471,6 +474,7 @@ __global__ void __launch_bounds__(128) tc_dx_kernel(Problem pr, const bf16 *__re
     store_row_f32(dr + 32 * cc, a);
   }
   tok[4 * (size_t)pr.b * pr.H * pr.L + ((size_t)bb * pr.H + h) * pr.L + id.t0 + j] = qsum;
+  }
   tc::tmem_free_cta(tmem, 128);
 }
 
@@ -479,7 +483,7 @@ void launch_tc_dx(const Problem &pr, const bf16 *u, const bf16 *dy, const float 
                   cudaStream_t s) {
   static bool once = (set_smem(tc_dx_kernel, dyn_smem<EngDx>()), true);
   (void)once;
-  tc_dx_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), 128, dyn_smem<EngDx>(), s>>>(pr, u, dy, dtv, acs, cb, dsl,
+  tc_dx_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngDx>(), s>>>(pr, u, dy, dtv, acs, cb, dsl,
                                                                                      gout, du, tok, status);
 }
 
@@ -492,7 +496,7 @@ void launch_tc_dx(const Problem &pr, const bf16 *u, const bf16 *dy, const float 
 // The off-diagonal dC term is also issued into a per-head accumulator for
 //   r_i = C_i . (em_i S_in^T dy_i)   (per head, the Y_off piece of the dt adjoint).
 using EngDcdb = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads) tc_dcdb_kernel(Problem pr, const bf16 *__restrict__ u,
                                                       const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                       const float *__restrict__ acs, const bf16 *__restrict__ wbuf,
                                                       const float *__restrict__ sst, const float *__restrict__ segin,
@@ -515,7 +519,7 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 512);
   const uint32_t accC = tmem, accB = tmem + 128, accR = tmem + 256;
-  const int r = 128 * I + threadIdx.x;  // this thread's row (i for dC, j for dB)
+  const int r = 128 * I + (threadIdx.x & (tc::kRows - 1));  // this thread's row (i for dC, j for dB)
   const bool has_off = c > 0;
   bool firstC = true, firstB = true;
   auto combine = [](const tc::F16 &raw, float s) {
@@ -585,8 +589,8 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
     }
     // ---- r for this head
     float rsum = 0.f;
-    if (has_off) {
-      eng.finish();
+    if (has_off) eng.finish();
+    if (has_off && tc::owns_row()) {
       for (int cc = 0; cc < 4; ++cc) {
         float b[32];
         sm100::tmem_ld32(tc::tmem_lane_addr(accR, 32 * cc), b);
@@ -599,10 +603,10 @@ __global__ void __launch_bounds__(128) tc_dcdb_kernel(Problem pr, const bf16 *__
         }
       }
     }
-    tok[3 * BHL + ((size_t)bb * pr.H + h) * pr.L + (size_t)c * Q + r] = rsum;
+    if (tc::owns_row()) tok[3 * BHL + ((size_t)bb * pr.H + h) * pr.L + (size_t)c * Q + r] = rsum;
   }
   eng.finish();
-  {
+  if (tc::owns_row()) {
     float *oc = dcp + (((size_t)bb * pr.L + (size_t)c * Q + r) * nsub + sub) * N;
     float *ob = dbp + (((size_t)bb * pr.L + (size_t)c * Q + r) * nsub + sub) * N;
     for (int cc = 0; cc < 4; ++cc) {
@@ -628,7 +632,7 @@ void launch_tc_dcdb(const Problem &pr, const bf16 *u, const bf16 *dy, const floa
   static bool once = (set_smem(tc_dcdb_kernel, dyn_smem<EngDcdb>()), true);
   (void)once;
   const int hs = tc_head_subset(pr);
-  tc_dcdb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H / hs, pr.b), 128, dyn_smem<EngDcdb>(), s>>>(
+  tc_dcdb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H / hs, pr.b), tc::kThreads, dyn_smem<EngDcdb>(), s>>>(
       pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, hs, status);
 }
 

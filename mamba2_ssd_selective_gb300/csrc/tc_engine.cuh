@@ -1,7 +1,7 @@
 // A small tcgen05 contraction engine for the chunk kernels of the bf16 path.
 //
-// One CTA of 128 threads owns a 128-row accumulator block in tensor memory
-// (TMEM lane = row).  A contraction  D[128 x NT] (+)= sum_k A[m,k] B[n,k]  is
+// One CTA of 256 threads owns a 128-row accumulator block in tensor memory
+// (TMEM lane = row, owned by threads 0..127; all 256 threads stage operands).  A contraction  D[128 x NT] (+)= sum_k A[m,k] B[n,k]  is
 // fed 64 k at a time: every thread stages its share of the A and B tiles
 // straight into shared memory in the 128-byte-swizzled UMMA layout (so masks,
 // decays and scalings are applied while staging and nothing is materialised in
@@ -28,7 +28,10 @@ namespace tc {
 using namespace sm100;
 
 enum Major : int { K_MAJOR = 0, MN_MAJOR = 1 };
-constexpr int kThreads = 128;
+// Every engine CTA has kThreads threads: all of them stage operands; the first
+// 128 (warps 0-3, one per TMEM lane quadrant) own the accumulator rows.
+constexpr int kThreads = 256;
+constexpr int kRows = 128;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -94,12 +97,13 @@ struct Engine {
   // returns the raw data, make(raw, m, k) turns it into 8 packed bf16.  Every
   // thread first issues the loads of kBatch chunks back to back, then
   // transforms and stores them, so kBatch loads per thread are in flight.
-  static constexpr int kBatch = 4;
+  static constexpr int kBatchMax = 4;
 
   template <int MA, class FL, class FM>
   __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FL &fl, const FM &fm) {
     using Raw = decltype(fl(0, 0));
     constexpr int PER = (128 * 8) / kThreads;  // 16-byte chunks per thread
+    constexpr int kBatch = PER < kBatchMax ? PER : kBatchMax;
     if constexpr (kIsAsync<FM>) {
       const uint32_t a0 = smem_u32(A);
 #pragma unroll
@@ -144,7 +148,8 @@ struct Engine {
     static_assert(MB == K_MAJOR || NT % 64 == 0, "MN-major B needs whole 64-wide atoms");
     constexpr int CPR = NT / 8;  // 16-byte chunks per k-row (MN-major)
     constexpr int PER = (NT * 8) / kThreads;
-    static_assert(PER % kBatch == 0, "B chunks per thread");
+    constexpr int kBatch = PER < kBatchMax ? PER : kBatchMax;
+    static_assert(PER >= 1 && PER % kBatch == 0, "B chunks per thread");
     if constexpr (kIsAsync<FM>) {
       const uint32_t b0 = smem_u32(B);
 #pragma unroll
@@ -271,10 +276,12 @@ __device__ __forceinline__ void tmem_free_cta(uint32_t base, uint32_t ncols) {
   if ((threadIdx.x >> 5) == 0) tmem_dealloc(base, ncols);
 }
 
-// TMEM address of (this thread's lane, column col) for a 128-thread CTA.
+// TMEM address of (this thread's lane, column col); threads 0..127 own lanes 0..127.
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int col) {
-  return base + ((uint32_t)((threadIdx.x >> 5) * 32) << 16) + (uint32_t)col;
+  return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
 }
+// true for the threads that own an accumulator row
+__device__ __forceinline__ bool owns_row() { return threadIdx.x < kRows; }
 
 }  // namespace tc
 }  // namespace ssd
