@@ -55,7 +55,7 @@ __device__ __forceinline__ void store_row_f32(float *dst, const float (&v)[32]) 
 // CTA = (chunk, row tile I, group, batch); for each column tile J <= I the
 // 128 x 128 block of C_i . B_j is written in fp32 (upper blocks never read).
 using EngCB = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(tc::kThreads) tc_cb_kernel(Problem pr, const bf16 *__restrict__ u, float *__restrict__ cb,
+__global__ void __launch_bounds__(tc::kThreads, 3) tc_cb_kernel(Problem pr, const bf16 *__restrict__ u, float *__restrict__ cb,
                                                     int *status) {
   extern __shared__ uint8_t smem_raw[];
   Carve<EngCB> sm(smem_raw);
@@ -96,7 +96,7 @@ void launch_tc_cb(const Problem &pr, const bf16 *u, float *cb, int *status, cuda
 // Sc^T[n, (h, p)] = sum_j B_j[n] wdt_h,j x_j[h, p] for a pair of heads of one
 // group: M = n (128), N = 2 x 64, K = the chunk's tokens.
 using EngPair = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(tc::kThreads) tc_state_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads, 3) tc_state_kernel(Problem pr, const bf16 *__restrict__ u,
                                                        const float *__restrict__ dtv, const float *__restrict__ acs,
                                                        float *__restrict__ sst, int *status) {
   extern __shared__ uint8_t smem_raw[];
@@ -150,7 +150,7 @@ void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const f
 //   Y_diag = (CB o L o dt) X over j < 128(I+1),  Y_off = C S_in^T,
 //   y = Y_diag + em * Y_off + D x.
 using EngOut = tc::Engine<64, 2>;
-__global__ void __launch_bounds__(tc::kThreads) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads, 3) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
                                                      const float *__restrict__ dtv, const float *__restrict__ acs,
                                                      const float *__restrict__ cb, const float *__restrict__ sst,
                                                      const float *__restrict__ segin, bf16 *__restrict__ y,
@@ -244,7 +244,7 @@ void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const flo
 
 // ---------------------------------------------------------------- backward: Z
 // Z^T[n, (h, p)] = sum_i C_i[n] em_h,i dy_i[h, p]  for a pair of heads.
-__global__ void __launch_bounds__(tc::kThreads) tc_z_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const bf16 *__restrict__ u,
                                                    const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                    const float *__restrict__ acs, float *__restrict__ dsl,
                                                    int *status) {
@@ -301,7 +301,7 @@ void launch_tc_z(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
 // with row sums vrow_i = sum_j V dt_j (tok[0]) and this row tile's partial
 // column sums vcol_j = sum_i V (tok[2] for tile 0, tok[5] for tile 1).
 using EngW = tc::Engine<128, 2>;
-__global__ void __launch_bounds__(tc::kThreads) tc_w_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads, 3) tc_w_kernel(Problem pr, const bf16 *__restrict__ u,
                                                    const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                    const float *__restrict__ acs, const float *__restrict__ cb,
                                                    bf16 *__restrict__ wbuf, float *__restrict__ tok, int *status) {
@@ -393,7 +393,7 @@ void launch_tc_w(const Problem &pr, const bf16 *u, const bf16 *dy, const float *
 // du_x[j] = T_j + wdt_j U_j + D dy_j, and q_j = x_j . U_j = B_j . (dS_end^T x_j),
 // the per-token piece of the chunk-state term of the dt adjoint.
 using EngDx = tc::Engine<64, 2>;
-__global__ void __launch_bounds__(tc::kThreads) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
+__global__ void __launch_bounds__(tc::kThreads, 3) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
                                                     const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                     const float *__restrict__ acs, const float *__restrict__ cb,
                                                     const float *__restrict__ dsl, const float *__restrict__ gout,
