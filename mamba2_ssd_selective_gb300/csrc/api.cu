@@ -129,9 +129,21 @@ bool use_tc(const Problem &pr) {
   return kIsBf16<T> && tc_envelope(pr);
 }
 
+// point the problem's decay tables at the workspace
+Problem with_tables(const Problem &in, char *ws, const Workspace &w) {
+  Problem pr = in;
+  float *tab = reinterpret_cast<float *>(ws + w.dtab);
+  const size_t n = (size_t)pr.b * pr.H * pr.nc;
+  pr.cdec = tab;
+  pr.dstart = tab + n;
+  pr.dend = tab + 2 * n;
+  return pr;
+}
+
 template <typename T>
-ssd_status forward_impl(const Problem &pr, T *y, float *final_state, float *segin_user, char *ws,
+ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *segin_user, char *ws,
                         const Workspace &w, cudaStream_t s) {
+  const Problem pr = with_tables(pr_in, ws, w);
   cudaMemsetAsync(ws + w.status, 0, sizeof(int), s);
   T *u = reinterpret_cast<T *>(ws + w.u);
   float *dtv = reinterpret_cast<float *>(ws + w.dtv), *acs = reinterpret_cast<float *>(ws + w.acs);
@@ -142,6 +154,8 @@ ssd_status forward_impl(const Problem &pr, T *y, float *final_state, float *segi
   const bool tc = use_tc<T>(pr);
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
+  SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
+                                                 const_cast<float *>(pr.dend), s));
   if constexpr (kIsBf16<T>) {
     if (tc) {
       SSD_LAUNCH("tc_cb", launch_tc_cb(pr, u, cb, status, s));
@@ -155,15 +169,20 @@ ssd_status forward_impl(const Problem &pr, T *y, float *final_state, float *segi
   SSD_LAUNCH("local_pass", launch_local_pass(pr, acs, sst, sext, ablk, s));
   SSD_LAUNCH("seg_scan", launch_seg_scan(pr, sext, ablk, segin, final_state, s));
   if constexpr (kIsBf16<T>) {
-    if (tc) SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, cb, sst, segin, y, status, s));
+    if (tc) {
+      __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
+      SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, 0, s));
+      SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, cb, sin16, y, status, s));
+    }
   }
   if (!tc) SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, y, s));
   return launch_status();
 }
 
 template <typename T>
-ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, const float *segin_user,
+ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal, const float *segin_user,
                          const ssd_grads *g, char *ws, const Workspace &w, cudaStream_t s) {
+  const Problem pr = with_tables(pr_in, ws, w);
   cudaMemsetAsync(ws + w.status, 0, sizeof(int), s);
   T *u = reinterpret_cast<T *>(ws + w.u);
   float *dtv = reinterpret_cast<float *>(ws + w.dtv), *acs = reinterpret_cast<float *>(ws + w.acs);
@@ -180,6 +199,8 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
   // recompute: conv, dt, CB, chunk states, local segment passes (and the scan)
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
+  SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
+                                                 const_cast<float *>(pr.dend), s));
   if constexpr (kIsBf16<T>) {
     if (tc) {
       SSD_LAUNCH("tc_cb", launch_tc_cb(pr, u, cb, status, s));
@@ -210,9 +231,12 @@ ssd_status backward_impl(const Problem &pr, const T *dy, const float *dfinal, co
     if (tc) {
       __nv_bfloat16 *wb = reinterpret_cast<__nv_bfloat16 *>(wbuf);
       SSD_LAUNCH("tc_chunk_w", launch_tc_w(pr, u, dy, dtv, acs, cb, wb, tok, status, s));
-      SSD_LAUNCH("tc_chunk_dx", launch_tc_dx(pr, u, dy, dtv, acs, cb, dsl, gout, du, tok, status, s));
-      SSD_LAUNCH("tc_chunk_dcdb",
-                 launch_tc_dcdb(pr, u, dy, dtv, acs, wb, sst, segin, dsl, gout, dcp, dbp, tok, status, s));
+      __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
+      __nv_bfloat16 *dse16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.dse16);
+      SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, 0, s));
+      SSD_LAUNCH("combine_state", launch_combine_state(pr, dsl, gout, dse16, 1, s));
+      SSD_LAUNCH("tc_chunk_dx", launch_tc_dx(pr, u, dy, dtv, acs, cb, dse16, du, tok, status, s));
+      SSD_LAUNCH("tc_chunk_dcdb", launch_tc_dcdb(pr, u, dy, dtv, acs, wb, sin16, dse16, dcp, dbp, tok, status, s));
       vcol_parts = pr.Q / 128;
       nsub = pr.H / tc_head_subset(pr);
       spg = pr.hpg / tc_head_subset(pr);

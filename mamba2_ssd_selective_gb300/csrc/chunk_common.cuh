@@ -61,20 +61,13 @@ __device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkId
 }
 
 // decay carrying the segment's initial state to the start of chunk c
-__device__ __forceinline__ float decay_seg_to_chunk(const Problem &pr, const float *acs_bh, int bb, int c) {
-  const int c0 = (c / pr.cps) * pr.cps;
-  float d = 1.f;
-  for (int cc = c0; cc < c; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
-  return d;
+__device__ __forceinline__ float decay_seg_to_chunk(const Problem &pr, int bb, int h, int c) {
+  return __ldg(pr.dstart + dtab_index(pr, bb, h, c));
 }
 
 // decay carrying the state at the end of chunk c to the end of its segment
-__device__ __forceinline__ float decay_chunk_to_seg_end(const Problem &pr, const float *acs_bh, int bb, int c) {
-  const int c1 = (c / pr.cps + 1) * pr.cps;
-  float d = 1.f;
-  for (int cc = c + 1; cc < c1; ++cc) d *= chunk_decay(pr, acs_bh, bb, cc);
-  return d;
+__device__ __forceinline__ float decay_chunk_to_seg_end(const Problem &pr, int bb, int h, int c) {
+  return __ldg(pr.dend + dtab_index(pr, bb, h, c));
 }
-
 
 }  // namespace ssd

@@ -18,6 +18,10 @@ struct Problem {
   long long xs, Bs, Cs, dts;  // token strides (elements)
   const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
   const int *seq_idx;  // (b, L) or nullptr
+  // per (b, h, chunk) decay tables, (b, H, nc) fp32, filled by decay_tables_kernel:
+  const float *cdec;    // product of the chunk's per-token decays (0 at row start / sequence start inside)
+  const float *dstart;  // product of cdec over the segment's chunks before this one
+  const float *dend;    // product of cdec over the segment's chunks after this one
 };
 
 // ---------------------------------------------------------------- dtypes
@@ -39,14 +43,22 @@ __device__ __forceinline__ int seq_of(const Problem &pr, int b, int t) {
 }
 
 // Product of the per-token decays over chunk c of row b, head h: the factor that
-// carries the state entering the chunk to its end.  Zero at the row start and
+// carries the state entering the chunk to its end (computed from Acs; kernels
+// read it from the decay tables through chunk_decay()).  Zero at the row start and
 // when a packed sequence starts inside the chunk.  acs_bh: chunk-local inclusive
 // cumsum of dt*A for (b, h), length L.
-__device__ __forceinline__ float chunk_decay(const Problem &pr, const float *acs_bh, int b, int c) {
+__device__ __forceinline__ float chunk_decay_raw(const Problem &pr, const float *acs_bh, int b, int c) {
   if (c == 0) return 0.f;
   int t0 = c * pr.Q, t1 = t0 + pr.Q - 1;
   if (pr.seq_idx && seq_of(pr, b, t0 - 1) != seq_of(pr, b, t1)) return 0.f;
   return expf(acs_bh[t1]);
+}
+
+__device__ __forceinline__ size_t dtab_index(const Problem &pr, int b, int h, int c) {
+  return ((size_t)b * pr.H + h) * pr.nc + c;
+}
+__device__ __forceinline__ float chunk_decay(const Problem &pr, int b, int h, int c) {
+  return __ldg(pr.cdec + dtab_index(pr, b, h, c));
 }
 
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -62,10 +74,13 @@ struct Workspace {
   size_t dtv, acs;                             // (b, H, L) f32: dt, chunk-local cumsum of dt*A
   size_t cb;                                   // (b, nc, G, Q, Q) f32: C_i . B_j per chunk
   size_t sst;                                  // (b, nc, H, P, N) f32: chunk states, then local S_in
+  size_t sin16;                                // (b, nc, H, P, N) bf16: true S_in (tensor-core path)
+  size_t dtab;                                 // 3 x (b, H, nc) f32: cdec, dstart, dend
   size_t sext, segin;                          // (b, S, H, P, N) f32
   size_t ablk;                                 // (b, S, H) f32
   // backward only
   size_t dsl;                                  // (b, nc, H, P, N) f32: Y_off adjoint, then local dS at chunk ends
+  size_t dse16;                                // (b, nc, H, P, N) bf16: true dS at chunk ends (tensor-core path)
   size_t gext, gout;                           // (b, S, H, P, N) f32
   size_t du;                                   // (b, L, Cd) f32: grad of post-conv activations
   size_t w;                                    // (b, nc, H, Q, Q) f32: dM o L o dt
@@ -96,9 +111,12 @@ inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward
   w.sext = take(b * S * H * P * N * 4);
   w.segin = take(b * S * H * P * N * 4);
   w.ablk = take(b * S * H * 4);
+  w.sin16 = take(b * nc * H * P * N * 2);
+  w.dtab = take(3 * b * H * nc * 4);
   w.ntb = (int)((L + kConvBwdTok - 1) / kConvBwdTok);
   if (backward) {
     w.dsl = take(b * nc * H * P * N * 4);
+    w.dse16 = take(b * nc * H * P * N * 2);
     w.gext = take(b * S * H * P * N * 4);
     w.gout = take(b * S * H * P * N * 4);
     w.du = take(b * L * Cd * 4);

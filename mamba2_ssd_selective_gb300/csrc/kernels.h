@@ -20,6 +20,9 @@ void launch_param_reduce(const Problem &pr, const float *chs, const float *convp
 void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStream_t s);
 
 // segment summaries and scans (scan.cu)
+void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, cudaStream_t s);
+void launch_combine_state(const Problem &pr, const float *a, const float *seg, __nv_bfloat16 *out, int mode,
+                          cudaStream_t s);
 void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s);
 void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, float *segin, float *final_state,
                      cudaStream_t s);
@@ -63,18 +66,17 @@ void launch_tc_cb(const Problem &pr, const __nv_bfloat16 *u, float *cb, int *sta
 void launch_tc_state(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, float *sst,
                      int *status, cudaStream_t s);
 void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, const float *cb,
-                   const float *sst, const float *segin, __nv_bfloat16 *y, int *status, cudaStream_t s);
+                   const __nv_bfloat16 *sin16, __nv_bfloat16 *y, int *status, cudaStream_t s);
 void launch_tc_z(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
                  const float *acs, float *dsl, int *status, cudaStream_t s);
 void launch_tc_w(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
                  const float *acs, const float *cb, __nv_bfloat16 *wbuf, float *tok, int *status, cudaStream_t s);
 void launch_tc_dx(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
-                  const float *acs, const float *cb, const float *dsl, const float *gout, float *du, float *tok,
-                  int *status, cudaStream_t s);
+                  const float *acs, const float *cb, const __nv_bfloat16 *dse16, float *du, float *tok, int *status,
+                  cudaStream_t s);
 void launch_tc_dcdb(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
-                    const float *acs, const __nv_bfloat16 *wbuf, const float *sst, const float *segin,
-                    const float *dsl, const float *gout, float *dcp, float *dbp, float *tok, int *status,
-                    cudaStream_t s);
+                    const float *acs, const __nv_bfloat16 *wbuf, const __nv_bfloat16 *sin16,
+                    const __nv_bfloat16 *dse16, float *dcp, float *dbp, float *tok, int *status, cudaStream_t s);
 int tc_head_subset(const Problem &pr);  // heads per dB/dC partial on the tensor-core path
 
 }  // namespace ssd

@@ -17,6 +17,67 @@ namespace ssd {
 
 constexpr int kScanBatch = 8;  // chunks whose loads are in flight together
 
+// Decay tables of one (b, h): cdec[c] = product of the chunk's per-token decays
+// (from Acs and seq_idx), then per segment the exclusive prefix and suffix
+// products dstart[c] = prod_{c' in seg, c' < c} cdec[c'], dend[c] = prod_{c' > c}.
+__global__ void __launch_bounds__(256) decay_tables_kernel(Problem pr, const float *__restrict__ acs, float *cdec,
+                                                           float *dstart, float *dend) {
+  const int h = blockIdx.x, bb = blockIdx.y;
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  const size_t base = ((size_t)bb * pr.H + h) * pr.nc;
+  for (int c = threadIdx.x; c < pr.nc; c += blockDim.x) cdec[base + c] = chunk_decay_raw(pr, acs_bh, bb, c);
+  __syncthreads();
+  for (int k = threadIdx.x; k < pr.S; k += blockDim.x) {
+    const int c0 = k * pr.cps, c1 = c0 + pr.cps;
+    float d = 1.f;
+    for (int c = c0; c < c1; ++c) {
+      dstart[base + c] = d;
+      d *= cdec[base + c];
+    }
+    d = 1.f;
+    for (int c = c1 - 1; c >= c0; --c) {
+      dend[base + c] = d;
+      d *= cdec[base + c];
+    }
+  }
+}
+
+void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, cudaStream_t s) {
+  decay_tables_kernel<<<dim3(pr.H, pr.b), 256, 0, s>>>(pr, acs, cdec, dstart, dend);
+}
+
+// out[b, c, h] = bf16(a[b, c, h] + d * seg[b, k(c), h]) over the P x N state, with
+// d = dstart (mode 0: the true state entering the chunk) or dend (mode 1: the
+// true state gradient at the chunk end).  8 elements per thread.
+__global__ void __launch_bounds__(256) combine_state_kernel(Problem pr, const float *__restrict__ a,
+                                                            const float *__restrict__ seg,
+                                                            __nv_bfloat16 *__restrict__ out, int mode) {
+  const int PN = pr.P * pr.N;
+  const int e = (blockIdx.x * 256 + threadIdx.x) * 8;
+  const int h = blockIdx.y, bc = blockIdx.z, bb = bc / pr.nc, c = bc % pr.nc, k = c / pr.cps;
+  if (e >= PN) return;
+  const float d = mode == 0 ? __ldg(pr.dstart + dtab_index(pr, bb, h, c)) : __ldg(pr.dend + dtab_index(pr, bb, h, c));
+  const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * PN + e;
+  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * PN + e;
+  const float4 a0 = *reinterpret_cast<const float4 *>(a + co), a1 = *reinterpret_cast<const float4 *>(a + co + 4);
+  const float4 s0 = *reinterpret_cast<const float4 *>(seg + so), s1 = *reinterpret_cast<const float4 *>(seg + so + 4);
+  const float v[8] = {a0.x + d * s0.x, a0.y + d * s0.y, a0.z + d * s0.z, a0.w + d * s0.w,
+                      a1.x + d * s1.x, a1.y + d * s1.y, a1.z + d * s1.z, a1.w + d * s1.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&b2);
+  }
+  *reinterpret_cast<uint4 *>(out + co) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+void launch_combine_state(const Problem &pr, const float *a, const float *seg, __nv_bfloat16 *out, int mode,
+                          cudaStream_t s) {
+  dim3 grid((pr.P * pr.N / 8 + 255) / 256, pr.H, pr.b * pr.nc);
+  combine_state_kernel<<<grid, 256, 0, s>>>(pr, a, seg, out, mode);
+}
+
 // Local pass of segment k: S <- a_c * S + Sc[c] over the segment's chunks from
 // S = 0.  Overwrites sst[c] (the chunk's own state contribution Sc) with the
 // local state entering the chunk, and writes S_ext[k] and a_block[k].  Each
@@ -31,7 +92,6 @@ __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float
   const int e4 = blockIdx.x * 256 + threadIdx.x;
   const bool active = e4 < PN4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
-  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
   const size_t cstride = (size_t)pr.H * PN;  // floats between consecutive chunks
   float4 *base = reinterpret_cast<float4 *>(sst + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN) + e4;
   float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -39,7 +99,7 @@ __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float
   for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
     const int nb = min(kScanBatch, pr.cps - c0);
     __syncthreads();
-    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, acs_bh, bb, k * pr.cps + c0 + threadIdx.x);
+    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, bb, h, k * pr.cps + c0 + threadIdx.x);
     __syncthreads();
     if (threadIdx.x == 0)
       for (int q = 0; q < nb; ++q) prod *= dec[q];
@@ -104,7 +164,6 @@ __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float 
   const int e4 = blockIdx.x * 256 + threadIdx.x;
   const bool active = e4 < PN4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
-  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
   const size_t cstride4 = (size_t)pr.H * PN / 4;
   float4 *base = reinterpret_cast<float4 *>(dsl + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN) + e4;
   float4 dS = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -112,7 +171,7 @@ __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float 
     const int nb = min(kScanBatch, c1);
     const int c0 = c1 - nb;  // this batch covers chunks [c0, c1) of the segment, walked downwards
     __syncthreads();
-    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, acs_bh, bb, k * pr.cps + c0 + threadIdx.x);
+    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, bb, h, k * pr.cps + c0 + threadIdx.x);
     __syncthreads();
     if (active) {
       float4 z[kScanBatch];

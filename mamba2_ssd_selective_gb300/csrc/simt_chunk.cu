@@ -109,8 +109,7 @@ __global__ void __launch_bounds__(256) out_kernel(Problem pr, const T *__restric
   const int offX = id.h * P, offC = HP + pr.G * N + id.g * N;
   const float *cbm = cb + (((size_t)id.bb * pr.nc + id.c) * pr.G + id.g) * Q * Q;
   const int k = id.c / pr.cps;
-  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
-  const float dc = decay_seg_to_chunk(pr, acs_bh, id.bb, id.c);
+  const float dc = decay_seg_to_chunk(pr, id.bb, id.h, id.c);
   const float *sloc = sst + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
   const float *sseg = segin + (((size_t)id.bb * pr.S + k) * pr.H + id.h) * P * N;
   const float Dh = pr.D[id.h];
@@ -257,8 +256,7 @@ __global__ void __launch_bounds__(256) dx_kernel(Problem pr, const T *__restrict
   const int offX = id.h * P, offB = HP + id.g * N;
   const float *cbm = cb + (((size_t)id.bb * pr.nc + id.c) * pr.G + id.g) * Q * Q;
   const int k = id.c / pr.cps;
-  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
-  const float de = decay_chunk_to_seg_end(pr, acs_bh, id.bb, id.c);
+  const float de = decay_chunk_to_seg_end(pr, id.bb, id.h, id.c);
   const float *dsc = dsl + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
   const float *gk = gout + (((size_t)id.bb * pr.S + k) * pr.H + id.h) * P * N;
   const float Dh = pr.D[id.h];
@@ -309,9 +307,8 @@ __global__ void __launch_bounds__(256) dcdb_kernel(Problem pr, const T *__restri
   const int offX = id.h * P, offB = HP + id.g * N, offC = HP + pr.G * N + id.g * N;
   const float *wm = wbuf + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * Q * Q;
   const int k = id.c / pr.cps;
-  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
-  const float dc = decay_seg_to_chunk(pr, acs_bh, id.bb, id.c);
-  const float de = decay_chunk_to_seg_end(pr, acs_bh, id.bb, id.c);
+  const float dc = decay_seg_to_chunk(pr, id.bb, id.h, id.c);
+  const float de = decay_chunk_to_seg_end(pr, id.bb, id.h, id.c);
   const size_t so = (((size_t)id.bb * pr.S + k) * pr.H + id.h) * P * N;
   const size_t co = (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * P * N;
   const float *sloc = sst + co, *sseg = segin + so, *dsc = dsl + co, *gk = gout + so;
@@ -409,10 +406,9 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
   const int PN = P * N;
   const int k = id.c / pr.cps;
-  const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L;
-  const float dc = decay_seg_to_chunk(pr, acs_bh, id.bb, id.c);
-  const float de = decay_chunk_to_seg_end(pr, acs_bh, id.bb, id.c);
-  const float ac = chunk_decay(pr, acs_bh, id.bb, id.c);
+  const float dc = decay_seg_to_chunk(pr, id.bb, id.h, id.c);
+  const float de = decay_chunk_to_seg_end(pr, id.bb, id.h, id.c);
+  const float ac = chunk_decay(pr, id.bb, id.h, id.c);
   const size_t so = (((size_t)id.bb * pr.S + k) * pr.H + id.h) * PN;
   const size_t co = (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * PN;
   // a_c <dS_end, S_in>

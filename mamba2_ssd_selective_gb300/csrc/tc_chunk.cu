@@ -152,9 +152,8 @@ void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const f
 using EngOut = tc::Engine<64, 2>;
 __global__ void __launch_bounds__(tc::kThreads, 3) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
                                                      const float *__restrict__ dtv, const float *__restrict__ acs,
-                                                     const float *__restrict__ cb, const float *__restrict__ sst,
-                                                     const float *__restrict__ segin, bf16 *__restrict__ y,
-                                                     int *status) {
+                                                     const float *__restrict__ cb, const bf16 *__restrict__ sin16,
+                                                     bf16 *__restrict__ y, int *status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ ChunkVecs v;
   Carve<EngOut> sm(smem_raw);
@@ -167,10 +166,7 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_out_kernel(Problem pr, con
   const int offX = h * P, offC = HP + pr.G * N + id.g * N;
   const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
   const int k = c / pr.cps;
-  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-  const float dc = decay_seg_to_chunk(pr, acs_bh, bb, c);
-  const float *sloc = sst + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
-  const float *sseg = segin + (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
+  const bf16 *sin = sin16 + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;  // true S_in, bf16
   EngOut eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
@@ -194,19 +190,9 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_out_kernel(Problem pr, con
   const bool has_off = c > 0;
   if (has_off) {
     auto fa2 = [&](int m, int k0) { return static_cast<const void *>(ub + (size_t)(128 * I + m) * Cd + offC + k0); };
-    auto fb2l = [&](int p, int k0) {
-      return tc::F16{tc::ldf8(sloc + (size_t)p * N + k0), tc::ldf8(sseg + (size_t)p * N + k0)};
-    };
-    auto fb2 = [&](const tc::F16 &raw, int, int) {
-      float a[8], b[8];
-      tc::f8_to(raw.x, a);
-      tc::f8_to(raw.y, b);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) a[q] += dc * b[q];
-      return tc::pack8(a);
-    };
+    auto fb2 = [&](int p, int k0) { return static_cast<const void *>(sin + (size_t)p * N + k0); };
     for (int k0 = 0; k0 < N; k0 += 64)
-      eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::Async{}, fb2l, fb2, k0 > 0);
+      eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::Async{}, fb2, tc::Async{}, k0 > 0);
   }
   eng.finish();
   if (tc::owns_row()) {
@@ -235,11 +221,11 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_out_kernel(Problem pr, con
 }
 
 void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, const float *cb,
-                   const float *sst, const float *segin, bf16 *y, int *status, cudaStream_t s) {
+                   const bf16 *sin16, bf16 *y, int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_out_kernel, dyn_smem<EngOut>()), true);
   (void)once;
-  tc_out_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngOut>(), s>>>(pr, u, dtv, acs, cb, sst,
-                                                                                       segin, y, status);
+  tc_out_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngOut>(), s>>>(pr, u, dtv, acs, cb, sin16,
+                                                                                       y, status);
 }
 
 // ---------------------------------------------------------------- backward: Z
@@ -396,8 +382,8 @@ using EngDx = tc::Engine<64, 2>;
 __global__ void __launch_bounds__(tc::kThreads, 3) tc_dx_kernel(Problem pr, const bf16 *__restrict__ u,
                                                     const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                     const float *__restrict__ acs, const float *__restrict__ cb,
-                                                    const float *__restrict__ dsl, const float *__restrict__ gout,
-                                                    float *__restrict__ du, float *__restrict__ tok, int *status) {
+                                                    const bf16 *__restrict__ dse16, float *__restrict__ du,
+                                                    float *__restrict__ tok, int *status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ ChunkVecs v;
   Carve<EngDx> sm(smem_raw);
@@ -411,10 +397,7 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_dx_kernel(Problem pr, cons
   const int offB = HP + id.g * N;
   const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
   const int k = c / pr.cps;
-  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-  const float de = decay_chunk_to_seg_end(pr, acs_bh, bb, c);
-  const float *dsc = dsl + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
-  const float *gk = gout + (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
+  const bf16 *dse = dse16 + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;  // true dS at the chunk end, bf16
   EngDx eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
@@ -436,19 +419,9 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_dx_kernel(Problem pr, cons
   for (int k0 = 128 * I; k0 < Q; k0 += 64)
     eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::Async{}, k0 > 128 * I);
   auto fa2l = [&](int m, int k0) { return static_cast<const void *>(ub + (size_t)(128 * I + m) * Cd + offB + k0); };
-  auto fb2l = [&](int p, int k0) {
-    return tc::F16{tc::ldf8(dsc + (size_t)p * N + k0), tc::ldf8(gk + (size_t)p * N + k0)};
-  };
-  auto fb2 = [&](const tc::F16 &raw, int, int) {
-    float a[8], b[8];
-    tc::f8_to(raw.x, a);
-    tc::f8_to(raw.y, b);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) a[q] += de * b[q];
-    return tc::pack8(a);
-  };
+  auto fb2 = [&](int p, int k0) { return static_cast<const void *>(dse + (size_t)p * N + k0); };
   for (int k0 = 0; k0 < N; k0 += 64)
-    eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2l, tc::Async{}, fb2l, fb2, k0 > 0);
+    eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2l, tc::Async{}, fb2, tc::Async{}, k0 > 0);
   eng.finish();
   if (tc::owns_row()) {
   const int j = 128 * I + threadIdx.x;
@@ -479,12 +452,11 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_dx_kernel(Problem pr, cons
 }
 
 void launch_tc_dx(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
-                  const float *cb, const float *dsl, const float *gout, float *du, float *tok, int *status,
-                  cudaStream_t s) {
+                  const float *cb, const bf16 *dse16, float *du, float *tok, int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_dx_kernel, dyn_smem<EngDx>()), true);
   (void)once;
-  tc_dx_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngDx>(), s>>>(pr, u, dy, dtv, acs, cb, dsl,
-                                                                                     gout, du, tok, status);
+  tc_dx_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngDx>(), s>>>(pr, u, dy, dtv, acs, cb, dse16,
+                                                                                     du, tok, status);
 }
 
 // ---------------------------------------------------------------- backward: dC, dB
@@ -499,8 +471,7 @@ using EngDcdb = tc::Engine<128, 2>;
 __global__ void __launch_bounds__(tc::kThreads) tc_dcdb_kernel(Problem pr, const bf16 *__restrict__ u,
                                                       const bf16 *__restrict__ dy, const float *__restrict__ dtv,
                                                       const float *__restrict__ acs, const bf16 *__restrict__ wbuf,
-                                                      const float *__restrict__ sst, const float *__restrict__ segin,
-                                                      const float *__restrict__ dsl, const float *__restrict__ gout,
+                                                      const bf16 *__restrict__ sin16, const bf16 *__restrict__ dse16,
                                                       float *__restrict__ dcp, float *__restrict__ dbp,
                                                       float *__restrict__ tok, int hs_size, int *status) {
   extern __shared__ uint8_t smem_raw[];
@@ -522,14 +493,6 @@ __global__ void __launch_bounds__(tc::kThreads) tc_dcdb_kernel(Problem pr, const
   const int r = 128 * I + (threadIdx.x & (tc::kRows - 1));  // this thread's row (i for dC, j for dB)
   const bool has_off = c > 0;
   bool firstC = true, firstB = true;
-  auto combine = [](const tc::F16 &raw, float s) {
-    float a[8], b[8];
-    tc::f8_to(raw.x, a);
-    tc::f8_to(raw.y, b);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) a[q] += s * b[q];
-    return tc::pack8(a);
-  };
   auto scaled = [](uint4 raw, float s) {
     float x[8];
     tc::unpack8(raw, x);
@@ -544,22 +507,16 @@ __global__ void __launch_bounds__(tc::kThreads) tc_dcdb_kernel(Problem pr, const
     load_chunk_vecs(pr, id, dtv, acs, v);
     const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
     const bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
-    const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-    const float dc = decay_seg_to_chunk(pr, acs_bh, bb, c);
-    const float de = decay_chunk_to_seg_end(pr, acs_bh, bb, c);
     const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * P * N;
     const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;
-    const float *sloc = sst + co, *sseg = segin + so, *dsc = dsl + co, *gk = gout + so;
+    const bf16 *sin = sin16 + co, *dse = dse16 + co;
     // ---- dC
     if (has_off) {
       auto fal = [&](int mm, int p0) { return tc::ldg16(dyb + (size_t)(128 * I + mm) * HP + p0); };
       auto fam = [&](uint4 raw, int mm, int) { return scaled(raw, v.em[128 * I + mm]); };
-      auto fbl = [&](int n0, int p) {
-        return tc::F16{tc::ldf8(sloc + (size_t)p * N + n0), tc::ldf8(sseg + (size_t)p * N + n0)};
-      };
-      auto fbm = [&](const tc::F16 &raw, int, int) { return combine(raw, dc); };
+      auto fb = [&](int n0, int p) { return static_cast<const void *>(sin + (size_t)p * N + n0); };
       for (int k0 = 0; k0 < P; k0 += 64)
-        eng.slice<K_MAJOR, MN_MAJOR>(accR, k0, fal, fam, fbl, fbm, k0 > 0, accC, !firstC || k0 > 0);
+        eng.slice<K_MAJOR, MN_MAJOR>(accR, k0, fal, fam, fb, tc::Async{}, k0 > 0, accC, !firstC || k0 > 0);
       firstC = false;
     }
     {
@@ -573,12 +530,9 @@ __global__ void __launch_bounds__(tc::kThreads) tc_dcdb_kernel(Problem pr, const
     {
       auto fal = [&](int mm, int p0) { return tc::ldg16(ub + (size_t)(128 * I + mm) * Cd + h * P + p0); };
       auto fam = [&](uint4 raw, int mm, int) { return scaled(raw, v.wdt[128 * I + mm]); };
-      auto fbl = [&](int n0, int p) {
-        return tc::F16{tc::ldf8(dsc + (size_t)p * N + n0), tc::ldf8(gk + (size_t)p * N + n0)};
-      };
-      auto fbm = [&](const tc::F16 &raw, int, int) { return combine(raw, de); };
+      auto fb = [&](int n0, int p) { return static_cast<const void *>(dse + (size_t)p * N + n0); };
       for (int k0 = 0; k0 < P; k0 += 64)
-        eng.slice<K_MAJOR, MN_MAJOR>(accB, k0, fal, fam, fbl, fbm, !firstB || k0 > 0);
+        eng.slice<K_MAJOR, MN_MAJOR>(accB, k0, fal, fam, fb, tc::Async{}, !firstB || k0 > 0);
       firstB = false;
     }
     {
@@ -627,13 +581,13 @@ int tc_head_subset(const Problem &pr) {
 }
 
 void launch_tc_dcdb(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
-                    const bf16 *wbuf, const float *sst, const float *segin, const float *dsl, const float *gout,
-                    float *dcp, float *dbp, float *tok, int *status, cudaStream_t s) {
+                    const bf16 *wbuf, const bf16 *sin16, const bf16 *dse16, float *dcp, float *dbp, float *tok,
+                    int *status, cudaStream_t s) {
   static bool once = (set_smem(tc_dcdb_kernel, dyn_smem<EngDcdb>()), true);
   (void)once;
   const int hs = tc_head_subset(pr);
   tc_dcdb_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H / hs, pr.b), tc::kThreads, dyn_smem<EngDcdb>(), s>>>(
-      pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, hs, status);
+      pr, u, dy, dtv, acs, wbuf, sin16, dse16, dcp, dbp, tok, hs, status);
 }
 
 }  // namespace ssd
