@@ -49,6 +49,23 @@ __device__ __forceinline__ void store_row_f32(float *dst, const float (&v)[32]) 
     reinterpret_cast<float4 *>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
+// Column sums over a warp: lane l holds row l's 32 values v[0..31]; after the
+// halving butterfly (offsets 16, 8, 4, 2, 1; 31 shuffles) lane l holds the sum
+// of column l over the warp's 32 rows.  Fixed order, so bit-reproducible.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int q = 0; q < o; ++q) {
+      const float send = upper ? v[q] : v[q + o];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[q] = (upper ? v[q + o] : v[q]) + recv;
+    }
+  }
+  return v[0];
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- CB = C B^T
@@ -293,9 +310,6 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_w_kernel(Problem pr, const
                                                    bf16 *__restrict__ wbuf, float *__restrict__ tok, int *status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ ChunkVecs v;
-  __shared__ float red[128][33];
-  __shared__ float part[4][32];
-  __shared__ float colacc[256];
   Carve<EngW> sm(smem_raw);
   const int NTI = pr.Q / 128;
   const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
@@ -306,7 +320,6 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_w_kernel(Problem pr, const
   const bf16 *dyb = dy + ((size_t)bb * pr.L + id.t0) * HP + h * P;
   const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
   bf16 *wm = wbuf + (((size_t)bb * pr.nc + c) * pr.H + h) * Q * Q;
-  for (int j = threadIdx.x; j < 256; j += tc::kThreads) colacc[j] = 0.f;
   EngW eng;
   eng.init(sm.ring, sm.bars, status);
   const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 256);
@@ -318,15 +331,21 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_w_kernel(Problem pr, const
   }
   eng.finish();
   const bool ep = tc::owns_row();
-  const int m = threadIdx.x & (tc::kRows - 1), i = 128 * I + m;
+  const int m = threadIdx.x & (tc::kRows - 1), i = 128 * I + m, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float ai = v.acs[i];
   const int si = v.seq[i];
   float rowsum = 0.f;
-  for (int J = 0; J <= I; ++J)
-    for (int cc = 0; cc < 4; ++cc) {
-      const int j0 = 128 * J + 32 * cc;
-      if (ep) {
-        float a[32];
+  float colpart[8];  // this warp's column sums of V, column (32 * slot + lane)
+#pragma unroll
+  for (int q = 0; q < 8; ++q) colpart[q] = 0.f;
+  if (ep) {
+#pragma unroll
+    for (int J = 0; J < 2; ++J) {
+      if (J > I) break;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int j0 = 128 * J + 32 * cc;
+        float a[32], vv[32];
         sm100::tmem_ld32(tc::tmem_lane_addr(tmem, j0), a);
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
@@ -336,31 +355,28 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_w_kernel(Problem pr, const
           for (int q = 0; q < 8; ++q) {
             const int j = j0 + 8 * q8 + q;
             const float dml = (j <= i && v.seq[j] == si) ? a[8 * q8 + q] * expf(ai - v.acs[j]) : 0.f;
-            const float vv = dml * cv[q];
+            vv[8 * q8 + q] = dml * cv[q];
             wv[q] = dml * v.dt[j];
-            rowsum += vv * v.dt[j];
-            red[m][8 * q8 + q] = vv;
+            rowsum += vv[8 * q8 + q] * v.dt[j];
           }
           *reinterpret_cast<uint4 *>(wm + (size_t)i * Q + j0 + 8 * q8) = tc::pack8(wv);
         }
+        colpart[4 * J + cc] = warp_colsum32(vv, lane);
       }
-      // column sums of V over this tile's 128 rows, fixed order
-      __syncthreads();
-      if (ep) {
-        const int q = m & 31, quarter = m >> 5;
-        float s2 = 0.f;
-        for (int rr = 0; rr < 32; ++rr) s2 += red[quarter * 32 + rr][q];
-        part[quarter][q] = s2;
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) colacc[j0 + m] += (part[0][m] + part[1][m]) + (part[2][m] + part[3][m]);
-      __syncthreads();
     }
+  }
+  __shared__ float wpart[4][256];
+  if (ep) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) wpart[warp][32 * q + lane] = colpart[q];
+  }
+  __syncthreads();
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
   const size_t tb = ((size_t)bb * pr.H + h) * pr.L + id.t0;
   if (ep) tok[tb + i] = rowsum;
   float *vcol = tok + (I == 0 ? 2 : 5) * BHL + tb;
-  for (int j = threadIdx.x; j < Q; j += tc::kThreads) vcol[j] = colacc[j];
+  for (int j = threadIdx.x; j < Q; j += tc::kThreads)
+    vcol[j] = (j < 128 * (I + 1)) ? (wpart[0][j] + wpart[1][j]) + (wpart[2][j] + wpart[3][j]) : 0.f;
   tc::tmem_free_cta(tmem, 256);
 }
 
