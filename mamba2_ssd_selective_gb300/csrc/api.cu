@@ -116,7 +116,8 @@ struct ProfScope {
   } while (0)
 
 ssd_status launch_status() {
-  return cudaPeekAtLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  const bool host_err = take_host_error();
+  return (cudaPeekAtLastError() == cudaSuccess && !host_err) ? SSD_OK : SSD_ERR_CUDA;
 }
 
 template <typename T>
@@ -157,10 +158,7 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
                                                  const_cast<float *>(pr.dend), s));
   if constexpr (kIsBf16<T>) {
-    if (tc) {
-      SSD_LAUNCH("tc_cb", launch_tc_cb(pr, u, cb, status, s));
-      SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));
-    }
+    if (tc) SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));  // CB: inside tc_out
   }
   if (!tc) {
     SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
@@ -172,7 +170,7 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
     if (tc) {
       __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
       SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, 0, s));
-      SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, cb, sin16, y, status, s));
+      SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, sin16, y, status, s));
     }
   }
   if (!tc) SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, y, s));

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tc_pipe.cuh"
 
 namespace ssd {
 
@@ -65,7 +66,8 @@ inline bool tc_envelope(const Problem &pr) {
 void launch_tc_cb(const Problem &pr, const __nv_bfloat16 *u, float *cb, int *status, cudaStream_t s);
 void launch_tc_state(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, float *sst,
                      int *status, cudaStream_t s);
-void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, const float *cb,
+// persistent output kernel (tc_out.cu)
+void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs,
                    const __nv_bfloat16 *sin16, __nv_bfloat16 *y, int *status, cudaStream_t s);
 void launch_tc_z(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
                  const float *acs, float *dsl, int *status, cudaStream_t s);

@@ -162,89 +162,6 @@ void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const f
   tc_state_kernel<<<dim3(pr.nc, pr.H / 2, pr.b), tc::kThreads, dyn_smem<EngPair>(), s>>>(pr, u, dtv, acs, sst, status);
 }
 
-// ---------------------------------------------------------------- output
-// CTA = (chunk, row tile I, head, batch):
-//   Y_diag = (CB o L o dt) X over j < 128(I+1),  Y_off = C S_in^T,
-//   y = Y_diag + em * Y_off + D x.
-using EngOut = tc::Engine<64, 2>;
-__global__ void __launch_bounds__(tc::kThreads, 3) tc_out_kernel(Problem pr, const bf16 *__restrict__ u,
-                                                     const float *__restrict__ dtv, const float *__restrict__ acs,
-                                                     const float *__restrict__ cb, const bf16 *__restrict__ sin16,
-                                                     bf16 *__restrict__ y, int *status) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ ChunkVecs v;
-  Carve<EngOut> sm(smem_raw);
-  const int NTI = pr.Q / 128;
-  const int c = blockIdx.x / NTI, I = blockIdx.x % NTI, h = blockIdx.y, bb = blockIdx.z;
-  const ChunkIds id = make_ids(pr, c, h, bb);
-  load_chunk_vecs(pr, id, dtv, acs, v);
-  const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
-  const bf16 *ub = u + ((size_t)bb * pr.L + id.t0) * Cd;
-  const int offX = h * P, offC = HP + pr.G * N + id.g * N;
-  const float *cbm = cb + (((size_t)bb * pr.nc + c) * pr.G + id.g) * Q * Q;
-  const int k = c / pr.cps;
-  const bf16 *sin = sin16 + (((size_t)bb * pr.nc + c) * pr.H + h) * P * N;  // true S_in, bf16
-  EngOut eng;
-  eng.init(sm.ring, sm.bars, status);
-  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
-  auto fa1l = [&](int m, int k0) { return tc::ldf8(cbm + (size_t)(128 * I + m) * Q + k0); };
-  auto fa1 = [&](const tc::F8 &raw, int m, int k0) {
-    const int i = 128 * I + m;
-    float cv[8], r[8];
-    tc::f8_to(raw, cv);
-    const float ai = v.acs[i];
-    const int si = v.seq[i];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = k0 + q;
-      r[q] = (j <= i && v.seq[j] == si) ? cv[q] * expf(ai - v.acs[j]) * v.dt[j] : 0.f;
-    }
-    return tc::pack8(r);
-  };
-  auto fb1 = [&](int n0, int j) { return static_cast<const void *>(ub + (size_t)j * Cd + offX + n0); };
-  for (int k0 = 0; k0 < 128 * (I + 1); k0 += 64)
-    eng.slice<K_MAJOR, MN_MAJOR>(tmem, k0, fa1l, fa1, fb1, tc::Async{}, k0 > 0);
-  const bool has_off = c > 0;
-  if (has_off) {
-    auto fa2 = [&](int m, int k0) { return static_cast<const void *>(ub + (size_t)(128 * I + m) * Cd + offC + k0); };
-    auto fb2 = [&](int p, int k0) { return static_cast<const void *>(sin + (size_t)p * N + k0); };
-    for (int k0 = 0; k0 < N; k0 += 64)
-      eng.slice<K_MAJOR, K_MAJOR>(tmem + 64, k0, fa2, tc::Async{}, fb2, tc::Async{}, k0 > 0);
-  }
-  eng.finish();
-  if (tc::owns_row()) {
-  const int i = 128 * I + threadIdx.x;
-  const float em = v.em[i], Dh = pr.D[h];
-  const bf16 *xr = ub + (size_t)i * Cd + offX;
-  bf16 *yr = y + ((size_t)bb * pr.L + id.t0 + i) * HP + offX;
-  for (int cc = 0; cc < 2; ++cc) {
-    float yd[32], yo[32];
-    sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 32 * cc), yd);
-    if (has_off) sm100::tmem_ld32(tc::tmem_lane_addr(tmem, 64 + 32 * cc), yo);
-#pragma unroll
-    for (int q8 = 0; q8 < 4; ++q8) {
-      float x[8], o[8];
-      tc::unpack8(tc::ldg16(xr + 32 * cc + 8 * q8), x);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int col = 8 * q8 + q;
-        o[q] = yd[col] + (has_off ? em * yo[col] : 0.f) + Dh * x[q];
-      }
-      *reinterpret_cast<uint4 *>(yr + 32 * cc + 8 * q8) = tc::pack8(o);
-    }
-  }
-  }
-  tc::tmem_free_cta(tmem, 128);
-}
-
-void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, const float *cb,
-                   const bf16 *sin16, bf16 *y, int *status, cudaStream_t s) {
-  static bool once = (set_smem(tc_out_kernel, dyn_smem<EngOut>()), true);
-  (void)once;
-  tc_out_kernel<<<dim3(pr.nc * (pr.Q / 128), pr.H, pr.b), tc::kThreads, dyn_smem<EngOut>(), s>>>(pr, u, dtv, acs, cb, sin16,
-                                                                                       y, status);
-}
-
 // ---------------------------------------------------------------- backward: Z
 // Z^T[n, (h, p)] = sum_i C_i[n] em_h,i dy_i[h, p]  for a pair of heads.
 __global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const bf16 *__restrict__ u,

@@ -1,0 +1,412 @@
+// Chunk output of the bf16 path (Mamba2 SSD, chunked form: the diagonal block
+// Y_diag = (C B^T o L o dt) X plus the off-diagonal term em o (C S_in^T)), as a
+// persistent, warp-specialised tcgen05 kernel.
+//
+// Work unit = (batch row, chunk, 128-token row tile I, block of HB heads of one
+// group).  Per unit the tensor cores first form CB = C_I B^T (K = dstate) into
+// tensor memory, once for all HB heads; then per head
+//   Yd  = A_h X_h,   A_h[i, j] = CB[i, j] exp(Acs_i - Acs_j) dt_j [j <= i, same sequence]
+//   Yo  = C_I S_in,h^T
+//   y_i = Yd_i + em_i Yo_i + D_h x_i.
+// Roles (22 warps, one CTA per SM):
+//   warp 0      TMA producer: C/B tiles per unit, per head the chunk vectors
+//               (Acs, dt, seq), 64-token X slices and the bf16 S_in tile;
+//   warp 1      TMEM owner and MMA issuer (one thread);
+//   warps 2-17  transform: read CB rows from TMEM, apply mask, decay and dt,
+//               write the bf16 A slice into shared memory (four warps per lane
+//               quadrant, one per 16-column group of the 64-wide slice);
+//   warps 18-21 epilogue: drain the two per-head accumulators and write y.
+// The decay and dt factor is one 2^x per element: per head the transform
+// warps tabulate a_i = Acs_i log2(e) and b_j = log2(dt_j) - Acs_j log2(e), so
+// A_h[i, j] = CB[i, j] 2^(a_i + b_j); the mask is the row's interval
+// [start_i, i], start_i the first token of i's sequence inside the chunk.
+// Accumulators are double-buffered, so the epilogue of head n overlaps the
+// transform and MMAs of head n+1; the A/X slice ring is kNS deep.
+#include "chunk_common.cuh"
+#include "kernels.h"
+#include "tc_engine.cuh"
+#include "tc_pipe.cuh"
+
+namespace ssd {
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+using namespace sm100;
+using pipe::parity;
+
+constexpr int kWarps = 22;
+constexpr int kEpiWarp0 = 18;
+constexpr int kThreads = kWarps * 32;
+constexpr int kNS = 3;  // A/X slice ring depth
+
+// shared memory map, offsets from the 1024-aligned base
+constexpr uint32_t kSmC = 0;                     // C_I: 2 K halves x [128 rows x 128 B]
+constexpr uint32_t kSmB = kSmC + 2 * 16384;      // B rows: 2 K halves x [256 rows x 128 B]
+constexpr uint32_t kSmA = kSmB + 2 * 32768;      // ring of A slices [128 x 64] bf16, K-major
+constexpr uint32_t kSmX = kSmA + kNS * 16384;    // ring of X slices [64 tokens x 64] bf16, MN-major
+constexpr uint32_t kSmS = kSmX + kNS * 8192;     // 2 x S_in,h: 2 K halves x [64 x 128 B]
+constexpr uint32_t kVecStride = 3200;            // acs[256] f32 | dt[256] f32 | seq[4 + 256] i32
+constexpr uint32_t kSmV = kSmS + 2 * 16384;      // 2 vector buffers
+constexpr uint32_t kSmD = kSmV + 2 * kVecStride;   // 2 x {a[256], b[256]} f32 (decay tables per head)
+constexpr uint32_t kSmBar = kSmD + 2 * 2048;
+constexpr int kNumBars = 9 + 3 * kNS + 8;
+constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
+constexpr int kSmemBytes = (int)kSmEnd + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Unit {
+  int bb, c, I, h0;
+};
+
+// Unit u of the launch.  Row tiles with more work (higher I) come first, so a
+// round-robin assignment gives every CTA the same mix; inside a class the head
+// blocks of one (row, chunk) are adjacent and share C/B in L2.
+__device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int HB, int u) {
+  const int per = pr.b * pr.nc * nhb;
+  const int cls = u / per, r = u % per;
+  Unit o;
+  o.I = NTI - 1 - cls;
+  const int hb = r % nhb, bc = r / nhb;
+  o.c = bc % pr.nc;
+  o.bb = bc / pr.nc;
+  o.h0 = hb * HB;
+  return o;
+}
+
+struct Bars {
+  uint64_t *unit_full, *b_free, *c_free, *cb_full, *cb_used;
+  uint64_t *vec_full, *vec_free;             // [2]
+  uint64_t *a_full, *x_full, *slot_free;     // [kNS]
+  uint64_t *s_full, *s_free;                 // [2]
+  uint64_t *acc_full, *acc_free;             // [2]
+  __device__ Bars(uint64_t *b) {
+    unit_full = b;
+    b_free = b + 1;
+    c_free = b + 2;
+    cb_full = b + 3;
+    cb_used = b + 4;
+    vec_full = b + 5;
+    vec_free = b + 7;
+    a_full = b + 9;
+    x_full = a_full + kNS;
+    slot_free = x_full + kNS;
+    s_full = slot_free + kNS;
+    s_free = s_full + 2;
+    acc_full = s_free + 2;
+    acc_free = acc_full + 2;
+  }
+};
+
+constexpr int kTransformThreads = 16 * 32;
+constexpr int kEpilogueThreads = 4 * 32;
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_out_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_s, Problem pr,
+                  const bf16 *__restrict__ u, const float *__restrict__ dtv, const float *__restrict__ acs,
+                  bf16 *__restrict__ y, int HB, int nunits, int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = tc::aligned_smem(smem_raw);
+  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar));
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NTI = pr.Q / 128, nhb = pr.H / HB, HP = pr.H * pr.P, Cd = pr.Cd;
+  const bool has_seq = pr.seq_idx != nullptr;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar.unit_full, 1);
+    mbar_init(bar.b_free, 1);
+    mbar_init(bar.c_free, 1);
+    mbar_init(bar.cb_full, 1);
+    mbar_init(bar.cb_used, kTransformThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.vec_full[i], 1);
+      mbar_init(&bar.vec_free[i], kTransformThreads + kEpilogueThreads);
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_free[i], 1);
+      mbar_init(&bar.acc_full[i], 1);
+      mbar_init(&bar.acc_free[i], kEpilogueThreads);
+    }
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(&bar.a_full[i], kTransformThreads);
+      mbar_init(&bar.x_full[i], 1);
+      mbar_init(&bar.slot_free[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;  // cols [0, 256): CB;  [256 + 128 b, +64): Yd[b];  [+64, +128): Yo[b]
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_u);
+      prefetch_tmap(&tm_s);
+      uint32_t nu = 0, nh = 0, ns = 0, k = 0;
+      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+        const Unit o = unit_of(pr, NTI, nhb, HB, ui);
+        const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, NB = 128 * (o.I + 1);
+        const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N;
+        if (nu > 0) {
+          mbar_wait(bar.b_free, parity(nu - 1), status);
+          mbar_wait(bar.c_free, parity(nu - 1), status);
+        }
+        mbar_expect_tx(bar.unit_full, 2 * 16384 + 2 * NB * 128);
+        for (int kh = 0; kh < 2; ++kh) {
+          for (int r = 0; r < 2; ++r)
+            tma_load_2d(sm + kSmC + kh * 16384 + r * 8192, &tm_u, bar.unit_full, offC + 64 * kh, row0 + 128 * o.I + 64 * r);
+          for (int r = 0; r < NB / 64; ++r)
+            tma_load_2d(sm + kSmB + kh * 32768 + r * 8192, &tm_u, bar.unit_full, offB + 64 * kh, row0 + 64 * r);
+        }
+        for (int hh = 0; hh < HB; ++hh, ++nh) {
+          const int h = o.h0 + hh, vb = nh & 1;
+          if (nh >= 2) mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status);
+          uint8_t *vec = sm + kSmV + vb * kVecStride;
+          const size_t bh = ((size_t)o.bb * pr.H + h) * pr.L + t0;
+          const uint32_t seq_bytes = !has_seq ? 0u : (uint32_t)(o.c > 0 ? (pr.Q + 4) * 4 : pr.Q * 4);
+          mbar_expect_tx(&bar.vec_full[vb], 2 * pr.Q * 4 + seq_bytes);
+          pipe::bulk_load(vec, acs + bh, pr.Q * 4, &bar.vec_full[vb]);
+          pipe::bulk_load(vec + 1024, dtv + bh, pr.Q * 4, &bar.vec_full[vb]);
+          if (has_seq) {
+            if (o.c > 0)
+              pipe::bulk_load(vec + 2048, pr.seq_idx + (size_t)o.bb * pr.L + t0 - 4, seq_bytes, &bar.vec_full[vb]);
+            else
+              pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
+          }
+          for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
+            const int slot = k % kNS;
+            if (k >= kNS) mbar_wait(&bar.slot_free[slot], parity(k / kNS - 1), status);
+            mbar_expect_tx(&bar.x_full[slot], 8192);
+            tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
+          }
+          if (o.c > 0) {
+            const int sb = ns & 1;
+            if (ns >= 2) mbar_wait(&bar.s_free[sb], parity(ns / 2 - 1), status);
+            mbar_expect_tx(&bar.s_full[sb], 16384);
+            const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
+            tma_load_2d(sm + kSmS + sb * 16384, &tm_s, &bar.s_full[sb], 0, srow);
+            tma_load_2d(sm + kSmS + sb * 16384 + 8192, &tm_s, &bar.s_full[sb], 64, srow);
+            ++ns;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sC = smem_u32(sm + kSmC), sB = smem_u32(sm + kSmB), sA = smem_u32(sm + kSmA),
+                     sX = smem_u32(sm + kSmX), sS = smem_u32(sm + kSmS);
+      constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);
+      constexpr uint32_t id_off = idesc_bf16(128, 64, false, false);
+      uint32_t nu = 0, nh = 0, ns = 0, k = 0;
+      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+        const Unit o = unit_of(pr, NTI, nhb, HB, ui);
+        const int NB = 128 * (o.I + 1);
+        mbar_wait(bar.unit_full, parity(nu), status);
+        if (nu > 0) mbar_wait(bar.cb_used, parity(nu - 1), status);
+        tc_fence_after();
+        const uint32_t id_cb = idesc_bf16(128, NB, false, false);
+        for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem, desc_sw128(sC + kh * 16384 + kk * 32, 16, 1024),
+                      desc_sw128(sB + kh * 32768 + kk * 32, 16, 1024), id_cb, (kh | kk) ? 1u : 0u);
+        umma_commit(bar.cb_full);
+        umma_commit(bar.b_free);
+        for (int hh = 0; hh < HB; ++hh, ++nh) {
+          const int ab = nh & 1;
+          const uint32_t tacc = tmem + 256 + 128 * ab;
+          if (nh >= 2) mbar_wait(&bar.acc_free[ab], parity(nh / 2 - 1), status);
+          tc_fence_after();
+          for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
+            const int slot = k % kNS;
+            mbar_wait(&bar.a_full[slot], parity(k / kNS), status);
+            mbar_wait(&bar.x_full[slot], parity(k / kNS), status);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tacc, desc_sw128(sA + slot * 16384 + kk * 32, 16, 1024),
+                        desc_sw128(sX + slot * 8192 + kk * 2048, 8192, 1024), id_acc, (s | kk) ? 1u : 0u);
+            umma_commit(&bar.slot_free[slot]);
+          }
+          if (o.c > 0) {
+            const int sb = ns & 1;
+            mbar_wait(&bar.s_full[sb], parity(ns / 2), status);
+            tc_fence_after();
+            for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tacc + 64, desc_sw128(sC + kh * 16384 + kk * 32, 16, 1024),
+                          desc_sw128(sS + sb * 16384 + kh * 8192 + kk * 32, 16, 1024), id_off, (kh | kk) ? 1u : 0u);
+            umma_commit(&bar.s_free[sb]);
+            ++ns;
+          }
+          umma_commit(&bar.acc_full[ab]);
+        }
+        umma_commit(bar.c_free);
+      }
+      // drain: the arrivals of commits no other role waits for must land
+      // before the CTA's shared memory is released
+      if (nu > 0) {
+        mbar_wait(bar.b_free, parity(nu - 1), status);
+        mbar_wait(bar.c_free, parity(nu - 1), status);
+      }
+      for (uint32_t m = k > (uint32_t)kNS ? k - kNS : 0u; m < k; ++m)
+        mbar_wait(&bar.slot_free[m % kNS], parity(m / kNS), status);
+      for (uint32_t m = ns > 2u ? ns - 2u : 0u; m < ns; ++m) mbar_wait(&bar.s_free[m & 1], parity(m / 2), status);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ transform
+    const int q = warp & 3, cg = (warp - 2) >> 2, il = 32 * q + lane, tt = threadIdx.x - 64;
+    const uint32_t sA = smem_u32(sm + kSmA), sV = smem_u32(sm + kSmV), sD = smem_u32(sm + kSmD);
+    const float kLog2e = 1.4426950408889634f;
+    uint32_t nu = 0, nh = 0, k = 0;
+    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      const Unit o = unit_of(pr, NTI, nhb, HB, ui);
+      const int i = 128 * o.I + il, row_lo = 128 * o.I + 32 * q, row_hi = row_lo + 31;
+      int start_i = 0;
+      mbar_wait(bar.cb_full, parity(nu), status);
+      tc_fence_after();
+      for (int hh = 0; hh < HB; ++hh, ++nh) {
+        const int vb = nh & 1;
+        mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
+        const uint32_t vacs = sV + vb * kVecStride, vdt = vacs + 1024, vseq = vacs + 2048 + 16;
+        const uint32_t da = sD + vb * 2048, db = da + 1024;
+        if (hh == 0 && has_seq) {  // first token of row i's sequence inside the chunk
+          const int si = pipe::lds_i(vseq + 4 * i);
+          start_i = i;
+          while (start_i > 0 && pipe::lds_i(vseq + 4 * (start_i - 1)) == si) --start_i;
+        }
+        if (tt < pr.Q) {
+          const float a = pipe::lds_f(vacs + 4 * tt) * kLog2e;
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(da + 4 * tt), "f"(a) : "memory");
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(db + 4 * tt), "f"(__log2f(pipe::lds_f(vdt + 4 * tt)) - a)
+                       : "memory");
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kTransformThreads) : "memory");
+        const float ai = pipe::lds_f(da + 4 * i);
+        for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
+          const int slot = k % kNS;
+          if (k >= kNS) mbar_wait(&bar.slot_free[slot], parity(k / kNS - 1), status);
+          const int j0 = 64 * s + 16 * cg;
+          uint4 pk[2];
+          if (j0 > row_hi) {
+            pk[0] = pk[1] = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            float v[16], r[16];
+            tmem_ld16(pipe::tmem_quad(tmem, j0), v);
+            const bool full = __all_sync(0xffffffffu, start_i <= j0 && j0 + 15 <= i);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+              const float4 b4 = pipe::lds_f4(db + 4 * (j0 + e));
+              const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+              if (full) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) r[e + m] = v[e + m] * ex2_approx(ai + bv[m]);
+              } else {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  const int j = j0 + e + m;
+                  r[e + m] = (unsigned)(j - start_i) <= (unsigned)(i - start_i) ? v[e + m] * ex2_approx(ai + bv[m]) : 0.f;
+                }
+              }
+            }
+            float r0[8], r1[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              r0[m] = r[m];
+              r1[m] = r[8 + m];
+            }
+            pk[0] = tc::pack8(r0);
+            pk[1] = tc::pack8(r1);
+          }
+          const uint32_t A = sA + slot * 16384;
+          pipe::sts_u4(A + sw128_offset(il, 16 * cg), pk[0]);
+          pipe::sts_u4(A + sw128_offset(il, 16 * cg + 8), pk[1]);
+          fence_async_smem();
+          mbar_arrive(&bar.a_full[slot]);
+        }
+        mbar_arrive(&bar.vec_free[vb]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar.cb_used);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3, il = 32 * q + lane;
+    const uint32_t sV = smem_u32(sm + kSmV);
+    uint32_t nh = 0;
+    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x) {
+      const Unit o = unit_of(pr, NTI, nhb, HB, ui);
+      const int i = 128 * o.I + il, t = o.c * pr.Q + i;
+      const bool has_off = o.c > 0;
+      const bf16 *xrow = u + ((size_t)o.bb * pr.L + t) * Cd;
+      bf16 *yrow = y + ((size_t)o.bb * pr.L + t) * HP;
+      for (int hh = 0; hh < HB; ++hh, ++nh) {
+        const int h = o.h0 + hh, vb = nh & 1, ab = nh & 1;
+        mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
+        const uint32_t vacs = sV + vb * kVecStride, vseq = vacs + 2048 + 16;
+        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(vseq - 4);
+        const float em = (has_off && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
+        mbar_arrive(&bar.vec_free[vb]);
+        const float Dh = __ldg(pr.D + h);
+        mbar_wait(&bar.acc_full[ab], parity(nh / 2), status);
+        tc_fence_after();
+        const uint32_t tacc = tmem + 256 + 128 * ab;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float yd[16], yo[16];
+          tmem_ld16(pipe::tmem_quad(tacc, 16 * cc), yd);
+          if (has_off) tmem_ld16(pipe::tmem_quad(tacc + 64, 16 * cc), yo);
+#pragma unroll
+          for (int q8 = 0; q8 < 2; ++q8) {
+            float x[8], o8[8];
+            tc::unpack8(tc::ldg16(xrow + h * pr.P + 16 * cc + 8 * q8), x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int col = 8 * q8 + e;
+              o8[e] = yd[col] + (has_off ? em * yo[col] : 0.f) + Dh * x[e];
+            }
+            *reinterpret_cast<uint4 *>(yrow + h * pr.P + 16 * cc + 8 * q8) = tc::pack8(o8);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.acc_free[ab]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, const bf16 *sin16, bf16 *y,
+                   int *status, cudaStream_t s) {
+  static bool once = (cudaFuncSetAttribute(tc_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
+                      true);
+  (void)once;
+  CUtensorMap tm_u, tm_s;
+  if (!encode_tmap_bf16_2d(&tm_u, u, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 2, 64, 64) ||
+      !encode_tmap_bf16_2d(&tm_s, sin16, pr.N, (uint64_t)pr.b * pr.nc * pr.H * pr.P, (uint64_t)pr.N * 2, 64, 64)) {
+    note_host_error();
+    return;
+  }
+  const int HB = tc_head_subset(pr);
+  const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
+  const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
+  tc_out_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_s, pr, u, dtv, acs, y, HB, nunits, status);
+}
+
+}  // namespace ssd

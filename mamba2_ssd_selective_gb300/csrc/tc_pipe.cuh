@@ -1,0 +1,77 @@
+// Pieces shared by the persistent, warp-specialised tensor-core kernels: 1-D
+// bulk copies, phase bookkeeping for mbarrier rings, and the host-side TMA
+// tensor-map encoder (fetched from the driver at run time, no libcuda link).
+//
+// Ring discipline used by every such kernel: the m-th completion of a barrier
+// has phase parity m & 1; a waiter on the m-th completion passes
+// mbar_wait(bar, m & 1).  Every barrier's (m+1)-th completion depends on an
+// arrival from each of its waiters' m-th use, so no barrier ever runs two
+// phases ahead of a waiter (which parity waits could not tell apart).
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "sm100.cuh"
+
+namespace ssd {
+namespace pipe {
+
+using namespace sm100;
+
+// 1-D bulk copy global -> this CTA's shared memory; completion counted in bytes
+// on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t parity(uint32_t m) { return m & 1u; }
+
+// explicit shared-memory accesses (32-bit shared addresses)
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int4 lds_i4(uint32_t a) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int lds_i(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_u4(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// TMEM address of (lane quadrant of this warp, column col)
+__device__ __forceinline__ uint32_t tmem_quad(uint32_t base, int col) {
+  return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
+}
+
+}  // namespace pipe
+
+// Host: 2-D bf16 tensor map over a row-major matrix (cols contiguous), box
+// box_cols x box_rows, 128-byte swizzle (box_cols * 2 must be 128).  Returns
+// false if the driver entry point is missing or the encoder rejects the map.
+bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                         uint32_t box_cols, uint32_t box_rows);
+// Host: SM count of the current device (cached per device).
+int device_sm_count();
+// Host: record an error found while preparing a launch; the pass then returns
+// SSD_ERR_CUDA (cleared when read).
+void note_host_error();
+bool take_host_error();
+
+}  // namespace ssd
