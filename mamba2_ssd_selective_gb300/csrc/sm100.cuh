@@ -34,18 +34,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase.  After kWaitPolls polls (well over a
-// second) it gives up, raises the device status word and returns false; the
-// caller carries on without the data (results are then garbage but the kernel
-// terminates, frees its tensor memory and the host sees SSD_ERR_DEVICE_TIMEOUT).
-// A waiter that finds the status word already raised (another wait gave up)
-// returns at once, so a broken pipeline drains in microseconds per wait.
-constexpr uint32_t kWaitPolls = 1u << 23;
+// try_wait with a suspend-time hint: the waiting thread is parked (not
+// spinning) until the phase completes or about hint_ns elapse.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.b32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  After kWaitTimeoutNs (well over a
+// second of wall time) it gives up, raises the device status word and returns
+// false; the caller carries on without the data (results are then garbage but
+// the kernel terminates, frees its tensor memory and the host sees
+// SSD_ERR_DEVICE_TIMEOUT).  A waiter that finds the status word already raised
+// (another wait gave up) returns at once, so a broken pipeline drains quickly.
+// Waiting threads are parked by the hardware between polls.
+constexpr uint64_t kWaitTimeoutNs = 1500ull * 1000ull * 1000ull;
+constexpr uint32_t kWaitHintNs = 20000u;
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 2047u) == 2047u && status && *reinterpret_cast<volatile int *>(status) != 0) return false;
-    if (i >= 64) __nanosleep(128);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_hint(bar, parity, kWaitHintNs)) return true;
+    if ((i & 7u) == 7u) {
+      if (status && *reinterpret_cast<volatile int *>(status) != 0) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+    }
   }
   if (status) atomicExch(status, 1);
   return false;

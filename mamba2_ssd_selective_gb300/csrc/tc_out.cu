@@ -16,9 +16,13 @@
 //               write the bf16 A slice into shared memory (four warps per lane
 //               quadrant, one per 16-column group of the 64-wide slice);
 //   warps 18-21 epilogue: drain the two per-head accumulators and write y.
-// The decay and dt factor is one 2^x per element: per head the transform
-// warps tabulate a_i = Acs_i log2(e) and b_j = log2(dt_j) - Acs_j log2(e), so
-// A_h[i, j] = CB[i, j] 2^(a_i + b_j); the mask is the row's interval
+// Decays without an exponential per element: Acs does not increase along the
+// chunk, so for a 16-column group ending at column m and rows i >= m
+//   exp(Acs_i - Acs_j) dt_j = exp(Acs_i - Acs_m) * [exp(Acs_m - Acs_j) dt_j],
+// both factors <= 1 (dt_j aside): the bracket is tabulated per head and
+// column, the first factor costs one 2^x per row and group.  Groups that
+// straddle the diagonal use 2^(a_i + b_j) per element, a_i = Acs_i log2(e),
+// b_j = log2(dt_j) - Acs_j log2(e).  The mask is the row's interval
 // [start_i, i], start_i the first token of i's sequence inside the chunk.
 // Accumulators are double-buffered, so the epilogue of head n overlaps the
 // transform and MMAs of head n+1; the A/X slice ring is kNS deep.
@@ -38,18 +42,19 @@ using pipe::parity;
 constexpr int kWarps = 22;
 constexpr int kEpiWarp0 = 18;
 constexpr int kThreads = kWarps * 32;
-constexpr int kNS = 3;  // A/X slice ring depth
+constexpr int kNS = 4;   // A/X slice ring depth
+constexpr int kNSB = 1;  // S_in buffers (a head of slack between load and use)
 
 // shared memory map, offsets from the 1024-aligned base
 constexpr uint32_t kSmC = 0;                     // C_I: 2 K halves x [128 rows x 128 B]
 constexpr uint32_t kSmB = kSmC + 2 * 16384;      // B rows: 2 K halves x [256 rows x 128 B]
 constexpr uint32_t kSmA = kSmB + 2 * 32768;      // ring of A slices [128 x 64] bf16, K-major
 constexpr uint32_t kSmX = kSmA + kNS * 16384;    // ring of X slices [64 tokens x 64] bf16, MN-major
-constexpr uint32_t kSmS = kSmX + kNS * 8192;     // 2 x S_in,h: 2 K halves x [64 x 128 B]
+constexpr uint32_t kSmS = kSmX + kNS * 8192;     // kNSB x S_in,h: 2 K halves x [64 x 128 B]
 constexpr uint32_t kVecStride = 3200;            // acs[256] f32 | dt[256] f32 | seq[4 + 256] i32
-constexpr uint32_t kSmV = kSmS + 2 * 16384;      // 2 vector buffers
-constexpr uint32_t kSmD = kSmV + 2 * kVecStride;   // 2 x {a[256], b[256]} f32 (decay tables per head)
-constexpr uint32_t kSmBar = kSmD + 2 * 2048;
+constexpr uint32_t kSmV = kSmS + kNSB * 16384;   // 2 vector buffers
+constexpr uint32_t kSmD = kSmV + 2 * kVecStride;   // 2 x {a[256], b[256], f[256]} f32 (decay tables per head)
+constexpr uint32_t kSmBar = kSmD + 2 * 3072;
 constexpr int kNumBars = 9 + 3 * kNS + 8;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
@@ -99,7 +104,15 @@ struct Bars {
 };
 
 constexpr int kTransformThreads = 16 * 32;
-constexpr int kEpilogueThreads = 4 * 32;
+constexpr int kTransformWarps = 16, kEpilogueWarps = 4;
+
+// Consumer arrivals are made once per warp: every lane's earlier shared-memory
+// writes (made visible to the async proxy by its own fence where needed) are
+// ordered before lane 0's release by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 
 }  // namespace
 
@@ -120,17 +133,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.b_free, 1);
     mbar_init(bar.c_free, 1);
     mbar_init(bar.cb_full, 1);
-    mbar_init(bar.cb_used, kTransformThreads);
+    mbar_init(bar.cb_used, kTransformWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.vec_full[i], 1);
-      mbar_init(&bar.vec_free[i], kTransformThreads + kEpilogueThreads);
+      mbar_init(&bar.vec_free[i], kTransformWarps + kEpilogueWarps);
       mbar_init(&bar.s_full[i], 1);
       mbar_init(&bar.s_free[i], 1);
       mbar_init(&bar.acc_full[i], 1);
-      mbar_init(&bar.acc_free[i], kEpilogueThreads);
+      mbar_init(&bar.acc_free[i], kEpilogueWarps);
     }
     for (int i = 0; i < kNS; ++i) {
-      mbar_init(&bar.a_full[i], kTransformThreads);
+      mbar_init(&bar.a_full[i], kTransformWarps);
       mbar_init(&bar.x_full[i], 1);
       mbar_init(&bar.slot_free[i], 1);
     }
@@ -188,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
           }
           if (o.c > 0) {
-            const int sb = ns & 1;
-            if (ns >= 2) mbar_wait(&bar.s_free[sb], parity(ns / 2 - 1), status);
+            const int sb = ns % kNSB;
+            if (ns >= kNSB) mbar_wait(&bar.s_free[sb], parity(ns / kNSB - 1), status);
             mbar_expect_tx(&bar.s_full[sb], 16384);
             const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
             tma_load_2d(sm + kSmS + sb * 16384, &tm_s, &bar.s_full[sb], 0, srow);
@@ -238,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&bar.slot_free[slot]);
           }
           if (o.c > 0) {
-            const int sb = ns & 1;
-            mbar_wait(&bar.s_full[sb], parity(ns / 2), status);
+            const int sb = ns % kNSB;
+            mbar_wait(&bar.s_full[sb], parity(ns / kNSB), status);
             tc_fence_after();
             for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
@@ -261,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (uint32_t m = k > (uint32_t)kNS ? k - kNS : 0u; m < k; ++m)
         mbar_wait(&bar.slot_free[m % kNS], parity(m / kNS), status);
-      for (uint32_t m = ns > 2u ? ns - 2u : 0u; m < ns; ++m) mbar_wait(&bar.s_free[m & 1], parity(m / 2), status);
+      for (uint32_t m = ns > (uint32_t)kNSB ? ns - kNSB : 0u; m < ns; ++m)
+        mbar_wait(&bar.s_free[m % kNSB], parity(m / kNSB), status);
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ transform
@@ -279,17 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vb = nh & 1;
         mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
         const uint32_t vacs = sV + vb * kVecStride, vdt = vacs + 1024, vseq = vacs + 2048 + 16;
-        const uint32_t da = sD + vb * 2048, db = da + 1024;
+        const uint32_t da = sD + vb * 3072, db = da + 1024, df = da + 2048;
         if (hh == 0 && has_seq) {  // first token of row i's sequence inside the chunk
           const int si = pipe::lds_i(vseq + 4 * i);
           start_i = i;
           while (start_i > 0 && pipe::lds_i(vseq + 4 * (start_i - 1)) == si) --start_i;
         }
         if (tt < pr.Q) {
-          const float a = pipe::lds_f(vacs + 4 * tt) * kLog2e;
+          const float acs_j = pipe::lds_f(vacs + 4 * tt), dt_j = pipe::lds_f(vdt + 4 * tt);
+          const float a = acs_j * kLog2e;
+          const float f = ex2_approx((pipe::lds_f(vacs + 4 * (tt | 15)) - acs_j) * kLog2e) * dt_j;
           asm volatile("st.shared.f32 [%0], %1;" ::"r"(da + 4 * tt), "f"(a) : "memory");
-          asm volatile("st.shared.f32 [%0], %1;" ::"r"(db + 4 * tt), "f"(__log2f(pipe::lds_f(vdt + 4 * tt)) - a)
-                       : "memory");
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(db + 4 * tt), "f"(__log2f(dt_j) - a) : "memory");
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(df + 4 * tt), "f"(f) : "memory");
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kTransformThreads) : "memory");
         const float ai = pipe::lds_f(da + 4 * i);
@@ -303,15 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             float v[16], r[16];
             tmem_ld16(pipe::tmem_quad(tmem, j0), v);
-            const bool full = __all_sync(0xffffffffu, start_i <= j0 && j0 + 15 <= i);
+            if (row_lo >= j0 + 15) {  // whole group below the diagonal: factorised decay
+              const float ei = ex2_approx(ai - pipe::lds_f(da + 4 * (j0 + 15)));
+              const bool nomask = __all_sync(0xffffffffu, start_i <= j0);
 #pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-              const float4 b4 = pipe::lds_f4(db + 4 * (j0 + e));
-              const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-              if (full) {
+              for (int e = 0; e < 16; e += 4) {
+                const float4 f4 = pipe::lds_f4(df + 4 * (j0 + e));
+                const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-                for (int m = 0; m < 4; ++m) r[e + m] = v[e + m] * ex2_approx(ai + bv[m]);
-              } else {
+                for (int m = 0; m < 4; ++m) {
+                  const float val = v[e + m] * fv[m] * ei;
+                  r[e + m] = (nomask || j0 + e + m >= start_i) ? val : 0.f;
+                }
+              }
+            } else {  // group on the diagonal: one 2^x per element
+#pragma unroll
+              for (int e = 0; e < 16; e += 4) {
+                const float4 b4 = pipe::lds_f4(db + 4 * (j0 + e));
+                const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                   const int j = j0 + e + m;
@@ -332,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           pipe::sts_u4(A + sw128_offset(il, 16 * cg), pk[0]);
           pipe::sts_u4(A + sw128_offset(il, 16 * cg + 8), pk[1]);
           fence_async_smem();
-          mbar_arrive(&bar.a_full[slot]);
+          warp_arrive(&bar.a_full[slot]);
         }
-        mbar_arrive(&bar.vec_free[vb]);
+        warp_arrive(&bar.vec_free[vb]);
       }
       tc_fence_before();
-      mbar_arrive(bar.cb_used);
+      warp_arrive(bar.cb_used);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -356,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vacs = sV + vb * kVecStride, vseq = vacs + 2048 + 16;
         const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(vseq - 4);
         const float em = (has_off && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
-        mbar_arrive(&bar.vec_free[vb]);
+        warp_arrive(&bar.vec_free[vb]);
         const float Dh = __ldg(pr.D + h);
         mbar_wait(&bar.acc_full[ab], parity(nh / 2), status);
         tc_fence_after();
@@ -379,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bar.acc_free[ab]);
+        warp_arrive(&bar.acc_free[ab]);
       }
     }
   }
