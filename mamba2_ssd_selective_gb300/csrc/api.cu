@@ -200,10 +200,7 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
                                                  const_cast<float *>(pr.dend), s));
   if constexpr (kIsBf16<T>) {
-    if (tc) {
-      SSD_LAUNCH("tc_cb", launch_tc_cb(pr, u, cb, status, s));
-      SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));
-    }
+    if (tc) SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));  // CB: in-kernel
   }
   if (!tc) {
     SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
@@ -227,15 +224,13 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   int vcol_parts = 1, nsub = pr.H, spg = pr.hpg;
   if constexpr (kIsBf16<T>) {
     if (tc) {
-      __nv_bfloat16 *wb = reinterpret_cast<__nv_bfloat16 *>(wbuf);
-      SSD_LAUNCH("tc_chunk_w", launch_tc_w(pr, u, dy, dtv, acs, cb, wb, tok, status, s));
       __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
       __nv_bfloat16 *dse16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.dse16);
       SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, 0, s));
       SSD_LAUNCH("combine_state", launch_combine_state(pr, dsl, gout, dse16, 1, s));
-      SSD_LAUNCH("tc_chunk_dx", launch_tc_dx(pr, u, dy, dtv, acs, cb, dse16, du, tok, status, s));
-      SSD_LAUNCH("tc_chunk_dcdb", launch_tc_dcdb(pr, u, dy, dtv, acs, wb, sin16, dse16, dcp, dbp, tok, status, s));
-      vcol_parts = pr.Q / 128;
+      SSD_LAUNCH("tc_bwd_row", launch_tc_bwd_row(pr, u, dy, dtv, acs, sin16, dcp, tok, status, s));
+      SSD_LAUNCH("tc_bwd_col", launch_tc_bwd_col(pr, u, dy, dtv, acs, dse16, du, dbp, tok, status, s));
+      vcol_parts = 1;
       nsub = pr.H / tc_head_subset(pr);
       spg = pr.hpg / tc_head_subset(pr);
     }
@@ -283,7 +278,8 @@ extern "C" {
 
 size_t ssd_workspace_size(const ssd_dims *dims, int backward) {
   if (check_dims(dims) != SSD_OK) return 0;
-  return plan_workspace(problem_from(dims), elem_bytes(dims->dtype), backward != 0).total;
+  const Problem pr = problem_from(dims);
+  return plan_workspace(pr, elem_bytes(dims->dtype), backward != 0, dims->dtype == SSD_BF16 && tc_envelope(pr)).total;
 }
 
 ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
@@ -297,7 +293,7 @@ ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, floa
   if (!aligned(y, 16) || (final_state && !aligned(final_state, 16)) ||
       (seg_init_states && !aligned(seg_init_states, 16)))
     return SSD_ERR_ALIGNMENT;
-  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false);
+  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false, dims->dtype == SSD_BF16 && tc_envelope(pr));
   if (!workspace || ws_bytes < w.total) return SSD_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return SSD_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -318,7 +314,7 @@ ssd_status ssd_forward_static(const ssd_dims *dims, const ssd_inputs *in, void *
   if (!aligned(y, 16) || (final_state && !aligned(final_state, 16)) ||
       (seg_init_states && !aligned(seg_init_states, 16)))
     return SSD_ERR_ALIGNMENT;
-  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false);
+  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false, dims->dtype == SSD_BF16 && tc_envelope(pr));
   if (w.total > SSD_STATIC_SCRATCH_BYTES) return SSD_ERR_WORKSPACE;
   void *scratch = static_scratch_ptr();
   if (!scratch) return SSD_ERR_CUDA;
@@ -352,7 +348,7 @@ ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *
       grads->dC_tok_stride % vec || (dfinal_state && !aligned(dfinal_state, 16)) ||
       (seg_init_states && !aligned(seg_init_states, 16)))
     return SSD_ERR_ALIGNMENT;
-  const Workspace w = plan_workspace(pr, eb, true);
+  const Workspace w = plan_workspace(pr, eb, true, dims->dtype == SSD_BF16 && tc_envelope(pr));
   if (!workspace || ws_bytes < w.total) return SSD_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return SSD_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

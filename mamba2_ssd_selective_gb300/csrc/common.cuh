@@ -72,7 +72,7 @@ struct Workspace {
   size_t status;                               // int32 device status word
   size_t u;                                    // (b, L, Cd) act dtype: post-conv activations
   size_t dtv, acs;                             // (b, H, L) f32: dt, chunk-local cumsum of dt*A
-  size_t cb;                                   // (b, nc, G, Q, Q) f32: C_i . B_j per chunk
+  size_t cb;                                   // (b, nc, G, Q, Q) f32: C_i . B_j per chunk (CUDA-core path)
   size_t sst;                                  // (b, nc, H, P, N) f32: chunk states, then local S_in
   size_t sin16;                                // (b, nc, H, P, N) bf16: true S_in (tensor-core path)
   size_t dtab;                                 // 3 x (b, H, nc) f32: cdec, dstart, dend
@@ -83,7 +83,7 @@ struct Workspace {
   size_t dse16;                                // (b, nc, H, P, N) bf16: true dS at chunk ends (tensor-core path)
   size_t gext, gout;                           // (b, S, H, P, N) f32
   size_t du;                                   // (b, L, Cd) f32: grad of post-conv activations
-  size_t w;                                    // (b, nc, H, Q, Q) f32: dM o L o dt
+  size_t w;                                    // (b, nc, H, Q, Q) f32: dM o L o dt (CUDA-core path)
   size_t tok;                                  // 6 x (b, H, L) f32 per-token adjoint pieces
   size_t dcp, dbp;                             // (b, L, H, N) f32 per-head dC / dB partials
   size_t chs;                                  // 4 x (b, nc, H) f32 per-chunk scalars
@@ -92,7 +92,9 @@ struct Workspace {
   int ntb;                                     // conv backward token blocks per row
 };
 
-inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward) {
+// tc: the tensor-core path, which forms CB inside its kernels and keeps W on
+// chip, so it needs neither the CB nor the W buffer.
+inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward, bool tc) {
   Workspace w{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -106,7 +108,7 @@ inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward
   w.u = take(b * L * Cd * elem_bytes);
   w.dtv = take(b * H * L * 4);
   w.acs = take(b * H * L * 4);
-  w.cb = take(b * nc * G * Q * Q * 4);
+  w.cb = take(tc ? 0 : b * nc * G * Q * Q * 4);
   w.sst = take(b * nc * H * P * N * 4);
   w.sext = take(b * S * H * P * N * 4);
   w.segin = take(b * S * H * P * N * 4);
@@ -120,7 +122,7 @@ inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward
     w.gext = take(b * S * H * P * N * 4);
     w.gout = take(b * S * H * P * N * 4);
     w.du = take(b * L * Cd * 4);
-    w.w = take(b * nc * H * Q * Q * 4);
+    w.w = take(tc ? 0 : b * nc * H * Q * Q * 4);
     w.tok = take(6 * b * H * L * 4);
     w.dcp = take(b * L * H * N * 4);
     w.dbp = take(b * L * H * N * 4);

@@ -63,7 +63,6 @@ void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int
 inline bool tc_envelope(const Problem &pr) {
   return pr.P == 64 && pr.N == 128 && (pr.Q == 128 || pr.Q == 256) && pr.hpg % 2 == 0;
 }
-void launch_tc_cb(const Problem &pr, const __nv_bfloat16 *u, float *cb, int *status, cudaStream_t s);
 void launch_tc_state(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, float *sst,
                      int *status, cudaStream_t s);
 // persistent output kernel (tc_out.cu)
@@ -71,14 +70,13 @@ void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, 
                    const __nv_bfloat16 *sin16, __nv_bfloat16 *y, int *status, cudaStream_t s);
 void launch_tc_z(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
                  const float *acs, float *dsl, int *status, cudaStream_t s);
-void launch_tc_w(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
-                 const float *acs, const float *cb, __nv_bfloat16 *wbuf, float *tok, int *status, cudaStream_t s);
-void launch_tc_dx(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
-                  const float *acs, const float *cb, const __nv_bfloat16 *dse16, float *du, float *tok, int *status,
-                  cudaStream_t s);
-void launch_tc_dcdb(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
-                    const float *acs, const __nv_bfloat16 *wbuf, const __nv_bfloat16 *sin16,
-                    const __nv_bfloat16 *dse16, float *dcp, float *dbp, float *tok, int *status, cudaStream_t s);
+// persistent backward kernels (tc_bwd_row.cu, tc_bwd_col.cu)
+void launch_tc_bwd_row(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
+                       const float *acs, const __nv_bfloat16 *sin16, float *dcp, float *tok, int *status,
+                       cudaStream_t s);
+void launch_tc_bwd_col(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,
+                       const float *acs, const __nv_bfloat16 *dse16, float *du, float *dbp, float *tok, int *status,
+                       cudaStream_t s);
 int tc_head_subset(const Problem &pr);  // heads per dB/dC partial on the tensor-core path
 
 }  // namespace ssd

@@ -1,0 +1,523 @@
+// Backward of the chunked Mamba2 SSD, column side, on the tensor cores: for the
+// rows j of one 128-token tile J of a chunk (columns i >= 128 J), per head h,
+//   dM^T = x_h dy_h^T,   CB^T = B_J C^T            (64-column slices, recomputed)
+//   M^T  = CB^T o L^T o dt_j,   W^T = dM^T o L^T o dt_j,  L^T[j, i] = exp(Acs_i - Acs_j)
+//   T_j  = sum_i M^T[j, i] dy_i,   U_j = dS_end,h B_j,     (tensor memory)
+//   du_x[j] = T_j + wdt_j U_j + D_h dy_j,   q_j = x_j . U_j,
+//   vcol_j = sum_i V[i, j] = sum_i dM^T CB^T L^T
+// and accumulates over the heads of a block
+//   dB_j += sum_i W^T[j, i] C_i + wdt_j dS_end,h^T x_j,
+// written as one fp32 partial per (token, head block).
+//
+// Roles as in the row kernel (22 warps, one CTA per SM).  Tensor memory:
+//   [0, 256) two slice slots {dM^T 64 | CB^T 64} | [256, 320) T | [320, 384) U |
+//   [384, 512) dB.
+#include "chunk_common.cuh"
+#include "kernels.h"
+#include "tc_engine.cuh"
+#include "tc_pipe.cuh"
+
+namespace ssd {
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+using namespace sm100;
+using pipe::parity;
+
+constexpr int kWarps = 22, kThreads = kWarps * 32, kEpiWarp0 = 18;
+constexpr int kTWarps = 16, kEWarps = 4, kTThreads = kTWarps * 32;
+constexpr int kNY = 3;  // dy slice ring
+constexpr int kNA = 2;  // transformed operand ring (M^T, W^T slices, wdt x)
+
+constexpr uint32_t kSmBJ = 0;                   // B_J: 2 K halves x [128 x 128 B]
+constexpr uint32_t kSmCR = kSmBJ + 32768;       // C rows i >= 128 J: 2 K halves x [256 x 128 B]
+constexpr uint32_t kSmXT = kSmCR + 65536;       // 2 x x_h tile [128 x 64] bf16
+constexpr uint32_t kSmDY = kSmXT + 2 * 16384;   // ring of dy slices [64 x 64] bf16
+constexpr uint32_t kSmA = kSmDY + kNY * 8192;   // ring of [128 x 64] bf16 operands
+constexpr uint32_t kSmDS = kSmA + kNA * 16384;  // dS_end,h: 2 K halves x [64 x 128 B]
+constexpr uint32_t kVecStride = 3200;           // acs[256] | dt[256] | seq[4 + 256]
+constexpr uint32_t kSmV = kSmDS + 16384;
+constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], g[256]}
+constexpr uint32_t kSmVC = kSmD + 2 * 2048;     // 2 x vcol partials [4][128] f32
+constexpr uint32_t kSmBar = kSmVC + 2 * 2048;
+constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA;
+constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
+constexpr int kSmemBytes = (int)kSmEnd + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kTmT = 256, kTmU = 320, kTmDB = 384;
+
+struct Unit {
+  int bb, c, J, h0;
+};
+
+// tiles with more columns (lower J) first; head blocks of one (row, chunk) adjacent
+__device__ __forceinline__ Unit unit_of(const Problem &pr, int nhb, int HB, int u) {
+  const int per = pr.b * pr.nc * nhb;
+  const int cls = u / per, r = u % per;
+  Unit o;
+  o.J = cls;
+  const int hb = r % nhb, bc = r / nhb;
+  o.c = bc % pr.nc;
+  o.bb = bc / pr.nc;
+  o.h0 = hb * HB;
+  return o;
+}
+
+struct Bars {
+  uint64_t *unit_full, *unit_free, *tu_full, *tu_free, *ds_full, *ds_free, *db_full, *db_free;
+  uint64_t *ring_full, *ring_free, *vec_full, *vec_free, *xt_full, *xt_free;  // [2]
+  uint64_t *dy_full, *dy_free;                                                // [kNY]
+  uint64_t *a_full, *a_free;                                                  // [kNA]
+  __device__ Bars(uint64_t *b) {
+    unit_full = b;
+    unit_free = b + 1;
+    tu_full = b + 2;
+    tu_free = b + 3;
+    ds_full = b + 4;
+    ds_free = b + 5;
+    db_full = b + 6;
+    db_free = b + 7;
+    ring_full = b + 8;
+    ring_free = b + 10;
+    vec_full = b + 12;
+    vec_free = b + 14;
+    xt_full = b + 16;
+    xt_free = b + 18;
+    dy_full = b + 20;
+    dy_free = dy_full + kNY;
+    a_full = dy_free + kNY;
+    a_free = a_full + kNA;
+  }
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_col_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dy,
+                      const __grid_constant__ CUtensorMap tm_ds, Problem pr, const bf16 *__restrict__ u,
+                      const bf16 *__restrict__ dy, const float *__restrict__ dtv, const float *__restrict__ acs,
+                      float *__restrict__ du, float *__restrict__ dbp, float *__restrict__ tok, int HB, int nunits,
+                      int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = tc::aligned_smem(smem_raw);
+  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar));
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NTI = pr.Q / 128, nhb = pr.H / HB, HP = pr.H * pr.P;
+  const bool has_seq = pr.seq_idx != nullptr;
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  (void)NTI;
+
+  if (threadIdx.x == 0) {
+    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.tu_full, bar.ds_full, bar.ds_free, bar.db_full};
+    for (uint64_t *b : ones) mbar_init(b, 1);
+    mbar_init(bar.tu_free, kEWarps);
+    mbar_init(bar.db_free, kEWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.ring_full[i], 1);
+      mbar_init(&bar.ring_free[i], kTWarps);
+      mbar_init(&bar.vec_full[i], 1);
+      mbar_init(&bar.vec_free[i], kTWarps + kEWarps);
+      mbar_init(&bar.xt_full[i], 1);
+      mbar_init(&bar.xt_free[i], 1 + kTWarps);
+    }
+    for (int i = 0; i < kNY; ++i) {
+      mbar_init(&bar.dy_full[i], 1);
+      mbar_init(&bar.dy_free[i], 1);
+    }
+    for (int i = 0; i < kNA; ++i) {
+      mbar_init(&bar.a_full[i], kTWarps);
+      mbar_init(&bar.a_free[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_u);
+      prefetch_tmap(&tm_dy);
+      prefetch_tmap(&tm_ds);
+      uint32_t nu = 0, nh = 0, m = 0, nd = 0;
+      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+        const Unit o = unit_of(pr, nhb, HB, ui);
+        const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, nsl = (pr.Q - 128 * o.J) / 64;
+        const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N, rJ = row0 + 128 * o.J;
+        if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
+        mbar_expect_tx(bar.unit_full, 32768 + 2 * nsl * 8192);
+        for (int kh = 0; kh < 2; ++kh) {
+          for (int r = 0; r < 2; ++r)
+            tma_load_2d(sm + kSmBJ + kh * 16384 + r * 8192, &tm_u, bar.unit_full, offB + 64 * kh, rJ + 64 * r);
+          for (int r = 0; r < nsl; ++r)
+            tma_load_2d(sm + kSmCR + kh * 32768 + r * 8192, &tm_u, bar.unit_full, offC + 64 * kh, rJ + 64 * r);
+        }
+        for (int hh = 0; hh < HB; ++hh, ++nh) {
+          const int h = o.h0 + hh, vb = nh & 1;
+          if (nh >= 2) mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status);
+          uint8_t *vec = sm + kSmV + vb * kVecStride;
+          const size_t bh = ((size_t)o.bb * pr.H + h) * pr.L + t0;
+          const uint32_t seq_bytes = !has_seq ? 0u : (uint32_t)(pr.Q * 4);
+          mbar_expect_tx(&bar.vec_full[vb], 2 * pr.Q * 4 + seq_bytes);
+          pipe::bulk_load(vec, acs + bh, pr.Q * 4, &bar.vec_full[vb]);
+          pipe::bulk_load(vec + 1024, dtv + bh, pr.Q * 4, &bar.vec_full[vb]);
+          if (has_seq)
+            pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
+          if (nh >= 2) mbar_wait(&bar.xt_free[vb], parity(nh / 2 - 1), status);
+          mbar_expect_tx(&bar.xt_full[vb], 16384);
+          for (int r = 0; r < 2; ++r)
+            tma_load_2d(sm + kSmXT + vb * 16384 + r * 8192, &tm_u, &bar.xt_full[vb], h * pr.P, rJ + 64 * r);
+          for (int s = 0; s < nsl; ++s, ++m) {
+            const int ys = m % kNY;
+            if (m >= kNY) mbar_wait(&bar.dy_free[ys], parity(m / kNY - 1), status);
+            mbar_expect_tx(&bar.dy_full[ys], 8192);
+            tma_load_2d(sm + kSmDY + ys * 8192, &tm_dy, &bar.dy_full[ys], h * pr.P, rJ + 64 * s);
+          }
+          if (nd >= 1) mbar_wait(bar.ds_free, parity(nd - 1), status);
+          mbar_expect_tx(bar.ds_full, 16384);
+          const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
+          tma_load_2d(sm + kSmDS, &tm_ds, bar.ds_full, 0, srow);
+          tma_load_2d(sm + kSmDS + 8192, &tm_ds, bar.ds_full, 64, srow);
+          ++nd;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sBJ = smem_u32(sm + kSmBJ), sCR = smem_u32(sm + kSmCR), sXT = smem_u32(sm + kSmXT),
+                     sDY = smem_u32(sm + kSmDY), sA = smem_u32(sm + kSmA), sDS = smem_u32(sm + kSmDS);
+      constexpr uint32_t id_64 = idesc_bf16(128, 64, false, false);    // x dy^T, B_J C^T, B_J dS^T
+      constexpr uint32_t id_t = idesc_bf16(128, 64, false, true);      // M^T dy
+      constexpr uint32_t id_db = idesc_bf16(128, 128, false, true);    // W^T C, (wdt x) dS
+      uint32_t nu = 0, nh = 0, m = 0, na = 0, nd = 0;
+      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+        const Unit o = unit_of(pr, nhb, HB, ui);
+        const int nsl = (pr.Q - 128 * o.J) / 64;
+        mbar_wait(bar.unit_full, parity(nu), status);
+        bool first_db = true;
+        for (int hh = 0; hh < HB; ++hh, ++nh) {
+          const int vb = nh & 1;
+          const uint32_t sxt = sXT + vb * 16384;
+          mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);
+          // slice item n: dM^T and CB^T of columns [64 s, 64 s + 64) into ring slot n % 2
+          auto issue_item = [&](uint32_t n, int s) {
+            const int rs = n & 1, ys = n % kNY;
+            if (n >= 2) mbar_wait(&bar.ring_free[rs], parity(n / 2 - 1), status);
+            mbar_wait(&bar.dy_full[ys], parity(n / kNY), status);
+            tc_fence_after();
+            const uint32_t td = tmem + 128 * rs;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(td, desc_sw128(sxt + kk * 32, 16, 1024), desc_sw128(sDY + ys * 8192 + kk * 32, 16, 1024),
+                        id_64, kk > 0 ? 1u : 0u);
+            for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(td + 64, desc_sw128(sBJ + kh * 16384 + kk * 32, 16, 1024),
+                          desc_sw128(sCR + kh * 32768 + 8192 * s + kk * 32, 16, 1024), id_64, (kh | kk) ? 1u : 0u);
+            umma_commit(&bar.ring_full[rs]);
+          };
+          issue_item(m, 0);
+          for (int s = 0; s < nsl; ++s) {
+            if (s + 1 < nsl) issue_item(m + s + 1, s + 1);
+            const int ys = (m + s) % kNY;
+            // T += M^T_s dy_s
+            int as = na % kNA;
+            mbar_wait(&bar.a_full[as], parity(na / kNA), status);
+            if (s == 0 && nh > 0) mbar_wait(bar.tu_free, parity(nh - 1), status);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + kTmT, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
+                        desc_sw128(sDY + ys * 8192 + kk * 2048, 8192, 1024), id_t, (s | kk) ? 1u : 0u);
+            umma_commit(&bar.a_free[as]);
+            umma_commit(&bar.dy_free[ys]);
+            ++na;
+            // dB += W^T_s C_s
+            as = na % kNA;
+            mbar_wait(&bar.a_full[as], parity(na / kNA), status);
+            if (first_db && nu > 0) mbar_wait(bar.db_free, parity(nu - 1), status);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + kTmDB, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
+                        desc_sw128(sCR + 8192 * s + kk * 2048, 32768, 1024), id_db, (first_db && kk == 0) ? 0u : 1u);
+            first_db = false;
+            umma_commit(&bar.a_free[as]);
+            ++na;
+          }
+          m += nsl;
+          // U = B_J dS^T, and dB += (wdt x) dS
+          mbar_wait(bar.ds_full, parity(nd), status);
+          tc_fence_after();
+          for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + kTmU, desc_sw128(sBJ + kh * 16384 + kk * 32, 16, 1024),
+                        desc_sw128(sDS + kh * 8192 + kk * 32, 16, 1024), id_64, (kh | kk) ? 1u : 0u);
+          umma_commit(bar.tu_full);
+          const int as = na % kNA;
+          mbar_wait(&bar.a_full[as], parity(na / kNA), status);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kTmDB, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
+                      desc_sw128(sDS + kk * 2048, 8192, 1024), id_db, 1u);
+          umma_commit(&bar.a_free[as]);
+          ++na;
+          umma_commit(bar.ds_free);
+          ++nd;
+          umma_commit(&bar.xt_free[vb]);
+        }
+        umma_commit(bar.db_full);
+        umma_commit(bar.unit_free);
+      }
+      if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
+      for (uint32_t n = m > (uint32_t)kNY ? m - kNY : 0u; n < m; ++n)
+        mbar_wait(&bar.dy_free[n % kNY], parity(n / kNY), status);
+      for (uint32_t n = na > (uint32_t)kNA ? na - kNA : 0u; n < na; ++n)
+        mbar_wait(&bar.a_free[n % kNA], parity(n / kNA), status);
+      if (nd > 0) mbar_wait(bar.ds_free, parity(nd - 1), status);
+      for (uint32_t n = nh > 2u ? nh - 2u : 0u; n < nh; ++n) mbar_wait(&bar.xt_free[n & 1], parity(n / 2), status);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ transform
+    // thread = row j of the tile (TMEM lane), 16 columns i per slice
+    const int q = warp & 3, cg = (warp - 2) >> 2, jl = 32 * q + lane, tt = threadIdx.x - 64;
+    const uint32_t sA = smem_u32(sm + kSmA), sV = smem_u32(sm + kSmV), sD = smem_u32(sm + kSmD),
+                   sVC = smem_u32(sm + kSmVC), sXT = smem_u32(sm + kSmXT);
+    const float kLog2e = 1.4426950408889634f;
+    uint32_t nu = 0, nh = 0, m = 0, na = 0;
+    size_t prev_tok = 0;
+    int prev_vb = -1;
+    auto flush_vcol = [&]() {
+      if (prev_vb >= 0 && cg == 0) {
+        const uint32_t base = sVC + prev_vb * 2048 + 4 * jl;
+        tok[prev_tok] = (pipe::lds_f(base) + pipe::lds_f(base + 512)) + (pipe::lds_f(base + 1024) + pipe::lds_f(base + 1536));
+      }
+    };
+    auto put = [&](const float (&v)[16]) {  // write 16 values of row jl as bf16 into the next A slot
+      const int as = na % kNA;
+      if (na >= (uint32_t)kNA) mbar_wait(&bar.a_free[as], parity(na / kNA - 1), status);
+      float v0[8], v1[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v0[e] = v[e];
+        v1[e] = v[8 + e];
+      }
+      const uint32_t A = sA + as * 16384;
+      pipe::sts_u4(A + sw128_offset(jl, 16 * cg), tc::pack8(v0));
+      pipe::sts_u4(A + sw128_offset(jl, 16 * cg + 8), tc::pack8(v1));
+      fence_async_smem();
+      pipe::warp_arrive(&bar.a_full[as]);
+      ++na;
+    };
+    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      const Unit o = unit_of(pr, nhb, HB, ui);
+      const int j = 128 * o.J + jl, row_lo = 128 * o.J + 32 * q, row_hi = row_lo + 31;
+      const int nsl = (pr.Q - 128 * o.J) / 64;
+      int end_j = pr.Q - 1;
+      for (int hh = 0; hh < HB; ++hh, ++nh) {
+        const int h = o.h0 + hh, vb = nh & 1;
+        mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
+        const uint32_t vacs = sV + vb * kVecStride, vdt = vacs + 1024, vseq = vacs + 2048 + 16;
+        const uint32_t ta = sD + vb * 2048, tg = ta + 1024;
+        if (hh == 0 && has_seq) {  // last token of row j's sequence inside the chunk
+          const int sj = pipe::lds_i(vseq + 4 * j);
+          end_j = j;
+          while (end_j < pr.Q - 1 && pipe::lds_i(vseq + 4 * (end_j + 1)) == sj) ++end_j;
+        }
+        const float acs_j = pipe::lds_f(vacs + 4 * j), dt_j = pipe::lds_f(vdt + 4 * j);
+        const bool in_last = !has_seq || pipe::lds_i(vseq + 4 * j) == pipe::lds_i(vseq + 4 * (pr.Q - 1));
+        const float wdt = in_last ? expf(pipe::lds_f(vacs + 4 * (pr.Q - 1)) - acs_j) * dt_j : 0.f;
+        if (tt < pr.Q) {
+          const float a = pipe::lds_f(vacs + 4 * tt) * kLog2e;
+          pipe::sts_f(ta + 4 * tt, a);
+          pipe::sts_f(tg + 4 * tt, ex2_approx(a - pipe::lds_f(vacs + 4 * (tt & ~15)) * kLog2e));
+        }
+        pipe::transform_sync<kTThreads>();
+        flush_vcol();
+        const float aj = acs_j * kLog2e;
+        float vcol = 0.f;
+        for (int s = 0; s < nsl; ++s, ++m) {
+          const int rs = m & 1, i0 = 128 * o.J + 64 * s + 16 * cg;
+          float mt[16], wt[16];
+          mbar_wait(&bar.ring_full[rs], parity(m / 2), status);
+          tc_fence_after();
+          if (i0 + 15 < row_lo) {  // every column before every row: zero
+            pipe::warp_arrive(&bar.ring_free[rs]);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mt[e] = wt[e] = 0.f;
+          } else {
+            float dm[16], cbv[16];
+            tmem_ld16(pipe::tmem_quad(tmem + 128 * rs, 16 * cg), dm);
+            tmem_ld16(pipe::tmem_quad(tmem + 128 * rs + 64, 16 * cg), cbv);
+            tc_fence_before();
+            pipe::warp_arrive(&bar.ring_free[rs]);
+            if (i0 >= row_hi) {  // every column at or after every row: factorised decay
+              const float e0 = ex2_approx(pipe::lds_f(ta + 4 * i0) - aj), ed = e0 * dt_j;
+              const bool nomask = __all_sync(0xffffffffu, end_j >= i0 + 15);
+              float vs = 0.f;
+#pragma unroll
+              for (int e = 0; e < 16; e += 4) {
+                const float4 g4 = pipe::lds_f4(tg + 4 * (i0 + e));
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                  const bool ok = nomask || i0 + e + k4 <= end_j;
+                  const float gi = ok ? gv[k4] : 0.f;
+                  const float t1 = gi * ed;
+                  vs = fmaf(dm[e + k4] * cbv[e + k4], gi, vs);
+                  mt[e + k4] = cbv[e + k4] * t1;
+                  wt[e + k4] = dm[e + k4] * t1;
+                }
+              }
+              vcol = fmaf(vs, e0, vcol);
+            } else {  // on the diagonal: one 2^x per element
+#pragma unroll
+              for (int e = 0; e < 16; e += 4) {
+                const float4 a4 = pipe::lds_f4(ta + 4 * (i0 + e));
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                  const int i = i0 + e + k4;
+                  const bool ok = (unsigned)(i - j) <= (unsigned)(end_j - j);
+                  const float ee = ok ? ex2_approx(av[k4] - aj) : 0.f;
+                  vcol = fmaf(dm[e + k4] * cbv[e + k4], ee, vcol);
+                  const float t1 = ee * dt_j;
+                  mt[e + k4] = cbv[e + k4] * t1;
+                  wt[e + k4] = dm[e + k4] * t1;
+                }
+              }
+            }
+          }
+          put(mt);
+          put(wt);
+        }
+        {  // wdt_j x_j, the A operand of the dS_end term of dB
+          mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);
+          float xv[16];
+          const uint32_t T = sXT + vb * 16384;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            float x8[8];
+            tc::unpack8(pipe::lds_sw128(T, jl, 2 * cg + t), x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[8 * t + e] = x8[e] * wdt;
+          }
+          put(xv);
+        }
+        pipe::sts_f(sVC + vb * 2048 + cg * 512 + 4 * jl, vcol);
+        prev_tok = 2 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + (size_t)o.c * pr.Q + j;
+        prev_vb = vb;
+        pipe::warp_arrive(&bar.xt_free[vb]);
+        pipe::warp_arrive(&bar.vec_free[vb]);
+      }
+    }
+    pipe::transform_sync<kTThreads>();
+    flush_vcol();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3, jl = 32 * q + lane;
+    const uint32_t sV = smem_u32(sm + kSmV);
+    uint32_t nu = 0, nh = 0;
+    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      const Unit o = unit_of(pr, nhb, HB, ui);
+      const int j = 128 * o.J + jl, t = o.c * pr.Q + j;
+      const bf16 *dyrow = dy + ((size_t)o.bb * pr.L + t) * HP;
+      const bf16 *xrow = u + ((size_t)o.bb * pr.L + t) * pr.Cd;
+      for (int hh = 0; hh < HB; ++hh, ++nh) {
+        const int h = o.h0 + hh, vb = nh & 1;
+        mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
+        const uint32_t vacs = sV + vb * kVecStride, vdt = vacs + 1024, vseq = vacs + 2048 + 16;
+        const bool in_last = !has_seq || pipe::lds_i(vseq + 4 * j) == pipe::lds_i(vseq + 4 * (pr.Q - 1));
+        const float wdt =
+            in_last ? expf(pipe::lds_f(vacs + 4 * (pr.Q - 1)) - pipe::lds_f(vacs + 4 * j)) * pipe::lds_f(vdt + 4 * j)
+                    : 0.f;
+        pipe::warp_arrive(&bar.vec_free[vb]);
+        const float Dh = __ldg(pr.D + h);
+        mbar_wait(bar.tu_full, parity(nh), status);
+        tc_fence_after();
+        float *dur = du + ((size_t)o.bb * pr.L + t) * pr.Cd + h * pr.P;
+        float qsum = 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          float tv[16], uv[16];
+          tmem_ld16(pipe::tmem_quad(tmem + kTmT, 16 * cc), tv);
+          tmem_ld16(pipe::tmem_quad(tmem + kTmU, 16 * cc), uv);
+#pragma unroll
+          for (int t8 = 0; t8 < 2; ++t8) {
+            float d8[8], x8[8];
+            tc::unpack8(tc::ldg16(dyrow + h * pr.P + 16 * cc + 8 * t8), d8);
+            tc::unpack8(tc::ldg16(xrow + h * pr.P + 16 * cc + 8 * t8), x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int col = 8 * t8 + e;
+              qsum = fmaf(x8[e], uv[col], qsum);
+              tv[col] += wdt * uv[col] + Dh * d8[e];
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            reinterpret_cast<float4 *>(dur + 16 * cc)[e] = make_float4(tv[4 * e], tv[4 * e + 1], tv[4 * e + 2], tv[4 * e + 3]);
+        }
+        tc_fence_before();
+        pipe::warp_arrive(bar.tu_free);
+        tok[4 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = qsum;
+      }
+      mbar_wait(bar.db_full, parity(nu), status);
+      tc_fence_after();
+      float *out = dbp + (((size_t)o.bb * pr.L + t) * nhb + o.h0 / HB) * pr.N;
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        float a[16];
+        tmem_ld16(pipe::tmem_quad(tmem + kTmDB, 16 * cc), a);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          reinterpret_cast<float4 *>(out + 16 * cc)[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+      }
+      tc_fence_before();
+      pipe::warp_arrive(bar.db_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+void launch_tc_bwd_col(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs,
+                       const bf16 *dse16, float *du, float *dbp, float *tok, int *status, cudaStream_t s) {
+  static bool once = (cudaFuncSetAttribute(tc_bwd_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes),
+                      true);
+  (void)once;
+  CUtensorMap tm_u, tm_dy, tm_ds;
+  const uint64_t HP = (uint64_t)pr.H * pr.P;
+  if (!encode_tmap_bf16_2d(&tm_u, u, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 2, 64, 64) ||
+      !encode_tmap_bf16_2d(&tm_dy, dy, HP, (uint64_t)pr.b * pr.L, HP * 2, 64, 64) ||
+      !encode_tmap_bf16_2d(&tm_ds, dse16, pr.N, (uint64_t)pr.b * pr.nc * pr.H * pr.P, (uint64_t)pr.N * 2, 64, 64)) {
+    note_host_error();
+    return;
+  }
+  const int HB = tc_head_subset(pr);
+  const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
+  const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
+  tc_bwd_col_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_ds, pr, u, dy, dtv, acs, du, dbp, tok, HB,
+                                                       nunits, status);
+}
+
+}  // namespace ssd

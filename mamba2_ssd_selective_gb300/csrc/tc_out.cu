@@ -106,13 +106,6 @@ struct Bars {
 constexpr int kTransformThreads = 16 * 32;
 constexpr int kTransformWarps = 16, kEpilogueWarps = 4;
 
-// Consumer arrivals are made once per warp: every lane's earlier shared-memory
-// writes (made visible to the async proxy by its own fence where needed) are
-// ordered before lane 0's release by the warp barrier.
-__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
 
 }  // namespace
 
@@ -357,12 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           pipe::sts_u4(A + sw128_offset(il, 16 * cg), pk[0]);
           pipe::sts_u4(A + sw128_offset(il, 16 * cg + 8), pk[1]);
           fence_async_smem();
-          warp_arrive(&bar.a_full[slot]);
+          pipe::warp_arrive(&bar.a_full[slot]);
         }
-        warp_arrive(&bar.vec_free[vb]);
+        pipe::warp_arrive(&bar.vec_free[vb]);
       }
       tc_fence_before();
-      warp_arrive(bar.cb_used);
+      pipe::warp_arrive(bar.cb_used);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -381,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vacs = sV + vb * kVecStride, vseq = vacs + 2048 + 16;
         const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(vseq - 4);
         const float em = (has_off && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
-        warp_arrive(&bar.vec_free[vb]);
+        pipe::warp_arrive(&bar.vec_free[vb]);
         const float Dh = __ldg(pr.D + h);
         mbar_wait(&bar.acc_full[ab], parity(nh / 2), status);
         tc_fence_after();
@@ -404,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        warp_arrive(&bar.acc_free[ab]);
+        pipe::warp_arrive(&bar.acc_free[ab]);
       }
     }
   }

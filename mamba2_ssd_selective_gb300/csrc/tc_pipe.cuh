@@ -55,6 +55,33 @@ __device__ __forceinline__ void sts_u4(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Consumer arrivals are made once per warp: every lane's earlier shared-memory
+// writes (made visible to the async proxy by its own fence where needed) are
+// ordered before lane 0's release by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ void sts_f(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+// barrier among the `n` threads of the transform warps (named barrier 1)
+template <int n>
+__device__ __forceinline__ void transform_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(n) : "memory");
+}
+
+// 8 bf16 from a 128-byte-swizzled [rows x 64] bf16 tile: row r, columns 8c..8c+7
+__device__ __forceinline__ uint4 lds_sw128(uint32_t tile, int r, int c) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(tile + sw128_offset(r, 8 * c)));
+  return v;
+}
+
 // TMEM address of (lane quadrant of this warp, column col)
 __device__ __forceinline__ uint32_t tmem_quad(uint32_t base, int col) {
   return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
