@@ -148,39 +148,49 @@ def kernel_work(shape, dtype: str) -> dict:
     bc = b * L * GN * eb
     cb = b * nc * G * tiles * 128 * 128 * 4
     st = b * nc * H * PN * 4  # one (b, chunk, head) state array
+    st16 = st // 2  # the same in bf16
     seg = b * S * H * PN * 4
-    wbytes = b * nc * H * tiles * 128 * 128 * 2
     tok = b * H * L * 4
-    parts = b * L * H * N * 4
+    hpg = H // G
+    hb = next((v for v in (16, 8, 4, 2) if hpg % v == 0), 1)
+    parts = b * L * (H // hb) * N * 4  # one fp32 dB or dC partial per token and head block
     f_state = b * nc * H * 2 * P * N * Q
-    f_out = b * nc * H * (tri * 2 * P + 2 * Q * N * P)
-    f_w = b * nc * H * tri * 2 * P
-    f_dcdb = b * nc * H * (2 * tri * 2 * N + 2 * 2 * Q * P * N)
     f_cb = b * nc * G * tri * 2 * N
+    f_diag = b * nc * H * tri * 2 * P        # (CB o L o dt) X, dM, M^T dy: causal Q x Q x P
+    f_off = b * nc * H * 2 * Q * N * P       # one Q x N x P product per chunk and head
+    f_bc = b * nc * H * tri * 2 * N          # W B or W^T C: causal Q x Q x N
     w = {
         "conv_fwd": ("mem", 0, b * L * Cd * 2 * eb),
         "dt_prep": ("mem", 0, b * L * H * (eb + 8)),
+        "decay_tables": ("mem", 0, tok + 3 * b * H * nc * 4),
         "local_pass": ("mem", 0, 2 * st + seg),
         "seg_scan": ("mem", 0, 2 * seg + b * H * PN * 4),
+        "combine_state": ("mem", 0, st + st16 + seg),
         "local_rev": ("mem", 0, 2 * st + seg),
         "seg_rscan": ("mem", 0, 2 * seg),
         "chunk_dt": ("mem", 0, 5 * tok + 4 * st + 2 * x + b * L * H * eb),
         "bc_reduce": ("mem", 0, 2 * parts + 2 * b * L * GN * 4),
         "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 32) * Cd * 20),
         "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 32) * Cd * 20),
-        "tc_cb": ("tensor", f_cb, 2 * bc + cb),
         "tc_chunk_state": ("tensor", f_state, x + bc + st),
-        "tc_chunk_out": ("tensor", f_out, 2 * x + bc + cb + st + seg),
         "tc_chunk_z": ("tensor", f_state, x + bc + st),
-        "tc_chunk_w": ("tensor", f_w, 2 * x + cb + wbytes + 3 * tok),
-        "tc_chunk_dx": ("tensor", f_out, cb + x + bc + st + seg + b * L * HP * 4),
-        "tc_chunk_dcdb": ("tensor", f_dcdb, wbytes + 2 * x + 2 * bc + 2 * st + 2 * seg + 2 * parts + 2 * tok),
+        # persistent kernels: CB is formed on chip, W never leaves the SM
+        "tc_chunk_out": ("tensor", f_cb + f_diag + f_off, 2 * x + bc + st16 + 2 * tok),
+        "tc_bwd_row": ("tensor", f_cb + f_diag + f_bc + 2 * f_off, 2 * x + bc + st16 + 4 * tok + parts),
+        "tc_bwd_col": ("tensor", f_cb + 2 * f_diag + f_bc + 2 * f_off,
+                       2 * x + bc + st16 + 4 * tok + parts + b * L * HP * 4),
     }
-    for name, tcname in (("cb", "tc_cb"), ("chunk_state", "tc_chunk_state"), ("chunk_out", "tc_chunk_out"),
-                         ("chunk_z", "tc_chunk_z"), ("chunk_w", "tc_chunk_w"), ("chunk_dx", "tc_chunk_dx"),
-                         ("chunk_dcdb", "tc_chunk_dcdb")):
-        _, f, by = w[tcname]
-        w[name] = ("alu", f, by)
+    # fp32 CUDA-core kernels: the same work with CB, chunk states and W through HBM
+    wbytes = b * nc * H * tiles * 128 * 128 * 4
+    w.update({
+        "cb": ("alu", f_cb, 2 * bc + cb),
+        "chunk_state": ("alu", f_state, x + bc + st),
+        "chunk_out": ("alu", f_diag + f_off, 2 * x + bc + cb + st + seg),
+        "chunk_z": ("alu", f_state, x + bc + st),
+        "chunk_w": ("alu", f_diag, 2 * x + cb + wbytes + 3 * tok),
+        "chunk_dx": ("alu", f_diag + f_off, cb + x + bc + st + seg + b * L * HP * 4),
+        "chunk_dcdb": ("alu", 2 * f_bc + 2 * f_off, wbytes + 2 * x + 2 * bc + 2 * st + 2 * seg + 2 * b * L * H * N * 4),
+    })
     return w
 
 

@@ -36,6 +36,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float softplus_f(float z) { return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z)); }
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.f / (1.f + expf(-v)); }
+// sigmoid on the fast intrinsics (relative error ~1e-6; -v clamped so 1 + e^-v
+// stays finite), for the conv activation where it is applied per element
+__device__ __forceinline__ float sigmoid_fast(float v) { return __fdividef(1.f, 1.f + __expf(fminf(-v, 80.f))); }
 
 // seq id of token t of row b (0 when there is no seq_idx)
 __device__ __forceinline__ int seq_of(const Problem &pr, int b, int t) {

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(128) conv_fwd_kernel(Problem pr, T *__restrict
       v += m2 ? w[q][2] * r2[q] : 0.f;
       v += m1 ? w[q][1] * r1[q] : 0.f;
       v += m0 ? w[q][0] * r0[q] : 0.f;
-      o[q] = v * sigmoid_f(v);
+      o[q] = v * sigmoid_fast(v);
       r0[q] = r1[q]; r1[q] = r2[q]; r2[q] = rt[q];
     }
     store8(dst + (size_t)t * pr.Cd, o);
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *
         v += m2 ? w[q][2] * r2[q] : 0.f;
         v += m1 ? w[q][1] * r1[q] : 0.f;
         v += m0 ? w[q][0] * r0[q] : 0.f;
-        const float sg = sigmoid_f(v);
+        const float sg = sigmoid_fast(v);
         dvt[q] = g8[q] * sg * (1.f + v * (1.f - sg));
         if (own) {
           db[q] += dvt[q];
