@@ -145,7 +145,7 @@ template <typename T>
 ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *segin_user, char *ws,
                         const Workspace &w, cudaStream_t s) {
   const Problem pr = with_tables(pr_in, ws, w);
-  cudaMemsetAsync(ws + w.status, 0, sizeof(int), s);
+  cudaMemsetAsync(ws + w.status, 0, kStatusBytes, s);  // status word and work counters
   T *u = reinterpret_cast<T *>(ws + w.u);
   float *dtv = reinterpret_cast<float *>(ws + w.dtv), *acs = reinterpret_cast<float *>(ws + w.acs);
   float *cb = reinterpret_cast<float *>(ws + w.cb), *sst = reinterpret_cast<float *>(ws + w.sst);
@@ -181,7 +181,7 @@ template <typename T>
 ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal, const float *segin_user,
                          const ssd_grads *g, char *ws, const Workspace &w, cudaStream_t s) {
   const Problem pr = with_tables(pr_in, ws, w);
-  cudaMemsetAsync(ws + w.status, 0, sizeof(int), s);
+  cudaMemsetAsync(ws + w.status, 0, kStatusBytes, s);  // status word and work counters
   T *u = reinterpret_cast<T *>(ws + w.u);
   float *dtv = reinterpret_cast<float *>(ws + w.dtv), *acs = reinterpret_cast<float *>(ws + w.acs);
   float *cb = reinterpret_cast<float *>(ws + w.cb), *sst = reinterpret_cast<float *>(ws + w.sst);

@@ -68,11 +68,16 @@ __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return
 
 constexpr int kConvBwdTok = 32;  // tokens per conv-backward block (one set of parameter partials each)
 
+// The workspace starts with the device status word followed by one work
+// counter per persistent kernel (zeroed with the status at every pass).
+constexpr int kStatusBytes = 64;
+enum CounterSlot : int { kCounterOut = 1, kCounterRow = 2, kCounterCol = 3 };
+
 // ---------------------------------------------------------------- workspace
 // Offsets (bytes) of every scratch buffer; computed identically on host and
 // used to carve one caller-provided workspace.
 struct Workspace {
-  size_t status;                               // int32 device status word
+  size_t status;                               // int32 device status word, then the work counters
   size_t u;                                    // (b, L, Cd) act dtype: post-conv activations
   size_t dtv, acs;                             // (b, H, L) f32: dt, chunk-local cumsum of dt*A
   size_t cb;                                   // (b, nc, G, Q, Q) f32: C_i . B_j per chunk (CUDA-core path)

@@ -41,7 +41,7 @@ constexpr uint32_t kSmV = kSmDS + 16384;
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], g[256]}
 constexpr uint32_t kSmVC = kSmD + 2 * 2048;     // 2 x vcol partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVC + 2 * 2048;
-constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA;
+constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -52,10 +52,13 @@ struct Unit {
   int bb, c, J, h0;
 };
 
-// tiles with more columns (lower J) first; head blocks of one (row, chunk) adjacent
-__device__ __forceinline__ Unit unit_of(const Problem &pr, int nhb, int HB, int u) {
+// Unit u of the launch, claimed dynamically in this order: the tiles with more
+// work first (every CTA then ends on light ones), and within a tile class the
+// head blocks of one (row, chunk) adjacent, sharing C and B in L2.
+__device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int HB, int u) {
   const int per = pr.b * pr.nc * nhb;
   const int cls = u / per, r = u % per;
+  (void)NTI;
   Unit o;
   o.J = cls;
   const int hb = r % nhb, bc = r / nhb;
@@ -70,7 +73,8 @@ struct Bars {
   uint64_t *ring_full, *ring_free, *vec_full, *vec_free, *xt_full, *xt_free;  // [2]
   uint64_t *dy_full, *dy_free;                                                // [kNY]
   uint64_t *a_full, *a_free;                                                  // [kNA]
-  __device__ Bars(uint64_t *b) {
+  pipe::UnitRing units;
+  __device__ Bars(uint64_t *b, int *slot) {
     unit_full = b;
     unit_free = b + 1;
     tu_full = b + 2;
@@ -89,6 +93,9 @@ struct Bars {
     dy_free = dy_full + kNY;
     a_full = dy_free + kNY;
     a_free = a_full + kNA;
+    units.full = a_free + kNA;
+    units.free = units.full + 2;
+    units.slot = slot;
   }
 };
 
@@ -99,16 +106,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_ds, Problem pr, const bf16 *__restrict__ u,
                       const bf16 *__restrict__ dy, const float *__restrict__ dtv, const float *__restrict__ acs,
                       float *__restrict__ du, float *__restrict__ dbp, float *__restrict__ tok, int HB, int nunits,
-                      int *status) {
+                      int *counter, int *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = tc::aligned_smem(smem_raw);
-  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar));
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
+  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar), reinterpret_cast<int *>(tslot + 1));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NTI = pr.Q / 128, nhb = pr.H / HB, HP = pr.H * pr.P;
   const bool has_seq = pr.seq_idx != nullptr;
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
-  (void)NTI;
 
   if (threadIdx.x == 0) {
     uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.tu_full, bar.ds_full, bar.ds_free, bar.db_full};
@@ -131,6 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.a_full[i], kTWarps);
       mbar_init(&bar.a_free[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.units.full[i], 1);
+      mbar_init(&bar.units.free[i], 1 + kTWarps + kEWarps);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -149,8 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_dy);
       prefetch_tmap(&tm_ds);
       uint32_t nu = 0, nh = 0, m = 0, nd = 0;
-      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
-        const Unit o = unit_of(pr, nhb, HB, ui);
+      int next = atomicAdd(counter, 1);
+      for (;; ++nu) {
+        const int ui = pipe::publish_unit(bar.units, nu, next, nunits, status);
+        if (ui >= nunits) break;
+        next = atomicAdd(counter, 1);
+        const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, nsl = (pr.Q - 128 * o.J) / 64;
         const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N, rJ = row0 + 128 * o.J;
         if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
@@ -200,8 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_t = idesc_bf16(128, 64, false, true);      // M^T dy
       constexpr uint32_t id_db = idesc_bf16(128, 128, false, true);    // W^T C, (wdt x) dS
       uint32_t nu = 0, nh = 0, m = 0, na = 0, nd = 0;
-      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
-        const Unit o = unit_of(pr, nhb, HB, ui);
+      for (;; ++nu) {
+        const int ui = pipe::next_unit(bar.units, nu, nunits, status, false);
+        if (ui >= nunits) break;
+        const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int nsl = (pr.Q - 128 * o.J) / 64;
         mbar_wait(bar.unit_full, parity(nu), status);
         bool first_db = true;
@@ -322,8 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       pipe::warp_arrive(&bar.a_full[as]);
       ++na;
     };
-    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
-      const Unit o = unit_of(pr, nhb, HB, ui);
+    for (;; ++nu) {
+      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      if (ui >= nunits) break;
+      const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int j = 128 * o.J + jl, row_lo = 128 * o.J + 32 * q, row_hi = row_lo + 31;
       const int nsl = (pr.Q - 128 * o.J) / 64;
       int end_j = pr.Q - 1;
@@ -431,8 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, jl = 32 * q + lane;
     const uint32_t sV = smem_u32(sm + kSmV);
     uint32_t nu = 0, nh = 0;
-    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
-      const Unit o = unit_of(pr, nhb, HB, ui);
+    for (;; ++nu) {
+      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      if (ui >= nunits) break;
+      const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int j = 128 * o.J + jl, t = o.c * pr.Q + j;
       const bf16 *dyrow = dy + ((size_t)o.bb * pr.L + t) * HP;
       const bf16 *xrow = u + ((size_t)o.bb * pr.L + t) * pr.Cd;
@@ -516,8 +536,9 @@ void launch_tc_bwd_col(const Problem &pr, const bf16 *u, const bf16 *dy, const f
   const int HB = tc_head_subset(pr);
   const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
   const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
+  int *counter = status + kCounterCol;  // zeroed with the status word
   tc_bwd_col_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_ds, pr, u, dy, dtv, acs, du, dbp, tok, HB,
-                                                       nunits, status);
+                                                       nunits, counter, status);
 }
 
 }  // namespace ssd

@@ -45,7 +45,7 @@ constexpr uint32_t kSmV = kSmS + 16384;         // 2 vector buffers
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], b[256], f[256]}
 constexpr uint32_t kSmVR = kSmD + 2 * 3072;     // 2 x vrow partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVR + 2 * 2048;
-constexpr int kNumBars = 20 + 2 * kNX + 2 * kNA;
+constexpr int kNumBars = 20 + 2 * kNX + 2 * kNA + 4;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -56,7 +56,9 @@ struct Unit {
   int bb, c, I, h0;
 };
 
-// heavier tiles (higher I) first; head blocks of one (row, chunk) adjacent
+// Unit u of the launch, claimed dynamically in this order: the tiles with more
+// work first (every CTA then ends on light ones), and within a tile class the
+// head blocks of one (row, chunk) adjacent, sharing C and B in L2.
 __device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int HB, int u) {
   const int per = pr.b * pr.nc * nhb;
   const int cls = u / per, r = u % per;
@@ -75,7 +77,8 @@ struct Bars {
   uint64_t *vec_full, *vec_free, *dy_full, *dy_free;  // [2]
   uint64_t *x_full, *x_free;                          // [kNX]
   uint64_t *a_full, *a_free;                          // [kNA]
-  __device__ Bars(uint64_t *b) {
+  pipe::UnitRing units;
+  __device__ Bars(uint64_t *b, int *slot) {
     unit_full = b;
     unit_free = b + 1;
     cb_full = b + 2;
@@ -96,6 +99,9 @@ struct Bars {
     x_free = x_full + kNX;
     a_full = x_free + kNX;
     a_free = a_full + kNA;
+    units.full = a_free + kNA;
+    units.free = units.full + 2;
+    units.slot = slot;
   }
 };
 
@@ -105,11 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_row_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dy,
                       const __grid_constant__ CUtensorMap tm_s, Problem pr, const bf16 *__restrict__ dy,
                       const float *__restrict__ dtv, const float *__restrict__ acs, float *__restrict__ dcp,
-                      float *__restrict__ tok, int HB, int nunits, int *status) {
+                      float *__restrict__ tok, int HB, int nunits, int *counter, int *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = tc::aligned_smem(smem_raw);
-  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar));
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
+  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar), reinterpret_cast<int *>(tslot + 1));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NTI = pr.Q / 128, nhb = pr.H / HB, HP = pr.H * pr.P;
   const bool has_seq = pr.seq_idx != nullptr;
@@ -137,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.a_full[i], kTWarps);
       mbar_init(&bar.a_free[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.units.full[i], 1);
+      mbar_init(&bar.units.free[i], 1 + kTWarps + kEWarps);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -155,7 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_dy);
       prefetch_tmap(&tm_s);
       uint32_t nu = 0, nh = 0, k = 0, ns = 0;
-      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      int next = atomicAdd(counter, 1);
+      for (;; ++nu) {
+        const int ui = pipe::publish_unit(bar.units, nu, next, nunits, status);
+        if (ui >= nunits) break;
+        next = atomicAdd(counter, 1);
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, NB = 128 * (o.I + 1);
         const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N;
@@ -213,7 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_yo = idesc_bf16(128, 64, false, false);   // C_I S^T
       constexpr uint32_t id_dc = idesc_bf16(128, 128, false, true);   // W B_s, (em dy) S
       uint32_t nu = 0, nh = 0, k = 0, na = 0, ns = 0;
-      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      for (;; ++nu) {
+        const int ui = pipe::next_unit(bar.units, nu, nunits, status, false);
+        if (ui >= nunits) break;
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int NB = 128 * (o.I + 1), nsl = 2 * (o.I + 1);
         mbar_wait(bar.unit_full, parity(nu), status);
@@ -312,7 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tok[prev_tok] = (pipe::lds_f(base) + pipe::lds_f(base + 512)) + (pipe::lds_f(base + 1024) + pipe::lds_f(base + 1536));
       }
     };
-    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+    for (;; ++nu) {
+      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, row_lo = 128 * o.I + 32 * q, row_hi = row_lo + 31, nsl = 2 * (o.I + 1);
       int start_i = 0;
@@ -432,7 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, il = 32 * q + lane;
     const uint32_t sV = smem_u32(sm + kSmV);
     uint32_t nu = 0, nh = 0, ny = 0;
-    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+    for (;; ++nu) {
+      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, t = o.c * pr.Q + i;
       const bf16 *dyrow = dy + ((size_t)o.bb * pr.L + t) * HP;
@@ -507,8 +527,8 @@ void launch_tc_bwd_row(const Problem &pr, const bf16 *u, const bf16 *dy, const f
   const int HB = tc_head_subset(pr);
   const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
   const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
-  tc_bwd_row_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_s, pr, dy, dtv, acs, dcp, tok, HB, nunits,
-                                                       status);
+  int *counter = status + kCounterRow;  // zeroed with the status word
+  tc_bwd_row_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_s, pr, dy, dtv, acs, dcp, tok, HB, nunits, counter, status);
 }
 
 }  // namespace ssd

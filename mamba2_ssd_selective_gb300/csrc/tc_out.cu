@@ -25,7 +25,8 @@
 // b_j = log2(dt_j) - Acs_j log2(e).  The mask is the row's interval
 // [start_i, i], start_i the first token of i's sequence inside the chunk.
 // Accumulators are double-buffered, so the epilogue of head n overlaps the
-// transform and MMAs of head n+1; the A/X slice ring is kNS deep.
+// transform and MMAs of head n+1.  The X slices have their own ring, deep
+// enough to cover the TMA latency; the A slices only cross the SM.
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "tc_engine.cuh"
@@ -42,20 +43,21 @@ using pipe::parity;
 constexpr int kWarps = 22;
 constexpr int kEpiWarp0 = 18;
 constexpr int kThreads = kWarps * 32;
-constexpr int kNS = 4;   // A/X slice ring depth
+constexpr int kNA = 2;   // A slice ring (transform -> MMA, on chip)
+constexpr int kNX = 8;   // X slice ring (TMA -> MMA; deep enough to cover the load latency)
 constexpr int kNSB = 1;  // S_in buffers (a head of slack between load and use)
 
 // shared memory map, offsets from the 1024-aligned base
 constexpr uint32_t kSmC = 0;                     // C_I: 2 K halves x [128 rows x 128 B]
 constexpr uint32_t kSmB = kSmC + 2 * 16384;      // B rows: 2 K halves x [256 rows x 128 B]
 constexpr uint32_t kSmA = kSmB + 2 * 32768;      // ring of A slices [128 x 64] bf16, K-major
-constexpr uint32_t kSmX = kSmA + kNS * 16384;    // ring of X slices [64 tokens x 64] bf16, MN-major
-constexpr uint32_t kSmS = kSmX + kNS * 8192;     // kNSB x S_in,h: 2 K halves x [64 x 128 B]
+constexpr uint32_t kSmX = kSmA + kNA * 16384;    // ring of X slices [64 tokens x 64] bf16, MN-major
+constexpr uint32_t kSmS = kSmX + kNX * 8192;     // kNSB x S_in,h: 2 K halves x [64 x 128 B]
 constexpr uint32_t kVecStride = 3200;            // acs[256] f32 | dt[256] f32 | seq[4 + 256] i32
 constexpr uint32_t kSmV = kSmS + kNSB * 16384;   // 2 vector buffers
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;   // 2 x {a[256], b[256], f[256]} f32 (decay tables per head)
 constexpr uint32_t kSmBar = kSmD + 2 * 3072;
-constexpr int kNumBars = 9 + 3 * kNS + 8;
+constexpr int kNumBars = 9 + 2 * kNA + 2 * kNX + 8 + 4;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -64,9 +66,9 @@ struct Unit {
   int bb, c, I, h0;
 };
 
-// Unit u of the launch.  Row tiles with more work (higher I) come first, so a
-// round-robin assignment gives every CTA the same mix; inside a class the head
-// blocks of one (row, chunk) are adjacent and share C/B in L2.
+// Unit u of the launch, claimed dynamically in this order: the tiles with more
+// work first (every CTA then ends on light ones), and within a tile class the
+// head blocks of one (row, chunk) adjacent, sharing C and B in L2.
 __device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int HB, int u) {
   const int per = pr.b * pr.nc * nhb;
   const int cls = u / per, r = u % per;
@@ -82,10 +84,12 @@ __device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int
 struct Bars {
   uint64_t *unit_full, *b_free, *c_free, *cb_full, *cb_used;
   uint64_t *vec_full, *vec_free;             // [2]
-  uint64_t *a_full, *x_full, *slot_free;     // [kNS]
+  uint64_t *a_full, *a_free;                 // [kNA]
+  uint64_t *x_full, *x_free;                 // [kNX]
   uint64_t *s_full, *s_free;                 // [2]
   uint64_t *acc_full, *acc_free;             // [2]
-  __device__ Bars(uint64_t *b) {
+  pipe::UnitRing units;
+  __device__ Bars(uint64_t *b, int *slot) {
     unit_full = b;
     b_free = b + 1;
     c_free = b + 2;
@@ -94,12 +98,16 @@ struct Bars {
     vec_full = b + 5;
     vec_free = b + 7;
     a_full = b + 9;
-    x_full = a_full + kNS;
-    slot_free = x_full + kNS;
-    s_full = slot_free + kNS;
+    a_free = a_full + kNA;
+    x_full = a_free + kNA;
+    x_free = x_full + kNX;
+    s_full = x_free + kNX;
     s_free = s_full + 2;
     acc_full = s_free + 2;
     acc_free = acc_full + 2;
+    units.full = acc_free + 2;
+    units.free = units.full + 2;
+    units.slot = slot;
   }
 };
 
@@ -112,11 +120,11 @@ constexpr int kTransformWarps = 16, kEpilogueWarps = 4;
 __global__ void __launch_bounds__(kThreads, 1)
     tc_out_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_s, Problem pr,
                   const bf16 *__restrict__ u, const float *__restrict__ dtv, const float *__restrict__ acs,
-                  bf16 *__restrict__ y, int HB, int nunits, int *status) {
+                  bf16 *__restrict__ y, int HB, int nunits, int *counter, int *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = tc::aligned_smem(smem_raw);
-  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar));
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
+  Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar), reinterpret_cast<int *>(tslot + 1));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NTI = pr.Q / 128, nhb = pr.H / HB, HP = pr.H * pr.P, Cd = pr.Cd;
   const bool has_seq = pr.seq_idx != nullptr;
@@ -135,10 +143,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.acc_full[i], 1);
       mbar_init(&bar.acc_free[i], kEpilogueWarps);
     }
-    for (int i = 0; i < kNS; ++i) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.units.full[i], 1);
+      mbar_init(&bar.units.free[i], 1 + kTransformWarps + kEpilogueWarps);
+    }
+    for (int i = 0; i < kNA; ++i) {
       mbar_init(&bar.a_full[i], kTransformWarps);
+      mbar_init(&bar.a_free[i], 1);
+    }
+    for (int i = 0; i < kNX; ++i) {
       mbar_init(&bar.x_full[i], 1);
-      mbar_init(&bar.slot_free[i], 1);
+      mbar_init(&bar.x_free[i], 1);
     }
     fence_mbar_init();
   }
@@ -157,7 +172,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_u);
       prefetch_tmap(&tm_s);
       uint32_t nu = 0, nh = 0, ns = 0, k = 0;
-      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      int next = atomicAdd(counter, 1);
+      for (;; ++nu) {
+        const int ui = pipe::publish_unit(bar.units, nu, next, nunits, status);
+        if (ui >= nunits) break;
+        next = atomicAdd(counter, 1);
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, NB = 128 * (o.I + 1);
         const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N;
@@ -188,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
           }
           for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
-            const int slot = k % kNS;
-            if (k >= kNS) mbar_wait(&bar.slot_free[slot], parity(k / kNS - 1), status);
+            const int slot = k % kNX;
+            if (k >= kNX) mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status);
             mbar_expect_tx(&bar.x_full[slot], 8192);
             tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
           }
@@ -213,7 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_off = idesc_bf16(128, 64, false, false);
       uint32_t nu = 0, nh = 0, ns = 0, k = 0;
-      for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+      for (;; ++nu) {
+        const int ui = pipe::next_unit(bar.units, nu, nunits, status, false);
+        if (ui >= nunits) break;
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int NB = 128 * (o.I + 1);
         mbar_wait(bar.unit_full, parity(nu), status);
@@ -233,15 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nh >= 2) mbar_wait(&bar.acc_free[ab], parity(nh / 2 - 1), status);
           tc_fence_after();
           for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
-            const int slot = k % kNS;
-            mbar_wait(&bar.a_full[slot], parity(k / kNS), status);
-            mbar_wait(&bar.x_full[slot], parity(k / kNS), status);
+            const int as = k % kNA, xs = k % kNX;
+            mbar_wait(&bar.a_full[as], parity(k / kNA), status);
+            mbar_wait(&bar.x_full[xs], parity(k / kNX), status);
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tacc, desc_sw128(sA + slot * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sX + slot * 8192 + kk * 2048, 8192, 1024), id_acc, (s | kk) ? 1u : 0u);
-            umma_commit(&bar.slot_free[slot]);
+              umma_bf16(tacc, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
+                        desc_sw128(sX + xs * 8192 + kk * 2048, 8192, 1024), id_acc, (s | kk) ? 1u : 0u);
+            umma_commit(&bar.a_free[as]);
+            umma_commit(&bar.x_free[xs]);
           }
           if (o.c > 0) {
             const int sb = ns % kNSB;
@@ -265,8 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar.b_free, parity(nu - 1), status);
         mbar_wait(bar.c_free, parity(nu - 1), status);
       }
-      for (uint32_t m = k > (uint32_t)kNS ? k - kNS : 0u; m < k; ++m)
-        mbar_wait(&bar.slot_free[m % kNS], parity(m / kNS), status);
+      for (uint32_t m = k > (uint32_t)kNA ? k - kNA : 0u; m < k; ++m)
+        mbar_wait(&bar.a_free[m % kNA], parity(m / kNA), status);
+      for (uint32_t m = k > (uint32_t)kNX ? k - kNX : 0u; m < k; ++m)
+        mbar_wait(&bar.x_free[m % kNX], parity(m / kNX), status);
       for (uint32_t m = ns > (uint32_t)kNSB ? ns - kNSB : 0u; m < ns; ++m)
         mbar_wait(&bar.s_free[m % kNSB], parity(m / kNSB), status);
     }
@@ -276,7 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sA = smem_u32(sm + kSmA), sV = smem_u32(sm + kSmV), sD = smem_u32(sm + kSmD);
     const float kLog2e = 1.4426950408889634f;
     uint32_t nu = 0, nh = 0, k = 0;
-    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x, ++nu) {
+    for (;; ++nu) {
+      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, row_lo = 128 * o.I + 32 * q, row_hi = row_lo + 31;
       int start_i = 0;
@@ -303,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, %0;" ::"n"(kTransformThreads) : "memory");
         const float ai = pipe::lds_f(da + 4 * i);
         for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
-          const int slot = k % kNS;
-          if (k >= kNS) mbar_wait(&bar.slot_free[slot], parity(k / kNS - 1), status);
+          const int slot = k % kNA;
+          if (k >= kNA) mbar_wait(&bar.a_free[slot], parity(k / kNA - 1), status);
           const int j0 = 64 * s + 16 * cg;
           uint4 pk[2];
           if (j0 > row_hi) {
@@ -362,7 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, il = 32 * q + lane;
     const uint32_t sV = smem_u32(sm + kSmV);
     uint32_t nh = 0;
-    for (int ui = blockIdx.x; ui < nunits; ui += gridDim.x) {
+    for (uint32_t nu = 0;; ++nu) {
+      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, t = o.c * pr.Q + i;
       const bool has_off = o.c > 0;
@@ -376,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float em = (has_off && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
         pipe::warp_arrive(&bar.vec_free[vb]);
         const float Dh = __ldg(pr.D + h);
+        // x row first: its loads are in flight while the accumulators finish
+        uint4 xr[8];
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) xr[q8] = tc::ldg16(xrow + h * pr.P + 8 * q8);
         mbar_wait(&bar.acc_full[ab], parity(nh / 2), status);
         tc_fence_after();
         const uint32_t tacc = tmem + 256 + 128 * ab;
@@ -387,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q8 = 0; q8 < 2; ++q8) {
             float x[8], o8[8];
-            tc::unpack8(tc::ldg16(xrow + h * pr.P + 16 * cc + 8 * q8), x);
+            tc::unpack8(xr[2 * cc + q8], x);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int col = 8 * q8 + e;
@@ -412,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, const bf16 *sin16, bf16 *y,
                    int *status, cudaStream_t s) {
+  int *counter = status + kCounterOut;  // zeroed with the status word
   static bool once = (cudaFuncSetAttribute(tc_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
                       true);
   (void)once;
@@ -424,7 +457,7 @@ void launch_tc_out(const Problem &pr, const bf16 *u, const float *dtv, const flo
   const int HB = tc_head_subset(pr);
   const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
   const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
-  tc_out_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_s, pr, u, dtv, acs, y, HB, nunits, status);
+  tc_out_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_s, pr, u, dtv, acs, y, HB, nunits, counter, status);
 }
 
 }  // namespace ssd
