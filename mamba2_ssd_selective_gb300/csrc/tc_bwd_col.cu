@@ -208,8 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sBJ = smem_u32(sm + kSmBJ), sCR = smem_u32(sm + kSmCR), sXT = smem_u32(sm + kSmXT),
-                     sDY = smem_u32(sm + kSmDY), sA = smem_u32(sm + kSmA), sDS = smem_u32(sm + kSmDS);
+      // operand descriptors, built once; ring slots and K steps are additions
+      const uint64_t dBJ = desc_sw128(smem_u32(sm + kSmBJ), 16, 1024), dCR = desc_sw128(smem_u32(sm + kSmCR), 16, 1024),
+                     dCRmn = desc_sw128(smem_u32(sm + kSmCR), 32768, 1024),
+                     dXT = desc_sw128(smem_u32(sm + kSmXT), 16, 1024), dDY = desc_sw128(smem_u32(sm + kSmDY), 16, 1024),
+                     dDYmn = desc_sw128(smem_u32(sm + kSmDY), 8192, 1024), dA = desc_sw128(smem_u32(sm + kSmA), 16, 1024),
+                     dDS = desc_sw128(smem_u32(sm + kSmDS), 16, 1024), dDSmn = desc_sw128(smem_u32(sm + kSmDS), 8192, 1024);
       constexpr uint32_t id_64 = idesc_bf16(128, 64, false, false);    // x dy^T, B_J C^T, B_J dS^T
       constexpr uint32_t id_t = idesc_bf16(128, 64, false, true);      // M^T dy
       constexpr uint32_t id_db = idesc_bf16(128, 128, false, true);    // W^T C, (wdt x) dS
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first_db = true;
         for (int hh = 0; hh < HB; ++hh, ++nh) {
           const int vb = nh & 1;
-          const uint32_t sxt = sXT + vb * 16384;
+          const uint64_t dxt = dXT + vb * (16384 / 16);
           mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);
           // slice item n: dM^T and CB^T of columns [64 s, 64 s + 64) into ring slot n % 2
           auto issue_item = [&](uint32_t n, int s) {
@@ -232,15 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.dy_full[ys], parity(n / kNY), status);
             tc_fence_after();
             const uint32_t td = tmem + 128 * rs;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(td, desc_sw128(sxt + kk * 32, 16, 1024), desc_sw128(sDY + ys * 8192 + kk * 32, 16, 1024),
-                        id_64, kk > 0 ? 1u : 0u);
-            for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(td + 64, desc_sw128(sBJ + kh * 16384 + kk * 32, 16, 1024),
-                          desc_sw128(sCR + kh * 32768 + 8192 * s + kk * 32, 16, 1024), id_64, (kh | kk) ? 1u : 0u);
+            pipe::umma_k<4>(td, dxt, dDY + ys * (8192 / 16), pipe::kStepK, pipe::kStepK, id_64, false);
+            const uint64_t dcs = dCR + s * (8192 / 16);
+            pipe::umma_k<4>(td + 64, dBJ, dcs, pipe::kStepK, pipe::kStepK, id_64, false);
+            pipe::umma_k<4>(td + 64, dBJ + 16384 / 16, dcs + 32768 / 16, pipe::kStepK, pipe::kStepK, id_64, true);
             umma_commit(&bar.ring_full[rs]);
           };
           issue_item(m, 0);
@@ -252,10 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             if (s == 0 && nh > 0) mbar_wait(bar.tu_free, parity(nh - 1), status);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + kTmT, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sDY + ys * 8192 + kk * 2048, 8192, 1024), id_t, (s | kk) ? 1u : 0u);
+            pipe::umma_k<4>(tmem + kTmT, dA + as * (16384 / 16), dDYmn + ys * (8192 / 16), pipe::kStepK, pipe::kStepMN,
+                            id_t, s > 0);
             umma_commit(&bar.a_free[as]);
             umma_commit(&bar.dy_free[ys]);
             ++na;
@@ -264,10 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             if (first_db && nu > 0) mbar_wait(bar.db_free, parity(nu - 1), status);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + kTmDB, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sCR + 8192 * s + kk * 2048, 32768, 1024), id_db, (first_db && kk == 0) ? 0u : 1u);
+            pipe::umma_k<4>(tmem + kTmDB, dA + as * (16384 / 16), dCRmn + s * (8192 / 16), pipe::kStepK, pipe::kStepMN,
+                            id_db, !first_db);
             first_db = false;
             umma_commit(&bar.a_free[as]);
             ++na;
@@ -276,19 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // U = B_J dS^T, and dB += (wdt x) dS
           mbar_wait(bar.ds_full, parity(nd), status);
           tc_fence_after();
-          for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + kTmU, desc_sw128(sBJ + kh * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sDS + kh * 8192 + kk * 32, 16, 1024), id_64, (kh | kk) ? 1u : 0u);
+          pipe::umma_k<4>(tmem + kTmU, dBJ, dDS, pipe::kStepK, pipe::kStepK, id_64, false);
+          pipe::umma_k<4>(tmem + kTmU, dBJ + 16384 / 16, dDS + 8192 / 16, pipe::kStepK, pipe::kStepK, id_64, true);
           umma_commit(bar.tu_full);
           const int as = na % kNA;
           mbar_wait(&bar.a_full[as], parity(na / kNA), status);
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + kTmDB, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
-                      desc_sw128(sDS + kk * 2048, 8192, 1024), id_db, 1u);
+          pipe::umma_k<4>(tmem + kTmDB, dA + as * (16384 / 16), dDSmn, pipe::kStepK, pipe::kStepMN, id_db, true);
           umma_commit(&bar.a_free[as]);
           ++na;
           umma_commit(bar.ds_free);

@@ -221,8 +221,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sC = smem_u32(sm + kSmC), sB = smem_u32(sm + kSmB), sDY = smem_u32(sm + kSmDY),
-                     sX = smem_u32(sm + kSmX), sA = smem_u32(sm + kSmA), sS = smem_u32(sm + kSmS);
+      // operand descriptors, built once; ring slots and K steps are additions
+      const uint64_t dC = desc_sw128(smem_u32(sm + kSmC), 16, 1024), dB = desc_sw128(smem_u32(sm + kSmB), 16, 1024),
+                     dBmn = desc_sw128(smem_u32(sm + kSmB), 32768, 1024),
+                     dDY = desc_sw128(smem_u32(sm + kSmDY), 16, 1024), dX = desc_sw128(smem_u32(sm + kSmX), 16, 1024),
+                     dA = desc_sw128(smem_u32(sm + kSmA), 16, 1024), dS = desc_sw128(smem_u32(sm + kSmS), 16, 1024),
+                     dSmn = desc_sw128(smem_u32(sm + kSmS), 8192, 1024);
       constexpr uint32_t id_dm = idesc_bf16(128, 64, false, false);   // dy_I x_s^T
       constexpr uint32_t id_yo = idesc_bf16(128, 64, false, false);   // C_I S^T
       constexpr uint32_t id_dc = idesc_bf16(128, 128, false, true);   // W B_s, (em dy) S
@@ -236,16 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nu > 0) mbar_wait(bar.cb_used, parity(nu - 1), status);
         tc_fence_after();
         const uint32_t id_cb = idesc_bf16(128, NB, false, false);
-        for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, desc_sw128(sC + kh * 16384 + kk * 32, 16, 1024),
-                      desc_sw128(sB + kh * 32768 + kk * 32, 16, 1024), id_cb, (kh | kk) ? 1u : 0u);
+        pipe::umma_k<4>(tmem, dC, dB, pipe::kStepK, pipe::kStepK, id_cb, false);
+        pipe::umma_k<4>(tmem, dC + 16384 / 16, dB + 32768 / 16, pipe::kStepK, pipe::kStepK, id_cb, true);
         umma_commit(bar.cb_full);
         bool first_dc = true;
         for (int hh = 0; hh < HB; ++hh, ++nh) {
           const int vb = nh & 1;
-          const uint32_t sdy = sDY + vb * 16384;
+          const uint64_t ddy = dDY + vb * (16384 / 16);
           mbar_wait(&bar.dy_full[vb], parity(nh / 2), status);
           // dM slice m of this head into the single dM slot (after the
           // transform has read the previous one)
@@ -254,10 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.x_full[slot], parity(m / kNX), status);
             if (m > 0) mbar_wait(bar.dm_free, parity(m - 1), status);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + kTmDM, desc_sw128(sdy + kk * 32, 16, 1024),
-                        desc_sw128(sX + slot * 8192 + kk * 32, 16, 1024), id_dm, kk > 0 ? 1u : 0u);
+            pipe::umma_k<4>(tmem + kTmDM, ddy, dX + slot * (8192 / 16), pipe::kStepK, pipe::kStepK, id_dm, false);
             umma_commit(&bar.x_free[slot]);
             umma_commit(bar.dm_full);
           };
@@ -268,10 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             if (first_dc && nu > 0) mbar_wait(bar.dc_free, parity(nu - 1), status);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + kTmDC, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sB + 8192 * s + kk * 2048, 32768, 1024), id_dc, (first_dc && kk == 0) ? 0u : 1u);
+            pipe::umma_k<4>(tmem + kTmDC, dA + as * (16384 / 16), dBmn + s * (8192 / 16), pipe::kStepK, pipe::kStepMN,
+                            id_dc, !first_dc);
             first_dc = false;
             umma_commit(&bar.a_free[as]);
             ++na;
@@ -281,19 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bar.s_full, parity(ns), status);
             if (ns > 0) mbar_wait(bar.yo_free, parity(ns - 1), status);
             tc_fence_after();
-            for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(tmem + kTmYo, desc_sw128(sC + kh * 16384 + kk * 32, 16, 1024),
-                          desc_sw128(sS + kh * 8192 + kk * 32, 16, 1024), id_yo, (kh | kk) ? 1u : 0u);
+            pipe::umma_k<4>(tmem + kTmYo, dC, dS, pipe::kStepK, pipe::kStepK, id_yo, false);
+            pipe::umma_k<4>(tmem + kTmYo, dC + 16384 / 16, dS + 8192 / 16, pipe::kStepK, pipe::kStepK, id_yo, true);
             umma_commit(bar.yo_full);
             const int as = na % kNA;
             mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + kTmDC, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sS + kk * 2048, 8192, 1024), id_dc, 1u);
+            pipe::umma_k<4>(tmem + kTmDC, dA + as * (16384 / 16), dSmn, pipe::kStepK, pipe::kStepMN, id_dc, true);
             umma_commit(&bar.a_free[as]);
             ++na;
             umma_commit(bar.s_free);

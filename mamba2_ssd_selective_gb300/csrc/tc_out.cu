@@ -227,8 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sC = smem_u32(sm + kSmC), sB = smem_u32(sm + kSmB), sA = smem_u32(sm + kSmA),
-                     sX = smem_u32(sm + kSmX), sS = smem_u32(sm + kSmS);
+      // operand descriptors, built once; ring slots and K steps are additions
+      const uint64_t dC = desc_sw128(smem_u32(sm + kSmC), 16, 1024), dB = desc_sw128(smem_u32(sm + kSmB), 16, 1024),
+                     dA = desc_sw128(smem_u32(sm + kSmA), 16, 1024), dX = desc_sw128(smem_u32(sm + kSmX), 8192, 1024),
+                     dS = desc_sw128(smem_u32(sm + kSmS), 16, 1024);
       constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_off = idesc_bf16(128, 64, false, false);
       uint32_t nu = 0, nh = 0, ns = 0, k = 0;
@@ -241,11 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nu > 0) mbar_wait(bar.cb_used, parity(nu - 1), status);
         tc_fence_after();
         const uint32_t id_cb = idesc_bf16(128, NB, false, false);
-        for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, desc_sw128(sC + kh * 16384 + kk * 32, 16, 1024),
-                      desc_sw128(sB + kh * 32768 + kk * 32, 16, 1024), id_cb, (kh | kk) ? 1u : 0u);
+        pipe::umma_k<4>(tmem, dC, dB, pipe::kStepK, pipe::kStepK, id_cb, false);
+        pipe::umma_k<4>(tmem, dC + 16384 / 16, dB + 32768 / 16, pipe::kStepK, pipe::kStepK, id_cb, true);
         umma_commit(bar.cb_full);
         umma_commit(bar.b_free);
         for (int hh = 0; hh < HB; ++hh, ++nh) {
@@ -258,10 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.a_full[as], parity(k / kNA), status);
             mbar_wait(&bar.x_full[xs], parity(k / kNX), status);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tacc, desc_sw128(sA + as * 16384 + kk * 32, 16, 1024),
-                        desc_sw128(sX + xs * 8192 + kk * 2048, 8192, 1024), id_acc, (s | kk) ? 1u : 0u);
+            pipe::umma_k<4>(tacc, dA + as * (16384 / 16), dX + xs * (8192 / 16), pipe::kStepK, pipe::kStepMN, id_acc,
+                            s > 0);
             umma_commit(&bar.a_free[as]);
             umma_commit(&bar.x_free[xs]);
           }
@@ -269,11 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sb = ns % kNSB;
             mbar_wait(&bar.s_full[sb], parity(ns / kNSB), status);
             tc_fence_after();
-            for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(tacc + 64, desc_sw128(sC + kh * 16384 + kk * 32, 16, 1024),
-                          desc_sw128(sS + sb * 16384 + kh * 8192 + kk * 32, 16, 1024), id_off, (kh | kk) ? 1u : 0u);
+            const uint64_t dSb = dS + sb * (16384 / 16);
+            pipe::umma_k<4>(tacc + 64, dC, dSb, pipe::kStepK, pipe::kStepK, id_off, false);
+            pipe::umma_k<4>(tacc + 64, dC + 16384 / 16, dSb + 8192 / 16, pipe::kStepK, pipe::kStepK, id_off, true);
             umma_commit(&bar.s_free[sb]);
             ++ns;
           }

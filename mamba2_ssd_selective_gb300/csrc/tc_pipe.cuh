@@ -113,6 +113,20 @@ __device__ __forceinline__ int next_unit(const UnitRing &r, uint32_t n, int stop
   return u;
 }
 
+// MMA issue with precomputed descriptors.  A 128-byte-swizzled descriptor's
+// start address (16-byte units, bits 0-13) advances by a constant per K step
+// of 16 elements: 2 for a K-major operand (32 bytes), 128 for an MN-major one
+// (16 rows of 128 bytes).  Shared addresses stay below 2^18, so the field never
+// carries.  D (+)= A B over K = 16 * NK, issued by the calling thread.
+constexpr uint64_t kStepK = 2, kStepMN = 128;
+template <int NK>
+__device__ __forceinline__ void umma_k(uint32_t d, uint64_t a, uint64_t b, uint64_t sa, uint64_t sb, uint32_t idesc,
+                                       bool accumulate) {
+  umma_bf16(d, a, b, idesc, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < NK; ++kk) umma_bf16(d, a + kk * sa, b + kk * sb, idesc, 1u);
+}
+
 // TMEM address of (lane quadrant of this warp, column col)
 __device__ __forceinline__ uint32_t tmem_quad(uint32_t base, int col) {
   return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
