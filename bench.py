@@ -239,7 +239,8 @@ def step_totals(kt: list, shape, dtype: str, ms_per_step: float, peaks: dict) ->
 def committed_traffic(kernel: str, shape):
     """DRAM bytes per launch from the committed ncu summary, scaled from the
     captured batch to this workload's batch, if it was taken on the current
-    source of the kernel's file; otherwise None."""
+    sources of the kernel (its file and the headers it is built from);
+    otherwise None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -248,12 +249,15 @@ def committed_traffic(kernel: str, shape):
     e = d.get(kernel)
     if not e:
         return None
-    src = os.path.join(ROOT, e["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as fh:
-        if hashlib.sha256(fh.read()).hexdigest() != e["source_sha256"]:
+    h = hashlib.sha256()
+    for rel in e["sources"]:
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
             return None
+        with open(src, "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != e["sources_sha256"]:
+        return None
     return int(e["dram_bytes_per_launch"] * shape.batch / e.get("captured_batch", shape.batch))
 
 
