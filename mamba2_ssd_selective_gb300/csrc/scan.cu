@@ -15,7 +15,7 @@
 
 namespace ssd {
 
-constexpr int kScanBatch = 8;  // chunks whose loads are in flight together
+constexpr int kScanBatch = 4;  // chunks whose loads are in flight together
 
 // Decay tables of one (b, h): cdec[c] = product of the chunk's per-token decays
 // (from Acs and seq_idx), then per segment the exclusive prefix and suffix
@@ -81,49 +81,66 @@ void launch_combine_state(const Problem &pr, const float *a, const float *seg, _
 // Local pass of segment k: S <- a_c * S + Sc[c] over the segment's chunks from
 // S = 0.  Overwrites sst[c] (the chunk's own state contribution Sc) with the
 // local state entering the chunk, and writes S_ext[k] and a_block[k].  Each
-// thread owns 4 consecutive state elements (16-byte accesses) and keeps the
-// loads of kScanBatch chunks in flight; the chunk decays of a batch are
-// computed once per block.
+// thread owns two 16-byte groups of state elements (kScanVec4 float4, one per
+// 256-thread stride, so every warp access stays contiguous), reads the chunk
+// decays itself (the same address for the whole block: one broadcast line) and
+// keeps the loads of kScanBatch chunks in flight.  No barriers.
+constexpr int kScanVec4 = 2;
+constexpr int kScanElems4 = 256 * kScanVec4;  // float4 groups per block
+
 __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float *__restrict__ acs,
                                                          float *__restrict__ sst, float *__restrict__ sext,
                                                          float *__restrict__ ablk) {
-  __shared__ float dec[kScanBatch];
   const int PN = pr.P * pr.N, PN4 = PN / 4;
-  const int e4 = blockIdx.x * 256 + threadIdx.x;
-  const bool active = e4 < PN4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
-  const size_t cstride = (size_t)pr.H * PN;  // floats between consecutive chunks
-  float4 *base = reinterpret_cast<float4 *>(sst + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN) + e4;
-  float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
+  const size_t cstride4 = (size_t)pr.H * PN / 4;  // float4 between consecutive chunks
+  float4 *base = reinterpret_cast<float4 *>(sst + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN);
+  int e4[kScanVec4];
+  float4 S[kScanVec4];
+#pragma unroll
+  for (int u = 0; u < kScanVec4; ++u) {
+    e4[u] = blockIdx.x * kScanElems4 + u * 256 + threadIdx.x;
+    S[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float prod = 1.f;
   for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
     const int nb = min(kScanBatch, pr.cps - c0);
-    __syncthreads();
-    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, bb, h, k * pr.cps + c0 + threadIdx.x);
-    __syncthreads();
-    if (threadIdx.x == 0)
-      for (int q = 0; q < nb; ++q) prod *= dec[q];
-    if (active) {
-      float4 v[kScanBatch];
+    float dec[kScanBatch];
+    float4 v[kScanBatch][kScanVec4];
 #pragma unroll
-      for (int q = 0; q < kScanBatch; ++q)
-        if (q < nb) v[q] = base[(size_t)(c0 + q) * (cstride / 4)];
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q < nb) {
+        dec[q] = chunk_decay(pr, bb, h, k * pr.cps + c0 + q);
 #pragma unroll
-      for (int q = 0; q < kScanBatch; ++q)
-        if (q < nb) {
-          base[(size_t)(c0 + q) * (cstride / 4)] = S;
-          const float a = dec[q];
-          S = make_float4(fmaf(a, S.x, v[q].x), fmaf(a, S.y, v[q].y), fmaf(a, S.z, v[q].z), fmaf(a, S.w, v[q].w));
+        for (int u = 0; u < kScanVec4; ++u)
+          if (e4[u] < PN4) v[q][u] = base[(size_t)(c0 + q) * cstride4 + e4[u]];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q < nb) {
+        const float a = dec[q];
+        prod *= a;
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u) {
+          if (e4[u] < PN4) {
+            base[(size_t)(c0 + q) * cstride4 + e4[u]] = S[u];
+            S[u] = make_float4(fmaf(a, S[u].x, v[q][u].x), fmaf(a, S[u].y, v[q][u].y), fmaf(a, S[u].z, v[q][u].z),
+                               fmaf(a, S[u].w, v[q][u].w));
+          }
         }
+      }
     }
   }
   const size_t so = (((size_t)bb * pr.S + k) * pr.H + h);
-  if (active) reinterpret_cast<float4 *>(sext + so * PN)[e4] = S;
+#pragma unroll
+  for (int u = 0; u < kScanVec4; ++u)
+    if (e4[u] < PN4) reinterpret_cast<float4 *>(sext + so * PN)[e4[u]] = S[u];
   if (blockIdx.x == 0 && threadIdx.x == 0) ablk[so] = prod;
 }
 
 void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s) {
-  dim3 grid((pr.P * pr.N / 4 + 255) / 256, pr.H, pr.b * pr.S);
+  dim3 grid((pr.P * pr.N / 4 + kScanElems4 - 1) / kScanElems4, pr.H, pr.b * pr.S);
   local_pass_kernel<<<grid, 256, 0, s>>>(pr, acs, sst, sext, ablk);
 }
 
@@ -159,40 +176,53 @@ void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, fl
 // Same access pattern as local_pass_kernel, walking the chunks backwards.
 __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float *__restrict__ acs,
                                                         float *__restrict__ dsl, float *__restrict__ gext) {
-  __shared__ float dec[kScanBatch];
   const int PN = pr.P * pr.N, PN4 = PN / 4;
-  const int e4 = blockIdx.x * 256 + threadIdx.x;
-  const bool active = e4 < PN4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
   const size_t cstride4 = (size_t)pr.H * PN / 4;
-  float4 *base = reinterpret_cast<float4 *>(dsl + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN) + e4;
-  float4 dS = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 *base = reinterpret_cast<float4 *>(dsl + (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN);
+  int e4[kScanVec4];
+  float4 dS[kScanVec4];
+#pragma unroll
+  for (int u = 0; u < kScanVec4; ++u) {
+    e4[u] = blockIdx.x * kScanElems4 + u * 256 + threadIdx.x;
+    dS[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int c1 = pr.cps; c1 > 0; c1 -= kScanBatch) {
     const int nb = min(kScanBatch, c1);
     const int c0 = c1 - nb;  // this batch covers chunks [c0, c1) of the segment, walked downwards
-    __syncthreads();
-    if (threadIdx.x < nb) dec[threadIdx.x] = chunk_decay(pr, bb, h, k * pr.cps + c0 + threadIdx.x);
-    __syncthreads();
-    if (active) {
-      float4 z[kScanBatch];
+    float dec[kScanBatch];
+    float4 z[kScanBatch][kScanVec4];
 #pragma unroll
-      for (int q = 0; q < kScanBatch; ++q)
-        if (q < nb) z[q] = base[(size_t)(c0 + q) * cstride4];
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q < nb) {
+        dec[q] = chunk_decay(pr, bb, h, k * pr.cps + c0 + q);
 #pragma unroll
-      for (int q = kScanBatch - 1; q >= 0; --q)
-        if (q < nb) {
-          base[(size_t)(c0 + q) * cstride4] = dS;
-          const float a = dec[q];
-          dS = make_float4(fmaf(a, dS.x, z[q].x), fmaf(a, dS.y, z[q].y), fmaf(a, dS.z, z[q].z),
-                           fmaf(a, dS.w, z[q].w));
+        for (int u = 0; u < kScanVec4; ++u)
+          if (e4[u] < PN4) z[q][u] = base[(size_t)(c0 + q) * cstride4 + e4[u]];
+      }
+    }
+#pragma unroll
+    for (int q = kScanBatch - 1; q >= 0; --q) {
+      if (q < nb) {
+        const float a = dec[q];
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u) {
+          if (e4[u] < PN4) {
+            base[(size_t)(c0 + q) * cstride4 + e4[u]] = dS[u];
+            dS[u] = make_float4(fmaf(a, dS[u].x, z[q][u].x), fmaf(a, dS[u].y, z[q][u].y),
+                                fmaf(a, dS[u].z, z[q][u].z), fmaf(a, dS[u].w, z[q][u].w));
+          }
         }
+      }
     }
   }
-  if (active) reinterpret_cast<float4 *>(gext + (((size_t)bb * pr.S + k) * pr.H + h) * PN)[e4] = dS;
+#pragma unroll
+  for (int u = 0; u < kScanVec4; ++u)
+    if (e4[u] < PN4) reinterpret_cast<float4 *>(gext + (((size_t)bb * pr.S + k) * pr.H + h) * PN)[e4[u]] = dS[u];
 }
 
 void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s) {
-  dim3 grid((pr.P * pr.N / 4 + 255) / 256, pr.H, pr.b * pr.S);
+  dim3 grid((pr.P * pr.N / 4 + kScanElems4 - 1) / kScanElems4, pr.H, pr.b * pr.S);
   local_rev_kernel<<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
 }
 
