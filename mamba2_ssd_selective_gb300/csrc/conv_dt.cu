@@ -44,7 +44,6 @@ __device__ __forceinline__ void grad_channel(const Problem &pr, const GradOut &g
   base = p;
 }
 
-constexpr int kConvTok = 32;
 
 // 8 consecutive channels of one token as fp32 (16-byte loads for bf16)
 template <typename T> __device__ __forceinline__ void load8(const T *p, float (&v)[8]);
@@ -76,6 +75,14 @@ template <> __device__ __forceinline__ void store8<float>(float *p, const float 
   reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// 2 consecutive channels
+__device__ __forceinline__ void store2(__nv_bfloat16 *p, const float (&v)[2]) {
+  *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v[0], v[1]);
+}
+__device__ __forceinline__ void store2(float *p, const float (&v)[2]) {
+  *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+}
+
 // 4 consecutive channels (8-byte loads for bf16)
 template <typename T> __device__ __forceinline__ void load4(const T *p, float (&v)[4]);
 template <> __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[4]) {
@@ -97,53 +104,86 @@ template <> __device__ __forceinline__ void store4<float>(float *p, const float 
 }
 
 // u[b, t, c] = silu(conv_b[c] + sum_k w[c,k] * xr[t-3+k, c]), taps masked at row
-// start and at seq_idx changes.  One thread owns 8 consecutive channels (every
-// part of [x | B | C] is a multiple of 8 wide) and walks kConvTok tokens.
+// start and at seq_idx changes.  A block owns a tile of kFwdTok tokens x
+// kFwdCh channels: all of its raw inputs (plus the 3-token halo) are brought
+// into shared memory with 16-byte cp.async copies at once (zero-filled before
+// token 0), then each thread walks kFwdTok/4 tokens of 2 channels from shared
+// memory; a warp's stores cover 64 consecutive channels of one token.
+constexpr int kFwdTok = 64, kFwdCh = 128;
+
 template <typename T>
-__global__ void __launch_bounds__(128) conv_fwd_kernel(Problem pr, T *__restrict__ u) {
-  const int c = (blockIdx.x * 128 + threadIdx.x) * 8;
-  if (c >= pr.Cd) return;
-  const int t0 = blockIdx.y * kConvTok, bb = blockIdx.z;
-  const int t1 = min(pr.L, t0 + kConvTok);
-  long long st;
-  const T *src = raw_channel<T>(pr, bb, c, st);
-  float w[8][4], bias[8];
+__global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict__ u) {
+  constexpr int kRows = kFwdTok + 3;
+  constexpr int kChunk = 16 / (int)sizeof(T);  // channels per 16-byte copy
+  constexpr int kCpr = kFwdCh / kChunk;          // copies per row
+  __shared__ __align__(16) T tile[kRows][kFwdCh];
+  __shared__ int seqs[kRows];
+  const int c0 = blockIdx.x * kFwdCh, t0 = blockIdx.y * kFwdTok, bb = blockIdx.z;
+  const int nch = min(kFwdCh, pr.Cd - c0);
+  for (int q = threadIdx.x; q < kRows * kCpr; q += 256) {
+    const int r = q / kCpr, cc = (q % kCpr) * kChunk, t = t0 - 3 + r;
+    if (cc >= nch) continue;
+    long long st;
+    const T *src = raw_channel<T>(pr, bb, c0 + cc, st);
+    const bool ok = t >= 0 && t < pr.L;
+    const void *g = ok ? static_cast<const void *>(src + (size_t)t * st) : static_cast<const void *>(src);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(
+                     &tile[r][cc]))),
+                 "l"(g), "r"(ok ? 16 : 0)
+                 : "memory");
+  }
+  for (int r = threadIdx.x; r < kRows; r += 256) {
+    const int t = t0 - 3 + r;
+    seqs[r] = (t >= 0 && t < pr.L) ? seq_of(pr, bb, t) : -1;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int cp = threadIdx.x % (kFwdCh / 2), tq = threadIdx.x / (kFwdCh / 2);
+  const int c = c0 + 2 * cp;
+  if (2 * cp >= nch) return;
+  float w[2][4], bias[2];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 2; ++q) {
     const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
     w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
     bias[q] = pr.conv_b[c + q];
   }
-  float r0[8], r1[8], r2[8];
-  int s0 = 0, s1 = 0, s2 = 0;
+  constexpr int kPer = kFwdTok / 4;
+  const int r0 = tq * kPer;  // first output row (token t0 + r0), inputs at rows r0 .. r0 + 3
+  float x0[2], x1[2], x2[2];
+  auto ld2 = [&](int r, float (&v)[2]) {
+    v[0] = to_f(tile[r][2 * cp]);
+    v[1] = to_f(tile[r][2 * cp + 1]);
+  };
+  ld2(r0, x0);
+  ld2(r0 + 1, x1);
+  ld2(r0 + 2, x2);
+  int s0 = seqs[r0], s1 = seqs[r0 + 1], s2 = seqs[r0 + 2];
+  T *dst = u + ((size_t)bb * pr.L + t0 + r0) * pr.Cd + c;
+  const int tend = min(kPer, pr.L - (t0 + r0));
+  for (int k = 0; k < tend; ++k) {
+    float x3[2];
+    ld2(r0 + 3 + k, x3);
+    const int sq = seqs[r0 + 3 + k];
+    const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;
+    float o[2];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) r0[q] = r1[q] = r2[q] = 0.f;
-  if (t0 - 3 >= 0) { load8(src + (size_t)(t0 - 3) * st, r0); s0 = seq_of(pr, bb, t0 - 3); }
-  if (t0 - 2 >= 0) { load8(src + (size_t)(t0 - 2) * st, r1); s1 = seq_of(pr, bb, t0 - 2); }
-  if (t0 - 1 >= 0) { load8(src + (size_t)(t0 - 1) * st, r2); s2 = seq_of(pr, bb, t0 - 1); }
-  T *dst = u + (size_t)bb * pr.L * pr.Cd + c;
-  for (int t = t0; t < t1; ++t) {
-    float rt[8], o[8];
-    load8(src + (size_t)t * st, rt);
-    const int sq = seq_of(pr, bb, t);
-    const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;  // r* = 0 before token 0
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float v = bias[q] + w[q][3] * rt[q];
-      v += m2 ? w[q][2] * r2[q] : 0.f;
-      v += m1 ? w[q][1] * r1[q] : 0.f;
-      v += m0 ? w[q][0] * r0[q] : 0.f;
+    for (int q = 0; q < 2; ++q) {
+      float v = bias[q] + w[q][3] * x3[q];
+      v += m2 ? w[q][2] * x2[q] : 0.f;
+      v += m1 ? w[q][1] * x1[q] : 0.f;
+      v += m0 ? w[q][0] * x0[q] : 0.f;
       o[q] = v * sigmoid_fast(v);
-      r0[q] = r1[q]; r1[q] = r2[q]; r2[q] = rt[q];
+      x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
     }
-    store8(dst + (size_t)t * pr.Cd, o);
+    store2(dst + (size_t)k * pr.Cd, o);
     s0 = s1; s1 = s2; s2 = sq;
   }
 }
 
 template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s) {
-  dim3 grid((pr.Cd / 8 + 127) / 128, (pr.L + kConvTok - 1) / kConvTok, pr.b);
-  conv_fwd_kernel<T><<<grid, 128, 0, s>>>(pr, u);
+  dim3 grid((pr.Cd + kFwdCh - 1) / kFwdCh, (pr.L + kFwdTok - 1) / kFwdTok, pr.b);
+  conv_fwd_kernel<T><<<grid, 256, 0, s>>>(pr, u);
 }
 
 // dt = softplus(dt_raw + dt_bias); acs = inclusive cumsum of dt*A within each
