@@ -66,7 +66,7 @@ __device__ __forceinline__ float chunk_decay(const Problem &pr, int b, int h, in
 
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kConvBwdTok = 32;  // tokens per conv-backward block (one set of parameter partials each)
+constexpr int kConvBwdTok = 64;  // tokens per conv-backward block (one set of parameter partials each)
 
 // The workspace starts with the device status word followed by one work
 // counter per persistent kernel (zeroed with the status at every pass).

@@ -215,103 +215,159 @@ template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *
   dt_prep_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 32, 0, s>>>(pr, dtv, acs);
 }
 
-// Conv + SiLU backward for 4 channels over a block of kConvBwdTok tokens:
+// Conv + SiLU backward over a tile of kConvBwdTok tokens x kBwdCh channels:
 //   dv = du * silu'(v);  dxr[s] = sum_k w[k] dv[s+3-k] (same sequence);
-//   per-block partials of dconv_w[c,k] = sum dv[t] xr[t-3+k] and dconv_b[c] = sum dv.
-// v is recomputed from the raw inputs.
+//   per-tile partials of dconv_w[c,k] = sum dv[t] xr[t-3+k] and dconv_b[c] = sum dv.
+// The raw inputs of tokens t0-3 .. t0+kConvBwdTok+2 and du of t0 .. t0+kConvBwdTok+2
+// are brought into shared memory with 16-byte cp.async copies at once (zero
+// outside the row); dv overwrites du in place (v recomputed from the raw
+// inputs), then dxr is formed from dv.  Each thread owns 2 channels and a
+// quarter of the rows; the parameter partials are summed over the quarters in
+// fixed order.
+constexpr int kBwdCh = 64;
+
 template <typename T>
-__global__ void __launch_bounds__(128) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
+__global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
                                                        float *__restrict__ convp, int ntb) {
-  const int c = (blockIdx.x * 128 + threadIdx.x) * 4;
-  if (c >= pr.Cd) return;
-  const int blk = blockIdx.y, bb = blockIdx.z;
-  const int t0 = blk * kConvBwdTok, tend = min(pr.L, t0 + kConvBwdTok);
-  long long st;
-  const T *src = raw_channel<T>(pr, bb, c, st);
-  void *dbase;
-  long long dstride;
-  grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
-  T *dst = static_cast<T *>(dbase);
-  float w[4][4], bias[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
-    w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
-    bias[q] = pr.conv_b[c + q];
+  constexpr int kTok = kConvBwdTok;
+  constexpr int kXRows = kTok + 6;  // raw inputs, tokens t0-3 .. t0+kTok+2
+  constexpr int kDRows = kTok + 3;  // du / dv, tokens t0 .. t0+kTok+2
+  constexpr int kChunk = 16 / (int)sizeof(T);
+  __shared__ __align__(16) T xr[kXRows][kBwdCh];
+  __shared__ __align__(16) float dv[kDRows][kBwdCh];
+  __shared__ int seqs[kXRows];
+  __shared__ float red[4][kBwdCh][5];
+  const int c0 = blockIdx.x * kBwdCh, blk = blockIdx.y, bb = blockIdx.z, t0 = blk * kTok;
+  const int nch = min(kBwdCh, pr.Cd - c0);
+  for (int q = threadIdx.x; q < kXRows * (kBwdCh / kChunk); q += 256) {
+    const int r = q / (kBwdCh / kChunk), cc = (q % (kBwdCh / kChunk)) * kChunk, t = t0 - 3 + r;
+    if (cc >= nch) continue;
+    long long st;
+    const T *src = raw_channel<T>(pr, bb, c0 + cc, st);
+    const bool ok = t >= 0 && t < pr.L;
+    const void *g = ok ? static_cast<const void *>(src + (size_t)t * st) : static_cast<const void *>(src);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(&xr[r][cc]))),
+                 "l"(g), "r"(ok ? 16 : 0)
+                 : "memory");
   }
-  float r0[4], r1[4], r2[4], d0[4], d1[4], d2[4], dw[4][4], db[4];
-  int s0 = 0, s1 = 0, s2 = 0, q0 = 0, q1 = 0, q2 = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    r0[q] = r1[q] = r2[q] = d0[q] = d1[q] = d2[q] = db[q] = 0.f;
-    dw[q][0] = dw[q][1] = dw[q][2] = dw[q][3] = 0.f;
+  const float *dub = du + (size_t)bb * pr.L * pr.Cd + c0;
+  for (int q = threadIdx.x; q < kDRows * (kBwdCh / 4); q += 256) {
+    const int r = q / (kBwdCh / 4), cc = (q % (kBwdCh / 4)) * 4, t = t0 + r;
+    if (cc >= nch) continue;
+    const bool ok = t < pr.L;
+    const void *g = ok ? static_cast<const void *>(dub + (size_t)t * pr.Cd + cc) : static_cast<const void *>(dub);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(&dv[r][cc]))),
+                 "l"(g), "r"(ok ? 16 : 0)
+                 : "memory");
   }
-  if (t0 - 3 >= 0) { load4(src + (size_t)(t0 - 3) * st, r0); s0 = seq_of(pr, bb, t0 - 3); }
-  if (t0 - 2 >= 0) { load4(src + (size_t)(t0 - 2) * st, r1); s1 = seq_of(pr, bb, t0 - 2); }
-  if (t0 - 1 >= 0) { load4(src + (size_t)(t0 - 1) * st, r2); s2 = seq_of(pr, bb, t0 - 1); }
-  const float *dub = du + (size_t)bb * pr.L * pr.Cd + c;
-  for (int t = t0; t < t0 + kConvBwdTok + 3; ++t) {
-    float dvt[4];
-    int sq = 0;
-    if (t < pr.L) {
-      float rt[4], g8[4];
-      load4(src + (size_t)t * st, rt);
-      load4(dub + (size_t)t * pr.Cd, g8);
-      sq = seq_of(pr, bb, t);
-      const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;
-      const bool own = t < tend;
+  for (int r = threadIdx.x; r < kXRows; r += 256) {
+    const int t = t0 - 3 + r;
+    seqs[r] = (t >= 0 && t < pr.L) ? seq_of(pr, bb, t) : -1;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int cp = threadIdx.x % (kBwdCh / 2), tq = threadIdx.x / (kBwdCh / 2);  // 8 row groups
+  const int c = c0 + 2 * cp;
+  const bool live = 2 * cp < nch;
+  float w[2][4] = {}, bias[2] = {}, dw[2][4] = {}, db[2] = {};
+  if (live) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v = bias[q] + w[q][3] * rt[q];
-        v += m2 ? w[q][2] * r2[q] : 0.f;
-        v += m1 ? w[q][1] * r1[q] : 0.f;
-        v += m0 ? w[q][0] * r0[q] : 0.f;
-        const float sg = sigmoid_fast(v);
-        dvt[q] = g8[q] * sg * (1.f + v * (1.f - sg));
-        if (own) {
-          db[q] += dvt[q];
-          dw[q][3] += dvt[q] * rt[q];
-          dw[q][2] += m2 ? dvt[q] * r2[q] : 0.f;
-          dw[q][1] += m1 ? dvt[q] * r1[q] : 0.f;
-          dw[q][0] += m0 ? dvt[q] * r0[q] : 0.f;
-        }
-        r0[q] = r1[q]; r1[q] = r2[q]; r2[q] = rt[q];
-      }
-      s0 = s1; s1 = s2; s2 = sq;
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dvt[q] = 0.f;
+    for (int q = 0; q < 2; ++q) {
+      const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
+      w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
+      bias[q] = pr.conv_b[c + q];
     }
-    // output token s = t - 3 reads dv[s..s+3] = (d0, d1, d2, dvt)
-    const int s = t - 3;
-    if (s >= t0 && s < tend) {
-      const bool m1 = q1 == q0, m2 = q2 == q0, m3 = sq == q0;
-      float g[4];
+  }
+  constexpr int kGroups = 256 / (kBwdCh / 2);
+  // phase 1: dv for rows [0, kDRows) (token t0 + r; its inputs are xr rows r .. r + 3)
+  if (live) {
+    for (int r = tq; r < kDRows; r += kGroups) {
+      if (t0 + r >= pr.L) break;
+      const int sq = seqs[r + 3];
+      const bool m2 = seqs[r + 2] == sq, m1 = seqs[r + 1] == sq, m0 = seqs[r] == sq;
+      const float2 g2 = *reinterpret_cast<const float2 *>(&dv[r][2 * cp]);
+      const float gv[2] = {g2.x, g2.y};
+      float out[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float a = w[q][3] * d0[q];
-        a += m1 ? w[q][2] * d1[q] : 0.f;
-        a += m2 ? w[q][1] * d2[q] : 0.f;
-        a += m3 ? w[q][0] * dvt[q] : 0.f;
+      for (int q = 0; q < 2; ++q) {
+        const float x0 = to_f(xr[r][2 * cp + q]), x1 = to_f(xr[r + 1][2 * cp + q]), x2 = to_f(xr[r + 2][2 * cp + q]),
+                    x3 = to_f(xr[r + 3][2 * cp + q]);
+        float v = bias[q] + w[q][3] * x3;
+        v += m2 ? w[q][2] * x2 : 0.f;
+        v += m1 ? w[q][1] * x1 : 0.f;
+        v += m0 ? w[q][0] * x0 : 0.f;
+        const float sg = sigmoid_fast(v);
+        const float d = gv[q] * sg * (1.f + v * (1.f - sg));
+        out[q] = d;
+        if (r < kTok) {
+          db[q] += d;
+          dw[q][3] += d * x3;
+          dw[q][2] += m2 ? d * x2 : 0.f;
+          dw[q][1] += m1 ? d * x1 : 0.f;
+          dw[q][0] += m0 ? d * x0 : 0.f;
+        }
+      }
+      *reinterpret_cast<float2 *>(&dv[r][2 * cp]) = make_float2(out[0], out[1]);  // own elements only
+    }
+  }
+  __syncthreads();
+  // phase 2: dxr for rows s in [0, kTok) (token t0 + s) from dv rows s .. s + 3
+  if (live) {
+    void *dbase;
+    long long dstride;
+    grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
+    T *dst = static_cast<T *>(dbase);
+    for (int sr = tq; sr < kTok; sr += kGroups) {
+      const int t = t0 + sr;
+      if (t >= pr.L) break;
+      const int q0 = seqs[sr + 3];  // token t
+      const bool m1 = seqs[sr + 4] == q0, m2 = seqs[sr + 5] == q0, m3 = seqs[sr + 6] == q0;
+      float g[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float a = w[q][3] * dv[sr][2 * cp + q];
+        a += m1 ? w[q][2] * dv[sr + 1][2 * cp + q] : 0.f;
+        a += m2 ? w[q][1] * dv[sr + 2][2 * cp + q] : 0.f;
+        a += m3 ? w[q][0] * dv[sr + 3][2 * cp + q] : 0.f;
         g[q] = a;
       }
-      store4(dst + (size_t)s * dstride, g);
+      store2(dst + (size_t)t * dstride, g);
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) { d0[q] = d1[q]; d1[q] = d2[q]; d2[q] = dvt[q]; }
-    q0 = q1; q1 = q2; q2 = sq;
   }
+  // parameter partials: fixed-order sum over the row groups
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float *pp = convp + (((size_t)bb * ntb + blk) * pr.Cd + c + q) * 5;
-    pp[0] = dw[q][0]; pp[1] = dw[q][1]; pp[2] = dw[q][2]; pp[3] = dw[q][3]; pp[4] = db[q];
+  for (int q = 0; q < 2; ++q) {
+    // groups 0..3 and 4..7 folded pairwise first (fixed order)
+    const int slot = tq & 3;
+    if (tq < 4) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) red[slot][2 * cp + q][kk] = dw[q][kk];
+      red[slot][2 * cp + q][4] = db[q];
+    }
+  }
+  __syncthreads();
+  if (tq >= 4) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) red[tq & 3][2 * cp + q][kk] += dw[q][kk];
+      red[tq & 3][2 * cp + q][4] += db[q];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < nch * 5; e += 256) {
+    const int ch = e / 5, k5 = e % 5;
+    const float v = (red[0][ch][k5] + red[1][ch][k5]) + (red[2][ch][k5] + red[3][ch][k5]);
+    convp[(((size_t)bb * ntb + blk) * pr.Cd + c0 + ch) * 5 + k5] = v;
   }
 }
 
 template <typename T>
 void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s) {
-  dim3 grid((pr.Cd / 4 + 127) / 128, ntb, pr.b);
-  conv_bwd_kernel<T><<<grid, 128, 0, s>>>(pr, du, go, convp, ntb);
+  dim3 grid((pr.Cd + kBwdCh - 1) / kBwdCh, ntb, pr.b);
+  conv_bwd_kernel<T><<<grid, 256, 0, s>>>(pr, du, go, convp, ntb);
 }
 
 // Parameter gradients: fixed-order sums of per-chunk / per-block partials.
