@@ -168,7 +168,9 @@ def kernel_work(shape, dtype: str) -> dict:
         "combine_state": ("mem", 0, st + st16 + seg),
         "local_rev": ("mem", 0, 2 * st + seg),
         "seg_rscan": ("mem", 0, 2 * seg),
-        "chunk_dt": ("mem", 0, 5 * tok + 4 * st + 2 * x + b * L * H * eb),
+        # bf16 path: the states' decay term (combine_bwd) and dy . x (tc_bwd_col) come precomputed
+        "chunk_dt": ("mem", 0, 6 * tok + (0 if dtype == "bf16" else 4 * st + 2 * x) + b * L * H * eb),
+        "combine_bwd": ("mem", 0, 2 * st + 2 * seg + 2 * st16 + b * nc * H * 4),
         "bc_reduce": ("mem", 0, 2 * parts + 2 * b * L * GN * 4),
         "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 32) * Cd * 20),
         "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 32) * Cd * 20),
@@ -178,7 +180,7 @@ def kernel_work(shape, dtype: str) -> dict:
         "tc_chunk_out": ("tensor", f_cb + f_diag + f_off, 2 * x + bc + st16 + 2 * tok),
         "tc_bwd_row": ("tensor", f_cb + f_diag + f_bc + 2 * f_off, 2 * x + bc + st16 + 4 * tok + parts),
         "tc_bwd_col": ("tensor", f_cb + 2 * f_diag + f_bc + 2 * f_off,
-                       2 * x + bc + st16 + 4 * tok + parts + b * L * HP * 4),
+                       2 * x + bc + st16 + 5 * tok + parts + b * L * HP * 4),
     }
     # fp32 CUDA-core kernels: the same work with CB, chunk states and W through HBM
     wbytes = b * nc * H * tiles * 128 * 128 * 4

@@ -222,12 +222,13 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   SSD_LAUNCH("seg_rscan", launch_seg_rscan(pr, gext, ablk, dfinal, gout, s));
   // chunk gradients
   int vcol_parts = 1, nsub = pr.H, spg = pr.hpg;
+  float *sdot = nullptr;  // a_c <dS_end, S_in> per chunk, when the combine pass computes it
   if constexpr (kIsBf16<T>) {
     if (tc) {
       __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
       __nv_bfloat16 *dse16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.dse16);
-      SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, 0, s));
-      SSD_LAUNCH("combine_state", launch_combine_state(pr, dsl, gout, dse16, 1, s));
+      sdot = chs + 3 * (size_t)pr.b * pr.nc * pr.H;  // free slot of the per-chunk scalars
+      SSD_LAUNCH("combine_bwd", launch_combine_bwd(pr, sst, segin, dsl, gout, sin16, dse16, sdot, s));
       SSD_LAUNCH("tc_bwd_row", launch_tc_bwd_row(pr, u, dy, dtv, acs, sin16, dcp, tok, status, s));
       SSD_LAUNCH("tc_bwd_col", launch_tc_bwd_col(pr, u, dy, dtv, acs, dse16, du, dbp, tok, status, s));
       vcol_parts = 1;
@@ -242,7 +243,7 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
                launch_chunk_dcdb<T>(pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, s));
   }
   SSD_LAUNCH("chunk_dt",
-             launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, go, chs, s));
+             launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, sdot, go, chs, s));
   SSD_LAUNCH("bc_reduce", launch_bc_reduce(pr, dcp, dbp, nsub, spg, du, s));
   // conv backward and parameter reductions
   SSD_LAUNCH("conv_bwd", launch_conv_bwd<T>(pr, du, go, convp, w.ntb, s));

@@ -12,6 +12,7 @@
 // thread owns a few elements and walks the chunks (or segments) in order: the
 // result is bit-identical from run to run.
 #include "kernels.h"
+#include "simt_gemm.cuh"
 
 namespace ssd {
 
@@ -76,6 +77,49 @@ void launch_combine_state(const Problem &pr, const float *a, const float *seg, _
                           cudaStream_t s) {
   dim3 grid((pr.P * pr.N / 8 + 255) / 256, pr.H, pr.b * pr.nc);
   combine_state_kernel<<<grid, 256, 0, s>>>(pr, a, seg, out, mode);
+}
+
+// Backward form of the combination, one block per (row, chunk, head): the true
+// state entering the chunk S_in = S_loc + dstart * S_seg and the true state
+// gradient at its end dS = dS_loc + dend * G_out, both written in bf16 (the
+// tensor-core operands), and in fp32 the chunk's decay term of the dt adjoint
+//   sdot[b, c, h] = a_c <dS, S_in>
+// summed in a fixed order (per thread, then the block tree).
+__global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const float *__restrict__ sst,
+                                                          const float *__restrict__ segin,
+                                                          const float *__restrict__ dsl,
+                                                          const float *__restrict__ gout,
+                                                          __nv_bfloat16 *__restrict__ sin16,
+                                                          __nv_bfloat16 *__restrict__ dse16, float *__restrict__ sdot) {
+  __shared__ float red[8];
+  const int PN = pr.P * pr.N;
+  const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z, k = c / pr.cps;
+  const size_t ti = dtab_index(pr, bb, h, c);
+  const float dc = __ldg(pr.dstart + ti), de = __ldg(pr.dend + ti), ac = __ldg(pr.cdec + ti);
+  const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * PN;
+  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * PN;
+  float part = 0.f;
+#pragma unroll 4
+  for (int e = threadIdx.x * 4; e < PN; e += 256 * 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(sst + co + e), b = *reinterpret_cast<const float4 *>(segin + so + e);
+    const float4 x = *reinterpret_cast<const float4 *>(dsl + co + e), y = *reinterpret_cast<const float4 *>(gout + so + e);
+    const float sv[4] = {a.x + dc * b.x, a.y + dc * b.y, a.z + dc * b.z, a.w + dc * b.w};
+    const float gv[4] = {x.x + de * y.x, x.y + de * y.y, x.z + de * y.z, x.w + de * y.w};
+    part += gv[0] * sv[0] + gv[1] * sv[1] + gv[2] * sv[2] + gv[3] * sv[3];
+    __nv_bfloat162 s01 = __floats2bfloat162_rn(sv[0], sv[1]), s23 = __floats2bfloat162_rn(sv[2], sv[3]);
+    __nv_bfloat162 g01 = __floats2bfloat162_rn(gv[0], gv[1]), g23 = __floats2bfloat162_rn(gv[2], gv[3]);
+    *reinterpret_cast<uint2 *>(sin16 + co + e) =
+        make_uint2(*reinterpret_cast<uint32_t *>(&s01), *reinterpret_cast<uint32_t *>(&s23));
+    *reinterpret_cast<uint2 *>(dse16 + co + e) =
+        make_uint2(*reinterpret_cast<uint32_t *>(&g01), *reinterpret_cast<uint32_t *>(&g23));
+  }
+  const float tot = block_sum256(part, red);
+  if (threadIdx.x == 0) sdot[((size_t)bb * pr.nc + c) * pr.H + h] = ac != 0.f ? ac * tot : 0.f;
+}
+
+void launch_combine_bwd(const Problem &pr, const float *sst, const float *segin, const float *dsl, const float *gout,
+                        __nv_bfloat16 *sin16, __nv_bfloat16 *dse16, float *sdot, cudaStream_t s) {
+  combine_bwd_kernel<<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, sst, segin, dsl, gout, sin16, dse16, sdot);
 }
 
 // Local pass of segment k: S <- a_c * S + Sc[c] over the segment's chunks from

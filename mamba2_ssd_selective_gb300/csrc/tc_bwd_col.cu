@@ -3,7 +3,7 @@
 //   dM^T = x_h dy_h^T,   CB^T = B_J C^T            (64-column slices, recomputed)
 //   M^T  = CB^T o L^T o dt_j,   W^T = dM^T o L^T o dt_j,  L^T[j, i] = exp(Acs_i - Acs_j)
 //   T_j  = sum_i M^T[j, i] dy_i,   U_j = dS_end,h B_j,     (tensor memory)
-//   du_x[j] = T_j + wdt_j U_j + D_h dy_j,   q_j = x_j . U_j,
+//   du_x[j] = T_j + wdt_j U_j + D_h dy_j,   q_j = x_j . U_j,   dy_j . x_j (for dD),
 //   vcol_j = sum_i V[i, j] = sum_i dM^T CB^T L^T
 // and accumulates over the heads of a block
 //   dB_j += sum_i W^T[j, i] C_i + wdt_j dS_end,h^T x_j,
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar.tu_full, parity(nh), status);
         tc_fence_after();
         float *dur = du + ((size_t)o.bb * pr.L + t) * pr.Cd + h * pr.P;
-        float qsum = 0.f;
+        float qsum = 0.f, ddsum = 0.f;  // q_j and dy_j . x_j (the dD piece)
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           float tv[16], uv[16];
@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) {
               const int col = 8 * t8 + e;
               qsum = fmaf(x8[e], uv[col], qsum);
+              ddsum = fmaf(d8[e], x8[e], ddsum);
               tv[col] += wdt * uv[col] + Dh * d8[e];
             }
           }
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         pipe::warp_arrive(bar.tu_free);
         tok[4 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = qsum;
+        tok[5 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = ddsum;
       }
       mbar_wait(bar.db_full, parity(nu), status);
       tc_fence_after();
