@@ -75,7 +75,17 @@ template <> __device__ __forceinline__ void store8<float>(float *p, const float 
   reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// 2 consecutive channels
+// 2 consecutive channels (one 32-bit load for bf16)
+__device__ __forceinline__ void load2(const __nv_bfloat16 *p, float (&v)[2]) {
+  const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+  v[0] = __uint_as_float(w << 16);
+  v[1] = __uint_as_float(w & 0xffff0000u);
+}
+__device__ __forceinline__ void load2(const float *p, float (&v)[2]) {
+  const float2 f = *reinterpret_cast<const float2 *>(p);
+  v[0] = f.x;
+  v[1] = f.y;
+}
 __device__ __forceinline__ void store2(__nv_bfloat16 *p, const float (&v)[2]) {
   *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v[0], v[1]);
 }
@@ -151,16 +161,27 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict
   constexpr int kPer = kFwdTok / 4;
   const int r0 = tq * kPer;  // first output row (token t0 + r0), inputs at rows r0 .. r0 + 3
   float x0[2], x1[2], x2[2];
-  auto ld2 = [&](int r, float (&v)[2]) {
-    v[0] = to_f(tile[r][2 * cp]);
-    v[1] = to_f(tile[r][2 * cp + 1]);
-  };
+  auto ld2 = [&](int r, float (&v)[2]) { load2(&tile[r][2 * cp], v); };
   ld2(r0, x0);
   ld2(r0 + 1, x1);
   ld2(r0 + 2, x2);
   int s0 = seqs[r0], s1 = seqs[r0 + 1], s2 = seqs[r0 + 2];
   T *dst = u + ((size_t)bb * pr.L + t0 + r0) * pr.Cd + c;
   const int tend = min(kPer, pr.L - (t0 + r0));
+  if (!pr.seq_idx) {  // one sequence per row: every tap counts (the halo before token 0 is zero)
+    for (int k = 0; k < tend; ++k) {
+      float x3[2], o[2];
+      ld2(r0 + 3 + k, x3);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float v = fmaf(w[q][0], x0[q], fmaf(w[q][1], x1[q], fmaf(w[q][2], x2[q], fmaf(w[q][3], x3[q], bias[q]))));
+        o[q] = v * sigmoid_fast(v);
+        x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
+      }
+      store2(dst + (size_t)k * pr.Cd, o);
+    }
+    return;
+  }
   for (int k = 0; k < tend; ++k) {
     float x3[2];
     ld2(r0 + 3 + k, x3);
@@ -226,6 +247,52 @@ template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *
 // fixed order.
 constexpr int kBwdCh = 64;
 
+// phase 1 of the conv backward for one thread's 2 channels: dv for rows r of
+// the tile (token t0 + r; its inputs are raw rows r .. r + 3), in place over du,
+// and the parameter partials of the tile's own rows.  HasSeq: taps masked at
+// sequence changes (without seq_idx every tap counts; the halo before token 0
+// is zero).
+template <bool HasSeq, typename T, int XR, int DR>
+__device__ __forceinline__ void conv_bwd_dv(const Problem &pr, const T (&xr)[XR][kBwdCh], float (&dv)[DR][kBwdCh],
+                                            const int *seqs, int t0, int cp, int tq, int groups,
+                                            const float (&w)[2][4], const float (&bias)[2], float (&dw)[2][4],
+                                            float (&db)[2]) {
+  for (int r = tq; r < DR; r += groups) {
+    if (t0 + r >= pr.L) break;
+    bool m2 = true, m1 = true, m0 = true;
+    if (HasSeq) {
+      const int sq = seqs[r + 3];
+      m2 = seqs[r + 2] == sq;
+      m1 = seqs[r + 1] == sq;
+      m0 = seqs[r] == sq;
+    }
+    float x0[2], x1[2], x2[2], x3[2];
+    load2(&xr[r][2 * cp], x0);
+    load2(&xr[r + 1][2 * cp], x1);
+    load2(&xr[r + 2][2 * cp], x2);
+    load2(&xr[r + 3][2 * cp], x3);
+    const float2 g2 = *reinterpret_cast<const float2 *>(&dv[r][2 * cp]);
+    const float gv[2] = {g2.x, g2.y};
+    float out[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float w2 = m2 ? w[q][2] : 0.f, w1 = m1 ? w[q][1] : 0.f, w0 = m0 ? w[q][0] : 0.f;
+      const float v = fmaf(w0, x0[q], fmaf(w1, x1[q], fmaf(w2, x2[q], fmaf(w[q][3], x3[q], bias[q]))));
+      const float sg = sigmoid_fast(v);
+      const float d = gv[q] * sg * (1.f + v * (1.f - sg));
+      out[q] = d;
+      if (r < DR - 3) {  // the tile's own tokens
+        db[q] += d;
+        dw[q][3] = fmaf(d, x3[q], dw[q][3]);
+        dw[q][2] = fmaf(m2 ? d : 0.f, x2[q], dw[q][2]);
+        dw[q][1] = fmaf(m1 ? d : 0.f, x1[q], dw[q][1]);
+        dw[q][0] = fmaf(m0 ? d : 0.f, x0[q], dw[q][0]);
+      }
+    }
+    *reinterpret_cast<float2 *>(&dv[r][2 * cp]) = make_float2(out[0], out[1]);  // own elements only
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
                                                        float *__restrict__ convp, int ntb) {
@@ -281,36 +348,11 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
     }
   }
   constexpr int kGroups = 256 / (kBwdCh / 2);
-  // phase 1: dv for rows [0, kDRows) (token t0 + r; its inputs are xr rows r .. r + 3)
   if (live) {
-    for (int r = tq; r < kDRows; r += kGroups) {
-      if (t0 + r >= pr.L) break;
-      const int sq = seqs[r + 3];
-      const bool m2 = seqs[r + 2] == sq, m1 = seqs[r + 1] == sq, m0 = seqs[r] == sq;
-      const float2 g2 = *reinterpret_cast<const float2 *>(&dv[r][2 * cp]);
-      const float gv[2] = {g2.x, g2.y};
-      float out[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float x0 = to_f(xr[r][2 * cp + q]), x1 = to_f(xr[r + 1][2 * cp + q]), x2 = to_f(xr[r + 2][2 * cp + q]),
-                    x3 = to_f(xr[r + 3][2 * cp + q]);
-        float v = bias[q] + w[q][3] * x3;
-        v += m2 ? w[q][2] * x2 : 0.f;
-        v += m1 ? w[q][1] * x1 : 0.f;
-        v += m0 ? w[q][0] * x0 : 0.f;
-        const float sg = sigmoid_fast(v);
-        const float d = gv[q] * sg * (1.f + v * (1.f - sg));
-        out[q] = d;
-        if (r < kTok) {
-          db[q] += d;
-          dw[q][3] += d * x3;
-          dw[q][2] += m2 ? d * x2 : 0.f;
-          dw[q][1] += m1 ? d * x1 : 0.f;
-          dw[q][0] += m0 ? d * x0 : 0.f;
-        }
-      }
-      *reinterpret_cast<float2 *>(&dv[r][2 * cp]) = make_float2(out[0], out[1]);  // own elements only
-    }
+    if (pr.seq_idx)
+      conv_bwd_dv<true, T>(pr, xr, dv, seqs, t0, cp, tq, kGroups, w, bias, dw, db);
+    else
+      conv_bwd_dv<false, T>(pr, xr, dv, seqs, t0, cp, tq, kGroups, w, bias, dw, db);
   }
   __syncthreads();
   // phase 2: dxr for rows s in [0, kTok) (token t0 + s) from dv rows s .. s + 3
@@ -319,18 +361,25 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
     long long dstride;
     grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
     T *dst = static_cast<T *>(dbase);
+    const bool has_seq = pr.seq_idx != nullptr;
     for (int sr = tq; sr < kTok; sr += kGroups) {
       const int t = t0 + sr;
       if (t >= pr.L) break;
       const int q0 = seqs[sr + 3];  // token t
-      const bool m1 = seqs[sr + 4] == q0, m2 = seqs[sr + 5] == q0, m3 = seqs[sr + 6] == q0;
+      const bool m1 = !has_seq || seqs[sr + 4] == q0, m2 = !has_seq || seqs[sr + 5] == q0,
+                 m3 = !has_seq || seqs[sr + 6] == q0;
+      const float2 d0 = *reinterpret_cast<const float2 *>(&dv[sr][2 * cp]);
+      const float2 d1 = *reinterpret_cast<const float2 *>(&dv[sr + 1][2 * cp]);
+      const float2 d2 = *reinterpret_cast<const float2 *>(&dv[sr + 2][2 * cp]);
+      const float2 d3 = *reinterpret_cast<const float2 *>(&dv[sr + 3][2 * cp]);
+      const float a0[2] = {d0.x, d0.y}, a1[2] = {d1.x, d1.y}, a2[2] = {d2.x, d2.y}, a3[2] = {d3.x, d3.y};
       float g[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        float a = w[q][3] * dv[sr][2 * cp + q];
-        a += m1 ? w[q][2] * dv[sr + 1][2 * cp + q] : 0.f;
-        a += m2 ? w[q][1] * dv[sr + 2][2 * cp + q] : 0.f;
-        a += m3 ? w[q][0] * dv[sr + 3][2 * cp + q] : 0.f;
+        float a = w[q][3] * a0[q];
+        a = fmaf(m1 ? w[q][2] : 0.f, a1[q], a);
+        a = fmaf(m2 ? w[q][1] : 0.f, a2[q], a);
+        a = fmaf(m3 ? w[q][0] : 0.f, a3[q], a);
         g[q] = a;
       }
       store2(dst + (size_t)t * dstride, g);
