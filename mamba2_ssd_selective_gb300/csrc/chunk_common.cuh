@@ -60,6 +60,35 @@ __device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkId
   __syncthreads();
 }
 
+// Only the weights a kernel needs, for a pair of heads h0, h0 + 1 of one chunk:
+// wdt[j] (chunk-state weights) or em[i] (weights of the state entering the
+// chunk), as defined for ChunkVecs.
+__device__ __forceinline__ void load_wdt_pair(const Problem &pr, int c, int h0, int bb, const float *dtv,
+                                              const float *acs, float (&w0)[256], float (&w1)[256]) {
+  const int Q = pr.Q, t0 = c * Q;
+  const int seq_last = seq_of(pr, bb, t0 + Q - 1);
+  for (int e = threadIdx.x; e < 2 * Q; e += blockDim.x) {
+    const int hh = e / Q, i = e % Q, h = h0 + hh;
+    const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L + t0;
+    const float *dt_bh = dtv + ((size_t)bb * pr.H + h) * pr.L + t0;
+    const float w = (seq_of(pr, bb, t0 + i) == seq_last) ? expf(acs_bh[Q - 1] - acs_bh[i]) * dt_bh[i] : 0.f;
+    (hh ? w1 : w0)[i] = w;
+  }
+  __syncthreads();
+}
+__device__ __forceinline__ void load_em_pair(const Problem &pr, int c, int h0, int bb, const float *acs,
+                                             float (&e0)[256], float (&e1)[256]) {
+  const int Q = pr.Q, t0 = c * Q;
+  const int seq_prev = c > 0 ? seq_of(pr, bb, t0 - 1) : 0;
+  for (int e = threadIdx.x; e < 2 * Q; e += blockDim.x) {
+    const int hh = e / Q, i = e % Q, h = h0 + hh;
+    const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L + t0;
+    const float m = (c > 0 && seq_of(pr, bb, t0 + i) == seq_prev) ? expf(acs_bh[i]) : 0.f;
+    (hh ? e1 : e0)[i] = m;
+  }
+  __syncthreads();
+}
+
 // decay carrying the segment's initial state to the start of chunk c
 __device__ __forceinline__ float decay_seg_to_chunk(const Problem &pr, int bb, int h, int c) {
   return __ldg(pr.dstart + dtab_index(pr, bb, h, c));

@@ -52,12 +52,11 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_state_kernel(Problem pr, c
                                                        const float *__restrict__ dtv, const float *__restrict__ acs,
                                                        float *__restrict__ sst, int *status) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ ChunkVecs v0, v1;
+  __shared__ float wdt0[256], wdt1[256];
   Carve<EngPair> sm(smem_raw);
   const int c = blockIdx.x, h0 = 2 * blockIdx.y, bb = blockIdx.z;
-  const ChunkIds id0 = make_ids(pr, c, h0, bb), id1 = make_ids(pr, c, h0 + 1, bb);
-  load_chunk_vecs(pr, id0, dtv, acs, v0);
-  load_chunk_vecs(pr, id1, dtv, acs, v1);
+  const ChunkIds id0 = make_ids(pr, c, h0, bb);
+  load_wdt_pair(pr, c, h0, bb, dtv, acs, wdt0, wdt1);
   const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
   const bf16 *ub = u + ((size_t)bb * pr.L + id0.t0) * Cd;
   const int offB = HP + id0.g * N;
@@ -69,7 +68,7 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_state_kernel(Problem pr, c
   auto fbm = [&](uint4 raw, int n0, int k) {
     float x[8];
     tc::unpack8(raw, x);
-    const float s = (n0 >> 6) ? v1.wdt[k] : v0.wdt[k];
+    const float s = (n0 >> 6) ? wdt1[k] : wdt0[k];
 #pragma unroll
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
@@ -104,12 +103,11 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const
                                                    const float *__restrict__ acs, float *__restrict__ dsl,
                                                    int *status) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ ChunkVecs v0, v1;
+  __shared__ float em0[256], em1[256];
   Carve<EngPair> sm(smem_raw);
   const int c = blockIdx.x, h0 = 2 * blockIdx.y, bb = blockIdx.z;
-  const ChunkIds id0 = make_ids(pr, c, h0, bb), id1 = make_ids(pr, c, h0 + 1, bb);
-  load_chunk_vecs(pr, id0, dtv, acs, v0);
-  load_chunk_vecs(pr, id1, dtv, acs, v1);
+  const ChunkIds id0 = make_ids(pr, c, h0, bb);
+  load_em_pair(pr, c, h0, bb, acs, em0, em1);
   const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
   const bf16 *ub = u + ((size_t)bb * pr.L + id0.t0) * Cd;
   const bf16 *dyb = dy + ((size_t)bb * pr.L + id0.t0) * HP;
@@ -122,7 +120,7 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const
   auto fbm = [&](uint4 raw, int n0, int i) {
     float x[8];
     tc::unpack8(raw, x);
-    const float s = (n0 >> 6) ? v1.em[i] : v0.em[i];
+    const float s = (n0 >> 6) ? em1[i] : em0[i];
 #pragma unroll
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
