@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.vec_full[i], 1);
       mbar_init(&bar.vec_free[i], kTWarps + kEWarps);
       mbar_init(&bar.xt_full[i], 1);
-      mbar_init(&bar.xt_free[i], 1 + kTWarps);
+      mbar_init(&bar.xt_free[i], 1 + kTWarps + kEWarps);
     }
     for (int i = 0; i < kNY; ++i) {
       mbar_init(&bar.dy_full[i], 1);
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, jl = 32 * q + lane;
-    const uint32_t sV = smem_u32(sm + kSmV);
+    const uint32_t sV = smem_u32(sm + kSmV), sXT = smem_u32(sm + kSmXT);
     uint32_t nu = 0, nh = 0;
     for (;; ++nu) {
       const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
@@ -444,9 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int j = 128 * o.J + jl, t = o.c * pr.Q + j;
       const bf16 *dyrow = dy + ((size_t)o.bb * pr.L + t) * HP;
-      const bf16 *xrow = u + ((size_t)o.bb * pr.L + t) * pr.Cd;
       for (int hh = 0; hh < HB; ++hh, ++nh) {
         const int h = o.h0 + hh, vb = nh & 1;
+        // the dy row is loaded first, in flight while the accumulators finish;
+        // x comes from the head's x tile in shared memory
+        uint4 dyr[8];
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) dyr[q8] = tc::ldg16(dyrow + h * pr.P + 8 * q8);
         mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
         const uint32_t vacs = sV + vb * kVecStride, vdt = vacs + 1024, vseq = vacs + 2048 + 16;
         const bool in_last = !has_seq || pipe::lds_i(vseq + 4 * j) == pipe::lds_i(vseq + 4 * (pr.Q - 1));
@@ -455,6 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     : 0.f;
         pipe::warp_arrive(&bar.vec_free[vb]);
         const float Dh = __ldg(pr.D + h);
+        mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);
+        const uint32_t xt = sXT + vb * 16384;
         mbar_wait(bar.tu_full, parity(nh), status);
         tc_fence_after();
         float *dur = du + ((size_t)o.bb * pr.L + t) * pr.Cd + h * pr.P;
@@ -467,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t8 = 0; t8 < 2; ++t8) {
             float d8[8], x8[8];
-            tc::unpack8(tc::ldg16(dyrow + h * pr.P + 16 * cc + 8 * t8), d8);
-            tc::unpack8(tc::ldg16(xrow + h * pr.P + 16 * cc + 8 * t8), x8);
+            tc::unpack8(dyr[2 * cc + t8], d8);
+            tc::unpack8(pipe::lds_sw128(xt, jl, 2 * cc + t8), x8);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int col = 8 * t8 + e;
@@ -483,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         pipe::warp_arrive(bar.tu_free);
+        pipe::warp_arrive(&bar.xt_free[vb]);
         tok[4 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = qsum;
         tok[5 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = ddsum;
       }
