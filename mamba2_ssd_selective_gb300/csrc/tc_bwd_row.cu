@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.vec_full[i], 1);
       mbar_init(&bar.vec_free[i], kTWarps + kEWarps);
       mbar_init(&bar.dy_full[i], 1);
-      mbar_init(&bar.dy_free[i], 1 + kTWarps);
+      mbar_init(&bar.dy_free[i], 1 + kTWarps + kEWarps);
     }
     for (int i = 0; i < kNX; ++i) {
       mbar_init(&bar.x_full[i], 1);
@@ -438,14 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, il = 32 * q + lane;
-    const uint32_t sV = smem_u32(sm + kSmV);
+    const uint32_t sV = smem_u32(sm + kSmV), sDY = smem_u32(sm + kSmDY);
     uint32_t nu = 0, nh = 0, ny = 0;
     for (;; ++nu) {
       const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, t = o.c * pr.Q + i;
-      const bf16 *dyrow = dy + ((size_t)o.bb * pr.L + t) * HP;
       for (int hh = 0; hh < HB; ++hh, ++nh) {
         const int h = o.h0 + hh, vb = nh & 1;
         mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
@@ -454,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float em = (o.c > 0 && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
         pipe::warp_arrive(&bar.vec_free[vb]);
         float r = 0.f;
+        mbar_wait(&bar.dy_full[vb], parity(nh / 2), status);  // dy row i from the head's tile
         if (o.c > 0) {
+          const uint32_t T = sDY + vb * 16384;
           mbar_wait(bar.yo_full, parity(ny), status);
           tc_fence_after();
 #pragma unroll
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t8 = 0; t8 < 2; ++t8) {
               float d8[8];
-              tc::unpack8(tc::ldg16(dyrow + h * pr.P + 16 * cc + 8 * t8), d8);
+              tc::unpack8(pipe::lds_sw128(T, il, 2 * cc + t8), d8);
 #pragma unroll
               for (int e = 0; e < 8; ++e) r = fmaf(d8[e], yo[8 * t8 + e], r);
             }
@@ -474,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ny;
           r *= em;
         }
+        pipe::warp_arrive(&bar.dy_free[vb]);
         tok[3 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = r;
       }
       mbar_wait(bar.dc_full, parity(nu), status);
