@@ -245,20 +245,28 @@ __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float 
           if (e4[u] < PN4) z[q][u] = base[(size_t)(c0 + q) * cstride4 + e4[u]];
       }
     }
+    // the recurrence runs down the chunks; results are kept and stored in
+    // increasing address order afterwards
+    float4 outv[kScanBatch][kScanVec4];
 #pragma unroll
     for (int q = kScanBatch - 1; q >= 0; --q) {
       if (q < nb) {
         const float a = dec[q];
 #pragma unroll
         for (int u = 0; u < kScanVec4; ++u) {
-          if (e4[u] < PN4) {
-            base[(size_t)(c0 + q) * cstride4 + e4[u]] = dS[u];
-            dS[u] = make_float4(fmaf(a, dS[u].x, z[q][u].x), fmaf(a, dS[u].y, z[q][u].y),
-                                fmaf(a, dS[u].z, z[q][u].z), fmaf(a, dS[u].w, z[q][u].w));
-          }
+          outv[q][u] = dS[u];
+          dS[u] = make_float4(fmaf(a, dS[u].x, z[q][u].x), fmaf(a, dS[u].y, z[q][u].y), fmaf(a, dS[u].z, z[q][u].z),
+                              fmaf(a, dS[u].w, z[q][u].w));
         }
       }
     }
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q)
+      if (q < nb) {
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u)
+          if (e4[u] < PN4) base[(size_t)(c0 + q) * cstride4 + e4[u]] = outv[q][u];
+      }
   }
 #pragma unroll
   for (int u = 0; u < kScanVec4; ++u)
