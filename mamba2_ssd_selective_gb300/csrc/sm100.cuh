@@ -62,7 +62,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 constexpr uint64_t kWaitTimeoutNs = 1500ull * 1000ull * 1000ull;
 constexpr uint32_t kWaitHintNs = 20000u;
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // the clock is read only once a parked wait has come back empty-handed, so
+  // that the common hand-off (completed within the first parked wait) does not
+  // carry its latency
+  if (mbar_try_wait(bar, parity) || mbar_try_wait_hint(bar, parity, kWaitHintNs)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait_hint(bar, parity, kWaitHintNs)) return true;

@@ -52,6 +52,33 @@ struct Unit {
   int bb, c, J, h0;
 };
 
+// NP transformed 16-column groups of TMEM lane row `row` into the next NP
+// slots of the A ring (bf16, 128-byte swizzle): each slot waited for only when
+// its values are ready, one proxy fence, then one arrival per slot.
+template <int NP>
+__device__ __forceinline__ void put_operands(const float (&v)[NP][16], uint32_t &na, uint32_t sA, int row, int cg,
+                                             uint64_t *a_full, uint64_t *a_free, int *status) {
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const uint32_t n = na + p, as = n % kNA;
+    float v0[8], v1[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v0[e] = v[p][e];
+      v1[e] = v[p][8 + e];
+    }
+    const uint4 lo = tc::pack8(v0), hi = tc::pack8(v1);
+    if (n >= (uint32_t)kNA) mbar_wait(&a_free[as], pipe::parity(n / kNA - 1), status);
+    const uint32_t A = sA + as * 16384;
+    pipe::sts_u4(A + sw128_offset(row, 16 * cg), lo);
+    pipe::sts_u4(A + sw128_offset(row, 16 * cg + 8), hi);
+  }
+  fence_async_smem();
+#pragma unroll
+  for (int p = 0; p < NP; ++p) pipe::warp_arrive(&a_full[(na + p) % kNA]);
+  na += NP;
+}
+
 // Unit u of the launch, claimed dynamically in this order: the tiles with more
 // work first (every CTA then ends on light ones), and within a tile class the
 // head blocks of one (row, chunk) adjacent, sharing C and B in L2.
@@ -311,22 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tok[prev_tok] = (pipe::lds_f(base) + pipe::lds_f(base + 512)) + (pipe::lds_f(base + 1024) + pipe::lds_f(base + 1536));
       }
     };
-    auto put = [&](const float (&v)[16]) {  // write 16 values of row jl as bf16 into the next A slot
-      const int as = na % kNA;
-      if (na >= (uint32_t)kNA) mbar_wait(&bar.a_free[as], parity(na / kNA - 1), status);
-      float v0[8], v1[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v0[e] = v[e];
-        v1[e] = v[8 + e];
-      }
-      const uint32_t A = sA + as * 16384;
-      pipe::sts_u4(A + sw128_offset(jl, 16 * cg), tc::pack8(v0));
-      pipe::sts_u4(A + sw128_offset(jl, 16 * cg + 8), tc::pack8(v1));
-      fence_async_smem();
-      pipe::warp_arrive(&bar.a_full[as]);
-      ++na;
-    };
     for (;; ++nu) {
       const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
       if (ui >= nunits) break;
@@ -358,13 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float vcol = 0.f;
         for (int s = 0; s < nsl; ++s, ++m) {
           const int rs = m & 1, i0 = 128 * o.J + 64 * s + 16 * cg;
-          float mt[16], wt[16];
+          float mw[2][16];  // M^T, W^T of this slice
           mbar_wait(&bar.ring_full[rs], parity(m / 2), status);
           tc_fence_after();
           if (i0 + 15 < row_lo) {  // every column before every row: zero
             pipe::warp_arrive(&bar.ring_free[rs]);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) mt[e] = wt[e] = 0.f;
+            for (int e = 0; e < 16; ++e) mw[0][e] = mw[1][e] = 0.f;
           } else {
             float dm[16], cbv[16];
             tmem_ld16(pipe::tmem_quad(tmem + 128 * rs, 16 * cg), dm);
@@ -385,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float gi = ok ? gv[k4] : 0.f;
                   const float t1 = gi * ed;
                   vs = fmaf(dm[e + k4] * cbv[e + k4], gi, vs);
-                  mt[e + k4] = cbv[e + k4] * t1;
-                  wt[e + k4] = dm[e + k4] * t1;
+                  mw[0][e + k4] = cbv[e + k4] * t1;
+                  mw[1][e + k4] = dm[e + k4] * t1;
                 }
               }
               vcol = fmaf(vs, e0, vcol);
@@ -402,27 +413,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float ee = ok ? ex2_approx(av[k4] - aj) : 0.f;
                   vcol = fmaf(dm[e + k4] * cbv[e + k4], ee, vcol);
                   const float t1 = ee * dt_j;
-                  mt[e + k4] = cbv[e + k4] * t1;
-                  wt[e + k4] = dm[e + k4] * t1;
+                  mw[0][e + k4] = cbv[e + k4] * t1;
+                  mw[1][e + k4] = dm[e + k4] * t1;
                 }
               }
             }
           }
-          put(mt);
-          put(wt);
+          put_operands<2>(mw, na, sA, jl, cg, bar.a_full, bar.a_free, status);
         }
         {  // wdt_j x_j, the A operand of the dS_end term of dB
           mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);
-          float xv[16];
+          float xv[1][16];
           const uint32_t T = sXT + vb * 16384;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             float x8[8];
             tc::unpack8(pipe::lds_sw128(T, jl, 2 * cg + t), x8);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xv[8 * t + e] = x8[e] * wdt;
+            for (int e = 0; e < 8; ++e) xv[0][8 * t + e] = x8[e] * wdt;
           }
-          put(xv);
+          put_operands<1>(xv, na, sA, jl, cg, bar.a_full, bar.a_free, status);
         }
         pipe::sts_f(sVC + vb * 2048 + cg * 512 + 4 * jl, vcol);
         prev_tok = 2 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + (size_t)o.c * pr.Q + j;

@@ -31,7 +31,7 @@ using pipe::parity;
 
 constexpr int kWarps = 22, kThreads = kWarps * 32, kEpiWarp0 = 18;
 constexpr int kTWarps = 16, kEWarps = 4, kTThreads = kTWarps * 32;
-constexpr int kNX = 3;  // x slice ring
+constexpr int kNX = 2;  // x slice ring
 constexpr int kNA = 2;  // transformed operand ring (W slices, em dy)
 
 constexpr uint32_t kSmC = 0;                    // C_I: 2 K halves x [128 x 128 B]
@@ -39,13 +39,13 @@ constexpr uint32_t kSmB = kSmC + 32768;         // B rows j < 128(I+1): 2 K halv
 constexpr uint32_t kSmDY = kSmB + 65536;        // 2 x dy_h tile [128 x 64] bf16
 constexpr uint32_t kSmX = kSmDY + 2 * 16384;    // ring of x slices [64 x 64] bf16
 constexpr uint32_t kSmA = kSmX + kNX * 8192;    // ring of [128 x 64] bf16 operands
-constexpr uint32_t kSmS = kSmA + kNA * 16384;   // S_in,h: 2 K halves x [64 x 128 B]
+constexpr uint32_t kSmS = kSmA + kNA * 16384;   // 2 x S_in,h: 2 K halves x [64 x 128 B]
 constexpr uint32_t kVecStride = 3200;           // acs[256] | dt[256] | seq[4 + 256]
-constexpr uint32_t kSmV = kSmS + 16384;         // 2 vector buffers
+constexpr uint32_t kSmV = kSmS + 2 * 16384;     // 2 vector buffers
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], b[256], f[256]}
 constexpr uint32_t kSmVR = kSmD + 2 * 3072;     // 2 x vrow partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVR + 2 * 2048;
-constexpr int kNumBars = 20 + 2 * kNX + 2 * kNA + 4;
+constexpr int kNumBars = 22 + 2 * kNX + 2 * kNA + 4;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -72,9 +72,8 @@ __device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int
 }
 
 struct Bars {
-  uint64_t *unit_full, *unit_free, *cb_full, *cb_used, *dm_full, *dm_free, *yo_full, *yo_free, *s_full, *s_free,
-      *dc_full, *dc_free;
-  uint64_t *vec_full, *vec_free, *dy_full, *dy_free;  // [2]
+  uint64_t *unit_full, *unit_free, *cb_full, *cb_used, *dm_full, *dm_free, *yo_full, *yo_free, *dc_full, *dc_free;
+  uint64_t *vec_full, *vec_free, *dy_full, *dy_free, *s_full, *s_free;  // [2]
   uint64_t *x_full, *x_free;                          // [kNX]
   uint64_t *a_full, *a_free;                          // [kNA]
   pipe::UnitRing units;
@@ -87,15 +86,15 @@ struct Bars {
     dm_free = b + 5;
     yo_full = b + 6;
     yo_free = b + 7;
-    s_full = b + 8;
-    s_free = b + 9;
-    dc_full = b + 10;
-    dc_free = b + 11;
-    vec_full = b + 12;
-    vec_free = b + 14;
-    dy_full = b + 16;
-    dy_free = b + 18;
-    x_full = b + 20;
+    dc_full = b + 8;
+    dc_free = b + 9;
+    vec_full = b + 10;
+    vec_free = b + 12;
+    dy_full = b + 14;
+    dy_free = b + 16;
+    s_full = b + 18;
+    s_free = b + 20;
+    x_full = b + 22;
     x_free = x_full + kNX;
     a_full = x_free + kNX;
     a_free = a_full + kNA;
@@ -122,8 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
 
   if (threadIdx.x == 0) {
-    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.cb_full, bar.dm_full,
-                        bar.yo_full,   bar.s_full,    bar.s_free,  bar.dc_full};
+    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.cb_full,   bar.dm_full,  bar.yo_full,
+                        bar.dc_full,   bar.s_full,    bar.s_full + 1, bar.s_free, bar.s_free + 1};
     for (uint64_t *b : ones) mbar_init(b, 1);
     mbar_init(bar.cb_used, kTWarps);
     mbar_init(bar.dm_free, kTWarps);
@@ -201,19 +200,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < 2; ++r)
             tma_load_2d(sm + kSmDY + vb * 16384 + r * 8192, &tm_dy, &bar.dy_full[vb], h * pr.P,
                         row0 + 128 * o.I + 64 * r);
+          if (o.c > 0) {  // S_in first: a whole head of slack before its use
+            const int sb = ns & 1;
+            if (ns >= 2) mbar_wait(&bar.s_free[sb], parity(ns / 2 - 1), status);
+            mbar_expect_tx(&bar.s_full[sb], 16384);
+            const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
+            tma_load_2d(sm + kSmS + sb * 16384, &tm_s, &bar.s_full[sb], 0, srow);
+            tma_load_2d(sm + kSmS + sb * 16384 + 8192, &tm_s, &bar.s_full[sb], 64, srow);
+            ++ns;
+          }
           for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
             const int slot = k % kNX;
             if (k >= kNX) mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status);
             mbar_expect_tx(&bar.x_full[slot], 8192);
             tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
-          }
-          if (o.c > 0) {
-            if (ns >= 1) mbar_wait(bar.s_free, parity(ns - 1), status);
-            mbar_expect_tx(bar.s_full, 16384);
-            const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
-            tma_load_2d(sm + kSmS, &tm_s, bar.s_full, 0, srow);
-            tma_load_2d(sm + kSmS + 8192, &tm_s, bar.s_full, 64, srow);
-            ++ns;
           }
         }
       }
@@ -274,19 +274,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           k += nsl;
           if (o.c > 0) {
-            mbar_wait(bar.s_full, parity(ns), status);
+            const int sb = ns & 1;
+            const uint64_t dSb = dS + sb * (16384 / 16);
+            mbar_wait(&bar.s_full[sb], parity(ns / 2), status);
             if (ns > 0) mbar_wait(bar.yo_free, parity(ns - 1), status);
             tc_fence_after();
-            pipe::umma_k<4>(tmem + kTmYo, dC, dS, pipe::kStepK, pipe::kStepK, id_yo, false);
-            pipe::umma_k<4>(tmem + kTmYo, dC + 16384 / 16, dS + 8192 / 16, pipe::kStepK, pipe::kStepK, id_yo, true);
+            pipe::umma_k<4>(tmem + kTmYo, dC, dSb, pipe::kStepK, pipe::kStepK, id_yo, false);
+            pipe::umma_k<4>(tmem + kTmYo, dC + 16384 / 16, dSb + 8192 / 16, pipe::kStepK, pipe::kStepK, id_yo, true);
             umma_commit(bar.yo_full);
             const int as = na % kNA;
             mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             tc_fence_after();
-            pipe::umma_k<4>(tmem + kTmDC, dA + as * (16384 / 16), dSmn, pipe::kStepK, pipe::kStepMN, id_dc, true);
+            pipe::umma_k<4>(tmem + kTmDC, dA + as * (16384 / 16), dSmn + sb * (16384 / 16), pipe::kStepK, pipe::kStepMN,
+                            id_dc, true);
             umma_commit(&bar.a_free[as]);
             ++na;
-            umma_commit(bar.s_free);
+            umma_commit(&bar.s_free[sb]);
             ++ns;
           }
           umma_commit(&bar.dy_free[vb]);
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bar.x_free[m % kNX], parity(m / kNX), status);
       for (uint32_t m = na > (uint32_t)kNA ? na - kNA : 0u; m < na; ++m)
         mbar_wait(&bar.a_free[m % kNA], parity(m / kNA), status);
-      if (ns > 0) mbar_wait(bar.s_free, parity(ns - 1), status);
+      for (uint32_t m = ns > 2u ? ns - 2u : 0u; m < ns; ++m) mbar_wait(&bar.s_free[m & 1], parity(m / 2), status);
       for (uint32_t m = nh > 2u ? nh - 2u : 0u; m < nh; ++m) mbar_wait(&bar.dy_free[m & 1], parity(m / 2), status);
     }
   } else if (warp < kEpiWarp0) {

@@ -44,8 +44,8 @@ constexpr int kWarps = 22;
 constexpr int kEpiWarp0 = 18;
 constexpr int kThreads = kWarps * 32;
 constexpr int kNA = 2;   // A slice ring (transform -> MMA, on chip)
-constexpr int kNX = 8;   // X slice ring (TMA -> MMA; deep enough to cover the load latency)
-constexpr int kNSB = 1;  // S_in buffers (a head of slack between load and use)
+constexpr int kNX = 6;   // X slice ring (TMA -> MMA; deep enough to cover the load latency)
+constexpr int kNSB = 2;  // S_in buffers (loaded a head ahead of use)
 
 // shared memory map, offsets from the 1024-aligned base
 constexpr uint32_t kSmC = 0;                     // C_I: 2 K halves x [128 rows x 128 B]
@@ -206,12 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
           }
-          for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
-            const int slot = k % kNX;
-            if (k >= kNX) mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status);
-            mbar_expect_tx(&bar.x_full[slot], 8192);
-            tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
-          }
           if (o.c > 0) {
             const int sb = ns % kNSB;
             if (ns >= kNSB) mbar_wait(&bar.s_free[sb], parity(ns / kNSB - 1), status);
@@ -220,6 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + kSmS + sb * 16384, &tm_s, &bar.s_full[sb], 0, srow);
             tma_load_2d(sm + kSmS + sb * 16384 + 8192, &tm_s, &bar.s_full[sb], 64, srow);
             ++ns;
+          }
+          for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
+            const int slot = k % kNX;
+            if (k >= kNX) mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status);
+            mbar_expect_tx(&bar.x_full[slot], 8192);
+            tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
           }
         }
       }
@@ -323,17 +323,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kTransformThreads) : "memory");
         const float ai = pipe::lds_f(da + 4 * i);
-        for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
-          const int slot = k % kNA;
-          if (k >= kNA) mbar_wait(&bar.a_free[slot], parity(k / kNA - 1), status);
-          const int j0 = 64 * s + 16 * cg;
-          uint4 pk[2];
-          if (j0 > row_hi) {
-            pk[0] = pk[1] = make_uint4(0u, 0u, 0u, 0u);
-          } else {
-            float v[16], r[16];
-            tmem_ld16(pipe::tmem_quad(tmem, j0), v);
-            if (row_lo >= j0 + 15) {  // whole group below the diagonal: factorised decay
+        // two 64-column slices per pass (a head has 2 or 4): both TMEM loads in
+        // flight at once, one proxy fence and two arrivals; the ring slots are
+        // waited for only when the values are ready to be stored
+        for (int s = 0; s < 2 * (o.I + 1); s += 2, k += 2) {
+          uint32_t raw[2][16];
+          bool live[2];
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            const int j0 = 64 * (s + p) + 16 * cg;
+            live[p] = j0 <= row_hi;  // warp-uniform
+            if (live[p]) {
+              tmem_ld16_async(pipe::tmem_quad(tmem, j0), raw[p]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) raw[p][e] = 0u;
+            }
+          }
+          tmem_wait_ld(raw[0], raw[1]);
+          uint4 pk[2][2];
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            const int j0 = 64 * (s + p) + 16 * cg;
+            float r[16];
+            if (!live[p]) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) r[e] = 0.f;
+            } else if (row_lo >= j0 + 15) {  // whole group below the diagonal: factorised decay
               const float ei = ex2_approx(ai - pipe::lds_f(da + 4 * (j0 + 15)));
               const bool nomask = __all_sync(0xffffffffu, start_i <= j0);
 #pragma unroll
@@ -342,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                  const float val = v[e + m] * fv[m] * ei;
+                  const float val = __uint_as_float(raw[p][e + m]) * fv[m] * ei;
                   r[e + m] = (nomask || j0 + e + m >= start_i) ? val : 0.f;
                 }
               }
@@ -354,7 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                   const int j = j0 + e + m;
-                  r[e + m] = (unsigned)(j - start_i) <= (unsigned)(i - start_i) ? v[e + m] * ex2_approx(ai + bv[m]) : 0.f;
+                  r[e + m] = (unsigned)(j - start_i) <= (unsigned)(i - start_i)
+                                 ? __uint_as_float(raw[p][e + m]) * ex2_approx(ai + bv[m])
+                                 : 0.f;
                 }
               }
             }
@@ -364,14 +382,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               r0[m] = r[m];
               r1[m] = r[8 + m];
             }
-            pk[0] = tc::pack8(r0);
-            pk[1] = tc::pack8(r1);
+            pk[p][0] = tc::pack8(r0);
+            pk[p][1] = tc::pack8(r1);
           }
-          const uint32_t A = sA + slot * 16384;
-          pipe::sts_u4(A + sw128_offset(il, 16 * cg), pk[0]);
-          pipe::sts_u4(A + sw128_offset(il, 16 * cg + 8), pk[1]);
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            const uint32_t kp = k + p, slot = kp % kNA;
+            if (kp >= (uint32_t)kNA) mbar_wait(&bar.a_free[slot], parity(kp / kNA - 1), status);
+            const uint32_t A = sA + slot * 16384;
+            pipe::sts_u4(A + sw128_offset(il, 16 * cg), pk[p][0]);
+            pipe::sts_u4(A + sw128_offset(il, 16 * cg + 8), pk[p][1]);
+          }
           fence_async_smem();
-          pipe::warp_arrive(&bar.a_full[slot]);
+#pragma unroll
+          for (int p = 0; p < 2; ++p) pipe::warp_arrive(&bar.a_full[(k + p) % kNA]);
         }
         pipe::warp_arrive(&bar.vec_free[vb]);
       }
