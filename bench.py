@@ -163,17 +163,18 @@ def kernel_work(shape, dtype: str) -> dict:
         "conv_fwd": ("mem", 0, b * L * Cd * 2 * eb),
         "dt_prep": ("mem", 0, b * L * H * (eb + 8)),
         "decay_tables": ("mem", 0, tok + 3 * b * H * nc * 4),
-        "local_pass": ("mem", 0, 2 * st + seg),
+        # bf16 tensor-core path: the local pass only reduces (its combine re-forms the local states)
+        "local_pass": ("mem", 0, (st if dtype == "bf16" else 2 * st) + seg),
         "seg_scan": ("mem", 0, 2 * seg + b * H * PN * 4),
         "combine_state": ("mem", 0, st + st16 + seg),
         "local_rev": ("mem", 0, 2 * st + seg),
         "seg_rscan": ("mem", 0, 2 * seg),
         # bf16 path: the states' decay term (combine_bwd) and dy . x (tc_bwd_col) come precomputed
         "chunk_dt": ("mem", 0, 6 * tok + (0 if dtype == "bf16" else 4 * st + 2 * x) + b * L * H * eb),
-        "combine_bwd": ("mem", 0, 2 * st + 2 * seg + 2 * st16 + b * nc * H * 4),
+        "combine_bwd": ("mem", 0, 2 * st + 2 * seg + 2 * st16 + b * nc * H * 4 * ((P * N + 2047) // 2048)),
         "bc_reduce": ("mem", 0, 2 * parts + 2 * b * L * GN * 4),
-        "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 32) * Cd * 20),
-        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 32) * Cd * 20),
+        "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 64) * Cd * 20),
+        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 64) * Cd * 20),
         "tc_chunk_state": ("tensor", f_state, x + bc + st),
         "tc_chunk_z": ("tensor", f_state, x + bc + st),
         # persistent kernels: CB is formed on chip, W never leaves the SM

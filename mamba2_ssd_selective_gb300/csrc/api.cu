@@ -156,7 +156,7 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
-                                                 const_cast<float *>(pr.dend), s));
+                                                 const_cast<float *>(pr.dend), ablk, s));
   if constexpr (kIsBf16<T>) {
     if (tc) SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));  // CB: inside tc_out
   }
@@ -164,12 +164,13 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
     SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
     SSD_LAUNCH("chunk_state", launch_chunk_state<T>(pr, u, dtv, acs, sst, s));
   }
-  SSD_LAUNCH("local_pass", launch_local_pass(pr, acs, sst, sext, ablk, s));
+  // the tensor-core path re-forms the local states from Sc in its combine pass
+  SSD_LAUNCH("local_pass", launch_local_pass(pr, sst, sext, !tc, s));
   SSD_LAUNCH("seg_scan", launch_seg_scan(pr, sext, ablk, segin, final_state, s));
   if constexpr (kIsBf16<T>) {
     if (tc) {
       __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
-      SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, 0, s));
+      SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, s));
       SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, sin16, y, status, s));
     }
   }
@@ -198,7 +199,7 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
-                                                 const_cast<float *>(pr.dend), s));
+                                                 const_cast<float *>(pr.dend), ablk, s));
   if constexpr (kIsBf16<T>) {
     if (tc) SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));  // CB: in-kernel
   }
@@ -206,7 +207,9 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
     SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
     SSD_LAUNCH("chunk_state", launch_chunk_state<T>(pr, u, dtv, acs, sst, s));
   }
-  SSD_LAUNCH("local_pass", launch_local_pass(pr, acs, sst, sext, ablk, s));
+  // with the forward's segment states given, the tensor-core path needs no local
+  // pass (its combine re-forms the local states from Sc)
+  if (!tc || !segin_user) SSD_LAUNCH("local_pass", launch_local_pass(pr, sst, sext, !tc, s));
   const float *segin = segin_user;
   if (!segin) {
     float *sg = reinterpret_cast<float *>(ws + w.segin);
@@ -222,13 +225,13 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   SSD_LAUNCH("seg_rscan", launch_seg_rscan(pr, gext, ablk, dfinal, gout, s));
   // chunk gradients
   int vcol_parts = 1, nsub = pr.H, spg = pr.hpg;
-  float *sdot = nullptr;  // a_c <dS_end, S_in> per chunk, when the combine pass computes it
+  float *sdp = nullptr;  // partial <dS_end, S_in> per chunk and element group, when the combine pass computes it
   if constexpr (kIsBf16<T>) {
     if (tc) {
       __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
       __nv_bfloat16 *dse16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.dse16);
-      sdot = chs + 3 * (size_t)pr.b * pr.nc * pr.H;  // free slot of the per-chunk scalars
-      SSD_LAUNCH("combine_bwd", launch_combine_bwd(pr, sst, segin, dsl, gout, sin16, dse16, sdot, s));
+      sdp = reinterpret_cast<float *>(ws + w.sdp);
+      SSD_LAUNCH("combine_bwd", launch_combine_bwd(pr, sst, segin, dsl, gout, sin16, dse16, sdp, s));
       SSD_LAUNCH("tc_bwd_row", launch_tc_bwd_row(pr, u, dy, dtv, acs, sin16, dcp, tok, status, s));
       SSD_LAUNCH("tc_bwd_col", launch_tc_bwd_col(pr, u, dy, dtv, acs, dse16, du, dbp, tok, status, s));
       vcol_parts = 1;
@@ -243,7 +246,8 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
                launch_chunk_dcdb<T>(pr, u, dy, dtv, acs, wbuf, sst, segin, dsl, gout, dcp, dbp, tok, s));
   }
   SSD_LAUNCH("chunk_dt",
-             launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, sdot, go, chs, s));
+             launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, sdp, scan_groups(pr), go,
+                                chs, s));
   SSD_LAUNCH("bc_reduce", launch_bc_reduce(pr, dcp, dbp, nsub, spg, du, s));
   // conv backward and parameter reductions
   SSD_LAUNCH("conv_bwd", launch_conv_bwd<T>(pr, du, go, convp, w.ntb, s));

@@ -63,10 +63,23 @@ __device__ __forceinline__ size_t dtab_index(const Problem &pr, int b, int h, in
 __device__ __forceinline__ float chunk_decay(const Problem &pr, int b, int h, int c) {
   return __ldg(pr.cdec + dtab_index(pr, b, h, c));
 }
+// decay from the start of chunk c's segment to the start of c, and from the end
+// of c to the end of its segment
+__device__ __forceinline__ float decay_start(const Problem &pr, int b, int h, int c) {
+  return __ldg(pr.dstart + dtab_index(pr, b, h, c));
+}
+__device__ __forceinline__ float decay_end(const Problem &pr, int b, int h, int c) {
+  return __ldg(pr.dend + dtab_index(pr, b, h, c));
+}
 
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kConvBwdTok = 64;  // tokens per conv-backward block (one set of parameter partials each)
+
+// Elements of the P x N state handled by one block of the segment-walk kernels
+// (local pass, reverse pass, combines): 256 threads x two float4 groups.
+constexpr int kScanGroupElems = 2048;
+inline int scan_groups(const Problem &pr) { return (pr.P * pr.N + kScanGroupElems - 1) / kScanGroupElems; }
 
 // The workspace starts with the device status word followed by one work
 // counter per persistent kernel (zeroed with the status at every pass).
@@ -95,6 +108,7 @@ struct Workspace {
   size_t tok;                                  // 6 x (b, H, L) f32 per-token adjoint pieces
   size_t dcp, dbp;                             // (b, L, H, N) f32 per-head dC / dB partials
   size_t chs;                                  // 4 x (b, nc, H) f32 per-chunk scalars
+  size_t sdp;                                  // (scan groups, b, nc, H) f32: partial <dS, S_in> (tensor-core path)
   size_t convp;                                // (b, ntb, Cd, 5) f32 conv parameter partials
   size_t total;
   int ntb;                                     // conv backward token blocks per row
@@ -135,6 +149,7 @@ inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward
     w.dcp = take(b * L * H * N * 4);
     w.dbp = take(b * L * H * N * 4);
     w.chs = take(4 * b * nc * H * 4);
+    w.sdp = take(tc ? (size_t)scan_groups(pr) * b * nc * H * 4 : 0);
     w.convp = take(b * (size_t)w.ntb * Cd * 5 * 4);
   }
   w.total = off;

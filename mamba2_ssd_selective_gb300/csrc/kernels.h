@@ -21,12 +21,13 @@ void launch_param_reduce(const Problem &pr, const float *chs, const float *convp
 void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStream_t s);
 
 // segment summaries and scans (scan.cu)
-void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, cudaStream_t s);
-void launch_combine_state(const Problem &pr, const float *a, const float *seg, __nv_bfloat16 *out, int mode,
-                          cudaStream_t s);
-void launch_combine_bwd(const Problem &pr, const float *sst, const float *segin, const float *dsl, const float *gout,
-                        __nv_bfloat16 *sin16, __nv_bfloat16 *dse16, float *sdot, cudaStream_t s);
-void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s);
+void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, float *ablk,
+                         cudaStream_t s);
+// sc: the chunk states Sc (the local states are re-formed inside)
+void launch_combine_state(const Problem &pr, const float *sc, const float *segin, __nv_bfloat16 *out, cudaStream_t s);
+void launch_combine_bwd(const Problem &pr, const float *sc, const float *segin, const float *dsl, const float *gout,
+                        __nv_bfloat16 *sin16, __nv_bfloat16 *dse16, float *sdp, cudaStream_t s);
+void launch_local_pass(const Problem &pr, float *sst, float *sext, bool write_local, cudaStream_t s);
 void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, float *segin, float *final_state,
                      cudaStream_t s);
 void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s);
@@ -55,7 +56,8 @@ void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *
 template <typename T>
 void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
-                     int vcol_parts, const float *sdot, const GradOut &go, float *chs, cudaStream_t s);
+                     int vcol_parts, const float *sdp, int sdp_groups, const GradOut &go, float *chs,
+                     cudaStream_t s);
 // du_B/du_C = fixed-order sums of per-token partials: nsub partials per token,
 // the partials of group g being [g*spg, (g+1)*spg)
 void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int nsub, int spg, float *du,

@@ -20,9 +20,10 @@ constexpr int kScanBatch = 4;  // chunks whose loads are in flight together
 
 // Decay tables of one (b, h): cdec[c] = product of the chunk's per-token decays
 // (from Acs and seq_idx), then per segment the exclusive prefix and suffix
-// products dstart[c] = prod_{c' in seg, c' < c} cdec[c'], dend[c] = prod_{c' > c}.
+// products dstart[c] = prod_{c' in seg, c' < c} cdec[c'], dend[c] = prod_{c' > c},
+// and the segment's whole product a_block[k] (the factor of the affine summary).
 __global__ void __launch_bounds__(256) decay_tables_kernel(Problem pr, const float *__restrict__ acs, float *cdec,
-                                                           float *dstart, float *dend) {
+                                                           float *dstart, float *dend, float *ablk) {
   const int h = blockIdx.x, bb = blockIdx.y;
   const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
   const size_t base = ((size_t)bb * pr.H + h) * pr.nc;
@@ -35,6 +36,7 @@ __global__ void __launch_bounds__(256) decay_tables_kernel(Problem pr, const flo
       dstart[base + c] = d;
       d *= cdec[base + c];
     }
+    ablk[((size_t)bb * pr.S + k) * pr.H + h] = d;
     d = 1.f;
     for (int c = c1 - 1; c >= c0; --c) {
       dend[base + c] = d;
@@ -43,98 +45,27 @@ __global__ void __launch_bounds__(256) decay_tables_kernel(Problem pr, const flo
   }
 }
 
-void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, cudaStream_t s) {
-  decay_tables_kernel<<<dim3(pr.H, pr.b), 256, 0, s>>>(pr, acs, cdec, dstart, dend);
-}
-
-// out[b, c, h] = bf16(a[b, c, h] + d * seg[b, k(c), h]) over the P x N state, with
-// d = dstart (mode 0: the true state entering the chunk) or dend (mode 1: the
-// true state gradient at the chunk end).  8 elements per thread.
-__global__ void __launch_bounds__(256) combine_state_kernel(Problem pr, const float *__restrict__ a,
-                                                            const float *__restrict__ seg,
-                                                            __nv_bfloat16 *__restrict__ out, int mode) {
-  const int PN = pr.P * pr.N;
-  const int e = (blockIdx.x * 256 + threadIdx.x) * 8;
-  const int h = blockIdx.y, bc = blockIdx.z, bb = bc / pr.nc, c = bc % pr.nc, k = c / pr.cps;
-  if (e >= PN) return;
-  const float d = mode == 0 ? __ldg(pr.dstart + dtab_index(pr, bb, h, c)) : __ldg(pr.dend + dtab_index(pr, bb, h, c));
-  const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * PN + e;
-  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * PN + e;
-  const float4 a0 = *reinterpret_cast<const float4 *>(a + co), a1 = *reinterpret_cast<const float4 *>(a + co + 4);
-  const float4 s0 = *reinterpret_cast<const float4 *>(seg + so), s1 = *reinterpret_cast<const float4 *>(seg + so + 4);
-  const float v[8] = {a0.x + d * s0.x, a0.y + d * s0.y, a0.z + d * s0.z, a0.w + d * s0.w,
-                      a1.x + d * s1.x, a1.y + d * s1.y, a1.z + d * s1.z, a1.w + d * s1.w};
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    w[i] = *reinterpret_cast<uint32_t *>(&b2);
-  }
-  *reinterpret_cast<uint4 *>(out + co) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-void launch_combine_state(const Problem &pr, const float *a, const float *seg, __nv_bfloat16 *out, int mode,
-                          cudaStream_t s) {
-  dim3 grid((pr.P * pr.N / 8 + 255) / 256, pr.H, pr.b * pr.nc);
-  combine_state_kernel<<<grid, 256, 0, s>>>(pr, a, seg, out, mode);
-}
-
-// Backward form of the combination, one block per (row, chunk, head): the true
-// state entering the chunk S_in = S_loc + dstart * S_seg and the true state
-// gradient at its end dS = dS_loc + dend * G_out, both written in bf16 (the
-// tensor-core operands), and in fp32 the chunk's decay term of the dt adjoint
-//   sdot[b, c, h] = a_c <dS, S_in>
-// summed in a fixed order (per thread, then the block tree).
-__global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const float *__restrict__ sst,
-                                                          const float *__restrict__ segin,
-                                                          const float *__restrict__ dsl,
-                                                          const float *__restrict__ gout,
-                                                          __nv_bfloat16 *__restrict__ sin16,
-                                                          __nv_bfloat16 *__restrict__ dse16, float *__restrict__ sdot) {
-  __shared__ float red[8];
-  const int PN = pr.P * pr.N;
-  const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z, k = c / pr.cps;
-  const size_t ti = dtab_index(pr, bb, h, c);
-  const float dc = __ldg(pr.dstart + ti), de = __ldg(pr.dend + ti), ac = __ldg(pr.cdec + ti);
-  const size_t co = (((size_t)bb * pr.nc + c) * pr.H + h) * PN;
-  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * PN;
-  float part = 0.f;
-#pragma unroll 4
-  for (int e = threadIdx.x * 4; e < PN; e += 256 * 4) {
-    const float4 a = *reinterpret_cast<const float4 *>(sst + co + e), b = *reinterpret_cast<const float4 *>(segin + so + e);
-    const float4 x = *reinterpret_cast<const float4 *>(dsl + co + e), y = *reinterpret_cast<const float4 *>(gout + so + e);
-    const float sv[4] = {a.x + dc * b.x, a.y + dc * b.y, a.z + dc * b.z, a.w + dc * b.w};
-    const float gv[4] = {x.x + de * y.x, x.y + de * y.y, x.z + de * y.z, x.w + de * y.w};
-    part += gv[0] * sv[0] + gv[1] * sv[1] + gv[2] * sv[2] + gv[3] * sv[3];
-    __nv_bfloat162 s01 = __floats2bfloat162_rn(sv[0], sv[1]), s23 = __floats2bfloat162_rn(sv[2], sv[3]);
-    __nv_bfloat162 g01 = __floats2bfloat162_rn(gv[0], gv[1]), g23 = __floats2bfloat162_rn(gv[2], gv[3]);
-    *reinterpret_cast<uint2 *>(sin16 + co + e) =
-        make_uint2(*reinterpret_cast<uint32_t *>(&s01), *reinterpret_cast<uint32_t *>(&s23));
-    *reinterpret_cast<uint2 *>(dse16 + co + e) =
-        make_uint2(*reinterpret_cast<uint32_t *>(&g01), *reinterpret_cast<uint32_t *>(&g23));
-  }
-  const float tot = block_sum256(part, red);
-  if (threadIdx.x == 0) sdot[((size_t)bb * pr.nc + c) * pr.H + h] = ac != 0.f ? ac * tot : 0.f;
-}
-
-void launch_combine_bwd(const Problem &pr, const float *sst, const float *segin, const float *dsl, const float *gout,
-                        __nv_bfloat16 *sin16, __nv_bfloat16 *dse16, float *sdot, cudaStream_t s) {
-  combine_bwd_kernel<<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, sst, segin, dsl, gout, sin16, dse16, sdot);
+void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, float *ablk,
+                         cudaStream_t s) {
+  decay_tables_kernel<<<dim3(pr.H, pr.b), 256, 0, s>>>(pr, acs, cdec, dstart, dend, ablk);
 }
 
 // Local pass of segment k: S <- a_c * S + Sc[c] over the segment's chunks from
-// S = 0.  Overwrites sst[c] (the chunk's own state contribution Sc) with the
-// local state entering the chunk, and writes S_ext[k] and a_block[k].  Each
-// thread owns two 16-byte groups of state elements (kScanVec4 float4, one per
-// 256-thread stride, so every warp access stays contiguous), reads the chunk
-// decays itself (the same address for the whole block: one broadcast line) and
-// keeps the loads of kScanBatch chunks in flight.  No barriers.
+// S = 0, giving S_ext[k] (the segment's summary; a_block[k] comes with the
+// decay tables).  WriteLocal: also overwrite sst[c] (the chunk's own state
+// contribution Sc) with the local state entering the chunk, for the kernels
+// that read it; the tensor-core path re-forms it in the combine passes instead.
+// Each thread owns two 16-byte groups of state elements (kScanVec4 float4, one
+// per 256-thread stride, so every warp access stays contiguous), reads the
+// chunk decays itself (the same address for the whole block: one broadcast
+// line) and keeps the loads of kScanBatch chunks in flight.  No barriers.
 constexpr int kScanVec4 = 2;
 constexpr int kScanElems4 = 256 * kScanVec4;  // float4 groups per block
+static_assert(kScanElems4 * 4 == kScanGroupElems, "segment-walk block size");
 
-__global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float *__restrict__ acs,
-                                                         float *__restrict__ sst, float *__restrict__ sext,
-                                                         float *__restrict__ ablk) {
+template <bool WriteLocal>
+__global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, float *__restrict__ sst,
+                                                         float *__restrict__ sext) {
   const int PN = pr.P * pr.N, PN4 = PN / 4;
   const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
   const size_t cstride4 = (size_t)pr.H * PN / 4;  // float4 between consecutive chunks
@@ -146,7 +77,6 @@ __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float
     e4[u] = blockIdx.x * kScanElems4 + u * 256 + threadIdx.x;
     S[u] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float prod = 1.f;
   for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
     const int nb = min(kScanBatch, pr.cps - c0);
     float dec[kScanBatch];
@@ -164,11 +94,10 @@ __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float
     for (int q = 0; q < kScanBatch; ++q) {
       if (q < nb) {
         const float a = dec[q];
-        prod *= a;
 #pragma unroll
         for (int u = 0; u < kScanVec4; ++u) {
           if (e4[u] < PN4) {
-            base[(size_t)(c0 + q) * cstride4 + e4[u]] = S[u];
+            if (WriteLocal) base[(size_t)(c0 + q) * cstride4 + e4[u]] = S[u];
             S[u] = make_float4(fmaf(a, S[u].x, v[q][u].x), fmaf(a, S[u].y, v[q][u].y), fmaf(a, S[u].z, v[q][u].z),
                                fmaf(a, S[u].w, v[q][u].w));
           }
@@ -180,12 +109,14 @@ __global__ void __launch_bounds__(256) local_pass_kernel(Problem pr, const float
 #pragma unroll
   for (int u = 0; u < kScanVec4; ++u)
     if (e4[u] < PN4) reinterpret_cast<float4 *>(sext + so * PN)[e4[u]] = S[u];
-  if (blockIdx.x == 0 && threadIdx.x == 0) ablk[so] = prod;
 }
 
-void launch_local_pass(const Problem &pr, const float *acs, float *sst, float *sext, float *ablk, cudaStream_t s) {
-  dim3 grid((pr.P * pr.N / 4 + kScanElems4 - 1) / kScanElems4, pr.H, pr.b * pr.S);
-  local_pass_kernel<<<grid, 256, 0, s>>>(pr, acs, sst, sext, ablk);
+void launch_local_pass(const Problem &pr, float *sst, float *sext, bool write_local, cudaStream_t s) {
+  dim3 grid(scan_groups(pr), pr.H, pr.b * pr.S);
+  if (write_local)
+    local_pass_kernel<true><<<grid, 256, 0, s>>>(pr, sst, sext);
+  else
+    local_pass_kernel<false><<<grid, 256, 0, s>>>(pr, sst, sext);
 }
 
 // Exclusive scan: S_in[0] = 0, S_in[k] = a_block[k-1] * S_in[k-1] + S_ext[k-1];
@@ -276,6 +207,155 @@ __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float 
 void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s) {
   dim3 grid((pr.P * pr.N / 4 + kScanElems4 - 1) / kScanElems4, pr.H, pr.b * pr.S);
   local_rev_kernel<<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
+}
+
+// 4 floats -> 4 bf16 (8 bytes)
+__device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  return make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+}
+
+// Forward combination, walking the chunks of segment k like the local pass:
+//   S_in[c] = S_loc[c] + dstart[c] * S_seg[k]   (the true state entering chunk c, bf16)
+//   S_loc[c + 1] = a_c * S_loc[c] + Sc[c],  S_loc[first] = 0,
+// so the local states are re-formed from the chunk states Sc instead of being
+// read back.  S_seg[k] is read once per segment.
+__global__ void __launch_bounds__(256) combine_fwd_kernel(Problem pr, const float *__restrict__ sc,
+                                                          const float *__restrict__ segin,
+                                                          __nv_bfloat16 *__restrict__ out) {
+  const int PN = pr.P * pr.N, PN4 = PN / 4;
+  const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
+  const size_t cstride4 = (size_t)pr.H * PN / 4;
+  const size_t first = (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN / 4;  // float4 index
+  const float4 *sc4 = reinterpret_cast<const float4 *>(sc) + first;
+  uint2 *out4 = reinterpret_cast<uint2 *>(out) + first;
+  const float4 *g4 = reinterpret_cast<const float4 *>(segin + (((size_t)bb * pr.S + k) * pr.H + h) * PN);
+  int e4[kScanVec4];
+  float4 S[kScanVec4], G[kScanVec4];
+#pragma unroll
+  for (int u = 0; u < kScanVec4; ++u) {
+    e4[u] = blockIdx.x * kScanElems4 + u * 256 + threadIdx.x;
+    S[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    G[u] = e4[u] < PN4 ? g4[e4[u]] : S[u];
+  }
+  for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
+    const int nb = min(kScanBatch, pr.cps - c0);
+    float dec[kScanBatch], dst[kScanBatch];
+    float4 v[kScanBatch][kScanVec4];
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q < nb) {
+        dec[q] = chunk_decay(pr, bb, h, k * pr.cps + c0 + q);
+        dst[q] = decay_start(pr, bb, h, k * pr.cps + c0 + q);
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u)
+          if (e4[u] < PN4) v[q][u] = sc4[(size_t)(c0 + q) * cstride4 + e4[u]];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q < nb) {
+        const float a = dec[q], d = dst[q];
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u) {
+          if (e4[u] < PN4) {
+            out4[(size_t)(c0 + q) * cstride4 + e4[u]] =
+                pack4_bf16(S[u].x + d * G[u].x, S[u].y + d * G[u].y, S[u].z + d * G[u].z, S[u].w + d * G[u].w);
+            S[u] = make_float4(fmaf(a, S[u].x, v[q][u].x), fmaf(a, S[u].y, v[q][u].y), fmaf(a, S[u].z, v[q][u].z),
+                               fmaf(a, S[u].w, v[q][u].w));
+          }
+        }
+      }
+    }
+  }
+}
+
+void launch_combine_state(const Problem &pr, const float *sc, const float *segin, __nv_bfloat16 *out,
+                          cudaStream_t s) {
+  combine_fwd_kernel<<<dim3(scan_groups(pr), pr.H, pr.b * pr.S), 256, 0, s>>>(pr, sc, segin, out);
+}
+
+// Backward combination, walking the chunks of segment k: the true state
+// entering chunk c (re-formed from the chunk states Sc as in the forward
+// combination) and the true state gradient at its end
+//   S_in[c] = S_loc[c] + dstart[c] * S_seg[k],   dS[c] = dS_loc[c] + dend[c] * G_out[k],
+// both written in bf16 (the tensor-core operands), and the block's partial of
+// the chunk's decay term of the dt adjoint, sdp[g, b, c, h] = <dS[c], S_in[c]>
+// over this block's elements (fp32; the consumer multiplies by a_c and sums
+// the groups in order).  S_seg and G_out are read once per segment.
+__global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const float *__restrict__ sc,
+                                                          const float *__restrict__ segin,
+                                                          const float *__restrict__ dsl,
+                                                          const float *__restrict__ gout,
+                                                          __nv_bfloat16 *__restrict__ sin16,
+                                                          __nv_bfloat16 *__restrict__ dse16, float *__restrict__ sdp) {
+  __shared__ float red[8];
+  const int PN = pr.P * pr.N, PN4 = PN / 4;
+  const int h = blockIdx.y, k = blockIdx.z % pr.S, bb = blockIdx.z / pr.S;
+  const size_t cstride4 = (size_t)pr.H * PN / 4;
+  const size_t first = (((size_t)bb * pr.nc + (size_t)k * pr.cps) * pr.H + h) * PN / 4;
+  const float4 *sc4 = reinterpret_cast<const float4 *>(sc) + first, *z4 = reinterpret_cast<const float4 *>(dsl) + first;
+  uint2 *s16 = reinterpret_cast<uint2 *>(sin16) + first, *d16 = reinterpret_cast<uint2 *>(dse16) + first;
+  const size_t so = (((size_t)bb * pr.S + k) * pr.H + h) * PN;
+  const float4 *gi4 = reinterpret_cast<const float4 *>(segin + so), *go4 = reinterpret_cast<const float4 *>(gout + so);
+  int e4[kScanVec4];
+  float4 S[kScanVec4], GI[kScanVec4], GO[kScanVec4];
+#pragma unroll
+  for (int u = 0; u < kScanVec4; ++u) {
+    e4[u] = blockIdx.x * kScanElems4 + u * 256 + threadIdx.x;
+    S[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    GI[u] = e4[u] < PN4 ? gi4[e4[u]] : S[u];
+    GO[u] = e4[u] < PN4 ? go4[e4[u]] : S[u];
+  }
+  const size_t BNH = (size_t)pr.b * pr.nc * pr.H;
+  for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
+    const int nb = min(kScanBatch, pr.cps - c0);
+    float dec[kScanBatch], dst[kScanBatch], den[kScanBatch];
+    float4 v[kScanBatch][kScanVec4], z[kScanBatch][kScanVec4];
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q < nb) {
+        const int c = k * pr.cps + c0 + q;
+        dec[q] = chunk_decay(pr, bb, h, c);
+        dst[q] = decay_start(pr, bb, h, c);
+        den[q] = decay_end(pr, bb, h, c);
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u)
+          if (e4[u] < PN4) {
+            v[q][u] = sc4[(size_t)(c0 + q) * cstride4 + e4[u]];
+            z[q][u] = z4[(size_t)(c0 + q) * cstride4 + e4[u]];
+          }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (q >= nb) break;  // block-uniform
+      const float a = dec[q], dc = dst[q], de = den[q];
+      float part = 0.f;
+#pragma unroll
+      for (int u = 0; u < kScanVec4; ++u) {
+        if (e4[u] < PN4) {
+          const float sv[4] = {S[u].x + dc * GI[u].x, S[u].y + dc * GI[u].y, S[u].z + dc * GI[u].z,
+                               S[u].w + dc * GI[u].w};
+          const float gv[4] = {z[q][u].x + de * GO[u].x, z[q][u].y + de * GO[u].y, z[q][u].z + de * GO[u].z,
+                               z[q][u].w + de * GO[u].w};
+          part += gv[0] * sv[0] + gv[1] * sv[1] + gv[2] * sv[2] + gv[3] * sv[3];
+          s16[(size_t)(c0 + q) * cstride4 + e4[u]] = pack4_bf16(sv[0], sv[1], sv[2], sv[3]);
+          d16[(size_t)(c0 + q) * cstride4 + e4[u]] = pack4_bf16(gv[0], gv[1], gv[2], gv[3]);
+          S[u] = make_float4(fmaf(a, S[u].x, v[q][u].x), fmaf(a, S[u].y, v[q][u].y), fmaf(a, S[u].z, v[q][u].z),
+                             fmaf(a, S[u].w, v[q][u].w));
+        }
+      }
+      const float tot = block_sum256(part, red);
+      if (threadIdx.x == 0) sdp[blockIdx.x * BNH + ((size_t)bb * pr.nc + k * pr.cps + c0 + q) * pr.H + h] = tot;
+    }
+  }
+}
+
+void launch_combine_bwd(const Problem &pr, const float *sc, const float *segin, const float *dsl, const float *gout,
+                        __nv_bfloat16 *sin16, __nv_bfloat16 *dse16, float *sdp, cudaStream_t s) {
+  combine_bwd_kernel<<<dim3(scan_groups(pr), pr.H, pr.b * pr.S), 256, 0, s>>>(pr, sc, segin, dsl, gout, sin16, dse16,
+                                                                             sdp);
 }
 
 // Reverse exclusive scan: G_out[S-1] = dfinal; G_out[k-1] = a_block[k]*G_out[k] + g_ext[k].

@@ -386,7 +386,7 @@ void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *
                                                           tok);
 }
 
-// dt / A / D gradients of one (chunk, head).  On the tensor-core path (sdot
+// dt / A / D gradients of one (chunk, head).  On the tensor-core path (sdp
 // given) the chunk's decay term and the per-token dy . x come precomputed.
 // With vcol = sum over the
 // vcol_parts per-row-tile partial column sums (tok[2], tok[5]) and dAcs_i the
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
                                                      const float *__restrict__ sst, const float *__restrict__ segin,
                                                      const float *__restrict__ dsl, const float *__restrict__ gout,
                                                      const float *__restrict__ tok, int vcol_parts,
-                                                     const float *__restrict__ sdot, GradOut go,
+                                                     const float *__restrict__ sdp, int sdp_groups, GradOut go,
                                                      float *__restrict__ chs) {
   __shared__ ChunkVecs v;
   __shared__ float red[8], dacs[256], dda[256];
@@ -414,9 +414,10 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   const float ac = chunk_decay(pr, id.bb, id.h, id.c);
   const size_t so = (((size_t)id.bb * pr.S + k) * pr.H + id.h) * PN;
   const size_t co = (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * PN;
-  // a_c <dS_end, S_in>, precomputed with the bf16 operands when sdot is given
+  // a_c <dS_end, S_in>; on the tensor-core path the combine pass left one
+  // partial sum per group of state elements (sdp), added here in order
   float part = 0.f;
-  if (!sdot && ac != 0.f) {
+  if (!sdp && ac != 0.f) {
     const float4 *a4 = reinterpret_cast<const float4 *>(dsl + co), *g4 = reinterpret_cast<const float4 *>(gout + so);
     const float4 *s4 = reinterpret_cast<const float4 *>(sst + co), *q4 = reinterpret_cast<const float4 *>(segin + so);
     for (int e = threadIdx.x; e < PN / 4; e += 256) {
@@ -425,7 +426,15 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
               (a.z + de * g.z) * (x.z + dc * y.z) + (a.w + de * g.w) * (x.w + dc * y.w);
     }
   }
-  const float dec = sdot ? sdot[((size_t)id.bb * pr.nc + id.c) * pr.H + id.h] : ac * block_sum256(part, red);
+  float dec;
+  if (sdp) {
+    const size_t BNH = (size_t)pr.b * pr.nc * pr.H, ci = ((size_t)id.bb * pr.nc + id.c) * pr.H + id.h;
+    float tot = 0.f;
+    for (int g = 0; g < sdp_groups; ++g) tot += sdp[g * BNH + ci];
+    dec = ac != 0.f ? ac * tot : 0.f;
+  } else {
+    dec = ac * block_sum256(part, red);
+  }
 
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
   const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
@@ -472,7 +481,7 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
     *dst = from_f<T>(dz);
     const T *xr = u + ((size_t)id.bb * pr.L + t) * Cd + id.h * P;
     const T *dyr = dy + ((size_t)id.bb * pr.L + t) * HP + id.h * P;
-    if (sdot) {  // tensor-core path: dy_t . x_t was written to tok[5] by the column kernel
+    if (sdp) {  // tensor-core path: dy_t . x_t was written to tok[5] by the column kernel
       dD_part = tok[5 * BHL + tb + i];
     } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
       for (int p = 0; p < P; p += 8) {
@@ -502,9 +511,10 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
 template <typename T>
 void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
-                     int vcol_parts, const float *sdot, const GradOut &go, float *chs, cudaStream_t s) {
+                     int vcol_parts, const float *sdp, int sdp_groups, const GradOut &go, float *chs,
+                     cudaStream_t s) {
   dt_bwd_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok,
-                                                            vcol_parts, sdot, go, chs);
+                                                            vcol_parts, sdp, sdp_groups, go, chs);
 }
 
 // du_B[t, g, n] = sum of the group's partials of dB[t, n] (one per head, or one
@@ -549,7 +559,7 @@ void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int
                                      float *, float *, float *, cudaStream_t);                                       \
   template void launch_chunk_dt<T>(const Problem &, const T *, const T *, const float *, const float *,              \
                                    const float *, const float *, const float *, const float *, const float *, int,   \
-                                   const float *, const GradOut &, float *, cudaStream_t);
+                                   const float *, int, const GradOut &, float *, cudaStream_t);
 
 SSD_INST(float)
 SSD_INST(__nv_bfloat16)
