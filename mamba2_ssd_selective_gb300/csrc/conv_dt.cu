@@ -12,39 +12,6 @@
 
 namespace ssd {
 
-template <typename T>
-__device__ __forceinline__ const T *raw_channel(const Problem &pr, int bb, int c, long long &stride) {
-  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
-  if (c < HP) {
-    stride = pr.xs;
-    return static_cast<const T *>(pr.x) + (size_t)bb * pr.L * pr.xs + c;
-  }
-  if (c < HP + GN) {
-    stride = pr.Bs;
-    return static_cast<const T *>(pr.B) + (size_t)bb * pr.L * pr.Bs + (c - HP);
-  }
-  stride = pr.Cs;
-  return static_cast<const T *>(pr.C) + (size_t)bb * pr.L * pr.Cs + (c - HP - GN);
-}
-
-__device__ __forceinline__ void grad_channel(const Problem &pr, const GradOut &go, int bb, int c, void *&base,
-                                             long long &stride, int elem) {
-  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
-  char *p;
-  if (c < HP) {
-    stride = go.dxs;
-    p = static_cast<char *>(go.dx) + ((size_t)bb * pr.L * go.dxs + c) * elem;
-  } else if (c < HP + GN) {
-    stride = go.dBs;
-    p = static_cast<char *>(go.dB) + ((size_t)bb * pr.L * go.dBs + (c - HP)) * elem;
-  } else {
-    stride = go.dCs;
-    p = static_cast<char *>(go.dC) + ((size_t)bb * pr.L * go.dCs + (c - HP - GN)) * elem;
-  }
-  base = p;
-}
-
-
 // 8 consecutive channels of one token as fp32 (16-byte loads for bf16)
 template <typename T> __device__ __forceinline__ void load8(const T *p, float (&v)[8]);
 template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[8]) {
@@ -113,6 +80,47 @@ template <> __device__ __forceinline__ void store4<float>(float *p, const float 
   *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
+// A tile of kCh channels that lies inside one of the x, B, C regions of xBC
+// (tiles are numbered region by region, the last tile of a region may be
+// partial): its raw-input and gradient bases for batch row bb, token strides,
+// first channel (global and within the region) and width.
+template <typename T> struct ChanTile {
+  const T *src;
+  T *grad;
+  long long st, gst;
+  int c0, nch;
+};
+template <typename T>
+__device__ __forceinline__ ChanTile<T> chan_tile(const Problem &pr, const GradOut *go, int bb, int tile, int kCh) {
+  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
+  const int ntx = (HP + kCh - 1) / kCh, ntg = (GN + kCh - 1) / kCh;
+  ChanTile<T> ct;
+  int rc0, width;
+  const void *base;
+  void *gbase = nullptr;
+  long long st, gst = 0;
+  if (tile < ntx) {
+    rc0 = tile * kCh, width = HP, ct.c0 = rc0, base = pr.x, st = pr.xs;
+    if (go) gbase = go->dx, gst = go->dxs;
+  } else if (tile < ntx + ntg) {
+    rc0 = (tile - ntx) * kCh, width = GN, ct.c0 = HP + rc0, base = pr.B, st = pr.Bs;
+    if (go) gbase = go->dB, gst = go->dBs;
+  } else {
+    rc0 = (tile - ntx - ntg) * kCh, width = GN, ct.c0 = HP + GN + rc0, base = pr.C, st = pr.Cs;
+    if (go) gbase = go->dC, gst = go->dCs;
+  }
+  ct.nch = min(kCh, width - rc0);
+  ct.src = static_cast<const T *>(base) + (size_t)bb * pr.L * st + rc0;
+  ct.grad = go ? static_cast<T *>(gbase) + (size_t)bb * pr.L * gst + rc0 : nullptr;
+  ct.st = st;
+  ct.gst = gst;
+  return ct;
+}
+__host__ __device__ inline int chan_tiles(const Problem &pr, int kCh) {
+  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
+  return (HP + kCh - 1) / kCh + 2 * ((GN + kCh - 1) / kCh);
+}
+
 // u[b, t, c] = silu(conv_b[c] + sum_k w[c,k] * xr[t-3+k, c]), taps masked at row
 // start and at seq_idx changes.  A block owns a tile of kFwdTok tokens x
 // kFwdCh channels: all of its raw inputs (plus the 3-token halo) are brought
@@ -128,15 +136,14 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict
   constexpr int kCpr = kFwdCh / kChunk;          // copies per row
   __shared__ __align__(16) T tile[kRows][kFwdCh];
   __shared__ int seqs[kRows];
-  const int c0 = blockIdx.x * kFwdCh, t0 = blockIdx.y * kFwdTok, bb = blockIdx.z;
-  const int nch = min(kFwdCh, pr.Cd - c0);
+  const int t0 = blockIdx.y * kFwdTok, bb = blockIdx.z;
+  const ChanTile<T> ct = chan_tile<T>(pr, nullptr, bb, blockIdx.x, kFwdCh);
+  const int c0 = ct.c0, nch = ct.nch;
   for (int q = threadIdx.x; q < kRows * kCpr; q += 256) {
     const int r = q / kCpr, cc = (q % kCpr) * kChunk, t = t0 - 3 + r;
     if (cc >= nch) continue;
-    long long st;
-    const T *src = raw_channel<T>(pr, bb, c0 + cc, st);
     const bool ok = t >= 0 && t < pr.L;
-    const void *g = ok ? static_cast<const void *>(src + (size_t)t * st) : static_cast<const void *>(src);
+    const T *g = ct.src + (ok ? (size_t)t * ct.st : 0) + cc;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(
                      &tile[r][cc]))),
                  "l"(g), "r"(ok ? 16 : 0)
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict
 }
 
 template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s) {
-  dim3 grid((pr.Cd + kFwdCh - 1) / kFwdCh, (pr.L + kFwdTok - 1) / kFwdTok, pr.b);
+  dim3 grid(chan_tiles(pr, kFwdCh), (pr.L + kFwdTok - 1) / kFwdTok, pr.b);
   conv_fwd_kernel<T><<<grid, 256, 0, s>>>(pr, u);
 }
 
@@ -236,64 +243,22 @@ template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *
   dt_prep_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 32, 0, s>>>(pr, dtv, acs);
 }
 
-// Conv + SiLU backward over a tile of kConvBwdTok tokens x kBwdCh channels:
+// Conv + SiLU backward over a tile of kConvBwdTok tokens x kBwdCh channels (one
+// region of xBC):
 //   dv = du * silu'(v);  dxr[s] = sum_k w[k] dv[s+3-k] (same sequence);
 //   per-tile partials of dconv_w[c,k] = sum dv[t] xr[t-3+k] and dconv_b[c] = sum dv.
 // The raw inputs of tokens t0-3 .. t0+kConvBwdTok+2 and du of t0 .. t0+kConvBwdTok+2
 // are brought into shared memory with 16-byte cp.async copies at once (zero
-// outside the row); dv overwrites du in place (v recomputed from the raw
-// inputs), then dxr is formed from dv.  Each thread owns 2 channels and a
-// quarter of the rows; the parameter partials are summed over the quarters in
-// fixed order.
+// outside the row, so tokens past the end give dv = 0).  Each thread owns 2
+// channels; in phase 1 it walks a run of consecutive rows with the last three
+// raw inputs in registers and overwrites du with dv in place (v recomputed from
+// the raw inputs), in phase 2 a run of output rows with the last three dv in
+// registers.  The parameter partials are summed over the row groups in fixed
+// order.  HasSeq: taps masked at sequence changes (without seq_idx every tap
+// counts; the halo before token 0 is zero).
 constexpr int kBwdCh = 64;
 
-// phase 1 of the conv backward for one thread's 2 channels: dv for rows r of
-// the tile (token t0 + r; its inputs are raw rows r .. r + 3), in place over du,
-// and the parameter partials of the tile's own rows.  HasSeq: taps masked at
-// sequence changes (without seq_idx every tap counts; the halo before token 0
-// is zero).
-template <bool HasSeq, typename T, int XR, int DR>
-__device__ __forceinline__ void conv_bwd_dv(const Problem &pr, const T (&xr)[XR][kBwdCh], float (&dv)[DR][kBwdCh],
-                                            const int *seqs, int t0, int cp, int tq, int groups,
-                                            const float (&w)[2][4], const float (&bias)[2], float (&dw)[2][4],
-                                            float (&db)[2]) {
-  for (int r = tq; r < DR; r += groups) {
-    if (t0 + r >= pr.L) break;
-    bool m2 = true, m1 = true, m0 = true;
-    if (HasSeq) {
-      const int sq = seqs[r + 3];
-      m2 = seqs[r + 2] == sq;
-      m1 = seqs[r + 1] == sq;
-      m0 = seqs[r] == sq;
-    }
-    float x0[2], x1[2], x2[2], x3[2];
-    load2(&xr[r][2 * cp], x0);
-    load2(&xr[r + 1][2 * cp], x1);
-    load2(&xr[r + 2][2 * cp], x2);
-    load2(&xr[r + 3][2 * cp], x3);
-    const float2 g2 = *reinterpret_cast<const float2 *>(&dv[r][2 * cp]);
-    const float gv[2] = {g2.x, g2.y};
-    float out[2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float w2 = m2 ? w[q][2] : 0.f, w1 = m1 ? w[q][1] : 0.f, w0 = m0 ? w[q][0] : 0.f;
-      const float v = fmaf(w0, x0[q], fmaf(w1, x1[q], fmaf(w2, x2[q], fmaf(w[q][3], x3[q], bias[q]))));
-      const float sg = sigmoid_fast(v);
-      const float d = gv[q] * sg * (1.f + v * (1.f - sg));
-      out[q] = d;
-      if (r < DR - 3) {  // the tile's own tokens
-        db[q] += d;
-        dw[q][3] = fmaf(d, x3[q], dw[q][3]);
-        dw[q][2] = fmaf(m2 ? d : 0.f, x2[q], dw[q][2]);
-        dw[q][1] = fmaf(m1 ? d : 0.f, x1[q], dw[q][1]);
-        dw[q][0] = fmaf(m0 ? d : 0.f, x0[q], dw[q][0]);
-      }
-    }
-    *reinterpret_cast<float2 *>(&dv[r][2 * cp]) = make_float2(out[0], out[1]);  // own elements only
-  }
-}
-
-template <typename T>
+template <typename T, bool HasSeq>
 __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
                                                        float *__restrict__ convp, int ntb) {
   constexpr int kTok = kConvBwdTok;
@@ -304,40 +269,40 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
   __shared__ __align__(16) float dv[kDRows][kBwdCh];
   __shared__ int seqs[kXRows];
   __shared__ float red[4][kBwdCh][5];
-  const int c0 = blockIdx.x * kBwdCh, blk = blockIdx.y, bb = blockIdx.z, t0 = blk * kTok;
-  const int nch = min(kBwdCh, pr.Cd - c0);
+  const int blk = blockIdx.y, bb = blockIdx.z, t0 = blk * kTok;
+  const ChanTile<T> ct = chan_tile<T>(pr, &go, bb, blockIdx.x, kBwdCh);
+  const int nch = ct.nch;
   for (int q = threadIdx.x; q < kXRows * (kBwdCh / kChunk); q += 256) {
     const int r = q / (kBwdCh / kChunk), cc = (q % (kBwdCh / kChunk)) * kChunk, t = t0 - 3 + r;
     if (cc >= nch) continue;
-    long long st;
-    const T *src = raw_channel<T>(pr, bb, c0 + cc, st);
     const bool ok = t >= 0 && t < pr.L;
-    const void *g = ok ? static_cast<const void *>(src + (size_t)t * st) : static_cast<const void *>(src);
+    const T *g = ct.src + (ok ? (size_t)t * ct.st : 0) + cc;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
                      static_cast<uint32_t>(__cvta_generic_to_shared(&xr[r][cc]))),
                  "l"(g), "r"(ok ? 16 : 0)
                  : "memory");
   }
-  const float *dub = du + (size_t)bb * pr.L * pr.Cd + c0;
+  const float *dub = du + (size_t)bb * pr.L * pr.Cd + ct.c0;
   for (int q = threadIdx.x; q < kDRows * (kBwdCh / 4); q += 256) {
     const int r = q / (kBwdCh / 4), cc = (q % (kBwdCh / 4)) * 4, t = t0 + r;
     if (cc >= nch) continue;
     const bool ok = t < pr.L;
-    const void *g = ok ? static_cast<const void *>(dub + (size_t)t * pr.Cd + cc) : static_cast<const void *>(dub);
+    const float *g = dub + (ok ? (size_t)t * pr.Cd : 0) + cc;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
                      static_cast<uint32_t>(__cvta_generic_to_shared(&dv[r][cc]))),
                  "l"(g), "r"(ok ? 16 : 0)
                  : "memory");
   }
-  for (int r = threadIdx.x; r < kXRows; r += 256) {
-    const int t = t0 - 3 + r;
-    seqs[r] = (t >= 0 && t < pr.L) ? seq_of(pr, bb, t) : -1;
-  }
+  if (HasSeq)
+    for (int r = threadIdx.x; r < kXRows; r += 256) {
+      const int t = t0 - 3 + r;
+      seqs[r] = (t >= 0 && t < pr.L) ? seq_of(pr, bb, t) : -1;
+    }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  const int cp = threadIdx.x % (kBwdCh / 2), tq = threadIdx.x / (kBwdCh / 2);  // 8 row groups
-  const int c = c0 + 2 * cp;
-  const bool live = 2 * cp < nch;
+  const int cp = threadIdx.x % (kBwdCh / 2), tq = threadIdx.x / (kBwdCh / 2);
+  const int c = ct.c0 + 2 * cp;
+  const bool live = 2 * cp < nch;  // nch is a multiple of 8
   float w[2][4] = {}, bias[2] = {}, dw[2][4] = {}, db[2] = {};
   if (live) {
 #pragma unroll
@@ -346,54 +311,96 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
       w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
       bias[q] = pr.conv_b[c + q];
     }
-  }
-  constexpr int kGroups = 256 / (kBwdCh / 2);
-  if (live) {
-    if (pr.seq_idx)
-      conv_bwd_dv<true, T>(pr, xr, dv, seqs, t0, cp, tq, kGroups, w, bias, dw, db);
-    else
-      conv_bwd_dv<false, T>(pr, xr, dv, seqs, t0, cp, tq, kGroups, w, bias, dw, db);
+    // phase 1: dv rows r0 .. r0 + n1 - 1 (the first 3 groups take 9 rows, the others 8)
+    const int r0 = tq * 8 + min(tq, 3), n1 = tq < 3 ? 9 : 8;
+    float x0[2], x1[2], x2[2];
+    load2(&xr[r0][2 * cp], x0);
+    load2(&xr[r0 + 1][2 * cp], x1);
+    load2(&xr[r0 + 2][2 * cp], x2);
+    int s0 = 0, s1 = 0, s2 = 0;
+    if (HasSeq) {
+      s0 = seqs[r0];
+      s1 = seqs[r0 + 1];
+      s2 = seqs[r0 + 2];
+    }
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+      if (k < n1) {
+        const int r = r0 + k;  // token t0 + r, inputs at raw rows r .. r + 3
+        float x3[2];
+        load2(&xr[r + 3][2 * cp], x3);
+        const int sq = HasSeq ? seqs[r + 3] : 0;
+        const bool m2 = !HasSeq || s2 == sq, m1 = !HasSeq || s1 == sq, m0 = !HasSeq || s0 == sq;
+        const float2 g2 = *reinterpret_cast<const float2 *>(&dv[r][2 * cp]);
+        const float gv[2] = {g2.x, g2.y};
+        float out[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float v = fmaf(w[q][3], x3[q], bias[q]);
+          v = fmaf(m2 ? w[q][2] : 0.f, x2[q], v);
+          v = fmaf(m1 ? w[q][1] : 0.f, x1[q], v);
+          v = fmaf(m0 ? w[q][0] : 0.f, x0[q], v);
+          const float sg = sigmoid_fast(v);
+          const float d = gv[q] * sg * (1.f + v * (1.f - sg));
+          out[q] = d;
+          if (r < kTok) {  // the tile's own tokens
+            db[q] += d;
+            dw[q][3] = fmaf(d, x3[q], dw[q][3]);
+            dw[q][2] = fmaf(m2 ? d : 0.f, x2[q], dw[q][2]);
+            dw[q][1] = fmaf(m1 ? d : 0.f, x1[q], dw[q][1]);
+            dw[q][0] = fmaf(m0 ? d : 0.f, x0[q], dw[q][0]);
+          }
+          x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
+        }
+        s0 = s1; s1 = s2; s2 = sq;
+        *reinterpret_cast<float2 *>(&dv[r][2 * cp]) = make_float2(out[0], out[1]);  // own elements only
+      }
+    }
   }
   __syncthreads();
-  // phase 2: dxr for rows s in [0, kTok) (token t0 + s) from dv rows s .. s + 3
+  // phase 2: dxr for rows s in [8 tq, 8 tq + 8) (token t0 + s) from dv rows s .. s + 3
   if (live) {
-    void *dbase;
-    long long dstride;
-    grad_channel(pr, go, bb, c, dbase, dstride, (int)sizeof(T));
-    T *dst = static_cast<T *>(dbase);
-    const bool has_seq = pr.seq_idx != nullptr;
-    for (int sr = tq; sr < kTok; sr += kGroups) {
-      const int t = t0 + sr;
-      if (t >= pr.L) break;
-      const int q0 = seqs[sr + 3];  // token t
-      const bool m1 = !has_seq || seqs[sr + 4] == q0, m2 = !has_seq || seqs[sr + 5] == q0,
-                 m3 = !has_seq || seqs[sr + 6] == q0;
-      const float2 d0 = *reinterpret_cast<const float2 *>(&dv[sr][2 * cp]);
-      const float2 d1 = *reinterpret_cast<const float2 *>(&dv[sr + 1][2 * cp]);
-      const float2 d2 = *reinterpret_cast<const float2 *>(&dv[sr + 2][2 * cp]);
-      const float2 d3 = *reinterpret_cast<const float2 *>(&dv[sr + 3][2 * cp]);
-      const float a0[2] = {d0.x, d0.y}, a1[2] = {d1.x, d1.y}, a2[2] = {d2.x, d2.y}, a3[2] = {d3.x, d3.y};
+    const int sr0 = tq * 8;
+    float d0[2], d1[2], d2[2];
+    {
+      const float2 a = *reinterpret_cast<const float2 *>(&dv[sr0][2 * cp]);
+      const float2 b = *reinterpret_cast<const float2 *>(&dv[sr0 + 1][2 * cp]);
+      const float2 e = *reinterpret_cast<const float2 *>(&dv[sr0 + 2][2 * cp]);
+      d0[0] = a.x; d0[1] = a.y; d1[0] = b.x; d1[1] = b.y; d2[0] = e.x; d2[1] = e.y;
+    }
+    T *dst = ct.grad + 2 * cp;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int sr = sr0 + k, t = t0 + sr;
+      const float2 f = *reinterpret_cast<const float2 *>(&dv[sr + 3][2 * cp]);
+      const float d3[2] = {f.x, f.y};
+      bool m1 = true, m2 = true, m3 = true;
+      if (HasSeq) {
+        const int q0 = seqs[sr + 3];  // token t
+        m1 = seqs[sr + 4] == q0;
+        m2 = seqs[sr + 5] == q0;
+        m3 = seqs[sr + 6] == q0;
+      }
       float g[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        float a = w[q][3] * a0[q];
-        a = fmaf(m1 ? w[q][2] : 0.f, a1[q], a);
-        a = fmaf(m2 ? w[q][1] : 0.f, a2[q], a);
-        a = fmaf(m3 ? w[q][0] : 0.f, a3[q], a);
+        float a = w[q][3] * d0[q];
+        a = fmaf(m1 ? w[q][2] : 0.f, d1[q], a);
+        a = fmaf(m2 ? w[q][1] : 0.f, d2[q], a);
+        a = fmaf(m3 ? w[q][0] : 0.f, d3[q], a);
         g[q] = a;
+        d0[q] = d1[q]; d1[q] = d2[q]; d2[q] = d3[q];
       }
-      store2(dst + (size_t)t * dstride, g);
+      if (t < pr.L) store2(dst + (size_t)t * ct.gst, g);
     }
   }
-  // parameter partials: fixed-order sum over the row groups
+  // parameter partials: fixed-order sum over the row groups (0..3 and 4..7 folded pairwise first)
+  if (tq < 4) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    // groups 0..3 and 4..7 folded pairwise first (fixed order)
-    const int slot = tq & 3;
-    if (tq < 4) {
+    for (int q = 0; q < 2; ++q) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) red[slot][2 * cp + q][kk] = dw[q][kk];
-      red[slot][2 * cp + q][4] = db[q];
+      for (int kk = 0; kk < 4; ++kk) red[tq][2 * cp + q][kk] = dw[q][kk];
+      red[tq][2 * cp + q][4] = db[q];
     }
   }
   __syncthreads();
@@ -409,14 +416,17 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
   for (int e = threadIdx.x; e < nch * 5; e += 256) {
     const int ch = e / 5, k5 = e % 5;
     const float v = (red[0][ch][k5] + red[1][ch][k5]) + (red[2][ch][k5] + red[3][ch][k5]);
-    convp[(((size_t)bb * ntb + blk) * pr.Cd + c0 + ch) * 5 + k5] = v;
+    convp[(((size_t)bb * ntb + blk) * pr.Cd + ct.c0 + ch) * 5 + k5] = v;
   }
 }
 
 template <typename T>
 void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s) {
-  dim3 grid((pr.Cd + kBwdCh - 1) / kBwdCh, ntb, pr.b);
-  conv_bwd_kernel<T><<<grid, 256, 0, s>>>(pr, du, go, convp, ntb);
+  dim3 grid(chan_tiles(pr, kBwdCh), ntb, pr.b);
+  if (pr.seq_idx)
+    conv_bwd_kernel<T, true><<<grid, 256, 0, s>>>(pr, du, go, convp, ntb);
+  else
+    conv_bwd_kernel<T, false><<<grid, 256, 0, s>>>(pr, du, go, convp, ntb);
 }
 
 // Parameter gradients: fixed-order sums of per-chunk / per-block partials.
