@@ -129,6 +129,43 @@ __host__ __device__ inline int chan_tiles(const Problem &pr, int kCh) {
 // memory; a warp's stores cover 64 consecutive channels of one token.
 constexpr int kFwdTok = 64, kFwdCh = 128;
 
+// One thread's run of n output rows (2 channels) from the shared tile, the
+// last three raw inputs kept in registers.  HasSeq: taps masked at sequence
+// changes.  With n a compile-time constant the loop unrolls completely.
+template <typename T, bool HasSeq>
+__device__ __forceinline__ void conv_fwd_rows(const T (*tile)[kFwdCh], const int *seqs, const float (&w)[2][4],
+                                              const float (&bias)[2], int r0, int cp, int n, T *dst, int Cd) {
+  float x0[2], x1[2], x2[2];
+  load2(&tile[r0][2 * cp], x0);
+  load2(&tile[r0 + 1][2 * cp], x1);
+  load2(&tile[r0 + 2][2 * cp], x2);
+  int s0 = 0, s1 = 0, s2 = 0;
+  if (HasSeq) {
+    s0 = seqs[r0];
+    s1 = seqs[r0 + 1];
+    s2 = seqs[r0 + 2];
+  }
+#pragma unroll
+  for (int k = 0; k < kFwdTok / 4; ++k) {
+    if (k >= n) break;
+    float x3[2], o[2];
+    load2(&tile[r0 + 3 + k][2 * cp], x3);
+    const int sq = HasSeq ? seqs[r0 + 3 + k] : 0;
+    const bool m2 = !HasSeq || s2 == sq, m1 = !HasSeq || s1 == sq, m0 = !HasSeq || s0 == sq;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float v = fmaf(w[q][3], x3[q], bias[q]);
+      v = fmaf(m2 ? w[q][2] : 0.f, x2[q], v);
+      v = fmaf(m1 ? w[q][1] : 0.f, x1[q], v);
+      v = fmaf(m0 ? w[q][0] : 0.f, x0[q], v);
+      o[q] = v * sigmoid_fast(v);
+      x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
+    }
+    s0 = s1; s1 = s2; s2 = sq;
+    store2(dst + (size_t)k * Cd, o);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict__ u) {
   constexpr int kRows = kFwdTok + 3;
@@ -167,45 +204,15 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict
   }
   constexpr int kPer = kFwdTok / 4;
   const int r0 = tq * kPer;  // first output row (token t0 + r0), inputs at rows r0 .. r0 + 3
-  float x0[2], x1[2], x2[2];
-  auto ld2 = [&](int r, float (&v)[2]) { load2(&tile[r][2 * cp], v); };
-  ld2(r0, x0);
-  ld2(r0 + 1, x1);
-  ld2(r0 + 2, x2);
-  int s0 = seqs[r0], s1 = seqs[r0 + 1], s2 = seqs[r0 + 2];
   T *dst = u + ((size_t)bb * pr.L + t0 + r0) * pr.Cd + c;
   const int tend = min(kPer, pr.L - (t0 + r0));
-  if (!pr.seq_idx) {  // one sequence per row: every tap counts (the halo before token 0 is zero)
-    for (int k = 0; k < tend; ++k) {
-      float x3[2], o[2];
-      ld2(r0 + 3 + k, x3);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float v = fmaf(w[q][0], x0[q], fmaf(w[q][1], x1[q], fmaf(w[q][2], x2[q], fmaf(w[q][3], x3[q], bias[q]))));
-        o[q] = v * sigmoid_fast(v);
-        x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
-      }
-      store2(dst + (size_t)k * pr.Cd, o);
-    }
-    return;
-  }
-  for (int k = 0; k < tend; ++k) {
-    float x3[2];
-    ld2(r0 + 3 + k, x3);
-    const int sq = seqs[r0 + 3 + k];
-    const bool m2 = s2 == sq, m1 = s1 == sq, m0 = s0 == sq;
-    float o[2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      float v = bias[q] + w[q][3] * x3[q];
-      v += m2 ? w[q][2] * x2[q] : 0.f;
-      v += m1 ? w[q][1] * x1[q] : 0.f;
-      v += m0 ? w[q][0] * x0[q] : 0.f;
-      o[q] = v * sigmoid_fast(v);
-      x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
-    }
-    store2(dst + (size_t)k * pr.Cd, o);
-    s0 = s1; s1 = s2; s2 = sq;
+  if (tend <= 0) return;
+  if (pr.seq_idx) {
+    conv_fwd_rows<T, true>(tile, seqs, w, bias, r0, cp, tend, dst, pr.Cd);
+  } else if (tend == kPer) {  // full run: constant trip count, unrolled
+    conv_fwd_rows<T, false>(tile, seqs, w, bias, r0, cp, kPer, dst, pr.Cd);
+  } else {
+    conv_fwd_rows<T, false>(tile, seqs, w, bias, r0, cp, tend, dst, pr.Cd);
   }
 }
 
@@ -430,61 +437,75 @@ void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, floa
 }
 
 // Parameter gradients: fixed-order sums of per-chunk / per-block partials.
-// One warp per channel (and per head for the dt / A / D grads): lane l sums the
-// partials l, l+32, ... in order, then a fixed xor-shuffle tree combines lanes.
+// Fixed xor-shuffle tree over a warp's lanes.
 __device__ __forceinline__ float warp_tree_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
+// Parameter gradients from the per-block partials, each sum in a fixed order.
+// Conv: a block takes 32 consecutive elements of a partial row (Cd x 5 floats:
+// dconv_w[c, 0..3], dconv_b[c]) and 8 interleaved slices of the b * ntb rows, so
+// every warp load is one contiguous 128-byte line; the slices are added in
+// order at the end.  Per head (one warp each, after the conv blocks): ddt_bias,
+// dA_log and dD from the per-chunk scalars.
+constexpr int kParamSlices = 8;
 __global__ void __launch_bounds__(256) param_reduce_kernel(Problem pr, const float *__restrict__ chs,
                                                            const float *__restrict__ convp, int ntb,
                                                            float *ddt_bias, float *dA_log, float *dD,
-                                                           float *dconv_w, float *dconv_b) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+                                                           float *dconv_w, float *dconv_b, int conv_blocks) {
+  __shared__ float part[kParamSlices][32];
+  const int lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
+  if ((int)blockIdx.x < conv_blocks) {
+    const int row = pr.Cd * 5, nparts = pr.b * ntb;
+    const int e = blockIdx.x * 32 + lane;
+    float acc = 0.f;
+    if (e < row) {
+      const float *pp = convp + e;
+#pragma unroll 8
+      for (int k = slice; k < nparts; k += kParamSlices) acc += pp[(size_t)k * row];
+    }
+    part[slice][lane] = acc;
+    __syncthreads();
+    if (slice == 0 && e < row) {
+      float t = 0.f;
+#pragma unroll
+      for (int q = 0; q < kParamSlices; ++q) t += part[q][lane];
+      const int c = e / 5, q = e % 5;
+      if (q < 4)
+        dconv_w[c * 4 + q] = t;
+      else
+        dconv_b[c] = t;
+    }
+    return;
+  }
+  const int h = (blockIdx.x - conv_blocks) * (blockDim.x >> 5) + slice;
+  if (h >= pr.H) return;
   const size_t nch = (size_t)pr.b * pr.nc * pr.H;
-  if (warp < pr.Cd) {
-    const int c = warp;
-    const int nparts = pr.b * ntb;
-    float acc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int k = lane; k < nparts; k += 32) {
-      const float *pp = convp + ((size_t)k * pr.Cd + c) * 5;  // partial k = bb * ntb + blk
-#pragma unroll
-      for (int q = 0; q < 5; ++q) acc[q] += pp[q];
-    }
-#pragma unroll
-    for (int q = 0; q < 5; ++q) acc[q] = warp_tree_sum(acc[q]);
-    if (lane == 0) {
-      for (int q = 0; q < 4; ++q) dconv_w[c * 4 + q] = acc[q];
-      dconv_b[c] = acc[4];
-    }
-  } else if (warp < pr.Cd + pr.H) {
-    const int h = warp - pr.Cd;
-    const int nparts = pr.b * pr.nc;
-    float sb = 0.f, sa = 0.f, sd = 0.f;
-    for (int k = lane; k < nparts; k += 32) {  // k = bb * nc + c
-      const size_t o = (size_t)k * pr.H + h;
-      sb += chs[o];
-      sa += chs[nch + o];
-      sd += chs[2 * nch + o];
-    }
-    sb = warp_tree_sum(sb);
-    sa = warp_tree_sum(sa);
-    sd = warp_tree_sum(sd);
-    if (lane == 0) {
-      ddt_bias[h] = sb;
-      dA_log[h] = sa * (-expf(pr.A_log[h]));  // dA/dA_log = A
-      dD[h] = sd;
-    }
+  const int nparts = pr.b * pr.nc;
+  float sb = 0.f, sa = 0.f, sd = 0.f;
+  for (int k = lane; k < nparts; k += 32) {  // k = bb * nc + c
+    const size_t o = (size_t)k * pr.H + h;
+    sb += chs[o];
+    sa += chs[nch + o];
+    sd += chs[2 * nch + o];
+  }
+  sb = warp_tree_sum(sb);
+  sa = warp_tree_sum(sa);
+  sd = warp_tree_sum(sd);
+  if (lane == 0) {
+    ddt_bias[h] = sb;
+    dA_log[h] = sa * (-expf(pr.A_log[h]));  // dA/dA_log = A
+    dD[h] = sd;
   }
 }
 
 void launch_param_reduce(const Problem &pr, const float *chs, const float *convp, int ntb, float *ddt_bias,
                          float *dA_log, float *dD, float *dconv_w, float *dconv_b, cudaStream_t s) {
-  const int warps = pr.Cd + pr.H;
-  param_reduce_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(pr, chs, convp, ntb, ddt_bias, dA_log, dD, dconv_w,
-                                                               dconv_b);
+  const int conv_blocks = (pr.Cd * 5 + 31) / 32, head_blocks = (pr.H + 7) / 8;
+  param_reduce_kernel<<<conv_blocks + head_blocks, 256, 0, s>>>(pr, chs, convp, ntb, ddt_bias, dA_log, dD, dconv_w,
+                                                                dconv_b, conv_blocks);
 }
 
 __global__ void cu_seqlens_kernel(const int *__restrict__ cu, int nseq, int *__restrict__ seq_idx, int total) {

@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
                                                      const float *__restrict__ sdp, int sdp_groups, GradOut go,
                                                      float *__restrict__ chs) {
   __shared__ ChunkVecs v;
-  __shared__ float red[8], dacs[256], dda[256];
+  __shared__ float red[8], red3[24], dacs[256], dda[256];
   const ChunkIds id = chunk_ids(pr);
   load_chunk_vecs(pr, id, dtv, acs, v);
   const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
@@ -496,9 +496,29 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
       for (int p = 0; p < P; ++p) dD_part += to_f(dyr[p]) * to_f(xr[p]);
     }
   }
-  const float s_dA = block_sum256(dA_part, red);
-  const float s_dz = block_sum256(dz, red);
-  const float s_dD = block_sum256(dD_part, red);
+  // the three block sums share one pair of barriers (same fixed order as block_sum256)
+  float s_dA = dA_part, s_dz = dz, s_dD = dD_part;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    s_dA += __shfl_xor_sync(0xffffffffu, s_dA, o);
+    s_dz += __shfl_xor_sync(0xffffffffu, s_dz, o);
+    s_dD += __shfl_xor_sync(0xffffffffu, s_dD, o);
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    const int w = threadIdx.x >> 5;
+    red3[w] = s_dA;
+    red3[8 + w] = s_dz;
+    red3[16 + w] = s_dD;
+  }
+  __syncthreads();
+  s_dA = s_dz = s_dD = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    s_dA += red3[w];
+    s_dz += red3[8 + w];
+    s_dD += red3[16 + w];
+  }
   if (threadIdx.x == 0) {
     const size_t nch = (size_t)pr.b * pr.nc * pr.H;
     const size_t o = ((size_t)id.bb * pr.nc + id.c) * pr.H + id.h;
