@@ -158,7 +158,7 @@ __device__ __forceinline__ void conv_fwd_rows(const T (*tile)[kFwdCh], const int
       v = fmaf(m2 ? w[q][2] : 0.f, x2[q], v);
       v = fmaf(m1 ? w[q][1] : 0.f, x1[q], v);
       v = fmaf(m0 ? w[q][0] : 0.f, x0[q], v);
-      o[q] = v * sigmoid_fast(v);
+      o[q] = v * act_sigmoid<T>(v);
       x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
     }
     s0 = s1; s1 = s2; s2 = sq;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
           v = fmaf(m2 ? w[q][2] : 0.f, x2[q], v);
           v = fmaf(m1 ? w[q][1] : 0.f, x1[q], v);
           v = fmaf(m0 ? w[q][0] : 0.f, x0[q], v);
-          const float sg = sigmoid_fast(v);
+          const float sg = act_sigmoid<T>(v);
           const float d = gv[q] * sg * (1.f + v * (1.f - sg));
           out[q] = d;
           if (r < kTok) {  // the tile's own tokens
