@@ -405,6 +405,20 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   __shared__ ChunkVecs v;
   __shared__ float red[8], red3[24], dacs[256], dda[256];
   const ChunkIds id = chunk_ids(pr);
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
+  const int i = threadIdx.x;
+  const bool valid = i < pr.Q;
+  // this token's inputs, loaded before the chunk vectors so that the loads overlap
+  float tk0 = 0.f, tk2 = 0.f, tk3 = 0.f, tk4 = 0.f, tk5 = 0.f, dt_raw = 0.f;
+  if (valid) {
+    tk0 = tok[0 * BHL + tb + i];
+    tk2 = tok[2 * BHL + tb + i];
+    tk3 = tok[3 * BHL + tb + i];
+    tk4 = tok[4 * BHL + tb + i];
+    if (vcol_parts > 1 || sdp) tk5 = tok[5 * BHL + tb + i];
+    dt_raw = to_f(static_cast<const T *>(pr.dt)[((size_t)id.bb * pr.L + id.t0 + i) * pr.dts + id.h]);
+  }
   load_chunk_vecs(pr, id, dtv, acs, v);
   const int Cd = pr.Cd, P = pr.P, N = pr.N, Q = pr.Q, HP = pr.H * pr.P;
   const int PN = P * N;
@@ -436,19 +450,15 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
     dec = ac * block_sum256(part, red);
   }
 
-  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
-  const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
-  const int i = threadIdx.x;
-  const bool valid = i < Q;
   float q = 0.f, wq = 0.f, vcol = 0.f;
   if (valid) {
-    q = tok[4 * BHL + tb + i];
+    q = tk4;
     wq = v.wdt[i] * q;
   }
   const float ssum = block_sum256(wq, red);
   if (valid) {
-    vcol = tok[2 * BHL + tb + i] + (vcol_parts > 1 ? tok[5 * BHL + tb + i] : 0.f);
-    float d = tok[0 * BHL + tb + i] - v.dt[i] * vcol + tok[3 * BHL + tb + i] - wq;
+    vcol = tk2 + (vcol_parts > 1 ? tk5 : 0.f);
+    float d = tk0 - v.dt[i] * vcol + tk3 - wq;
     if (i == Q - 1) d += ssum + dec;
     dacs[i] = d;
   }
@@ -474,15 +484,14 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
     const int t = id.t0 + i;
     const float ddt = vcol + v.w[i] * q + A * dda[i];
     dA_part = v.dt[i] * dda[i];
-    const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)id.bb * pr.L + t) * pr.dts + id.h;
-    const float z = to_f(*dtr) + pr.dt_bias[id.h];
+    const float z = dt_raw + pr.dt_bias[id.h];
     dz = ddt * sigmoid_f(z);
     T *dst = static_cast<T *>(go.ddt) + ((size_t)id.bb * pr.L + t) * go.ddts + id.h;
     *dst = from_f<T>(dz);
     const T *xr = u + ((size_t)id.bb * pr.L + t) * Cd + id.h * P;
     const T *dyr = dy + ((size_t)id.bb * pr.L + t) * HP + id.h * P;
     if (sdp) {  // tensor-core path: dy_t . x_t was written to tok[5] by the column kernel
-      dD_part = tok[5 * BHL + tb + i];
+      dD_part = tk5;
     } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
       for (int p = 0; p < P; p += 8) {
         const uint4 a = *reinterpret_cast<const uint4 *>(xr + p), b = *reinterpret_cast<const uint4 *>(dyr + p);
