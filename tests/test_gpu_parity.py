@@ -46,6 +46,8 @@ SHAPES = [
     # boundaries at token 256 (a chunk start), 512 (a segment start), 1-3 token
     # sequences, and sequences shorter than a chunk
     (SsdShape(1, 2048, 4, 64, 128, 1, 256, 4), [256, 256, 1, 2, 3, 90, 160, 700, 580]),
+    # the tensor-core path with 128-token chunks (one row tile per chunk), packed
+    (SsdShape(2, 1024, 4, 64, 128, 1, 128, 2), [128, 5, 300, 77, 514]),
 ]
 
 
