@@ -175,7 +175,10 @@ void launch_chunk_z(const Problem &pr, const T *u, const T *dy, const float *acs
 // With dM[i,j] = dy_i . x_j (over P) and L = exp(Acs_i - Acs_j) (causal, same seq):
 //   W[i,j] = dM L dt_j       -- the adjoint of CB[i,j], stored for the dB / dC products
 //   V[i,j] = dM CB L         -- reduced to per-token sums for the dt / Acs adjoints:
-//   vrow_i = sum_j V dt_j,  vcol_dt_j = sum_i V dt_j,  vcol_j = sum_i V.
+//   vrow_i = sum_{j<i} V dt_j,  vcol_j = sum_{i>j} V,  vdiag_j = V[j,j].
+// The diagonal is kept apart: in the Acs adjoint vrow_i - dt_i vcol_i its two
+// copies cancel exactly, and summing them separately would leave only rounding
+// noise there (large for heads that forget within a token).
 template <typename T>
 __global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
                                                 const float *__restrict__ dtv, const float *__restrict__ acs,
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict_
                                                 float *__restrict__ tok) {
   __shared__ __align__(16) float smem[kGemmSmemFloats];
   __shared__ ChunkVecs v;
-  __shared__ float rowacc[kTile], colacc_dt[256], colacc[256], scratch[8 * kTile];
+  __shared__ float rowacc[kTile], colacc[256], scratch[8 * kTile];
   const ChunkIds id = chunk_ids(pr);
   load_chunk_vecs(pr, id, dtv, acs, v);
   const int Cd = pr.Cd, P = pr.P, Q = pr.Q, HP = pr.H * pr.P;
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict_
   float *wm = wbuf + (((size_t)id.bb * pr.nc + id.c) * pr.H + id.h) * Q * Q;
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
   const size_t tb = ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
-  for (int i = threadIdx.x; i < 256; i += 256) { colacc_dt[i] = 0.f; colacc[i] = 0.f; }
+  for (int i = threadIdx.x; i < 256; i += 256) colacc[i] = 0.f;
   __syncthreads();
   auto fa = [&](int i, int p) { return to_f(dyb[(size_t)i * HP + p]); };
   auto fb = [&](int p, int j) { return to_f(ub[(size_t)j * Cd + offX + p]); };
@@ -217,21 +220,19 @@ __global__ void __launch_bounds__(256) w_kernel(Problem pr, const T *__restrict_
             cbij = cbm[(size_t)i * Q + j];
           }
           const float dtj = (j < Q) ? v.dt[j] : 0.f;
-          vv[a][b2] = dML * cbij;       // V = dM o CB o L
-          wv[a][b2] = vv[a][b2] * dtj;  // V o dt: the dt / Acs adjoint pieces
+          const float vij = dML * cbij;  // V = dM o CB o L
           if (i < Q && j < Q) wm[(size_t)i * Q + j] = dML * dtj;  // adjoint of CB
+          if (i == j && i < Q) tok[1 * BHL + tb + i] = vij;   // the diagonal, kept apart
+          vv[a][b2] = i == j ? 0.f : vij;
+          wv[a][b2] = vv[a][b2] * dtj;  // V o dt: the dt / Acs adjoint pieces
         }
       tile_rowsum_add(wv, rowacc);
-      tile_colsum_add(wv, colacc_dt + tj * kTile, scratch);
       tile_colsum_add(vv, colacc + tj * kTile, scratch);
     }
     if (threadIdx.x < kTile && ti * kTile + threadIdx.x < Q) tok[0 * BHL + tb + ti * kTile + threadIdx.x] = rowacc[threadIdx.x];
     __syncthreads();
   }
-  for (int j = threadIdx.x; j < Q; j += 256) {
-    tok[1 * BHL + tb + j] = colacc_dt[j];
-    tok[2 * BHL + tb + j] = colacc[j];
-  }
+  for (int j = threadIdx.x; j < Q; j += 256) tok[2 * BHL + tb + j] = colacc[j];
 }
 
 template <typename T>
@@ -388,11 +389,12 @@ void launch_chunk_dcdb(const Problem &pr, const T *u, const T *dy, const float *
 
 // dt / A / D gradients of one (chunk, head).  On the tensor-core path (sdp
 // given) the chunk's decay term and the per-token dy . x come precomputed.
-// With vcol = sum over the
-// vcol_parts per-row-tile partial column sums (tok[2], tok[5]) and dAcs_i the
-// total adjoint of the chunk-local cumsum:
+// With vrow, vcol the row and column sums of V without its diagonal (tok[0];
+// tok[2] plus, for vcol_parts > 1, tok[5]), vdiag the diagonal (tok[1]) and
+// dAcs_i the total adjoint of the chunk-local cumsum:
 //   dAcs_i = vrow_i - dt_i vcol_i + r_i - wdt_i q_i  (+ sum_j wdt_j q_j + a_c <dS_end, S_in> at the last token)
-//   d(dA_t) = sum_{i>=t} dAcs_i;   d dt_t = vcol_t + w_t q_t + A d(dA_t);   dA += dt_t d(dA_t)
+//   d(dA_t) = sum_{i>=t} dAcs_i;   d dt_t = vcol_t + vdiag_t + w_t q_t + A d(dA_t);   dA += dt_t d(dA_t)
+// (the diagonal's two contributions to dAcs cancel exactly, so it enters d dt only).
 //   d dt_raw = d dt * sigmoid(dt_raw + dt_bias)
 template <typename T>
 __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__restrict__ u, const T *__restrict__ dy,
@@ -410,9 +412,10 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   const int i = threadIdx.x;
   const bool valid = i < pr.Q;
   // this token's inputs, loaded before the chunk vectors so that the loads overlap
-  float tk0 = 0.f, tk2 = 0.f, tk3 = 0.f, tk4 = 0.f, tk5 = 0.f, dt_raw = 0.f;
+  float tk0 = 0.f, tk1 = 0.f, tk2 = 0.f, tk3 = 0.f, tk4 = 0.f, tk5 = 0.f, dt_raw = 0.f;
   if (valid) {
     tk0 = tok[0 * BHL + tb + i];
+    tk1 = tok[1 * BHL + tb + i];
     tk2 = tok[2 * BHL + tb + i];
     tk3 = tok[3 * BHL + tb + i];
     tk4 = tok[4 * BHL + tb + i];
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   float dA_part = 0.f, dz = 0.f, dD_part = 0.f;
   if (valid) {
     const int t = id.t0 + i;
-    const float ddt = vcol + v.w[i] * q + A * dda[i];
+    const float ddt = vcol + tk1 + v.w[i] * q + A * dda[i];
     dA_part = v.dt[i] * dda[i];
     const float z = dt_raw + pr.dt_bias[id.h];
     dz = ddt * sigmoid_f(z);

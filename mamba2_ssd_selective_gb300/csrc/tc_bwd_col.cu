@@ -4,7 +4,8 @@
 //   M^T  = CB^T o L^T o dt_j,   W^T = dM^T o L^T o dt_j,  L^T[j, i] = exp(Acs_i - Acs_j)
 //   T_j  = sum_i M^T[j, i] dy_i,   U_j = dS_end,h B_j,     (tensor memory)
 //   du_x[j] = T_j + wdt_j U_j + D_h dy_j,   q_j = x_j . U_j,   dy_j . x_j (for dD),
-//   vcol_j = sum_i V[i, j] = sum_i dM^T CB^T L^T
+//   vcol_j = sum_{i>j} V[i, j] = sum_{i>j} dM^T CB^T L^T,  vdiag_j = V[j, j]
+//            (kept apart: the diagonal cancels in the Acs adjoint, not in dt's)
 // and accumulates over the heads of a block
 //   dB_j += sum_i W^T[j, i] C_i + wdt_j dS_end,h^T x_j,
 // written as one fp32 partial per (token, head block).
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               vcol = fmaf(vs, e0, vcol);
             } else {  // on the diagonal: one 2^x per element
+              float vdiag = 0.f;
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
                 const float4 a4 = pipe::lds_f4(ta + 4 * (i0 + e));
@@ -411,12 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int i = i0 + e + k4;
                   const bool ok = (unsigned)(i - j) <= (unsigned)(end_j - j);
                   const float ee = ok ? ex2_approx(av[k4] - aj) : 0.f;
-                  vcol = fmaf(dm[e + k4] * cbv[e + k4], ee, vcol);
+                  const float vij = dm[e + k4] * cbv[e + k4];
+                  // the column sum leaves out i = j (it cancels exactly against the row
+                  // sum's in the Acs adjoint); that term V_jj goes to its own slot
+                  if (i == j) vdiag = vij;
+                  vcol = fmaf(i == j ? 0.f : vij, ee, vcol);
                   const float t1 = ee * dt_j;
                   mw[0][e + k4] = cbv[e + k4] * t1;
                   mw[1][e + k4] = dm[e + k4] * t1;
                 }
               }
+              if ((unsigned)(j - i0) < 16u) tok[1 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + (size_t)o.c * pr.Q + j] = vdiag;
             }
           }
           put_operands<2>(mw, na, sA, jl, cg, bar.a_full, bar.a_free, status);

@@ -2,7 +2,8 @@
 // rows i of one 128-token tile I of a chunk it forms, per head h,
 //   dM = dy_h x_h^T                         (only the blocks j <= i)
 //   W  = dM o L_h o dt,   L_h[i, j] = exp(Acs_i - Acs_j) [j <= i, same sequence]
-//   vrow_i = sum_j V[i, j] dt_j = sum_j W[i, j] CB[i, j]      (V = dM o CB o L)
+//   vrow_i = sum_{j<i} V[i, j] dt_j = sum_{j<i} W[i, j] CB[i, j]   (V = dM o CB o L;
+//            the diagonal cancels in the Acs adjoint and is left out)
 //   r_i    = em_i dy_i . (C_i S_in,h^T)     (the Y_off piece of the dt adjoint)
 // and accumulates over the heads of a block (in tensor memory)
 //   dC_i  += sum_j W[i, j] B_j + em_i dy_i S_in,h,
@@ -380,6 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   w[e + m] = (nomask || j0 + e + m >= start_i) ? val : 0.f;
                 }
               }
+#pragma unroll
+              for (int e = 0; e < 16; ++e) vrow = fmaf(w[e], cbv[e], vrow);
             } else {  // on the diagonal
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
@@ -391,9 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   w[e + m] = (unsigned)(j - start_i) <= (unsigned)(i - start_i) ? dm[e + m] * ex2_approx(ai + bv[m]) : 0.f;
                 }
               }
-            }
+              // the row sum leaves out j = i: that term cancels exactly against the
+              // column sum's in the Acs adjoint (the column kernel keeps it apart)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) vrow = fmaf(w[e], cbv[e], vrow);
+              for (int e = 0; e < 16; ++e) vrow = fmaf(j0 + e == i ? 0.f : w[e], cbv[e], vrow);
+            }
           }
           const int as = na % kNA;
           if (na >= (uint32_t)kNA) mbar_wait(&bar.a_free[as], parity(na / kNA - 1), status);

@@ -61,6 +61,20 @@ def test_forward_backward_parity(oracle_lib, shape, seq, dtype):
     compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_heads_that_forget_within_a_token(oracle_lib, dtype):
+    """Heads 0-1 with dt near 2 (per-token decay e^-2|A|): the diagonal of V
+    enters the Acs adjoint twice with opposite signs, so it must cancel exactly
+    for dA_log to keep its accuracy; heads 2-3 keep the workload's decays."""
+    shape = SsdShape(1, 1024, 4, 64, 128, 1, 256, 2)
+    inp = make_inputs(shape, 11, dtype, dfinal=True, seq_lengths=[300, 1, 211, 512])
+    inp["dt_bias"][:2] = 2.0
+    got, _ = gpu_forward(shape, dtype, inp)
+    compare_forward(got, oracle_lib.forward(inp, shape), TOL[dtype])
+    g = gpu_backward(shape, dtype, inp)
+    compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
+
+
 @pytest.mark.parametrize("dtype,seq", [("f32", None), ("bf16", None), ("bf16", [1000, 3, 2093, 1000])])
 @pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
 def test_segment_count_sweep(oracle_lib, S, dtype, seq):
