@@ -17,8 +17,6 @@ namespace ssd {
 namespace {
 
 using bf16 = __nv_bfloat16;
-using tc::K_MAJOR;
-using tc::MN_MAJOR;
 
 template <class E>
 constexpr int dyn_smem() {
@@ -73,7 +71,7 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_state_kernel(Problem pr, c
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
+  eng.contract_pipelined(tmem, pr.Q, fa, fbl, fbm);
   eng.finish();
   if (tc::owns_row()) {
   const int n = threadIdx.x;
@@ -125,7 +123,7 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  for (int k0 = 0; k0 < pr.Q; k0 += 64) eng.slice<MN_MAJOR, MN_MAJOR>(tmem, k0, fa, tc::Async{}, fbl, fbm, k0 > 0);
+  eng.contract_pipelined(tmem, pr.Q, fa, fbl, fbm);
   eng.finish();
   if (tc::owns_row()) {
   const int n = threadIdx.x;

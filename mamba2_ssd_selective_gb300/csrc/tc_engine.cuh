@@ -1,24 +1,19 @@
-// A small tcgen05 contraction engine for the chunk kernels of the bf16 path.
+// A small tcgen05 contraction engine for the chunk-state and Z kernels of the
+// bf16 path.
 //
 // One CTA of 256 threads owns a 128-row accumulator block in tensor memory
-// (TMEM lane = row, owned by threads 0..127; all 256 threads stage operands).  A contraction  D[128 x NT] (+)= sum_k A[m,k] B[n,k]  is
-// fed 64 k at a time: every thread stages its share of the A and B tiles
-// straight into shared memory in the 128-byte-swizzled UMMA layout (so masks,
-// decays and scalings are applied while staging and nothing is materialised in
-// HBM), then one thread issues four 128 x NT x 16 tcgen05.mma and commits them
-// to the stage's mbarrier.  A ring of NSTAGE stages lets the staging of the
-// next 64-k slice overlap the tensor-core work of the previous ones.
-//
-// Each operand is given as fetch(m, k) -> raw data and make(raw, m, k) -> 8 bf16
-// packed in a uint4:
-//   K-major operand:  elements (m, k .. k+7)
-//   MN-major operand: elements (m .. m+7, k)
-// (pick the one whose 8 elements are contiguous in the source).
+// (TMEM lane = row; all 256 threads stage operands, threads 0..127 drain it).
+// A contraction  D[128 x NT] = sum_k A[m,k] B[n,k]  with both operands MN-major
+// (8 consecutive m or n of one k contiguous in the source) is fed 64 k at a
+// time: A is copied as it is with cp.async, B goes through registers as
+// fetch(n, k) -> raw data and make(raw, n, k) -> 8 packed bf16 (so scalings are
+// applied while staging and nothing is materialised in HBM), both straight into
+// the 128-byte-swizzled UMMA layout; one thread then issues four 128 x NT x 16
+// tcgen05.mma and commits them to the stage's mbarrier.  The loads of the next
+// slice are in flight while the current one is staged and its MMAs run.
 #pragma once
 
 #include <cuda_bf16.h>
-
-#include <type_traits>
 
 #include "sm100.cuh"
 
@@ -27,11 +22,9 @@ namespace tc {
 
 using namespace sm100;
 
-enum Major : int { K_MAJOR = 0, MN_MAJOR = 1 };
 // Every engine CTA has kThreads threads: all of them stage operands; the first
-// 128 (warps 0-3, one per TMEM lane quadrant) own the accumulator rows.
+// 128 (warps 0-3, one per TMEM lane quadrant) drain the accumulator rows.
 constexpr int kThreads = 256;
-constexpr int kRows = 128;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -50,17 +43,6 @@ __device__ __forceinline__ void unpack8(uint4 u, float (&v)[8]) {
   }
 }
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
-__device__ __forceinline__ void ld8f(const float *p, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-// make() marker for operands copied as they are: fetch(m, k) then returns the
-// global address of the 16 bytes, and the engine copies them with cp.async
-// straight into their swizzled slot (no registers, every copy in flight at once).
-struct Async {};
-template <class FM>
-constexpr bool kIsAsync = std::is_same<FM, Async>::value;
 
 template <int NT, int NSTAGE>
 struct Engine {
@@ -76,7 +58,6 @@ struct Engine {
   int *status;
   uint32_t uses[NSTAGE];
   uint32_t done_uses;
-  int stage;
 
   // call from all threads; thread 0 initialises the barriers (sync afterwards)
   __device__ void init(uint8_t *ring_, uint64_t *bars_, int *status_) {
@@ -86,142 +67,85 @@ struct Engine {
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) uses[s] = 0;
     done_uses = 0;
-    stage = 0;
     if (threadIdx.x == 0) {
       for (int s = 0; s <= NSTAGE; ++s) mbar_init(&bars[s], 1);
       fence_mbar_init();
     }
   }
 
-  // Operands come as two callables: fetch(m, k) issues the global loads and
-  // returns the raw data, make(raw, m, k) turns it into 8 packed bf16.  Every
-  // thread first issues the loads of kBatch chunks back to back, then
-  // transforms and stores them, so kBatch loads per thread are in flight.
-  static constexpr int kBatchMax = 4;
-
-  template <int MA, class FL, class FM>
-  __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FL &fl, const FM &fm) {
-    using Raw = decltype(fl(0, 0));
+  // cp.async of the A tile of the 64-wide k slice [k0, k0+64) into its stage:
+  // fl(m, k) is the global address of the 16 bytes holding A[m .. m+7, k].
+  template <class FL>
+  __device__ __forceinline__ void stage_A(uint8_t *A, int k0, const FL &fl) {
     constexpr int PER = (128 * 8) / kThreads;  // 16-byte chunks per thread
-    constexpr int kBatch = PER < kBatchMax ? PER : kBatchMax;
-    if constexpr (kIsAsync<FM>) {
-      const uint32_t a0 = smem_u32(A);
+    const uint32_t a0 = smem_u32(A);
 #pragma unroll
-      for (int q = 0; q < PER; ++q) {
-        const int e = threadIdx.x + q * kThreads;
-        if constexpr (MA == K_MAJOR) {
-          const int m = e >> 3, c = e & 7;
-          cp_async16(a0 + sw128_offset(m, c * 8), fl(m, k0 + c * 8));
-        } else {
-          const int r = e >> 4, c = e & 15;
-          cp_async16(a0 + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8), fl(c * 8, k0 + r));
-        }
-      }
-      return;
-    } else {
-#pragma unroll
-    for (int g = 0; g < PER; g += kBatch) {
-      Raw raw[kBatch];
-      int mm[kBatch], kk[kBatch];
-      uint32_t off[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int e = threadIdx.x + (g + q) * kThreads;
-        if constexpr (MA == K_MAJOR) {
-          const int m = e >> 3, c = e & 7;
-          mm[q] = m; kk[q] = k0 + c * 8; off[q] = sw128_offset(m, c * 8);
-        } else {  // two 64-wide MN atoms, 64 k-rows each
-          const int r = e >> 4, c = e & 15;
-          mm[q] = c * 8; kk[q] = k0 + r; off[q] = (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8);
-        }
-        raw[q] = fl(mm[q], kk[q]);
-      }
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) *reinterpret_cast<uint4 *>(A + off[q]) = fm(raw[q], mm[q], kk[q]);
-    }
+    for (int q = 0; q < PER; ++q) {
+      const int e = threadIdx.x + q * kThreads;
+      const int r = e >> 4, c = e & 15;  // two 64-wide MN atoms, 64 k-rows each
+      cp_async16(a0 + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8), fl(c * 8, k0 + r));
     }
   }
 
-  template <int MB, class FL, class FM>
-  __device__ __forceinline__ void stage_B(uint8_t *B, int k0, const FL &fl, const FM &fm) {
-    using Raw = decltype(fl(0, 0));
-    static_assert(MB == K_MAJOR || NT % 64 == 0, "MN-major B needs whole 64-wide atoms");
-    constexpr int CPR = NT / 8;  // 16-byte chunks per k-row (MN-major)
-    constexpr int PER = (NT * 8) / kThreads;
-    constexpr int kBatch = PER < kBatchMax ? PER : kBatchMax;
-    static_assert(PER >= 1 && PER % kBatch == 0, "B chunks per thread");
-    if constexpr (kIsAsync<FM>) {
-      const uint32_t b0 = smem_u32(B);
+  // A whole contraction over k in [0, nk) (nk a multiple of 64) with both
+  // operands MN-major, A copied as it is (cp.async) and B through fetch/make,
+  // software-pipelined: the loads of slice s+1 (A's copies and B's registers)
+  // are issued before slice s's B is transformed and stored and its MMAs
+  // issued, so a slice of loads is always in flight behind the one being
+  // staged.  Must be called by all threads.
+  template <class FAL, class FBL, class FBM>
+  __device__ __forceinline__ void contract_pipelined(uint32_t tmem_d, int nk, const FAL &fal, const FBL &fbl,
+                                                     const FBM &fbm) {
+    static_assert(NSTAGE >= 2 && NT % 64 == 0, "pipelined contraction: two stages, whole MN atoms");
+    using Raw = decltype(fbl(0, 0));
+    constexpr int CPR = NT / 8, PER_B = (NT * 8) / kThreads;
+    Raw cur[PER_B], nxt[PER_B];
+    auto issue = [&](int s, Raw(&raw)[PER_B]) {
+      const int st = s % NSTAGE, k0 = 64 * s;
+      if (uses[st] > 0) mbar_wait(&bars[st], (uses[st] - 1) & 1, status);
+      stage_A(ring + st * STAGE_BYTES, k0, fal);
+      asm volatile("cp.async.commit_group;" ::: "memory");
 #pragma unroll
-      for (int q = 0; q < PER; ++q) {
-        const int e = threadIdx.x + q * kThreads;
-        if constexpr (MB == K_MAJOR) {
-          const int n = e >> 3, c = e & 7;
-          cp_async16(b0 + sw128_offset(n, c * 8), fl(n, k0 + c * 8));
-        } else {
-          const int r = e / CPR, c = e % CPR;
-          cp_async16(b0 + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8), fl(c * 8, k0 + r));
-        }
+      for (int q = 0; q < PER_B; ++q) {
+        const int e = threadIdx.x + q * kThreads, r = e / CPR, c = e % CPR;
+        raw[q] = fbl(c * 8, k0 + r);
       }
-      return;
-    } else {
+    };
+    const int ns = nk / 64;
+    issue(0, cur);
+    for (int s = 0; s < ns; ++s) {
+      const int st = s % NSTAGE, k0 = 64 * s;
+      const bool more = s + 1 < ns;
+      if (more) issue(s + 1, nxt);
+      uint8_t *A = ring + st * STAGE_BYTES, *B = A + A_BYTES;
 #pragma unroll
-    for (int g = 0; g < PER; g += kBatch) {
-      Raw raw[kBatch];
-      int nn[kBatch], kk[kBatch];
-      uint32_t off[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int e = threadIdx.x + (g + q) * kThreads;
-        if constexpr (MB == K_MAJOR) {
-          const int n = e >> 3, c = e & 7;
-          nn[q] = n; kk[q] = k0 + c * 8; off[q] = sw128_offset(n, c * 8);
-        } else {
-          const int r = e / CPR, c = e % CPR;
-          nn[q] = c * 8; kk[q] = k0 + r; off[q] = (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8);
-        }
-        raw[q] = fl(nn[q], kk[q]);
+      for (int q = 0; q < PER_B; ++q) {
+        const int e = threadIdx.x + q * kThreads, r = e / CPR, c = e % CPR;
+        *reinterpret_cast<uint4 *>(B + (c >> 3) * 8192 + sw128_offset(r, (c & 7) * 8)) = fbm(cur[q], c * 8, k0 + r);
       }
+      if (more)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // this slice's copies; the next may fly
+      else
+        cp_async_wait_all();
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+        constexpr uint32_t idesc = idesc_bf16(128, NT, true, true);
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) *reinterpret_cast<uint4 *>(B + off[q]) = fm(raw[q], nn[q], kk[q]);
-    }
-    }
-  }
-
-  // Stage the 64-wide k slice [k0, k0+64) of A and B and issue its MMAs into the
-  // accumulator at TMEM address tmem_d.  Must be called by all 128 threads.
-  // With tmem_d2 != kNone the same staged operands are also issued into a
-  // second accumulator (accumulate2 selects whether that one accumulates).
-  static constexpr uint32_t kNone = 0xffffffffu;
-  template <int MA, int MB, class FAL, class FAM, class FBL, class FBM>
-  __device__ __forceinline__ void slice(uint32_t tmem_d, int k0, const FAL &fal, const FAM &fam, const FBL &fbl,
-                                        const FBM &fbm, bool accumulate, uint32_t tmem_d2 = kNone,
-                                        bool accumulate2 = false) {
-    const int s = stage;
-    if (uses[s] > 0) mbar_wait(&bars[s], (uses[s] - 1) & 1, status);
-    uint8_t *A = ring + s * STAGE_BYTES;
-    uint8_t *B = A + A_BYTES;
-    stage_A<MA>(A, k0, fal, fam);
-    stage_B<MB>(B, k0, fbl, fbm);
-    if constexpr (kIsAsync<FAM> || kIsAsync<FBM>) cp_async_wait_all();
-    fence_async_smem();
-    tc_fence_before();  // order this thread's earlier TMEM reads before the MMAs below
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
-      constexpr uint32_t idesc = idesc_bf16(128, NT, MA == MN_MAJOR, MB == MN_MAJOR);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = MA == K_MAJOR ? desc_sw128(a0 + kk * 32, 16, 1024) : desc_sw128(a0 + kk * 2048, 8192, 1024);
-        const uint64_t bd = MB == K_MAJOR ? desc_sw128(b0 + kk * 32, 16, 1024) : desc_sw128(b0 + kk * 2048, 8192, 1024);
-        umma_bf16(tmem_d, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
-        if (tmem_d2 != kNone) umma_bf16(tmem_d2, ad, bd, idesc, (accumulate2 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem_d, desc_sw128(a0 + kk * 2048, 8192, 1024), desc_sw128(b0 + kk * 2048, 8192, 1024), idesc,
+                    (s > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[st]);
       }
-      umma_commit(&bars[s]);
+      uses[st] += 1;
+      if (more) {
+#pragma unroll
+        for (int q = 0; q < PER_B; ++q) cur[q] = nxt[q];
+      }
     }
-    uses[s] += 1;
-    stage = (s + 1 == NSTAGE) ? 0 : s + 1;
   }
 
   // Wait until every MMA issued so far has completed (all threads).
@@ -231,25 +155,6 @@ struct Engine {
     done_uses += 1;
     tc_fence_after();
   }
-};
-
-// make() for operands that are already 8 packed bf16
-struct AsIs {
-  __device__ __forceinline__ uint4 operator()(uint4 r, int, int) const { return r; }
-};
-// 8 fp32 values fetched as two float4
-struct F8 {
-  float4 a, b;
-};
-__device__ __forceinline__ F8 ldf8(const float *p) {
-  return F8{__ldg(reinterpret_cast<const float4 *>(p)), __ldg(reinterpret_cast<const float4 *>(p) + 1)};
-}
-__device__ __forceinline__ void f8_to(const F8 &r, float (&v)[8]) {
-  v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w; v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
-}
-// two fp32 rows fetched together (state + segment state, combined in make())
-struct F16 {
-  F8 x, y;
 };
 
 // Shared-memory carve-up helper for kernels built on the engine: returns the
@@ -280,8 +185,8 @@ __device__ __forceinline__ void tmem_free_cta(uint32_t base, uint32_t ncols) {
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int col) {
   return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
 }
-// true for the threads that own an accumulator row
-__device__ __forceinline__ bool owns_row() { return threadIdx.x < kRows; }
+// true for the threads that drain an accumulator row
+__device__ __forceinline__ bool owns_row() { return threadIdx.x < 128; }
 
 }  // namespace tc
 }  // namespace ssd
