@@ -88,6 +88,44 @@ def test_segment_count_sweep(oracle_lib, S, dtype, seq):
     compare_backward(g, oracle_lib.backward(inp, shape, use_dfinal=False), shape, TOL[dtype])
 
 
+def test_reads_the_in_projection_output_in_place(oracle_lib):
+    """x, B, C and dt read straight out of one (b, L, z | x | B | C | dt) buffer, the
+    layout the in-projection GEMM writes, through token strides; the gradients
+    written into the matching slots of one such buffer.  Nothing is copied."""
+    shape = SsdShape(1, 1024, 8, 64, 128, 1, 256, 2)
+    inp = make_inputs(shape, 13, "bf16", dfinal=True, seq_lengths=[700, 324])
+    s = shape
+    HP, GN, H, Cd = s.nheads * s.headdim, s.ngroups * s.dstate, s.nheads, s.conv_dim
+    D_in = 2 * HP + 2 * GN + H  # z | x | B | C | dt, a multiple of 8 elements here
+    t = to_dev(inp)
+    zxbcdt = torch.randn(s.batch, s.seqlen, D_in, device="cuda").to(torch.bfloat16)
+    zxbcdt[..., HP:HP + Cd] = t["xBC"]
+    zxbcdt[..., HP + Cd:] = t["dt_raw"]
+    es, base = zxbcdt.element_size(), zxbcdt.data_ptr()
+    ins = ssd.SsdInputs(base + HP * es, D_in, base + 2 * HP * es, D_in, base + (2 * HP + GN) * es, D_in,
+                        base + (HP + Cd) * es, D_in, t["dt_bias"].data_ptr(), t["A_log"].data_ptr(),
+                        t["D"].data_ptr(), t["conv_w"].data_ptr(), t["conv_b"].data_ptr(), t["seq_idx"].data_ptr())
+    r = ssd.SsdRunner(shape, "bf16")
+    y, fin, seg = r.alloc_outputs()
+    ssd.ssd_forward(r.dims, ins, y, fin, seg, r.workspace)
+    torch.cuda.synchronize()
+    got = {"y": y.float().cpu().numpy().reshape(s.batch, s.seqlen, H, s.headdim),
+           "final_state": fin.cpu().numpy(), "seg_in": seg.cpu().numpy()}
+    compare_forward(got, oracle_lib.forward(inp, shape), TOL["bf16"])
+    dbuf = torch.full_like(zxbcdt, float("nan"))  # the z slot must stay untouched
+    g = r.alloc_grads()
+    gb, dbase = dbuf.element_size(), dbuf.data_ptr()
+    gs = ssd.SsdGrads(dbase + HP * gb, D_in, dbase + 2 * HP * gb, D_in, dbase + (2 * HP + GN) * gb, D_in,
+                      dbase + (HP + Cd) * gb, D_in, g["ddt_bias"].data_ptr(), g["dA_log"].data_ptr(),
+                      g["dD"].data_ptr(), g["dconv_w"].data_ptr(), g["dconv_b"].data_ptr())
+    ssd.ssd_backward(r.dims, ins, t["dy"], t["dfinal"], seg, gs, r.workspace)
+    torch.cuda.synchronize()
+    assert torch.isnan(dbuf[..., :HP].float()).all()
+    out = {"dxBC": dbuf[..., HP:HP + Cd].float().cpu().numpy(), "ddt_raw": dbuf[..., HP + Cd:].float().cpu().numpy()}
+    out.update({k: g[k].float().cpu().numpy() for k in ("ddt_bias", "dA_log", "dD", "dconv_w", "dconv_b")})
+    compare_backward(out, oracle_lib.backward(inp, shape), shape, TOL["bf16"])
+
+
 def test_backward_recomputes_segment_states(oracle_lib):
     shape = SsdShape(1, 1024, 4, 64, 128, 1, 128, 4)
     inp = make_inputs(shape, 12, "bf16", dfinal=True)
