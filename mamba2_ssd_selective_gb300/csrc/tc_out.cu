@@ -57,7 +57,7 @@ constexpr uint32_t kVecStride = 3200;            // acs[256] f32 | dt[256] f32 |
 constexpr uint32_t kSmV = kSmS + kNSB * 16384;   // 2 vector buffers
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;   // 2 x {a[256], b[256], f[256]} f32 (decay tables per head)
 constexpr uint32_t kSmBar = kSmD + 2 * 3072;
-constexpr int kNumBars = 9 + 2 * kNA + 2 * kNX + 8 + 4;
+constexpr int kNumBars = 9 + 2 * kNA + 2 * kNX + 2 * kNSB + 4 + 4;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -86,7 +86,7 @@ struct Bars {
   uint64_t *vec_full, *vec_free;             // [2]
   uint64_t *a_full, *a_free;                 // [kNA]
   uint64_t *x_full, *x_free;                 // [kNX]
-  uint64_t *s_full, *s_free;                 // [2]
+  uint64_t *s_full, *s_free;                 // [kNSB]
   uint64_t *acc_full, *acc_free;             // [2]
   pipe::UnitRing units;
   __device__ Bars(uint64_t *b, int *slot) {
@@ -102,8 +102,8 @@ struct Bars {
     x_full = a_free + kNA;
     x_free = x_full + kNX;
     s_full = x_free + kNX;
-    s_free = s_full + 2;
-    acc_full = s_free + 2;
+    s_free = s_full + kNSB;
+    acc_full = s_free + kNSB;
     acc_free = acc_full + 2;
     units.full = acc_free + 2;
     units.free = units.full + 2;
@@ -138,10 +138,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.vec_full[i], 1);
       mbar_init(&bar.vec_free[i], kTransformWarps + kEpilogueWarps);
-      mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_free[i], 1);
       mbar_init(&bar.acc_full[i], 1);
       mbar_init(&bar.acc_free[i], kEpilogueWarps);
+    }
+    for (int i = 0; i < kNSB; ++i) {
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.units.full[i], 1);
