@@ -12,36 +12,6 @@
 
 namespace ssd {
 
-// 8 consecutive channels of one token as fp32 (16-byte loads for bf16)
-template <typename T> __device__ __forceinline__ void load8(const T *p, float (&v)[8]);
-template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4 *>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-template <> __device__ __forceinline__ void load8<float>(const float *p, float (&v)[8]) {
-  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-template <typename T> __device__ __forceinline__ void store8(T *p, const float (&v)[8]);
-template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *p, const float (&v)[8]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    w[i] = *reinterpret_cast<uint32_t *>(&b);
-  }
-  *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-template <> __device__ __forceinline__ void store8<float>(float *p, const float (&v)[8]) {
-  reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-
 // 2 consecutive channels (one 32-bit load for bf16)
 __device__ __forceinline__ void load2(const __nv_bfloat16 *p, float (&v)[2]) {
   const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
@@ -58,26 +28,6 @@ __device__ __forceinline__ void store2(__nv_bfloat16 *p, const float (&v)[2]) {
 }
 __device__ __forceinline__ void store2(float *p, const float (&v)[2]) {
   *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
-}
-
-// 4 consecutive channels (8-byte loads for bf16)
-template <typename T> __device__ __forceinline__ void load4(const T *p, float (&v)[4]);
-template <> __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[4]) {
-  const uint2 u = *reinterpret_cast<const uint2 *>(p);
-  v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
-  v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
-}
-template <> __device__ __forceinline__ void load4<float>(const float *p, float (&v)[4]) {
-  const float4 a = *reinterpret_cast<const float4 *>(p);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-}
-template <typename T> __device__ __forceinline__ void store4(T *p, const float (&v)[4]);
-template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, const float (&v)[4]) {
-  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
-  *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
-}
-template <> __device__ __forceinline__ void store4<float>(float *p, const float (&v)[4]) {
-  *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // A tile of kCh channels that lies inside one of the x, B, C regions of xBC
