@@ -136,8 +136,10 @@ ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *
  * device looks up the array's device address (make that first call before any
  * stream capture); no call allocates or frees memory.  All calls share the one
  * array, so calls whose GPU work may overlap (other streams, other host
- * threads) race on it and must be serialised by the caller.  This entry point
- * has no counterpart in the pages the method comes from. */
+ * threads) race on it and must be serialised by the caller.  The array's
+ * status word (a device-side wait that gave up) is read with
+ * ssd_device_status(NULL, stream).  This entry point has no counterpart in the
+ * pages the method comes from. */
 #define SSD_STATIC_SCRATCH_BYTES (32u << 20)
 ssd_status ssd_forward_static(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
                               float *seg_init_states, ssd_stream_t stream);
@@ -152,8 +154,23 @@ ssd_status ssd_cu_seqlens_to_seq_idx(const int32_t *cu_seqlens, int32_t nseq, in
 
 /* Reads the device status word kept in `workspace` by the last call that used
  * it (synchronises `stream`): SSD_OK, or SSD_ERR_DEVICE_TIMEOUT if a bounded
- * device-side wait gave up. */
+ * device-side wait gave up (the outputs of that call are then garbage; the
+ * context stays usable and the next call starts from a cleared word).
+ * workspace = NULL reads the word of ssd_forward_static's fixed scratch array
+ * on the current device instead.  Returns SSD_ERR_CUDA if the read fails. */
 ssd_status ssd_device_status(const void *workspace, ssd_stream_t stream);
+
+/* Failure detection.  Every wait of one role of a kernel on another (mbarrier
+ * hand-offs inside the tensor-core kernels) gives up after this limit,
+ * raises the status word that ssd_device_status reads and lets the kernel
+ * finish: it drains the copies and tensor-core operations it started, frees
+ * its tensor memory and returns, so the process can carry on.  Applies to the
+ * calls made after it, from any host thread; returns the previous limit.  The
+ * default, SSD_DEFAULT_WAIT_LIMIT_NS (1.5 s), is far above any real hand-off;
+ * a limit of 0 makes every wait that is not already satisfied give up (a way
+ * to exercise the failure path). */
+#define SSD_DEFAULT_WAIT_LIMIT_NS 1500000000ull
+uint64_t ssd_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Per-kernel timing for benchmarks.  After ssd_profile_begin(), every kernel
  * that ssd_forward / ssd_backward launch (from this host thread) is bracketed

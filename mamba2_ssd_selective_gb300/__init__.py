@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "SsdError", "SsdDims", "SsdInputs", "SsdGrads", "load", "ssd_workspace_size", "ssd_forward", "ssd_backward",
     "ssd_forward_static", "STATIC_SCRATCH_BYTES",
-    "ssd_cu_seqlens_to_seq_idx", "ssd_device_status", "ssd_status_string", "ssd_profile_begin",
+    "ssd_cu_seqlens_to_seq_idx", "ssd_device_status", "ssd_set_wait_limit_ns", "DEFAULT_WAIT_LIMIT_NS",
+    "ssd_status_string", "ssd_profile_begin",
     "ssd_profile_end", "SsdKernelTime", "SsdRunner",
     "SSD_BF16", "SSD_F32",
 ]
@@ -86,6 +87,8 @@ def load():
         lib.ssd_cu_seqlens_to_seq_idx.restype = I
         lib.ssd_device_status.argtypes = [P, P]
         lib.ssd_device_status.restype = I
+        lib.ssd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.ssd_set_wait_limit_ns.restype = ctypes.c_uint64
         lib.ssd_profile_begin.argtypes = []
         lib.ssd_profile_begin.restype = I
         lib.ssd_profile_end.argtypes = [ctypes.POINTER(SsdKernelTime), ctypes.c_int32]
@@ -156,7 +159,17 @@ def ssd_cu_seqlens_to_seq_idx(cu_seqlens, seq_idx, stream=None) -> None:
 
 
 def ssd_device_status(workspace, stream=None) -> int:
+    """Status word of the last call that used ``workspace`` (None: the static
+    scratch of ssd_forward_static); 0 = ok, -9 = a device-side wait gave up."""
     return int(load().ssd_device_status(_ptr(workspace), _stream(stream)))
+
+
+DEFAULT_WAIT_LIMIT_NS = 1_500_000_000
+
+
+def ssd_set_wait_limit_ns(limit_ns: int) -> int:
+    """Limit of the kernels' bounded device-side waits for later calls; returns the previous one."""
+    return int(load().ssd_set_wait_limit_ns(int(limit_ns)))
 
 
 def ssd_profile_begin() -> None:

@@ -1,5 +1,6 @@
 // libssd C ABI: argument validation, workspace carving and the launch sequence
 // of the forward and backward passes.  Nothing here allocates or synchronises.
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -10,6 +11,9 @@
 using namespace ssd;
 
 namespace {
+
+// limit of the kernels' bounded hand-off waits, for every later call
+std::atomic<unsigned long long> g_wait_limit_ns{sm100::kDefaultWaitLimitNs};
 
 int elem_bytes(int dtype) { return dtype == SSD_BF16 ? 2 : 4; }
 
@@ -46,6 +50,7 @@ Problem problem_from(const ssd_dims *d) {
   pr.nc = pr.L / pr.Q;
   pr.cps = pr.nc / pr.S;
   pr.hpg = pr.H / pr.G;
+  pr.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   return pr;
 }
 
@@ -374,12 +379,17 @@ ssd_status ssd_cu_seqlens_to_seq_idx(const int32_t *cu_seqlens, int32_t nseq, in
 }
 
 ssd_status ssd_device_status(const void *workspace, ssd_stream_t stream) {
-  if (!workspace) return SSD_ERR_NULL_PTR;
+  const void *word = workspace ? workspace : static_scratch_ptr();
+  if (!word) return SSD_ERR_CUDA;
   int v = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSD_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
   return v == 0 ? SSD_OK : SSD_ERR_DEVICE_TIMEOUT;
+}
+
+uint64_t ssd_set_wait_limit_ns(uint64_t limit_ns) {
+  return g_wait_limit_ns.exchange(limit_ns);
 }
 
 ssd_status ssd_profile_begin(void) {

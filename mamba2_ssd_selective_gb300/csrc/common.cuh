@@ -22,6 +22,7 @@ struct Problem {
   const float *cdec;    // product of the chunk's per-token decays (0 at row start / sequence start inside)
   const float *dstart;  // product of cdec over the segment's chunks before this one
   const float *dend;    // product of cdec over the segment's chunks after this one
+  unsigned long long wait_ns;  // limit of the kernels' bounded hand-off waits (ssd_set_wait_limit_ns)
 };
 
 // ---------------------------------------------------------------- dtypes

@@ -52,30 +52,55 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase.  After kWaitTimeoutNs (well over a
-// second of wall time) it gives up, raises the device status word and returns
-// false; the caller carries on without the data (results are then garbage but
-// the kernel terminates, frees its tensor memory and the host sees
-// SSD_ERR_DEVICE_TIMEOUT).  A waiter that finds the status word already raised
-// (another wait gave up) returns at once, so a broken pipeline drains quickly.
-// Waiting threads are parked by the hardware between polls.
-constexpr uint64_t kWaitTimeoutNs = 1500ull * 1000ull * 1000ull;
+// Bounded waits on mbarrier phases.
+//
+// WaitCtl travels with every kernel that waits: the device status word and
+// the wait limit (ssd_set_wait_limit_ns on the host; 1.5 s by default).
+//
+// mbar_wait: a hand-off between roles of a kernel.  After limit_ns it gives
+// up, raises the status word and returns false; the caller carries on without
+// the data (results are then garbage; the host sees SSD_ERR_DEVICE_TIMEOUT).
+// A waiter that finds the status word already raised (another wait gave up)
+// returns at once, so a broken pipeline drains quickly.  Waiting threads are
+// parked by the hardware between polls, for at most min(limit, 20 us) each.
+//
+// mbar_wait_drain: a completion the waiting thread is owed by the hardware
+// (a TMA load it issued, a commit of MMAs it issued).  These always arrive,
+// so the wait ignores the status word: a CTA uses it before it releases the
+// shared or tensor memory those operations touch.  It is bounded by
+// kDrainLimitNs all the same.
+struct WaitCtl {
+  int *status;        // device status word
+  uint64_t limit_ns;  // give up a hand-off wait after this long
+};
+constexpr uint64_t kDefaultWaitLimitNs = 1500ull * 1000ull * 1000ull;
+constexpr uint64_t kDrainLimitNs = 2000ull * 1000ull * 1000ull;
 constexpr uint32_t kWaitHintNs = 20000u;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &w) {
   // the clock is read only once a parked wait has come back empty-handed, so
   // that the common hand-off (completed within the first parked wait) does not
   // carry its latency
-  if (mbar_try_wait(bar, parity) || mbar_try_wait_hint(bar, parity, kWaitHintNs)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = w.limit_ns < kWaitHintNs ? (uint32_t)w.limit_ns : kWaitHintNs;
+  if (mbar_try_wait_hint(bar, parity, hint)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
+    if ((i & 7u) == 7u) {
+      if (*reinterpret_cast<volatile int *>(w.status) != 0) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) break;
+    }
+  }
+  atomicExch(w.status, 1);
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait_hint(bar, parity, kWaitHintNs)) return true;
-    if ((i & 7u) == 7u) {
-      if (status && *reinterpret_cast<volatile int *>(status) != 0) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
-    }
+    if ((i & 7u) == 7u && globaltimer_ns() - t0 > kDrainLimitNs) return false;
   }
-  if (status) atomicExch(status, 1);
-  return false;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -42,7 +42,7 @@ constexpr uint32_t kSmV = kSmDS + 16384;
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], g[256]}
 constexpr uint32_t kSmVC = kSmD + 2 * 2048;     // 2 x vcol partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVC + 2 * 2048;
-constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4;
+constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4 + 1;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -58,7 +58,7 @@ struct Unit {
 // its values are ready, one proxy fence, then one arrival per slot.
 template <int NP>
 __device__ __forceinline__ void put_operands(const float (&v)[NP][16], uint32_t &na, uint32_t sA, int row, int cg,
-                                             uint64_t *a_full, uint64_t *a_free, int *status) {
+                                             uint64_t *a_full, uint64_t *a_free, const WaitCtl &status) {
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const uint32_t n = na + p, as = n % kNA;
@@ -101,6 +101,7 @@ struct Bars {
   uint64_t *ring_full, *ring_free, *vec_full, *vec_free, *xt_full, *xt_free;  // [2]
   uint64_t *dy_full, *dy_free;                                                // [kNY]
   uint64_t *a_full, *a_free;                                                  // [kNA]
+  uint64_t *drain;                                                            // the MMA issuer's final commit
   pipe::UnitRing units;
   __device__ Bars(uint64_t *b, int *slot) {
     unit_full = b;
@@ -123,6 +124,7 @@ struct Bars {
     a_free = a_full + kNA;
     units.full = a_free + kNA;
     units.free = units.full + 2;
+    drain = units.free + 2;
     units.slot = slot;
   }
 };
@@ -134,8 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_ds, Problem pr, const bf16 *__restrict__ u,
                       const bf16 *__restrict__ dy, const float *__restrict__ dtv, const float *__restrict__ acs,
                       float *__restrict__ du, float *__restrict__ dbp, float *__restrict__ tok, int HB, int nunits,
-                      int *counter, int *status) {
+                      int *counter, int *status_word) {
   extern __shared__ uint8_t smem_raw[];
+  const WaitCtl status{status_word, pr.wait_ns};
   uint8_t *sm = tc::aligned_smem(smem_raw);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
   Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar), reinterpret_cast<int *>(tslot + 1));
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
 
   if (threadIdx.x == 0) {
-    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.tu_full, bar.ds_full, bar.ds_free, bar.db_full};
+    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.tu_full, bar.ds_full, bar.ds_free, bar.db_full, bar.drain};
     for (uint64_t *b : ones) mbar_init(b, 1);
     mbar_init(bar.tu_free, kEWarps);
     mbar_init(bar.db_free, kEWarps);
@@ -186,16 +189,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_u);
       prefetch_tmap(&tm_dy);
       prefetch_tmap(&tm_ds);
-      uint32_t nu = 0, nh = 0, m = 0, nd = 0;
+      // counts of armed loads per barrier (nua: unit operand sets); once a
+      // wait has failed (ok = false) no further load is issued, stop is
+      // published, and the loads in flight are drained before the CTA ends
+      uint32_t nu = 0, nua = 0, nh = 0, nxt = 0, m = 0, nd = 0;
+      bool ok = true;
       int next = atomicAdd(counter, 1);
       for (;; ++nu) {
-        const int ui = pipe::publish_unit(bar.units, nu, next, nunits, status);
+        const int ui = pipe::publish_unit(bar.units, nu, ok ? next : nunits, nunits);
         if (ui >= nunits) break;
         next = atomicAdd(counter, 1);
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, nsl = (pr.Q - 128 * o.J) / 64;
         const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N, rJ = row0 + 128 * o.J;
-        if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
+        if (nu > 0) ok = mbar_wait(bar.unit_free, parity(nu - 1), status);
+        if (!ok) continue;
         mbar_expect_tx(bar.unit_full, 32768 + 2 * nsl * 8192);
         for (int kh = 0; kh < 2; ++kh) {
           for (int r = 0; r < 2; ++r)
@@ -203,9 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < nsl; ++r)
             tma_load_2d(sm + kSmCR + kh * 32768 + r * 8192, &tm_u, bar.unit_full, offC + 64 * kh, rJ + 64 * r);
         }
-        for (int hh = 0; hh < HB; ++hh, ++nh) {
+        ++nua;
+        for (int hh = 0; hh < HB && ok; ++hh) {
           const int h = o.h0 + hh, vb = nh & 1;
-          if (nh >= 2) mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status);
+          if (nh >= 2 && !mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status)) {
+            ok = false;
+            break;
+          }
           uint8_t *vec = sm + kSmV + vb * kVecStride;
           const size_t bh = ((size_t)o.bb * pr.H + h) * pr.L + t0;
           const uint32_t seq_bytes = !has_seq ? 0u : (uint32_t)(pr.Q * 4);
@@ -214,17 +226,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           pipe::bulk_load(vec + 1024, dtv + bh, pr.Q * 4, &bar.vec_full[vb]);
           if (has_seq)
             pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
-          if (nh >= 2) mbar_wait(&bar.xt_free[vb], parity(nh / 2 - 1), status);
+          ++nh;
+          if (nxt >= 2 && !mbar_wait(&bar.xt_free[vb], parity(nxt / 2 - 1), status)) {
+            ok = false;
+            break;
+          }
           mbar_expect_tx(&bar.xt_full[vb], 16384);
           for (int r = 0; r < 2; ++r)
             tma_load_2d(sm + kSmXT + vb * 16384 + r * 8192, &tm_u, &bar.xt_full[vb], h * pr.P, rJ + 64 * r);
-          for (int s = 0; s < nsl; ++s, ++m) {
+          ++nxt;
+          for (int s = 0; s < nsl; ++s) {
             const int ys = m % kNY;
-            if (m >= kNY) mbar_wait(&bar.dy_free[ys], parity(m / kNY - 1), status);
+            if (m >= kNY && !mbar_wait(&bar.dy_free[ys], parity(m / kNY - 1), status)) {
+              ok = false;
+              break;
+            }
             mbar_expect_tx(&bar.dy_full[ys], 8192);
             tma_load_2d(sm + kSmDY + ys * 8192, &tm_dy, &bar.dy_full[ys], h * pr.P, rJ + 64 * s);
+            ++m;
           }
-          if (nd >= 1) mbar_wait(bar.ds_free, parity(nd - 1), status);
+          if (!ok) break;
+          if (nd >= 1 && !mbar_wait(bar.ds_free, parity(nd - 1), status)) {
+            ok = false;
+            break;
+          }
           mbar_expect_tx(bar.ds_full, 16384);
           const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
           tma_load_2d(sm + kSmDS, &tm_ds, bar.ds_full, 0, srow);
@@ -232,6 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nd;
         }
       }
+      // every load issued has landed before the CTA releases its shared memory
+      if (nua > 0) mbar_wait_drain(bar.unit_full, parity(nua - 1));
+      for (uint32_t n = nh > 2u ? nh - 2u : 0u; n < nh; ++n) mbar_wait_drain(&bar.vec_full[n & 1], parity(n / 2));
+      for (uint32_t n = nxt > 2u ? nxt - 2u : 0u; n < nxt; ++n) mbar_wait_drain(&bar.xt_full[n & 1], parity(n / 2));
+      for (uint32_t n = m > (uint32_t)kNY ? m - kNY : 0u; n < m; ++n)
+        mbar_wait_drain(&bar.dy_full[n % kNY], parity(n / kNY));
+      if (nd > 0) mbar_wait_drain(bar.ds_full, parity(nd - 1));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -247,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_db = idesc_bf16(128, 128, false, true);    // W^T C, (wdt x) dS
       uint32_t nu = 0, nh = 0, m = 0, na = 0, nd = 0;
       for (;; ++nu) {
-        const int ui = pipe::next_unit(bar.units, nu, nunits, status, false);
+        const int ui = pipe::next_unit(bar.units, nu, nunits, false);
         if (ui >= nunits) break;
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int nsl = (pr.Q - 128 * o.J) / 64;
@@ -315,13 +347,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bar.db_full);
         umma_commit(bar.unit_free);
       }
-      if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
+      // drain: every MMA issued here has completed and every commit arrival
+      // has landed before the CTA releases its shared and tensor memory
+      umma_commit(bar.drain);
+      mbar_wait_drain(bar.drain, 0);
+      if (nu > 0) {
+        mbar_wait_drain(bar.unit_free, parity(nu - 1));
+        mbar_wait_drain(bar.db_full, parity(nu - 1));
+      }
+      if (nh > 0) mbar_wait_drain(bar.tu_full, parity(nh - 1));
+      for (uint32_t n = m > 2u ? m - 2u : 0u; n < m; ++n) mbar_wait_drain(&bar.ring_full[n & 1], parity(n / 2));
       for (uint32_t n = m > (uint32_t)kNY ? m - kNY : 0u; n < m; ++n)
-        mbar_wait(&bar.dy_free[n % kNY], parity(n / kNY), status);
+        mbar_wait_drain(&bar.dy_free[n % kNY], parity(n / kNY));
       for (uint32_t n = na > (uint32_t)kNA ? na - kNA : 0u; n < na; ++n)
-        mbar_wait(&bar.a_free[n % kNA], parity(n / kNA), status);
-      if (nd > 0) mbar_wait(bar.ds_free, parity(nd - 1), status);
-      for (uint32_t n = nh > 2u ? nh - 2u : 0u; n < nh; ++n) mbar_wait(&bar.xt_free[n & 1], parity(n / 2), status);
+        mbar_wait_drain(&bar.a_free[n % kNA], parity(n / kNA));
+      if (nd > 0) mbar_wait_drain(bar.ds_free, parity(nd - 1));
+      for (uint32_t n = nh > 2u ? nh - 2u : 0u; n < nh; ++n) mbar_wait_drain(&bar.xt_free[n & 1], parity(n / 2));
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ transform
@@ -340,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     for (;; ++nu) {
-      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int j = 128 * o.J + jl, row_lo = 128 * o.J + 32 * q, row_hi = row_lo + 31;
@@ -456,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = smem_u32(sm + kSmV), sXT = smem_u32(sm + kSmXT);
     uint32_t nu = 0, nh = 0;
     for (;; ++nu) {
-      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int j = 128 * o.J + jl, t = o.c * pr.Q + j;

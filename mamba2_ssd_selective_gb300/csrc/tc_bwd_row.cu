@@ -46,7 +46,7 @@ constexpr uint32_t kSmV = kSmS + 2 * 16384;     // 2 vector buffers
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], b[256], f[256]}
 constexpr uint32_t kSmVR = kSmD + 2 * 3072;     // 2 x vrow partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVR + 2 * 2048;
-constexpr int kNumBars = 22 + 2 * kNX + 2 * kNA + 4;
+constexpr int kNumBars = 22 + 2 * kNX + 2 * kNA + 4 + 1;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -77,6 +77,7 @@ struct Bars {
   uint64_t *vec_full, *vec_free, *dy_full, *dy_free, *s_full, *s_free;  // [2]
   uint64_t *x_full, *x_free;                          // [kNX]
   uint64_t *a_full, *a_free;                          // [kNA]
+  uint64_t *drain;                                    // the MMA issuer's final commit
   pipe::UnitRing units;
   __device__ Bars(uint64_t *b, int *slot) {
     unit_full = b;
@@ -101,6 +102,7 @@ struct Bars {
     a_free = a_full + kNA;
     units.full = a_free + kNA;
     units.free = units.full + 2;
+    drain = units.free + 2;
     units.slot = slot;
   }
 };
@@ -111,8 +113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_row_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dy,
                       const __grid_constant__ CUtensorMap tm_s, Problem pr, const bf16 *__restrict__ dy,
                       const float *__restrict__ dtv, const float *__restrict__ acs, float *__restrict__ dcp,
-                      float *__restrict__ tok, int HB, int nunits, int *counter, int *status) {
+                      float *__restrict__ tok, int HB, int nunits, int *counter, int *status_word) {
   extern __shared__ uint8_t smem_raw[];
+  const WaitCtl status{status_word, pr.wait_ns};
   uint8_t *sm = tc::aligned_smem(smem_raw);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
   Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar), reinterpret_cast<int *>(tslot + 1));
@@ -122,8 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
 
   if (threadIdx.x == 0) {
-    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.cb_full,   bar.dm_full,  bar.yo_full,
-                        bar.dc_full,   bar.s_full,    bar.s_full + 1, bar.s_free, bar.s_free + 1};
+    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.cb_full, bar.dm_full,  bar.yo_full, bar.dc_full,
+                        bar.s_full,    bar.s_full + 1, bar.s_free, bar.s_free + 1, bar.drain};
     for (uint64_t *b : ones) mbar_init(b, 1);
     mbar_init(bar.cb_used, kTWarps);
     mbar_init(bar.dm_free, kTWarps);
@@ -164,16 +167,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_u);
       prefetch_tmap(&tm_dy);
       prefetch_tmap(&tm_s);
-      uint32_t nu = 0, nh = 0, k = 0, ns = 0;
+      // counts of armed loads per barrier (nua: unit operand sets); once a
+      // wait has failed (ok = false) no further load is issued, stop is
+      // published, and the loads in flight are drained before the CTA ends
+      uint32_t nu = 0, nua = 0, nh = 0, ndy = 0, k = 0, ns = 0;
+      bool ok = true;
       int next = atomicAdd(counter, 1);
       for (;; ++nu) {
-        const int ui = pipe::publish_unit(bar.units, nu, next, nunits, status);
+        const int ui = pipe::publish_unit(bar.units, nu, ok ? next : nunits, nunits);
         if (ui >= nunits) break;
         next = atomicAdd(counter, 1);
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, NB = 128 * (o.I + 1);
         const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N;
-        if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
+        if (nu > 0) ok = mbar_wait(bar.unit_free, parity(nu - 1), status);
+        if (!ok) continue;
         mbar_expect_tx(bar.unit_full, 32768 + 2 * NB * 128);
         for (int kh = 0; kh < 2; ++kh) {
           for (int r = 0; r < 2; ++r)
@@ -181,9 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < NB / 64; ++r)
             tma_load_2d(sm + kSmB + kh * 32768 + r * 8192, &tm_u, bar.unit_full, offB + 64 * kh, row0 + 64 * r);
         }
-        for (int hh = 0; hh < HB; ++hh, ++nh) {
+        ++nua;
+        for (int hh = 0; hh < HB && ok; ++hh) {
           const int h = o.h0 + hh, vb = nh & 1;
-          if (nh >= 2) mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status);
+          if (nh >= 2 && !mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status)) {
+            ok = false;
+            break;
+          }
           uint8_t *vec = sm + kSmV + vb * kVecStride;
           const size_t bh = ((size_t)o.bb * pr.H + h) * pr.L + t0;
           const uint32_t seq_bytes = !has_seq ? 0u : (uint32_t)(o.c > 0 ? (pr.Q + 4) * 4 : pr.Q * 4);
@@ -196,28 +208,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
           }
-          if (nh >= 2) mbar_wait(&bar.dy_free[vb], parity(nh / 2 - 1), status);
+          ++nh;
+          if (ndy >= 2 && !mbar_wait(&bar.dy_free[vb], parity(ndy / 2 - 1), status)) {
+            ok = false;
+            break;
+          }
           mbar_expect_tx(&bar.dy_full[vb], 16384);
           for (int r = 0; r < 2; ++r)
             tma_load_2d(sm + kSmDY + vb * 16384 + r * 8192, &tm_dy, &bar.dy_full[vb], h * pr.P,
                         row0 + 128 * o.I + 64 * r);
+          ++ndy;
           if (o.c > 0) {  // S_in first: a whole head of slack before its use
             const int sb = ns & 1;
-            if (ns >= 2) mbar_wait(&bar.s_free[sb], parity(ns / 2 - 1), status);
+            if (ns >= 2 && !mbar_wait(&bar.s_free[sb], parity(ns / 2 - 1), status)) {
+              ok = false;
+              break;
+            }
             mbar_expect_tx(&bar.s_full[sb], 16384);
             const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
             tma_load_2d(sm + kSmS + sb * 16384, &tm_s, &bar.s_full[sb], 0, srow);
             tma_load_2d(sm + kSmS + sb * 16384 + 8192, &tm_s, &bar.s_full[sb], 64, srow);
             ++ns;
           }
-          for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
+          for (int s = 0; s < 2 * (o.I + 1); ++s) {
             const int slot = k % kNX;
-            if (k >= kNX) mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status);
+            if (k >= kNX && !mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status)) {
+              ok = false;
+              break;
+            }
             mbar_expect_tx(&bar.x_full[slot], 8192);
             tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
+            ++k;
           }
         }
       }
+      // every load issued has landed before the CTA releases its shared memory
+      if (nua > 0) mbar_wait_drain(bar.unit_full, parity(nua - 1));
+      for (uint32_t m = nh > 2u ? nh - 2u : 0u; m < nh; ++m) mbar_wait_drain(&bar.vec_full[m & 1], parity(m / 2));
+      for (uint32_t m = ndy > 2u ? ndy - 2u : 0u; m < ndy; ++m) mbar_wait_drain(&bar.dy_full[m & 1], parity(m / 2));
+      for (uint32_t m = ns > 2u ? ns - 2u : 0u; m < ns; ++m) mbar_wait_drain(&bar.s_full[m & 1], parity(m / 2));
+      for (uint32_t m = k > (uint32_t)kNX ? k - kNX : 0u; m < k; ++m)
+        mbar_wait_drain(&bar.x_full[m % kNX], parity(m / kNX));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -233,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_dc = idesc_bf16(128, 128, false, true);   // W B_s, (em dy) S
       uint32_t nu = 0, nh = 0, k = 0, na = 0, ns = 0;
       for (;; ++nu) {
-        const int ui = pipe::next_unit(bar.units, nu, nunits, status, false);
+        const int ui = pipe::next_unit(bar.units, nu, nunits, false);
         if (ui >= nunits) break;
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int NB = 128 * (o.I + 1), nsl = 2 * (o.I + 1);
@@ -298,14 +329,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bar.dc_full);
         umma_commit(bar.unit_free);
       }
-      // drain: arrivals of commits nobody else waits for
-      if (nu > 0) mbar_wait(bar.unit_free, parity(nu - 1), status);
+      // drain: every MMA issued here has completed and every commit arrival
+      // has landed before the CTA releases its shared and tensor memory
+      umma_commit(bar.drain);
+      mbar_wait_drain(bar.drain, 0);
+      if (nu > 0) {
+        mbar_wait_drain(bar.cb_full, parity(nu - 1));
+        mbar_wait_drain(bar.dc_full, parity(nu - 1));
+        mbar_wait_drain(bar.unit_free, parity(nu - 1));
+      }
+      if (k > 0) mbar_wait_drain(bar.dm_full, parity(k - 1));
+      if (ns > 0) mbar_wait_drain(bar.yo_full, parity(ns - 1));
       for (uint32_t m = k > (uint32_t)kNX ? k - kNX : 0u; m < k; ++m)
-        mbar_wait(&bar.x_free[m % kNX], parity(m / kNX), status);
+        mbar_wait_drain(&bar.x_free[m % kNX], parity(m / kNX));
       for (uint32_t m = na > (uint32_t)kNA ? na - kNA : 0u; m < na; ++m)
-        mbar_wait(&bar.a_free[m % kNA], parity(m / kNA), status);
-      for (uint32_t m = ns > 2u ? ns - 2u : 0u; m < ns; ++m) mbar_wait(&bar.s_free[m & 1], parity(m / 2), status);
-      for (uint32_t m = nh > 2u ? nh - 2u : 0u; m < nh; ++m) mbar_wait(&bar.dy_free[m & 1], parity(m / 2), status);
+        mbar_wait_drain(&bar.a_free[m % kNA], parity(m / kNA));
+      for (uint32_t m = ns > 2u ? ns - 2u : 0u; m < ns; ++m) mbar_wait_drain(&bar.s_free[m & 1], parity(m / 2));
+      for (uint32_t m = nh > 2u ? nh - 2u : 0u; m < nh; ++m) mbar_wait_drain(&bar.dy_free[m & 1], parity(m / 2));
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ transform
@@ -323,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     for (;; ++nu) {
-      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, row_lo = 128 * o.I + 32 * q, row_hi = row_lo + 31, nsl = 2 * (o.I + 1);
@@ -449,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = smem_u32(sm + kSmV), sDY = smem_u32(sm + kSmDY);
     uint32_t nu = 0, nh = 0, ny = 0;
     for (;; ++nu) {
-      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, t = o.c * pr.Q + i;

@@ -55,7 +55,7 @@ struct Engine {
 
   uint8_t *ring;   // 1024-aligned
   uint64_t *bars;  // [0, NSTAGE): stage free;  [NSTAGE]: all issued MMAs done
-  int *status;
+  int *status;     // raised if an MMA completion ever fails to arrive in time
   uint32_t uses[NSTAGE];
   uint32_t done_uses;
 
@@ -71,6 +71,13 @@ struct Engine {
       for (int s = 0; s <= NSTAGE; ++s) mbar_init(&bars[s], 1);
       fence_mbar_init();
     }
+  }
+
+  // The engine's only waits are for completions of MMAs this CTA issued, which
+  // always arrive: they ignore the status word (so a failure elsewhere in the
+  // pass does not corrupt this kernel's results) and are bounded all the same.
+  __device__ __forceinline__ void wait_mma(uint64_t *bar, uint32_t parity) {
+    if (!mbar_wait_drain(bar, parity)) atomicExch(status, 1);
   }
 
   // cp.async of the A tile of the 64-wide k slice [k0, k0+64) into its stage:
@@ -102,7 +109,7 @@ struct Engine {
     Raw cur[PER_B], nxt[PER_B];
     auto issue = [&](int s, Raw(&raw)[PER_B]) {
       const int st = s % NSTAGE, k0 = 64 * s;
-      if (uses[st] > 0) mbar_wait(&bars[st], (uses[st] - 1) & 1, status);
+      if (uses[st] > 0) wait_mma(&bars[st], (uses[st] - 1) & 1);
       stage_A(ring + st * STAGE_BYTES, k0, fal);
       asm volatile("cp.async.commit_group;" ::: "memory");
 #pragma unroll
@@ -151,7 +158,7 @@ struct Engine {
   // Wait until every MMA issued so far has completed (all threads).
   __device__ __forceinline__ void finish() {
     if (threadIdx.x == 0) umma_commit(&bars[NSTAGE]);
-    mbar_wait(&bars[NSTAGE], done_uses & 1, status);
+    wait_mma(&bars[NSTAGE], done_uses & 1);
     done_uses += 1;
     tc_fence_after();
   }

@@ -57,7 +57,7 @@ constexpr uint32_t kVecStride = 3200;            // acs[256] f32 | dt[256] f32 |
 constexpr uint32_t kSmV = kSmS + kNSB * 16384;   // 2 vector buffers
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;   // 2 x {a[256], b[256], f[256]} f32 (decay tables per head)
 constexpr uint32_t kSmBar = kSmD + 2 * 3072;
-constexpr int kNumBars = 9 + 2 * kNA + 2 * kNX + 2 * kNSB + 4 + 4;
+constexpr int kNumBars = 9 + 2 * kNA + 2 * kNX + 2 * kNSB + 4 + 4 + 1;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -88,6 +88,7 @@ struct Bars {
   uint64_t *x_full, *x_free;                 // [kNX]
   uint64_t *s_full, *s_free;                 // [kNSB]
   uint64_t *acc_full, *acc_free;             // [2]
+  uint64_t *drain;                           // the MMA issuer's final commit
   pipe::UnitRing units;
   __device__ Bars(uint64_t *b, int *slot) {
     unit_full = b;
@@ -107,6 +108,7 @@ struct Bars {
     acc_free = acc_full + 2;
     units.full = acc_free + 2;
     units.free = units.full + 2;
+    drain = units.free + 2;
     units.slot = slot;
   }
 };
@@ -120,8 +122,9 @@ constexpr int kTransformWarps = 16, kEpilogueWarps = 4;
 __global__ void __launch_bounds__(kThreads, 1)
     tc_out_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_s, Problem pr,
                   const bf16 *__restrict__ u, const float *__restrict__ dtv, const float *__restrict__ acs,
-                  bf16 *__restrict__ y, int HB, int nunits, int *counter, int *status) {
+                  bf16 *__restrict__ y, int HB, int nunits, int *counter, int *status_word) {
   extern __shared__ uint8_t smem_raw[];
+  const WaitCtl status{status_word, pr.wait_ns};
   uint8_t *sm = tc::aligned_smem(smem_raw);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kSmBar + kNumBars * 8);
   Bars bar(reinterpret_cast<uint64_t *>(sm + kSmBar), reinterpret_cast<int *>(tslot + 1));
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.c_free, 1);
     mbar_init(bar.cb_full, 1);
     mbar_init(bar.cb_used, kTransformWarps);
+    mbar_init(bar.drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.vec_full[i], 1);
       mbar_init(&bar.vec_free[i], kTransformWarps + kEpilogueWarps);
@@ -173,19 +177,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_u);
       prefetch_tmap(&tm_s);
-      uint32_t nu = 0, nh = 0, ns = 0, k = 0;
+      // counts of armed loads per barrier (nua: unit operand sets); once a
+      // wait has failed (ok = false) no further load is issued, stop is
+      // published, and the loads in flight are drained before the CTA ends
+      uint32_t nu = 0, nua = 0, nh = 0, ns = 0, k = 0;
+      bool ok = true;
       int next = atomicAdd(counter, 1);
       for (;; ++nu) {
-        const int ui = pipe::publish_unit(bar.units, nu, next, nunits, status);
+        const int ui = pipe::publish_unit(bar.units, nu, ok ? next : nunits, nunits);
         if (ui >= nunits) break;
         next = atomicAdd(counter, 1);
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int g = o.h0 / pr.hpg, t0 = o.c * pr.Q, row0 = o.bb * pr.L + t0, NB = 128 * (o.I + 1);
         const int offB = HP + g * pr.N, offC = HP + pr.G * pr.N + g * pr.N;
-        if (nu > 0) {
-          mbar_wait(bar.b_free, parity(nu - 1), status);
-          mbar_wait(bar.c_free, parity(nu - 1), status);
-        }
+        if (nu > 0) ok = mbar_wait(bar.b_free, parity(nu - 1), status) && mbar_wait(bar.c_free, parity(nu - 1), status);
+        if (!ok) continue;
         mbar_expect_tx(bar.unit_full, 2 * 16384 + 2 * NB * 128);
         for (int kh = 0; kh < 2; ++kh) {
           for (int r = 0; r < 2; ++r)
@@ -193,9 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < NB / 64; ++r)
             tma_load_2d(sm + kSmB + kh * 32768 + r * 8192, &tm_u, bar.unit_full, offB + 64 * kh, row0 + 64 * r);
         }
-        for (int hh = 0; hh < HB; ++hh, ++nh) {
+        ++nua;
+        for (int hh = 0; hh < HB && ok; ++hh) {
           const int h = o.h0 + hh, vb = nh & 1;
-          if (nh >= 2) mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status);
+          if (nh >= 2 && !mbar_wait(&bar.vec_free[vb], parity(nh / 2 - 1), status)) {
+            ok = false;
+            break;
+          }
           uint8_t *vec = sm + kSmV + vb * kVecStride;
           const size_t bh = ((size_t)o.bb * pr.H + h) * pr.L + t0;
           const uint32_t seq_bytes = !has_seq ? 0u : (uint32_t)(o.c > 0 ? (pr.Q + 4) * 4 : pr.Q * 4);
@@ -208,23 +218,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
           }
+          ++nh;
           if (o.c > 0) {
             const int sb = ns % kNSB;
-            if (ns >= kNSB) mbar_wait(&bar.s_free[sb], parity(ns / kNSB - 1), status);
+            if (ns >= kNSB && !mbar_wait(&bar.s_free[sb], parity(ns / kNSB - 1), status)) {
+              ok = false;
+              break;
+            }
             mbar_expect_tx(&bar.s_full[sb], 16384);
             const int srow = (int)((((size_t)o.bb * pr.nc + o.c) * pr.H + h) * pr.P);
             tma_load_2d(sm + kSmS + sb * 16384, &tm_s, &bar.s_full[sb], 0, srow);
             tma_load_2d(sm + kSmS + sb * 16384 + 8192, &tm_s, &bar.s_full[sb], 64, srow);
             ++ns;
           }
-          for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
+          for (int s = 0; s < 2 * (o.I + 1); ++s) {
             const int slot = k % kNX;
-            if (k >= kNX) mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status);
+            if (k >= kNX && !mbar_wait(&bar.x_free[slot], parity(k / kNX - 1), status)) {
+              ok = false;
+              break;
+            }
             mbar_expect_tx(&bar.x_full[slot], 8192);
             tma_load_2d(sm + kSmX + slot * 8192, &tm_u, &bar.x_full[slot], h * pr.P, row0 + 64 * s);
+            ++k;
           }
         }
       }
+      // every load issued has landed before the CTA releases its shared memory
+      if (nua > 0) mbar_wait_drain(bar.unit_full, parity(nua - 1));
+      for (uint32_t m = nh > 2u ? nh - 2u : 0u; m < nh; ++m) mbar_wait_drain(&bar.vec_full[m & 1], parity(m / 2));
+      for (uint32_t m = ns > (uint32_t)kNSB ? ns - kNSB : 0u; m < ns; ++m)
+        mbar_wait_drain(&bar.s_full[m % kNSB], parity(m / kNSB));
+      for (uint32_t m = k > (uint32_t)kNX ? k - kNX : 0u; m < k; ++m)
+        mbar_wait_drain(&bar.x_full[m % kNX], parity(m / kNX));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -237,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_off = idesc_bf16(128, 64, false, false);
       uint32_t nu = 0, nh = 0, ns = 0, k = 0;
       for (;; ++nu) {
-        const int ui = pipe::next_unit(bar.units, nu, nunits, status, false);
+        const int ui = pipe::next_unit(bar.units, nu, nunits, false);
         if (ui >= nunits) break;
         const Unit o = unit_of(pr, NTI, nhb, HB, ui);
         const int NB = 128 * (o.I + 1);
@@ -278,18 +303,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(bar.c_free);
       }
-      // drain: the arrivals of commits no other role waits for must land
-      // before the CTA's shared memory is released
+      // drain: every MMA issued here has completed and every commit arrival
+      // has landed before the CTA releases its shared and tensor memory
+      umma_commit(bar.drain);
+      mbar_wait_drain(bar.drain, 0);
       if (nu > 0) {
-        mbar_wait(bar.b_free, parity(nu - 1), status);
-        mbar_wait(bar.c_free, parity(nu - 1), status);
+        mbar_wait_drain(bar.cb_full, parity(nu - 1));
+        mbar_wait_drain(bar.b_free, parity(nu - 1));
+        mbar_wait_drain(bar.c_free, parity(nu - 1));
       }
+      for (uint32_t m = nh > 2u ? nh - 2u : 0u; m < nh; ++m) mbar_wait_drain(&bar.acc_full[m & 1], parity(m / 2));
       for (uint32_t m = k > (uint32_t)kNA ? k - kNA : 0u; m < k; ++m)
-        mbar_wait(&bar.a_free[m % kNA], parity(m / kNA), status);
+        mbar_wait_drain(&bar.a_free[m % kNA], parity(m / kNA));
       for (uint32_t m = k > (uint32_t)kNX ? k - kNX : 0u; m < k; ++m)
-        mbar_wait(&bar.x_free[m % kNX], parity(m / kNX), status);
+        mbar_wait_drain(&bar.x_free[m % kNX], parity(m / kNX));
       for (uint32_t m = ns > (uint32_t)kNSB ? ns - kNSB : 0u; m < ns; ++m)
-        mbar_wait(&bar.s_free[m % kNSB], parity(m / kNSB), status);
+        mbar_wait_drain(&bar.s_free[m % kNSB], parity(m / kNSB));
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ transform
@@ -298,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float kLog2e = 1.4426950408889634f;
     uint32_t nu = 0, nh = 0, k = 0;
     for (;; ++nu) {
-      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, row_lo = 128 * o.I + 32 * q, row_hi = row_lo + 31;
@@ -410,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = smem_u32(sm + kSmV);
     uint32_t nh = 0;
     for (uint32_t nu = 0;; ++nu) {
-      const int ui = pipe::next_unit(bar.units, nu, nunits, status, true);
+      const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, t = o.c * pr.Q + i;

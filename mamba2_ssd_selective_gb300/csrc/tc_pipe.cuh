@@ -85,26 +85,32 @@ __device__ __forceinline__ uint4 lds_sw128(uint32_t tile, int r, int c) {
 // Dynamic work distribution for the persistent kernels: the producer lane
 // claims the next work unit from a global counter and hands it to the other
 // roles through a two-entry ring in shared memory (full[b]: count 1; free[b]:
-// one arrival per consumer warp or thread).  A role whose wait gave up sees
-// `stop` instead of a unit, so a broken pipeline ends without stray indices.
+// one arrival per consumer warp or thread).
+//
+// Both sides wait on this ring with mbar_wait_drain, which does not give up
+// when the status word is raised: every consumer reads every published value,
+// in order, so all warps of a role work through the same units and reach
+// their named barriers the same number of times, even on a failing pass.  The
+// producer always publishes: after one of its own waits has failed it
+// publishes `stop`, and the consumers end together.
 struct UnitRing {
   uint64_t *full, *free;  // [2] each
   int *slot;              // [2]
 };
 // Producer lane: publish unit `u` (claimed earlier with atomicAdd, so the
 // atomic's latency hides behind the previous unit's loads) as the n-th unit.
-__device__ __forceinline__ int publish_unit(const UnitRing &r, uint32_t n, int u, int stop, int *status) {
+__device__ __forceinline__ int publish_unit(const UnitRing &r, uint32_t n, int u, int stop) {
   const int b = n & 1;
-  if (n >= 2 && !mbar_wait(&r.free[b], parity(n / 2 - 1), status)) u = stop;
+  if (n >= 2 && !mbar_wait_drain(&r.free[b], parity(n / 2 - 1))) u = stop;
   if (u > stop) u = stop;
   *reinterpret_cast<volatile int *>(&r.slot[b]) = u;
   mbar_arrive(&r.full[b]);
   return u;
 }
 // consumers: warp_level = one arrival per warp (all lanes call), else one per thread
-__device__ __forceinline__ int next_unit(const UnitRing &r, uint32_t n, int stop, int *status, bool warp_level) {
+__device__ __forceinline__ int next_unit(const UnitRing &r, uint32_t n, int stop, bool warp_level) {
   const int b = n & 1;
-  const bool ok = mbar_wait(&r.full[b], parity(n / 2), status);
+  const bool ok = mbar_wait_drain(&r.full[b], parity(n / 2));
   const int u = ok ? *reinterpret_cast<volatile int *>(&r.slot[b]) : stop;
   if (warp_level)
     warp_arrive(&r.free[b]);

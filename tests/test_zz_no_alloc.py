@@ -2,9 +2,11 @@
 memory (host frameworks that own every allocation, latency-bound loops where a
 cudaMalloc would synchronise the device).  Its scratch is the library's fixed
 device array, so the test checks, through the C ABI, that two calls in a row
-(on different inputs, so stale scratch contents would show) give what the
-workspace-taking ssd_forward gives, and that a problem too large for the array
-is rejected before launch.  Collected last on purpose."""
+(on different inputs, so stale scratch contents would show) give exactly what
+the workspace-taking ssd_forward gives (the same kernels on the same inputs),
+that the first call agrees with the fp64 oracle, that the array's status word
+reads ok afterwards, and that a problem too large for the array is rejected
+before launch.  Collected last on purpose."""
 from __future__ import annotations
 
 import pytest
@@ -12,7 +14,7 @@ import torch
 
 import mamba2_ssd_selective_gb300 as ssd
 from mamba2_ssd_selective_gb300.inputs import SsdShape, make_inputs
-from tests.gpu_util import TOL, np_, rel, to_dev
+from tests.gpu_util import TOL, compare_forward, np_, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -29,19 +31,23 @@ def _built():
     ssd.load()
 
 
-def test_static_scratch_forward_matches_workspace_forward():
+def test_static_scratch_forward_matches_workspace_forward(oracle_lib):
     dims = ssd.make_dims(SHAPE, "bf16")
     assert ssd.ssd_workspace_size(dims, False) <= ssd.STATIC_SCRATCH_BYTES
     runner = ssd.SsdRunner(SHAPE, "bf16")
-    for seed in (31, 32):  # two calls in a row on different inputs
-        t = to_dev(make_inputs(SHAPE, seed, "bf16", seq_lengths=[300, 2, 722]))
+    for n, seed in enumerate((31, 32)):  # two calls in a row on different inputs
+        inp = make_inputs(SHAPE, seed, "bf16", seq_lengths=[300, 2, 722])
+        t = to_dev(inp)
         y_ref, fin_ref, seg_ref = runner.forward(t)
         y, fin, seg = runner.alloc_outputs()
         ssd.ssd_forward_static(dims, runner.inputs(t), y, fin, seg)
         torch.cuda.synchronize()
-        assert rel(np_(y), np_(y_ref)) <= TOL["bf16"]
-        assert rel(np_(fin), np_(fin_ref)) <= TOL["bf16"]
-        assert rel(np_(seg), np_(seg_ref)) <= TOL["bf16"]
+        assert torch.equal(y, y_ref) and torch.equal(fin, fin_ref) and torch.equal(seg, seg_ref)
+        assert ssd.ssd_device_status(None) == 0
+        if n == 0:
+            got = {"y": np_(y).reshape(1, SHAPE.seqlen, SHAPE.nheads, SHAPE.headdim), "final_state": np_(fin),
+                   "seg_in": np_(seg)}
+            compare_forward(got, oracle_lib.forward(inp, SHAPE), TOL["bf16"])
 
 
 def test_static_scratch_rejects_oversized_problem():
