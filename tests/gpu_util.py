@@ -11,6 +11,18 @@ import mamba2_ssd_selective_gb300 as ssd
 
 TOL = {"f32": 1e-4, "bf16": 1e-2}
 
+# ddt_bias = sum over every token of ddt_raw.  In these bf16 parity cases (few
+# tokens per head) the sum is only 0.26-0.40 times the root-sum-square of its
+# terms, and rounding the post-conv activations to bf16, with every other step
+# exact, already moves it by the relative error listed (the floor, pinned by
+# tests/test_bf16_rounding_floor.py).  There the plain relative-L2 bound is
+# max(1e-2, 1.5 x floor); everywhere else it is 1e-2 like every other gradient.
+DDT_BIAS_FLOOR = {"packed-2048-q256": 1.42e-2, "packed-2x1024-q128": 1.45e-2, "forget-1024": 7.69e-3}
+
+
+def ddt_bias_tol(case: str | None, tol: float) -> float:
+    return max(tol, 1.5 * DDT_BIAS_FLOOR[case]) if case in DDT_BIAS_FLOOR else tol
+
 
 def rel(a, b) -> float:
     a = np.asarray(a, dtype=np.float64)
@@ -62,10 +74,13 @@ def compare_forward(got: dict, ref: dict, tol: float, heads=None, rows=None):
     return errs
 
 
-REPORT_ONLY = {"ddt_bias_rel"}
+# reported, not asserted: ddt_bias's error against the root-sum-square of its
+# per-token terms (the scale that per-term rounding produces), beside the plain
+# relative L2 that is asserted like every other gradient's
+REPORT_ONLY = {"ddt_bias_rss"}
 
 
-def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=None):
+def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=None, floor_case=None):
     rows = list(range(shape.batch)) if rows is None else rows
     h0, h1 = heads if heads else (0, shape.nheads)
     ch = ref["channels"]
@@ -77,15 +92,13 @@ def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=N
         errs.update({
             "dconv_w": rel(got["dconv_w"][ch], ref["dconv_w"]),
             "dconv_b": rel(got["dconv_b"][ch], ref["dconv_b"]) if np.any(ref["dconv_b"]) else 0.0,
-            # a sum over b*L tokens with heavy cancellation: its error is judged
-            # against the root-sum-square of its per-token terms (the scale that
-            # per-term rounding produces), not against the cancelled sum itself
-            "ddt_bias": float(np.linalg.norm(got["ddt_bias"][h0:h1] - ref["ddt_bias"])
-                              / np.linalg.norm(np.sqrt(np.sum(ref["ddt_raw"] ** 2, axis=(0, 1))))),
-            "ddt_bias_rel": rel(got["ddt_bias"][h0:h1], ref["ddt_bias"]),
+            "ddt_bias": rel(got["ddt_bias"][h0:h1], ref["ddt_bias"]),
+            "ddt_bias_rss": float(np.linalg.norm(got["ddt_bias"][h0:h1] - ref["ddt_bias"])
+                                  / np.linalg.norm(np.sqrt(np.sum(ref["ddt_raw"] ** 2, axis=(0, 1))))),
             "dA_log": rel(got["dA_log"][h0:h1], ref["dA_log"]),
             "dD": rel(got["dD"][h0:h1], ref["dD"]),
         })
     for k, e in errs.items():
-        assert k in REPORT_ONLY or e <= tol, (k, e, errs)
+        bound = ddt_bias_tol(floor_case, tol) if k == "ddt_bias" else tol
+        assert k in REPORT_ONLY or e <= bound, (k, e, bound, errs)
     return errs

@@ -69,3 +69,50 @@ def quadratic_ssd(inp: dict, shape) -> tuple[np.ndarray, np.ndarray]:
             w_last = Lm[L - 1]  # weights of every token in the final state
             fin[r, h] = (w_last[:, None] * Xs).T @ uB[r, :, g]
     return y, fin
+
+
+def ssd_dt_bias_grad_f64(inp: dict, shape, round_u: bool) -> tuple[np.ndarray, np.ndarray]:
+    """(ddt_bias, ddt_raw) of L = <dy, y> + <dfinal, final_state> by float64
+    autograd through the quadratic form of the whole row, conv + SiLU per packed
+    sequence.  With round_u the
+    post-conv activations u are rounded to bf16 in the forward (the gradient
+    passes straight through the rounding): everything else stays exact, so the
+    difference to round_u=False is the error that storing u in bf16 alone puts
+    into the dt gradients of any implementation that does so."""
+    b, L, H, P, N, G = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    Cd, HP, GN = shape.conv_dim, H * P, G * N
+    f64 = torch.float64
+    xBC = inp["xBC"].to(f64)
+    w = inp["conv_w"].to(f64)[:, None, :]
+    dt_raw = inp["dt_raw"].to(f64).clone().requires_grad_(True)
+    bias = inp["dt_bias"].to(f64).clone().requires_grad_(True)
+    A = -torch.exp(inp["A_log"].to(f64))
+    D = inp["D"].to(f64)
+    dy = inp["dy"].to(f64)
+    dfin = inp["dfinal"].to(f64)
+    loss = torch.zeros((), dtype=f64)
+    for r in range(b):
+        si = None if inp.get("seq_idx") is None else inp["seq_idx"][r].numpy()
+        cuts = [0] + ([t for t in range(1, L) if si[t] != si[t - 1]] if si is not None else []) + [L]
+        v = torch.empty(L, Cd, dtype=f64)
+        for s0, s1 in zip(cuts[:-1], cuts[1:]):
+            seg = xBC[r, s0:s1].T[None]
+            v[s0:s1] = torch.nn.functional.conv1d(seg, w, inp["conv_b"].to(f64), padding=3, groups=Cd)[0, :, :s1 - s0].T
+        u = v * torch.sigmoid(v)
+        if round_u:
+            u = u + (u.to(torch.bfloat16).to(f64) - u).detach()
+        same = torch.ones(L, L, dtype=torch.bool) if si is None else torch.from_numpy(si[:, None] == si[None, :])
+        mask = torch.tril(torch.ones(L, L, dtype=torch.bool)) & same
+        dt = torch.nn.functional.softplus(dt_raw[r] + bias)
+        for h in range(H):
+            g = h // (H // G)
+            x, Bm, Cm = u[:, h * P:(h + 1) * P], u[:, HP + g * N:HP + (g + 1) * N], u[:, HP + GN + g * N:HP + GN + (g + 1) * N]
+            cs = torch.cumsum(dt[:, h] * A[h], 0)
+            Lm = torch.exp(torch.where(mask, cs[:, None] - cs[None, :], torch.full((L, L), -1e300, dtype=f64)))
+            y = ((Cm @ Bm.T) * Lm * dt[None, :, h]) @ x + D[h] * x
+            loss = loss + (y * dy[r, :, h * P:(h + 1) * P]).sum()
+            wl = Lm[L - 1] * dt[:, h]  # the last token's weights (its own sequence only)
+            fin = (x * wl[:, None]).T @ Bm  # state after the row's last token, P x N
+            loss = loss + (fin * dfin[r, h]).sum()
+    loss.backward()
+    return bias.grad.numpy().copy(), dt_raw.grad.numpy().copy()
