@@ -8,6 +8,11 @@ correction/output, and the backward mirror) over one batch of the
 chunk 256, 8 segments, bf16 activations, seeded synthetic inputs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--segments S]
+
+Other workloads: "mamba2-1b-fwd" times the forward alone (same shape),
+"long-131k" (b1 L131072 G8, --segments 1..16) and "packed-32k" (packed
+sequences) time forward+backward.
 
 Prints ONE JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own
 batch (weak scaling, no data-path collective); the timed region is bracketed by
@@ -197,6 +202,57 @@ def kernel_work(shape, dtype: str) -> dict:
     return w
 
 
+def method_work(shape, dtype: str) -> dict:
+    """The method's own work per token, independent of how this library splits it
+    into kernels: every input read and every output written once per pass
+    (forward: xBC, dt in, y out; backward: xBC, dt, dy in, dxBC, ddt out), and
+    the chunked algorithm's flops counting only the causal half of the Q x Q
+    products, with CB and the dB/dC diagonal products once per group and dM
+    once.  Also the share of those flops each tensor-core kernel carries."""
+    H, P, N, G, Q = shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.chunk
+    eb = 2 if dtype == "bf16" else 4
+    Cd, HP = shape.conv_dim, H * P
+    gqn, hpq, hpn2 = G * Q * N, H * P * Q, 2 * H * P * N  # causal CB, causal Q x Q x P, one P x N contraction
+    per_kernel = {
+        "tc_chunk_out": gqn + hpq + hpn2,           # CB, (CB o L o dt) X, C S_in^T
+        "tc_chunk_state": hpn2,                     # chunk states (forward, and the backward's recompute)
+        "tc_chunk_z": hpn2,                         # Z = C^T (em dy)
+        "tc_bwd_row": 2 * gqn + hpq + hpn2,         # CB, dM, (sum_h W) B, (em dy) S_in
+        "tc_bwd_col": gqn + hpq + 2 * hpn2,         # M^T dy, (sum_h W)^T C, B dS^T, (wdt x) dS
+    }
+    return {
+        "fwd_bytes": (Cd + H + HP) * eb, "bwd_bytes": (Cd + H + HP) * eb + (Cd + H) * eb,
+        "fwd_flop": gqn + hpq + 2 * hpn2, "bwd_flop": 3 * gqn + 2 * hpq + 5 * hpn2,
+        "per_kernel_flop_per_token": per_kernel,
+    }
+
+
+def method_roofline(kt: list, shape, dtype: str, ms_per_step: float, peaks: dict, backward: bool) -> dict:
+    """The step against the method's own minimum: its bytes at the measured HBM
+    copy bandwidth and its causal flops at the sustained bf16 tensor peak.  The
+    step floor is the larger of the two times; frac = floor / measured step."""
+    m = method_work(shape, dtype)
+    tok = shape.tokens
+    bpt = m["fwd_bytes"] + (m["bwd_bytes"] if backward else 0)
+    fpt = m["fwd_flop"] + (m["bwd_flop"] if backward else 0)
+    hbm, tpk = peaks["hbm_gbs"], peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    t_b, t_f = bpt * tok / (hbm * 1e9), fpt * tok / (tpk * 1e12)
+    floor_ms = max(t_b, t_f) * 1e3
+    out = {"bytes_per_token": bpt, "flop_per_token": fpt, "bytes_per_step": bpt * tok, "flop_per_step": fpt * tok,
+           "bound": "hbm" if t_b >= t_f else "tensor", "floor_ms": round(floor_ms, 4),
+           "frac": round(floor_ms / ms_per_step, 4)}
+    tc = [r for r in kt if r[0] in m["per_kernel_flop_per_token"]]
+    if tc:
+        name, launches, total_ms = max(tc, key=lambda r: r[2] / max(r[1], 1))
+        avg_s = total_ms / 1e3 / max(launches, 1)
+        f = m["per_kernel_flop_per_token"][name] * tok  # every launch covers all tokens
+        ach = f / avg_s / 1e12
+        out["dominant_contraction"] = {"kernel": name, "method_flop_per_launch": f, "avg_launch_ms": round(avg_s * 1e3, 4),
+                                       "achieved_tflops": round(ach, 2), "peak_tflops": tpk,
+                                       "frac_compute": round(ach / tpk, 4)}
+    return out
+
+
 def roofline_for(kt: list, shape, dtype: str, peaks: dict, peak_src: str, clocks: dict | None) -> dict:
     """Roofline of the kernel with the largest share of the step.  Kernels are
     timed inside the step, so the tensor peak is the sustained one."""
@@ -226,10 +282,10 @@ def roofline_for(kt: list, shape, dtype: str, peaks: dict, peak_src: str, clocks
             "frac_hbm": round(frac_m, 4), "frac_compute": None if frac_c is None else round(frac_c, 4)}
 
 
-def step_totals(kt: list, shape, dtype: str, ms_per_step: float, peaks: dict) -> dict:
-    """Whole-step algorithmic work against the peaks (all kernels, per step)."""
+def step_totals(kt: list, shape, dtype: str, ms_per_step: float, peaks: dict, steps: int) -> dict:
+    """Whole-step algorithmic work of this decomposition against the peaks
+    (all kernels; kt covers `steps` steps)."""
     work = kernel_work(shape, dtype)
-    steps = max(r[1] for r in kt if r[0] in ("local_rev", "chunk_dt", "conv_bwd")) if kt else 1
     flops = sum(work.get(n, ("mem", 0, 0))[1] * c for n, c, _ in kt) / steps
     nbytes = sum(work.get(n, ("mem", 0, 0))[2] * c for n, c, _ in kt) / steps
     s = ms_per_step / 1e3
@@ -266,27 +322,35 @@ def committed_traffic(kernel: str, shape):
 
 # ---------------------------------------------------------------- CPU oracle timings
 
-def oracle_sample(inp: dict, shape, heads: tuple, nthreads: int = 0) -> float:
+def oracle_sample(inp: dict, shape, heads: tuple, nthreads: int = 0, backward: bool = True) -> float:
     import oracle
 
     t0 = time.perf_counter()
     oracle.forward(inp, shape, heads=heads, rows=[0], nthreads=nthreads)
-    oracle.backward(inp, shape, heads=heads, rows=[0], nthreads=nthreads)
+    if backward:
+        oracle.backward(inp, shape, heads=heads, rows=[0], nthreads=nthreads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(inp: dict, shape) -> dict:
+def cpu_baseline(inp: dict, shape, backward: bool) -> dict:
     import oracle
 
     oracle.build()
     cores = oracle.default_threads()
-    dt = oracle_sample(inp, shape, (0, shape.nheads))
-    return {"value": round(shape.seqlen / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"fp64 C oracle, fwd (S={shape.n_segments}) + bwd of batch row 0 (all {shape.nheads} heads, "
-                      f"{shape.seqlen} tokens) of the same workload: {dt:.1f} s"}
+    what = "fwd + bwd" if backward else "fwd"
+    dt = oracle_sample(inp, shape, (0, shape.nheads), backward=backward)
+    out = {"value": round(shape.seqlen / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"fp64 C oracle, {what} (S={shape.n_segments}) of batch row 0 (all {shape.nheads} heads, "
+                     f"{shape.seqlen} tokens) of the same workload, {cores} threads: {dt:.1f} s"}
+    if not backward:  # the forward on one host core as well
+        dt1 = oracle_sample(inp, shape, (0, shape.nheads), nthreads=1, backward=False)
+        out["one_thread"] = {"value": round(shape.seqlen / dt1, 2), "unit": UNIT, "cores": 1, "seconds": round(dt1, 2)}
+    return out
 
 
-def run_reference(args, shape, dtype, seed):
+def run_reference(args, shape, dtype, seed, backward: bool):
+    """The oracle as it stands, on the host cores: each step is batch row 0 of
+    the workload (all heads), the same sample as the line's cpu_baseline."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
@@ -295,41 +359,49 @@ def run_reference(args, shape, dtype, seed):
     oracle.build()
     cores = oracle.default_threads()
     inp = make_inputs(shape, seed, dtype)
-    heads = (0, min(8, shape.nheads))
-    frac = (heads[1] - heads[0]) / shape.nheads
+    heads = (0, shape.nheads)
     for _ in range(args.warmup):
-        oracle_sample(inp, shape, heads)
-    times = [oracle_sample(inp, shape, heads) for _ in range(args.steps)]
+        oracle_sample(inp, shape, heads, backward=backward)
+    times = [oracle_sample(inp, shape, heads, backward=backward) for _ in range(args.steps)]
     total = sum(times)
-    tok_per_step = shape.seqlen * frac
-    value = tok_per_step * args.steps / total
+    value = shape.seqlen * args.steps / total
+    what = "fwd + bwd" if backward else "fwd"
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "impl": "reference", "metric": metric_for(args, backward), "value": round(value, 2), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3),
+        "ms_per_step_p50": round(statistics.median(times) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(shape, dtype, seed),
+        "config": config_dict(args, shape, dtype, seed),
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"each step: fp64 C oracle fwd+bwd of batch row 0, heads {heads[0]}-{heads[1] - 1} "
-                                   f"of {shape.nheads}, {shape.seqlen} tokens; value counts "
-                                   f"{tok_per_step:.0f} token-equivalents per step"},
+                         "sample": f"each step: fp64 C oracle {what} of batch row 0 (all {shape.nheads} heads, "
+                                   f"{shape.seqlen} tokens) of the workload, {cores} threads"},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def config_dict(shape, dtype, seed) -> dict:
-    return {"workload": DEFAULT_WORKLOAD if shape == WORKLOADS[DEFAULT_WORKLOAD][0] else "custom",
-            "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads, "headdim": shape.headdim,
-            "dstate": shape.dstate, "ngroups": shape.ngroups, "d_conv": shape.d_conv, "chunk": shape.chunk,
-            "n_segments": shape.n_segments, "activations": dtype, "seed": seed,
-            "l2": f"inputs larger than L2 (xBC {shape.tokens * shape.conv_dim * (2 if dtype == 'bf16' else 4) / 1e6:.0f}"
-                  f" MB, dy {shape.tokens * shape.nheads * shape.headdim * (2 if dtype == 'bf16' else 4) / 1e6:.0f}"
+def metric_for(args, backward: bool) -> str:
+    if args.workload == DEFAULT_WORKLOAD and args.segments is None and args.batch is None:
+        return METRIC
+    what = "fwd+bwd" if backward else "fwd"
+    return f"SSD {what} tokens/s on 1 GB300 ({args.workload}, bf16) + % of tensor/HBM roofline"
+
+
+def config_dict(args, shape, dtype, seed) -> dict:
+    eb = 2 if dtype == "bf16" else 4
+    return {"workload": args.workload, "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads,
+            "headdim": shape.headdim, "dstate": shape.dstate, "ngroups": shape.ngroups, "d_conv": shape.d_conv,
+            "chunk": shape.chunk, "n_segments": shape.n_segments, "packed": shape.packed, "activations": dtype,
+            "seed": seed,
+            "l2": f"inputs larger than L2 (xBC {shape.tokens * shape.conv_dim * eb / 1e6:.0f}"
+                  f" MB, dy {shape.tokens * shape.nheads * shape.headdim * eb / 1e6:.0f}"
                   f" MB per step; L2 is 129 MB)"}
 
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, shape, dtype, seed):
+def run_ours(args, shape, dtype, seed, backward: bool):
     import mamba2_ssd_selective_gb300 as ssd
     from mamba2_ssd_selective_gb300.build import build
 
@@ -352,24 +424,27 @@ def run_ours(args, shape, dtype, seed):
 
     def step():
         runner.forward(t, out=(y, fin, seg))
-        runner.backward(t, t["dy"], dfinal, seg, grads=grads)
+        if backward:
+            runner.backward(t, t["dy"], dfinal, seg, grads=grads)
 
     sampler = ClockSampler(local)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     sampler.start()
-    # timed region 1: throughput
+    # timed region 1: throughput over exactly K steps, with an event between
+    # steps for the per-step median
     barrier(ws)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for k in range(args.steps):
         step()
-    e1.record(stream)
+        ev[k + 1].record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    elapsed = e0.elapsed_time(e1) / 1e3
+    elapsed = ev[0].elapsed_time(ev[-1]) / 1e3
+    step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
     # timed region 2: the same steps with per-kernel events on the launch stream
     ssd.ssd_profile_begin()
     for _ in range(args.steps):
@@ -379,10 +454,12 @@ def run_ours(args, shape, dtype, seed):
     # end to end through the public API with host buffers (pinned)
     e2e = None
     if not args.no_e2e:
-        host_in = {k: inp[k].pin_memory() for k in ("xBC", "dt_raw", "dy")}
+        in_keys = ("xBC", "dt_raw", "dy") if backward else ("xBC", "dt_raw")
+        host_in = {k: inp[k].pin_memory() for k in in_keys}
         host_out = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
                     "final_state": torch.empty(fin.shape, dtype=fin.dtype).pin_memory()}
-        host_out.update({k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()})
+        if backward:
+            host_out.update({k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()})
         h2d = sum(v.numel() * v.element_size() for v in host_in.values())
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
@@ -414,14 +491,16 @@ def run_ours(args, shape, dtype, seed):
                 if k >= 2:
                     stream.wait_event(ev_out[sl])  # step k-2's results were read back
                 runner.forward(ti, out=(yo, fo, so))
-                runner.backward(ti, ti["dy"], dfinal, so, grads=go)
+                if backward:
+                    runner.backward(ti, ti["dy"], dfinal, so, grads=go)
                 ev_done[sl].record(stream)
                 with torch.cuda.stream(down):
                     down.wait_event(ev_done[sl])
                     host_out["y"].copy_(yo, non_blocking=True)
                     host_out["final_state"].copy_(fo, non_blocking=True)
-                    for key, v in go.items():
-                        host_out[key].copy_(v, non_blocking=True)
+                    if backward:
+                        for key, v in go.items():
+                            host_out[key].copy_(v, non_blocking=True)
                     ev_out[sl].record(down)
             stream.wait_event(ev_out[(n - 1) % 2])  # the last download is inside the region
 
@@ -441,31 +520,35 @@ def run_ours(args, shape, dtype, seed):
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
+    ms = el / args.steps * 1e3
     line = {
-        "metric": METRIC, "value": round(units / el, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "metric": metric_for(args, backward), "value": round(units / el, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "ms_per_step_p50": round(statistics.median(step_ms), 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-        "config": config_dict(shape, dtype, seed),
+        "config": config_dict(args, shape, dtype, seed),
         "roofline": roofline_for(kt, shape, dtype, peaks, peak_src, clocks),
-        "step_roofline": step_totals(kt, shape, dtype, el / args.steps * 1e3, peaks),
+        "method_roofline": method_roofline(kt, shape, dtype, ms, peaks, backward),
+        "step_roofline": step_totals(kt, shape, dtype, ms, peaks, args.steps),
         "e2e": e2e,
         "gpu_launches": int(sum(r[1] for r in kt)),
         "clocks": clocks,
-        "kernels": [{"name": n, "launches": c, "ms_per_launch": round(ms / max(c, 1), 4),
-                     "share": round(ms / max(sum(r[2] for r in kt), 1e-9), 4)} for n, c, ms in kt],
+        "kernels": [{"name": n, "launches": c, "ms_per_launch": round(ms_ / max(c, 1), 4),
+                     "share": round(ms_ / max(sum(r[2] for r in kt), 1e-9), 4)} for n, c, ms_ in kt],
     }
     if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, shape)
+        line["cpu_baseline"] = cpu_baseline(inp, shape, backward)
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--segments", type=int, default=None, help="override the workload's segment count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")
@@ -474,10 +557,13 @@ def main():
     shape, dtype, seed = WORKLOADS[args.workload]
     if args.batch is not None:
         shape = shape.with_(batch=args.batch)
+    if args.segments is not None:
+        shape = shape.with_(n_segments=args.segments)
+    backward = args.workload != "mamba2-1b-fwd"  # that workload is the forward alone
     if args.impl == "reference":
-        run_reference(args, shape, dtype, seed)
+        run_reference(args, shape, dtype, seed, backward)
     else:
-        run_ours(args, shape, dtype, seed)
+        run_ours(args, shape, dtype, seed, backward)
     ws, _, _ = dist_env()
     if ws > 1 and torch.distributed.is_initialized():
         torch.distributed.destroy_process_group()
