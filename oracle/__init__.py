@@ -43,7 +43,7 @@ class _Row(ctypes.Structure):
         ("L", ctypes.c_int), ("H", ctypes.c_int), ("P", ctypes.c_int), ("N", ctypes.c_int), ("G", ctypes.c_int),
         ("xBC", ctypes.c_void_p), ("dt_raw", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
         ("A_log", ctypes.c_void_p), ("D", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
-        ("conv_b", ctypes.c_void_p), ("seq_idx", ctypes.c_void_p),
+        ("conv_b", ctypes.c_void_p), ("seq_idx", ctypes.c_void_p), ("init", ctypes.c_void_p),
     ]
 
 
@@ -57,7 +57,7 @@ def _load():
             I = ctypes.c_int
             lib.orc_forward.argtypes = [ctypes.POINTER(_Row), I, I, I, P, P, P, P, P, I]
             lib.orc_forward.restype = I
-            lib.orc_backward.argtypes = [ctypes.POINTER(_Row), I, I, P, P, P, P, P, P, P, P, P, I]
+            lib.orc_backward.argtypes = [ctypes.POINTER(_Row), I, I, P, P, P, P, P, P, P, P, P, P, I]
             lib.orc_backward.restype = I
             lib.orc_conv.argtypes = [ctypes.POINTER(_Row), I, I, P, P, I]
             lib.orc_conv.restype = I
@@ -66,6 +66,10 @@ def _load():
             lib.orc_subset_channel.argtypes = [ctypes.POINTER(_Row), I, I, I]
             lib.orc_subset_channel.restype = I
             lib.orc_default_threads.restype = I
+            lib.orc_seq_finals.argtypes = [ctypes.POINTER(_Row), I, I, P, I]
+            lib.orc_seq_finals.restype = I
+            lib.orc_num_seqs.argtypes = [ctypes.POINTER(_Row)]
+            lib.orc_num_seqs.restype = I
             _lib = lib
     return _lib
 
@@ -101,8 +105,10 @@ class _RowArgs:
         si = inp.get("seq_idx")
         self.seq_idx = None if si is None else np.ascontiguousarray(
             si[b].cpu().numpy() if hasattr(si, "cpu") else si[b], dtype=np.int32)
+        h0 = inp.get("init")
+        self.init = None if h0 is None else _f64(h0[b])
         self.row = _Row(L, H, P, N, G, _ptr(self.xBC), _ptr(self.dt_raw), _ptr(self.dt_bias), _ptr(self.A_log),
-                        _ptr(self.D), _ptr(self.conv_w), _ptr(self.conv_b), _ptr(self.seq_idx))
+                        _ptr(self.D), _ptr(self.conv_w), _ptr(self.conv_b), _ptr(self.seq_idx), _ptr(self.init))
 
 
 def _dims(shape) -> tuple:
@@ -128,7 +134,8 @@ def conv(inp: dict, shape, b: int = 0, heads: tuple | None = None, nthreads: int
 def forward(inp: dict, shape, n_segments: int | None = None, heads: tuple | None = None,
             rows: list | None = None, nthreads: int = 0) -> dict:
     """y (rows, L, nh, P), final_state (rows, nh, P, N) and, for S > 1, the
-    segment summaries: seg_in / s_ext (rows, S, nh, P, N), a_block (rows, S, nh)."""
+    segment summaries: seg_in / s_ext (rows, S, nh, P, N), a_block (rows, S, nh).
+    inp["init"] (b, H, P, N), when present, is each row's initial state."""
     lib = _load()
     S = shape.n_segments if n_segments is None else n_segments
     h0, h1 = heads or (0, shape.nheads)
@@ -154,19 +161,21 @@ def forward(inp: dict, shape, n_segments: int | None = None, heads: tuple | None
 
 def backward(inp: dict, shape, heads: tuple | None = None, rows: list | None = None,
              use_dfinal: bool = True, nthreads: int = 0) -> dict:
-    """Gradients of L = <dy, y> + <dfinal, final_state> w.r.t. every input.
+    """Gradients of L = <dy, y> + <dfinal, final_state> w.r.t. every input
+    (with inp["init"] present, also w.r.t. each row's initial state: dinit).
 
     For heads=(h0,h1) covering whole groups the results are exact for those heads'
     x channels / dt columns and their groups' B/C channels.  Returns float64:
       dxBC (rows, L, nsub) with ``channels`` (global channel of each column),
-      ddt_raw (rows, L, nh), dconv_w (nsub, 4), dconv_b (nsub), ddt_bias, dA_log, dD (nh)
+      ddt_raw (rows, L, nh), dconv_w (nsub, 4), dconv_b (nsub), ddt_bias, dA_log, dD (nh),
+      dinit (rows, nh, P, N) or None
     with parameter gradients summed over the rows in row order."""
     lib = _load()
     h0, h1 = heads or (0, shape.nheads)
     nh = h1 - h0
     rows = list(range(shape.batch)) if rows is None else list(rows)
     L = shape.seqlen
-    dxs, ddts = [], []
+    dxs, ddts, dinits = [], [], []
     acc = None
     ch = None
     for b in rows:
@@ -183,15 +192,31 @@ def backward(inp: dict, shape, heads: tuple | None = None, rows: list | None = N
         dbias = np.empty(nh)
         dalog = np.empty(nh)
         dD = np.empty(nh)
+        dinit = np.empty((nh, shape.headdim, shape.dstate)) if ra.init is not None else None
         rc = lib.orc_backward(ctypes.byref(ra.row), h0, h1, _ptr(dy), _ptr(dfin), _ptr(dxr), _ptr(dw), _ptr(db),
-                              _ptr(ddt), _ptr(dbias), _ptr(dalog), _ptr(dD), nthreads)
+                              _ptr(ddt), _ptr(dbias), _ptr(dalog), _ptr(dD), _ptr(dinit), nthreads)
         if rc != 0:
             raise ValueError("oracle backward rejected its arguments")
         dxs.append(dxr)
         ddts.append(ddt)
+        dinits.append(dinit)
         part = (dw, db, dbias, dalog, dD)
         acc = part if acc is None else tuple(a + p for a, p in zip(acc, part))
     return {
         "dxBC": np.stack(dxs), "channels": ch, "ddt_raw": np.stack(ddts),
         "dconv_w": acc[0], "dconv_b": acc[1], "ddt_bias": acc[2], "dA_log": acc[3], "dD": acc[4],
+        "dinit": None if dinits[0] is None else np.stack(dinits),
     }
+
+
+def seq_finals(inp: dict, shape, b: int = 0, heads: tuple | None = None, nthreads: int = 0) -> np.ndarray:
+    """The state after the last token of every packed sequence of row b, in order:
+    (nseq, nh, P, N) float64 (the plain token recurrence, from inp["init"][b] if given)."""
+    lib = _load()
+    h0, h1 = heads or (0, shape.nheads)
+    ra = _RowArgs(inp, _dims(shape), b)
+    nseq = lib.orc_num_seqs(ctypes.byref(ra.row))
+    out = np.empty((nseq, h1 - h0, shape.headdim, shape.dstate))
+    if lib.orc_seq_finals(ctypes.byref(ra.row), h0, h1, _ptr(out), nthreads) != nseq:
+        raise ValueError("oracle seq_finals rejected its arguments")
+    return out

@@ -35,6 +35,13 @@
  *   resets at packed-sequence boundaries (seq_idx from cu_seqlens:
  *   NeMo Automodel PR #1441 "feat: context-parallel with nemotron v3",
  *   Key changes): reset(t) = (t == 0) or seq_idx[t] != seq_idx[t-1].
+ *   Initial states (listed as not supported yet in the Megatron-LM PR's
+ *   description; read here as in the Mamba2 chunked scan): the state before a
+ *   row's first token is init[h] instead of zero, so token 0 is then no reset
+ *   and its decay applies to init; later packed sequences still start from
+ *   zero.  In the segmented variant the exclusive scan starts from it:
+ *   S_in[0] = init.  The state after the last token of every packed sequence
+ *   is available as well (orc_seq_finals).
  *
  *   Backward: the adjoint of the recurrence run in reverse (the reverse
  *   boundary scan of the Megatron-LM PR), with states recomputed from
@@ -65,6 +72,7 @@ typedef struct {
   const double *conv_w;  /* Cd x 4, tap 3 multiplies the current token */
   const double *conv_b;  /* Cd */
   const int *seq_idx;    /* L, non-decreasing, or NULL */
+  const double *init;    /* H x P x N: the state before token 0, or NULL (zero) */
 } orc_row;
 
 /* ------------------------------------------------------------------ */
@@ -77,7 +85,7 @@ static double softplus(double z) { return z > 0 ? z + log1p(exp(-z)) : log1p(exp
 static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
 
 static int is_reset(const orc_row *r, int t) {
-  if (t == 0) return 1;
+  if (t == 0) return r->init == NULL;
   return r->seq_idx != NULL && r->seq_idx[t] != r->seq_idx[t - 1];
 }
 
@@ -307,14 +315,18 @@ static void fwd_task(void *vc, int i) {
     memcpy(sext + PN * k, st, sizeof(double) * PN);
     ablk[k] = prod;
   }
-  /* exclusive causal scan over the segment summaries */
-  memset(sin_, 0, sizeof(double) * PN);
+  /* exclusive causal scan over the segment summaries, from the row's initial state */
+  if (r->init)
+    memcpy(sin_, r->init + (size_t)h * PN, sizeof(double) * PN);
+  else
+    memset(sin_, 0, sizeof(double) * PN);
   for (int k = 1; k < S; ++k)
     for (size_t e = 0; e < PN; ++e) sin_[PN * k + e] = ablk[k - 1] * sin_[PN * (k - 1) + e] + sext[PN * (k - 1) + e];
   double *fin = c->final_st + PN * i;
   for (size_t e = 0; e < PN; ++e) fin[e] = ablk[S - 1] * sin_[PN * (S - 1) + e] + sext[PN * (S - 1) + e];
-  /* correction: carry each segment's true initial state into its outputs */
-  for (int k = 1; k < S; ++k) {
+  /* correction: carry each segment's true initial state into its outputs
+   * (segment 0's is zero unless the row has an initial state) */
+  for (int k = r->init ? 0 : 1; k < S; ++k) {
     const double *si = sin_ + PN * k;
     double prod = 1.0;
     for (int t = k * Ls; t < (k + 1) * Ls; ++t) {
@@ -369,6 +381,7 @@ typedef struct {
   double *du_x;         /* nh x L x P */
   double *du_B;         /* nh x L x N, per-head partials */
   double *du_C;         /* nh x L x N */
+  double *dinit;        /* nh x P x N: grad of the row's initial state, or NULL */
   double *ddt_raw;      /* L x nh */
   double *dA;           /* nh: dL/dA */
   double *dD;           /* nh */
@@ -390,7 +403,8 @@ static void bwd_task(void *vc, int i) {
   double *blk = (double *)malloc(sizeof(double) * PN * CKPT); /* states h_t inside a block */
   double *st = (double *)calloc(PN, sizeof(double));
   double *G = (double *)calloc(PN, sizeof(double));
-  /* forward sweep, checkpointing every CKPT tokens */
+  if (r->init) memcpy(st, r->init + (size_t)h * PN, sizeof(double) * PN);
+  /* forward sweep from the state before token 0, checkpointing every CKPT tokens */
   for (int t = 0; t < L; ++t) {
     if (t % CKPT == 0) memcpy(ck + PN * (t / CKPT), st, sizeof(double) * PN);
     double dt = dt_of(r, t, h);
@@ -453,6 +467,8 @@ static void bwd_task(void *vc, int i) {
   }
   c->dA[i] = dA;
   c->dD[i] = dD;
+  /* after the carry past token 0, G is the gradient of the state before it */
+  if (c->dinit) memcpy(c->dinit + (size_t)i * PN, G, sizeof(double) * PN);
   free(x);
   free(B);
   free(C);
@@ -513,10 +529,11 @@ static void convb_task(void *vc, int j) {
  * heads in [h0,h1) only, in head order):
  *   dxr     L x nsub      grad of the raw conv input
  *   dconv_w nsub x 4      dconv_b nsub
- * and per head:  ddt_raw L x nh,  ddt_bias nh,  dA_log nh,  dD nh. */
+ * and per head:  ddt_raw L x nh,  ddt_bias nh,  dA_log nh,  dD nh, and with an
+ * initial state  dinit nh x P x N  (may be NULL). */
 int orc_backward(const orc_row *r, int h0, int h1, const double *dy, const double *dfinal, double *dxr,
                  double *dconv_w, double *dconv_b, double *ddt_raw, double *ddt_bias, double *dA_log,
-                 double *dD, int nthreads) {
+                 double *dD, double *dinit, int nthreads) {
   if (h0 < 0 || h1 > r->H || h0 >= h1 || r->H % r->G != 0) return -1;
   chan_set s = make_set(r, h0, h1);
   int L = r->L, P = r->P, N = r->N, nh = h1 - h0;
@@ -530,7 +547,7 @@ int orc_backward(const orc_row *r, int h0, int h1, const double *dy, const doubl
   double *du_B = (double *)malloc(sizeof(double) * nh * Ls * N);
   double *du_C = (double *)malloc(sizeof(double) * nh * Ls * N);
   double *dA = (double *)malloc(sizeof(double) * nh);
-  bwd_ctx bc = {r, &s, u, dy, dfinal, du_x, du_B, du_C, ddt_raw, dA, dD};
+  bwd_ctx bc = {r, &s, u, dy, dfinal, du_x, du_B, du_C, r->init ? dinit : NULL, ddt_raw, dA, dD};
   run_tasks(bwd_task, &bc, nh, nthreads);
 
   /* gradient of the post-conv channels, channel-major; B/C summed in head order */
@@ -568,4 +585,64 @@ int orc_backward(const orc_row *r, int h0, int h1, const double *dy, const doubl
   free(dA);
   free(du);
   return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* per-sequence final states                                           */
+
+typedef struct {
+  const orc_row *r;
+  const chan_set *s;
+  const double *u;
+  int nseq;
+  double *out; /* nseq x nh x P x N */
+} fin_ctx;
+
+static void fin_task(void *vc, int i) {
+  fin_ctx *c = (fin_ctx *)vc;
+  const orc_row *r = c->r;
+  int L = r->L, P = r->P, N = r->N, h = c->s->h0 + i, nh = c->s->h1 - c->s->h0;
+  size_t PN = (size_t)P * N;
+  double *x = (double *)malloc(sizeof(double) * (size_t)L * P);
+  double *B = (double *)malloc(sizeof(double) * (size_t)L * N);
+  double *C = (double *)malloc(sizeof(double) * (size_t)L * N);
+  double *st = (double *)calloc(PN, sizeof(double));
+  gather_head(r, c->s, c->u, h, x, B, C);
+  if (r->init) memcpy(st, r->init + (size_t)h * PN, sizeof(double) * PN);
+  int q = 0;
+  for (int t = 0; t < L; ++t) {
+    if (t > 0 && !same_seq(r, t - 1, t)) { /* the previous token ended a sequence */
+      memcpy(c->out + ((size_t)q * nh + i) * PN, st, sizeof(double) * PN);
+      ++q;
+    }
+    double dt = dt_of(r, t, h);
+    rec_step(st, P, N, decay_of(r, t, h, dt), dt, x + (size_t)t * P, B + (size_t)t * N);
+  }
+  memcpy(c->out + ((size_t)q * nh + i) * PN, st, sizeof(double) * PN);
+  free(x);
+  free(B);
+  free(C);
+  free(st);
+}
+
+/* Number of packed sequences in the row (1 + the number of seq_idx changes). */
+int orc_num_seqs(const orc_row *r) {
+  int n = 1;
+  for (int t = 1; t < r->L; ++t) n += !same_seq(r, t - 1, t);
+  return n;
+}
+
+/* Public: the state after the last token of every packed sequence of the row,
+ * in order, for heads [h0,h1): out is nseq x nh x P x N (the plain recurrence,
+ * token by token).  Returns nseq, or -1 on bad args. */
+int orc_seq_finals(const orc_row *r, int h0, int h1, double *out, int nthreads) {
+  if (h0 < 0 || h1 > r->H || h0 >= h1 || r->H % r->G != 0) return -1;
+  chan_set s = make_set(r, h0, h1);
+  double *u = (double *)malloc(sizeof(double) * (size_t)s.nsub * r->L);
+  conv_ctx cc = {r, &s, NULL, u};
+  run_tasks(conv_task, &cc, s.nsub, nthreads);
+  fin_ctx c = {r, &s, u, orc_num_seqs(r), out};
+  run_tasks(fin_task, &c, h1 - h0, nthreads);
+  free(u);
+  return c.nseq;
 }

@@ -38,7 +38,10 @@ def quadratic_ssd(inp: dict, shape) -> tuple[np.ndarray, np.ndarray]:
     """y (b, L, H, P) and final state (b, H, P, N) from the masked-attention form
 
         Y = (Lmask o (C B^T)) (dt o X) + D X,   Lmask[t,s] = exp(sum_{r=s+1..t} dt_r A)
-                                                 for s <= t in the same sequence, else 0.
+                                                 for s <= t in the same sequence, else 0,
+
+    plus, with an initial state h0 (inp["init"]), the term exp(sum_{r=0..t} dt_r A) C_t h0
+    for every token t of the row's first sequence (h0 is the state before token 0).
     """
     b, L, H, P, N, G = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups
     _, u = conv_silu_torch(inp, shape)
@@ -68,6 +71,12 @@ def quadratic_ssd(inp: dict, shape) -> tuple[np.ndarray, np.ndarray]:
             y[r, :, h] = (Lm * (uC[r, :, g] @ uB[r, :, g].T)) @ Xs + D[h] * ux[r, :, h]
             w_last = Lm[L - 1]  # weights of every token in the final state
             fin[r, h] = (w_last[:, None] * Xs).T @ uB[r, :, g]
+            if inp.get("init") is not None:
+                h0 = inp["init"][r, h].double().numpy()  # P x N
+                first = same[0]  # tokens of the row's first sequence
+                e = np.where(first, np.exp(cs), 0.0)
+                y[r, :, h] += e[:, None] * (uC[r, :, g] @ h0.T)
+                fin[r, h] += e[L - 1] * h0
     return y, fin
 
 

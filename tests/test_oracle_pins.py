@@ -11,8 +11,15 @@ independent formulation, a special case or an invariant the pages state:
   affine in its initial state, S_out = a_block * S_in + S_ext (Megatron-LM PR
   #6808 "Add state-passing context parallelism for Mamba2", description);
 * seq_idx resets make a packed row equal separate per-sequence runs (NeMo
-  Automodel PR #1441, Key changes: seq_idx from cu_seqlens);
-* the backward equals central finite differences of the forward in every input.
+  Automodel PR #1441, Key changes: seq_idx from cu_seqlens), and the state after
+  each packed sequence equals that run's final state;
+* an initial state (listed as not supported yet by the Megatron-LM PR, read as
+  the state before a row's first token): the quadratic form with its decayed
+  term, segment-count invariance with it, and continuation -- a row cut in two,
+  the second part started from the first part's final state, gives the uncut
+  row's outputs and final state;
+* the backward equals central finite differences of the forward in every input,
+  the initial state included.
 """
 from __future__ import annotations
 
@@ -163,6 +170,61 @@ def test_packed_equals_separate_runs(oracle_lib):
     assert rel(out["final_state"], o["final_state"]) < 1e-14
 
 
+def test_packed_sequence_finals_equal_separate_runs(oracle_lib):
+    lens = [37, 3, 90, 1, 125]
+    L = sum(lens)
+    shape = SsdShape(1, L, 2, 6, 4, 1, 8, 1)
+    inp = make_inputs(shape, 14, "f32", seq_lengths=lens, init_states=True)
+    fins = oracle_lib.seq_finals(inp, shape)
+    assert fins.shape == (len(lens), 2, 6, 4)
+    s0 = 0
+    for q, n in enumerate(lens):
+        sub = {k: (v[:, s0:s0 + n] if k in ("xBC", "dt_raw") else v) for k, v in inp.items()}
+        sub["seq_idx"] = None
+        if q > 0:
+            sub["init"] = None  # only the row's first sequence starts from the initial state
+        o = oracle_lib.forward(sub, shape.with_(seqlen=n), n_segments=1)
+        assert rel(fins[q], o["final_state"][0]) < 1e-14
+        s0 += n
+    assert rel(fins[-1], oracle_lib.forward(inp, shape, n_segments=1)["final_state"][0]) < 1e-14
+
+
+@pytest.mark.parametrize("shape,seq", [
+    (SMALL, None),
+    (SMALL, [30, 2, 41, 23]),
+    (SsdShape(1, 200, 3, 5, 7, 1, 8, 1), [1, 1, 3, 195]),
+])
+def test_initial_state_equals_quadratic_form(oracle_lib, shape, seq):
+    inp = make_inputs(shape, 6, "f32", seq_lengths=seq, init_states=True)
+    y_ref, fin_ref = quadratic_ssd(inp, shape)
+    out = oracle_lib.forward(inp, shape, n_segments=1)
+    assert rel(out["y"], y_ref) < 1e-12
+    assert rel(out["final_state"], fin_ref) < 1e-12
+    for S in (2, 4, 8):
+        o = oracle_lib.forward(inp, shape, n_segments=S)
+        assert rel(o["y"], y_ref) < 1e-12 and rel(o["final_state"], fin_ref) < 1e-12, S
+        assert rel(o["seg_in"][:, 0], inp["init"].double().numpy()) == 0.0  # the scan starts from it
+
+
+@pytest.mark.parametrize("cut", [1, 57, 128])
+def test_continuation_from_a_final_state(oracle_lib, cut):
+    """A row cut at token `cut`: the second part, started from the first part's
+    final state, reproduces the uncut row.  Conv taps before the current token
+    are zeroed so that the conv carries nothing across the cut."""
+    shape = SsdShape(2, 256, 4, 8, 6, 2, 16, 1)
+    inp = make_inputs(shape, 15, "f32", init_states=True)
+    inp["conv_w"][:, :3] = 0.0
+    full = oracle_lib.forward(inp, shape, n_segments=1)
+    a = {k: (v[:, :cut] if k in ("xBC", "dt_raw") else v) for k, v in inp.items()}
+    pa = oracle_lib.forward(a, shape.with_(seqlen=cut), n_segments=1)
+    b = {k: (v[:, cut:] if k in ("xBC", "dt_raw") else v) for k, v in inp.items()}
+    b["init"] = torch.from_numpy(pa["final_state"])
+    pb = oracle_lib.forward(b, shape.with_(seqlen=256 - cut), n_segments=1)
+    assert rel(pa["y"], full["y"][:, :cut]) < 1e-13
+    assert rel(pb["y"], full["y"][:, cut:]) < 1e-12
+    assert rel(pb["final_state"], full["final_state"]) < 1e-12
+
+
 def test_head_subsets_match_full(oracle_lib):
     shape = SsdShape(1, 64, 6, 4, 3, 3, 8, 2)
     inp = make_inputs(shape, 17, "f32", dfinal=True)
@@ -184,14 +246,17 @@ def _loss(oracle_lib, inp, shape):
     return float(np.sum(inp["dy"].double().numpy() * y) + np.sum(inp["dfinal"].double().numpy() * out["final_state"]))
 
 
-@pytest.mark.parametrize("shape,seq", [
-    (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), None),
-    (SsdShape(1, 60, 2, 4, 3, 1, 8, 1), [17, 1, 2, 40]),
+@pytest.mark.parametrize("shape,seq,init", [
+    (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), None, False),
+    (SsdShape(1, 60, 2, 4, 3, 1, 8, 1), [17, 1, 2, 40], False),
     # longer than the oracle's 256-token checkpoint interval
-    (SsdShape(1, 600, 2, 3, 2, 1, 8, 1), [255, 1, 344]),
+    (SsdShape(1, 600, 2, 3, 2, 1, 8, 1), [255, 1, 344], False),
+    # with initial states: every input and the initial state itself
+    (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), None, True),
+    (SsdShape(1, 300, 2, 4, 3, 1, 8, 1), [260, 1, 39], True),
 ])
-def test_backward_matches_finite_differences(oracle_lib, shape, seq):
-    inp = f64(make_inputs(shape, 23, "f32", dfinal=True, seq_lengths=seq))
+def test_backward_matches_finite_differences(oracle_lib, shape, seq, init):
+    inp = f64(make_inputs(shape, 23, "f32", dfinal=True, seq_lengths=seq, init_states=init))
     g = oracle_lib.backward(inp, shape, nthreads=1)
     dxBC = np.zeros((shape.batch, shape.seqlen, shape.conv_dim))
     dxBC[..., g["channels"]] = g["dxBC"]
@@ -201,6 +266,8 @@ def test_backward_matches_finite_differences(oracle_lib, shape, seq):
     dconv_b[g["channels"]] = g["dconv_b"]
     grads = {"xBC": dxBC, "dt_raw": g["ddt_raw"], "dt_bias": g["ddt_bias"], "A_log": g["dA_log"], "D": g["dD"],
              "conv_w": dconv_w, "conv_b": dconv_b}
+    if init:
+        grads["init"] = g["dinit"]
     rng = np.random.default_rng(0)
     HP, GN = shape.nheads * shape.headdim, shape.ngroups * shape.dstate
     parts = {"x": slice(0, HP), "B": slice(HP, HP + GN), "C": slice(HP + GN, HP + 2 * GN)}
