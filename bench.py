@@ -382,7 +382,7 @@ def run_reference(args, shape, dtype, seed, backward: bool):
 
 
 def metric_for(args, backward: bool) -> str:
-    if args.workload == DEFAULT_WORKLOAD and args.segments is None and args.batch is None:
+    if args.workload == DEFAULT_WORKLOAD and args.segments is None and args.batch is None and args.chunk is None:
         return METRIC
     what = "fwd+bwd" if backward else "fwd"
     return f"SSD {what} tokens/s on 1 GB300 ({args.workload}, bf16) + % of tensor/HBM roofline"
@@ -549,6 +549,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--segments", type=int, default=None, help="override the workload's segment count")
+    ap.add_argument("--chunk", type=int, default=None, help="override the workload's chunk length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")
@@ -559,6 +560,8 @@ def main():
         shape = shape.with_(batch=args.batch)
     if args.segments is not None:
         shape = shape.with_(n_segments=args.segments)
+    if args.chunk is not None:
+        shape = shape.with_(chunk=args.chunk)
     backward = args.workload != "mamba2-1b-fwd"  # that workload is the forward alone
     if args.impl == "reference":
         run_reference(args, shape, dtype, seed, backward)

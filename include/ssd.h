@@ -79,7 +79,13 @@ typedef struct {
  * 16-byte aligned, where tap 3 multiplies the current token; conv_b (Cd);
  * Cd = H*P + 2*G*N and the conv channel order is [x | B | C].
  * seq_idx (b, L) int32, non-decreasing within a row, or NULL (one sequence per
- * row).  The state and the conv taps are reset where it changes. */
+ * row).  The state and the conv taps are reset where it changes.
+ * initial_states (b, H, P, N) fp32, 16-byte aligned, or NULL (zero): each row's
+ * state before its first token, to which that token's decay applies (the
+ * Mamba2 chunked-scan convention; the pages list initial states as not
+ * supported yet: "Add state-passing context parallelism for Mamba2", "Not
+ * supported yet").  With packed rows it seeds the row's first sequence only;
+ * later sequences start from zero.  The exclusive segment scan starts from it. */
 typedef struct {
   const void *x;  int64_t x_tok_stride;
   const void *B;  int64_t B_tok_stride;
@@ -87,18 +93,23 @@ typedef struct {
   const void *dt; int64_t dt_tok_stride;
   const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
   const int32_t *seq_idx;
+  const float *initial_states;
 } ssd_inputs;
 
 /* Gradients, written (not accumulated).  dx, dB, dC, ddt have the layout and
  * alignment rules of x, B, C, dt, with their own token strides (they may be
  * views into one d(zxBCdt) buffer).  ddt_bias, dA_log, dD (H), dconv_w (Cd,4),
- * dconv_b (Cd) are fp32 and summed over batch and tokens. */
+ * dconv_b (Cd) are fp32 and summed over batch and tokens.  dinitial_states
+ * (b, H, P, N) fp32, 16-byte aligned: the gradient of the initial states, the
+ * reverse segment scan carried one step past the first segment; written only
+ * when the inputs have initial_states, and may be NULL. */
 typedef struct {
   void *dx;  int64_t dx_tok_stride;
   void *dB;  int64_t dB_tok_stride;
   void *dC;  int64_t dC_tok_stride;
   void *ddt; int64_t ddt_tok_stride;
   float *ddt_bias, *dA_log, *dD, *dconv_w, *dconv_b;
+  float *dinitial_states;
 } ssd_grads;
 
 /* Bytes of device workspace ssd_forward (backward = 0) or ssd_backward
@@ -114,6 +125,20 @@ size_t ssd_workspace_size(const ssd_dims *dims, int backward);
  * multiple of 32 and <= 256, n_segments <= 1024; otherwise SSD_ERR_UNSUPPORTED. */
 ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
                        float *seg_init_states, void *workspace, size_t ws_bytes, ssd_stream_t stream);
+
+/* Forward of a packed row of sequences (THD layout, dims.batch = 1) that also
+ * returns the state after every sequence's last token: seq_final_states
+ * (nseq, H, P, N) fp32, 16-byte aligned, sequence s covering tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]) (cu_seqlens: nseq + 1 int32 device values, the
+ * layout of "feat: context-parallel with nemotron v3", Key changes).  in->seq_idx
+ * is required and must describe the same sequences (ssd_cu_seqlens_to_seq_idx
+ * makes it; neither is checked against the other on the host).  Sequences
+ * that are empty or fall outside [0, seqlen) get a zero state.  Everything else
+ * as ssd_forward, same workspace size.  No gradient flows back through
+ * seq_final_states (ssd_backward's dfinal_state is the row's last token's). */
+ssd_status ssd_forward_varlen(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
+                              float *seg_init_states, const int32_t *cu_seqlens, int32_t nseq,
+                              float *seq_final_states, void *workspace, size_t ws_bytes, ssd_stream_t stream);
 
 /* Backward of  L = <dy, y> + <dfinal_state, final_state>.
  * dy (b, L, H*P) activation dtype, contiguous; dfinal_state (b, H, P, N) fp32 or

@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "SsdError", "SsdDims", "SsdInputs", "SsdGrads", "load", "ssd_workspace_size", "ssd_forward", "ssd_backward",
-    "ssd_forward_static", "STATIC_SCRATCH_BYTES",
+    "ssd_forward_static", "STATIC_SCRATCH_BYTES", "ssd_forward_varlen",
     "ssd_cu_seqlens_to_seq_idx", "ssd_device_status", "ssd_set_wait_limit_ns", "DEFAULT_WAIT_LIMIT_NS",
     "ssd_status_string", "ssd_profile_begin",
     "ssd_profile_end", "SsdKernelTime", "SsdRunner",
@@ -48,6 +48,7 @@ class SsdInputs(ctypes.Structure):
         ("dt", ctypes.c_void_p), ("dt_tok_stride", ctypes.c_int64),
         ("dt_bias", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("D", ctypes.c_void_p),
         ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p), ("seq_idx", ctypes.c_void_p),
+        ("initial_states", ctypes.c_void_p),
     ]
 
 
@@ -58,7 +59,7 @@ class SsdGrads(ctypes.Structure):
         ("dC", ctypes.c_void_p), ("dC_tok_stride", ctypes.c_int64),
         ("ddt", ctypes.c_void_p), ("ddt_tok_stride", ctypes.c_int64),
         ("ddt_bias", ctypes.c_void_p), ("dA_log", ctypes.c_void_p), ("dD", ctypes.c_void_p),
-        ("dconv_w", ctypes.c_void_p), ("dconv_b", ctypes.c_void_p),
+        ("dconv_w", ctypes.c_void_p), ("dconv_b", ctypes.c_void_p), ("dinitial_states", ctypes.c_void_p),
     ]
 
 
@@ -80,6 +81,9 @@ def load():
         lib.ssd_forward.restype = I
         lib.ssd_forward_static.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(SsdInputs), P, P, P, P]
         lib.ssd_forward_static.restype = I
+        lib.ssd_forward_varlen.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(SsdInputs), P, P, P, P,
+                                           ctypes.c_int32, P, P, S, P]
+        lib.ssd_forward_varlen.restype = I
         lib.ssd_backward.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(SsdInputs), P, P, P,
                                      ctypes.POINTER(SsdGrads), P, S, P]
         lib.ssd_backward.restype = I
@@ -133,6 +137,17 @@ def ssd_forward(dims: SsdDims, inputs: SsdInputs, y, final_state, seg_init_state
     ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
     _check(load().ssd_forward(ctypes.byref(dims), ctypes.byref(inputs), _ptr(y), _ptr(final_state),
                               _ptr(seg_init_states), _ptr(workspace), ws_bytes, _stream(stream)), "ssd_forward")
+
+
+def ssd_forward_varlen(dims: SsdDims, inputs: SsdInputs, y, final_state, seg_init_states, cu_seqlens,
+                       seq_final_states, workspace, ws_bytes=None, stream=None) -> None:
+    """ssd_forward of one packed row that also writes the state after every
+    sequence's last token into seq_final_states (nseq, H, P, N)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(load().ssd_forward_varlen(ctypes.byref(dims), ctypes.byref(inputs), _ptr(y), _ptr(final_state),
+                                     _ptr(seg_init_states), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                     _ptr(seq_final_states), _ptr(workspace), ws_bytes, _stream(stream)),
+           "ssd_forward_varlen")
 
 
 def ssd_forward_static(dims: SsdDims, inputs: SsdInputs, y, final_state, seg_init_states, stream=None) -> None:
@@ -217,7 +232,7 @@ class SsdRunner:
         base = xBC.data_ptr()
         return SsdInputs(base, Cd, base + HP * es, Cd, base + (HP + GN) * es, Cd, t["dt_raw"].data_ptr(), s.nheads,
                          _ptr(t["dt_bias"]), _ptr(t["A_log"]), _ptr(t["D"]), _ptr(t["conv_w"]), _ptr(t["conv_b"]),
-                         _ptr(t.get("seq_idx")))
+                         _ptr(t.get("seq_idx")), _ptr(t.get("init")))
 
     def alloc_outputs(self):
         s = self.shape
@@ -227,7 +242,7 @@ class SsdRunner:
                           device=self.device)
         return y, fin, seg
 
-    def alloc_grads(self):
+    def alloc_grads(self, init: bool = False):
         s = self.shape
         g = {
             "dxBC": torch.empty(s.batch, s.seqlen, s.conv_dim, dtype=self.tdtype, device=self.device),
@@ -238,6 +253,8 @@ class SsdRunner:
             "dconv_w": torch.empty(s.conv_dim, 4, dtype=torch.float32, device=self.device),
             "dconv_b": torch.empty(s.conv_dim, dtype=torch.float32, device=self.device),
         }
+        if init:
+            g["dinit"] = torch.empty(s.batch, s.nheads, s.headdim, s.dstate, dtype=torch.float32, device=self.device)
         return g
 
     def grads_struct(self, g: dict) -> SsdGrads:
@@ -248,7 +265,17 @@ class SsdRunner:
         base = d.data_ptr()
         return SsdGrads(base, Cd, base + HP * es, Cd, base + (HP + GN) * es, Cd, g["ddt_raw"].data_ptr(), s.nheads,
                         _ptr(g["ddt_bias"]), _ptr(g["dA_log"]), _ptr(g["dD"]), _ptr(g["dconv_w"]),
-                        _ptr(g["dconv_b"]))
+                        _ptr(g["dconv_b"]), _ptr(g.get("dinit")))
+
+    def forward_varlen(self, t: dict, out=None, stream=None):
+        """Forward of a packed row (t["cu_seqlens"], t["seq_idx"]); returns y,
+        final_state, seg_init_states and the per-sequence final states."""
+        y, fin, seg = out if out is not None else self.alloc_outputs()
+        cu = t["cu_seqlens"]
+        s = self.shape
+        sf = torch.empty(cu.numel() - 1, s.nheads, s.headdim, s.dstate, dtype=torch.float32, device=self.device)
+        ssd_forward_varlen(self.dims, self.inputs(t), y, fin, seg, cu, sf, self.workspace, stream=stream)
+        return y, fin, seg, sf
 
     def forward(self, t: dict, out=None, stream=None):
         y, fin, seg = out if out is not None else self.alloc_outputs()
@@ -256,7 +283,7 @@ class SsdRunner:
         return y, fin, seg
 
     def backward(self, t: dict, dy, dfinal=None, seg=None, grads=None, stream=None):
-        g = grads if grads is not None else self.alloc_grads()
+        g = grads if grads is not None else self.alloc_grads(init=t.get("init") is not None)
         ssd_backward(self.dims, self.inputs(t), dy, dfinal, seg, self.grads_struct(g), self.workspace,
                      stream=stream)
         return g

@@ -69,7 +69,8 @@ ssd_status check_inputs(const ssd_dims *d, const ssd_inputs *in, Problem &pr) {
       in->x_tok_stride % vec || in->B_tok_stride % vec || in->C_tok_stride % vec)
     return SSD_ERR_ALIGNMENT;
   if (!aligned(in->dt_bias, 4) || !aligned(in->A_log, 4) || !aligned(in->D, 4) || !aligned(in->conv_w, 16) ||
-      !aligned(in->conv_b, 4) || (in->seq_idx && !aligned(in->seq_idx, 4)))
+      !aligned(in->conv_b, 4) || (in->seq_idx && !aligned(in->seq_idx, 4)) ||
+      (in->initial_states && !aligned(in->initial_states, 16)))
     return SSD_ERR_ALIGNMENT;
   pr = problem_from(d);
   pr.x = in->x;
@@ -86,6 +87,7 @@ ssd_status check_inputs(const ssd_dims *d, const ssd_inputs *in, Problem &pr) {
   pr.conv_w = in->conv_w;
   pr.conv_b = in->conv_b;
   pr.seq_idx = in->seq_idx;
+  pr.init = in->initial_states;
   return SSD_OK;
 }
 
@@ -146,9 +148,16 @@ Problem with_tables(const Problem &in, char *ws, const Workspace &w) {
   return pr;
 }
 
+// Per-sequence final states of a packed row (ssd_forward_varlen).
+struct SeqFinals {
+  const int *cu_seqlens = nullptr;
+  int nseq = 0;
+  float *out = nullptr;
+};
+
 template <typename T>
 ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *segin_user, char *ws,
-                        const Workspace &w, cudaStream_t s) {
+                        const Workspace &w, cudaStream_t s, const SeqFinals &sf = SeqFinals()) {
   const Problem pr = with_tables(pr_in, ws, w);
   cudaMemsetAsync(ws + w.status, 0, kStatusBytes, s);  // status word and work counters
   T *u = reinterpret_cast<T *>(ws + w.u);
@@ -180,6 +189,8 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
     }
   }
   if (!tc) SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, y, s));
+  if (sf.out)  // the chunk states (tensor-core path) or local states (CUDA-core path) are still in sst
+    SSD_LAUNCH("seq_finals", launch_seq_finals<T>(pr, u, dtv, acs, sst, !tc, segin, sf.cu_seqlens, sf.nseq, sf.out, s));
   return launch_status();
 }
 
@@ -227,7 +238,8 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   }
   if (!tc) SSD_LAUNCH("chunk_z", launch_chunk_z<T>(pr, u, dy, acs, dsl, s));
   SSD_LAUNCH("local_rev", launch_local_rev(pr, acs, dsl, gext, s));
-  SSD_LAUNCH("seg_rscan", launch_seg_rscan(pr, gext, ablk, dfinal, gout, s));
+  SSD_LAUNCH("seg_rscan",
+             launch_seg_rscan(pr, gext, ablk, dfinal, gout, pr.init ? g->dinitial_states : nullptr, s));
   // chunk gradients
   int vcol_parts = 1, nsub = pr.H, spg = pr.hpg;
   float *sdp = nullptr;  // partial <dS_end, S_in> per chunk and element group, when the combine pass computes it
@@ -292,47 +304,81 @@ size_t ssd_workspace_size(const ssd_dims *dims, int backward) {
   return plan_workspace(pr, elem_bytes(dims->dtype), backward != 0, dims->dtype == SSD_BF16 && tc_envelope(pr)).total;
 }
 
-ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
-                       float *seg_init_states, void *workspace, size_t ws_bytes, ssd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation shared by the forward entry points (everything but the scratch).
+ssd_status check_forward(const ssd_dims *dims, const ssd_inputs *in, const void *y, const float *final_state,
+                         const float *seg_init_states, Problem &pr, Workspace &w) {
   ssd_status st = check_dims(dims);
   if (st != SSD_OK) return st;
-  Problem pr;
   st = check_inputs(dims, in, pr);
   if (st != SSD_OK) return st;
   if (!y) return SSD_ERR_NULL_PTR;
   if (!aligned(y, 16) || (final_state && !aligned(final_state, 16)) ||
       (seg_init_states && !aligned(seg_init_states, 16)))
     return SSD_ERR_ALIGNMENT;
-  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false, dims->dtype == SSD_BF16 && tc_envelope(pr));
+  w = plan_workspace(pr, elem_bytes(dims->dtype), false, dims->dtype == SSD_BF16 && tc_envelope(pr));
+  return SSD_OK;
+}
+
+ssd_status run_forward(const ssd_dims *dims, const Problem &pr, const Workspace &w, void *y, float *final_state,
+                       float *seg_init_states, char *ws, cudaStream_t s, const SeqFinals &sf = SeqFinals()) {
+  if (dims->dtype == SSD_BF16)
+    return forward_impl<__nv_bfloat16>(pr, static_cast<__nv_bfloat16 *>(y), final_state, seg_init_states, ws, w, s,
+                                       sf);
+  return forward_impl<float>(pr, static_cast<float *>(y), final_state, seg_init_states, ws, w, s, sf);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_forward(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
+                       float *seg_init_states, void *workspace, size_t ws_bytes, ssd_stream_t stream) {
+  Problem pr;
+  Workspace w;
+  const ssd_status st = check_forward(dims, in, y, final_state, seg_init_states, pr, w);
+  if (st != SSD_OK) return st;
   if (!workspace || ws_bytes < w.total) return SSD_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return SSD_ERR_ALIGNMENT;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char *ws = static_cast<char *>(workspace);
-  if (dims->dtype == SSD_BF16)
-    return forward_impl<__nv_bfloat16>(pr, static_cast<__nv_bfloat16 *>(y), final_state, seg_init_states, ws, w, s);
-  return forward_impl<float>(pr, static_cast<float *>(y), final_state, seg_init_states, ws, w, s);
+  return run_forward(dims, pr, w, y, final_state, seg_init_states, static_cast<char *>(workspace),
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+ssd_status ssd_forward_varlen(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
+                              float *seg_init_states, const int32_t *cu_seqlens, int32_t nseq,
+                              float *seq_final_states, void *workspace, size_t ws_bytes, ssd_stream_t stream) {
+  Problem pr;
+  Workspace w;
+  const ssd_status st = check_forward(dims, in, y, final_state, seg_init_states, pr, w);
+  if (st != SSD_OK) return st;
+  if (!cu_seqlens || !seq_final_states || !in->seq_idx) return SSD_ERR_NULL_PTR;
+  if (nseq <= 0) return SSD_ERR_INVALID_DIMS;
+  if (dims->batch != 1) return SSD_ERR_UNSUPPORTED;  // packed rows: one row of sequences
+  if (!aligned(cu_seqlens, 4) || !aligned(seq_final_states, 16)) return SSD_ERR_ALIGNMENT;
+  if (!workspace || ws_bytes < w.total) return SSD_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return SSD_ERR_ALIGNMENT;
+  SeqFinals sf;
+  sf.cu_seqlens = cu_seqlens;
+  sf.nseq = nseq;
+  sf.out = seq_final_states;
+  return run_forward(dims, pr, w, y, final_state, seg_init_states, static_cast<char *>(workspace),
+                     reinterpret_cast<cudaStream_t>(stream), sf);
 }
 
 ssd_status ssd_forward_static(const ssd_dims *dims, const ssd_inputs *in, void *y, float *final_state,
                               float *seg_init_states, ssd_stream_t stream) {
-  ssd_status st = check_dims(dims);
-  if (st != SSD_OK) return st;
   Problem pr;
-  st = check_inputs(dims, in, pr);
+  Workspace w;
+  const ssd_status st = check_forward(dims, in, y, final_state, seg_init_states, pr, w);
   if (st != SSD_OK) return st;
-  if (!y) return SSD_ERR_NULL_PTR;
-  if (!aligned(y, 16) || (final_state && !aligned(final_state, 16)) ||
-      (seg_init_states && !aligned(seg_init_states, 16)))
-    return SSD_ERR_ALIGNMENT;
-  const Workspace w = plan_workspace(pr, elem_bytes(dims->dtype), false, dims->dtype == SSD_BF16 && tc_envelope(pr));
   if (w.total > SSD_STATIC_SCRATCH_BYTES) return SSD_ERR_WORKSPACE;
   void *scratch = static_scratch_ptr();
   if (!scratch) return SSD_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char *ws = static_cast<char *>(scratch);
-  if (dims->dtype == SSD_BF16)
-    return forward_impl<__nv_bfloat16>(pr, static_cast<__nv_bfloat16 *>(y), final_state, seg_init_states, ws, w, s);
-  return forward_impl<float>(pr, static_cast<float *>(y), final_state, seg_init_states, ws, w, s);
+  return run_forward(dims, pr, w, y, final_state, seg_init_states, static_cast<char *>(scratch),
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *dy, const float *dfinal_state,
@@ -347,6 +393,7 @@ ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *
   if (!grads->dx || !grads->dB || !grads->dC || !grads->ddt || !grads->ddt_bias || !grads->dA_log || !grads->dD ||
       !grads->dconv_w || !grads->dconv_b)
     return SSD_ERR_NULL_PTR;
+  if (grads->dinitial_states && !aligned(grads->dinitial_states, 16)) return SSD_ERR_ALIGNMENT;
   const int eb = elem_bytes(dims->dtype);
   const long long vec = 16 / eb;
   const long long HP = (long long)dims->nheads * dims->headdim, GN = (long long)dims->ngroups * dims->dstate;

@@ -35,7 +35,8 @@ struct ChunkVecs {
   int seq[256];
 };
 
-// em[i]  = exp(Acs_i) * [token i continues the sequence of the token before the chunk]
+// em[i]  = exp(Acs_i) * [token i continues the state entering the chunk: the
+//          sequence of the token before it, or the row's initial state]
 // w[j]   = exp(Acs_last - Acs_j) * [token j is in the last token's sequence]
 // wdt[j] = w[j] * dt_j
 __device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkIds &id, const float *dtv,
@@ -43,7 +44,8 @@ __device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkId
   const float *acs_bh = acs + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
   const float *dt_bh = dtv + ((size_t)id.bb * pr.H + id.h) * pr.L + id.t0;
   const int Q = pr.Q;
-  const int seq_prev = id.c > 0 ? seq_of(pr, id.bb, id.t0 - 1) : 0;
+  const bool inc = chunk_has_incoming(pr, id.c);
+  const int seq_prev = inc ? seq_before_chunk(pr, id.bb, id.c) : 0;
   const int seq_last = seq_of(pr, id.bb, id.t0 + Q - 1);
   const float acs_last = acs_bh[Q - 1];
   for (int i = threadIdx.x; i < Q; i += blockDim.x) {
@@ -52,7 +54,7 @@ __device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkId
     v.acs[i] = a;
     v.dt[i] = d;
     v.seq[i] = sq;
-    v.em[i] = (id.c > 0 && sq == seq_prev) ? expf(a) : 0.f;
+    v.em[i] = (inc && sq == seq_prev) ? expf(a) : 0.f;
     const float w = (sq == seq_last) ? expf(acs_last - a) : 0.f;
     v.w[i] = w;
     v.wdt[i] = w * d;
@@ -79,11 +81,12 @@ __device__ __forceinline__ void load_wdt_pair(const Problem &pr, int c, int h0, 
 __device__ __forceinline__ void load_em_pair(const Problem &pr, int c, int h0, int bb, const float *acs,
                                              float (&e0)[256], float (&e1)[256]) {
   const int Q = pr.Q, t0 = c * Q;
-  const int seq_prev = c > 0 ? seq_of(pr, bb, t0 - 1) : 0;
+  const bool inc = chunk_has_incoming(pr, c);
+  const int seq_prev = inc ? seq_before_chunk(pr, bb, c) : 0;
   for (int e = threadIdx.x; e < 2 * Q; e += blockDim.x) {
     const int hh = e / Q, i = e % Q, h = h0 + hh;
     const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L + t0;
-    const float m = (c > 0 && seq_of(pr, bb, t0 + i) == seq_prev) ? expf(acs_bh[i]) : 0.f;
+    const float m = (inc && seq_of(pr, bb, t0 + i) == seq_prev) ? expf(acs_bh[i]) : 0.f;
     (hh ? e1 : e0)[i] = m;
   }
   __syncthreads();

@@ -18,6 +18,7 @@ struct Problem {
   long long xs, Bs, Cs, dts;  // token strides (elements)
   const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
   const int *seq_idx;  // (b, L) or nullptr
+  const float *init;   // (b, H, P, N): each row's initial state (the state before token 0), or nullptr
   // per (b, h, chunk) decay tables, (b, H, nc) fp32, filled by decay_tables_kernel:
   const float *cdec;    // product of the chunk's per-token decays (0 at row start / sequence start inside)
   const float *dstart;  // product of cdec over the segment's chunks before this one
@@ -57,15 +58,29 @@ __device__ __forceinline__ int seq_of(const Problem &pr, int b, int t) {
   return pr.seq_idx ? __ldg(pr.seq_idx + (size_t)b * pr.L + t) : 0;
 }
 
+// Whether the first tokens of chunk c receive a state from before the chunk:
+// every chunk but a row's first, and the first one too when the row has an
+// initial state (the state before token 0, which its decay then applies to).
+__host__ __device__ __forceinline__ bool chunk_has_incoming(const Problem &pr, int c) {
+  return c > 0 || pr.init != nullptr;
+}
+// The sequence that state belongs to: that of the token before the chunk, or
+// for a row's first chunk the row's first sequence (only it starts from the
+// initial state; later packed sequences start from zero).
+__device__ __forceinline__ int seq_before_chunk(const Problem &pr, int b, int c) {
+  return seq_of(pr, b, c > 0 ? c * pr.Q - 1 : 0);
+}
+
 // Product of the per-token decays over chunk c of row b, head h: the factor that
 // carries the state entering the chunk to its end (computed from Acs; kernels
-// read it from the decay tables through chunk_decay()).  Zero at the row start and
-// when a packed sequence starts inside the chunk.  acs_bh: chunk-local inclusive
-// cumsum of dt*A for (b, h), length L.
+// read it from the decay tables through chunk_decay()).  Zero when no state
+// enters the chunk (a row start without an initial state) and when a packed
+// sequence starts inside it.  acs_bh: chunk-local inclusive cumsum of dt*A for
+// (b, h), length L.
 __device__ __forceinline__ float chunk_decay_raw(const Problem &pr, const float *acs_bh, int b, int c) {
-  if (c == 0) return 0.f;
+  if (!chunk_has_incoming(pr, c)) return 0.f;
   int t0 = c * pr.Q, t1 = t0 + pr.Q - 1;
-  if (pr.seq_idx && seq_of(pr, b, t0 - 1) != seq_of(pr, b, t1)) return 0.f;
+  if (pr.seq_idx && seq_before_chunk(pr, b, c) != seq_of(pr, b, t1)) return 0.f;
   return expf(acs_bh[t1]);
 }
 

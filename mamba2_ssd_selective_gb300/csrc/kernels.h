@@ -32,7 +32,14 @@ void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, fl
                      cudaStream_t s);
 void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s);
 void launch_seg_rscan(const Problem &pr, const float *gext, const float *ablk, const float *dfinal, float *gout,
-                      cudaStream_t s);
+                      float *dinit, cudaStream_t s);
+// per-sequence final states of a packed row (varlen.cu); sst_local: sst holds
+// the local states entering each chunk (CUDA-core path) rather than the chunk
+// states Sc (tensor-core path)
+template <typename T>
+void launch_seq_finals(const Problem &pr, const T *u, const float *dtv, const float *acs, const float *sst,
+                       bool sst_local, const float *segin, const int *cu_seqlens, int nseq, float *out,
+                       cudaStream_t s);
 
 // fp32 SIMT chunk kernels (simt_chunk.cu)
 template <typename T> void launch_cb(const Problem &pr, const T *u, float *cb, cudaStream_t s);

@@ -119,7 +119,8 @@ void launch_local_pass(const Problem &pr, float *sst, float *sext, bool write_lo
     local_pass_kernel<false><<<grid, 256, 0, s>>>(pr, sst, sext);
 }
 
-// Exclusive scan: S_in[0] = 0, S_in[k] = a_block[k-1] * S_in[k-1] + S_ext[k-1];
+// Exclusive scan: S_in[0] = the row's initial state (zero without one),
+// S_in[k] = a_block[k-1] * S_in[k-1] + S_ext[k-1];
 // final state = a_block[S-1] * S_in[S-1] + S_ext[S-1].
 __global__ void __launch_bounds__(256) seg_scan_kernel(Problem pr, const float *__restrict__ sext,
                                                        const float *__restrict__ ablk, float *__restrict__ segin,
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(Problem pr, const float *
   const int e = blockIdx.x * 256 + threadIdx.x;
   const int h = blockIdx.y, bb = blockIdx.z;
   if (e >= PN) return;
-  float s = 0.f;
+  float s = pr.init ? pr.init[((size_t)bb * pr.H + h) * PN + e] : 0.f;
   for (int k = 0; k < pr.S; ++k) {
     const size_t so = ((size_t)bb * pr.S + k) * pr.H + h;
     segin[so * PN + e] = s;
@@ -359,10 +360,13 @@ void launch_combine_bwd(const Problem &pr, const float *sc, const float *segin, 
 }
 
 // Reverse exclusive scan: G_out[S-1] = dfinal; G_out[k-1] = a_block[k]*G_out[k] + g_ext[k].
-// G_out[k] is the gradient w.r.t. the state at the end of segment k.
+// G_out[k] is the gradient w.r.t. the state at the end of segment k; one step
+// past segment 0, a_block[0]*G_out[0] + g_ext[0], is the gradient w.r.t. the
+// row's initial state (written to dinit when given).
 __global__ void __launch_bounds__(256) seg_rscan_kernel(Problem pr, const float *__restrict__ gext,
                                                         const float *__restrict__ ablk,
-                                                        const float *__restrict__ dfinal, float *__restrict__ gout) {
+                                                        const float *__restrict__ dfinal, float *__restrict__ gout,
+                                                        float *__restrict__ dinit) {
   const int PN = pr.P * pr.N;
   const int e = blockIdx.x * 256 + threadIdx.x;
   const int h = blockIdx.y, bb = blockIdx.z;
@@ -373,12 +377,13 @@ __global__ void __launch_bounds__(256) seg_rscan_kernel(Problem pr, const float 
     gout[so * PN + e] = g;
     g = fmaf(ablk[so], g, gext[so * PN + e]);
   }
+  if (dinit) dinit[((size_t)bb * pr.H + h) * PN + e] = g;
 }
 
 void launch_seg_rscan(const Problem &pr, const float *gext, const float *ablk, const float *dfinal, float *gout,
-                      cudaStream_t s) {
+                      float *dinit, cudaStream_t s) {
   dim3 grid((pr.P * pr.N + 255) / 256, pr.H, pr.b);
-  seg_rscan_kernel<<<grid, 256, 0, s>>>(pr, gext, ablk, dfinal, gout);
+  seg_rscan_kernel<<<grid, 256, 0, s>>>(pr, gext, ablk, dfinal, gout, dinit);
 }
 
 }  // namespace ssd

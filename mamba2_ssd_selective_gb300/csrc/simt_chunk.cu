@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) out_kernel(Problem pr, const T *__restric
       float acc[4][4];
       zero_acc(acc);
       gemm_tile<true, true>(acc, ti * kTile, Q, tp * kTile, P, 0, min(Q, (ti + 1) * kTile), fa1, fb1, smem);
-      if (id.c > 0) gemm_tile<true, false>(acc, ti * kTile, Q, tp * kTile, P, 0, N, fa2, fb2, smem);
+      if (chunk_has_incoming(pr, id.c)) gemm_tile<true, false>(acc, ti * kTile, Q, tp * kTile, P, 0, N, fa2, fb2, smem);
       for_tile(acc, ti * kTile, Q, tp * kTile, P, [&](int i, int p, float x) {
         yb[(size_t)i * HP + p] = from_f<T>(x + Dh * to_f(ub[(size_t)i * Cd + offX + p]));
       });
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(256) dcdb_kernel(Problem pr, const T *__restri
       for (int tq = 0; tq * kTile < N; ++tq) {
         float acc[4][4], prod[4][4];
         zero_acc(acc);
-        if (id.c > 0) gemm_tile<true, true>(acc, ti * kTile, Q, tq * kTile, N, 0, P, fa2, fb2, smem);
+        if (chunk_has_incoming(pr, id.c)) gemm_tile<true, true>(acc, ti * kTile, Q, tq * kTile, N, 0, P, fa2, fb2, smem);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll

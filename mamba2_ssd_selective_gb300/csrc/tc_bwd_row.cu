@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm + kSmDY + vb * 16384 + r * 8192, &tm_dy, &bar.dy_full[vb], h * pr.P,
                         row0 + 128 * o.I + 64 * r);
           ++ndy;
-          if (o.c > 0) {  // S_in first: a whole head of slack before its use
+          if (chunk_has_incoming(pr, o.c)) {  // S_in first: a whole head of slack before its use
             const int sb = ns & 1;
             if (ns >= 2 && !mbar_wait(&bar.s_free[sb], parity(ns / 2 - 1), status)) {
               ok = false;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++na;
           }
           k += nsl;
-          if (o.c > 0) {
+          if (chunk_has_incoming(pr, o.c)) {
             const int sb = ns & 1;
             const uint64_t dSb = dS + sb * (16384 / 16);
             mbar_wait(&bar.s_full[sb], parity(ns / 2), status);
@@ -380,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           start_i = i;
           while (start_i > 0 && pipe::lds_i(vseq + 4 * (start_i - 1)) == si) --start_i;
         }
-        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(vseq - 4);
-        const float em = (o.c > 0 && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
+        const bool inc = chunk_has_incoming(pr, o.c);
+        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(o.c > 0 ? vseq - 4 : vseq);
+        const float em = (inc && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
         if (tt < pr.Q) {
           const float acs_j = pipe::lds_f(vacs + 4 * tt), dt_j = pipe::lds_f(vdt + 4 * tt);
           const float a = acs_j * kLog2e;
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pipe::warp_arrive(&bar.a_full[as]);
           ++na;
         }
-        if (o.c > 0) {  // em_i dy_i, the A operand of the S_in term of dC
+        if (inc) {  // em_i dy_i, the A operand of the S_in term of dC
           mbar_wait(&bar.dy_full[vb], parity(nh / 2), status);
           const int as = na % kNA;
           if (na >= (uint32_t)kNA) mbar_wait(&bar.a_free[as], parity(na / kNA - 1), status);
@@ -497,12 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = o.h0 + hh, vb = nh & 1;
         mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
         const uint32_t vacs = sV + vb * kVecStride, vseq = vacs + 2048 + 16;
-        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(vseq - 4);
-        const float em = (o.c > 0 && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
+        const bool inc = chunk_has_incoming(pr, o.c);
+        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(o.c > 0 ? vseq - 4 : vseq);
+        const float em = (inc && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
         pipe::warp_arrive(&bar.vec_free[vb]);
         float r = 0.f;
         mbar_wait(&bar.dy_full[vb], parity(nh / 2), status);  // dy row i from the head's tile
-        if (o.c > 0) {
+        if (inc) {
           const uint32_t T = sDY + vb * 16384;
           mbar_wait(bar.yo_full, parity(ny), status);
           tc_fence_after();

@@ -6,7 +6,8 @@
 // group).  Per unit the tensor cores first form CB = C_I B^T (K = dstate) into
 // tensor memory, once for all HB heads; then per head
 //   Yd  = A_h X_h,   A_h[i, j] = CB[i, j] exp(Acs_i - Acs_j) dt_j [j <= i, same sequence]
-//   Yo  = C_I S_in,h^T
+//   Yo  = C_I S_in,h^T       (every chunk that receives a state: all but a row's
+//                            first, and that one too when the row has an initial state)
 //   y_i = Yd_i + em_i Yo_i + D_h x_i.
 // Roles (22 warps, one CTA per SM):
 //   warp 0      TMA producer: C/B tiles per unit, per head the chunk vectors
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pipe::bulk_load(vec + 2048 + 16, pr.seq_idx + (size_t)o.bb * pr.L + t0, seq_bytes, &bar.vec_full[vb]);
           }
           ++nh;
-          if (o.c > 0) {
+          if (chunk_has_incoming(pr, o.c)) {
             const int sb = ns % kNSB;
             if (ns >= kNSB && !mbar_wait(&bar.s_free[sb], parity(ns / kNSB - 1), status)) {
               ok = false;
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&bar.a_free[as]);
             umma_commit(&bar.x_free[xs]);
           }
-          if (o.c > 0) {
+          if (chunk_has_incoming(pr, o.c)) {
             const int sb = ns % kNSB;
             mbar_wait(&bar.s_full[sb], parity(ns / kNSB), status);
             tc_fence_after();
@@ -443,14 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int i = 128 * o.I + il, t = o.c * pr.Q + i;
-      const bool has_off = o.c > 0;
+      const bool has_off = chunk_has_incoming(pr, o.c);
       const bf16 *xrow = u + ((size_t)o.bb * pr.L + t) * Cd;
       bf16 *yrow = y + ((size_t)o.bb * pr.L + t) * HP;
       for (int hh = 0; hh < HB; ++hh, ++nh) {
         const int h = o.h0 + hh, vb = nh & 1, ab = nh & 1;
         mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
         const uint32_t vacs = sV + vb * kVecStride, vseq = vacs + 2048 + 16;
-        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(vseq - 4);
+        // row i continues the state entering the chunk (the sequence before it,
+        // or in a row's first chunk the first sequence, which takes the initial state)
+        const bool cont = !has_seq || pipe::lds_i(vseq + 4 * i) == pipe::lds_i(o.c > 0 ? vseq - 4 : vseq);
         const float em = (has_off && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
         pipe::warp_arrive(&bar.vec_free[vb]);
         const float Dh = __ldg(pr.D + h);

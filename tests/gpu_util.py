@@ -98,6 +98,8 @@ def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=N
             "dA_log": rel(got["dA_log"][h0:h1], ref["dA_log"]),
             "dD": rel(got["dD"][h0:h1], ref["dD"]),
         })
+    if ref.get("dinit") is not None:
+        errs["dinit"] = rel(got["dinit"][rows][:, h0:h1], ref["dinit"])
     for k, e in errs.items():
         bound = ddt_bias_tol(floor_case, tol) if k == "ddt_bias" else tol
         assert k in REPORT_ONLY or e <= bound, (k, e, bound, errs)

@@ -7,7 +7,9 @@ oracle on samples it can compute: whole batch rows, or whole groups of heads
   mamba2-1b-fwdbwd  same shape, forward + backward, all rows, all heads
   long-131k         b1 L131072 H64 G8, segment count swept over 1..16: heads 0-7
                     (group 0) against one unsegmented oracle run (invariance)
-  packed-32k        b1 T32768 H48 G1, packed sequences, forward + backward, all heads
+  packed-32k        b1 T32768 H48 G1, packed sequences, forward + backward, all heads;
+                    and again from a random initial state, with every sequence's
+                    final state (ssd_forward_varlen) and the initial state's gradient
 """
 from __future__ import annotations
 
@@ -94,3 +96,23 @@ def test_packed_32k(oracle_lib):
     errs = compare_forward(got, oracle_lib.forward(inp, shape), TOL[dtype])
     gerrs = compare_backward(g, oracle_lib.backward(inp, shape, use_dfinal=False), shape, TOL[dtype])
     print("packed-32k", errs, gerrs)
+
+
+def test_packed_32k_initial_state_and_sequence_finals(oracle_lib):
+    shape, dtype, seed = WORKLOADS["packed-32k"]
+    inp = make_inputs(shape, seed, dtype, init_states=True)
+    r = ssd.SsdRunner(shape, dtype)
+    t = to_dev(inp)
+    y, fin, seg, sf = r.forward_varlen(t)
+    g = r.backward(t, t["dy"], None, seg)
+    torch.cuda.synchronize()
+    got = {"y": np_(y).reshape(1, shape.seqlen, shape.nheads, shape.headdim), "final_state": np_(fin),
+           "seg_in": np_(seg)}
+    errs = compare_forward(got, oracle_lib.forward(inp, shape), TOL[dtype])
+    fins = oracle_lib.seq_finals(inp, shape)
+    errs["seq_finals"] = float(np.linalg.norm(np_(sf) - fins) / np.linalg.norm(fins))
+    assert errs["seq_finals"] <= TOL[dtype]
+    gerrs = compare_backward({k: np_(v) for k, v in g.items()}, oracle_lib.backward(inp, shape, use_dfinal=False),
+                             shape, TOL[dtype])
+    assert "dinit" in gerrs
+    print("packed-32k init", errs, gerrs)

@@ -1,10 +1,11 @@
 """GPU parity: libssd through its C ABI against the fp64 oracle (relative L2).
 
 Tolerances: 1e-4 for the fp32 path, 1e-2 for bf16 activations with fp32
-accumulation.  Shapes span several chunk tiles, partial tiles (chunk 96,
+accumulation (ddt_bias in three named small cases: see tests/gpu_util.py).  Shapes span several chunk tiles, partial tiles (chunk 96,
 headdim 32, dstate 40), group mapping (G > 1), packed sequences with edge
 cases (a boundary at a chunk start, at a segment start, sequences of 1-3
-tokens and sequences shorter than a chunk), every segment count 1..16, and the
+tokens and sequences shorter than a chunk), every segment count 1..16, initial
+states with their gradient, per-sequence final states of packed rows, and the
 bitwise replay the pages require of summaries, scans and outputs.
 """
 from __future__ import annotations
@@ -15,7 +16,7 @@ import torch
 
 import mamba2_ssd_selective_gb300 as ssd
 from mamba2_ssd_selective_gb300.inputs import WORKLOADS, SsdShape, make_inputs
-from tests.gpu_util import TOL, compare_backward, compare_forward, gpu_backward, gpu_forward, rel, to_dev
+from tests.gpu_util import TOL, compare_backward, compare_forward, gpu_backward, gpu_forward, np_, rel, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -126,6 +127,58 @@ def test_reads_the_in_projection_output_in_place(oracle_lib):
     out = {"dxBC": dbuf[..., HP:HP + Cd].float().cpu().numpy(), "ddt_raw": dbuf[..., HP + Cd:].float().cpu().numpy()}
     out.update({k: g[k].float().cpu().numpy() for k in ("ddt_bias", "dA_log", "dD", "dconv_w", "dconv_b")})
     compare_backward(out, oracle_lib.backward(inp, shape), shape, TOL["bf16"])
+
+
+INIT_SHAPES = [
+    (SsdShape(2, 1024, 8, 64, 128, 2, 256, 2), None),
+    (SsdShape(1, 768, 4, 64, 64, 1, 96, 4), [70, 3, 695]),
+    # the tensor-core path with 128-token chunks: the first sequence ends inside chunk 0
+    (SsdShape(1, 1024, 4, 64, 128, 1, 128, 4), [100, 5, 919]),
+    (SsdShape(1, 2048, 4, 64, 128, 1, 256, 8), [1300, 748]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape,seq", INIT_SHAPES)
+def test_initial_states_forward_backward(oracle_lib, shape, seq, dtype):
+    """Each row starts from its own initial state; with packed rows only the
+    first sequence does.  The gradient of the initial states comes from the
+    reverse segment scan carried one step past the first segment."""
+    inp = make_inputs(shape, 19, dtype, dfinal=True, seq_lengths=seq, init_states=True)
+    got, _ = gpu_forward(shape, dtype, inp)
+    ref = oracle_lib.forward(inp, shape)
+    compare_forward(got, ref, TOL[dtype])
+    assert np.array_equal(got["seg_in"][:, 0], inp["init"].numpy())  # the scan starts from it
+    g = gpu_backward(shape, dtype, inp)
+    errs = compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
+    assert "dinit" in errs
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("init", [False, True])
+def test_varlen_sequence_final_states(oracle_lib, dtype, init):
+    """ssd_forward_varlen: the state after every packed sequence's last token,
+    including sequences of 1-3 tokens, one ending on a chunk's last token and one
+    inside the row's first chunk."""
+    lens = [200, 56, 1, 2, 3, 250, 512, 1000, 24]
+    shape = SsdShape(1, sum(lens), 4, 64, 128, 1, 256, 4)
+    inp = make_inputs(shape, 20, dtype, seq_lengths=lens, init_states=init)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    r = ssd.SsdRunner(shape, dtype)
+    t = to_dev(inp)
+    t["cu_seqlens"] = cu.cuda()
+    y, fin, seg, sf = r.forward_varlen(t)
+    torch.cuda.synchronize()
+    ref = oracle_lib.forward(inp, shape)
+    got = {"y": np_(y).reshape(1, shape.seqlen, shape.nheads, shape.headdim), "final_state": np_(fin),
+           "seg_in": np_(seg)}
+    compare_forward(got, ref, TOL[dtype])
+    fins = oracle_lib.seq_finals(inp, shape)
+    assert rel(np_(sf), fins) <= TOL[dtype]
+    for q in range(len(lens)):
+        assert rel(np_(sf[q]), fins[q]) <= 2 * TOL[dtype], q
+    # the row's last sequence ends at the row's last token: its state is the final state
+    assert rel(np_(sf[-1]), np_(fin)[0]) <= TOL[dtype]
 
 
 def test_backward_recomputes_segment_states(oracle_lib):
