@@ -16,7 +16,8 @@ benchmarks, which time the mixer core on random post-projection activations):
 
 Draw order from ``numpy.random.default_rng(seed)`` (PCG64), all in float32:
 x, B, C, dt_raw, dt_bias, A_log, D, conv_w, [sequence lengths], dy, [dfinal],
-[initial states ~ N(0, 1), (batch, H, P, N)].
+[initial states ~ N(0, 1), (batch, H, P, N)], [the gate z ~ N(0, 1), (batch, L, H*P),
+then the norm weight ~ U(0.5, 1.5), (H*P)]; the norm's eps is 1e-5.
 Activations are then rounded to the activation dtype (round to nearest even);
 parameters stay float32.
 """
@@ -82,14 +83,15 @@ def seq_idx_from_lengths(lengths: list[int]) -> np.ndarray:
 
 
 def make_inputs(shape: SsdShape, seed: int, dtype: str = "bf16", *, dfinal: bool = False,
-                seq_lengths: list[int] | None = None, init_states: bool = False) -> dict:
+                seq_lengths: list[int] | None = None, init_states: bool = False, gated_norm: bool = False) -> dict:
     """Return a dict of CPU tensors.
 
     ``xBC`` is one (batch, seqlen, conv_dim) activation buffer with channels
     [x (H*P) | B (G*N) | C (G*N)], the layout the in-projection produces; x, B and C
     are token-strided views into it.  ``seq_idx`` is None unless the shape is packed or
     ``seq_lengths`` (per batch row, summing to seqlen) is given.  ``init`` (each
-    row's initial state, fp32) is None unless ``init_states``.
+    row's initial state, fp32) is None unless ``init_states``; ``z`` (the gate,
+    activation dtype) and ``norm_weight`` are None unless ``gated_norm``.
     """
     rng = np.random.default_rng(seed)
     b, L, H, P, N, G = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups
@@ -121,6 +123,8 @@ def make_inputs(shape: SsdShape, seed: int, dtype: str = "bf16", *, dfinal: bool
     dy = rng.standard_normal((b, L, H * P), dtype=f32)
     df = rng.standard_normal((b, H, P, N), dtype=f32) if dfinal else np.zeros((b, H, P, N), f32)
     h0 = rng.standard_normal((b, H, P, N), dtype=f32) if init_states else None
+    z = rng.standard_normal((b, L, H * P), dtype=f32) if gated_norm else None
+    nw = rng.uniform(0.5, 1.5, size=H * P).astype(f32) if gated_norm else None
 
     tdt = TORCH_DTYPES[dtype]
     xBC = torch.from_numpy(np.concatenate([x, Bm, Cm], axis=-1)).to(tdt).contiguous()
@@ -137,5 +141,8 @@ def make_inputs(shape: SsdShape, seed: int, dtype: str = "bf16", *, dfinal: bool
         "dy": torch.from_numpy(dy).to(tdt).contiguous(),
         "dfinal": torch.from_numpy(df),
         "init": None if h0 is None else torch.from_numpy(h0),
+        "z": None if z is None else torch.from_numpy(z).to(tdt).contiguous(),
+        "norm_weight": None if nw is None else torch.from_numpy(nw),
+        "norm_eps": 1e-5,
     }
     return out

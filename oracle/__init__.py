@@ -70,6 +70,11 @@ def _load():
             lib.orc_seq_finals.restype = I
             lib.orc_num_seqs.argtypes = [ctypes.POINTER(_Row)]
             lib.orc_num_seqs.restype = I
+            D = ctypes.c_double
+            lib.orc_gated_norm_fwd.argtypes = [I, I, I, P, P, P, D, P]
+            lib.orc_gated_norm_fwd.restype = I
+            lib.orc_gated_norm_bwd.argtypes = [I, I, I, P, P, P, D, P, P, P, P]
+            lib.orc_gated_norm_bwd.restype = I
             _lib = lib
     return _lib
 
@@ -131,11 +136,48 @@ def conv(inp: dict, shape, b: int = 0, heads: tuple | None = None, nthreads: int
     return u.T.copy(), v.T.copy(), ch
 
 
+def gated_norm(y: np.ndarray, z: np.ndarray, w: np.ndarray, ngroups: int, eps: float) -> np.ndarray:
+    """Gated RMSNorm of one or more rows: y, z (rows, L, C), w (C) -> out (rows, L, C)."""
+    lib = _load()
+    y, z, w = _f64(y), _f64(z), _f64(w)
+    out = np.empty_like(y)
+    for r in range(y.shape[0]):
+        if lib.orc_gated_norm_fwd(y.shape[1], y.shape[2], ngroups, _ptr(y[r]), _ptr(z[r]), _ptr(w), eps,
+                                  _ptr(out[r])) != 0:
+            raise ValueError("oracle gated_norm rejected its arguments")
+    return out
+
+
+def gated_norm_backward(y, z, w, ngroups: int, eps: float, dout) -> tuple:
+    """(dy, dz, dw) of the gated RMSNorm given dout; dw summed over rows in row order."""
+    lib = _load()
+    y, z, w, dout = _f64(y), _f64(z), _f64(w), _f64(dout)
+    dy, dz = np.empty_like(y), np.empty_like(y)
+    dw = np.zeros_like(w)
+    for r in range(y.shape[0]):
+        if lib.orc_gated_norm_bwd(y.shape[1], y.shape[2], ngroups, _ptr(y[r]), _ptr(z[r]), _ptr(w), eps,
+                                  _ptr(dout[r]), _ptr(dy[r]), _ptr(dz[r]), _ptr(dw)) != 0:
+            raise ValueError("oracle gated_norm_backward rejected its arguments")
+    return dy, dz, dw
+
+
+def _norm_slices(inp: dict, shape, h0: int, h1: int, rows: list):
+    """z and the norm weight of heads [h0, h1) (whole groups) and the groups they cover."""
+    hpg, P = shape.nheads // shape.ngroups, shape.headdim
+    if h0 % hpg or h1 % hpg:
+        raise ValueError("the gated norm needs whole groups of heads")
+    z = _f64(inp["z"])[rows][..., h0 * P:h1 * P]
+    w = _f64(inp["norm_weight"])[h0 * P:h1 * P]
+    return z, w, (h1 - h0) // hpg
+
+
 def forward(inp: dict, shape, n_segments: int | None = None, heads: tuple | None = None,
             rows: list | None = None, nthreads: int = 0) -> dict:
     """y (rows, L, nh, P), final_state (rows, nh, P, N) and, for S > 1, the
     segment summaries: seg_in / s_ext (rows, S, nh, P, N), a_block (rows, S, nh).
-    inp["init"] (b, H, P, N), when present, is each row's initial state."""
+    inp["init"] (b, H, P, N), when present, is each row's initial state.  With
+    inp["z"] present, y is the gated RMSNorm of the mixer output (norm_weight,
+    norm_eps) and the output before the norm is returned as y_pre."""
     lib = _load()
     S = shape.n_segments if n_segments is None else n_segments
     h0, h1 = heads or (0, shape.nheads)
@@ -156,13 +198,21 @@ def forward(inp: dict, shape, n_segments: int | None = None, heads: tuple | None
             raise ValueError("oracle forward rejected its arguments")
         for k, v in zip(out, (y, fin, seg_in, s_ext, a_blk)):
             out[k].append(v)
-    return {k: np.stack(v) for k, v in out.items()}
+    res = {k: np.stack(v) for k, v in out.items()}
+    if inp.get("z") is not None:
+        z, w, ng = _norm_slices(inp, shape, h0, h1, rows)
+        res["y_pre"] = res["y"]
+        nr = len(rows)
+        res["y"] = gated_norm(res["y"].reshape(nr, L, nh * P), z, w, ng, float(inp["norm_eps"])).reshape(nr, L, nh, P)
+    return res
 
 
 def backward(inp: dict, shape, heads: tuple | None = None, rows: list | None = None,
              use_dfinal: bool = True, nthreads: int = 0) -> dict:
     """Gradients of L = <dy, y> + <dfinal, final_state> w.r.t. every input
-    (with inp["init"] present, also w.r.t. each row's initial state: dinit).
+    (with inp["init"] present, also w.r.t. each row's initial state: dinit;
+    with inp["z"] present y is the gated norm's output, and dz (rows, L, nh*P)
+    and dnorm_weight (nh*P) are returned too).
 
     For heads=(h0,h1) covering whole groups the results are exact for those heads'
     x channels / dt columns and their groups' B/C channels.  Returns float64:
@@ -175,6 +225,17 @@ def backward(inp: dict, shape, heads: tuple | None = None, rows: list | None = N
     nh = h1 - h0
     rows = list(range(shape.batch)) if rows is None else list(rows)
     L = shape.seqlen
+    P = shape.headdim
+    norm = None
+    if inp.get("z") is not None:
+        # the gated norm's backward turns dout into the mixer output's gradient
+        # (every head of the row: the mixer's backward reads dy of all heads)
+        y_pre = forward(inp, shape, n_segments=1, rows=rows, nthreads=nthreads)["y_pre"]
+        nr = len(rows)
+        z, w, ng = _norm_slices(inp, shape, 0, shape.nheads, rows)
+        dout = _f64(inp["dy"])[rows]
+        dyn, dzn, dwn = gated_norm_backward(y_pre.reshape(nr, L, -1), z, w, ng, float(inp["norm_eps"]), dout)
+        norm = {"dy": dyn, "dz": dzn[..., h0 * P:h1 * P], "dnorm_weight": dwn[h0 * P:h1 * P]}
     dxs, ddts, dinits = [], [], []
     acc = None
     ch = None
@@ -183,7 +244,7 @@ def backward(inp: dict, shape, heads: tuple | None = None, rows: list | None = N
         nsub = lib.orc_subset_size(ctypes.byref(ra.row), h0, h1)
         if ch is None:
             ch = np.array([lib.orc_subset_channel(ctypes.byref(ra.row), h0, h1, j) for j in range(nsub)])
-        dy = _f64(inp["dy"][b])
+        dy = _f64(inp["dy"][b]) if norm is None else np.ascontiguousarray(norm["dy"][rows.index(b)])
         dfin = _f64(inp["dfinal"][b]) if use_dfinal and inp.get("dfinal") is not None else None
         dxr = np.empty((L, nsub))
         dw = np.empty((nsub, 4))
@@ -206,6 +267,8 @@ def backward(inp: dict, shape, heads: tuple | None = None, rows: list | None = N
         "dxBC": np.stack(dxs), "channels": ch, "ddt_raw": np.stack(ddts),
         "dconv_w": acc[0], "dconv_b": acc[1], "ddt_bias": acc[2], "dA_log": acc[3], "dD": acc[4],
         "dinit": None if dinits[0] is None else np.stack(dinits),
+        "dz": None if norm is None else norm["dz"],
+        "dnorm_weight": None if norm is None else norm["dnorm_weight"],
     }
 
 

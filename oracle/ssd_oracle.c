@@ -646,3 +646,68 @@ int orc_seq_finals(const orc_row *r, int h0, int h1, double *out, int nthreads) 
   free(u);
   return c.nseq;
 }
+
+/* ------------------------------------------------------------------ */
+/* gated RMSNorm after the mixer core                                   */
+/*
+ * The Mamba2 block normalises the mixer output gated by z before its output
+ * projection; the Megatron-LM PR keeps this step outside its fused function
+ * ("Add state-passing context parallelism for Mamba2", description).  The
+ * reading taken (Mamba2's gated RMSNorm, gate applied before the norm, one
+ * norm group per B/C group of heads):
+ *     g_c   = y_c * silu(z_c)
+ *     r     = 1 / sqrt(mean_{c in group} g_c^2 + eps)
+ *     out_c = g_c * r * w_c
+ * For one row of L tokens, HP = H*P channels, G groups of HP/G channels.
+ */
+int orc_gated_norm_fwd(int L, int HP, int G, const double *y, const double *z, const double *w, double eps,
+                       double *out) {
+  if (L <= 0 || HP <= 0 || G <= 0 || HP % G != 0) return -1;
+  int gs = HP / G;
+  for (int t = 0; t < L; ++t)
+    for (int g = 0; g < G; ++g) {
+      const double *yt = y + (size_t)t * HP + (size_t)g * gs, *zt = z + (size_t)t * HP + (size_t)g * gs;
+      double ss = 0.0;
+      for (int c = 0; c < gs; ++c) {
+        double gc = yt[c] * zt[c] * sigmoid(zt[c]);
+        ss += gc * gc;
+      }
+      double r = 1.0 / sqrt(ss / gs + eps);
+      for (int c = 0; c < gs; ++c) {
+        double gc = yt[c] * zt[c] * sigmoid(zt[c]);
+        out[(size_t)t * HP + (size_t)g * gs + c] = gc * r * w[(size_t)g * gs + c];
+      }
+    }
+  return 0;
+}
+
+/* Backward of the gated RMSNorm for one row, given dout:
+ *     dg_c = r w_c dout_c - g_c r^3 mean_{k in group}(w_k dout_k g_k)
+ *     dy_c = dg_c silu(z_c),   dz_c = dg_c y_c silu'(z_c),
+ *     dw_c += sum_t dout_c g_c r        (accumulated into dw). */
+int orc_gated_norm_bwd(int L, int HP, int G, const double *y, const double *z, const double *w, double eps,
+                       const double *dout, double *dy, double *dz, double *dw) {
+  if (L <= 0 || HP <= 0 || G <= 0 || HP % G != 0) return -1;
+  int gs = HP / G;
+  for (int t = 0; t < L; ++t)
+    for (int g = 0; g < G; ++g) {
+      size_t o = (size_t)t * HP + (size_t)g * gs;
+      double ss = 0.0, wdg = 0.0;
+      for (int c = 0; c < gs; ++c) {
+        double gc = y[o + c] * z[o + c] * sigmoid(z[o + c]);
+        ss += gc * gc;
+        wdg += w[(size_t)g * gs + c] * dout[o + c] * gc;
+      }
+      double r = 1.0 / sqrt(ss / gs + eps);
+      double m = wdg / gs;
+      for (int c = 0; c < gs; ++c) {
+        double zc = z[o + c], sg = sigmoid(zc), s = zc * sg;
+        double gc = y[o + c] * s;
+        double dg = r * w[(size_t)g * gs + c] * dout[o + c] - gc * r * r * r * m;
+        dy[o + c] = dg * s;
+        dz[o + c] = dg * y[o + c] * sg * (1.0 + zc * (1.0 - sg));
+        dw[(size_t)g * gs + c] += dout[o + c] * gc * r;
+      }
+    }
+  return 0;
+}

@@ -19,7 +19,12 @@ independent formulation, a special case or an invariant the pages state:
   the second part started from the first part's final state, gives the uncut
   row's outputs and final state;
 * the backward equals central finite differences of the forward in every input,
-  the initial state included.
+  the initial state included;
+* the gated RMSNorm after the mixer (kept outside the fused function by the
+  Megatron-LM PR; Mamba2's gated norm, one norm group per B/C group): equal to
+  torch's rms_norm of y * silu(z) per group (library routines), unit RMS per
+  group with eps = 0 and unit weight, and its backward -- alone and through the
+  whole path -- equal to central finite differences.
 """
 from __future__ import annotations
 
@@ -254,9 +259,12 @@ def _loss(oracle_lib, inp, shape):
     # with initial states: every input and the initial state itself
     (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), None, True),
     (SsdShape(1, 300, 2, 4, 3, 1, 8, 1), [260, 1, 39], True),
+    # the whole path through the gated norm: also z and the norm weight
+    (SsdShape(2, 40, 4, 3, 5, 2, 8, 1), [15, 25], "norm"),
 ])
 def test_backward_matches_finite_differences(oracle_lib, shape, seq, init):
-    inp = f64(make_inputs(shape, 23, "f32", dfinal=True, seq_lengths=seq, init_states=init))
+    norm = init == "norm"
+    inp = f64(make_inputs(shape, 23, "f32", dfinal=True, seq_lengths=seq, init_states=init is True, gated_norm=norm))
     g = oracle_lib.backward(inp, shape, nthreads=1)
     dxBC = np.zeros((shape.batch, shape.seqlen, shape.conv_dim))
     dxBC[..., g["channels"]] = g["dxBC"]
@@ -266,8 +274,11 @@ def test_backward_matches_finite_differences(oracle_lib, shape, seq, init):
     dconv_b[g["channels"]] = g["dconv_b"]
     grads = {"xBC": dxBC, "dt_raw": g["ddt_raw"], "dt_bias": g["ddt_bias"], "A_log": g["dA_log"], "D": g["dD"],
              "conv_w": dconv_w, "conv_b": dconv_b}
-    if init:
+    if init is True:
         grads["init"] = g["dinit"]
+    if norm:
+        grads["z"] = g["dz"]
+        grads["norm_weight"] = g["dnorm_weight"]
     rng = np.random.default_rng(0)
     HP, GN = shape.nheads * shape.headdim, shape.ngroups * shape.dstate
     parts = {"x": slice(0, HP), "B": slice(HP, HP + GN), "C": slice(HP + GN, HP + 2 * GN)}
@@ -285,3 +296,48 @@ def test_backward_matches_finite_differences(oracle_lib, shape, seq, init):
         fd = (_loss(oracle_lib, plus, shape) - _loss(oracle_lib, minus, shape)) / (2 * eps)
         an = float(np.sum(grads[name] * v))
         assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, part, fd, an)
+
+
+# ---------------------------------------------------------------- gated RMSNorm
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_gated_norm_equals_torch_rms_norm(oracle_lib, G):
+    rng = np.random.default_rng(31)
+    L, C = 50, 96
+    y, z = rng.standard_normal((2, L, C)), rng.standard_normal((2, L, C))
+    w = rng.uniform(0.5, 1.5, C)
+    out = oracle_lib.gated_norm(y, z, w, G, 1e-5)
+    g = torch.from_numpy(y) * torch.nn.functional.silu(torch.from_numpy(z))
+    ref = torch.nn.functional.rms_norm(g.reshape(2, L, G, C // G), (C // G,), eps=1e-5).reshape(2, L, C)
+    ref = ref * torch.from_numpy(w)
+    assert rel(out, ref.numpy()) < 1e-14
+
+
+def test_gated_norm_unit_rms_per_group(oracle_lib):
+    rng = np.random.default_rng(32)
+    L, C, G = 20, 64, 4
+    y, z = rng.standard_normal((1, L, C)) * 7.0, rng.standard_normal((1, L, C))
+    out = oracle_lib.gated_norm(y, z, np.ones(C), G, 0.0)
+    ms = np.mean(out.reshape(1, L, G, C // G) ** 2, axis=-1)
+    np.testing.assert_allclose(ms, 1.0, rtol=1e-13)
+    # and a scaled input gives the same output (the norm removes the scale)
+    assert rel(oracle_lib.gated_norm(3.5 * y, z, np.ones(C), G, 0.0), out) < 1e-14
+
+
+def test_gated_norm_backward_matches_finite_differences(oracle_lib):
+    rng = np.random.default_rng(33)
+    L, C, G, eps = 7, 24, 2, 1e-5
+    y, z = rng.standard_normal((2, L, C)), rng.standard_normal((2, L, C))
+    w, dout = rng.uniform(0.5, 1.5, C), rng.standard_normal((2, L, C))
+    dy, dz, dw = oracle_lib.gated_norm_backward(y, z, w, G, eps, dout)
+    loss = lambda yy, zz, ww: float(np.sum(dout * oracle_lib.gated_norm(yy, zz, ww, G, eps)))  # noqa: E731
+    h = 1e-6
+    for name, grad in (("y", dy), ("z", dz), ("w", dw)):
+        v = rng.standard_normal(grad.shape)
+        args_p = {"y": y, "z": z, "w": w}
+        args_m = dict(args_p)
+        args_p[name] = args_p[name] + h * v
+        args_m[name] = args_m[name] - h * v
+        fd = (loss(args_p["y"], args_p["z"], args_p["w"]) - loss(args_m["y"], args_m["z"], args_m["w"])) / (2 * h)
+        an = float(np.sum(grad * v))
+        assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, fd, an)
