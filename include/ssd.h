@@ -68,6 +68,8 @@ typedef struct {
   int32_t chunk;      /* Q: SSD chunk length */
   int32_t n_segments; /* S: equal causal segments; each must be a multiple of chunk */
   int32_t dtype;      /* ssd_dtype of the activations */
+  int32_t gated_norm; /* 1: y is the gated RMSNorm of the mixer output (needs z and
+                         norm_weight in ssd_inputs; at most 8192 channels per group), 0: none */
 } ssd_dims;
 
 /* Pre-conv activations as laid out by the in-projection (zero-copy views into
@@ -85,7 +87,15 @@ typedef struct {
  * Mamba2 chunked-scan convention; the pages list initial states as not
  * supported yet: "Add state-passing context parallelism for Mamba2", "Not
  * supported yet").  With packed rows it seeds the row's first sequence only;
- * later sequences start from zero.  The exclusive segment scan starts from it. */
+ * later sequences start from zero.  The exclusive segment scan starts from it.
+ * Gated RMSNorm (dims.gated_norm = 1; else z and norm_weight must be NULL): the
+ * step after the mixer core in a Mamba2 block, which the Megatron-LM PR keeps
+ * outside its fused function (description); Mamba2's gated norm with one norm
+ * group per B/C group of heads (H*P/G channels):
+ *     g = y * silu(z),   out = g * norm_weight / sqrt(mean_group(g^2) + norm_eps)
+ * z (b, L, H*P) activation dtype with its own token stride (a view into the
+ * zxBCdt buffer), 16-byte aligned, stride a multiple of 8 (bf16) or 4 (fp32)
+ * elements; norm_weight (H*P) fp32, 16-byte aligned; norm_eps >= 0. */
 typedef struct {
   const void *x;  int64_t x_tok_stride;
   const void *B;  int64_t B_tok_stride;
@@ -94,6 +104,9 @@ typedef struct {
   const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
   const int32_t *seq_idx;
   const float *initial_states;
+  const void *z;  int64_t z_tok_stride;
+  const float *norm_weight;
+  float norm_eps;
 } ssd_inputs;
 
 /* Gradients, written (not accumulated).  dx, dB, dC, ddt have the layout and
@@ -102,7 +115,9 @@ typedef struct {
  * dconv_b (Cd) are fp32 and summed over batch and tokens.  dinitial_states
  * (b, H, P, N) fp32, 16-byte aligned: the gradient of the initial states, the
  * reverse segment scan carried one step past the first segment; written only
- * when the inputs have initial_states, and may be NULL. */
+ * when the inputs have initial_states, and may be NULL.  With the gated norm:
+ * dz (layout rules of z, its own token stride) and dnorm_weight (H*P) fp32,
+ * both required. */
 typedef struct {
   void *dx;  int64_t dx_tok_stride;
   void *dB;  int64_t dB_tok_stride;
@@ -110,6 +125,8 @@ typedef struct {
   void *ddt; int64_t ddt_tok_stride;
   float *ddt_bias, *dA_log, *dD, *dconv_w, *dconv_b;
   float *dinitial_states;
+  void *dz;  int64_t dz_tok_stride;
+  float *dnorm_weight;
 } ssd_grads;
 
 /* Bytes of device workspace ssd_forward (backward = 0) or ssd_backward
@@ -117,7 +134,8 @@ typedef struct {
  * scratch: its contents need not survive between calls. */
 size_t ssd_workspace_size(const ssd_dims *dims, int backward);
 
-/* Forward.  y (b, L, H*P) activation dtype, contiguous; final_state (b, H, P, N)
+/* Forward.  y (b, L, H*P) activation dtype, contiguous (with the gated norm: its
+ * output; the mixer output itself is not written); final_state (b, H, P, N)
  * fp32 = the state after each row's last token (with packing: of the row's last
  * sequence), or NULL; seg_init_states (b, S, H, P, N) fp32 = each segment's true
  * initial state recovered by the exclusive scan (what ssd_backward may reuse),
@@ -140,7 +158,8 @@ ssd_status ssd_forward_varlen(const ssd_dims *dims, const ssd_inputs *in, void *
                               float *seg_init_states, const int32_t *cu_seqlens, int32_t nseq,
                               float *seq_final_states, void *workspace, size_t ws_bytes, ssd_stream_t stream);
 
-/* Backward of  L = <dy, y> + <dfinal_state, final_state>.
+/* Backward of  L = <dy, y> + <dfinal_state, final_state>  (y the forward's output:
+ * with the gated norm, the normalised output; the mixer output is recomputed).
  * dy (b, L, H*P) activation dtype, contiguous; dfinal_state (b, H, P, N) fp32 or
  * NULL (zero); seg_init_states from ssd_forward on the same inputs, or NULL to
  * have them recomputed.  Everything that scales with L is recomputed. */

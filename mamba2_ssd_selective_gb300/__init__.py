@@ -37,7 +37,8 @@ class SsdError(RuntimeError):
 
 class SsdDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
-        "batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "d_conv", "chunk", "n_segments", "dtype")]
+        "batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "d_conv", "chunk", "n_segments", "dtype",
+        "gated_norm")]
 
 
 class SsdInputs(ctypes.Structure):
@@ -49,6 +50,8 @@ class SsdInputs(ctypes.Structure):
         ("dt_bias", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("D", ctypes.c_void_p),
         ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p), ("seq_idx", ctypes.c_void_p),
         ("initial_states", ctypes.c_void_p),
+        ("z", ctypes.c_void_p), ("z_tok_stride", ctypes.c_int64), ("norm_weight", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_float),
     ]
 
 
@@ -60,6 +63,7 @@ class SsdGrads(ctypes.Structure):
         ("ddt", ctypes.c_void_p), ("ddt_tok_stride", ctypes.c_int64),
         ("ddt_bias", ctypes.c_void_p), ("dA_log", ctypes.c_void_p), ("dD", ctypes.c_void_p),
         ("dconv_w", ctypes.c_void_p), ("dconv_b", ctypes.c_void_p), ("dinitial_states", ctypes.c_void_p),
+        ("dz", ctypes.c_void_p), ("dz_tok_stride", ctypes.c_int64), ("dnorm_weight", ctypes.c_void_p),
     ]
 
 
@@ -202,9 +206,10 @@ def ssd_profile_end(max_entries: int = 64) -> list[tuple[str, int, float]]:
 
 # ---------------------------------------------------------------- marshalling helpers
 
-def make_dims(shape, dtype: str) -> SsdDims:
+def make_dims(shape, dtype: str, gated_norm: bool = False) -> SsdDims:
     return SsdDims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
-                   shape.d_conv, shape.chunk, shape.n_segments, SSD_BF16 if dtype == "bf16" else SSD_F32)
+                   shape.d_conv, shape.chunk, shape.n_segments, SSD_BF16 if dtype == "bf16" else SSD_F32,
+                   int(bool(gated_norm)))
 
 
 class SsdRunner:
@@ -212,11 +217,12 @@ class SsdRunner:
 
     ``t`` is a dict of device tensors as produced by ``inputs.make_inputs`` (moved
     to the GPU): xBC (b, L, Cd) with x, B, C as token-strided views, dt_raw,
-    parameters and optional seq_idx."""
+    parameters and optional seq_idx, init, z / norm_weight (gated_norm=True)."""
 
-    def __init__(self, shape, dtype: str, device="cuda"):
+    def __init__(self, shape, dtype: str, device="cuda", gated_norm: bool = False):
         self.shape, self.dtype, self.device = shape, dtype, torch.device(device)
-        self.dims = make_dims(shape, dtype)
+        self.gated_norm = gated_norm
+        self.dims = make_dims(shape, dtype, gated_norm)
         self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
         self.ws_fwd = ssd_workspace_size(self.dims, False)
         self.ws_bwd = ssd_workspace_size(self.dims, True)
@@ -232,7 +238,10 @@ class SsdRunner:
         base = xBC.data_ptr()
         return SsdInputs(base, Cd, base + HP * es, Cd, base + (HP + GN) * es, Cd, t["dt_raw"].data_ptr(), s.nheads,
                          _ptr(t["dt_bias"]), _ptr(t["A_log"]), _ptr(t["D"]), _ptr(t["conv_w"]), _ptr(t["conv_b"]),
-                         _ptr(t.get("seq_idx")), _ptr(t.get("init")))
+                         _ptr(t.get("seq_idx")), _ptr(t.get("init")),
+                         _ptr(t.get("z")) if self.gated_norm else None, s.nheads * s.headdim,
+                         _ptr(t.get("norm_weight")) if self.gated_norm else None,
+                         float(t.get("norm_eps", 1e-5)))
 
     def alloc_outputs(self):
         s = self.shape
@@ -255,6 +264,9 @@ class SsdRunner:
         }
         if init:
             g["dinit"] = torch.empty(s.batch, s.nheads, s.headdim, s.dstate, dtype=torch.float32, device=self.device)
+        if self.gated_norm:
+            g["dz"] = torch.empty(s.batch, s.seqlen, s.nheads * s.headdim, dtype=self.tdtype, device=self.device)
+            g["dnorm_weight"] = torch.empty(s.nheads * s.headdim, dtype=torch.float32, device=self.device)
         return g
 
     def grads_struct(self, g: dict) -> SsdGrads:
@@ -265,7 +277,8 @@ class SsdRunner:
         base = d.data_ptr()
         return SsdGrads(base, Cd, base + HP * es, Cd, base + (HP + GN) * es, Cd, g["ddt_raw"].data_ptr(), s.nheads,
                         _ptr(g["ddt_bias"]), _ptr(g["dA_log"]), _ptr(g["dD"]), _ptr(g["dconv_w"]),
-                        _ptr(g["dconv_b"]), _ptr(g.get("dinit")))
+                        _ptr(g["dconv_b"]), _ptr(g.get("dinit")), _ptr(g.get("dz")), s.nheads * s.headdim,
+                        _ptr(g.get("dnorm_weight")))
 
     def forward_varlen(self, t: dict, out=None, stream=None):
         """Forward of a packed row (t["cu_seqlens"], t["seq_idx"]); returns y,

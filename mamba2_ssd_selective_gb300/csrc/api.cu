@@ -33,6 +33,9 @@ ssd_status check_dims(const ssd_dims *d) {
   if ((long long)d->batch * d->seqlen > (1LL << 30) || (long long)d->nheads * d->headdim > (1 << 16) ||
       (long long)d->ngroups * d->dstate > (1 << 16))
     return SSD_ERR_UNSUPPORTED;
+  if (d->gated_norm != 0 && d->gated_norm != 1) return SSD_ERR_INVALID_DIMS;
+  // the norm kernels hold a group's channels in registers: up to 8192 per group
+  if (d->gated_norm && (long long)d->nheads * d->headdim / d->ngroups > 8192) return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
 }
 
@@ -72,6 +75,14 @@ ssd_status check_inputs(const ssd_dims *d, const ssd_inputs *in, Problem &pr) {
       !aligned(in->conv_b, 4) || (in->seq_idx && !aligned(in->seq_idx, 4)) ||
       (in->initial_states && !aligned(in->initial_states, 16)))
     return SSD_ERR_ALIGNMENT;
+  // the gated norm: z and its weight exactly when dims ask for it
+  if (d->gated_norm) {
+    if (!in->z || !in->norm_weight) return SSD_ERR_NULL_PTR;
+    if (in->z_tok_stride < HP || !(in->norm_eps >= 0.f) || in->norm_eps > 1e30f) return SSD_ERR_INVALID_DIMS;
+    if (!aligned(in->z, 16) || in->z_tok_stride % vec || !aligned(in->norm_weight, 16)) return SSD_ERR_ALIGNMENT;
+  } else if (in->z || in->norm_weight) {
+    return SSD_ERR_INVALID_DIMS;  // a gate given without dims.gated_norm would be ignored: rejected instead
+  }
   pr = problem_from(d);
   pr.x = in->x;
   pr.B = in->B;
@@ -88,7 +99,15 @@ ssd_status check_inputs(const ssd_dims *d, const ssd_inputs *in, Problem &pr) {
   pr.conv_b = in->conv_b;
   pr.seq_idx = in->seq_idx;
   pr.init = in->initial_states;
+  pr.z = d->gated_norm ? in->z : nullptr;
+  pr.zs = in->z_tok_stride;
+  pr.norm_w = in->norm_weight;
+  pr.norm_eps = in->norm_eps;
   return SSD_OK;
+}
+
+Workspace plan_for(const ssd_dims *d, const Problem &pr, bool backward) {
+  return plan_workspace(pr, elem_bytes(d->dtype), backward, d->dtype == SSD_BF16 && tc_envelope(pr), d->gated_norm != 0);
 }
 
 // ---------------------------------------------------------------- profiling
@@ -167,6 +186,8 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
   float *segin = segin_user ? segin_user : reinterpret_cast<float *>(ws + w.segin);
   int *status = reinterpret_cast<int *>(ws + w.status);
   const bool tc = use_tc<T>(pr);
+  T *const y_out = y;
+  if (pr.z) y = reinterpret_cast<T *>(ws + w.ypre);  // the mixer output before the gated norm
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
@@ -189,6 +210,7 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
     }
   }
   if (!tc) SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, y, s));
+  if (pr.z) SSD_LAUNCH("gated_norm", launch_gated_norm_fwd<T>(pr, y, y_out, s));
   if (sf.out)  // the chunk states (tensor-core path) or local states (CUDA-core path) are still in sst
     SSD_LAUNCH("seq_finals", launch_seq_finals<T>(pr, u, dtv, acs, sst, !tc, segin, sf.cu_seqlens, sf.nseq, sf.out, s));
   return launch_status();
@@ -208,7 +230,8 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   float *wbuf = reinterpret_cast<float *>(ws + w.w), *tok = reinterpret_cast<float *>(ws + w.tok);
   float *dcp = reinterpret_cast<float *>(ws + w.dcp), *dbp = reinterpret_cast<float *>(ws + w.dbp);
   float *chs = reinterpret_cast<float *>(ws + w.chs), *convp = reinterpret_cast<float *>(ws + w.convp);
-  GradOut go{g->dx, g->dB, g->dC, g->ddt, g->dx_tok_stride, g->dB_tok_stride, g->dC_tok_stride, g->ddt_tok_stride};
+  GradOut go{g->dx,           g->dB,           g->dC,           g->ddt,    g->dx_tok_stride,
+             g->dB_tok_stride, g->dC_tok_stride, g->ddt_tok_stride, g->dz, g->dz_tok_stride};
   int *status = reinterpret_cast<int *>(ws + w.status);
   const bool tc = use_tc<T>(pr);
   // recompute: conv, dt, CB, chunk states, local segment passes (and the scan)
@@ -231,6 +254,22 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
     float *sg = reinterpret_cast<float *>(ws + w.segin);
     SSD_LAUNCH("seg_scan", launch_seg_scan(pr, sext, ablk, sg, nullptr, s));
     segin = sg;
+  }
+  // the gated norm's backward: the mixer output is recomputed (it scales with L
+  // and is not saved), then dout becomes the mixer output's gradient dy
+  if (pr.z) {
+    T *ypre = reinterpret_cast<T *>(ws + w.ypre), *dyn = reinterpret_cast<T *>(ws + w.dyn);
+    if constexpr (kIsBf16<T>) {
+      if (tc) {
+        __nv_bfloat16 *sin16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.sin16);
+        SSD_LAUNCH("combine_state", launch_combine_state(pr, sst, segin, sin16, s));
+        SSD_LAUNCH("tc_chunk_out", launch_tc_out(pr, u, dtv, acs, sin16, ypre, status, s));
+      }
+    }
+    if (!tc) SSD_LAUNCH("chunk_out", launch_chunk_out<T>(pr, u, dtv, acs, cb, sst, segin, ypre, s));
+    SSD_LAUNCH("gated_norm_bwd", launch_gated_norm_bwd<T>(pr, ypre, dy, dyn, go, reinterpret_cast<float *>(ws + w.normp),
+                                                          g->dnorm_weight, s));
+    dy = dyn;
   }
   // reverse boundary scan
   if constexpr (kIsBf16<T>) {
@@ -301,7 +340,7 @@ extern "C" {
 size_t ssd_workspace_size(const ssd_dims *dims, int backward) {
   if (check_dims(dims) != SSD_OK) return 0;
   const Problem pr = problem_from(dims);
-  return plan_workspace(pr, elem_bytes(dims->dtype), backward != 0, dims->dtype == SSD_BF16 && tc_envelope(pr)).total;
+  return plan_for(dims, pr, backward != 0).total;
 }
 
 }  // extern "C"
@@ -319,7 +358,7 @@ ssd_status check_forward(const ssd_dims *dims, const ssd_inputs *in, const void 
   if (!aligned(y, 16) || (final_state && !aligned(final_state, 16)) ||
       (seg_init_states && !aligned(seg_init_states, 16)))
     return SSD_ERR_ALIGNMENT;
-  w = plan_workspace(pr, elem_bytes(dims->dtype), false, dims->dtype == SSD_BF16 && tc_envelope(pr));
+  w = plan_for(dims, pr, false);
   return SSD_OK;
 }
 
@@ -397,6 +436,12 @@ ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *
   const int eb = elem_bytes(dims->dtype);
   const long long vec = 16 / eb;
   const long long HP = (long long)dims->nheads * dims->headdim, GN = (long long)dims->ngroups * dims->dstate;
+  if (dims->gated_norm) {
+    if (!grads->dz || !grads->dnorm_weight) return SSD_ERR_NULL_PTR;
+    if (grads->dz_tok_stride < HP) return SSD_ERR_INVALID_DIMS;
+    if (!aligned(grads->dz, 16) || grads->dz_tok_stride % vec || !aligned(grads->dnorm_weight, 4))
+      return SSD_ERR_ALIGNMENT;
+  }
   if (grads->dx_tok_stride < HP || grads->dB_tok_stride < GN || grads->dC_tok_stride < GN ||
       grads->ddt_tok_stride < dims->nheads)
     return SSD_ERR_INVALID_DIMS;
@@ -405,7 +450,7 @@ ssd_status ssd_backward(const ssd_dims *dims, const ssd_inputs *in, const void *
       grads->dC_tok_stride % vec || (dfinal_state && !aligned(dfinal_state, 16)) ||
       (seg_init_states && !aligned(seg_init_states, 16)))
     return SSD_ERR_ALIGNMENT;
-  const Workspace w = plan_workspace(pr, eb, true, dims->dtype == SSD_BF16 && tc_envelope(pr));
+  const Workspace w = plan_for(dims, pr, true);
   if (!workspace || ws_bytes < w.total) return SSD_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return SSD_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -19,6 +19,11 @@ struct Problem {
   const float *dt_bias, *A_log, *D, *conv_w, *conv_b;
   const int *seq_idx;  // (b, L) or nullptr
   const float *init;   // (b, H, P, N): each row's initial state (the state before token 0), or nullptr
+  // gated RMSNorm after the mixer (z == nullptr: none): z (b, L, H*P) token stride zs
+  const void *z;
+  long long zs;
+  const float *norm_w;  // (H*P)
+  float norm_eps;
   // per (b, h, chunk) decay tables, (b, H, nc) fp32, filled by decay_tables_kernel:
   const float *cdec;    // product of the chunk's per-token decays (0 at row start / sequence start inside)
   const float *dstart;  // product of cdec over the segment's chunks before this one
@@ -137,13 +142,19 @@ struct Workspace {
   size_t chs;                                  // 4 x (b, nc, H) f32 per-chunk scalars
   size_t sdp;                                  // (scan groups, b, nc, H) f32: partial <dS, S_in> (tensor-core path)
   size_t convp;                                // (b, ntb, Cd, 5) f32 conv parameter partials
+  // gated RMSNorm
+  size_t ypre;                                 // (b, L, H*P) act dtype: the mixer output before the norm
+  size_t dyn;                                  // backward: (b, L, H*P) act dtype, the mixer output's gradient
+  size_t normp;                                // backward: (norm tiles, H*P) f32 norm-weight partials
   size_t total;
   int ntb;                                     // conv backward token blocks per row
 };
 
 // tc: the tensor-core path, which forms CB inside its kernels and keeps W on
 // chip, so it needs neither the CB nor the W buffer.
-inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward, bool tc) {
+int norm_bwd_tiles(const Problem &pr);  // norm.cu
+
+inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward, bool tc, bool norm) {
   Workspace w{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -178,6 +189,13 @@ inline Workspace plan_workspace(const Problem &pr, int elem_bytes, bool backward
     w.chs = take(4 * b * nc * H * 4);
     w.sdp = take(tc ? (size_t)scan_groups(pr) * b * nc * H * 4 : 0);
     w.convp = take(b * (size_t)w.ntb * Cd * 5 * 4);
+  }
+  if (norm) {
+    w.ypre = take(b * L * H * P * elem_bytes);
+    if (backward) {
+      w.dyn = take(b * L * H * P * elem_bytes);
+      w.normp = take((size_t)norm_bwd_tiles(pr) * H * P * 4);
+    }
   }
   w.total = off;
   return w;

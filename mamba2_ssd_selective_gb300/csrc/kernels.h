@@ -9,6 +9,8 @@ namespace ssd {
 struct GradOut {  // raw-input gradient destinations (activation dtype)
   void *dx, *dB, *dC, *ddt;
   long long dxs, dBs, dCs, ddts;
+  void *dz;  // the gate's gradient (gated RMSNorm), token stride dzs
+  long long dzs;
 };
 
 // conv + dt (conv_dt.cu)
@@ -19,6 +21,13 @@ void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, floa
 void launch_param_reduce(const Problem &pr, const float *chs, const float *convp, int ntb, float *ddt_bias,
                          float *dA_log, float *dD, float *dconv_w, float *dconv_b, cudaStream_t s);
 void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStream_t s);
+
+// gated RMSNorm after the mixer (norm.cu): out = norm(ypre * silu(z)) * w, and its
+// backward (dy, dz, and the norm weight's gradient via per-tile partials dwp)
+template <typename T> void launch_gated_norm_fwd(const Problem &pr, const T *ypre, T *y, cudaStream_t s);
+template <typename T>
+void launch_gated_norm_bwd(const Problem &pr, const T *ypre, const T *dout, T *dy, const GradOut &go, float *dwp,
+                           float *dnorm_w, cudaStream_t s);
 
 // segment summaries and scans (scan.cu)
 void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, float *ablk,

@@ -39,7 +39,7 @@ def np_(t) -> np.ndarray:
 
 
 def gpu_forward(shape, dtype, inp, runner=None):
-    r = runner or ssd.SsdRunner(shape, dtype)
+    r = runner or ssd.SsdRunner(shape, dtype, gated_norm=inp.get("z") is not None)
     t = to_dev(inp)
     y, fin, seg = r.forward(t)
     torch.cuda.synchronize()
@@ -52,7 +52,7 @@ def gpu_forward(shape, dtype, inp, runner=None):
 
 
 def gpu_backward(shape, dtype, inp, use_dfinal=True, pass_seg=True):
-    r = ssd.SsdRunner(shape, dtype)
+    r = ssd.SsdRunner(shape, dtype, gated_norm=inp.get("z") is not None)
     t = to_dev(inp)
     y, fin, seg = r.forward(t)
     g = r.backward(t, t["dy"], t["dfinal"] if use_dfinal else None, seg if pass_seg else None)
@@ -100,6 +100,11 @@ def compare_backward(got: dict, ref: dict, shape, tol: float, rows=None, heads=N
         })
     if ref.get("dinit") is not None:
         errs["dinit"] = rel(got["dinit"][rows][:, h0:h1], ref["dinit"])
+    if ref.get("dz") is not None:
+        P = shape.headdim
+        errs["dz"] = rel(got["dz"][rows][..., h0 * P:h1 * P], ref["dz"])
+        if len(rows) == shape.batch:
+            errs["dnorm_weight"] = rel(got["dnorm_weight"][h0 * P:h1 * P], ref["dnorm_weight"])
     for k, e in errs.items():
         bound = ddt_bias_tol(floor_case, tol) if k == "ddt_bias" else tol
         assert k in REPORT_ONLY or e <= bound, (k, e, bound, errs)

@@ -5,8 +5,9 @@ accumulation (ddt_bias in three named small cases: see tests/gpu_util.py).  Shap
 headdim 32, dstate 40), group mapping (G > 1), packed sequences with edge
 cases (a boundary at a chunk start, at a segment start, sequences of 1-3
 tokens and sequences shorter than a chunk), every segment count 1..16, initial
-states with their gradient, per-sequence final states of packed rows, and the
-bitwise replay the pages require of summaries, scans and outputs.
+states with their gradient, per-sequence final states of packed rows, the
+gated RMSNorm after the mixer with its backward, and the bitwise replay the
+pages require of summaries, scans and outputs.
 """
 from __future__ import annotations
 
@@ -179,6 +180,64 @@ def test_varlen_sequence_final_states(oracle_lib, dtype, init):
         assert rel(np_(sf[q]), fins[q]) <= 2 * TOL[dtype], q
     # the row's last sequence ends at the row's last token: its state is the final state
     assert rel(np_(sf[-1]), np_(fin)[0]) <= TOL[dtype]
+
+
+NORM_SHAPES = [
+    (SsdShape(2, 1024, 8, 64, 128, 1, 256, 2), None),
+    (SsdShape(1, 1024, 8, 64, 128, 2, 256, 4), [300, 3, 721]),
+    (SsdShape(1, 512, 8, 32, 40, 4, 64, 2), None),  # CUDA-core path (headdim 32) in bf16 as well
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape,seq", NORM_SHAPES)
+def test_gated_norm_forward_backward(oracle_lib, shape, seq, dtype):
+    """y = gated RMSNorm of the mixer output (one norm group per B/C group);
+    the backward recomputes the mixer output and returns dz and the norm
+    weight's gradient besides every other gradient."""
+    inp = make_inputs(shape, 29, dtype, dfinal=True, seq_lengths=seq, gated_norm=True)
+    got, _ = gpu_forward(shape, dtype, inp)
+    compare_forward(got, oracle_lib.forward(inp, shape), TOL[dtype])
+    g = gpu_backward(shape, dtype, inp)
+    errs = compare_backward(g, oracle_lib.backward(inp, shape), shape, TOL[dtype])
+    assert "dz" in errs and "dnorm_weight" in errs
+
+
+def test_gated_norm_reads_z_from_the_in_projection_output(oracle_lib):
+    """z, x, B, C and dt all read in place from one (z | x | B | C | dt) buffer, and
+    dz, dx, dB, dC, ddt written into the slots of one such gradient buffer."""
+    shape = SsdShape(1, 1024, 8, 64, 128, 1, 256, 2)
+    inp = make_inputs(shape, 30, "bf16", dfinal=True, seq_lengths=[600, 424], gated_norm=True)
+    s = shape
+    HP, GN, H, Cd = s.nheads * s.headdim, s.ngroups * s.dstate, s.nheads, s.conv_dim
+    D_in = 2 * HP + 2 * GN + H
+    t = to_dev(inp)
+    buf = torch.empty(s.batch, s.seqlen, D_in, device="cuda", dtype=torch.bfloat16)
+    buf[..., :HP] = t["z"]
+    buf[..., HP:HP + Cd] = t["xBC"]
+    buf[..., HP + Cd:] = t["dt_raw"]
+    es, base = buf.element_size(), buf.data_ptr()
+    ins = ssd.SsdInputs(base + HP * es, D_in, base + 2 * HP * es, D_in, base + (2 * HP + GN) * es, D_in,
+                        base + (HP + Cd) * es, D_in, t["dt_bias"].data_ptr(), t["A_log"].data_ptr(),
+                        t["D"].data_ptr(), t["conv_w"].data_ptr(), t["conv_b"].data_ptr(), t["seq_idx"].data_ptr(),
+                        None, base, D_in, t["norm_weight"].data_ptr(), inp["norm_eps"])
+    r = ssd.SsdRunner(shape, "bf16", gated_norm=True)
+    y, fin, seg = r.alloc_outputs()
+    ssd.ssd_forward(r.dims, ins, y, fin, seg, r.workspace)
+    dbuf = torch.full_like(buf, float("nan"))
+    g = r.alloc_grads()
+    gb, dbase = dbuf.element_size(), dbuf.data_ptr()
+    gs = ssd.SsdGrads(dbase + HP * gb, D_in, dbase + 2 * HP * gb, D_in, dbase + (2 * HP + GN) * gb, D_in,
+                      dbase + (HP + Cd) * gb, D_in, g["ddt_bias"].data_ptr(), g["dA_log"].data_ptr(),
+                      g["dD"].data_ptr(), g["dconv_w"].data_ptr(), g["dconv_b"].data_ptr(), None, dbase, D_in,
+                      g["dnorm_weight"].data_ptr())
+    ssd.ssd_backward(r.dims, ins, t["dy"], t["dfinal"], seg, gs, r.workspace)
+    torch.cuda.synchronize()
+    got = {"y": np_(y).reshape(1, s.seqlen, H, s.headdim), "final_state": np_(fin), "seg_in": np_(seg)}
+    compare_forward(got, oracle_lib.forward(inp, shape), TOL["bf16"])
+    out = {"dxBC": np_(dbuf[..., HP:HP + Cd]), "ddt_raw": np_(dbuf[..., HP + Cd:]), "dz": np_(dbuf[..., :HP])}
+    out.update({k: np_(g[k]) for k in ("ddt_bias", "dA_log", "dD", "dconv_w", "dconv_b", "dnorm_weight")})
+    compare_backward(out, oracle_lib.backward(inp, shape), shape, TOL["bf16"])
 
 
 def test_backward_recomputes_segment_states(oracle_lib):
