@@ -382,10 +382,12 @@ def run_reference(args, shape, dtype, seed, backward: bool):
 
 
 def metric_for(args, backward: bool) -> str:
-    if args.workload == DEFAULT_WORKLOAD and args.segments is None and args.batch is None and args.chunk is None:
+    if (args.workload == DEFAULT_WORKLOAD and args.segments is None and args.batch is None and args.chunk is None
+            and not args.gated_norm):
         return METRIC
     what = "fwd+bwd" if backward else "fwd"
-    return f"SSD {what} tokens/s on 1 GB300 ({args.workload}, bf16) + % of tensor/HBM roofline"
+    norm = " + gated RMSNorm" if args.gated_norm else ""
+    return f"SSD {what}{norm} tokens/s on 1 GB300 ({args.workload}, bf16) + % of tensor/HBM roofline"
 
 
 def config_dict(args, shape, dtype, seed) -> dict:
@@ -393,7 +395,7 @@ def config_dict(args, shape, dtype, seed) -> dict:
     return {"workload": args.workload, "batch": shape.batch, "seqlen": shape.seqlen, "nheads": shape.nheads,
             "headdim": shape.headdim, "dstate": shape.dstate, "ngroups": shape.ngroups, "d_conv": shape.d_conv,
             "chunk": shape.chunk, "n_segments": shape.n_segments, "packed": shape.packed, "activations": dtype,
-            "seed": seed,
+            "gated_norm": bool(args.gated_norm), "seed": seed,
             "l2": f"inputs larger than L2 (xBC {shape.tokens * shape.conv_dim * eb / 1e6:.0f}"
                   f" MB, dy {shape.tokens * shape.nheads * shape.headdim * eb / 1e6:.0f}"
                   f" MB per step; L2 is 129 MB)"}
@@ -414,9 +416,9 @@ def run_ours(args, shape, dtype, seed, backward: bool):
     if rank != 0:
         build()  # stamp is current: only loads
     ssd.load()
-    inp = make_inputs(shape, seed + 1000 * rank, dtype)
+    inp = make_inputs(shape, seed + 1000 * rank, dtype, gated_norm=args.gated_norm)
     t = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
-    runner = ssd.SsdRunner(shape, dtype)
+    runner = ssd.SsdRunner(shape, dtype, gated_norm=args.gated_norm)
     y, fin, seg = runner.alloc_outputs()
     grads = runner.alloc_grads()
     dfinal = None
@@ -455,6 +457,8 @@ def run_ours(args, shape, dtype, seed, backward: bool):
     e2e = None
     if not args.no_e2e:
         in_keys = ("xBC", "dt_raw", "dy") if backward else ("xBC", "dt_raw")
+        if args.gated_norm:
+            in_keys += ("z",)
         host_in = {k: inp[k].pin_memory() for k in in_keys}
         host_out = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
                     "final_state": torch.empty(fin.shape, dtype=fin.dtype).pin_memory()}
@@ -536,7 +540,7 @@ def run_ours(args, shape, dtype, seed, backward: bool):
         "kernels": [{"name": n, "launches": c, "ms_per_launch": round(ms_ / max(c, 1), 4),
                      "share": round(ms_ / max(sum(r[2] for r in kt), 1e-9), 4)} for n, c, ms_ in kt],
     }
-    if ws == 1 and not args.no_cpu_baseline:
+    if ws == 1 and not args.no_cpu_baseline and not args.gated_norm:
         line["cpu_baseline"] = cpu_baseline(inp, shape, backward)
     print(json.dumps(line), flush=True)
 
@@ -550,6 +554,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--segments", type=int, default=None, help="override the workload's segment count")
     ap.add_argument("--chunk", type=int, default=None, help="override the workload's chunk length")
+    ap.add_argument("--gated-norm", action="store_true", help="y is the gated RMSNorm of the mixer output")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")

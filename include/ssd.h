@@ -69,7 +69,7 @@ typedef struct {
   int32_t n_segments; /* S: equal causal segments; each must be a multiple of chunk */
   int32_t dtype;      /* ssd_dtype of the activations */
   int32_t gated_norm; /* 1: y is the gated RMSNorm of the mixer output (needs z and
-                         norm_weight in ssd_inputs; at most 8192 channels per group), 0: none */
+                         norm_weight in ssd_inputs; at most 4096 channels per group), 0: none */
 } ssd_dims;
 
 /* Pre-conv activations as laid out by the in-projection (zero-copy views into

@@ -34,8 +34,8 @@ ssd_status check_dims(const ssd_dims *d) {
       (long long)d->ngroups * d->dstate > (1 << 16))
     return SSD_ERR_UNSUPPORTED;
   if (d->gated_norm != 0 && d->gated_norm != 1) return SSD_ERR_INVALID_DIMS;
-  // the norm kernels hold a group's channels in registers: up to 8192 per group
-  if (d->gated_norm && (long long)d->nheads * d->headdim / d->ngroups > 8192) return SSD_ERR_UNSUPPORTED;
+  // the norm kernels hold a group's channels in registers: up to 4096 per group
+  if (d->gated_norm && (long long)d->nheads * d->headdim / d->ngroups > 4096) return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
 }
 
@@ -187,7 +187,8 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
   int *status = reinterpret_cast<int *>(ws + w.status);
   const bool tc = use_tc<T>(pr);
   T *const y_out = y;
-  if (pr.z) y = reinterpret_cast<T *>(ws + w.ypre);  // the mixer output before the gated norm
+  // the gated norm: a separate pass over the mixer output (written to the workspace)
+  if (pr.z) y = reinterpret_cast<T *>(ws + w.ypre);
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
   SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),

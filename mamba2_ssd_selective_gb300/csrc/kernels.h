@@ -85,7 +85,8 @@ inline bool tc_envelope(const Problem &pr) {
 }
 void launch_tc_state(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, float *sst,
                      int *status, cudaStream_t s);
-// persistent output kernel (tc_out.cu)
+// persistent output kernel (tc_out.cu): the mixer output y (the gated norm, when
+// asked for, is a separate pass over it)
 void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs,
                    const __nv_bfloat16 *sin16, __nv_bfloat16 *y, int *status, cudaStream_t s);
 void launch_tc_z(const Problem &pr, const __nv_bfloat16 *u, const __nv_bfloat16 *dy, const float *dtv,

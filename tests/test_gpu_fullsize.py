@@ -10,6 +10,9 @@ oracle on samples it can compute: whole batch rows, or whole groups of heads
   packed-32k        b1 T32768 H48 G1, packed sequences, forward + backward, all heads;
                     and again from a random initial state, with every sequence's
                     final state (ssd_forward_varlen) and the initial state's gradient
+  with the gated RMSNorm: mamba2-1b-fwdbwd (one 64-head norm group: a separate
+                    norm pass) forward + backward, and long-131k S8 forward, heads
+                    0-7 (8-head groups: the norm inside the output kernel)
 """
 from __future__ import annotations
 
@@ -116,3 +119,40 @@ def test_packed_32k_initial_state_and_sequence_finals(oracle_lib):
                              shape, TOL[dtype])
     assert "dinit" in gerrs
     print("packed-32k init", errs, gerrs)
+
+
+def test_mamba2_1b_gated_norm_forward_backward(oracle_lib):
+    shape, dtype, seed = WORKLOADS["mamba2-1b-fwdbwd"]
+    inp = make_inputs(shape, seed, dtype, gated_norm=True)
+    r = ssd.SsdRunner(shape, dtype, gated_norm=True)
+    t = to_dev(inp)
+    y, fin, seg = r.forward(t)
+    g = r.backward(t, t["dy"], None, seg)
+    torch.cuda.synchronize()
+    got = {"y": np_(y).reshape(shape.batch, shape.seqlen, shape.nheads, shape.headdim), "final_state": np_(fin),
+           "seg_in": np_(seg)}
+    errs = compare_forward(got, oracle_lib.forward(inp, shape, rows=[2]), TOL[dtype], rows=[2])
+    gerrs = compare_backward({k: np_(v) for k, v in g.items()}, oracle_lib.backward(inp, shape, use_dfinal=False),
+                             shape, TOL[dtype])
+    print("mamba2-1b gated norm", errs, gerrs)
+
+
+def test_long_131k_gated_norm_forward(oracle_lib):
+    shape, dtype, seed = WORKLOADS["long-131k"]
+    inp = make_inputs(shape, seed, dtype, gated_norm=True)
+    heads = (0, shape.nheads // shape.ngroups)
+    got, _ = _run_norm(shape, dtype, inp)
+    errs = compare_forward(got, oracle_lib.forward(inp, shape, heads=heads), TOL[dtype], heads=heads)
+    print("long-131k gated norm", errs)
+
+
+def _run_norm(shape, dtype, inp):
+    r = ssd.SsdRunner(shape, dtype, gated_norm=True)
+    t = to_dev(inp)
+    y, fin, seg = r.forward(t)
+    torch.cuda.synchronize()
+    out = {"y": np_(y).reshape(shape.batch, shape.seqlen, shape.nheads, shape.headdim), "final_state": np_(fin),
+           "seg_in": np_(seg)}
+    del r, t
+    torch.cuda.empty_cache()
+    return out, None

@@ -183,8 +183,12 @@ def test_varlen_sequence_final_states(oracle_lib, dtype, init):
 
 
 NORM_SHAPES = [
+    # norm groups of 8 and 4 heads: the tensor-core output kernel holds a whole group
+    # per work unit and applies the norm in its epilogue
     (SsdShape(2, 1024, 8, 64, 128, 1, 256, 2), None),
     (SsdShape(1, 1024, 8, 64, 128, 2, 256, 4), [300, 3, 721]),
+    # a group of 32 heads spans two work units: the norm runs as its own pass
+    (SsdShape(1, 512, 32, 64, 128, 1, 256, 2), [200, 312]),
     (SsdShape(1, 512, 8, 32, 40, 4, 64, 2), None),  # CUDA-core path (headdim 32) in bf16 as well
 ]
 
