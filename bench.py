@@ -175,10 +175,10 @@ def kernel_work(shape, dtype: str) -> dict:
         "local_rev": ("mem", 0, 2 * st + seg),
         "seg_rscan": ("mem", 0, 2 * seg),
         # bf16 path: the states' decay term (combine_bwd) and dy . x (tc_bwd_col) come precomputed
-        "chunk_dt": ("mem", 0, 6 * tok + (0 if dtype == "bf16" else 4 * st + 2 * x) + b * L * H * eb),
+        "chunk_dt": ("mem", 0, 8 * tok + (0 if dtype == "bf16" else 4 * st + 2 * x) + 2 * b * L * H * eb),
         "combine_bwd": ("mem", 0, 2 * st + 2 * seg + 2 * st16 + b * nc * H * 4 * ((P * N + 2047) // 2048)),
-        "bc_reduce": ("mem", 0, 2 * parts + 2 * b * L * GN * 4),
-        "conv_bwd": ("mem", 0, b * L * Cd * (2 * eb + 4) + b * (L // 64) * Cd * 20),
+        # the B / C channels' gradients come as head-block partials, summed while staging
+        "conv_bwd": ("mem", 0, b * L * (Cd * 2 * eb + HP * 4) + 2 * parts + b * (L // 64) * Cd * 20),
         "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 64) * Cd * 20),
         "tc_chunk_state": ("tensor", f_state, x + bc + st),
         "tc_chunk_z": ("tensor", f_state, x + bc + st),

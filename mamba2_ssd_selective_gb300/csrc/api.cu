@@ -305,9 +305,10 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   SSD_LAUNCH("chunk_dt",
              launch_chunk_dt<T>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok, vcol_parts, sdp, scan_groups(pr), go,
                                 chs, s));
-  SSD_LAUNCH("bc_reduce", launch_bc_reduce(pr, dcp, dbp, nsub, spg, du, s));
-  // conv backward and parameter reductions
-  SSD_LAUNCH("conv_bwd", launch_conv_bwd<T>(pr, du, go, convp, w.ntb, s));
+  // conv backward (it sums the dB / dC partials for the B and C channels) and
+  // parameter reductions
+  const BcParts bc{dbp, dcp, nsub, spg};
+  SSD_LAUNCH("conv_bwd", launch_conv_bwd<T>(pr, du, bc, go, convp, w.ntb, s));
   SSD_LAUNCH("param_reduce", launch_param_reduce(pr, chs, convp, w.ntb, g->ddt_bias, g->dA_log, g->dD, g->dconv_w, g->dconv_b, s));
   return launch_status();
 }

@@ -172,43 +172,62 @@ template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t
 }
 
 // dt = softplus(dt_raw + dt_bias); acs = inclusive cumsum of dt*A within each
-// chunk (A = -exp(A_log)).  One warp per (b, h, chunk); layouts (b, H, L).  The
-// chunk's raw dt (one strided element per token) is loaded up front, so the
-// warp waits for one round of loads rather than one per 32 tokens.
-constexpr int kMaxChunk = 256;
+// chunk (A = -exp(A_log)); layouts (b, H, L).  A block takes one chunk of one
+// row and 8 heads: the chunk's dt_raw for those heads (16 contiguous bytes per
+// token in bf16) is staged in shared memory, then each warp takes a head, a
+// lane 8 consecutive tokens: softplus, the lane's running sum, and the lanes'
+// exclusive prefix by shuffles.
+constexpr int kMaxChunk = 256, kDtHeads = 8, kDtPer = kMaxChunk / 32;
 template <typename T>
-__global__ void __launch_bounds__(32) dt_prep_kernel(Problem pr, float *__restrict__ dtv, float *__restrict__ acs) {
-  const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z, lane = threadIdx.x;
-  const float A = -expf(pr.A_log[h]), bias = pr.dt_bias[h];
-  const T *dtr = static_cast<const T *>(pr.dt) + (size_t)bb * pr.L * pr.dts + h;
-  const size_t ob = ((size_t)bb * pr.H + h) * pr.L;
-  float raw[kMaxChunk / 32];
-#pragma unroll
-  for (int k = 0; k < kMaxChunk / 32; ++k) {
-    const int i = 32 * k + lane;
-    raw[k] = i < pr.Q ? to_f(dtr[(size_t)(c * pr.Q + i) * pr.dts]) : 0.f;
+__global__ void __launch_bounds__(256) dt_prep_kernel(Problem pr, float *__restrict__ dtv, float *__restrict__ acs) {
+  __shared__ float tile[kMaxChunk][kDtHeads + 1];
+  const int c = blockIdx.x, h0 = blockIdx.y * kDtHeads, bb = blockIdx.z;
+  const int nh = min(kDtHeads, pr.H - h0), t0 = c * pr.Q;
+  const T *src = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h0;
+  for (int e = threadIdx.x; e < pr.Q * kDtHeads; e += 256) {
+    const int t = e / kDtHeads, hh = e % kDtHeads;
+    if (hh < nh) tile[t][hh] = to_f(src[(size_t)t * pr.dts + hh]);
   }
-  float carry = 0.f;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, i0 = lane * kDtPer;
+  for (int hh = warp; hh < nh; hh += 8) {
+    const int h = h0 + hh;
+    const float A = -expf(pr.A_log[h]), bias = pr.dt_bias[h];
+    float d[kDtPer], a[kDtPer], run = 0.f;
 #pragma unroll
-  for (int k = 0; k < kMaxChunk / 32; ++k) {
-    if (32 * k >= pr.Q) break;
-    const int t = c * pr.Q + 32 * k + lane;
-    const float d = softplus_f(raw[k] + bias);
-    float v = d * A;
+    for (int k = 0; k < kDtPer; ++k) {
+      const int i = i0 + k;
+      d[k] = i < pr.Q ? softplus_f(tile[i][hh] + bias) : 0.f;
+      run += d[k] * A;
+      a[k] = run;
+    }
+    float pre = run;  // inclusive prefix of the lanes' totals
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      float n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
+      const float y = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += y;
     }
-    v += carry;
-    dtv[ob + t] = d;
-    acs[ob + t] = v;
-    carry = __shfl_sync(0xffffffffu, v, 31);
+    pre -= run;  // the lanes before this one
+    const size_t ob = ((size_t)bb * pr.H + h) * pr.L + t0;
+    if (i0 + kDtPer <= pr.Q) {  // the lane's 8 tokens: two 16-byte stores per array
+      float4 *dv4 = reinterpret_cast<float4 *>(dtv + ob + i0), *av4 = reinterpret_cast<float4 *>(acs + ob + i0);
+      dv4[0] = make_float4(d[0], d[1], d[2], d[3]);
+      dv4[1] = make_float4(d[4], d[5], d[6], d[7]);
+      av4[0] = make_float4(a[0] + pre, a[1] + pre, a[2] + pre, a[3] + pre);
+      av4[1] = make_float4(a[4] + pre, a[5] + pre, a[6] + pre, a[7] + pre);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kDtPer; ++k)
+        if (i0 + k < pr.Q) {
+          dtv[ob + i0 + k] = d[k];
+          acs[ob + i0 + k] = a[k] + pre;
+        }
+    }
   }
 }
 
 template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *acs, cudaStream_t s) {
-  dt_prep_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 32, 0, s>>>(pr, dtv, acs);
+  dt_prep_kernel<T><<<dim3(pr.nc, (pr.H + kDtHeads - 1) / kDtHeads, pr.b), 256, 0, s>>>(pr, dtv, acs);
 }
 
 // Conv + SiLU backward over a tile of kConvBwdTok tokens x kBwdCh channels (one
@@ -227,8 +246,8 @@ template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *
 constexpr int kBwdCh = 64;
 
 template <typename T, bool HasSeq>
-__global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *__restrict__ du, GradOut go,
-                                                       float *__restrict__ convp, int ntb) {
+__global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *__restrict__ du, BcParts bc,
+                                                       GradOut go, float *__restrict__ convp, int ntb) {
   constexpr int kTok = kConvBwdTok;
   constexpr int kXRows = kTok + 6;  // raw inputs, tokens t0-3 .. t0+kTok+2
   constexpr int kDRows = kTok + 3;  // du / dv, tokens t0 .. t0+kTok+2
@@ -250,16 +269,47 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
                  "l"(g), "r"(ok ? 16 : 0)
                  : "memory");
   }
-  const float *dub = du + (size_t)bb * pr.L * pr.Cd + ct.c0;
-  for (int q = threadIdx.x; q < kDRows * (kBwdCh / 4); q += 256) {
-    const int r = q / (kBwdCh / 4), cc = (q % (kBwdCh / 4)) * 4, t = t0 + r;
-    if (cc >= nch) continue;
-    const bool ok = t < pr.L;
-    const float *g = dub + (ok ? (size_t)t * pr.Cd : 0) + cc;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(&dv[r][cc]))),
-                 "l"(g), "r"(ok ? 16 : 0)
-                 : "memory");
+  const int HP = pr.H * pr.P, GN = pr.G * pr.N;
+  if (ct.c0 < HP) {  // x channels: du as the chunk kernels wrote it
+    const float *dub = du + (size_t)bb * pr.L * pr.Cd + ct.c0;
+    for (int q = threadIdx.x; q < kDRows * (kBwdCh / 4); q += 256) {
+      const int r = q / (kBwdCh / 4), cc = (q % (kBwdCh / 4)) * 4, t = t0 + r;
+      if (cc >= nch) continue;
+      const bool ok = t < pr.L;
+      const float *g = dub + (ok ? (size_t)t * pr.Cd : 0) + cc;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                       static_cast<uint32_t>(__cvta_generic_to_shared(&dv[r][cc]))),
+                   "l"(g), "r"(ok ? 16 : 0)
+                   : "memory");
+    }
+  } else {  // B / C channels: the sum of the group's head-block partials, in block order
+    const bool isB = ct.c0 < HP + GN;
+    const float *parts = isB ? bc.dbp : bc.dcp;
+    const int idx0 = ct.c0 - HP - (isB ? 0 : GN);  // channel within the region: g * N + n
+    for (int q = threadIdx.x; q < kDRows * (kBwdCh / 4); q += 256) {
+      const int r = q / (kBwdCh / 4), cc = (q % (kBwdCh / 4)) * 4, t = t0 + r;
+      if (cc >= nch) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < pr.L) {
+        const int idx = idx0 + cc, g = idx / pr.N, n = idx % pr.N;  // 4 channels of one group (N % 4 == 0)
+        const float4 *pp = reinterpret_cast<const float4 *>(parts + ((size_t)bb * pr.L + t) * bc.nsub * pr.N + n);
+        const int k0 = g * bc.spg, kN4 = pr.N / 4;
+        int k = 0;
+        for (; k + 4 <= bc.spg; k += 4) {  // four partials' loads in flight, added in order
+          const float4 v0 = pp[(size_t)(k0 + k) * kN4], v1 = pp[(size_t)(k0 + k + 1) * kN4];
+          const float4 v2 = pp[(size_t)(k0 + k + 2) * kN4], v3 = pp[(size_t)(k0 + k + 3) * kN4];
+          acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
+          acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
+          acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
+          acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
+        }
+        for (; k < bc.spg; ++k) {
+          const float4 v = pp[(size_t)(k0 + k) * kN4];
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+      }
+      *reinterpret_cast<float4 *>(&dv[r][cc]) = acc;
+    }
   }
   if (HasSeq)
     for (int r = threadIdx.x; r < kXRows; r += 256) {
@@ -389,12 +439,13 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
 }
 
 template <typename T>
-void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s) {
+void launch_conv_bwd(const Problem &pr, const float *du, const BcParts &bc, const GradOut &go, float *convp, int ntb,
+                     cudaStream_t s) {
   dim3 grid(chan_tiles(pr, kBwdCh), ntb, pr.b);
   if (pr.seq_idx)
-    conv_bwd_kernel<T, true><<<grid, 256, 0, s>>>(pr, du, go, convp, ntb);
+    conv_bwd_kernel<T, true><<<grid, 256, 0, s>>>(pr, du, bc, go, convp, ntb);
   else
-    conv_bwd_kernel<T, false><<<grid, 256, 0, s>>>(pr, du, go, convp, ntb);
+    conv_bwd_kernel<T, false><<<grid, 256, 0, s>>>(pr, du, bc, go, convp, ntb);
 }
 
 // Parameter gradients: fixed-order sums of per-chunk / per-block partials.
@@ -492,8 +543,10 @@ template void launch_conv_fwd<float>(const Problem &, float *, cudaStream_t);
 template void launch_conv_fwd<__nv_bfloat16>(const Problem &, __nv_bfloat16 *, cudaStream_t);
 template void launch_dt_prep<float>(const Problem &, float *, float *, cudaStream_t);
 template void launch_dt_prep<__nv_bfloat16>(const Problem &, float *, float *, cudaStream_t);
-template void launch_conv_bwd<float>(const Problem &, const float *, const GradOut &, float *, int, cudaStream_t);
-template void launch_conv_bwd<__nv_bfloat16>(const Problem &, const float *, const GradOut &, float *, int,
+template void launch_conv_bwd<float>(const Problem &, const float *, const BcParts &, const GradOut &, float *, int,
+                                     cudaStream_t);
+template void launch_conv_bwd<__nv_bfloat16>(const Problem &, const float *, const BcParts &, const GradOut &, float *,
+                                             int,
                                              cudaStream_t);
 
 }  // namespace ssd

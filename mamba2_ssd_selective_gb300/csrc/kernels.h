@@ -16,8 +16,16 @@ struct GradOut {  // raw-input gradient destinations (activation dtype)
 // conv + dt (conv_dt.cu)
 template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s);
 template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *acs, cudaStream_t s);
+// dB / dC of the post-conv B and C channels as fixed-order sums of per-head-block
+// partials (b, L, nsub, N): the partials of group g are [g * spg, (g + 1) * spg)
+struct BcParts {
+  const float *dbp, *dcp;
+  int nsub, spg;
+};
+// du: the x channels' gradient (b, L, Cd; the B/C columns are not read)
 template <typename T>
-void launch_conv_bwd(const Problem &pr, const float *du, const GradOut &go, float *convp, int ntb, cudaStream_t s);
+void launch_conv_bwd(const Problem &pr, const float *du, const BcParts &bc, const GradOut &go, float *convp, int ntb,
+                     cudaStream_t s);
 void launch_param_reduce(const Problem &pr, const float *chs, const float *convp, int ntb, float *ddt_bias,
                          float *dA_log, float *dD, float *dconv_w, float *dconv_b, cudaStream_t s);
 void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStream_t s);
@@ -74,10 +82,6 @@ void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dt
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
                      int vcol_parts, const float *sdp, int sdp_groups, const GradOut &go, float *chs,
                      cudaStream_t s);
-// du_B/du_C = fixed-order sums of per-token partials: nsub partials per token,
-// the partials of group g being [g*spg, (g+1)*spg)
-void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int nsub, int spg, float *du,
-                      cudaStream_t s);
 
 // bf16 tensor-core chunk kernels (tc_chunk.cu); envelope: see tc_envelope()
 inline bool tc_envelope(const Problem &pr) {

@@ -540,39 +540,123 @@ __global__ void __launch_bounds__(256) dt_bwd_kernel(Problem pr, const T *__rest
   }
 }
 
+// The same dt / A / D gradients on the tensor-core path, where every per-token
+// piece comes precomputed (vrow, vdiag, vcol, r, q, dy . x in tok; the chunk's
+// decay term as sdp partials): one warp per (chunk, head), a lane per 8
+// consecutive tokens, the suffix sums and totals by shuffles (no block-wide
+// barrier until the gradients of dt_raw are written back through shared memory
+// so that the 8 heads of a block store whole tokens).
+constexpr int kDtTok = 8;  // tokens per lane (chunks of up to 256 tokens)
+template <typename T>
+__global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const float *__restrict__ dtv,
+                                                          const float *__restrict__ acs, const float *__restrict__ tok,
+                                                          const float *__restrict__ sdp, int sdp_groups, GradOut go,
+                                                          float *__restrict__ chs) {
+  __shared__ float dzs[256][8];  // [token in chunk][head in block]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x, h = blockIdx.y * 8 + warp, bb = blockIdx.z, Q = pr.Q, t0 = c * Q;
+  const bool live = h < pr.H;  // warp-uniform
+  const size_t BHL = (size_t)pr.b * pr.H * pr.L;
+  const int i0 = lane * kDtTok;  // this lane's first token in the chunk
+  float dsum = 0.f, dAp = 0.f, dDp = 0.f, dzp = 0.f;
+  if (live) {
+    const size_t tb = ((size_t)bb * pr.H + h) * pr.L + t0;
+    const float A = -expf(pr.A_log[h]), bias = pr.dt_bias[h];
+    const float acs_last = acs[tb + Q - 1];
+    const int seq_last = seq_of(pr, bb, t0 + Q - 1);
+    const size_t BNH = (size_t)pr.b * pr.nc * pr.H, ci = ((size_t)bb * pr.nc + c) * pr.H + h;
+    float dtot = 0.f;  // the chunk's decay term a_c <dS_end, S_in>, partials in order
+    for (int g = 0; g < sdp_groups; ++g) dtot += sdp[g * BNH + ci];
+    const float ac = chunk_decay(pr, bb, h, c);
+    const float dec = ac != 0.f ? ac * dtot : 0.f;
+    float base[kDtTok], vcol[kDtTok], vd[kDtTok], wq[kDtTok], wv[kDtTok], qv[kDtTok], dtk[kDtTok];
+    float wqsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kDtTok; ++k) {
+      const int i = i0 + k;
+      base[k] = vcol[k] = vd[k] = wq[k] = wv[k] = qv[k] = dtk[k] = 0.f;
+      if (i < Q) {
+        const size_t o = tb + i;
+        const float dti = dtv[o], ai = acs[o];
+        const float w = seq_of(pr, bb, t0 + i) == seq_last ? expf(acs_last - ai) : 0.f;
+        const float q = tok[4 * BHL + o];
+        vcol[k] = tok[2 * BHL + o];
+        vd[k] = tok[1 * BHL + o];
+        wv[k] = w;
+        qv[k] = q;
+        dtk[k] = dti;
+        wq[k] = w * dti * q;
+        base[k] = tok[0 * BHL + o] - dti * vcol[k] + tok[3 * BHL + o] - wq[k];
+        dDp += tok[5 * BHL + o];
+        wqsum += wq[k];
+      }
+    }
+    // dAcs at the chunk's last token also gets sum_j wdt_j q_j and the decay term,
+    // which every suffix sum then contains: add them to all tokens' suffix sums
+    float tail = 0.f;
+    for (int o = 16; o >= 1; o >>= 1) wqsum += __shfl_xor_sync(0xffffffffu, wqsum, o);
+    tail = wqsum + dec;
+    // suffix sums over the chunk: within the lane, then the later lanes' totals
+    float run = 0.f, suf[kDtTok];
+#pragma unroll
+    for (int k = kDtTok - 1; k >= 0; --k) {
+      run += base[k];
+      suf[k] = run;
+    }
+    float later = run;  // inclusive suffix over lanes >= this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, later, o);
+      if (lane + o < 32) later += y;
+    }
+    later -= run;  // exclusive: the lanes after this one
+    const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h;
+#pragma unroll
+    for (int k = 0; k < kDtTok; ++k) {
+      const int i = i0 + k;
+      if (i < Q) {
+        const float dda = suf[k] + later + tail;
+        const float ddt = vcol[k] + vd[k] + wv[k] * qv[k] + A * dda;
+        dAp = fmaf(dtk[k], dda, dAp);
+        const float dz = ddt * sigmoid_f(to_f(dtr[(size_t)i * pr.dts]) + bias);
+        dzp += dz;
+        dzs[i][warp] = dz;
+      }
+    }
+    dsum = dzp;
+  }
+  // fixed-order warp totals of the parameter pieces
+  for (int o = 16; o >= 1; o >>= 1) {
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
+    dDp += __shfl_xor_sync(0xffffffffu, dDp, o);
+  }
+  if (live && lane == 0) {
+    const size_t nch = (size_t)pr.b * pr.nc * pr.H, o = ((size_t)bb * pr.nc + c) * pr.H + h;
+    chs[o] = dsum;
+    chs[nch + o] = dAp;
+    chs[2 * nch + o] = dDp;
+  }
+  __syncthreads();
+  const int nh = min(8, pr.H - (int)blockIdx.y * 8);
+  T *dst = static_cast<T *>(go.ddt) + ((size_t)bb * pr.L + t0) * go.ddts + blockIdx.y * 8;
+  for (int e = threadIdx.x; e < Q * 8; e += 256) {
+    const int i = e >> 3, hh = e & 7;
+    if (hh < nh) dst[(size_t)i * go.ddts + hh] = from_f<T>(dzs[i][hh]);
+  }
+}
+
 template <typename T>
 void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dtv, const float *acs,
                      const float *sst, const float *segin, const float *dsl, const float *gout, const float *tok,
                      int vcol_parts, const float *sdp, int sdp_groups, const GradOut &go, float *chs,
                      cudaStream_t s) {
-  dt_bwd_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok,
-                                                            vcol_parts, sdp, sdp_groups, go, chs);
-}
-
-// du_B[t, g, n] = sum of the group's partials of dB[t, n] (one per head, or one
-// per head subset), du_C likewise, in a fixed order.
-__global__ void __launch_bounds__(256) bc_reduce_kernel(Problem pr, const float *__restrict__ dcp,
-                                                        const float *__restrict__ dbp, int nsub, int spg,
-                                                        float *__restrict__ du) {
-  const int GN = pr.G * pr.N;
-  const int idx = blockIdx.y * 256 + threadIdx.x;
-  if (idx >= GN) return;
-  const int g = idx / pr.N, n = idx % pr.N;
-  const size_t tok = blockIdx.x;  // flat (b, t) token index
-  float sb = 0.f, sc = 0.f;
-  for (int k = g * spg; k < (g + 1) * spg; ++k) {
-    sb += dbp[(tok * nsub + k) * pr.N + n];
-    sc += dcp[(tok * nsub + k) * pr.N + n];
-  }
-  const int HP = pr.H * pr.P;
-  du[tok * pr.Cd + HP + idx] = sb;
-  du[tok * pr.Cd + HP + GN + idx] = sc;
-}
-
-void launch_bc_reduce(const Problem &pr, const float *dcp, const float *dbp, int nsub, int spg, float *du,
-                      cudaStream_t s) {
-  dim3 grid((unsigned)((size_t)pr.b * pr.L), (pr.G * pr.N + 255) / 256);
-  bc_reduce_kernel<<<grid, 256, 0, s>>>(pr, dcp, dbp, nsub, spg, du);
+  if (sdp && vcol_parts == 1 && pr.Q <= 32 * kDtTok)  // tensor-core path: every piece precomputed
+    dt_bwd_warp_kernel<T><<<dim3(pr.nc, (pr.H + 7) / 8, pr.b), 256, 0, s>>>(pr, dtv, acs, tok, sdp, sdp_groups, go,
+                                                                            chs);
+  else
+    dt_bwd_kernel<T><<<dim3(pr.nc, pr.H, pr.b), 256, 0, s>>>(pr, u, dy, dtv, acs, sst, segin, dsl, gout, tok,
+                                                              vcol_parts, sdp, sdp_groups, go, chs);
 }
 
 #define SSD_INST(T)                                                                                                  \

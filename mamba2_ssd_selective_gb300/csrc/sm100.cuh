@@ -209,6 +209,27 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[16], uint32_t (&b)[16
                : "memory");
 }
 
+// Packed fp32 arithmetic of the sm_100 family: two fp32 lanes in one 64-bit
+// register, one instruction for both (PTX mul/fma .rn.f32x2, IEEE rounding per lane).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // 2^x on the special-function unit (PTX ex2.approx.ftz; relative error ~2^-22)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -427,22 +427,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i0 >= row_hi) {  // every column at or after every row: factorised decay
               const float e0 = ex2_approx(pipe::lds_f(ta + 4 * i0) - aj), ed = e0 * dt_j;
               const bool nomask = __all_sync(0xffffffffu, end_j >= i0 + 15);
-              float vs = 0.f;
+              // two columns per packed fp32 instruction
+              const uint64_t ed2 = pk2(ed, ed);
+              uint64_t vs2 = pk2(0.f, 0.f);
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
                 const float4 g4 = pipe::lds_f4(tg + 4 * (i0 + e));
-                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+                float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+                if (!nomask) {
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                  const bool ok = nomask || i0 + e + k4 <= end_j;
-                  const float gi = ok ? gv[k4] : 0.f;
-                  const float t1 = gi * ed;
-                  vs = fmaf(dm[e + k4] * cbv[e + k4], gi, vs);
-                  mw[0][e + k4] = cbv[e + k4] * t1;
-                  mw[1][e + k4] = dm[e + k4] * t1;
+                  for (int k4 = 0; k4 < 4; ++k4) gv[k4] = i0 + e + k4 <= end_j ? gv[k4] : 0.f;
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 4; k4 += 2) {
+                  const uint64_t g2 = pk2(gv[k4], gv[k4 + 1]), t2 = mul2(g2, ed2);
+                  const uint64_t dm2 = pk2(dm[e + k4], dm[e + k4 + 1]), cb2 = pk2(cbv[e + k4], cbv[e + k4 + 1]);
+                  vs2 = fma2(mul2(dm2, cb2), g2, vs2);
+                  upk2(mul2(cb2, t2), mw[0][e + k4], mw[0][e + k4 + 1]);
+                  upk2(mul2(dm2, t2), mw[1][e + k4], mw[1][e + k4 + 1]);
                 }
               }
-              vcol = fmaf(vs, e0, vcol);
+              float vs_lo, vs_hi;
+              upk2(vs2, vs_lo, vs_hi);
+              vcol = fmaf(vs_lo + vs_hi, e0, vcol);
             } else {  // on the diagonal: one 2^x per element
               float vdiag = 0.f;
 #pragma unroll
