@@ -412,18 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_lo >= j0 + 15) {  // below the diagonal: factorised decay
               const float ei = ex2_approx(ai - pipe::lds_f(da + 4 * (j0 + 15)));
               const bool nomask = __all_sync(0xffffffffu, start_i <= j0);
+              const uint64_t ei2 = pk2(ei, ei);
+              uint64_t vr2 = pk2(0.f, 0.f);
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
                 const float4 f4 = pipe::lds_f4(df + 4 * (j0 + e));
-                const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
+                // two columns per packed fp32 instruction
+                upk2(mul2(pk2(dm[e], dm[e + 1]), mul2(pk2(f4.x, f4.y), ei2)), w[e], w[e + 1]);
+                upk2(mul2(pk2(dm[e + 2], dm[e + 3]), mul2(pk2(f4.z, f4.w), ei2)), w[e + 2], w[e + 3]);
+                if (!nomask) {
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  const float val = dm[e + m] * fv[m] * ei;
-                  w[e + m] = (nomask || j0 + e + m >= start_i) ? val : 0.f;
+                  for (int m = 0; m < 4; ++m) w[e + m] = j0 + e + m >= start_i ? w[e + m] : 0.f;
                 }
+                vr2 = fma2(pk2(w[e], w[e + 1]), pk2(cbv[e], cbv[e + 1]), vr2);
+                vr2 = fma2(pk2(w[e + 2], w[e + 3]), pk2(cbv[e + 2], cbv[e + 3]), vr2);
               }
-#pragma unroll
-              for (int e = 0; e < 16; ++e) vrow = fmaf(w[e], cbv[e], vrow);
+              float vr_lo, vr_hi;
+              upk2(vr2, vr_lo, vr_hi);
+              vrow += vr_lo + vr_hi;
             } else {  // on the diagonal
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {

@@ -384,14 +384,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (row_lo >= j0 + 15) {  // whole group below the diagonal: factorised decay
               const float ei = ex2_approx(ai - pipe::lds_f(da + 4 * (j0 + 15)));
               const bool nomask = __all_sync(0xffffffffu, start_i <= j0);
+              const uint64_t ei2 = pk2(ei, ei);
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
                 const float4 f4 = pipe::lds_f4(df + 4 * (j0 + e));
-                const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
+                // two columns per packed fp32 instruction
+                const uint64_t v01 = mul2(pk2(__uint_as_float(raw[p][e]), __uint_as_float(raw[p][e + 1])),
+                                          mul2(pk2(f4.x, f4.y), ei2));
+                const uint64_t v23 = mul2(pk2(__uint_as_float(raw[p][e + 2]), __uint_as_float(raw[p][e + 3])),
+                                          mul2(pk2(f4.z, f4.w), ei2));
+                upk2(v01, r[e], r[e + 1]);
+                upk2(v23, r[e + 2], r[e + 3]);
+                if (!nomask) {
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  const float val = __uint_as_float(raw[p][e + m]) * fv[m] * ei;
-                  r[e + m] = (nomask || j0 + e + m >= start_i) ? val : 0.f;
+                  for (int m = 0; m < 4; ++m) r[e + m] = j0 + e + m >= start_i ? r[e + m] : 0.f;
                 }
               }
             } else {  // group on the diagonal: one 2^x per element
