@@ -13,6 +13,13 @@
 // Roles as in the row kernel (22 warps, one CTA per SM).  Tensor memory:
 //   [0, 256) two slice slots {dM^T 64 | CB^T 64} | [256, 320) T | [320, 384) U |
 //   [384, 512) dB.
+// The transform warps write M^T and W^T, rounded to bf16, back into the slot's
+// CB^T columns they have just read (each warp its own 16 columns: M^T in the
+// first 8, W^T in the last 8, two values per column); the T and dB products
+// take their A operand from there, so the slice's operands never pass through
+// shared memory.  A slot's dM^T columns are refilled as soon as the transform
+// has read them; its CB^T columns once the T and dB products have read M^T and
+// W^T (slot_free).
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "tc_engine.cuh"
@@ -29,7 +36,7 @@ using pipe::parity;
 constexpr int kWarps = 22, kThreads = kWarps * 32, kEpiWarp0 = 18;
 constexpr int kTWarps = 16, kEWarps = 4, kTThreads = kTWarps * 32;
 constexpr int kNY = 3;  // dy slice ring
-constexpr int kNA = 2;  // transformed operand ring (M^T, W^T slices, wdt x)
+constexpr int kNA = 1;  // transformed operand in shared memory (wdt x, once per head)
 
 constexpr uint32_t kSmBJ = 0;                   // B_J: 2 K halves x [128 x 128 B]
 constexpr uint32_t kSmCR = kSmBJ + 32768;       // C rows i >= 128 J: 2 K halves x [256 x 128 B]
@@ -42,7 +49,7 @@ constexpr uint32_t kSmV = kSmDS + 16384;
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], g[256]}
 constexpr uint32_t kSmVC = kSmD + 2 * 2048;     // 2 x vcol partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVC + 2 * 2048;
-constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4 + 1;
+constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4 + 1 + 2;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -54,8 +61,9 @@ struct Unit {
 };
 
 // NP transformed 16-column groups of TMEM lane row `row` into the next NP
-// slots of the A ring (bf16, 128-byte swizzle): each slot waited for only when
-// its values are ready, one proxy fence, then one arrival per slot.
+// slots of the shared-memory operand ring (bf16, 128-byte swizzle): each slot
+// waited for only when its values are ready, one proxy fence, then one arrival
+// per slot.
 template <int NP>
 __device__ __forceinline__ void put_operands(const float (&v)[NP][16], uint32_t &na, uint32_t sA, int row, int cg,
                                              uint64_t *a_full, uint64_t *a_free, const WaitCtl &status) {
@@ -98,7 +106,8 @@ __device__ __forceinline__ Unit unit_of(const Problem &pr, int NTI, int nhb, int
 
 struct Bars {
   uint64_t *unit_full, *unit_free, *tu_full, *tu_free, *ds_full, *ds_free, *db_full, *db_free;
-  uint64_t *ring_full, *ring_free, *vec_full, *vec_free, *xt_full, *xt_free;  // [2]
+  uint64_t *ring_full, *slot_free, *vec_full, *vec_free, *xt_full, *xt_free;  // [2]
+  uint64_t *op_full;                                                          // [2]
   uint64_t *dy_full, *dy_free;                                                // [kNY]
   uint64_t *a_full, *a_free;                                                  // [kNA]
   uint64_t *drain;                                                            // the MMA issuer's final commit
@@ -113,7 +122,7 @@ struct Bars {
     db_full = b + 6;
     db_free = b + 7;
     ring_full = b + 8;
-    ring_free = b + 10;
+    slot_free = b + 10;
     vec_full = b + 12;
     vec_free = b + 14;
     xt_full = b + 16;
@@ -125,6 +134,7 @@ struct Bars {
     units.full = a_free + kNA;
     units.free = units.full + 2;
     drain = units.free + 2;
+    op_full = drain + 1;
     units.slot = slot;
   }
 };
@@ -154,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar.db_free, kEWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.ring_full[i], 1);
-      mbar_init(&bar.ring_free[i], kTWarps);
+      mbar_init(&bar.slot_free[i], 1);
+      mbar_init(&bar.op_full[i], kTWarps);
       mbar_init(&bar.vec_full[i], 1);
       mbar_init(&bar.vec_free[i], kTWarps + kEWarps);
       mbar_init(&bar.xt_full[i], 1);
@@ -289,14 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vb = nh & 1;
           const uint64_t dxt = dXT + vb * (16384 / 16);
           mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);
-          // slice item n: dM^T and CB^T of columns [64 s, 64 s + 64) into ring slot n % 2
+          // slice item n: dM^T and CB^T of columns [64 s, 64 s + 64) into slot n % 2.
+          // The transform of item n - 2 has read the slot (its op_full was waited
+          // for before item n - 1's products); CB^T waits for those products too.
           auto issue_item = [&](uint32_t n, int s) {
             const int rs = n & 1, ys = n % kNY;
-            if (n >= 2) mbar_wait(&bar.ring_free[rs], parity(n / 2 - 1), status);
             mbar_wait(&bar.dy_full[ys], parity(n / kNY), status);
             tc_fence_after();
             const uint32_t td = tmem + 128 * rs;
             pipe::umma_k<4>(td, dxt, dDY + ys * (8192 / 16), pipe::kStepK, pipe::kStepK, id_64, false);
+            if (n >= 2) mbar_wait(&bar.slot_free[rs], parity(n / 2 - 1), status);
+            tc_fence_after();
             const uint64_t dcs = dCR + s * (8192 / 16);
             pipe::umma_k<4>(td + 64, dBJ, dcs, pipe::kStepK, pipe::kStepK, id_64, false);
             pipe::umma_k<4>(td + 64, dBJ + 16384 / 16, dcs + 32768 / 16, pipe::kStepK, pipe::kStepK, id_64, true);
@@ -305,27 +319,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_item(m, 0);
           for (int s = 0; s < nsl; ++s) {
             if (s + 1 < nsl) issue_item(m + s + 1, s + 1);
-            const int ys = (m + s) % kNY;
-            // T += M^T_s dy_s
-            int as = na % kNA;
-            mbar_wait(&bar.a_full[as], parity(na / kNA), status);
+            const uint32_t n = m + s;
+            const int rs = n & 1, ys = n % kNY;
+            // M^T and W^T of item n in its slot (tensor memory): K step kk is the
+            // 16 columns of transform warp group kk
+            mbar_wait(&bar.op_full[rs], parity(n / 2), status);
             if (s == 0 && nh > 0) mbar_wait(bar.tu_free, parity(nh - 1), status);
             tc_fence_after();
-            pipe::umma_k<4>(tmem + kTmT, dA + as * (16384 / 16), dDYmn + ys * (8192 / 16), pipe::kStepK, pipe::kStepMN,
-                            id_t, s > 0);
-            umma_commit(&bar.a_free[as]);
+            const uint32_t top = tmem + 128 * rs + 64;
+            // T += M^T_s dy_s
+            pipe::umma_ts_k<4>(tmem + kTmT, top, dDYmn + ys * (8192 / 16), 16, pipe::kStepMN, id_t, s > 0);
             umma_commit(&bar.dy_free[ys]);
-            ++na;
             // dB += W^T_s C_s
-            as = na % kNA;
-            mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             if (first_db && nu > 0) mbar_wait(bar.db_free, parity(nu - 1), status);
             tc_fence_after();
-            pipe::umma_k<4>(tmem + kTmDB, dA + as * (16384 / 16), dCRmn + s * (8192 / 16), pipe::kStepK, pipe::kStepMN,
-                            id_db, !first_db);
+            pipe::umma_ts_k<4>(tmem + kTmDB, top + 8, dCRmn + s * (8192 / 16), 16, pipe::kStepMN, id_db, !first_db);
             first_db = false;
-            umma_commit(&bar.a_free[as]);
-            ++na;
+            umma_commit(&bar.slot_free[rs]);
           }
           m += nsl;
           // U = B_J dS^T, and dB += (wdt x) dS
@@ -356,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bar.db_full, parity(nu - 1));
       }
       if (nh > 0) mbar_wait_drain(bar.tu_full, parity(nh - 1));
-      for (uint32_t n = m > 2u ? m - 2u : 0u; n < m; ++n) mbar_wait_drain(&bar.ring_full[n & 1], parity(n / 2));
+      for (uint32_t n = m > 2u ? m - 2u : 0u; n < m; ++n) {
+        mbar_wait_drain(&bar.ring_full[n & 1], parity(n / 2));
+        mbar_wait_drain(&bar.slot_free[n & 1], parity(n / 2));
+      }
       for (uint32_t n = m > (uint32_t)kNY ? m - kNY : 0u; n < m; ++n)
         mbar_wait_drain(&bar.dy_free[n % kNY], parity(n / kNY));
       for (uint32_t n = na > (uint32_t)kNA ? na - kNA : 0u; n < na; ++n)
@@ -411,19 +424,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         float vcol = 0.f;
         for (int s = 0; s < nsl; ++s, ++m) {
           const int rs = m & 1, i0 = 128 * o.J + 64 * s + 16 * cg;
-          float mw[2][16];  // M^T, W^T of this slice
+          // M^T and W^T of this slice go, as bf16 pairs, over the CB^T columns this
+          // warp has just read (no other warp reads them): M^T in the first 8,
+          // W^T in the last 8, each half stored as soon as it is packed
+          const uint32_t tdst = pipe::tmem_quad(tmem + 128 * rs + 64, 16 * cg);
+          uint32_t mw[4], ww[4];
+          auto put_half = [tdst](int e, const uint32_t(&a)[4], const uint32_t(&b)[4]) {
+            const int off = e < 8 ? 0 : 4;  // columns 0-7 (e = 4) or 8-15 (e = 12) are packed
+            tmem_st4_async(tdst + off, a[0], a[1], a[2], a[3]);
+            tmem_st4_async(tdst + 8 + off, b[0], b[1], b[2], b[3]);
+          };
           mbar_wait(&bar.ring_full[rs], parity(m / 2), status);
           tc_fence_after();
           if (i0 + 15 < row_lo) {  // every column before every row: zero
-            pipe::warp_arrive(&bar.ring_free[rs]);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) mw[0][e] = mw[1][e] = 0.f;
+            for (int e = 0; e < 4; ++e) mw[e] = ww[e] = 0u;
+            put_half(4, mw, ww);
+            put_half(12, mw, ww);
           } else {
             float dm[16], cbv[16];
             tmem_ld16(pipe::tmem_quad(tmem + 128 * rs, 16 * cg), dm);
             tmem_ld16(pipe::tmem_quad(tmem + 128 * rs + 64, 16 * cg), cbv);
-            tc_fence_before();
-            pipe::warp_arrive(&bar.ring_free[rs]);
             if (i0 >= row_hi) {  // every column at or after every row: factorised decay
               const float e0 = ex2_approx(pipe::lds_f(ta + 4 * i0) - aj), ed = e0 * dt_j;
               const bool nomask = __all_sync(0xffffffffu, end_j >= i0 + 15);
@@ -443,38 +464,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint64_t g2 = pk2(gv[k4], gv[k4 + 1]), t2 = mul2(g2, ed2);
                   const uint64_t dm2 = pk2(dm[e + k4], dm[e + k4 + 1]), cb2 = pk2(cbv[e + k4], cbv[e + k4 + 1]);
                   vs2 = fma2(mul2(dm2, cb2), g2, vs2);
-                  upk2(mul2(cb2, t2), mw[0][e + k4], mw[0][e + k4 + 1]);
-                  upk2(mul2(dm2, t2), mw[1][e + k4], mw[1][e + k4 + 1]);
+                  float m0, m1, w0, w1;
+                  upk2(mul2(cb2, t2), m0, m1);
+                  upk2(mul2(dm2, t2), w0, w1);
+                  mw[((e + k4) / 2) & 3] = tc::pack_bf16x2(m0, m1);
+                  ww[((e + k4) / 2) & 3] = tc::pack_bf16x2(w0, w1);
                 }
+                if (e == 4 || e == 12) put_half(e, mw, ww);
               }
               float vs_lo, vs_hi;
               upk2(vs2, vs_lo, vs_hi);
               vcol = fmaf(vs_lo + vs_hi, e0, vcol);
-            } else {  // on the diagonal: one 2^x per element
+            } else {  // on the diagonal: one 2^x per element, the products two columns at a time
               float vdiag = 0.f;
+              const uint64_t dt2 = pk2(dt_j, dt_j);
+              uint64_t vc2 = pk2(0.f, 0.f);
 #pragma unroll
               for (int e = 0; e < 16; e += 4) {
                 const float4 a4 = pipe::lds_f4(ta + 4 * (i0 + e));
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                float ee[4], vx[4];
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
                   const int i = i0 + e + k4;
                   const bool ok = (unsigned)(i - j) <= (unsigned)(end_j - j);
-                  const float ee = ok ? ex2_approx(av[k4] - aj) : 0.f;
-                  const float vij = dm[e + k4] * cbv[e + k4];
+                  ee[k4] = ok ? ex2_approx(av[k4] - aj) : 0.f;
                   // the column sum leaves out i = j (it cancels exactly against the row
                   // sum's in the Acs adjoint); that term V_jj goes to its own slot
-                  if (i == j) vdiag = vij;
-                  vcol = fmaf(i == j ? 0.f : vij, ee, vcol);
-                  const float t1 = ee * dt_j;
-                  mw[0][e + k4] = cbv[e + k4] * t1;
-                  mw[1][e + k4] = dm[e + k4] * t1;
+                  const float vij = dm[e + k4] * cbv[e + k4];
+                  vdiag = i == j ? vij : vdiag;
+                  vx[k4] = i == j ? 0.f : vij;
                 }
+#pragma unroll
+                for (int k4 = 0; k4 < 4; k4 += 2) {
+                  const uint64_t e2 = pk2(ee[k4], ee[k4 + 1]), t2 = mul2(e2, dt2);
+                  vc2 = fma2(pk2(vx[k4], vx[k4 + 1]), e2, vc2);
+                  float m0, m1, w0, w1;
+                  upk2(mul2(pk2(cbv[e + k4], cbv[e + k4 + 1]), t2), m0, m1);
+                  upk2(mul2(pk2(dm[e + k4], dm[e + k4 + 1]), t2), w0, w1);
+                  mw[((e + k4) / 2) & 3] = tc::pack_bf16x2(m0, m1);
+                  ww[((e + k4) / 2) & 3] = tc::pack_bf16x2(w0, w1);
+                }
+                if (e == 4 || e == 12) put_half(e, mw, ww);
               }
+              float vc_lo, vc_hi;
+              upk2(vc2, vc_lo, vc_hi);
+              vcol += vc_lo + vc_hi;
               if ((unsigned)(j - i0) < 16u) tok[1 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + (size_t)o.c * pr.Q + j] = vdiag;
             }
           }
-          put_operands<2>(mw, na, sA, jl, cg, bar.a_full, bar.a_free, status);
+          tmem_wait_st();
+          tc_fence_before();
+          pipe::warp_arrive(&bar.op_full[rs]);
         }
         {  // wdt_j x_j, the A operand of the dS_end term of dB
           mbar_wait(&bar.xt_full[vb], parity(nh / 2), status);

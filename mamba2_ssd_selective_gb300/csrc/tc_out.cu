@@ -463,22 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float em = (has_off && cont) ? expf(pipe::lds_f(vacs + 4 * i)) : 0.f;
         pipe::warp_arrive(&bar.vec_free[vb]);
         const float Dh = __ldg(pr.D + h);
-        // x row first: its loads are in flight while the accumulators finish
-        uint4 xr[8];
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) xr[q8] = tc::ldg16(xrow + h * pr.P + 8 * q8);
+        // the x row's first 16 columns are loaded first, in flight while the
+        // accumulators finish, and each next 16 one step ahead
+        const bf16 *xh = xrow + h * pr.P;
+        uint4 xr0 = tc::ldg16(xh), xr1 = tc::ldg16(xh + 8);
         mbar_wait(&bar.acc_full[ab], parity(nh / 2), status);
         tc_fence_after();
         const uint32_t tacc = tmem + 256 + 128 * ab;
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
+          const uint4 xr[2] = {xr0, xr1};
+          const int cn = cc < 3 ? 16 * cc + 16 : 48;  // the last step reloads its own columns
+          xr0 = tc::ldg16(xh + cn);
+          xr1 = tc::ldg16(xh + cn + 8);
           float yd[16], yo[16];
           tmem_ld16(pipe::tmem_quad(tacc, 16 * cc), yd);
           if (has_off) tmem_ld16(pipe::tmem_quad(tacc + 64, 16 * cc), yo);
 #pragma unroll
           for (int q8 = 0; q8 < 2; ++q8) {
             float x[8], o8[8];
-            tc::unpack8(xr[2 * cc + q8], x);
+            tc::unpack8(xr[q8], x);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int col = 8 * q8 + e;

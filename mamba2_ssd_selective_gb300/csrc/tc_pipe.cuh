@@ -133,6 +133,16 @@ __device__ __forceinline__ void umma_k(uint32_t d, uint64_t a, uint64_t b, uint6
   for (int kk = 1; kk < NK; ++kk) umma_bf16(d, a + kk * sa, b + kk * sb, idesc, 1u);
 }
 
+// The same with A in tensor memory: K step kk takes A from the 8 columns at
+// a + kk * sa (sa >= 8 columns; the K steps need not be adjacent).
+template <int NK>
+__device__ __forceinline__ void umma_ts_k(uint32_t d, uint32_t a, uint64_t b, uint32_t sa, uint64_t sb, uint32_t idesc,
+                                          bool accumulate) {
+  umma_bf16_ts(d, a, b, idesc, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < NK; ++kk) umma_bf16_ts(d, a + kk * sa, b + kk * sb, idesc, 1u);
+}
+
 // TMEM address of (lane quadrant of this warp, column col)
 __device__ __forceinline__ uint32_t tmem_quad(uint32_t base, int col) {
   return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
