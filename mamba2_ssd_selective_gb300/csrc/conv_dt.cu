@@ -184,9 +184,26 @@ __global__ void __launch_bounds__(256) dt_prep_kernel(Problem pr, float *__restr
   const int c = blockIdx.x, h0 = blockIdx.y * kDtHeads, bb = blockIdx.z;
   const int nh = min(kDtHeads, pr.H - h0), t0 = c * pr.Q;
   const T *src = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h0;
-  for (int e = threadIdx.x; e < pr.Q * kDtHeads; e += 256) {
-    const int t = e / kDtHeads, hh = e % kDtHeads;
-    if (hh < nh) tile[t][hh] = to_f(src[(size_t)t * pr.dts + hh]);
+  // the block's heads of one token are contiguous: one 16-byte load per token
+  // (two for fp32) when the rows allow it, else one load per element
+  constexpr int kVec = 16 / (int)sizeof(T);
+  const bool vec = nh == kDtHeads && pr.dts % kVec == 0 && ((uintptr_t)pr.dt % 16) == 0;
+  if (vec) {
+    for (int t = threadIdx.x; t < pr.Q; t += 256) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(src + (size_t)t * pr.dts);
+#pragma unroll
+      for (int v = 0; v < kDtHeads / kVec; ++v) {
+        const uint4 u = __ldg(p + v);
+        const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) tile[t][v * kVec + k] = to_f(e[k]);
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < pr.Q * kDtHeads; e += 256) {
+      const int t = e / kDtHeads, hh = e % kDtHeads;
+      if (hh < nh) tile[t][hh] = to_f(src[(size_t)t * pr.dts + hh]);
+    }
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, i0 = lane * kDtPer;

@@ -571,24 +571,37 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
     const float dec = ac != 0.f ? ac * dtot : 0.f;
     float base[kDtTok], vcol[kDtTok], vd[kDtTok], wq[kDtTok], wv[kDtTok], qv[kDtTok], dtk[kDtTok];
     float wqsum = 0.f;
+    // the lane's kDtTok consecutive tokens of each per-token array: two 16-byte
+    // loads per array, all issued before any use (L and Q are multiples of 8)
+    float t0v[kDtTok], t3v[kDtTok], t5v[kDtTok], acv[kDtTok];
+    auto ld8 = [&](const float *a, float (&v)[kDtTok]) {
+      const float4 lo = __ldg(reinterpret_cast<const float4 *>(a)), hi = __ldg(reinterpret_cast<const float4 *>(a) + 1);
+      v[0] = lo.x, v[1] = lo.y, v[2] = lo.z, v[3] = lo.w, v[4] = hi.x, v[5] = hi.y, v[6] = hi.z, v[7] = hi.w;
+    };
+    const bool has = i0 < Q;  // Q is a multiple of kDtTok: a lane has all or none of its tokens
+    if (has) {
+      const size_t o = tb + i0;
+      ld8(dtv + o, dtk);
+      ld8(acs + o, acv);
+      ld8(tok + 4 * BHL + o, qv);
+      ld8(tok + 2 * BHL + o, vcol);
+      ld8(tok + 1 * BHL + o, vd);
+      ld8(tok + 0 * BHL + o, t0v);
+      ld8(tok + 3 * BHL + o, t3v);
+      ld8(tok + 5 * BHL + o, t5v);
+    }
 #pragma unroll
     for (int k = 0; k < kDtTok; ++k) {
-      const int i = i0 + k;
-      base[k] = vcol[k] = vd[k] = wq[k] = wv[k] = qv[k] = dtk[k] = 0.f;
-      if (i < Q) {
-        const size_t o = tb + i;
-        const float dti = dtv[o], ai = acs[o];
-        const float w = seq_of(pr, bb, t0 + i) == seq_last ? expf(acs_last - ai) : 0.f;
-        const float q = tok[4 * BHL + o];
-        vcol[k] = tok[2 * BHL + o];
-        vd[k] = tok[1 * BHL + o];
+      base[k] = wq[k] = wv[k] = 0.f;
+      if (has) {
+        const float w = seq_of(pr, bb, t0 + i0 + k) == seq_last ? expf(acs_last - acv[k]) : 0.f;
         wv[k] = w;
-        qv[k] = q;
-        dtk[k] = dti;
-        wq[k] = w * dti * q;
-        base[k] = tok[0 * BHL + o] - dti * vcol[k] + tok[3 * BHL + o] - wq[k];
-        dDp += tok[5 * BHL + o];
+        wq[k] = w * dtk[k] * qv[k];
+        base[k] = t0v[k] - dtk[k] * vcol[k] + t3v[k] - wq[k];
+        dDp += t5v[k];
         wqsum += wq[k];
+      } else {
+        vcol[k] = vd[k] = qv[k] = dtk[k] = 0.f;
       }
     }
     // dAcs at the chunk's last token also gets sum_j wdt_j q_j and the decay term,
@@ -611,6 +624,9 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
     }
     later -= run;  // exclusive: the lanes after this one
     const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h;
+    float zr[kDtTok];  // the raw dt inputs (one per token row), loaded together
+#pragma unroll
+    for (int k = 0; k < kDtTok; ++k) zr[k] = has ? to_f(dtr[(size_t)(i0 + k) * pr.dts]) : 0.f;
 #pragma unroll
     for (int k = 0; k < kDtTok; ++k) {
       const int i = i0 + k;
@@ -618,7 +634,7 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
         const float dda = suf[k] + later + tail;
         const float ddt = vcol[k] + vd[k] + wv[k] * qv[k] + A * dda;
         dAp = fmaf(dtk[k], dda, dAp);
-        const float dz = ddt * sigmoid_f(to_f(dtr[(size_t)i * pr.dts]) + bias);
+        const float dz = ddt * sigmoid_f(zr[k] + bias);
         dzp += dz;
         dzs[i][warp] = dz;
       }
