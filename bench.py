@@ -165,8 +165,8 @@ def kernel_work(shape, dtype: str) -> dict:
     f_off = b * nc * H * 2 * Q * N * P       # one Q x N x P product per chunk and head
     f_bc = b * nc * H * tri * 2 * N          # W B or W^T C: causal Q x Q x N
     w = {
-        "conv_fwd": ("mem", 0, b * L * Cd * 2 * eb),
-        "dt_prep": ("mem", 0, b * L * H * (eb + 8)),
+        # the conv forward's launch also runs the dt preparation (dt_raw in; dt, Acs out)
+        "conv_fwd": ("mem", 0, b * L * Cd * 2 * eb + b * L * H * (eb + 8)),
         "decay_tables": ("mem", 0, tok + 3 * b * H * nc * 4),
         # bf16 tensor-core path: the local pass only reduces (its combine re-forms the local states)
         "local_pass": ("mem", 0, (st if dtype == "bf16" else 2 * st) + seg),

@@ -189,8 +189,7 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
   T *const y_out = y;
   // the gated norm: a separate pass over the mixer output (written to the workspace)
   if (pr.z) y = reinterpret_cast<T *>(ws + w.ypre);
-  SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
-  SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
+  SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, dtv, acs, s));  // and dt_prep
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
                                                  const_cast<float *>(pr.dend), ablk, s));
   if constexpr (kIsBf16<T>) {
@@ -236,8 +235,7 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   int *status = reinterpret_cast<int *>(ws + w.status);
   const bool tc = use_tc<T>(pr);
   // recompute: conv, dt, CB, chunk states, local segment passes (and the scan)
-  SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, s));
-  SSD_LAUNCH("dt_prep", launch_dt_prep<T>(pr, dtv, acs, s));
+  SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, dtv, acs, s));  // and dt_prep
   SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
                                                  const_cast<float *>(pr.dend), ablk, s));
   if constexpr (kIsBf16<T>) {

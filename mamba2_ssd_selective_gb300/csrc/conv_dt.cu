@@ -116,72 +116,18 @@ __device__ __forceinline__ void conv_fwd_rows(const T (*tile)[kFwdCh], const int
   }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict__ u) {
-  constexpr int kRows = kFwdTok + 3;
-  constexpr int kChunk = 16 / (int)sizeof(T);  // channels per 16-byte copy
-  constexpr int kCpr = kFwdCh / kChunk;          // copies per row
-  __shared__ __align__(16) T tile[kRows][kFwdCh];
-  __shared__ int seqs[kRows];
-  const int t0 = blockIdx.y * kFwdTok, bb = blockIdx.z;
-  const ChanTile<T> ct = chan_tile<T>(pr, nullptr, bb, blockIdx.x, kFwdCh);
-  const int c0 = ct.c0, nch = ct.nch;
-  for (int q = threadIdx.x; q < kRows * kCpr; q += 256) {
-    const int r = q / kCpr, cc = (q % kCpr) * kChunk, t = t0 - 3 + r;
-    if (cc >= nch) continue;
-    const bool ok = t >= 0 && t < pr.L;
-    const T *g = ct.src + (ok ? (size_t)t * ct.st : 0) + cc;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(
-                     &tile[r][cc]))),
-                 "l"(g), "r"(ok ? 16 : 0)
-                 : "memory");
-  }
-  for (int r = threadIdx.x; r < kRows; r += 256) {
-    const int t = t0 - 3 + r;
-    seqs[r] = (t >= 0 && t < pr.L) ? seq_of(pr, bb, t) : -1;
-  }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
-  const int cp = threadIdx.x % (kFwdCh / 2), tq = threadIdx.x / (kFwdCh / 2);
-  const int c = c0 + 2 * cp;
-  if (2 * cp >= nch) return;
-  float w[2][4], bias[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
-    w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
-    bias[q] = pr.conv_b[c + q];
-  }
-  constexpr int kPer = kFwdTok / 4;
-  const int r0 = tq * kPer;  // first output row (token t0 + r0), inputs at rows r0 .. r0 + 3
-  T *dst = u + ((size_t)bb * pr.L + t0 + r0) * pr.Cd + c;
-  const int tend = min(kPer, pr.L - (t0 + r0));
-  if (tend <= 0) return;
-  if (pr.seq_idx) {
-    conv_fwd_rows<T, true>(tile, seqs, w, bias, r0, cp, tend, dst, pr.Cd);
-  } else if (tend == kPer) {  // full run: constant trip count, unrolled
-    conv_fwd_rows<T, false>(tile, seqs, w, bias, r0, cp, kPer, dst, pr.Cd);
-  } else {
-    conv_fwd_rows<T, false>(tile, seqs, w, bias, r0, cp, tend, dst, pr.Cd);
-  }
-}
-
-template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s) {
-  dim3 grid(chan_tiles(pr, kFwdCh), (pr.L + kFwdTok - 1) / kFwdTok, pr.b);
-  conv_fwd_kernel<T><<<grid, 256, 0, s>>>(pr, u);
-}
-
 // dt = softplus(dt_raw + dt_bias); acs = inclusive cumsum of dt*A within each
 // chunk (A = -exp(A_log)); layouts (b, H, L).  A block takes one chunk of one
 // row and 8 heads: the chunk's dt_raw for those heads (16 contiguous bytes per
 // token in bf16) is staged in shared memory, then each warp takes a head, a
 // lane 8 consecutive tokens: softplus, the lane's running sum, and the lanes'
-// exclusive prefix by shuffles.
+// exclusive prefix by shuffles.  These blocks run inside the conv forward's
+// launch (its last grid columns), in the conv tile's shared memory.
 constexpr int kMaxChunk = 256, kDtHeads = 8, kDtPer = kMaxChunk / 32;
 template <typename T>
-__global__ void __launch_bounds__(256) dt_prep_kernel(Problem pr, float *__restrict__ dtv, float *__restrict__ acs) {
-  __shared__ float tile[kMaxChunk][kDtHeads + 1];
-  const int c = blockIdx.x, h0 = blockIdx.y * kDtHeads, bb = blockIdx.z;
+__device__ __forceinline__ void dt_prep_block(const Problem &pr, float *__restrict__ dtv, float *__restrict__ acs,
+                                              int c, int hgrp, int bb, float (*tile)[kDtHeads + 1]) {
+  const int h0 = hgrp * kDtHeads;
   const int nh = min(kDtHeads, pr.H - h0), t0 = c * pr.Q;
   const T *src = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h0;
   // the block's heads of one token are contiguous: one 16-byte load per token
@@ -243,9 +189,73 @@ __global__ void __launch_bounds__(256) dt_prep_kernel(Problem pr, float *__restr
   }
 }
 
-template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *acs, cudaStream_t s) {
-  dt_prep_kernel<T><<<dim3(pr.nc, (pr.H + kDtHeads - 1) / kDtHeads, pr.b), 256, 0, s>>>(pr, dtv, acs);
+// Grid columns [0, conv_x) are conv tiles; the columns after them take the dt
+// preparation of (chunk, group of kDtHeads heads) pairs, numbered column-major
+// over (column, token tile) within a batch row.
+template <typename T>
+__global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict__ u, float *__restrict__ dtv,
+                                                       float *__restrict__ acs, int conv_x, int dt_hg) {
+  constexpr int kRows = kFwdTok + 3;
+  constexpr int kChunk = 16 / (int)sizeof(T);  // channels per 16-byte copy
+  constexpr int kCpr = kFwdCh / kChunk;          // copies per row
+  __shared__ __align__(16) T tile[kRows][kFwdCh];
+  __shared__ int seqs[kRows];
+  static_assert(sizeof(tile) >= sizeof(float) * kMaxChunk * (kDtHeads + 1), "dt tile inside the conv tile");
+  if ((int)blockIdx.x >= conv_x) {
+    const int id = ((int)blockIdx.x - conv_x) * (int)gridDim.y + (int)blockIdx.y, c = id / dt_hg;
+    if (c < pr.nc)
+      dt_prep_block<T>(pr, dtv, acs, c, id % dt_hg, blockIdx.z, reinterpret_cast<float(*)[kDtHeads + 1]>(&tile[0][0]));
+    return;
+  }
+  const int t0 = blockIdx.y * kFwdTok, bb = blockIdx.z;
+  const ChanTile<T> ct = chan_tile<T>(pr, nullptr, bb, blockIdx.x, kFwdCh);
+  const int c0 = ct.c0, nch = ct.nch;
+  for (int q = threadIdx.x; q < kRows * kCpr; q += 256) {
+    const int r = q / kCpr, cc = (q % kCpr) * kChunk, t = t0 - 3 + r;
+    if (cc >= nch) continue;
+    const bool ok = t >= 0 && t < pr.L;
+    const T *g = ct.src + (ok ? (size_t)t * ct.st : 0) + cc;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(
+                     &tile[r][cc]))),
+                 "l"(g), "r"(ok ? 16 : 0)
+                 : "memory");
+  }
+  for (int r = threadIdx.x; r < kRows; r += 256) {
+    const int t = t0 - 3 + r;
+    seqs[r] = (t >= 0 && t < pr.L) ? seq_of(pr, bb, t) : -1;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const int cp = threadIdx.x % (kFwdCh / 2), tq = threadIdx.x / (kFwdCh / 2);
+  const int c = c0 + 2 * cp;
+  if (2 * cp >= nch) return;
+  float w[2][4], bias[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float4 wq = reinterpret_cast<const float4 *>(pr.conv_w)[c + q];
+    w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
+    bias[q] = pr.conv_b[c + q];
+  }
+  constexpr int kPer = kFwdTok / 4;
+  const int r0 = tq * kPer;  // first output row (token t0 + r0), inputs at rows r0 .. r0 + 3
+  T *dst = u + ((size_t)bb * pr.L + t0 + r0) * pr.Cd + c;
+  const int tend = min(kPer, pr.L - (t0 + r0));
+  if (tend <= 0) return;
+  if (pr.seq_idx) {
+    conv_fwd_rows<T, true>(tile, seqs, w, bias, r0, cp, tend, dst, pr.Cd);
+  } else if (tend == kPer) {  // full run: constant trip count, unrolled
+    conv_fwd_rows<T, false>(tile, seqs, w, bias, r0, cp, kPer, dst, pr.Cd);
+  } else {
+    conv_fwd_rows<T, false>(tile, seqs, w, bias, r0, cp, tend, dst, pr.Cd);
+  }
 }
+
+template <typename T> void launch_conv_fwd(const Problem &pr, T *u, float *dtv, float *acs, cudaStream_t s) {
+  const int conv_x = chan_tiles(pr, kFwdCh), ny = (pr.L + kFwdTok - 1) / kFwdTok;
+  const int dt_hg = (pr.H + kDtHeads - 1) / kDtHeads, dt_x = (pr.nc * dt_hg + ny - 1) / ny;
+  conv_fwd_kernel<T><<<dim3(conv_x + dt_x, ny, pr.b), 256, 0, s>>>(pr, u, dtv, acs, conv_x, dt_hg);
+}
+
 
 // Conv + SiLU backward over a tile of kConvBwdTok tokens x kBwdCh channels (one
 // region of xBC):
@@ -556,10 +566,8 @@ void launch_cu_seqlens(const int *cu, int nseq, int *seq_idx, int total, cudaStr
   cu_seqlens_kernel<<<(total + 255) / 256, 256, 0, s>>>(cu, nseq, seq_idx, total);
 }
 
-template void launch_conv_fwd<float>(const Problem &, float *, cudaStream_t);
-template void launch_conv_fwd<__nv_bfloat16>(const Problem &, __nv_bfloat16 *, cudaStream_t);
-template void launch_dt_prep<float>(const Problem &, float *, float *, cudaStream_t);
-template void launch_dt_prep<__nv_bfloat16>(const Problem &, float *, float *, cudaStream_t);
+template void launch_conv_fwd<float>(const Problem &, float *, float *, float *, cudaStream_t);
+template void launch_conv_fwd<__nv_bfloat16>(const Problem &, __nv_bfloat16 *, float *, float *, cudaStream_t);
 template void launch_conv_bwd<float>(const Problem &, const float *, const BcParts &, const GradOut &, float *, int,
                                      cudaStream_t);
 template void launch_conv_bwd<__nv_bfloat16>(const Problem &, const float *, const BcParts &, const GradOut &, float *,

@@ -14,8 +14,8 @@ struct GradOut {  // raw-input gradient destinations (activation dtype)
 };
 
 // conv + dt (conv_dt.cu)
-template <typename T> void launch_conv_fwd(const Problem &pr, T *u, cudaStream_t s);
-template <typename T> void launch_dt_prep(const Problem &pr, float *dtv, float *acs, cudaStream_t s);
+// conv + SiLU forward, with the dt preparation (dt and the chunk-local Acs) in the same launch
+template <typename T> void launch_conv_fwd(const Problem &pr, T *u, float *dtv, float *acs, cudaStream_t s);
 // dB / dC of the post-conv B and C channels as fixed-order sums of per-head-block
 // partials (b, L, nsub, N): the partials of group g are [g * spg, (g + 1) * spg)
 struct BcParts {
