@@ -54,13 +54,11 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_state_kernel(Problem pr, c
   Carve<EngPair> sm(smem_raw);
   const int c = blockIdx.x, h0 = 2 * blockIdx.y, bb = blockIdx.z;
   const ChunkIds id0 = make_ids(pr, c, h0, bb);
-  load_wdt_pair(pr, c, h0, bb, dtv, acs, wdt0, wdt1);
   const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
   const bf16 *ub = u + ((size_t)bb * pr.L + id0.t0) * Cd;
   const int offB = HP + id0.g * N;
   EngPair eng;
   eng.init(sm.ring, sm.bars, status);
-  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
   auto fa = [&](int m0, int k) { return static_cast<const void *>(ub + (size_t)k * Cd + offB + m0); };
   auto fbl = [&](int n0, int k) { return tc::ldg16(ub + (size_t)k * Cd + (h0 + (n0 >> 6)) * P + (n0 & 63)); };
   auto fbm = [&](uint4 raw, int n0, int k) {
@@ -71,7 +69,19 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_state_kernel(Problem pr, c
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  eng.contract_pipelined(tmem, pr.Q, fa, fbl, fbm);
+  // the first slice's loads fly while the weights are formed and TMEM is allocated
+  uint4 cur[EngPair::PER_B];
+  eng.prefetch0(fa, fbl, cur);
+  // the rest of the chunk's rows hinted into L2 at once: per token the B row and
+  // the pair's x row (two 128-byte lines each), one line per thread and pass
+  for (int k0 = 64; k0 < pr.Q; k0 += 64) {
+    const int r = threadIdx.x >> 2, q = threadIdx.x & 3;
+    const bf16 *row = ub + (size_t)(k0 + r) * Cd + (q < 2 ? offB + 64 * q : h0 * P + 64 * (q - 2));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+  }
+  load_wdt_pair(pr, c, h0, bb, dtv, acs, wdt0, wdt1);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
+  eng.contract(tmem, pr.Q, fa, fbl, fbm, cur);
   eng.finish();
   if (tc::owns_row()) {
   const int n = threadIdx.x;
@@ -105,14 +115,12 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const
   Carve<EngPair> sm(smem_raw);
   const int c = blockIdx.x, h0 = 2 * blockIdx.y, bb = blockIdx.z;
   const ChunkIds id0 = make_ids(pr, c, h0, bb);
-  load_em_pair(pr, c, h0, bb, acs, em0, em1);
   const int Cd = pr.Cd, P = pr.P, N = pr.N, HP = pr.H * pr.P;
   const bf16 *ub = u + ((size_t)bb * pr.L + id0.t0) * Cd;
   const bf16 *dyb = dy + ((size_t)bb * pr.L + id0.t0) * HP;
   const int offC = HP + pr.G * N + id0.g * N;
   EngPair eng;
   eng.init(sm.ring, sm.bars, status);
-  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
   auto fa = [&](int m0, int i) { return static_cast<const void *>(ub + (size_t)i * Cd + offC + m0); };
   auto fbl = [&](int n0, int i) { return tc::ldg16(dyb + (size_t)i * HP + (h0 + (n0 >> 6)) * P + (n0 & 63)); };
   auto fbm = [&](uint4 raw, int n0, int i) {
@@ -123,7 +131,20 @@ __global__ void __launch_bounds__(tc::kThreads, 3) tc_z_kernel(Problem pr, const
     for (int q = 0; q < 8; ++q) x[q] *= s;
     return tc::pack8(x);
   };
-  eng.contract_pipelined(tmem, pr.Q, fa, fbl, fbm);
+  // the first slice's loads fly while the weights are formed and TMEM is allocated
+  uint4 cur[EngPair::PER_B];
+  eng.prefetch0(fa, fbl, cur);
+  // the rest of the chunk's rows hinted into L2 at once: per token the C row and
+  // the pair's dy row (two 128-byte lines each), one line per thread and pass
+  for (int k0 = 64; k0 < pr.Q; k0 += 64) {
+    const int r = threadIdx.x >> 2, q = threadIdx.x & 3;
+    const bf16 *row =
+        q < 2 ? ub + (size_t)(k0 + r) * Cd + offC + 64 * q : dyb + (size_t)(k0 + r) * HP + h0 * P + 64 * (q - 2);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+  }
+  load_em_pair(pr, c, h0, bb, acs, em0, em1);
+  const uint32_t tmem = tc::tmem_alloc_cta(sm.tslot, 128);
+  eng.contract(tmem, pr.Q, fa, fbl, fbm, cur);
   eng.finish();
   if (tc::owns_row()) {
   const int n = threadIdx.x;

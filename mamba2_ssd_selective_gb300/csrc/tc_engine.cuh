@@ -99,31 +99,37 @@ struct Engine {
   // software-pipelined: the loads of slice s+1 (A's copies and B's registers)
   // are issued before slice s's B is transformed and stored and its MMAs
   // issued, so a slice of loads is always in flight behind the one being
-  // staged.  Must be called by all threads.
-  template <class FAL, class FBL, class FBM>
-  __device__ __forceinline__ void contract_pipelined(uint32_t tmem_d, int nk, const FAL &fal, const FBL &fbl,
-                                                     const FBM &fbm) {
-    static_assert(NSTAGE >= 2 && NT % 64 == 0, "pipelined contraction: two stages, whole MN atoms");
-    using Raw = decltype(fbl(0, 0));
-    constexpr int CPR = NT / 8, PER_B = (NT * 8) / kThreads;
-    Raw cur[PER_B], nxt[PER_B];
-    auto issue = [&](int s, Raw(&raw)[PER_B]) {
-      const int st = s % NSTAGE, k0 = 64 * s;
-      if (uses[st] > 0) wait_mma(&bars[st], (uses[st] - 1) & 1);
-      stage_A(ring + st * STAGE_BYTES, k0, fal);
-      asm volatile("cp.async.commit_group;" ::: "memory");
+  // staged.  Split in two so that the caller can issue slice 0's loads first
+  // and overlap them with its own prologue (per-token weights, TMEM
+  // allocation): prefetch0() issues them into `cur`, contract() runs the rest.
+  // Both must be called by all threads.
+  static constexpr int CPR = NT / 8, PER_B = (NT * 8) / kThreads;
+  template <class FAL, class FBL, class Raw>
+  __device__ __forceinline__ void issue(int s, const FAL &fal, const FBL &fbl, Raw (&raw)[PER_B]) {
+    const int st = s % NSTAGE, k0 = 64 * s;
+    if (uses[st] > 0) wait_mma(&bars[st], (uses[st] - 1) & 1);
+    stage_A(ring + st * STAGE_BYTES, k0, fal);
+    asm volatile("cp.async.commit_group;" ::: "memory");
 #pragma unroll
-      for (int q = 0; q < PER_B; ++q) {
-        const int e = threadIdx.x + q * kThreads, r = e / CPR, c = e % CPR;
-        raw[q] = fbl(c * 8, k0 + r);
-      }
-    };
+    for (int q = 0; q < PER_B; ++q) {
+      const int e = threadIdx.x + q * kThreads, r = e / CPR, c = e % CPR;
+      raw[q] = fbl(c * 8, k0 + r);
+    }
+  }
+  template <class FAL, class FBL, class Raw>
+  __device__ __forceinline__ void prefetch0(const FAL &fal, const FBL &fbl, Raw (&cur)[PER_B]) {
+    static_assert(NSTAGE >= 2 && NT % 64 == 0, "pipelined contraction: two stages, whole MN atoms");
+    issue(0, fal, fbl, cur);
+  }
+  template <class FAL, class FBL, class FBM, class Raw>
+  __device__ __forceinline__ void contract(uint32_t tmem_d, int nk, const FAL &fal, const FBL &fbl, const FBM &fbm,
+                                           Raw (&cur)[PER_B]) {
+    Raw nxt[PER_B];
     const int ns = nk / 64;
-    issue(0, cur);
     for (int s = 0; s < ns; ++s) {
       const int st = s % NSTAGE, k0 = 64 * s;
       const bool more = s + 1 < ns;
-      if (more) issue(s + 1, nxt);
+      if (more) issue(s + 1, fal, fbl, nxt);
       uint8_t *A = ring + st * STAGE_BYTES, *B = A + A_BYTES;
 #pragma unroll
       for (int q = 0; q < PER_B; ++q) {
