@@ -172,7 +172,9 @@ def kernel_work(shape, dtype: str) -> dict:
         "local_pass": ("mem", 0, (st if dtype == "bf16" else 2 * st) + seg),
         "seg_scan": ("mem", 0, 2 * seg + b * H * PN * 4),
         "combine_state": ("mem", 0, st + st16 + seg),
-        "local_rev": ("mem", 0, 2 * st + seg),
+        # Z in, and the local gradients out only when the backward combine does not
+        # re-form them itself (bf16 path with up to 8 chunks per segment)
+        "local_rev": ("mem", 0, (1 if (dtype == "bf16" and nc // S <= 8) else 2) * st + seg),
         "seg_rscan": ("mem", 0, 2 * seg),
         # bf16 path: the states' decay term (combine_bwd) and dy . x (tc_bwd_col) come precomputed
         "chunk_dt": ("mem", 0, 8 * tok + (0 if dtype == "bf16" else 4 * st + 2 * x) + 2 * b * L * H * eb),

@@ -275,7 +275,13 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
     if (tc) SSD_LAUNCH("tc_chunk_z", launch_tc_z(pr, u, dy, dtv, acs, dsl, status, s));
   }
   if (!tc) SSD_LAUNCH("chunk_z", launch_chunk_z<T>(pr, u, dy, acs, dsl, s));
-  SSD_LAUNCH("local_rev", launch_local_rev(pr, acs, dsl, gext, s));
+  // the tensor-core path's backward combine re-forms the local gradients from Z
+  // for segments of up to 8 chunks, so the local pass then writes only summaries
+  bool write_local = true;
+  if constexpr (kIsBf16<T>) {
+    if (tc && combine_bwd_local_cps(pr) > 0) write_local = false;
+  }
+  SSD_LAUNCH("local_rev", launch_local_rev(pr, acs, dsl, gext, write_local, s));
   SSD_LAUNCH("seg_rscan",
              launch_seg_rscan(pr, gext, ablk, dfinal, gout, pr.init ? g->dinitial_states : nullptr, s));
   // chunk gradients

@@ -47,7 +47,13 @@ void launch_combine_bwd(const Problem &pr, const float *sc, const float *segin, 
 void launch_local_pass(const Problem &pr, float *sst, float *sext, bool write_local, cudaStream_t s);
 void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, float *segin, float *final_state,
                      cudaStream_t s);
-void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s);
+// write_local: overwrite dsl's Z with the local gradients at the chunk ends
+// (else only the segment summaries gext are written)
+void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, bool write_local,
+                      cudaStream_t s);
+// chunks per segment up to which the backward combine re-forms the local
+// gradients from Z itself (0: it reads them as the local pass wrote them)
+int combine_bwd_local_cps(const Problem &pr);
 void launch_seg_rscan(const Problem &pr, const float *gext, const float *ablk, const float *dfinal, float *gout,
                       float *dinit, cudaStream_t s);
 // per-sequence final states of a packed row (varlen.cu); sst_local: sst holds

@@ -147,9 +147,12 @@ void launch_seg_scan(const Problem &pr, const float *sext, const float *ablk, fl
 // Local reverse pass of segment k from dS = 0 at the segment end:
 //   dS_end[c] = dS;  dS <- Z[c] + a_c * dS   (c from the last chunk down)
 // where Z[c] (held in dsl on entry) is the adjoint the chunk's own outputs send
-// to the state entering it.  Overwrites dsl[c] with the local gradient at the
-// chunk's end and writes g_ext[k] = gradient w.r.t. the segment's initial state.
-// Same access pattern as local_pass_kernel, walking the chunks backwards.
+// to the state entering it.  Writes g_ext[k] = gradient w.r.t. the segment's
+// initial state and (WriteLocal) overwrites dsl[c] with the local gradient at
+// the chunk's end; without it dsl keeps Z and the backward combine re-forms the
+// local gradients itself.  Same access pattern as local_pass_kernel, walking the
+// chunks backwards.
+template <bool WriteLocal>
 __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float *__restrict__ acs,
                                                         float *__restrict__ dsl, float *__restrict__ gext) {
   const int PN = pr.P * pr.N, PN4 = PN / 4;
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float 
       }
     }
     // the recurrence runs down the chunks; results are kept and stored in
-    // increasing address order afterwards
+    // increasing address order afterwards (when the per-chunk states are wanted)
     float4 outv[kScanBatch][kScanVec4];
 #pragma unroll
     for (int q = kScanBatch - 1; q >= 0; --q) {
@@ -192,22 +195,28 @@ __global__ void __launch_bounds__(256) local_rev_kernel(Problem pr, const float 
         }
       }
     }
+    if (WriteLocal) {
 #pragma unroll
-    for (int q = 0; q < kScanBatch; ++q)
-      if (q < nb) {
+      for (int q = 0; q < kScanBatch; ++q)
+        if (q < nb) {
 #pragma unroll
-        for (int u = 0; u < kScanVec4; ++u)
-          if (e4[u] < PN4) base[(size_t)(c0 + q) * cstride4 + e4[u]] = outv[q][u];
-      }
+          for (int u = 0; u < kScanVec4; ++u)
+            if (e4[u] < PN4) base[(size_t)(c0 + q) * cstride4 + e4[u]] = outv[q][u];
+        }
+    }
   }
 #pragma unroll
   for (int u = 0; u < kScanVec4; ++u)
     if (e4[u] < PN4) reinterpret_cast<float4 *>(gext + (((size_t)bb * pr.S + k) * pr.H + h) * PN)[e4[u]] = dS[u];
 }
 
-void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, cudaStream_t s) {
+void launch_local_rev(const Problem &pr, const float *acs, float *dsl, float *gext, bool write_local,
+                      cudaStream_t s) {
   dim3 grid((pr.P * pr.N / 4 + kScanElems4 - 1) / kScanElems4, pr.H, pr.b * pr.S);
-  local_rev_kernel<<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
+  if (write_local)
+    local_rev_kernel<true><<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
+  else
+    local_rev_kernel<false><<<grid, 256, 0, s>>>(pr, acs, dsl, gext);
 }
 
 // 4 floats -> 4 bf16 (8 bytes)
@@ -284,6 +293,7 @@ void launch_combine_state(const Problem &pr, const float *sc, const float *segin
 // the chunk's decay term of the dt adjoint, sdp[g, b, c, h] = <dS[c], S_in[c]>
 // over this block's elements (fp32; the consumer multiplies by a_c and sums
 // the groups in order).  S_seg and G_out are read once per segment.
+template <int MaxCps>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const float *__restrict__ sc,
                                                           const float *__restrict__ segin,
                                                           const float *__restrict__ dsl,
@@ -308,6 +318,38 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const floa
     GI[u] = e4[u] < PN4 ? gi4[e4[u]] : S[u];
     GO[u] = e4[u] < PN4 ? go4[e4[u]] : S[u];
   }
+  // MaxCps > 0: dsl still holds Z (the local pass kept only the segment
+  // summaries); the local gradients dS[c] at the chunk ends are re-formed here
+  // by the same downward recurrence, dS[c] = sum_{c' > c} (decays) Z[c'], into
+  // this thread's own shared-memory slots (no barrier needed)
+  extern __shared__ float4 zloc[];  // [MaxCps][kScanVec4][256]
+  if constexpr (MaxCps > 0) {
+    // all of the segment's Z loads first (in flight together), then the recurrence
+    float4 zz[MaxCps][kScanVec4];
+    float dec[MaxCps];
+#pragma unroll
+    for (int c = 0; c < MaxCps; ++c) {
+      dec[c] = c < pr.cps ? chunk_decay(pr, bb, h, k * pr.cps + c) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kScanVec4; ++u)
+        zz[c][u] = (c < pr.cps && e4[u] < PN4) ? z4[(size_t)c * cstride4 + e4[u]] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 G[kScanVec4];
+#pragma unroll
+    for (int u = 0; u < kScanVec4; ++u) G[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = MaxCps - 1; c >= 0; --c) {
+      if (c < pr.cps) {
+        const float a = dec[c];
+#pragma unroll
+        for (int u = 0; u < kScanVec4; ++u) {
+          zloc[(c * kScanVec4 + u) * 256 + threadIdx.x] = G[u];
+          G[u] = make_float4(fmaf(a, G[u].x, zz[c][u].x), fmaf(a, G[u].y, zz[c][u].y), fmaf(a, G[u].z, zz[c][u].z),
+                             fmaf(a, G[u].w, zz[c][u].w));
+        }
+      }
+    }
+  }
   const size_t BNH = (size_t)pr.b * pr.nc * pr.H;
   for (int c0 = 0; c0 < pr.cps; c0 += kScanBatch) {
     const int nb = min(kScanBatch, pr.cps - c0);
@@ -324,7 +366,8 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const floa
         for (int u = 0; u < kScanVec4; ++u)
           if (e4[u] < PN4) {
             v[q][u] = sc4[(size_t)(c0 + q) * cstride4 + e4[u]];
-            z[q][u] = z4[(size_t)(c0 + q) * cstride4 + e4[u]];
+            z[q][u] = MaxCps > 0 ? zloc[((c0 + q) * kScanVec4 + u) * 256 + threadIdx.x]
+                                 : z4[(size_t)(c0 + q) * cstride4 + e4[u]];
           }
       }
     }
@@ -353,10 +396,24 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(Problem pr, const floa
   }
 }
 
+int combine_bwd_local_cps(const Problem &pr) { return pr.cps <= 4 ? 4 : pr.cps <= 8 ? 8 : 0; }
+
 void launch_combine_bwd(const Problem &pr, const float *sc, const float *segin, const float *dsl, const float *gout,
                         __nv_bfloat16 *sin16, __nv_bfloat16 *dse16, float *sdp, cudaStream_t s) {
-  combine_bwd_kernel<<<dim3(scan_groups(pr), pr.H, pr.b * pr.S), 256, 0, s>>>(pr, sc, segin, dsl, gout, sin16, dse16,
-                                                                             sdp);
+  const dim3 grid(scan_groups(pr), pr.H, pr.b * pr.S);
+  const int m = combine_bwd_local_cps(pr);
+  const int smem = m * kScanVec4 * 256 * (int)sizeof(float4);
+  if (m == 4) {
+    combine_bwd_kernel<4><<<grid, 256, smem, s>>>(pr, sc, segin, dsl, gout, sin16, dse16, sdp);
+  } else if (m == 8) {
+    static bool once = (cudaFuncSetAttribute(combine_bwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             8 * kScanVec4 * 256 * (int)sizeof(float4)),
+                        true);
+    (void)once;
+    combine_bwd_kernel<8><<<grid, 256, smem, s>>>(pr, sc, segin, dsl, gout, sin16, dse16, sdp);
+  } else {
+    combine_bwd_kernel<0><<<grid, 256, 0, s>>>(pr, sc, segin, dsl, gout, sin16, dse16, sdp);
+  }
 }
 
 // Reverse exclusive scan: G_out[S-1] = dfinal; G_out[k-1] = a_block[k]*G_out[k] + g_ext[k].
