@@ -180,8 +180,8 @@ def kernel_work(shape, dtype: str) -> dict:
         "chunk_dt": ("mem", 0, 8 * tok + (0 if dtype == "bf16" else 4 * st + 2 * x) + 2 * b * L * H * eb),
         "combine_bwd": ("mem", 0, 2 * st + 2 * seg + 2 * st16 + b * nc * H * 4 * ((P * N + 2047) // 2048)),
         # the B / C channels' gradients come as head-block partials, summed while staging
-        "conv_bwd": ("mem", 0, b * L * (Cd * 2 * eb + HP * 4) + 2 * parts + b * (L // 64) * Cd * 20),
-        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 64) * Cd * 20),
+        "conv_bwd": ("mem", 0, b * L * (Cd * 2 * eb + HP * 4) + 2 * parts + b * (L // 128) * Cd * 20),
+        "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 128) * Cd * 20),
         "tc_chunk_state": ("tensor", f_state, x + bc + st),
         "tc_chunk_z": ("tensor", f_state, x + bc + st),
         # persistent kernels: CB is formed on chip, W never leaves the SM

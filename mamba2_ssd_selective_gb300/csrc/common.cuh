@@ -106,7 +106,7 @@ __device__ __forceinline__ float decay_end(const Problem &pr, int b, int h, int 
 
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kConvBwdTok = 64;  // tokens per conv-backward block (one set of parameter partials each)
+constexpr int kConvBwdTok = 128;  // tokens per conv-backward block (one set of parameter partials each)
 
 // Elements of the P x N state handled by one block of the segment-walk kernels
 // (local pass, reverse pass, combines): 256 threads x two float4 groups.

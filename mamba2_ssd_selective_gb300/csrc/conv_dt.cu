@@ -279,10 +279,12 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
   constexpr int kXRows = kTok + 6;  // raw inputs, tokens t0-3 .. t0+kTok+2
   constexpr int kDRows = kTok + 3;  // du / dv, tokens t0 .. t0+kTok+2
   constexpr int kChunk = 16 / (int)sizeof(T);
-  __shared__ __align__(16) T xr[kXRows][kBwdCh];
-  __shared__ __align__(16) float dv[kDRows][kBwdCh];
-  __shared__ int seqs[kXRows];
-  __shared__ float red[4][kBwdCh][5];
+  // dynamic shared memory (conv_bwd_smem bytes): dv | xr | seqs | red
+  extern __shared__ __align__(16) uint8_t conv_smem[];
+  float(*dv)[kBwdCh] = reinterpret_cast<float(*)[kBwdCh]>(conv_smem);
+  T(*xr)[kBwdCh] = reinterpret_cast<T(*)[kBwdCh]>(conv_smem + sizeof(float) * kDRows * kBwdCh);
+  int *seqs = reinterpret_cast<int *>(conv_smem + sizeof(float) * kDRows * kBwdCh + sizeof(T) * kXRows * kBwdCh);
+  float(*red)[kBwdCh][5] = reinterpret_cast<float(*)[kBwdCh][5]>(seqs + ((kXRows + 3) & ~3));
   const int blk = blockIdx.y, bb = blockIdx.z, t0 = blk * kTok;
   const ChanTile<T> ct = chan_tile<T>(pr, &go, bb, blockIdx.x, kBwdCh);
   const int nch = ct.nch;
@@ -356,8 +358,10 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
       w[q][0] = wq.x; w[q][1] = wq.y; w[q][2] = wq.z; w[q][3] = wq.w;
       bias[q] = pr.conv_b[c + q];
     }
-    // phase 1: dv rows r0 .. r0 + n1 - 1 (the first 3 groups take 9 rows, the others 8)
-    const int r0 = tq * 8 + min(tq, 3), n1 = tq < 3 ? 9 : 8;
+    // phase 1: dv rows r0 .. r0 + n1 - 1 (kTok + 3 rows over 8 row groups: the
+    // first 3 groups take kRun + 1 rows, the others kRun)
+    constexpr int kRun = kTok / 8;
+    const int r0 = tq * kRun + min(tq, 3), n1 = tq < 3 ? kRun + 1 : kRun;
     float x0[2], x1[2], x2[2];
     load2(&xr[r0][2 * cp], x0);
     load2(&xr[r0 + 1][2 * cp], x1);
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
       s2 = seqs[r0 + 2];
     }
 #pragma unroll
-    for (int k = 0; k < 9; ++k) {
+    for (int k = 0; k < kRun + 1; ++k) {
       if (k < n1) {
         const int r = r0 + k;  // token t0 + r, inputs at raw rows r .. r + 3
         float x3[2];
@@ -403,9 +407,10 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
     }
   }
   __syncthreads();
-  // phase 2: dxr for rows s in [8 tq, 8 tq + 8) (token t0 + s) from dv rows s .. s + 3
+  // phase 2: dxr for rows s in [kRun tq, kRun tq + kRun) (token t0 + s) from dv rows s .. s + 3
   if (live) {
-    const int sr0 = tq * 8;
+    constexpr int kRun = kTok / 8;
+    const int sr0 = tq * kRun;
     float d0[2], d1[2], d2[2];
     {
       const float2 a = *reinterpret_cast<const float2 *>(&dv[sr0][2 * cp]);
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
     }
     T *dst = ct.grad + 2 * cp;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kRun; ++k) {
       const int sr = sr0 + k, t = t0 + sr;
       const float2 f = *reinterpret_cast<const float2 *>(&dv[sr + 3][2 * cp]);
       const float d3[2] = {f.x, f.y};
@@ -465,14 +470,24 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
   }
 }
 
+template <typename T> constexpr int conv_bwd_smem() {
+  return (int)(sizeof(float) * (kConvBwdTok + 3) * kBwdCh + sizeof(T) * (kConvBwdTok + 6) * kBwdCh +
+               sizeof(int) * ((kConvBwdTok + 6 + 3) & ~3) + sizeof(float) * 4 * kBwdCh * 5);
+}
+
 template <typename T>
 void launch_conv_bwd(const Problem &pr, const float *du, const BcParts &bc, const GradOut &go, float *convp, int ntb,
                      cudaStream_t s) {
+  constexpr int smem = conv_bwd_smem<T>();
+  static bool once = (cudaFuncSetAttribute(conv_bwd_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                      cudaFuncSetAttribute(conv_bwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                      true);
+  (void)once;
   dim3 grid(chan_tiles(pr, kBwdCh), ntb, pr.b);
   if (pr.seq_idx)
-    conv_bwd_kernel<T, true><<<grid, 256, 0, s>>>(pr, du, bc, go, convp, ntb);
+    conv_bwd_kernel<T, true><<<grid, 256, smem, s>>>(pr, du, bc, go, convp, ntb);
   else
-    conv_bwd_kernel<T, false><<<grid, 256, 0, s>>>(pr, du, bc, go, convp, ntb);
+    conv_bwd_kernel<T, false><<<grid, 256, smem, s>>>(pr, du, bc, go, convp, ntb);
 }
 
 // Parameter gradients: fixed-order sums of per-chunk / per-block partials.
