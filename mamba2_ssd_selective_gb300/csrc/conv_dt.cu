@@ -77,7 +77,7 @@ __host__ __device__ inline int chan_tiles(const Problem &pr, int kCh) {
 // into shared memory with 16-byte cp.async copies at once (zero-filled before
 // token 0), then each thread walks kFwdTok/4 tokens of 2 channels from shared
 // memory; a warp's stores cover 64 consecutive channels of one token.
-constexpr int kFwdTok = 64, kFwdCh = 128;
+constexpr int kFwdTok = 128, kFwdCh = 128;
 
 // One thread's run of n output rows (2 channels) from the shared tile, the
 // last three raw inputs kept in registers.  HasSeq: taps masked at sequence
@@ -198,9 +198,11 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict
   constexpr int kRows = kFwdTok + 3;
   constexpr int kChunk = 16 / (int)sizeof(T);  // channels per 16-byte copy
   constexpr int kCpr = kFwdCh / kChunk;          // copies per row
-  __shared__ __align__(16) T tile[kRows][kFwdCh];
-  __shared__ int seqs[kRows];
-  static_assert(sizeof(tile) >= sizeof(float) * kMaxChunk * (kDtHeads + 1), "dt tile inside the conv tile");
+  // dynamic shared memory (conv_fwd_smem bytes): tile | seqs
+  extern __shared__ __align__(16) uint8_t conv_smem[];
+  T(*tile)[kFwdCh] = reinterpret_cast<T(*)[kFwdCh]>(conv_smem);
+  int *seqs = reinterpret_cast<int *>(conv_smem + sizeof(T) * kRows * kFwdCh);
+  static_assert(sizeof(T) * kRows * kFwdCh >= sizeof(float) * kMaxChunk * (kDtHeads + 1), "dt tile inside the conv tile");
   if ((int)blockIdx.x >= conv_x) {
     const int id = ((int)blockIdx.x - conv_x) * (int)gridDim.y + (int)blockIdx.y, c = id / dt_hg;
     if (c < pr.nc)
@@ -250,10 +252,17 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(Problem pr, T *__restrict
   }
 }
 
+template <typename T> constexpr int conv_fwd_smem() {
+  return (int)(sizeof(T) * (kFwdTok + 3) * kFwdCh + sizeof(int) * (kFwdTok + 3));
+}
+
 template <typename T> void launch_conv_fwd(const Problem &pr, T *u, float *dtv, float *acs, cudaStream_t s) {
+  constexpr int smem = conv_fwd_smem<T>();
+  static bool once = (cudaFuncSetAttribute(conv_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem), true);
+  (void)once;
   const int conv_x = chan_tiles(pr, kFwdCh), ny = (pr.L + kFwdTok - 1) / kFwdTok;
   const int dt_hg = (pr.H + kDtHeads - 1) / kDtHeads, dt_x = (pr.nc * dt_hg + ny - 1) / ny;
-  conv_fwd_kernel<T><<<dim3(conv_x + dt_x, ny, pr.b), 256, 0, s>>>(pr, u, dtv, acs, conv_x, dt_hg);
+  conv_fwd_kernel<T><<<dim3(conv_x + dt_x, ny, pr.b), 256, smem, s>>>(pr, u, dtv, acs, conv_x, dt_hg);
 }
 
 
