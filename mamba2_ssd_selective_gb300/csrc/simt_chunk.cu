@@ -569,39 +569,43 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
     for (int g = 0; g < sdp_groups; ++g) dtot += sdp[g * BNH + ci];
     const float ac = chunk_decay(pr, bb, h, c);
     const float dec = ac != 0.f ? ac * dtot : 0.f;
-    float base[kDtTok], vcol[kDtTok], vd[kDtTok], wq[kDtTok], wv[kDtTok], qv[kDtTok], dtk[kDtTok];
+    // per token only what the later passes need stays live: base (the suffix-sum
+    // term), pre (vcol + vdiag + w q, the dt adjoint's own terms) and dt
+    float base[kDtTok], pre[kDtTok], dtk[kDtTok];
     float wqsum = 0.f;
-    // the lane's kDtTok consecutive tokens of each per-token array: two 16-byte
-    // loads per array, all issued before any use (L and Q are multiples of 8)
-    float t0v[kDtTok], t3v[kDtTok], t5v[kDtTok], acv[kDtTok];
-    auto ld8 = [&](const float *a, float (&v)[kDtTok]) {
-      const float4 lo = __ldg(reinterpret_cast<const float4 *>(a)), hi = __ldg(reinterpret_cast<const float4 *>(a) + 1);
-      v[0] = lo.x, v[1] = lo.y, v[2] = lo.z, v[3] = lo.w, v[4] = hi.x, v[5] = hi.y, v[6] = hi.z, v[7] = hi.w;
-    };
     const bool has = i0 < Q;  // Q is a multiple of kDtTok: a lane has all or none of its tokens
-    if (has) {
-      const size_t o = tb + i0;
-      ld8(dtv + o, dtk);
-      ld8(acs + o, acv);
-      ld8(tok + 4 * BHL + o, qv);
-      ld8(tok + 2 * BHL + o, vcol);
-      ld8(tok + 1 * BHL + o, vd);
-      ld8(tok + 0 * BHL + o, t0v);
-      ld8(tok + 3 * BHL + o, t3v);
-      ld8(tok + 5 * BHL + o, t5v);
-    }
-#pragma unroll
-    for (int k = 0; k < kDtTok; ++k) {
-      base[k] = wq[k] = wv[k] = 0.f;
+    {
+      // the lane's kDtTok consecutive tokens of each per-token array: two 16-byte
+      // loads per array, all issued before any use (L and Q are multiples of 8)
+      float t0v[kDtTok], t3v[kDtTok], t5v[kDtTok], acv[kDtTok], qv[kDtTok], vc[kDtTok], vdg[kDtTok];
+      auto ld8 = [&](const float *a, float (&v)[kDtTok]) {
+        const float4 lo = __ldg(reinterpret_cast<const float4 *>(a)), hi = __ldg(reinterpret_cast<const float4 *>(a) + 1);
+        v[0] = lo.x, v[1] = lo.y, v[2] = lo.z, v[3] = lo.w, v[4] = hi.x, v[5] = hi.y, v[6] = hi.z, v[7] = hi.w;
+      };
       if (has) {
-        const float w = seq_of(pr, bb, t0 + i0 + k) == seq_last ? expf(acs_last - acv[k]) : 0.f;
-        wv[k] = w;
-        wq[k] = w * dtk[k] * qv[k];
-        base[k] = t0v[k] - dtk[k] * vcol[k] + t3v[k] - wq[k];
-        dDp += t5v[k];
-        wqsum += wq[k];
-      } else {
-        vcol[k] = vd[k] = qv[k] = dtk[k] = 0.f;
+        const size_t o = tb + i0;
+        ld8(dtv + o, dtk);
+        ld8(acs + o, acv);
+        ld8(tok + 4 * BHL + o, qv);
+        ld8(tok + 2 * BHL + o, vc);
+        ld8(tok + 1 * BHL + o, vdg);
+        ld8(tok + 0 * BHL + o, t0v);
+        ld8(tok + 3 * BHL + o, t3v);
+        ld8(tok + 5 * BHL + o, t5v);
+      }
+#pragma unroll
+      for (int k = 0; k < kDtTok; ++k) {
+        base[k] = pre[k] = 0.f;
+        if (has) {
+          const float w = seq_of(pr, bb, t0 + i0 + k) == seq_last ? expf(acs_last - acv[k]) : 0.f;
+          const float wq = w * dtk[k] * qv[k];
+          base[k] = t0v[k] - dtk[k] * vc[k] + t3v[k] - wq;
+          pre[k] = vc[k] + vdg[k] + w * qv[k];
+          dDp += t5v[k];
+          wqsum += wq;
+        } else {
+          dtk[k] = 0.f;
+        }
       }
     }
     // dAcs at the chunk's last token also gets sum_j wdt_j q_j and the decay term,
@@ -632,7 +636,7 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
       const int i = i0 + k;
       if (i < Q) {
         const float dda = suf[k] + later + tail;
-        const float ddt = vcol[k] + vd[k] + wv[k] * qv[k] + A * dda;
+        const float ddt = pre[k] + A * dda;
         dAp = fmaf(dtk[k], dda, dAp);
         const float dz = ddt * sigmoid_f(zr[k] + bias);
         dzp += dz;
