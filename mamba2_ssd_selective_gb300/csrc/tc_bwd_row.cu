@@ -276,24 +276,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         pipe::umma_k<4>(tmem, dC + 16384 / 16, dB + 32768 / 16, pipe::kStepK, pipe::kStepK, id_cb, true);
         umma_commit(bar.cb_full);
         bool first_dc = true;
+        // dM slice m (of the head numbered hn) into the single dM slot (after the
+        // transform has read the previous one)
+        auto issue_dm = [&](uint32_t m, uint32_t hn) {
+          const int slot = m % kNX;
+          const uint64_t ddy = dDY + (hn & 1) * (16384 / 16);
+          mbar_wait(&bar.x_full[slot], parity(m / kNX), status);
+          if (m > 0) mbar_wait(bar.dm_free, parity(m - 1), status);
+          tc_fence_after();
+          pipe::umma_k<4>(tmem + kTmDM, ddy, dX + slot * (8192 / 16), pipe::kStepK, pipe::kStepK, id_dm, false);
+          umma_commit(&bar.x_free[slot]);
+          umma_commit(bar.dm_full);
+        };
+        mbar_wait(&bar.dy_full[nh & 1], parity(nh / 2), status);
+        issue_dm(k, nh);
         for (int hh = 0; hh < HB; ++hh, ++nh) {
           const int vb = nh & 1;
-          const uint64_t ddy = dDY + vb * (16384 / 16);
-          mbar_wait(&bar.dy_full[vb], parity(nh / 2), status);
-          // dM slice m of this head into the single dM slot (after the
-          // transform has read the previous one)
-          auto issue_dm = [&](uint32_t m) {
-            const int slot = m % kNX;
-            mbar_wait(&bar.x_full[slot], parity(m / kNX), status);
-            if (m > 0) mbar_wait(bar.dm_free, parity(m - 1), status);
-            tc_fence_after();
-            pipe::umma_k<4>(tmem + kTmDM, ddy, dX + slot * (8192 / 16), pipe::kStepK, pipe::kStepK, id_dm, false);
-            umma_commit(&bar.x_free[slot]);
-            umma_commit(bar.dm_full);
-          };
-          issue_dm(k);
           for (int s = 0; s < nsl; ++s) {
-            if (s + 1 < nsl) issue_dm(k + s + 1);
+            if (s + 1 < nsl) {
+              issue_dm(k + s + 1, nh);
+            } else if (hh + 1 < HB) {  // the next head's first slice, ahead of this head's closing products
+              mbar_wait(&bar.dy_full[(nh + 1) & 1], parity((nh + 1) / 2), status);
+              issue_dm(k + s + 1, nh + 1);
+            }
             const int as = na % kNA;
             mbar_wait(&bar.a_full[as], parity(na / kNA), status);
             if (first_dc && nu > 0) mbar_wait(bar.dc_free, parity(nu - 1), status);
