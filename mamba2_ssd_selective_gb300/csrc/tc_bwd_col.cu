@@ -20,6 +20,10 @@
 // shared memory.  A slot's dM^T columns are refilled as soon as the transform
 // has read them; its CB^T columns once the T and dB products have read M^T and
 // W^T (slot_free).
+// The epilogue takes the tile's dy rows from a 16 KB tile the producer loads
+// per head, and writes du_x back through the same buffer: each epilogue warp
+// stages its 32 rows x 32 columns of fp32 there and stores them with one TMA
+// store, so the rows leave as whole lines rather than as one line per thread.
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "tc_engine.cuh"
@@ -44,12 +48,13 @@ constexpr uint32_t kSmXT = kSmCR + 65536;       // 2 x x_h tile [128 x 64] bf16
 constexpr uint32_t kSmDY = kSmXT + 2 * 16384;   // ring of dy slices [64 x 64] bf16
 constexpr uint32_t kSmA = kSmDY + kNY * 8192;   // ring of [128 x 64] bf16 operands
 constexpr uint32_t kSmDS = kSmA + kNA * 16384;  // dS_end,h: 2 K halves x [64 x 128 B]
+constexpr uint32_t kSmE = kSmDS + 16384;        // epilogue: dy rows [128 x 64] bf16, then du_x staging
 constexpr uint32_t kVecStride = 3200;           // acs[256] | dt[256] | seq[4 + 256]
-constexpr uint32_t kSmV = kSmDS + 16384;
+constexpr uint32_t kSmV = kSmE + 16384;
 constexpr uint32_t kSmD = kSmV + 2 * kVecStride;  // 2 x {a[256], g[256]}
 constexpr uint32_t kSmVC = kSmD + 2 * 2048;     // 2 x vcol partials [4][128] f32
 constexpr uint32_t kSmBar = kSmVC + 2 * 2048;
-constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4 + 1 + 2;
+constexpr int kNumBars = 20 + 2 * kNY + 2 * kNA + 4 + 1 + 2 + 2;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -108,6 +113,7 @@ struct Bars {
   uint64_t *unit_full, *unit_free, *tu_full, *tu_free, *ds_full, *ds_free, *db_full, *db_free;
   uint64_t *ring_full, *slot_free, *vec_full, *vec_free, *xt_full, *xt_free;  // [2]
   uint64_t *op_full;                                                          // [2]
+  uint64_t *ey_full, *ey_free;                                                // the epilogue's dy tile
   uint64_t *dy_full, *dy_free;                                                // [kNY]
   uint64_t *a_full, *a_free;                                                  // [kNA]
   uint64_t *drain;                                                            // the MMA issuer's final commit
@@ -135,6 +141,8 @@ struct Bars {
     units.free = units.full + 2;
     drain = units.free + 2;
     op_full = drain + 1;
+    ey_full = op_full + 2;
+    ey_free = ey_full + 1;
     units.slot = slot;
   }
 };
@@ -143,10 +151,9 @@ struct Bars {
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_col_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dy,
-                      const __grid_constant__ CUtensorMap tm_ds, Problem pr, const bf16 *__restrict__ u,
-                      const bf16 *__restrict__ dy, const float *__restrict__ dtv, const float *__restrict__ acs,
-                      float *__restrict__ du, float *__restrict__ dbp, float *__restrict__ tok, int HB, int nunits,
-                      int *counter, int *status_word) {
+                      const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_du, Problem pr,
+                      const float *__restrict__ dtv, const float *__restrict__ acs, float *__restrict__ dbp,
+                      float *__restrict__ tok, int HB, int nunits, int *counter, int *status_word) {
   extern __shared__ uint8_t smem_raw[];
   const WaitCtl status{status_word, pr.wait_ns};
   uint8_t *sm = tc::aligned_smem(smem_raw);
@@ -158,10 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t BHL = (size_t)pr.b * pr.H * pr.L;
 
   if (threadIdx.x == 0) {
-    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.tu_full, bar.ds_full, bar.ds_free, bar.db_full, bar.drain};
+    uint64_t *ones[] = {bar.unit_full, bar.unit_free, bar.tu_full, bar.ds_full,
+                        bar.ds_free,   bar.db_full,   bar.drain,   bar.ey_full};
     for (uint64_t *b : ones) mbar_init(b, 1);
     mbar_init(bar.tu_free, kEWarps);
     mbar_init(bar.db_free, kEWarps);
+    mbar_init(bar.ey_free, kEWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.ring_full[i], 1);
       mbar_init(&bar.slot_free[i], 1);
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // counts of armed loads per barrier (nua: unit operand sets); once a
       // wait has failed (ok = false) no further load is issued, stop is
       // published, and the loads in flight are drained before the CTA ends
-      uint32_t nu = 0, nua = 0, nh = 0, nxt = 0, m = 0, nd = 0;
+      uint32_t nu = 0, nua = 0, nh = 0, nxt = 0, m = 0, nd = 0, ne = 0;
       bool ok = true;
       int next = atomicAdd(counter, 1);
       for (;; ++nu) {
@@ -266,6 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sm + kSmDS, &tm_ds, bar.ds_full, 0, srow);
           tma_load_2d(sm + kSmDS + 8192, &tm_ds, bar.ds_full, 64, srow);
           ++nd;
+          // the epilogue's dy rows, once it has stored the previous head's du_x
+          if (ne >= 1 && !mbar_wait(bar.ey_free, parity(ne - 1), status)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar.ey_full, 16384);
+          for (int r = 0; r < 2; ++r) tma_load_2d(sm + kSmE + r * 8192, &tm_dy, bar.ey_full, h * pr.P, rJ + 64 * r);
+          ++ne;
         }
       }
       // every load issued has landed before the CTA releases its shared memory
@@ -275,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t n = m > (uint32_t)kNY ? m - kNY : 0u; n < m; ++n)
         mbar_wait_drain(&bar.dy_full[n % kNY], parity(n / kNY));
       if (nd > 0) mbar_wait_drain(bar.ds_full, parity(nd - 1));
+      if (ne > 0) mbar_wait_drain(bar.ey_full, parity(ne - 1));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -542,21 +560,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, jl = 32 * q + lane;
-    const uint32_t sV = smem_u32(sm + kSmV), sXT = smem_u32(sm + kSmXT);
+    const uint32_t sV = smem_u32(sm + kSmV), sXT = smem_u32(sm + kSmXT), sE = smem_u32(sm + kSmE);
+    // this warp's 32 rows of the dy tile, reused as its du_x staging: a box of
+    // 32 rows x 32 fp32 columns, 128-byte rows in the 128-byte swizzle
+    const uint32_t stage = sE + 4096 * q, srow = stage + 128 * lane;
     uint32_t nu = 0, nh = 0;
     for (;; ++nu) {
       const int ui = pipe::next_unit(bar.units, nu, nunits, true);
       if (ui >= nunits) break;
       const Unit o = unit_of(pr, NTI, nhb, HB, ui);
       const int j = 128 * o.J + jl, t = o.c * pr.Q + j;
-      const bf16 *dyrow = dy + ((size_t)o.bb * pr.L + t) * HP;
+      const int ybox = o.bb * pr.L + o.c * pr.Q + 128 * o.J + 32 * q;  // du row of the warp's first row
       for (int hh = 0; hh < HB; ++hh, ++nh) {
         const int h = o.h0 + hh, vb = nh & 1;
-        // the dy row is loaded first, in flight while the accumulators finish;
-        // x comes from the head's x tile in shared memory
+        // this thread's dy row from the head's dy tile; x from the x tile
+        mbar_wait(bar.ey_full, parity(nh), status);
         uint4 dyr[8];
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) dyr[q8] = tc::ldg16(dyrow + h * pr.P + 8 * q8);
+        for (int q8 = 0; q8 < 8; ++q8) dyr[q8] = pipe::lds_sw128(sE, jl, q8);
         mbar_wait(&bar.vec_full[vb], parity(nh / 2), status);
         const uint32_t vacs = sV + vb * kVecStride, vdt = vacs + 1024, vseq = vacs + 2048 + 16;
         const bool in_last = !has_seq || pipe::lds_i(vseq + 4 * j) == pipe::lds_i(vseq + 4 * (pr.Q - 1));
@@ -569,7 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t xt = sXT + vb * 16384;
         mbar_wait(bar.tu_full, parity(nh), status);
         tc_fence_after();
-        float *dur = du + ((size_t)o.bb * pr.L + t) * pr.Cd + h * pr.P;
         float qsum = 0.f, ddsum = 0.f;  // q_j and dy_j . x_j (the dD piece)
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -589,15 +609,36 @@ __global__ void __launch_bounds__(kThreads, 1)
               tv[col] += wdt * uv[col] + Dh * d8[e];
             }
           }
+          // columns 16 cc.. of the row into the staging box of columns 32 (cc / 2)..;
+          // the second box reuses the first's buffer once its store has read it
+          if (cc == 2) {
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+          }
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            reinterpret_cast<float4 *>(dur + 16 * cc)[e] = make_float4(tv[4 * e], tv[4 * e + 1], tv[4 * e + 2], tv[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t k = 4 * (cc & 1) + e;  // 16-byte chunk of the 128-byte row
+            pipe::sts_u4(srow + 16 * (k ^ (uint32_t)(lane & 7)),
+                         make_uint4(__float_as_uint(tv[4 * e]), __float_as_uint(tv[4 * e + 1]),
+                                    __float_as_uint(tv[4 * e + 2]), __float_as_uint(tv[4 * e + 3])));
+          }
+          if (cc & 1) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_du, stage, h * pr.P + 32 * (cc >> 1), ybox);
+              bulk_commit();
+            }
+          }
         }
         tc_fence_before();
         pipe::warp_arrive(bar.tu_free);
         pipe::warp_arrive(&bar.xt_free[vb]);
         tok[4 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = qsum;
         tok[5 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = ddsum;
+        // the buffer takes the next head's dy rows once the stores have read it
+        if (lane == 0) bulk_wait_read0();
+        pipe::warp_arrive(bar.ey_free);
       }
       mbar_wait(bar.db_full, parity(nu), status);
       tc_fence_after();
@@ -613,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       pipe::warp_arrive(bar.db_free);
     }
+    if (lane == 0) bulk_wait0();  // the du_x stores have completed
   }
 
   tc_fence_before();
@@ -629,11 +671,12 @@ void launch_tc_bwd_col(const Problem &pr, const bf16 *u, const bf16 *dy, const f
                                            kSmemBytes),
                       true);
   (void)once;
-  CUtensorMap tm_u, tm_dy, tm_ds;
+  CUtensorMap tm_u, tm_dy, tm_ds, tm_du;
   const uint64_t HP = (uint64_t)pr.H * pr.P;
   if (!encode_tmap_bf16_2d(&tm_u, u, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 2, 64, 64) ||
       !encode_tmap_bf16_2d(&tm_dy, dy, HP, (uint64_t)pr.b * pr.L, HP * 2, 64, 64) ||
-      !encode_tmap_bf16_2d(&tm_ds, dse16, pr.N, (uint64_t)pr.b * pr.nc * pr.H * pr.P, (uint64_t)pr.N * 2, 64, 64)) {
+      !encode_tmap_bf16_2d(&tm_ds, dse16, pr.N, (uint64_t)pr.b * pr.nc * pr.H * pr.P, (uint64_t)pr.N * 2, 64, 64) ||
+      !encode_tmap_f32_2d(&tm_du, du, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 4, 32, 32)) {
     note_host_error();
     return;
   }
@@ -641,8 +684,8 @@ void launch_tc_bwd_col(const Problem &pr, const bf16 *u, const bf16 *dy, const f
   const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
   const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
   int *counter = status + kCounterCol;  // zeroed with the status word
-  tc_bwd_col_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_ds, pr, u, dy, dtv, acs, du, dbp, tok, HB,
-                                                       nunits, counter, status);
+  tc_bwd_col_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_ds, tm_du, pr, dtv, acs, dbp, tok, HB, nunits,
+                                                       counter, status);
 }
 
 }  // namespace ssd

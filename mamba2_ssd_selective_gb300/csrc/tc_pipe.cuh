@@ -155,6 +155,9 @@ __device__ __forceinline__ uint32_t tmem_quad(uint32_t base, int col) {
 // false if the driver entry point is missing or the encoder rejects the map.
 bool encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
                          uint32_t box_cols, uint32_t box_rows);
+// Host: the same for fp32 (box_cols * 4 must be 128).
+bool encode_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_cols, uint32_t box_rows);
 // Host: SM count of the current device (cached per device).
 int device_sm_count();
 // Host: record an error found while preparing a launch; the pass then returns
