@@ -80,8 +80,9 @@ typedef struct {
  * Parameters (fp32, contiguous): dt_bias, A_log, D (H); conv_w (Cd, 4),
  * 16-byte aligned, where tap 3 multiplies the current token; conv_b (Cd);
  * Cd = H*P + 2*G*N and the conv channel order is [x | B | C].
- * seq_idx (b, L) int32, non-decreasing within a row, or NULL (one sequence per
- * row).  The state and the conv taps are reset where it changes.
+ * seq_idx (b, L) int32, 16-byte aligned (the tensor-core kernels copy it into
+ * shared memory in 16-byte units), non-decreasing within a row, or NULL (one
+ * sequence per row).  The state and the conv taps are reset where it changes.
  * initial_states (b, H, P, N) fp32, 16-byte aligned, or NULL (zero): each row's
  * state before its first token, to which that token's decay applies (the
  * Mamba2 chunked-scan convention; the pages list initial states as not

@@ -72,7 +72,7 @@ ssd_status check_inputs(const ssd_dims *d, const ssd_inputs *in, Problem &pr) {
       in->x_tok_stride % vec || in->B_tok_stride % vec || in->C_tok_stride % vec)
     return SSD_ERR_ALIGNMENT;
   if (!aligned(in->dt_bias, 4) || !aligned(in->A_log, 4) || !aligned(in->D, 4) || !aligned(in->conv_w, 16) ||
-      !aligned(in->conv_b, 4) || (in->seq_idx && !aligned(in->seq_idx, 4)) ||
+      !aligned(in->conv_b, 4) || (in->seq_idx && !aligned(in->seq_idx, 16)) ||
       (in->initial_states && !aligned(in->initial_states, 16)))
     return SSD_ERR_ALIGNMENT;
   // the gated norm: z and its weight exactly when dims ask for it

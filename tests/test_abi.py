@@ -95,6 +95,9 @@ def test_null_and_alignment_and_workspace_rejected(lib):
     inp = _fake_inputs(misalign=2)
     assert lib.ssd_forward(ctypes.byref(d), ctypes.byref(inp), 1 << 20, None, None, 1 << 24, ws, None) == -4
     inp = _fake_inputs()
+    inp.seq_idx = (1 << 20) + 4  # seq_idx must be 16-byte aligned
+    assert lib.ssd_forward(ctypes.byref(d), ctypes.byref(inp), 1 << 20, None, None, 1 << 24, ws, None) == -4
+    inp = _fake_inputs()
     inp.B_tok_stride = SHAPE.conv_dim + 1  # not a multiple of 8 bf16 elements
     assert lib.ssd_forward(ctypes.byref(d), ctypes.byref(inp), 1 << 20, None, None, 1 << 24, ws, None) == -4
     inp = _fake_inputs()
