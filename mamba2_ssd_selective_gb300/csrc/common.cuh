@@ -116,7 +116,7 @@ inline int scan_groups(const Problem &pr) { return (pr.P * pr.N + kScanGroupElem
 // The workspace starts with the device status word followed by one work
 // counter per persistent kernel (zeroed with the status at every pass).
 constexpr int kStatusBytes = 64;
-enum CounterSlot : int { kCounterOut = 1, kCounterRow = 2, kCounterCol = 3 };
+enum CounterSlot : int { kCounterOut = 1, kCounterRow = 2, kCounterCol = 3, kCounterState = 4, kCounterZ = 5 };
 
 // ---------------------------------------------------------------- workspace
 // Offsets (bytes) of every scratch buffer; computed identically on host and

@@ -26,7 +26,7 @@
 // store, so the rows leave as whole lines rather than as one line per thread.
 #include "chunk_common.cuh"
 #include "kernels.h"
-#include "tc_engine.cuh"
+#include "tc_util.cuh"
 #include "tc_pipe.cuh"
 
 namespace ssd {

@@ -19,7 +19,7 @@
 //                [320, 384) Y_off = C_I S_in^T | [384, 512) dC.
 #include "chunk_common.cuh"
 #include "kernels.h"
-#include "tc_engine.cuh"
+#include "tc_util.cuh"
 #include "tc_pipe.cuh"
 
 namespace ssd {

@@ -30,7 +30,7 @@
 // enough to cover the TMA latency; the A slices only cross the SM.
 #include "chunk_common.cuh"
 #include "kernels.h"
-#include "tc_engine.cuh"
+#include "tc_util.cuh"
 #include "tc_pipe.cuh"
 
 namespace ssd {
