@@ -151,9 +151,10 @@ struct Bars {
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_col_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dy,
-                      const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_du, Problem pr,
-                      const float *__restrict__ dtv, const float *__restrict__ acs, float *__restrict__ dbp,
-                      float *__restrict__ tok, int HB, int nunits, int *counter, int *status_word) {
+                      const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_du,
+                      const __grid_constant__ CUtensorMap tm_db, Problem pr, const float *__restrict__ dtv,
+                      const float *__restrict__ acs, float *__restrict__ tok, int HB, int nunits, int *counter,
+                      int *status_word) {
   extern __shared__ uint8_t smem_raw[];
   const WaitCtl status{status_word, pr.wait_ns};
   uint8_t *sm = tc::aligned_smem(smem_raw);
@@ -596,6 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float tv[16], uv[16];
           tmem_ld16(pipe::tmem_quad(tmem + kTmT, 16 * cc), tv);
           tmem_ld16(pipe::tmem_quad(tmem + kTmU, 16 * cc), uv);
+          if (cc == 3) {  // T and U read: the next head's products may start
+            tc_fence_before();
+            pipe::warp_arrive(bar.tu_free);
+          }
 #pragma unroll
           for (int t8 = 0; t8 < 2; ++t8) {
             float d8[8], x8[8];
@@ -631,30 +636,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        pipe::warp_arrive(bar.tu_free);
         pipe::warp_arrive(&bar.xt_free[vb]);
         tok[4 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = qsum;
         tok[5 * BHL + ((size_t)o.bb * pr.H + h) * pr.L + t] = ddsum;
         // the buffer takes the next head's dy rows once the stores have read it
-        if (lane == 0) bulk_wait_read0();
-        pipe::warp_arrive(bar.ey_free);
+        // (after the unit's last head, once the dB stores below have read it too)
+        if (hh + 1 < HB) {
+          if (lane == 0) bulk_wait_read0();
+          pipe::warp_arrive(bar.ey_free);
+        }
       }
+      // the unit's dB partial (columns of its head block in the (b L, H/HB N)
+      // partial rows) through the same staging box, 32 columns at a time
       mbar_wait(bar.db_full, parity(nu), status);
       tc_fence_after();
-      float *out = dbp + (((size_t)o.bb * pr.L + t) * nhb + o.h0 / HB) * pr.N;
+      const int xdb = (o.h0 / HB) * pr.N;
 #pragma unroll 1
       for (int cc = 0; cc < 8; ++cc) {
         float a[16];
         tmem_ld16(pipe::tmem_quad(tmem + kTmDB, 16 * cc), a);
+        if (cc == 7) {
+          tc_fence_before();
+          pipe::warp_arrive(bar.db_free);
+        }
+        if ((cc & 1) == 0) {  // a new box: the buffer's previous store has read it
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          reinterpret_cast<float4 *>(out + 16 * cc)[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t k = 4 * (cc & 1) + e;
+          pipe::sts_u4(srow + 16 * (k ^ (uint32_t)(lane & 7)),
+                       make_uint4(__float_as_uint(a[4 * e]), __float_as_uint(a[4 * e + 1]),
+                                  __float_as_uint(a[4 * e + 2]), __float_as_uint(a[4 * e + 3])));
+        }
+        if (cc & 1) {
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_db, stage, xdb + 32 * (cc >> 1), ybox);
+            bulk_commit();
+          }
+        }
       }
-      tc_fence_before();
-      pipe::warp_arrive(bar.db_free);
+      if (lane == 0) bulk_wait_read0();
+      pipe::warp_arrive(bar.ey_free);
     }
-    if (lane == 0) bulk_wait0();  // the du_x stores have completed
+    if (lane == 0) bulk_wait0();  // the du_x and dB stores have completed
   }
 
   tc_fence_before();
@@ -671,20 +699,22 @@ void launch_tc_bwd_col(const Problem &pr, const bf16 *u, const bf16 *dy, const f
                                            kSmemBytes),
                       true);
   (void)once;
-  CUtensorMap tm_u, tm_dy, tm_ds, tm_du;
+  CUtensorMap tm_u, tm_dy, tm_ds, tm_du, tm_db;
   const uint64_t HP = (uint64_t)pr.H * pr.P;
+  const int HB = tc_head_subset(pr);
+  const uint64_t dbcols = (uint64_t)(pr.H / HB) * pr.N;  // the dB partial rows: (b L, H / HB, N)
   if (!encode_tmap_bf16_2d(&tm_u, u, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 2, 64, 64) ||
       !encode_tmap_bf16_2d(&tm_dy, dy, HP, (uint64_t)pr.b * pr.L, HP * 2, 64, 64) ||
       !encode_tmap_bf16_2d(&tm_ds, dse16, pr.N, (uint64_t)pr.b * pr.nc * pr.H * pr.P, (uint64_t)pr.N * 2, 64, 64) ||
-      !encode_tmap_f32_2d(&tm_du, du, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 4, 32, 32)) {
+      !encode_tmap_f32_2d(&tm_du, du, pr.Cd, (uint64_t)pr.b * pr.L, (uint64_t)pr.Cd * 4, 32, 32) ||
+      !encode_tmap_f32_2d(&tm_db, dbp, dbcols, (uint64_t)pr.b * pr.L, dbcols * 4, 32, 32)) {
     note_host_error();
     return;
   }
-  const int HB = tc_head_subset(pr);
   const int nunits = (pr.Q / 128) * pr.b * pr.nc * (pr.H / HB);
   const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
   int *counter = status + kCounterCol;  // zeroed with the status word
-  tc_bwd_col_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_ds, tm_du, pr, dtv, acs, dbp, tok, HB, nunits,
+  tc_bwd_col_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_dy, tm_ds, tm_du, tm_db, pr, dtv, acs, tok, HB, nunits,
                                                        counter, status);
 }
 
