@@ -572,6 +572,9 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
     // per token only what the later passes need stays live: base (the suffix-sum
     // term), pre (vcol + vdiag + w q, the dt adjoint's own terms) and dt
     float base[kDtTok], pre[kDtTok], dtk[kDtTok];
+    float zr[kDtTok];  // the raw dt inputs (one per token row), loaded with the rest
+#pragma unroll
+    for (int k = 0; k < kDtTok; ++k) zr[k] = 0.f;
     float wqsum = 0.f;
     const bool has = i0 < Q;  // Q is a multiple of kDtTok: a lane has all or none of its tokens
     {
@@ -584,6 +587,9 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
       };
       if (has) {
         const size_t o = tb + i0;
+        const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h;
+#pragma unroll
+        for (int k = 0; k < kDtTok; ++k) zr[k] = to_f(dtr[(size_t)(i0 + k) * pr.dts]);
         ld8(dtv + o, dtk);
         ld8(acs + o, acv);
         ld8(tok + 4 * BHL + o, qv);
@@ -627,10 +633,6 @@ __global__ void __launch_bounds__(256) dt_bwd_warp_kernel(Problem pr, const floa
       if (lane + o < 32) later += y;
     }
     later -= run;  // exclusive: the lanes after this one
-    const T *dtr = static_cast<const T *>(pr.dt) + ((size_t)bb * pr.L + t0) * pr.dts + h;
-    float zr[kDtTok];  // the raw dt inputs (one per token row), loaded together
-#pragma unroll
-    for (int k = 0; k < kDtTok; ++k) zr[k] = has ? to_f(dtr[(size_t)(i0 + k) * pr.dts]) : 0.f;
 #pragma unroll
     for (int k = 0; k < kDtTok; ++k) {
       const int i = i0 + k;
