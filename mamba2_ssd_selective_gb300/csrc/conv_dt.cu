@@ -12,22 +12,49 @@
 
 namespace ssd {
 
-// 2 consecutive channels (one 32-bit load for bf16)
-__device__ __forceinline__ void load2(const __nv_bfloat16 *p, float (&v)[2]) {
+// Two consecutive channels as one packed fp32 pair (sm100.cuh: pk2 / mul2 /
+// fma2; one 32-bit load for bf16), so that the arithmetic of a thread's two
+// channels takes one instruction for both (IEEE rounding per lane).
+using sm100::fma2;
+using sm100::mul2;
+using sm100::pk2;
+using sm100::upk2;
+__device__ __forceinline__ uint64_t loadp(const __nv_bfloat16 *p) {
   const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
-  v[0] = __uint_as_float(w << 16);
-  v[1] = __uint_as_float(w & 0xffff0000u);
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-__device__ __forceinline__ void load2(const float *p, float (&v)[2]) {
-  const float2 f = *reinterpret_cast<const float2 *>(p);
-  v[0] = f.x;
-  v[1] = f.y;
+__device__ __forceinline__ uint64_t loadp(const float *p) { return *reinterpret_cast<const uint64_t *>(p); }
+__device__ __forceinline__ void storep(__nv_bfloat16 *p, uint64_t v) {
+  float lo, hi;
+  upk2(v, lo, hi);
+  *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(lo, hi);
 }
-__device__ __forceinline__ void store2(__nv_bfloat16 *p, const float (&v)[2]) {
-  *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v[0], v[1]);
+__device__ __forceinline__ void storep(float *p, uint64_t v) { *reinterpret_cast<uint64_t *>(p) = v; }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
-__device__ __forceinline__ void store2(float *p, const float (&v)[2]) {
-  *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the conv activation's sigmoid of both lanes
+template <typename T> __device__ __forceinline__ uint64_t act_sigmoid2(uint64_t v) {
+  float lo, hi;
+  upk2(v, lo, hi);
+  return pk2(act_sigmoid<T>(lo), act_sigmoid<T>(hi));
+}
+template <> __device__ __forceinline__ uint64_t act_sigmoid2<__nv_bfloat16>(uint64_t v) {
+  // 1/2 + tanh(v/2)/2 (sigmoid_tanh) with the two multiply-adds packed
+  const uint64_t half = pk2(0.5f, 0.5f);
+  float lo, hi;
+  upk2(mul2(v, half), lo, hi);
+  float tl, th;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(tl) : "f"(lo));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hi));
+  return fma2(half, pk2(tl, th), half);
 }
 
 // A tile of kCh channels that lies inside one of the x, B, C regions of xBC
@@ -85,10 +112,9 @@ constexpr int kFwdTok = 128, kFwdCh = 128;
 template <typename T, bool HasSeq>
 __device__ __forceinline__ void conv_fwd_rows(const T (*tile)[kFwdCh], const int *seqs, const float (&w)[2][4],
                                               const float (&bias)[2], int r0, int cp, int n, T *dst, int Cd) {
-  float x0[2], x1[2], x2[2];
-  load2(&tile[r0][2 * cp], x0);
-  load2(&tile[r0 + 1][2 * cp], x1);
-  load2(&tile[r0 + 2][2 * cp], x2);
+  const uint64_t w0 = pk2(w[0][0], w[1][0]), w1 = pk2(w[0][1], w[1][1]), w2 = pk2(w[0][2], w[1][2]),
+                 w3 = pk2(w[0][3], w[1][3]), bp = pk2(bias[0], bias[1]);
+  uint64_t x0 = loadp(&tile[r0][2 * cp]), x1 = loadp(&tile[r0 + 1][2 * cp]), x2 = loadp(&tile[r0 + 2][2 * cp]);
   int s0 = 0, s1 = 0, s2 = 0;
   if (HasSeq) {
     s0 = seqs[r0];
@@ -98,21 +124,18 @@ __device__ __forceinline__ void conv_fwd_rows(const T (*tile)[kFwdCh], const int
 #pragma unroll
   for (int k = 0; k < kFwdTok / 4; ++k) {
     if (k >= n) break;
-    float x3[2], o[2];
-    load2(&tile[r0 + 3 + k][2 * cp], x3);
+    const uint64_t x3 = loadp(&tile[r0 + 3 + k][2 * cp]);
     const int sq = HasSeq ? seqs[r0 + 3 + k] : 0;
     const bool m2 = !HasSeq || s2 == sq, m1 = !HasSeq || s1 == sq, m0 = !HasSeq || s0 == sq;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      float v = fmaf(w[q][3], x3[q], bias[q]);
-      v = fmaf(m2 ? w[q][2] : 0.f, x2[q], v);
-      v = fmaf(m1 ? w[q][1] : 0.f, x1[q], v);
-      v = fmaf(m0 ? w[q][0] : 0.f, x0[q], v);
-      o[q] = v * act_sigmoid<T>(v);
-      x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
-    }
+    uint64_t v = fma2(w3, x3, bp);
+    v = fma2(m2 ? w2 : 0ull, x2, v);
+    v = fma2(m1 ? w1 : 0ull, x1, v);
+    v = fma2(m0 ? w0 : 0ull, x0, v);
+    storep(dst + (size_t)k * Cd, mul2(v, act_sigmoid2<T>(v)));
+    x0 = x1;
+    x1 = x2;
+    x2 = x3;
     s0 = s1; s1 = s2; s2 = sq;
-    store2(dst + (size_t)k * Cd, o);
   }
 }
 
@@ -368,13 +391,14 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
       bias[q] = pr.conv_b[c + q];
     }
     // phase 1: dv rows r0 .. r0 + n1 - 1 (kTok + 3 rows over 8 row groups: the
-    // first 3 groups take kRun + 1 rows, the others kRun)
+    // first 3 groups take kRun + 1 rows, the others kRun); both channels of the
+    // thread as one packed pair
     constexpr int kRun = kTok / 8;
     const int r0 = tq * kRun + min(tq, 3), n1 = tq < 3 ? kRun + 1 : kRun;
-    float x0[2], x1[2], x2[2];
-    load2(&xr[r0][2 * cp], x0);
-    load2(&xr[r0 + 1][2 * cp], x1);
-    load2(&xr[r0 + 2][2 * cp], x2);
+    const uint64_t w0 = pk2(w[0][0], w[1][0]), w1 = pk2(w[0][1], w[1][1]), w2 = pk2(w[0][2], w[1][2]),
+                   w3 = pk2(w[0][3], w[1][3]), bp = pk2(bias[0], bias[1]), one = pk2(1.f, 1.f);
+    uint64_t x0 = loadp(&xr[r0][2 * cp]), x1 = loadp(&xr[r0 + 1][2 * cp]), x2 = loadp(&xr[r0 + 2][2 * cp]);
+    uint64_t dw0 = 0ull, dw1 = 0ull, dw2 = 0ull, dw3 = 0ull, dbp = 0ull;
     int s0 = 0, s1 = 0, s2 = 0;
     if (HasSeq) {
       s0 = seqs[r0];
@@ -385,54 +409,52 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
     for (int k = 0; k < kRun + 1; ++k) {
       if (k < n1) {
         const int r = r0 + k;  // token t0 + r, inputs at raw rows r .. r + 3
-        float x3[2];
-        load2(&xr[r + 3][2 * cp], x3);
+        const uint64_t x3 = loadp(&xr[r + 3][2 * cp]);
         const int sq = HasSeq ? seqs[r + 3] : 0;
         const bool m2 = !HasSeq || s2 == sq, m1 = !HasSeq || s1 == sq, m0 = !HasSeq || s0 == sq;
-        const float2 g2 = *reinterpret_cast<const float2 *>(&dv[r][2 * cp]);
-        const float gv[2] = {g2.x, g2.y};
-        float out[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float v = fmaf(w[q][3], x3[q], bias[q]);
-          v = fmaf(m2 ? w[q][2] : 0.f, x2[q], v);
-          v = fmaf(m1 ? w[q][1] : 0.f, x1[q], v);
-          v = fmaf(m0 ? w[q][0] : 0.f, x0[q], v);
-          const float sg = act_sigmoid<T>(v);
-          const float d = gv[q] * sg * (1.f + v * (1.f - sg));
-          out[q] = d;
-          if (r < kTok) {  // the tile's own tokens
-            db[q] += d;
-            dw[q][3] = fmaf(d, x3[q], dw[q][3]);
-            dw[q][2] = fmaf(m2 ? d : 0.f, x2[q], dw[q][2]);
-            dw[q][1] = fmaf(m1 ? d : 0.f, x1[q], dw[q][1]);
-            dw[q][0] = fmaf(m0 ? d : 0.f, x0[q], dw[q][0]);
-          }
-          x0[q] = x1[q]; x1[q] = x2[q]; x2[q] = x3[q];
+        const uint64_t g = *reinterpret_cast<const uint64_t *>(&dv[r][2 * cp]);
+        uint64_t v = fma2(w3, x3, bp);
+        v = fma2(m2 ? w2 : 0ull, x2, v);
+        v = fma2(m1 ? w1 : 0ull, x1, v);
+        v = fma2(m0 ? w0 : 0ull, x0, v);
+        const uint64_t sg = act_sigmoid2<T>(v);
+        // d = (g sg) (1 + v (1 - sg))
+        const uint64_t d = mul2(mul2(g, sg), fma2(v, sub2(one, sg), one));
+        if (r < kTok) {  // the tile's own tokens
+          dbp = add2(dbp, d);
+          dw3 = fma2(d, x3, dw3);
+          dw2 = fma2(m2 ? d : 0ull, x2, dw2);
+          dw1 = fma2(m1 ? d : 0ull, x1, dw1);
+          dw0 = fma2(m0 ? d : 0ull, x0, dw0);
         }
+        x0 = x1;
+        x1 = x2;
+        x2 = x3;
         s0 = s1; s1 = s2; s2 = sq;
-        *reinterpret_cast<float2 *>(&dv[r][2 * cp]) = make_float2(out[0], out[1]);  // own elements only
+        *reinterpret_cast<uint64_t *>(&dv[r][2 * cp]) = d;  // own elements only
       }
     }
+    upk2(dw0, dw[0][0], dw[1][0]);
+    upk2(dw1, dw[0][1], dw[1][1]);
+    upk2(dw2, dw[0][2], dw[1][2]);
+    upk2(dw3, dw[0][3], dw[1][3]);
+    upk2(dbp, db[0], db[1]);
   }
   __syncthreads();
   // phase 2: dxr for rows s in [kRun tq, kRun tq + kRun) (token t0 + s) from dv rows s .. s + 3
   if (live) {
     constexpr int kRun = kTok / 8;
     const int sr0 = tq * kRun;
-    float d0[2], d1[2], d2[2];
-    {
-      const float2 a = *reinterpret_cast<const float2 *>(&dv[sr0][2 * cp]);
-      const float2 b = *reinterpret_cast<const float2 *>(&dv[sr0 + 1][2 * cp]);
-      const float2 e = *reinterpret_cast<const float2 *>(&dv[sr0 + 2][2 * cp]);
-      d0[0] = a.x; d0[1] = a.y; d1[0] = b.x; d1[1] = b.y; d2[0] = e.x; d2[1] = e.y;
-    }
+    const uint64_t w0 = pk2(w[0][0], w[1][0]), w1 = pk2(w[0][1], w[1][1]), w2 = pk2(w[0][2], w[1][2]),
+                   w3 = pk2(w[0][3], w[1][3]);
+    uint64_t d0 = *reinterpret_cast<const uint64_t *>(&dv[sr0][2 * cp]),
+             d1 = *reinterpret_cast<const uint64_t *>(&dv[sr0 + 1][2 * cp]),
+             d2 = *reinterpret_cast<const uint64_t *>(&dv[sr0 + 2][2 * cp]);
     T *dst = ct.grad + 2 * cp;
 #pragma unroll
     for (int k = 0; k < kRun; ++k) {
       const int sr = sr0 + k, t = t0 + sr;
-      const float2 f = *reinterpret_cast<const float2 *>(&dv[sr + 3][2 * cp]);
-      const float d3[2] = {f.x, f.y};
+      const uint64_t d3 = *reinterpret_cast<const uint64_t *>(&dv[sr + 3][2 * cp]);
       bool m1 = true, m2 = true, m3 = true;
       if (HasSeq) {
         const int q0 = seqs[sr + 3];  // token t
@@ -440,17 +462,14 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(Problem pr, const float *
         m2 = seqs[sr + 5] == q0;
         m3 = seqs[sr + 6] == q0;
       }
-      float g[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float a = w[q][3] * d0[q];
-        a = fmaf(m1 ? w[q][2] : 0.f, d1[q], a);
-        a = fmaf(m2 ? w[q][1] : 0.f, d2[q], a);
-        a = fmaf(m3 ? w[q][0] : 0.f, d3[q], a);
-        g[q] = a;
-        d0[q] = d1[q]; d1[q] = d2[q]; d2[q] = d3[q];
-      }
-      if (t < pr.L) store2(dst + (size_t)t * ct.gst, g);
+      uint64_t a = mul2(w3, d0);
+      a = fma2(m1 ? w2 : 0ull, d1, a);
+      a = fma2(m2 ? w1 : 0ull, d2, a);
+      a = fma2(m3 ? w0 : 0ull, d3, a);
+      d0 = d1;
+      d1 = d2;
+      d2 = d3;
+      if (t < pr.L) storep(dst + (size_t)t * ct.gst, a);
     }
   }
   // parameter partials: fixed-order sum over the row groups (0..3 and 4..7 folded pairwise first)
