@@ -50,6 +50,10 @@ SHAPES = [
     (SsdShape(1, 2048, 4, 64, 128, 1, 256, 4), [256, 256, 1, 2, 3, 90, 160, 700, 580], "packed-2048-q256"),
     # the tensor-core path with 128-token chunks (one row tile per chunk), packed
     (SsdShape(2, 1024, 4, 64, 128, 1, 128, 2), [128, 5, 300, 77, 514], "packed-2x1024-q128"),
+    # two heads per group (the tensor-core kernels' smallest head blocks) and sixteen
+    # (their largest at this size), with more units than SMs in neither case
+    (SsdShape(1, 1024, 8, 64, 128, 4, 256, 2), None, None),
+    (SsdShape(2, 1024, 16, 64, 128, 1, 256, 4), None, None),
 ]
 
 
@@ -183,11 +187,10 @@ def test_varlen_sequence_final_states(oracle_lib, dtype, init):
 
 
 NORM_SHAPES = [
-    # norm groups of 8 and 4 heads: the tensor-core output kernel holds a whole group
-    # per work unit and applies the norm in its epilogue
+    # norm groups of 8 and 4 heads (512 and 256 channels: a warp per token and group)
     (SsdShape(2, 1024, 8, 64, 128, 1, 256, 2), None),
     (SsdShape(1, 1024, 8, 64, 128, 2, 256, 4), [300, 3, 721]),
-    # a group of 32 heads spans two work units: the norm runs as its own pass
+    # a group of 32 heads (2048 channels: a block per token and group)
     (SsdShape(1, 512, 32, 64, 128, 1, 256, 2), [200, 312]),
     (SsdShape(1, 512, 8, 32, 40, 4, 64, 2), None),  # CUDA-core path (headdim 32) in bf16 as well
 ]
