@@ -19,16 +19,6 @@ __device__ __forceinline__ ChunkIds chunk_ids(const Problem &pr) {
   return id;
 }
 
-__device__ __forceinline__ ChunkIds make_ids(const Problem &pr, int c, int h, int bb) {
-  ChunkIds id;
-  id.c = c;
-  id.h = h;
-  id.bb = bb;
-  id.g = h / pr.hpg;
-  id.t0 = c * pr.Q;
-  return id;
-}
-
 // Shared per-chunk vectors: Acs, dt, seq ids, and three derived weights.
 struct ChunkVecs {
   float acs[256], dt[256], em[256], wdt[256], w[256];
@@ -58,36 +48,6 @@ __device__ __forceinline__ void load_chunk_vecs(const Problem &pr, const ChunkId
     const float w = (sq == seq_last) ? expf(acs_last - a) : 0.f;
     v.w[i] = w;
     v.wdt[i] = w * d;
-  }
-  __syncthreads();
-}
-
-// Only the weights a kernel needs, for a pair of heads h0, h0 + 1 of one chunk:
-// wdt[j] (chunk-state weights) or em[i] (weights of the state entering the
-// chunk), as defined for ChunkVecs.
-__device__ __forceinline__ void load_wdt_pair(const Problem &pr, int c, int h0, int bb, const float *dtv,
-                                              const float *acs, float (&w0)[256], float (&w1)[256]) {
-  const int Q = pr.Q, t0 = c * Q;
-  const int seq_last = seq_of(pr, bb, t0 + Q - 1);
-  for (int e = threadIdx.x; e < 2 * Q; e += blockDim.x) {
-    const int hh = e / Q, i = e % Q, h = h0 + hh;
-    const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L + t0;
-    const float *dt_bh = dtv + ((size_t)bb * pr.H + h) * pr.L + t0;
-    const float w = (seq_of(pr, bb, t0 + i) == seq_last) ? expf(acs_bh[Q - 1] - acs_bh[i]) * dt_bh[i] : 0.f;
-    (hh ? w1 : w0)[i] = w;
-  }
-  __syncthreads();
-}
-__device__ __forceinline__ void load_em_pair(const Problem &pr, int c, int h0, int bb, const float *acs,
-                                             float (&e0)[256], float (&e1)[256]) {
-  const int Q = pr.Q, t0 = c * Q;
-  const bool inc = chunk_has_incoming(pr, c);
-  const int seq_prev = inc ? seq_before_chunk(pr, bb, c) : 0;
-  for (int e = threadIdx.x; e < 2 * Q; e += blockDim.x) {
-    const int hh = e / Q, i = e % Q, h = h0 + hh;
-    const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L + t0;
-    const float m = (inc && seq_of(pr, bb, t0 + i) == seq_prev) ? expf(acs_bh[i]) : 0.f;
-    (hh ? e1 : e0)[i] = m;
   }
   __syncthreads();
 }

@@ -27,7 +27,6 @@
 //
 // Envelope (checked on the host): bf16 activations, headdim 64, dstate 128,
 // chunk 128 or 256, an even number of heads per group.
-#include "chunk_common.cuh"
 #include "kernels.h"
 #include "tc_util.cuh"
 #include "tc_pipe.cuh"
