@@ -14,8 +14,9 @@
 //               (Acs, dt, seq), 64-token X slices and the bf16 S_in tile;
 //   warp 1      TMEM owner and MMA issuer (one thread);
 //   warps 2-17  transform: read CB rows from TMEM, apply mask, decay and dt,
-//               write the bf16 A slice into shared memory (four warps per lane
-//               quadrant, one per 16-column group of the 64-wide slice);
+//               write the bf16 A slice back into tensor memory, where the MMA
+//               takes it as its A operand (four warps per lane quadrant, one per
+//               16-column group of the 64-wide slice = one K step of 8 columns);
 //   warps 18-21 epilogue: drain the two per-head accumulators and write y.
 // Decays without an exponential per element: Acs does not increase along the
 // chunk, so for a 16-column group ending at column m and rows i >= m
@@ -25,9 +26,11 @@
 // straddle the diagonal use 2^(a_i + b_j) per element, a_i = Acs_i log2(e),
 // b_j = log2(dt_j) - Acs_j log2(e).  The mask is the row's interval
 // [start_i, i], start_i the first token of i's sequence inside the chunk.
-// Accumulators are double-buffered, so the epilogue of head n overlaps the
-// transform and MMAs of head n+1.  The X slices have their own ring, deep
-// enough to cover the TMA latency; the A slices only cross the SM.
+// The Yd accumulator is double-buffered, so the epilogue of head n overlaps the
+// transform and MMAs of head n+1; Yo, formed at the end of a head, has one
+// buffer (the epilogue has read the previous head's long before).  The X
+// slices have their own ring, deep enough to cover the TMA latency; the A
+// slices never leave tensor memory.
 #include "chunk_common.cuh"
 #include "kernels.h"
 #include "tc_util.cuh"
@@ -44,15 +47,14 @@ using pipe::parity;
 constexpr int kWarps = 22;
 constexpr int kEpiWarp0 = 18;
 constexpr int kThreads = kWarps * 32;
-constexpr int kNA = 2;   // A slice ring (transform -> MMA, on chip)
+constexpr int kNA = 2;   // A slice slots in tensor memory (transform -> MMA)
 constexpr int kNX = 6;   // X slice ring (TMA -> MMA; deep enough to cover the load latency)
 constexpr int kNSB = 2;  // S_in buffers (loaded a head ahead of use)
 
 // shared memory map, offsets from the 1024-aligned base
 constexpr uint32_t kSmC = 0;                     // C_I: 2 K halves x [128 rows x 128 B]
 constexpr uint32_t kSmB = kSmC + 2 * 16384;      // B rows: 2 K halves x [256 rows x 128 B]
-constexpr uint32_t kSmA = kSmB + 2 * 32768;      // ring of A slices [128 x 64] bf16, K-major
-constexpr uint32_t kSmX = kSmA + kNA * 16384;    // ring of X slices [64 tokens x 64] bf16, MN-major
+constexpr uint32_t kSmX = kSmB + 2 * 32768;      // ring of X slices [64 tokens x 64] bf16, MN-major
 constexpr uint32_t kSmS = kSmX + kNX * 8192;     // kNSB x S_in,h: 2 K halves x [64 x 128 B]
 constexpr uint32_t kVecStride = 3200;            // acs[256] f32 | dt[256] f32 | seq[4 + 256] i32
 constexpr uint32_t kSmV = kSmS + kNSB * 16384;   // 2 vector buffers
@@ -62,6 +64,10 @@ constexpr int kNumBars = 9 + 2 * kNA + 2 * kNX + 2 * kNSB + 4 + 4 + 1;
 constexpr uint32_t kSmEnd = kSmBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = (int)kSmEnd + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// tensor memory: [0, 256) CB | [256, 384) Yd[2] | [384, 448) Yo | [448, 512) A[2]
+// (a slot: 4 K steps x 8 columns of bf16 pairs, element 2c in the low half of column c)
+constexpr uint32_t kTmYd = 256, kTmYo = 384, kTmA = 448;
 
 struct Unit {
   int bb, c, I, h0;
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot;  // cols [0, 256): CB;  [256 + 128 b, +64): Yd[b];  [+64, +128): Yo[b]
+  const uint32_t tmem = *tslot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // operand descriptors, built once; ring slots and K steps are additions
       const uint64_t dC = desc_sw128(smem_u32(sm + kSmC), 16, 1024), dB = desc_sw128(smem_u32(sm + kSmB), 16, 1024),
-                     dA = desc_sw128(smem_u32(sm + kSmA), 16, 1024), dX = desc_sw128(smem_u32(sm + kSmX), 8192, 1024),
+                     dX = desc_sw128(smem_u32(sm + kSmX), 8192, 1024),
                      dS = desc_sw128(smem_u32(sm + kSmS), 16, 1024);
       constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_off = idesc_bf16(128, 64, false, false);
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bar.b_free);
         for (int hh = 0; hh < HB; ++hh, ++nh) {
           const int ab = nh & 1;
-          const uint32_t tacc = tmem + 256 + 128 * ab;
+          const uint32_t tyd = tmem + kTmYd + 64 * ab;
           if (nh >= 2) mbar_wait(&bar.acc_free[ab], parity(nh / 2 - 1), status);
           tc_fence_after();
           for (int s = 0; s < 2 * (o.I + 1); ++s, ++k) {
@@ -285,18 +291,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar.a_full[as], parity(k / kNA), status);
             mbar_wait(&bar.x_full[xs], parity(k / kNX), status);
             tc_fence_after();
-            pipe::umma_k<4>(tacc, dA + as * (16384 / 16), dX + xs * (8192 / 16), pipe::kStepK, pipe::kStepMN, id_acc,
-                            s > 0);
+            pipe::umma_ts_k<4>(tyd, tmem + kTmA + 32 * as, dX + xs * (8192 / 16), 8, pipe::kStepMN, id_acc, s > 0);
             umma_commit(&bar.a_free[as]);
             umma_commit(&bar.x_free[xs]);
           }
           if (chunk_has_incoming(pr, o.c)) {
             const int sb = ns % kNSB;
             mbar_wait(&bar.s_full[sb], parity(ns / kNSB), status);
+            // one Yo buffer: the previous head's epilogue has read it
+            if (nh >= 1) mbar_wait(&bar.acc_free[(nh - 1) & 1], parity((nh - 1) / 2), status);
             tc_fence_after();
             const uint64_t dSb = dS + sb * (16384 / 16);
-            pipe::umma_k<4>(tacc + 64, dC, dSb, pipe::kStepK, pipe::kStepK, id_off, false);
-            pipe::umma_k<4>(tacc + 64, dC + 16384 / 16, dSb + 8192 / 16, pipe::kStepK, pipe::kStepK, id_off, true);
+            pipe::umma_k<4>(tmem + kTmYo, dC, dSb, pipe::kStepK, pipe::kStepK, id_off, false);
+            pipe::umma_k<4>(tmem + kTmYo, dC + 16384 / 16, dSb + 8192 / 16, pipe::kStepK, pipe::kStepK, id_off, true);
             umma_commit(&bar.s_free[sb]);
             ++ns;
           }
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ transform
     const int q = warp & 3, cg = (warp - 2) >> 2, il = 32 * q + lane, tt = threadIdx.x - 64;
-    const uint32_t sA = smem_u32(sm + kSmA), sV = smem_u32(sm + kSmV), sD = smem_u32(sm + kSmD);
+    const uint32_t sV = smem_u32(sm + kSmV), sD = smem_u32(sm + kSmD);
     const float kLog2e = 1.4426950408889634f;
     uint32_t nu = 0, nh = 0, k = 0;
     for (;; ++nu) {
@@ -427,11 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int p = 0; p < 2; ++p) {
             const uint32_t kp = k + p, slot = kp % kNA;
             if (kp >= (uint32_t)kNA) mbar_wait(&bar.a_free[slot], parity(kp / kNA - 1), status);
-            const uint32_t A = sA + slot * 16384;
-            pipe::sts_u4(A + sw128_offset(il, 16 * cg), pk[p][0]);
-            pipe::sts_u4(A + sw128_offset(il, 16 * cg + 8), pk[p][1]);
+            // this warp's K step (8 columns) of the slot, in its lane quadrant
+            const uint32_t tdst = pipe::tmem_quad(tmem + kTmA + 32 * slot, 8 * cg);
+            tmem_st4_async(tdst, pk[p][0].x, pk[p][0].y, pk[p][0].z, pk[p][0].w);
+            tmem_st4_async(tdst + 4, pk[p][1].x, pk[p][1].y, pk[p][1].z, pk[p][1].w);
           }
-          fence_async_smem();
+          tmem_wait_st();
+          tc_fence_before();
 #pragma unroll
           for (int p = 0; p < 2; ++p) pipe::warp_arrive(&bar.a_full[(k + p) % kNA]);
         }
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 xr0 = tc::ldg16(xh), xr1 = tc::ldg16(xh + 8);
         mbar_wait(&bar.acc_full[ab], parity(nh / 2), status);
         tc_fence_after();
-        const uint32_t tacc = tmem + 256 + 128 * ab;
+        const uint32_t tyd = tmem + kTmYd + 64 * ab;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           const uint4 xr[2] = {xr0, xr1};
@@ -477,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           xr0 = tc::ldg16(xh + cn);
           xr1 = tc::ldg16(xh + cn + 8);
           float yd[16], yo[16];
-          tmem_ld16(pipe::tmem_quad(tacc, 16 * cc), yd);
-          if (has_off) tmem_ld16(pipe::tmem_quad(tacc + 64, 16 * cc), yo);
+          tmem_ld16(pipe::tmem_quad(tyd, 16 * cc), yd);
+          if (has_off) tmem_ld16(pipe::tmem_quad(tmem + kTmYo, 16 * cc), yo);
 #pragma unroll
           for (int q8 = 0; q8 < 2; ++q8) {
             float x[8], o8[8];
