@@ -48,7 +48,7 @@ constexpr int kWarps = 22;
 constexpr int kEpiWarp0 = 18;
 constexpr int kThreads = kWarps * 32;
 constexpr int kNA = 2;   // A slice slots in tensor memory (transform -> MMA)
-constexpr int kNX = 6;   // X slice ring (TMA -> MMA; deep enough to cover the load latency)
+constexpr int kNX = 4;   // X slice ring (TMA -> MMA; a head of a 256-token tile; deeper rings measured slower)
 constexpr int kNSB = 2;  // S_in buffers (loaded a head ahead of use)
 
 // shared memory map, offsets from the 1024-aligned base
