@@ -182,7 +182,8 @@ def kernel_work(shape, dtype: str) -> dict:
         # the B / C channels' gradients come as head-block partials, summed while staging
         "conv_bwd": ("mem", 0, b * L * (Cd * 2 * eb + HP * 4) + 2 * parts + b * (L // 128) * Cd * 20),
         "param_reduce": ("mem", 0, b * nc * H * 12 + b * (L // 128) * Cd * 20),
-        "tc_chunk_state": ("tensor", f_state, x + bc + st),
+        # bf16 path: the state kernel also forms the decay tables (Acs at chunk ends in, three tables out)
+        "tc_chunk_state": ("tensor", f_state, x + bc + st + 4 * b * H * nc * 4),
         "tc_chunk_z": ("tensor", f_state, x + bc + st),
         # persistent kernels: CB is formed on chip, W never leaves the SM
         "tc_chunk_out": ("tensor", f_cb + f_diag + f_off, 2 * x + bc + st16 + 2 * tok),

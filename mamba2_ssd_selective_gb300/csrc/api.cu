@@ -190,10 +190,13 @@ ssd_status forward_impl(const Problem &pr_in, T *y, float *final_state, float *s
   // the gated norm: a separate pass over the mixer output (written to the workspace)
   if (pr.z) y = reinterpret_cast<T *>(ws + w.ypre);
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, dtv, acs, s));  // and dt_prep
-  SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
-                                                 const_cast<float *>(pr.dend), ablk, s));
+  float *cdec = const_cast<float *>(pr.cdec), *dstart = const_cast<float *>(pr.dstart),
+        *dend = const_cast<float *>(pr.dend);
+  // the tensor-core chunk-state kernel forms the decay tables in the same launch
+  if (!tc) SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, cdec, dstart, dend, ablk, s));
   if constexpr (kIsBf16<T>) {
-    if (tc) SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));  // CB: inside tc_out
+    if (tc)  // CB: inside tc_out
+      SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, cdec, dstart, dend, ablk, status, s));
   }
   if (!tc) {
     SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));
@@ -236,10 +239,12 @@ ssd_status backward_impl(const Problem &pr_in, const T *dy, const float *dfinal,
   const bool tc = use_tc<T>(pr);
   // recompute: conv, dt, CB, chunk states, local segment passes (and the scan)
   SSD_LAUNCH("conv_fwd", launch_conv_fwd<T>(pr, u, dtv, acs, s));  // and dt_prep
-  SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, const_cast<float *>(pr.cdec), const_cast<float *>(pr.dstart),
-                                                 const_cast<float *>(pr.dend), ablk, s));
+  float *cdec = const_cast<float *>(pr.cdec), *dstart = const_cast<float *>(pr.dstart),
+        *dend = const_cast<float *>(pr.dend);
+  if (!tc) SSD_LAUNCH("decay_tables", launch_decay_tables(pr, acs, cdec, dstart, dend, ablk, s));
   if constexpr (kIsBf16<T>) {
-    if (tc) SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, status, s));  // CB: in-kernel
+    if (tc)  // CB: in-kernel; the decay tables in the same launch
+      SSD_LAUNCH("tc_chunk_state", launch_tc_state(pr, u, dtv, acs, sst, cdec, dstart, dend, ablk, status, s));
   }
   if (!tc) {
     SSD_LAUNCH("cb", launch_cb<T>(pr, u, cb, s));

@@ -104,6 +104,36 @@ __device__ __forceinline__ float decay_end(const Problem &pr, int b, int h, int 
   return __ldg(pr.dend + dtab_index(pr, b, h, c));
 }
 
+// Decay tables of one (b, h), by `nthr` cooperating threads (this one `tid`):
+// cdec[c] = product of the chunk's per-token decays (from Acs and seq_idx),
+// then per segment the exclusive prefix and suffix products
+// dstart[c] = prod_{c' in seg, c' < c} cdec[c'], dend[c] = prod_{c' > c}, and the
+// segment's whole product a_block[k] (the factor of the affine summary).  `sync`
+// makes the cdec writes visible to the cooperating threads before they are read.
+template <class Sync>
+__device__ __forceinline__ void decay_tables_bh(const Problem &pr, const float *acs, int bb, int h, float *cdec,
+                                                float *dstart, float *dend, float *ablk, int tid, int nthr,
+                                                Sync sync) {
+  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
+  const size_t base = ((size_t)bb * pr.H + h) * pr.nc;
+  for (int c = tid; c < pr.nc; c += nthr) cdec[base + c] = chunk_decay_raw(pr, acs_bh, bb, c);
+  sync();
+  for (int k = tid; k < pr.S; k += nthr) {
+    const int c0 = k * pr.cps, c1 = c0 + pr.cps;
+    float d = 1.f;
+    for (int c = c0; c < c1; ++c) {
+      dstart[base + c] = d;
+      d *= cdec[base + c];
+    }
+    ablk[((size_t)bb * pr.S + k) * pr.H + h] = d;
+    d = 1.f;
+    for (int c = c1 - 1; c >= c0; --c) {
+      dend[base + c] = d;
+      d *= cdec[base + c];
+    }
+  }
+}
+
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kConvBwdTok = 128;  // tokens per conv-backward block (one set of parameter partials each)

@@ -93,8 +93,9 @@ void launch_chunk_dt(const Problem &pr, const T *u, const T *dy, const float *dt
 inline bool tc_envelope(const Problem &pr) {
   return pr.P == 64 && pr.N == 128 && (pr.Q == 128 || pr.Q == 256) && pr.hpg % 2 == 0;
 }
+// the chunk states, and the decay tables (as launch_decay_tables) in the same launch
 void launch_tc_state(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs, float *sst,
-                     int *status, cudaStream_t s);
+                     float *cdec, float *dstart, float *dend, float *ablk, int *status, cudaStream_t s);
 // persistent output kernel (tc_out.cu): the mixer output y (the gated norm, when
 // asked for, is a separate pass over it)
 void launch_tc_out(const Problem &pr, const __nv_bfloat16 *u, const float *dtv, const float *acs,

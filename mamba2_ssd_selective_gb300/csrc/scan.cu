@@ -18,31 +18,11 @@ namespace ssd {
 
 constexpr int kScanBatch = 4;  // chunks whose loads are in flight together
 
-// Decay tables of one (b, h): cdec[c] = product of the chunk's per-token decays
-// (from Acs and seq_idx), then per segment the exclusive prefix and suffix
-// products dstart[c] = prod_{c' in seg, c' < c} cdec[c'], dend[c] = prod_{c' > c},
-// and the segment's whole product a_block[k] (the factor of the affine summary).
+// Decay tables (common.cuh: decay_tables_bh), one block of 256 threads per (b, h).
 __global__ void __launch_bounds__(256) decay_tables_kernel(Problem pr, const float *__restrict__ acs, float *cdec,
                                                            float *dstart, float *dend, float *ablk) {
-  const int h = blockIdx.x, bb = blockIdx.y;
-  const float *acs_bh = acs + ((size_t)bb * pr.H + h) * pr.L;
-  const size_t base = ((size_t)bb * pr.H + h) * pr.nc;
-  for (int c = threadIdx.x; c < pr.nc; c += blockDim.x) cdec[base + c] = chunk_decay_raw(pr, acs_bh, bb, c);
-  __syncthreads();
-  for (int k = threadIdx.x; k < pr.S; k += blockDim.x) {
-    const int c0 = k * pr.cps, c1 = c0 + pr.cps;
-    float d = 1.f;
-    for (int c = c0; c < c1; ++c) {
-      dstart[base + c] = d;
-      d *= cdec[base + c];
-    }
-    ablk[((size_t)bb * pr.S + k) * pr.H + h] = d;
-    d = 1.f;
-    for (int c = c1 - 1; c >= c0; --c) {
-      dend[base + c] = d;
-      d *= cdec[base + c];
-    }
-  }
+  decay_tables_bh(pr, acs, blockIdx.y, blockIdx.x, cdec, dstart, dend, ablk, threadIdx.x, blockDim.x,
+                  [] { __syncthreads(); });
 }
 
 void launch_decay_tables(const Problem &pr, const float *acs, float *cdec, float *dstart, float *dend, float *ablk,

@@ -9,7 +9,7 @@
 // in simt_chunk.cu.  The output and the chunk gradients run in the persistent
 // kernels of tc_out.cu, tc_bwd_row.cu and tc_bwd_col.cu.
 //
-// One persistent, warp-specialised kernel serves both (one CTA per SM, 14
+// One persistent, warp-specialised kernel serves both (one CTA per SM, 15
 // warps).  Work unit = (batch row, chunk, block of HB heads of one group):
 //   warp 0      TMA producer: the unit's A tile (B or C of the group, all Q
 //               tokens, double-buffered across units), per head the chunk
@@ -21,7 +21,10 @@
 //   warps 2-9   transform: scale each landed slice in place by the per-token
 //               weight (wdt or em), rounded to bf16 as the MMA's operand;
 //   warps 10-13 epilogue: drain an accumulator (TMEM lane = n) into the
-//               (P, N) state, 128 consecutive n per store instruction.
+//               (P, N) state, 128 consecutive n per store instruction;
+//   warp 14     the chunk-state instance only: the decay tables of a share of
+//               the (row, head) pairs (cdec, dstart, dend, a_block), which no
+//               other part of this kernel reads, instead of a launch of their own.
 // The slice ring keeps about 88 KB of loads in flight per SM, and the next
 // unit's A tile loads while the current one is still in use.
 //
@@ -39,9 +42,10 @@ using bf16 = __nv_bfloat16;
 using namespace sm100;
 using pipe::parity;
 
-constexpr int kWarps = 14, kThreads = kWarps * 32;
+constexpr int kWarps = 15, kThreads = kWarps * 32;
 constexpr int kTWarp0 = 2, kTWarps = 8;              // transform: warps 2-9
 constexpr int kEWarp0 = kTWarp0 + kTWarps, kEWarps = 4;  // epilogue: warps 10-13
+constexpr int kTabWarp = kEWarp0 + kEWarps;          // decay tables: warp 14
 constexpr int kNX = 11;   // operand slice ring, [64 tokens x 64 columns] bf16 each
 constexpr int kNAcc = 4;  // accumulators in tensor memory, 64 columns each
 
@@ -57,6 +61,10 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Unit {
   int bb, c, h0;
+};
+
+struct DecayTabs {
+  float *cdec, *dstart, *dend, *ablk;
 };
 
 // Unit u: the head blocks of one (row, chunk) adjacent, so that the CTAs
@@ -96,14 +104,15 @@ struct Bars {
 
 }  // namespace
 
-// kZ = false: S_c (A = B, operand x, weight wdt, out = sst);
-// kZ = true:  Z_c (A = C, operand dy, weight em, out = dsl).
+// kZ = false: S_c (A = B, operand x, weight wdt, out = sst), and the decay
+//             tables into tab = {cdec, dstart, dend, ablk};
+// kZ = true:  Z_c (A = C, operand dy, weight em, out = dsl); tab unused.
 // Both outputs are (b, nc, H, P, N) fp32.
 template <bool kZ>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_sz_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_x, Problem pr,
-                 const float *__restrict__ dtv, const float *__restrict__ acs, float *__restrict__ out, int HB,
-                 int nunits, int *counter, int *status_word) {
+                 const float *__restrict__ dtv, const float *__restrict__ acs, float *__restrict__ out,
+                 DecayTabs tab, int HB, int nunits, int *counter, int *status_word) {
   extern __shared__ uint8_t smem_raw[];
   const WaitCtl status{status_word, pr.wait_ns};
   uint8_t *sm = tc::aligned_smem(smem_raw);
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < kTabWarp) {
     // ------------------------------------------------------------ epilogue
     // thread = state column n (TMEM lane); out[(b, c, h), p, n]
     const int n = 32 * (warp & 3) + lane;
@@ -339,6 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         pipe::warp_arrive(&bar.acc_free[as]);
       }
     }
+  } else if constexpr (!kZ) {
+    // ------------------------------------------------------------ decay tables
+    // (row, head) pairs blockIdx.x, blockIdx.x + gridDim.x, ..., a lane per chunk
+    for (int p = blockIdx.x; p < pr.b * pr.H; p += gridDim.x)
+      decay_tables_bh(pr, acs, p / pr.H, p % pr.H, tab.cdec, tab.dstart, tab.dend, tab.ablk, lane, 32,
+                      [] { __syncwarp(); });
   }
 
   tc_fence_before();
@@ -360,7 +375,7 @@ int sz_head_block(const Problem &pr) {
 
 template <bool kZ>
 void launch_sz(const Problem &pr, const bf16 *u, const bf16 *xsrc, const float *dtv, const float *acs, float *out,
-               int *status, cudaStream_t s) {
+               DecayTabs tab, int *status, cudaStream_t s) {
   static bool once = (cudaFuncSetAttribute(tc_sz_kernel<kZ>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
                       true);
   (void)once;
@@ -376,19 +391,20 @@ void launch_sz(const Problem &pr, const bf16 *u, const bf16 *xsrc, const float *
   const int nunits = pr.b * pr.nc * (pr.H / HB);
   const int grid = nunits < device_sm_count() ? nunits : device_sm_count();
   int *counter = status + (kZ ? kCounterZ : kCounterState);  // zeroed with the status word
-  tc_sz_kernel<kZ><<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_x, pr, dtv, acs, out, HB, nunits, counter, status);
+  tc_sz_kernel<kZ><<<grid, kThreads, kSmemBytes, s>>>(tm_u, tm_x, pr, dtv, acs, out, tab, HB, nunits, counter,
+                                                      status);
 }
 
 }  // namespace
 
-void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, float *sst, int *status,
-                     cudaStream_t s) {
-  launch_sz<false>(pr, u, u, dtv, acs, sst, status, s);
+void launch_tc_state(const Problem &pr, const bf16 *u, const float *dtv, const float *acs, float *sst, float *cdec,
+                     float *dstart, float *dend, float *ablk, int *status, cudaStream_t s) {
+  launch_sz<false>(pr, u, u, dtv, acs, sst, DecayTabs{cdec, dstart, dend, ablk}, status, s);
 }
 
 void launch_tc_z(const Problem &pr, const bf16 *u, const bf16 *dy, const float *dtv, const float *acs, float *dsl,
                  int *status, cudaStream_t s) {
-  launch_sz<true>(pr, u, dy, dtv, acs, dsl, status, s);
+  launch_sz<true>(pr, u, dy, dtv, acs, dsl, DecayTabs{}, status, s);
 }
 
 int tc_head_subset(const Problem &pr) {
